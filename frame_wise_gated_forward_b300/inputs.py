@@ -1,0 +1,112 @@
+"""Seeded synthetic inputs for the frame-wise GDN forward.
+
+This module holds no arithmetic of the method itself: it only draws random
+tensors with the distributions of the workloads and rounds them to the dtypes
+the C ABI takes.  Both the CUDA path and the CPU oracle are fed from here.
+
+Workload shapes come from the SANA-WM pages: a 60 s, 16 fps, 720p clip
+(article "NVIDIA's New 2.6B World Model...", intro and "The Architecture")
+with 8 raw frames per latent frame ("Camera Control") and native 8k+1 windows
+(WorldFoundry model card, "What it is for") gives F = 8*15 + 1 = 121 latent
+frames; a 1280x704 frame (model card intro) at 32x spatial compression gives a
+40x22 grid, N = 880 tokens per frame.
+
+Distributions (one CPU ``torch.Generator`` per stream, seeded; the draw order
+is fixed as q, k, v, beta, alpha, S_0):
+  q, k  ~ N(0, 1), L2-normalised per (token, head) in fp32, then rounded to
+          bf16 with round-to-nearest-even;
+  v     ~ N(0, 1), rounded to bf16;
+  beta  = sigmoid(N(0, 1)) / N                      fp32 [B, F, N, H]
+  alpha = exp(-softplus(N(0, 1)) * 0.05)            fp32 [B, F, H]  (no clamp)
+  S_0   = 0, or N(0, 0.01) read as variance 0.01 (std 0.1), fp32 [B, H, dv, dk]
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    F: int
+    N: int
+    dk: int
+    dv: int
+    # per batch stream: (seed, S_0 std or 0.0)
+    streams: tuple
+    # True: F sequential single-frame step calls, frame f drawn from seed+f
+    streaming: bool = False
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.F * self.N
+
+
+WORKLOADS = {
+    # tiny case the oracle finishes instantly; fp32 draws through the bf16 ABI
+    "tiny": Workload("tiny", 1, 2, 4, 16, 32, 32, ((0, 0.0),)),
+    # one 9-latent-frame native window (8k+1, k=1) at 1280x704
+    "window9": Workload("window9", 1, 8, 9, 880, 64, 64, ((0, 0.1),)),
+    # the 60 s 720p sequence: 121 x 880 = 106,480 tokens, 16 heads, d = 128
+    "seq60s": Workload("seq60s", 1, 16, 121, 880, 128, 128, ((0, 0.0),)),
+    # guidance-doubled batch: two independent streams, second with S_0 != 0
+    "cfg2": Workload("cfg2", 2, 16, 121, 880, 128, 128, ((0, 0.0), (1, 0.1))),
+    # interactive rollout: 121 single-frame steps on a resident state
+    "stream121": Workload("stream121", 1, 16, 121, 880, 128, 128, ((0, 0.0),),
+                          streaming=True),
+}
+
+
+def draw(B: int, H: int, F: int, N: int, dk: int, dv: int, seed: int,
+         s0_std: float = 0.0) -> dict:
+    """Draw one set of inputs (all batch rows from one generator)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = torch.randn((B, F, N, H, dk), generator=g, dtype=torch.float32)
+    k = torch.randn((B, F, N, H, dk), generator=g, dtype=torch.float32)
+    v = torch.randn((B, F, N, H, dv), generator=g, dtype=torch.float32)
+    braw = torch.randn((B, F, N, H), generator=g, dtype=torch.float32)
+    araw = torch.randn((B, F, H), generator=g, dtype=torch.float32)
+    if s0_std > 0.0:
+        s0 = torch.randn((B, H, dv, dk), generator=g, dtype=torch.float32) * s0_std
+    else:
+        s0 = torch.zeros((B, H, dv, dk), dtype=torch.float32)
+    q = torch.nn.functional.normalize(q, dim=-1).to(torch.bfloat16)
+    k = torch.nn.functional.normalize(k, dim=-1).to(torch.bfloat16)
+    v = v.to(torch.bfloat16)
+    beta = torch.sigmoid(braw) / float(max(N, 1))
+    alpha = torch.exp(-torch.nn.functional.softplus(araw) * 0.05)
+    return {"q": q, "k": k, "v": v, "alpha": alpha.contiguous(),
+            "beta": beta.contiguous(), "state_in": s0.contiguous()}
+
+
+def workload_inputs(w: Workload) -> dict:
+    """Inputs of a named workload, concatenated over its batch streams.
+
+    For a streaming workload frame f is drawn from seed (stream seed + f) as a
+    one-frame draw; the frames are concatenated along F, and the initial
+    state is that of the stream (zero for the shipped workload).
+    """
+    parts = []
+    for seed, std in w.streams:
+        if w.streaming:
+            frames = [draw(1, w.H, 1, w.N, w.dk, w.dv, seed + f, 0.0) for f in range(w.F)]
+            p = {name: torch.cat([fr[name] for fr in frames], dim=1)
+                 for name in ("q", "k", "v", "alpha", "beta")}
+            if std > 0.0:
+                p["state_in"] = draw(1, w.H, 1, 1, w.dk, w.dv, seed, std)["state_in"]
+            else:
+                p["state_in"] = torch.zeros((1, w.H, w.dv, w.dk), dtype=torch.float32)
+            parts.append(p)
+        else:
+            parts.append(draw(1, w.H, w.F, w.N, w.dk, w.dv, seed, std))
+    return {name: torch.cat([p[name] for p in parts], dim=0).contiguous()
+            for name in parts[0]}
+
+
+def has_zero_state(w: Workload) -> bool:
+    return all(std == 0.0 for _, std in w.streams)

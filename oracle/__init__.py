@@ -1,0 +1,153 @@
+"""fp64 CPU oracle for the frame-wise Gated DeltaNet forward.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package.  It shares no code with
+the CUDA library and never imports the product package.
+
+The arithmetic lives in ``gdn_oracle.c`` (plain loops, fp64); this module only
+builds it with gcc, loads it with ctypes and marshals numpy/torch arrays.
+
+What it computes (SANA-WM article, "The Architecture": a recurrent layer that
+processes one whole latent frame per step with a fixed-size state matrix, a
+decay gate and a delta-rule correction; wispaper summary, "Methodology" 1:
+frames scanned one by one), per (batch, head):
+
+    S_f = alpha_f * S_{f-1} (I - K_f^T B_f K_f) + V_f^T B_f K_f
+    O_f = Q_f S_f^T
+
+Every function here is pinned by ``tests/test_oracle.py`` against properties
+that the definition and the mathematics fix (token-level gated delta rule at
+N=1, closed forms, exact delta writes, linearity, a brute-force unrolled
+product, permutation invariance, split/resume, contraction).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+
+MODE_GDN = 0
+MODE_NODELTA = 1
+MODE_REVERSE = 2
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``gdn_oracle.c`` into ``liboracle.so`` beside it (gcc, OpenMP)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-Wall",
+           _SRC, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        p = ctypes.c_void_p
+        i = ctypes.c_int
+        lib.oracle_gdn_frame_forward.argtypes = [
+            p, p, p, p, p, p, p, p, p, p, ctypes.c_int64, p,
+            i, i, i, i, i, i, i, i]
+        lib.oracle_gdn_frame_forward.restype = ctypes.c_int
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def _bits16(x) -> np.ndarray:
+    """bf16 values -> contiguous uint16 bit patterns (torch bf16 tensor, or
+    a numpy uint16 array that already holds bf16 bits)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            if x.dtype != torch.bfloat16:
+                raise TypeError("oracle expects bf16 q/k/v tensors")
+            return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(x)
+    if a.dtype != np.uint16:
+        raise TypeError("oracle expects bf16 bit patterns (uint16)")
+    return a
+
+
+def _f32(x) -> np.ndarray:
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return x.detach().cpu().to(torch.float32).contiguous().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def frame_forward(q, k, v, alpha, beta, state_in=None, *, B, H, F, N, dk, dv,
+                  want_out=True, want_states=False, sample_tokens=None,
+                  mode=MODE_GDN, n_threads=0):
+    """Run the fp64 oracle.
+
+    q, k: bf16 [B,F,N,H,dk]; v: bf16 [B,F,N,H,dv]; alpha fp32 [B,F,H];
+    beta fp32 [B,F,N,H]; state_in fp32 [B,H,dv,dk] or None (zero state).
+    Returns a dict with ``state`` fp64 [B,H,dv,dk], and optionally ``out``
+    fp64 [B,F,N,H,dv], ``states`` fp64 [B,H,F,dv,dk] (state after each frame),
+    ``sample_out`` fp64 [S,H,dv] for the flat token indices ``sample_tokens``.
+    """
+    lib = _load()
+    kb, vb = _bits16(k), _bits16(v)
+    qb = _bits16(q) if q is not None else None
+    al, be = _f32(alpha), _f32(beta)
+    s0 = _f32(state_in) if state_in is not None else None
+    if kb.size != B * F * N * H * dk or vb.size != B * F * N * H * dv:
+        raise ValueError("k/v size does not match B,F,N,H,d")
+    if qb is not None and qb.size != B * F * N * H * dk:
+        raise ValueError("q size does not match B,F,N,H,dk")
+    if al.size != B * F * H or be.size != B * F * N * H:
+        raise ValueError("alpha/beta size mismatch")
+    if s0 is not None and s0.size != B * H * dv * dk:
+        raise ValueError("state_in size mismatch")
+    state = np.empty((B, H, dv, dk), dtype=np.float64)
+    out = np.empty((B, F, N, H, dv), dtype=np.float64) if want_out else None
+    states = np.empty((B, H, F, dv, dk), dtype=np.float64) if want_states else None
+    if sample_tokens is not None:
+        st = np.ascontiguousarray(sample_tokens, dtype=np.int64)
+        sout = np.zeros((st.size, H, dv), dtype=np.float64)
+    else:
+        st, sout = None, None
+    rc = lib.oracle_gdn_frame_forward(
+        _ptr(qb), _ptr(kb), _ptr(vb), _ptr(al), _ptr(be), _ptr(s0),
+        _ptr(out), _ptr(state), _ptr(states),
+        _ptr(st), 0 if st is None else int(st.size), _ptr(sout),
+        B, H, F, N, dk, dv, int(mode), int(n_threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gdn_frame_forward failed with code {rc}")
+    res = {"state": state}
+    if out is not None:
+        res["out"] = out
+    if states is not None:
+        res["states"] = states
+    if sout is not None:
+        res["sample_out"] = sout
+    return res
