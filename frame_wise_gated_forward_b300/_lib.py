@@ -1,0 +1,72 @@
+"""ctypes binding of libgdn_b300.so (argument marshalling only).
+
+Every step of the computation runs in the CUDA library; this module only
+checks tensor shapes/dtypes, passes raw device pointers and the current CUDA
+stream, and turns status codes into exceptions.  If the library is missing it
+raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+STATUS = {
+    0: "GDN_OK", 1: "GDN_ERR_NULL_PTR", 2: "GDN_ERR_BAD_DIM", 3: "GDN_ERR_UNSUPPORTED",
+    4: "GDN_ERR_MISALIGNED", 5: "GDN_ERR_ALLOC", 6: "GDN_ERR_LAUNCH", 7: "GDN_ERR_TIMEOUT",
+    8: "GDN_ERR_ALIAS", 9: "GDN_ERR_NO_DEVICE",
+}
+EXPORTS = (
+    "gdn_frame_forward", "gdn_frame_step", "gdn_workspace_bytes", "gdn_step_workspace_bytes",
+    "gdn_status_string", "gdn_sync_status", "gdn_set_wait_limit_ns", "gdn_selftest_wait_timeout",
+    "gdn_version",
+)
+
+
+class GDNError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        self.status = STATUS.get(code, f"code {code}")
+        super().__init__(f"{what}: {self.status}")
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built: {p} (run frame_wise_gated_forward_b300.build.build())")
+    lib = ctypes.CDLL(p)
+    vp, fp, i, st = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
+    lib.gdn_frame_forward.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, st]
+    lib.gdn_frame_forward.restype = ctypes.c_int
+    lib.gdn_frame_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, st]
+    lib.gdn_frame_step.restype = ctypes.c_int
+    lib.gdn_workspace_bytes.argtypes = [i] * 6
+    lib.gdn_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_step_workspace_bytes.argtypes = [i] * 5
+    lib.gdn_step_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_status_string.argtypes = [ctypes.c_int]
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_sync_status.argtypes = [st]
+    lib.gdn_sync_status.restype = ctypes.c_int
+    lib.gdn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.gdn_set_wait_limit_ns.restype = None
+    lib.gdn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, st]
+    lib.gdn_selftest_wait_timeout.restype = ctypes.c_int
+    lib.gdn_version.argtypes = []
+    lib.gdn_version.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def check(code: int, what: str) -> None:
+    if code != 0:
+        raise GDNError(code, what)

@@ -1,0 +1,408 @@
+// gdn_api.cu -- the C ABI of libgdn_b300.so: argument validation, workspace,
+// tensor-map encoding and the three-phase launch sequence of the frame-wise
+// Gated DeltaNet forward (see include/gdn.h for the contract).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "gdn.h"
+#include "gdn_k1_contract.cuh"
+#include "gdn_k2_scan.cuh"
+#include "gdn_k3_output.cuh"
+
+namespace {
+
+
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ULL};
+
+// ------------------------------------------------------------------ devices
+struct DeviceState {
+    bool probed = false;
+    bool ok = false;
+    int sms = 0;
+    cudaMemPool_t pool = nullptr;
+    bool attrs_set = false;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+gdn_status device_ready(int* dev_out, DeviceState** st_out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GDN_ERR_NO_DEVICE;
+    }
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.probed) {
+        d.probed = true;
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) { cudaGetLastError(); return GDN_ERR_NO_DEVICE; }
+        // the kernels are built for sm_103a only
+        if (prop.major != 10 || prop.minor != 3) return GDN_ERR_NO_DEVICE;
+        d.sms = prop.multiProcessorCount;
+        if (g_encode == nullptr) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr) {
+                cudaGetLastError();
+                return GDN_ERR_NO_DEVICE;
+            }
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        cudaMemPoolProps props;
+        std::memset(&props, 0, sizeof(props));
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) { cudaGetLastError(); return GDN_ERR_ALLOC; }
+        unsigned long long keep = ~0ULL;  // keep freed workspace cached in the pool
+        cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (cudaFuncSetAttribute(gdn::k1::contract_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(gdn::k1::SMEM_BYTES)) != cudaSuccess ||
+            cudaFuncSetAttribute(gdn::k2::scan_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(gdn::k2::Cfg<16>::SMEM_BYTES)) != cudaSuccess ||
+            cudaFuncSetAttribute(gdn::k2::scan_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(gdn::k2::Cfg<32>::SMEM_BYTES)) != cudaSuccess ||
+            cudaFuncSetAttribute(gdn::k3::output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(gdn::k3::SMEM_BYTES)) != cudaSuccess) {
+            cudaGetLastError();
+            return GDN_ERR_LAUNCH;
+        }
+        d.ok = true;
+    }
+    if (!d.ok) return GDN_ERR_NO_DEVICE;
+    *dev_out = dev;
+    *st_out = &d;
+    return GDN_OK;
+}
+
+// ------------------------------------------------------------- validation
+bool dim_ok(int d) { return d >= 16 && d <= 128 && d % 16 == 0; }
+
+struct Range {
+    uintptr_t lo, hi;
+};
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+gdn_status validate(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
+                    const float* state_in, const void* out, const float* state_out, int B, int H, int F, int N,
+                    int dk, int dv) {
+    if (!q || !k || !v || !alpha || !beta || !out) return GDN_ERR_NULL_PTR;
+    if (B < 1 || H < 1 || F < 1 || N < 1) return GDN_ERR_BAD_DIM;
+    if (!dim_ok(dk) || !dim_ok(dv)) return GDN_ERR_UNSUPPORTED;
+    const long long tok = static_cast<long long>(B) * F * N;
+    const long long elems = tok * H * std::max(dk, dv);
+    if (elems >= (1LL << 31) || static_cast<long long>(B) * F * H >= (1LL << 31)) return GDN_ERR_BAD_DIM;
+    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+    if (!a16(q) || !a16(k) || !a16(v) || !a16(out)) return GDN_ERR_MISALIGNED;
+    if (!a4(alpha) || !a4(beta) || (state_in && !a4(state_in)) || (state_out && !a4(state_out)))
+        return GDN_ERR_MISALIGNED;
+    const uintptr_t qb = reinterpret_cast<uintptr_t>(q), kb = reinterpret_cast<uintptr_t>(k),
+                    vb = reinterpret_cast<uintptr_t>(v), ob = reinterpret_cast<uintptr_t>(out);
+    const Range rq{qb, qb + static_cast<uintptr_t>(tok * H * dk * 2)};
+    const Range rk{kb, kb + static_cast<uintptr_t>(tok * H * dk * 2)};
+    const Range rv{vb, vb + static_cast<uintptr_t>(tok * H * dv * 2)};
+    const Range ro{ob, ob + static_cast<uintptr_t>(tok * H * dv * 2)};
+    const uintptr_t ab = reinterpret_cast<uintptr_t>(alpha), bb = reinterpret_cast<uintptr_t>(beta);
+    const Range ra{ab, ab + static_cast<uintptr_t>(static_cast<long long>(B) * F * H * 4)};
+    const Range rb{bb, bb + static_cast<uintptr_t>(tok * H * 4)};
+    const uintptr_t sbytes = static_cast<uintptr_t>(static_cast<long long>(B) * H * dv * dk * 4);
+    if (overlap(ro, rq) || overlap(ro, rk) || overlap(ro, rv) || overlap(ro, ra) || overlap(ro, rb))
+        return GDN_ERR_ALIAS;
+    if (state_in) {
+        const Range rs{reinterpret_cast<uintptr_t>(state_in), reinterpret_cast<uintptr_t>(state_in) + sbytes};
+        if (overlap(ro, rs)) return GDN_ERR_ALIAS;
+        if (state_out && state_out != state_in) {
+            const Range rso{reinterpret_cast<uintptr_t>(state_out), reinterpret_cast<uintptr_t>(state_out) + sbytes};
+            if (overlap(rs, rso)) return GDN_ERR_ALIAS;
+        }
+    }
+    if (state_out) {
+        const Range rso{reinterpret_cast<uintptr_t>(state_out), reinterpret_cast<uintptr_t>(state_out) + sbytes};
+        if (overlap(ro, rso) || overlap(rq, rso) || overlap(rk, rso) || overlap(rv, rso) || overlap(ra, rso) ||
+            overlap(rb, rso))
+            return GDN_ERR_ALIAS;
+    }
+    return GDN_OK;
+}
+
+// Every pointer the kernels dereference must be device memory: a host pointer
+// handed to a kernel would be an illegal access.
+bool is_device_ptr(const void* p) {
+    if (p == nullptr) return true;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+// ------------------------------------------------------------- workspace
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Layout {
+    size_t a_off, u_off, s_off, p_off, total;
+};
+Layout layout_of(long long items, int dk, int dv, int nsplit) {
+    Layout L;
+    L.a_off = 0;
+    L.u_off = align256(L.a_off + static_cast<size_t>(items) * dk * dk * 2);
+    L.s_off = align256(L.u_off + static_cast<size_t>(items) * dv * dk * 4);
+    L.p_off = align256(L.s_off + static_cast<size_t>(items) * dv * dk * 2);
+    L.total = L.p_off;
+    if (nsplit > 1) L.total = align256(L.p_off + static_cast<size_t>(nsplit) * items * (dk * dk + dv * dk) * 4);
+    return L;
+}
+
+int step_nsplit(int sms, int B, int H, int N) {
+    const int items = B * H;
+    const int chunks = (N + gdn::k1::CHUNK - 1) / gdn::k1::CHUNK;
+    int ns = std::max(1, sms / std::max(items, 1));
+    return std::min(ns, chunks);
+}
+
+// ------------------------------------------------------------ tensor maps
+bool encode(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
+            const cuuint32_t* box) {
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, dims, strides_bytes, box, es,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+// token tensor [BF, N, H, d] bf16, box (64, 1, rows, 1)
+bool encode_tokens(CUtensorMap* m, const void* base, int BF, int N, int H, int d, int rows) {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BF)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2,
+                                   static_cast<cuuint64_t>(N) * H * d * 2};
+    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(rows), 1};
+    return encode(m, const_cast<void*>(base), 4, dims, strides, box);
+}
+// per-item matrix [items, rows_total, cols] bf16, box (64, rows, 1)
+bool encode_mats(CUtensorMap* m, const void* base, long long items, int rows_total, int cols, int rows) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows_total),
+                                static_cast<cuuint64_t>(items)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
+                                   static_cast<cuuint64_t>(rows_total) * cols * 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
+    return encode(m, const_cast<void*>(base), 3, dims, strides, box);
+}
+
+// ------------------------------------------------------------- the pass
+gdn_status run_pass(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
+                    const float* state_in, void* out, float* state_out, int B, int H, int F, int N, int dk, int dv,
+                    bool step, cudaStream_t stream) {
+    int dev;
+    DeviceState* ds;
+    gdn_status st = device_ready(&dev, &ds);
+    if (st != GDN_OK) return st;
+    if (!is_device_ptr(q) || !is_device_ptr(k) || !is_device_ptr(v) || !is_device_ptr(alpha) ||
+        !is_device_ptr(beta) || !is_device_ptr(state_in) || !is_device_ptr(out) || !is_device_ptr(state_out))
+        return GDN_ERR_NULL_PTR;
+
+    const long long items = static_cast<long long>(B) * F * H;
+    const int BF = B * F;
+    const int chunks = (N + gdn::k1::CHUNK - 1) / gdn::k1::CHUNK;
+    const int nsplit = step ? step_nsplit(ds->sms, B, H, N) : 1;
+    const Layout L = layout_of(items, dk, dv, nsplit);
+
+    uint8_t* ws = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), L.total, ds->pool, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_ALLOC;
+    }
+    __nv_bfloat16* A_ws = reinterpret_cast<__nv_bfloat16*>(ws + L.a_off);
+    float* U_ws = reinterpret_cast<float*>(ws + L.u_off);
+    __nv_bfloat16* S_all = reinterpret_cast<__nv_bfloat16*>(ws + L.s_off);
+    float* partial = nsplit > 1 ? reinterpret_cast<float*>(ws + L.p_off) : nullptr;
+
+    const int R = (dv % 32 == 0) ? 32 : 16;
+    CUtensorMap tm_k, tm_v, tm_q, tm_out, tm_A, tm_S_store, tm_S_load;
+    bool enc = encode_tokens(&tm_k, k, BF, N, H, dk, gdn::k1::CHUNK) &&
+               encode_tokens(&tm_v, v, BF, N, H, dv, gdn::k1::CHUNK) &&
+               encode_tokens(&tm_q, q, BF, N, H, dk, gdn::k3::TILE_M) &&
+               encode_tokens(&tm_out, out, BF, N, H, dv, 32) && encode_mats(&tm_A, A_ws, items, dk, dk, 128) &&
+               encode_mats(&tm_S_store, S_all, items, dv, dk, R) && encode_mats(&tm_S_load, S_all, items, dv, dk, 128);
+    gdn_status result = GDN_OK;
+    if (!enc) {
+        result = GDN_ERR_LAUNCH;
+    } else {
+        const unsigned long long lim = g_wait_limit_ns.load();
+        // phase 1
+        gdn::k1::Params p1;
+        p1.beta = beta;
+        p1.A_ws = A_ws;
+        p1.U_ws = U_ws;
+        p1.partial = partial;
+        p1.H = H;
+        p1.N = N;
+        p1.dk = dk;
+        p1.dv = dv;
+        p1.items = static_cast<int>(items);
+        p1.nsplit = nsplit;
+        p1.chunks = chunks;
+        p1.work = static_cast<int>(items * nsplit);
+        p1.wait_limit_ns = lim;
+        const int g1 = std::min(p1.work, ds->sms);
+        gdn::k1::contract_kernel<<<g1, gdn::k1::THREADS, gdn::k1::SMEM_BYTES, stream>>>(tm_k, tm_v, p1);
+        if (nsplit > 1) {
+            const size_t total = static_cast<size_t>(items) * (dk * dk + dv * dk);
+            const int blocks = static_cast<int>(std::min<size_t>((total + 255) / 256, 4 * ds->sms));
+            gdn::k1::reduce_partials_kernel<<<blocks, 256, 0, stream>>>(partial, A_ws, U_ws, static_cast<int>(items),
+                                                                       nsplit, dk, dv);
+        }
+        // phase 2
+        gdn::k2::Params p2;
+        p2.alpha = alpha;
+        p2.U_ws = U_ws;
+        p2.state_in = state_in;
+        p2.state_out = state_out;
+        p2.H = H;
+        p2.F = F;
+        p2.dk = dk;
+        p2.dv = dv;
+        p2.rsplit = dv / R;
+        p2.wait_limit_ns = lim;
+        const int g2 = B * H * p2.rsplit;
+        if (R == 32)
+            gdn::k2::scan_kernel<32><<<g2, gdn::k2::THREADS, gdn::k2::Cfg<32>::SMEM_BYTES, stream>>>(tm_A, tm_S_store, p2);
+        else
+            gdn::k2::scan_kernel<16><<<g2, gdn::k2::THREADS, gdn::k2::Cfg<16>::SMEM_BYTES, stream>>>(tm_A, tm_S_store, p2);
+        // phase 3
+        gdn::k3::Params p3;
+        p3.H = H;
+        p3.N = N;
+        p3.dk = dk;
+        p3.dv = dv;
+        p3.ntile = (N + gdn::k3::TILE_M - 1) / gdn::k3::TILE_M;
+        p3.total = items * p3.ntile;
+        p3.wait_limit_ns = lim;
+        const int g3 = static_cast<int>(std::min<long long>(p3.total, ds->sms));
+        gdn::k3::output_kernel<<<g3, gdn::k3::THREADS, gdn::k3::SMEM_BYTES, stream>>>(tm_q, tm_S_load, tm_out, p3);
+        if (cudaGetLastError() != cudaSuccess) result = GDN_ERR_LAUNCH;
+    }
+    cudaFreeAsync(ws, stream);
+    return result;
+}
+
+__global__ void selftest_timeout_kernel(unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        gdn::mbar_init(&bar, 1);  // nothing ever arrives on it
+        abort_flag = 0;
+        gdn::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) gdn::mbar_wait(&bar, 0, limit_ns, &abort_flag);
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_frame_forward(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
+                             const float* state_in, void* out, float* state_out, int B, int H, int F, int N, int dk,
+                             int dv, gdn_stream_t stream) {
+    gdn_status s = validate(q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv);
+    if (s != GDN_OK) return s;
+    return run_pass(q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv, false,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_frame_step(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
+                          const float* state_in, void* out, float* state_out, int B, int H, int N, int dk, int dv,
+                          gdn_stream_t stream) {
+    gdn_status s = validate(q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv);
+    if (s != GDN_OK) return s;
+    return run_pass(q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv, true,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t gdn_workspace_bytes(int B, int H, int F, int N, int dk, int dv) {
+    if (B < 1 || H < 1 || F < 1 || N < 1 || !dim_ok(dk) || !dim_ok(dv)) return 0;
+    return layout_of(static_cast<long long>(B) * F * H, dk, dv, 1).total;
+}
+
+size_t gdn_step_workspace_bytes(int B, int H, int N, int dk, int dv) {
+    if (B < 1 || H < 1 || N < 1 || !dim_ok(dk) || !dim_ok(dv)) return 0;
+    int sms = 148;
+    int dev = -1;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) sms = n;
+    }
+    cudaGetLastError();
+    return layout_of(static_cast<long long>(B) * H, dk, dv, step_nsplit(sms, B, H, N)).total;
+}
+
+const char* gdn_status_string(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_NULL_PTR: return "GDN_ERR_NULL_PTR: a required pointer is NULL or not device memory";
+        case GDN_ERR_BAD_DIM: return "GDN_ERR_BAD_DIM: B, H, F or N < 1, or a tensor is too large";
+        case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: dk and dv must be multiples of 16 in [16, 128]";
+        case GDN_ERR_MISALIGNED: return "GDN_ERR_MISALIGNED: q/k/v/out need 16-byte, fp32 arrays 4-byte alignment";
+        case GDN_ERR_ALLOC: return "GDN_ERR_ALLOC: workspace allocation failed";
+        case GDN_ERR_LAUNCH: return "GDN_ERR_LAUNCH: a CUDA call or kernel launch failed";
+        case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a device-side bounded wait ran out";
+        case GDN_ERR_ALIAS: return "GDN_ERR_ALIAS: an output overlaps an input";
+        case GDN_ERR_NO_DEVICE: return "GDN_ERR_NO_DEVICE: no usable sm_103 device is current";
+    }
+    return "GDN_ERR_UNKNOWN";
+}
+
+gdn_status gdn_sync_status(gdn_stream_t stream) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return GDN_ERR_NO_DEVICE; }
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_LAUNCH;
+    }
+    int code = 0;
+    if (cudaMemcpyFromSymbol(&code, gdn::g_error, sizeof(int)) != cudaSuccess) { cudaGetLastError(); return GDN_ERR_LAUNCH; }
+    if (code != 0) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(gdn::g_error, &zero, sizeof(int));
+        return static_cast<gdn_status>(code);
+    }
+    return GDN_OK;
+}
+
+void gdn_set_wait_limit_ns(unsigned long long limit_ns) {
+    g_wait_limit_ns.store(limit_ns < 1000ULL ? 1000ULL : limit_ns);
+}
+
+gdn_status gdn_selftest_wait_timeout(unsigned long long limit_ns, gdn_stream_t stream) {
+    int dev;
+    DeviceState* ds;
+    gdn_status st = device_ready(&dev, &ds);
+    if (st != GDN_OK) return st;
+    if (limit_ns < 1000ULL) limit_ns = 1000ULL;
+    if (limit_ns > 5000000000ULL) limit_ns = 5000000000ULL;
+    selftest_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+
+const char* gdn_version(void) { return "gdn-b300 0.1 (sm_103a, tcgen05)"; }
+
+}  // extern "C"

@@ -1,0 +1,325 @@
+// gdn_k1_contract.cuh -- phase 1 of the frame-wise GDN forward.
+//
+// For every (batch b, latent frame f, head h) -- one "item" -- the two
+// frame-parallel contractions of the delta rule
+//     A_f = K_f^T B_f K_f = sum_n beta_n k_n k_n^T      (dk x dk)
+//     U_f = V_f^T B_f K_f = sum_n beta_n v_n k_n^T      (dv x dk)
+// (SANA-WM article, "The Architecture": the state is updated once per latent
+// frame by a decay gate and a delta-rule correction; these two matrices are
+// everything the frame contributes to that update).
+//
+// Formulation on the tensor core: one MMA  D = (B K)^T [K | V]  with
+//     M = 128   rows j of (beta k)^T      (dk, zero-padded to 128)
+//     N = 256   columns [k (128) | v (128)]
+//     K = tokens, 16 per instruction, 64 per pipeline stage
+// so that TMEM lane j holds row j of A (columns 0..127) and column j of U
+// (columns 128..255).  Both operands are read straight from the TMA tiles
+// of q/k/v's natural token-major layout, i.e. MN-major in the MMA's terms.
+// beta is applied in fp32 to a copy of the K tile (rounded to bf16 once).
+//
+// Warp roles (256 threads): warp 0 TMA producer; warp 1 TMEM owner and MMA
+// issuer; warps 2-3 beta scalers (one token row per thread); warps 4-7
+// epilogue (TMEM lane quarter = warp % 4).  TMEM holds two 256-column
+// accumulators so one item's epilogue overlaps the next item's MMAs.
+#pragma once
+
+#include "gdn_ptx.cuh"
+
+namespace gdn {
+namespace k1 {
+
+constexpr int CHUNK = 64;                   // tokens per stage (MMA K extent per stage)
+constexpr int STAGES = 4;
+constexpr int BOX_BYTES = CHUNK * 128;      // 64 token rows x 128 B (64 bf16)
+constexpr int TILE_BYTES = 2 * BOX_BYTES;   // d padded to 128 -> two 64-column boxes
+constexpr int STAGE_BYTES = 3 * TILE_BYTES; // K tile, V tile, beta*K tile
+constexpr int THREADS = 256;
+constexpr int TMEM_COLS = 512;
+constexpr int ACC_COLS = 256;
+// MN-major operand with 128-byte swizzle: 64 MN-elements per 128-byte row,
+// 8 K-rows per 1024-byte swizzle atom.  LBO = distance between 64-element
+// MN blocks (the two 64-column TMA boxes), SBO = distance between 8-row K
+// groups.
+constexpr uint32_t MN_LBO = BOX_BYTES;
+constexpr uint32_t MN_SBO = 1024;
+constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
+
+struct Params {
+    const float* beta;     // [B, F, N, H]
+    __nv_bfloat16* A_ws;   // [items][dk][dk]  (nsplit == 1)
+    float* U_ws;           // [items][dv][dk]  (nsplit == 1)
+    float* partial;        // [nsplit][items][dk*dk + dv*dk]  (nsplit > 1)
+    int H, N, dk, dv;
+    int items;             // B * F * H, item = (b*F + f)*H + h
+    int nsplit;            // token splits per item
+    int chunks;            // ceil(N / CHUNK)
+    int work;              // items * nsplit
+    unsigned long long wait_limit_ns;
+};
+
+struct Unit {
+    int item, split, c_begin, c_end;
+};
+__device__ __forceinline__ Unit unit_of(const Params& p, int w) {
+    Unit u;
+    u.item = w / p.nsplit;
+    u.split = w % p.nsplit;
+    u.c_begin = static_cast<int>((static_cast<long long>(u.split) * p.chunks) / p.nsplit);
+    u.c_end = static_cast<int>((static_cast<long long>(u.split + 1) * p.chunks) / p.nsplit);
+    return u;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    contract_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stage_base = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* full = bars;                  // [STAGES]  TMA landed K and V
+    uint64_t* scaled = bars + STAGES;       // [STAGES]  beta*K written
+    uint64_t* empty = bars + 2 * STAGES;    // [STAGES]  MMA finished reading the stage
+    uint64_t* tfull = bars + 3 * STAGES;    // [2]       accumulator ready
+    uint64_t* tempty = bars + 3 * STAGES + 2; // [2]     accumulator drained
+    uint64_t* final_bar = bars + 3 * STAGES + 4; // [1]     every issued MMA retired
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int w_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * p.work) / gridDim.x);
+    const int w_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.work) / gridDim.x);
+    const int kboxes = p.dk > 64 ? 2 : 1;
+    const int vboxes = p.dv > 64 ? 2 : 1;
+
+    // Zero every stage once: boxes that are never loaded (d <= 64) must read as 0.
+    for (int i = threadIdx.x; i < STAGES * STAGE_BYTES / 16; i += THREADS)
+        reinterpret_cast<uint4*>(stage_base)[i] = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&scaled[s], 64);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
+        mbar_init(final_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            for (int w = w_begin; w < w_end && !*abort_flag; ++w) {
+                const Unit u = unit_of(p, w);
+                const int frame = u.item / p.H, h = u.item % p.H;
+                for (int c = u.c_begin; c < u.c_end; ++c) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, abort_flag)) break;
+                    uint8_t* st = stage_base + stage * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full[stage], (kboxes + vboxes) * BOX_BYTES);
+                    for (int bx = 0; bx < kboxes; ++bx)
+                        tma_load_4d(st + bx * BOX_BYTES, &tm_k, &full[stage], 64 * bx, h, c * CHUNK, frame);
+                    for (int bx = 0; bx < vboxes; ++bx)
+                        tma_load_4d(st + TILE_BYTES + bx * BOX_BYTES, &tm_v, &full[stage], 64 * bx, h,
+                                    c * CHUNK, frame);
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            // Drain: the most recent fill of every stage must have landed before exit
+            // (only matters when a wait gave up; otherwise the MMA issuer consumed all).
+            for (long long kf = (issued > STAGES ? issued - STAGES : 0); kf < issued; ++kf)
+                mbar_wait_drain(&full[kf % STAGES], static_cast<uint32_t>((kf / STAGES) & 1), p.wait_limit_ns);
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_bf16(128, 256, 1, 1);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int w = w_begin; w < w_end && !*abort_flag; ++w) {
+                const Unit u = unit_of(p, w);
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1, p.wait_limit_ns, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+                bool ok = true;
+                for (int c = u.c_begin; c < u.c_end; ++c) {
+                    if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag) ||
+                        !mbar_wait(&scaled[stage], phase, p.wait_limit_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = smem_u32(stage_base + stage * STAGE_BYTES);
+                    const uint32_t a_base = st + 2 * TILE_BYTES;  // beta*K
+                    const uint32_t b_base = st;                   // [K | V]
+#pragma unroll
+                    for (int kk = 0; kk < CHUNK / 16; ++kk) {
+                        const uint64_t ad = smem_desc(a_base + kk * 2048, MN_LBO, MN_SBO);
+                        const uint64_t bd = smem_desc(b_base + kk * 2048, MN_LBO, MN_SBO);
+                        mma_bf16(d_tmem, ad, bd, IDESC, (c > u.c_begin || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(&tfull[acc]);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            }
+            mma_commit(final_bar);
+            mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
+        }
+    } else if (warp < 4) {
+        // ------------------------------------------------------ beta scalers
+        const int r = threadIdx.x - 64;  // token row within the stage, 0..63
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int w = w_begin; w < w_end && !*abort_flag; ++w) {
+            const Unit u = unit_of(p, w);
+            const int frame = u.item / p.H, h = u.item % p.H;
+            bool ok = true;
+            for (int c = u.c_begin; c < u.c_end; ++c) {
+                const int tok = c * CHUNK + r;
+                const float bval =
+                    (tok < p.N) ? __ldg(p.beta + (static_cast<size_t>(frame) * p.N + tok) * p.H + h) : 0.0f;
+                if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag)) { ok = false; break; }
+                uint8_t* st = stage_base + stage * STAGE_BYTES;
+                for (int bx = 0; bx < kboxes; ++bx) {
+                    const uint8_t* src = st + bx * BOX_BYTES + r * 128;
+                    uint8_t* dst = st + 2 * TILE_BYTES + bx * BOX_BYTES + r * 128;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int ch = (i + r) & 7;  // rotate so 8 consecutive rows hit 8 distinct bank groups
+                        uint4 x = *reinterpret_cast<const uint4*>(src + ch * 16);
+                        uint32_t* xs = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            __nv_bfloat162 pr = *reinterpret_cast<__nv_bfloat162*>(&xs[e]);
+                            float2 f2 = __bfloat1622float2(pr);
+                            xs[e] = pack_bf16x2(f2.x * bval, f2.y * bval);
+                        }
+                        *reinterpret_cast<uint4*>(dst + ch * 16) = x;
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&scaled[stage]);
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+            if (!ok) break;
+        }
+    } else {
+        // ----------------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        const int j = quarter * 32 + lane;  // TMEM lane = row j of (beta K)^T = dk index
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int w = w_begin; w < w_end && !*abort_flag; ++w) {
+            const Unit u = unit_of(p, w);
+            if (!mbar_wait(&tfull[acc], acc_phase, p.wait_limit_ns, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(quarter * 32) << 16);
+            const bool jv = j < p.dk;
+            if (p.nsplit == 1) {
+                __nv_bfloat16* Aout = p.A_ws + static_cast<size_t>(u.item) * p.dk * p.dk;
+                float* Uout = p.U_ws + static_cast<size_t>(u.item) * p.dv * p.dk;
+                for (int c0 = 0; c0 < p.dk; c0 += 32) {
+                    uint32_t r32[32];
+                    tmem_ld32(tbase + c0, r32);
+                    tmem_wait_ld();
+                    if (jv) {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (c0 + t < p.dk)
+                                Aout[static_cast<size_t>(c0 + t) * p.dk + j] =
+                                    __float2bfloat16_rn(__uint_as_float(r32[t]));
+                    }
+                }
+                for (int c0 = 0; c0 < p.dv; c0 += 32) {
+                    uint32_t r32[32];
+                    tmem_ld32(tbase + 128 + c0, r32);
+                    tmem_wait_ld();
+                    if (jv) {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (c0 + t < p.dv) Uout[static_cast<size_t>(c0 + t) * p.dk + j] = __uint_as_float(r32[t]);
+                    }
+                }
+            } else {
+                const size_t per = static_cast<size_t>(p.dk) * p.dk + static_cast<size_t>(p.dv) * p.dk;
+                float* out = p.partial + (static_cast<size_t>(u.split) * p.items + u.item) * per;
+                for (int c0 = 0; c0 < p.dk; c0 += 32) {
+                    uint32_t r32[32];
+                    tmem_ld32(tbase + c0, r32);
+                    tmem_wait_ld();
+                    if (jv) {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (c0 + t < p.dk) out[static_cast<size_t>(c0 + t) * p.dk + j] = __uint_as_float(r32[t]);
+                    }
+                }
+                float* outU = out + static_cast<size_t>(p.dk) * p.dk;
+                for (int c0 = 0; c0 < p.dv; c0 += 32) {
+                    uint32_t r32[32];
+                    tmem_ld32(tbase + 128 + c0, r32);
+                    tmem_wait_ld();
+                    if (jv) {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (c0 + t < p.dv) outU[static_cast<size_t>(c0 + t) * p.dk + j] = __uint_as_float(r32[t]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    // Wait for all outstanding MMAs before releasing TMEM.
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// Step path: sum the per-split fp32 partials in split order (deterministic)
+// and write A (bf16) and U (fp32) in the layout phase 2 reads.
+__global__ void reduce_partials_kernel(const float* __restrict__ partial, __nv_bfloat16* __restrict__ A_ws,
+                                       float* __restrict__ U_ws, int items, int nsplit, int dk, int dv) {
+    const size_t per = static_cast<size_t>(dk) * dk + static_cast<size_t>(dv) * dk;
+    const size_t total = per * items;
+    for (size_t e = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t item = e / per, off = e % per;
+        float s = 0.0f;
+        for (int sp = 0; sp < nsplit; ++sp) s += partial[(static_cast<size_t>(sp) * items + item) * per + off];
+        if (off < static_cast<size_t>(dk) * dk)
+            A_ws[item * dk * dk + off] = __float2bfloat16_rn(s);
+        else
+            U_ws[item * dv * dk + (off - static_cast<size_t>(dk) * dk)] = s;
+    }
+}
+
+}  // namespace k1
+}  // namespace gdn

@@ -1,0 +1,234 @@
+// gdn_k3_output.cuh -- phase 3 of the frame-wise GDN forward: every token of
+// latent frame f reads the state after frame f,
+//     O_f = Q_f S_f^T        (o_n = S_f q_n)
+// (SANA-WM article, "The Architecture": the layer processes one entire latent
+// frame per step, so all tokens of a frame see the same state).
+//
+// Frame-parallel: tiles of 128 tokens of one (b, f, h) item.  Per tile one
+// MMA chain D = Q_tile S_f^T with
+//     M = 128 tokens, N = 128 (dv, zero-padded), K = dk (<= 128)
+// both operands K-major in 128-byte-swizzled shared memory, loaded by TMA
+// straight from q's token-major layout and from the bf16 per-frame states.
+// A persistent grid walks a contiguous range of tiles; S_f is loaded once per
+// item (2-deep ring), q through a 3-deep ring, four 128-column accumulators in
+// TMEM let the MMA run up to three tiles ahead of the epilogue.  Epilogue:
+// each of four warps drains its 32-lane quarter, rounds to bf16 (RNE), writes
+// a swizzled staging tile and stores it with its own TMA store (rows past N
+// are clipped by the tensor map).
+//
+// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
+// issuer, warps 2-5 epilogue (TMEM lane quarter = warp % 4).
+#pragma once
+
+#include "gdn_ptx.cuh"
+
+namespace gdn {
+namespace k3 {
+
+constexpr int THREADS = 192;
+constexpr int TILE_M = 128;                  // tokens per tile
+constexpr int QSTAGES = 3;
+constexpr int SSTAGES = 2;
+constexpr int ACCS = 4;
+constexpr int BOX_BYTES = TILE_M * 128;      // 128 rows x 128 B
+constexpr int QTILE_BYTES = 2 * BOX_BYTES;   // dk padded to 128
+constexpr int STILE_BYTES = 2 * BOX_BYTES;   // S_f: 128 rows (dv) x dk
+constexpr int OBOX_BYTES = 32 * 128;         // one warp's 32 rows x 64 columns
+constexpr int OSTAGE_BYTES = 2 * OBOX_BYTES; // 32 rows x 128 columns
+constexpr int TMEM_COLS = 512;
+constexpr size_t SMEM_BYTES =
+    1024 + QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES + 4 * 2 * OSTAGE_BYTES + 256;
+
+struct Params {
+    int H, N, dk, dv;
+    int ntile;              // ceil(N / 128) tiles per item
+    long long total;        // items * ntile
+    unsigned long long wait_limit_ns;
+};
+
+__global__ void __launch_bounds__(THREADS, 1)
+    output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
+                  const __grid_constant__ CUtensorMap tm_out, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* qring = smem;
+    uint8_t* sring = qring + QSTAGES * QTILE_BYTES;
+    uint8_t* ostage = sring + SSTAGES * STILE_BYTES;   // [4 warps][2][OSTAGE_BYTES]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ostage + 4 * 2 * OSTAGE_BYTES);
+    uint64_t* qfull = bars;
+    uint64_t* qempty = qfull + QSTAGES;
+    uint64_t* sfull = qempty + QSTAGES;
+    uint64_t* sempty = sfull + SSTAGES;
+    uint64_t* tfull = sempty + SSTAGES;
+    uint64_t* tempty = tfull + ACCS;
+    uint64_t* final_bar = tempty + ACCS;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long t_begin = (static_cast<long long>(blockIdx.x) * p.total) / gridDim.x;
+    const long long t_end = (static_cast<long long>(blockIdx.x + 1) * p.total) / gridDim.x;
+    const int kboxes = p.dk > 64 ? 2 : 1;
+    const int vboxes = p.dv > 64 ? 2 : 1;
+
+    // never-loaded boxes (d <= 64) must read as zero
+    for (int i = threadIdx.x; i < (QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES) / 16; i += THREADS)
+        reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < QSTAGES; ++s) { mbar_init(&qfull[s], 1); mbar_init(&qempty[s], 1); }
+        for (int s = 0; s < SSTAGES; ++s) { mbar_init(&sfull[s], 1); mbar_init(&sempty[s], 1); }
+        for (int a = 0; a < ACCS; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 128); }
+        mbar_init(final_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_s);
+        prefetch_tmap(&tm_out);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int qs = 0, ss = 0;
+            uint32_t qph = 0, sph = 0;
+            long long q_issued = 0, s_issued = 0;
+            long long prev_item = -1;
+            for (long long t = t_begin; t < t_end && !*abort_flag; ++t) {
+                const long long item = t / p.ntile;
+                const int nt = static_cast<int>(t % p.ntile);
+                const int frame = static_cast<int>(item / p.H), h = static_cast<int>(item % p.H);
+                if (item != prev_item) {
+                    if (prev_item >= 0) { if (++ss == SSTAGES) { ss = 0; sph ^= 1; } }
+                    if (!mbar_wait(&sempty[ss], sph ^ 1, p.wait_limit_ns, abort_flag)) break;
+                    mbar_arrive_expect_tx(&sfull[ss], kboxes * BOX_BYTES);
+                    for (int bx = 0; bx < kboxes; ++bx)
+                        tma_load_3d(sring + ss * STILE_BYTES + bx * BOX_BYTES, &tm_s, &sfull[ss], 64 * bx, 0,
+                                    static_cast<int>(item));
+                    ++s_issued;
+                    prev_item = item;
+                }
+                if (!mbar_wait(&qempty[qs], qph ^ 1, p.wait_limit_ns, abort_flag)) break;
+                mbar_arrive_expect_tx(&qfull[qs], kboxes * BOX_BYTES);
+                for (int bx = 0; bx < kboxes; ++bx)
+                    tma_load_4d(qring + qs * QTILE_BYTES + bx * BOX_BYTES, &tm_q, &qfull[qs], 64 * bx, h,
+                                nt * TILE_M, frame);
+                ++q_issued;
+                if (++qs == QSTAGES) { qs = 0; qph ^= 1; }
+            }
+            for (long long k = (q_issued > QSTAGES ? q_issued - QSTAGES : 0); k < q_issued; ++k)
+                mbar_wait_drain(&qfull[k % QSTAGES], static_cast<uint32_t>((k / QSTAGES) & 1), p.wait_limit_ns);
+            for (long long k = (s_issued > SSTAGES ? s_issued - SSTAGES : 0); k < s_issued; ++k)
+                mbar_wait_drain(&sfull[k % SSTAGES], static_cast<uint32_t>((k / SSTAGES) & 1), p.wait_limit_ns);
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_bf16(128, 128, 0, 0);
+            const int nk = (p.dk + 15) / 16;
+            int qs = 0, ss = 0, acc = 0;
+            uint32_t qph = 0, sph = 0, aph = 0;
+            long long prev_item = -1;
+            for (long long t = t_begin; t < t_end && !*abort_flag; ++t) {
+                const long long item = t / p.ntile;
+                const bool last_of_item = (t + 1 == t_end) || ((t + 1) / p.ntile != item);
+                if (item != prev_item) {
+                    if (prev_item >= 0) { if (++ss == SSTAGES) { ss = 0; sph ^= 1; } }
+                    if (!mbar_wait(&sfull[ss], sph, p.wait_limit_ns, abort_flag)) break;
+                    prev_item = item;
+                }
+                if (!mbar_wait(&tempty[acc], aph ^ 1, p.wait_limit_ns, abort_flag)) break;
+                if (!mbar_wait(&qfull[qs], qph, p.wait_limit_ns, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t a_base = smem_u32(qring + qs * QTILE_BYTES);
+                const uint32_t b_base = smem_u32(sring + ss * STILE_BYTES);
+                const uint32_t d_tmem = tmem_base + acc * 128;
+                for (int kk = 0; kk < nk; ++kk) {
+                    const uint64_t ad = smem_desc(a_base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc(b_base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
+                    mma_bf16(d_tmem, ad, bd, IDESC, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&qempty[qs]);
+                mma_commit(&tfull[acc]);
+                if (last_of_item) mma_commit(&sempty[ss]);
+                if (++qs == QSTAGES) { qs = 0; qph ^= 1; }
+                if (++acc == ACCS) { acc = 0; aph ^= 1; }
+            }
+            mma_commit(final_bar);
+            mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
+        }
+    } else {
+        // ----------------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        uint8_t* my_stage = ostage + quarter * 2 * OSTAGE_BYTES;
+        int acc = 0, ob = 0;
+        uint32_t aph = 0;
+        const int ncol32 = (p.dv + 31) / 32;
+        for (long long t = t_begin; t < t_end && !*abort_flag; ++t) {
+            const long long item = t / p.ntile;
+            const int nt = static_cast<int>(t % p.ntile);
+            const int frame = static_cast<int>(item / p.H), h = static_cast<int>(item % p.H);
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, p.wait_limit_ns, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + acc * 128 + (static_cast<uint32_t>(quarter * 32) << 16);
+            uint32_t packed[64];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (c < ncol32) {
+                    uint32_t r32[32];
+                    tmem_ld32(tbase + c * 32, r32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        packed[c * 16 + e] = pack_bf16x2(__uint_as_float(r32[2 * e]), __uint_as_float(r32[2 * e + 1]));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+            if (++acc == ACCS) { acc = 0; aph ^= 1; }
+
+            // staging buffer `ob` was last read by the TMA store issued two tiles ago
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+            uint8_t* stg = my_stage + ob * OSTAGE_BYTES;
+            const int row = lane;  // token row within this warp's 32
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {
+                const int box = ch >> 3, c8 = ch & 7;
+                if (box < vboxes) {
+                    uint4 v = make_uint4(packed[ch * 4 + 0], packed[ch * 4 + 1], packed[ch * 4 + 2], packed[ch * 4 + 3]);
+                    *reinterpret_cast<uint4*>(stg + box * OBOX_BYTES + row * 128 + ((c8 ^ (row & 7)) << 4)) = v;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                for (int bx = 0; bx < vboxes; ++bx)
+                    tma_store_4d(&tm_out, stg + bx * OBOX_BYTES, 64 * bx, h, nt * TILE_M + quarter * 32, frame);
+                bulk_commit();
+            }
+            ob ^= 1;
+        }
+        if (lane == 0) bulk_wait<0>();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace k3
+}  // namespace gdn

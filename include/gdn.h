@@ -1,0 +1,144 @@
+/*
+ * gdn.h -- C ABI of the B300-native frame-wise Gated DeltaNet (GDN) forward.
+ *
+ * The operation (SANA-WM article, davidborish.com, section "The Architecture":
+ * a recurrent layer that processes one entire latent frame per step and keeps
+ * a fixed-size state matrix updated by a decay gate and a delta-rule
+ * correction; wispaper summary, "Methodology" 1: frames are scanned one by
+ * one).  Per batch row b and head h, with K_f, Q_f (N x dk) and V_f (N x dv)
+ * the N tokens of latent frame f, B_f = diag(beta) and alpha_f the frame's
+ * decay:
+ *
+ *     S_f = alpha_f * S_{f-1} * (I - K_f^T B_f K_f) + V_f^T B_f K_f
+ *     O_f = Q_f * S_f^T                 (every token of frame f reads S_f)
+ *
+ * S is an fp32 dv x dk matrix, S_0 = state_in (or zero).
+ *
+ * Layouts (all contiguous, row-major, tokens frame-major):
+ *     q, k        bf16  [B, F, N, H, dk]
+ *     v, out      bf16  [B, F, N, H, dv]
+ *     alpha       fp32  [B, F, H]
+ *     beta        fp32  [B, F, N, H]
+ *     state_in,
+ *     state_out   fp32  [B, H, dv, dk]      S[i][j], i in dv, j in dk
+ *
+ * Ownership: every pointer is caller-owned DEVICE memory on the current CUDA
+ * device; the library never frees it.  The library owns its workspace
+ * (per-frame A_f, U_f and the bf16 per-frame states, see
+ * gdn_workspace_bytes), taken with stream-ordered allocation on `stream` from
+ * a library memory pool and returned on the same stream, so calls on
+ * different streams do not share scratch.
+ *
+ * Semantics: every entry point validates its arguments on the host first and
+ * launches nothing if they are bad.  A launched call is asynchronous on
+ * `stream`; kernel-side failures (a bounded wait that ran out) are recorded
+ * on the device and reported by gdn_sync_status().  No entry point throws,
+ * exits or aborts.  Results are deterministic: no atomics take part in any
+ * sum, and every reduction runs in a fixed order.
+ *
+ * Supported sizes: B, H, F, N >= 1; dk and dv multiples of 16 in [16, 128];
+ * B*F*N*H*max(dk,dv) < 2^31 elements per tensor.  Pointers must be 16-byte
+ * aligned (tensor-memory-accelerator copies require it).
+ */
+#ifndef GDN_B300_H
+#define GDN_B300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st* gdn_stream_t;
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_NULL_PTR = 1,     /* a required pointer is NULL                       */
+    GDN_ERR_BAD_DIM = 2,      /* B, H, F or N < 1, or a tensor too large           */
+    GDN_ERR_UNSUPPORTED = 3,  /* dk or dv not a multiple of 16 in [16,128]        */
+    GDN_ERR_MISALIGNED = 4,   /* a pointer is not 16-byte aligned                 */
+    GDN_ERR_ALLOC = 5,        /* workspace allocation failed                       */
+    GDN_ERR_LAUNCH = 6,       /* a kernel launch or CUDA runtime call failed       */
+    GDN_ERR_TIMEOUT = 7,      /* a device-side bounded wait ran out (sync_status) */
+    GDN_ERR_ALIAS = 8,        /* out overlaps an input                             */
+    GDN_ERR_NO_DEVICE = 9     /* no usable sm_103 device is current               */
+} gdn_status;
+
+/*
+ * Whole-sequence forward: runs all F frames of every (b, h) and writes every
+ * O_f to `out` and S_F to `state_out`.
+ *   state_in   may be NULL (S_0 = 0).
+ *   state_out  may be NULL (final state not wanted) or equal to state_in
+ *              (in-place resident state); it must not partially overlap it.
+ *   out        must not overlap q, k, v, alpha, beta or the states.
+ * Phases (one launch each, in stream order): frame-parallel contractions
+ * A_f = K_f^T B_f K_f and U_f = V_f^T B_f K_f on tcgen05 tensor cores; the
+ * sequential scan S_f = alpha_f (S_{f-1} - S_{f-1} A_f) + U_f; the
+ * frame-parallel output O_f = Q_f S_f^T on tcgen05 tensor cores.
+ */
+gdn_status gdn_frame_forward(const void* q, const void* k, const void* v,
+                             const float* alpha, const float* beta,
+                             const float* state_in, void* out, float* state_out,
+                             int B, int H, int F, int N, int dk, int dv,
+                             gdn_stream_t stream);
+
+/*
+ * One-frame step for interactive rollout (WorldFoundry model card, "What it
+ * is for": a resident pipeline that advances in native 8k+1 windows): the same
+ * operation with F = 1 on a resident state.
+ *   q, k   bf16 [B, N, H, dk];  v, out bf16 [B, N, H, dv];
+ *   alpha  fp32 [B, H];         beta fp32 [B, N, H];
+ *   state_in / state_out fp32 [B, H, dv, dk]; state_out may equal state_in.
+ * The frame's tokens are split across CTAs; the per-split partial sums are
+ * added in a fixed order, so the result is deterministic.
+ */
+gdn_status gdn_frame_step(const void* q, const void* k, const void* v,
+                          const float* alpha, const float* beta,
+                          const float* state_in, void* out, float* state_out,
+                          int B, int H, int N, int dk, int dv,
+                          gdn_stream_t stream);
+
+/* Bytes of library workspace one gdn_frame_forward call of this shape takes
+ * (0 for invalid shapes). */
+size_t gdn_workspace_bytes(int B, int H, int F, int N, int dk, int dv);
+
+/* Bytes of library workspace one gdn_frame_step call of this shape takes. */
+size_t gdn_step_workspace_bytes(int B, int H, int N, int dk, int dv);
+
+/* Static, human-readable name of a status code. */
+const char* gdn_status_string(gdn_status s);
+
+/*
+ * Synchronises `stream`, then returns the first error any kernel of this
+ * library recorded on the current device since the last call (for example
+ * GDN_ERR_TIMEOUT from a bounded wait), or GDN_ERR_LAUNCH if the stream
+ * reports a CUDA error; clears the recorded device error.
+ */
+gdn_status gdn_sync_status(gdn_stream_t stream);
+
+/*
+ * Upper bound, in nanoseconds, of every device-side wait (mbarrier phase
+ * waits) in this library's kernels; a wait that runs out records
+ * GDN_ERR_TIMEOUT and the kernel returns early.  Default 2e9 (2 s).
+ * Values < 1000 are raised to 1000.  Applies to launches after the call.
+ */
+void gdn_set_wait_limit_ns(unsigned long long limit_ns);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one small kernel that
+ * waits on a shared-memory barrier that nothing ever completes, with a wait
+ * limit of `limit_ns`; the wait runs out, the kernel records GDN_ERR_TIMEOUT
+ * and returns.  No fault, trap or hang is involved.  Read the result with
+ * gdn_sync_status().
+ */
+gdn_status gdn_selftest_wait_timeout(unsigned long long limit_ns, gdn_stream_t stream);
+
+/* Library version string. */
+const char* gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_B300_H */
