@@ -1,0 +1,365 @@
+#!/usr/bin/env python3
+"""Benchmark of the frame-wise Gated DeltaNet forward on B300.
+
+One step = one gdn_frame_forward call over the 60 s 720p latent sequence
+(B=1, H=16, F=121 latent frames x N=880 tokens, dk=dv=128; inputs resident in
+HBM).  Prints ONE JSON line (rank 0):
+
+  value       whole-job tokens/s (device time, CUDA events, max over ranks)
+  roofline    the dominant kernel's algorithmic bytes / its event-timed
+              duration against the measured HBM copy bandwidth
+  e2e         the same metric through gdn_frame_forward_host on pinned host
+              buffers, host<->device copies inside the timed region
+  cpu_baseline  the fp64 CPU oracle on the host cores (rank 0, N=1 only)
+  clocks      nvidia-smi samples taken during the timed region
+
+--impl reference times the fp64 CPU oracle on the same workload instead
+(a bounded sample of frames per step).
+
+Multi-GPU: launch under torchrun; each rank runs its own sequence (weak
+scaling, replicas only: no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN fwd tokens/s (121×880 tok, 16 heads, d=128) and % tensor/HBM roofline"
+UNIT = "tokens/s"
+WORKLOAD = "seq60s"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-budget-s", type=float, default=90.0,
+                    help="wall-clock budget of the --impl reference run")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def kernel_costs(w):
+    """Algorithmic bytes and FLOPs of one launch of each phase."""
+    T = w.B * w.F * w.N            # tokens
+    items = w.B * w.F * w.H        # (b, f, h) items
+    dk, dv, H = w.dk, w.dv, w.H
+    ws_a = items * dk * dk * 2     # A_f bf16
+    ws_u = items * dv * dk * 4     # U_f fp32
+    ws_s = items * dv * dk * 2     # S_f bf16
+    state = w.B * H * dv * dk * 4
+    return {
+        "k1_contract": {"bytes": T * H * (dk + dv) * 2 + T * H * 4 + ws_a + ws_u,
+                        "flops": 2 * T * H * dk * (dk + dv)},
+        "k2_scan": {"bytes": ws_a + ws_u + ws_s + w.B * w.F * H * 4 + 2 * state,
+                    "flops": 2 * items * dv * dk * dk},
+        "k3_output": {"bytes": T * H * dk * 2 + ws_s + T * H * dv * 2,
+                      "flops": 2 * T * H * dk * dv},
+    }
+
+
+def path_floor_bytes(w):
+    """Compulsory HBM bytes of the whole forward: q, k, v read, out written, beta, alpha, state."""
+    T = w.B * w.F * w.N
+    return (T * w.H * (2 * w.dk + w.dv) * 2 + T * w.H * w.dv * 2 + T * w.H * 4 + w.B * w.F * w.H * 4
+            + w.B * w.H * w.dv * w.dk * 4)
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "frame_wise_gated_forward_b300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """dram bytes per launch of `kernel` from the committed ncu summary, or None
+    if absent or taken on a different kernel source."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    d = json.load(open(PROFILE_TRAFFIC))
+    if d.get("source_sha") != kernel_source_sha():
+        return None
+    k = d.get("kernels", {}).get(kernel)
+    return None if k is None else k.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock, max clock, power and throttle reasons."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 9:
+                self.samples.append((time.perf_counter(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        used = inside if inside else [p for (t, p) in self.samples]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in used if num(p[1]) is not None]
+        mx = [num(p[2]) for p in used if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in used for i in range(4) if p[5 + i].lower() == "active"})
+        pw = [num(p[3]) for p in used if num(p[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(used), "samples_in_region": len(inside),
+                "power_w_max": max(pw) if pw else None}
+
+
+def cpu_baseline_run(w, x, frames):
+    """Time the fp64 oracle (as it stands) on the first `frames` frames of the workload."""
+    import oracle
+    sub = {k: (v[:, :frames].contiguous() if k != "state_in" else v) for k, v in x.items()}
+    t0 = time.perf_counter()
+    oracle.frame_forward(sub["q"], sub["k"], sub["v"], sub["alpha"], sub["beta"], sub["state_in"],
+                         B=w.B, H=w.H, F=frames, N=w.N, dk=w.dk, dv=w.dv, want_out=True)
+    dt = time.perf_counter() - t0
+    return w.B * frames * w.N, dt, oracle.max_threads()
+
+
+def run_reference(args, w):
+    """--impl reference: the fp64 CPU oracle on a bounded sample of the workload per step."""
+    from frame_wise_gated_forward_b300 import inputs, replicas
+    rank, _, world = replicas.env_world()
+    if rank != 0:
+        return
+    import oracle
+    x = inputs.workload_inputs(w)
+    # calibrate: one frame, then size the per-step sample to the budget
+    _, t1, cores = cpu_baseline_run(w, x, 1)
+    per_step = args.reference_budget_s / max(1, args.steps + args.warmup)
+    frames = int(max(1, min(w.F, per_step / max(t1, 1e-6))))
+    for _ in range(args.warmup):
+        cpu_baseline_run(w, x, frames)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cpu_baseline_run(w, x, frames)
+    dt = time.perf_counter() - t0
+    tokens = w.B * frames * w.N
+    value = tokens * args.steps / dt
+    sample = f"first {frames} of {w.F} latent frames ({tokens} tokens x {w.H} heads, all outputs) per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"{w.name}: B={w.B} H={w.H} F={w.F} N={w.N} dk={w.dk} dv={w.dv}",
+                                        "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    import torch
+
+    from frame_wise_gated_forward_b300 import inputs, replicas
+    w = inputs.WORKLOADS[WORKLOAD]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    from frame_wise_gated_forward_b300 import api, build
+    rank, local_rank, world = replicas.env_world()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the product path has no CPU fallback)")
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    replicas.init("nccl")
+    build.build()
+    peaks = load_peaks()
+
+    x = inputs.workload_inputs(w)
+    xd = {k: v.to(device) for k, v in x.items()}
+    zero_state = inputs.has_zero_state(w)
+    s_in = None if zero_state else xd["state_in"]
+    out = torch.empty((w.B, w.F, w.N, w.H, w.dv), dtype=torch.bfloat16, device=device)
+    st = torch.empty((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        api.frame_forward(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], s_in, out=out, state_out=st)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    api.sync_status()
+
+    # ---------------------------------------------------------------- timed region
+    cvd = [c for c in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if c.strip()]
+    sampler = ClockSampler(cvd[local_rank].strip() if local_rank < len(cvd) else local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(device)
+    replicas.barrier(device)
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    tw0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    tw1 = time.perf_counter()
+    replicas.barrier(device)
+    torch.cuda.synchronize(device)
+    sampler.stop()
+    api.sync_status()
+    sec = e0.elapsed_time(e1) / 1e3
+    sec_max = replicas.max_over_ranks(sec, device)
+    tokens = w.tokens
+    value = replicas.throughput(tokens, args.steps, sec_max, world)
+    clocks = sampler.summary(tw0, tw1)
+
+    # ------------------------------------------------ per-kernel event timing
+    nk = min(args.steps, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nk)]
+    for row in evs:
+        for e in row:
+            e.record(stream)  # materialise the CUDA event handles
+    torch.cuda.synchronize(device)
+    for i in range(nk):
+        api.frame_forward_timed(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], s_in, out, st, evs[i])
+    torch.cuda.synchronize(device)
+    api.sync_status()
+    names = ["k1_contract", "k2_scan", "k3_output"]
+    phase_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(nk))
+                for j, n in enumerate(names)}
+    costs = kernel_costs(w)
+    phases = {}
+    for n in names:
+        t = phase_ms[n] / 1e3
+        phases[n] = {"ms": phase_ms[n], "GB/s": costs[n]["bytes"] / t / 1e9,
+                     "hbm_frac": costs[n]["bytes"] / t / 1e9 / peaks["hbm_gbs"],
+                     "TFLOP/s": costs[n]["flops"] / t / 1e12,
+                     "tensor_frac": costs[n]["flops"] / t / 1e12 / peaks["bf16_tflops"]}
+    dom = max(names, key=lambda n: phase_ms[n])
+    achieved = costs[dom]["bytes"] / (phase_ms[dom] / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(dom), "kernel": dom,
+                "peak_source": peaks["source"], "algorithmic_bytes": costs[dom]["bytes"]}
+    ms_per_step = sec_max / args.steps * 1e3
+    floor_ms = path_floor_bytes(w) / (peaks["hbm_gbs"] * 1e9) * 1e3
+
+    # ---------------------------------------------------------------------- e2e
+    hx = {k: v.pin_memory() for k, v in x.items()}
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h_st = torch.empty(st.shape, dtype=st.dtype, pin_memory=True)
+    hs_in = None if zero_state else hx["state_in"]
+    api.frame_forward_host(hx["q"], hx["k"], hx["v"], hx["alpha"], hx["beta"], hs_in, out=h_out, state_out=h_st)
+    torch.cuda.synchronize(device)
+    replicas.barrier(device)
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.e2e_steps):
+        api.frame_forward_host(hx["q"], hx["k"], hx["v"], hx["alpha"], hx["beta"], hs_in,
+                               out=h_out, state_out=h_st)
+    g1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_sec = replicas.max_over_ranks(g0.elapsed_time(g1) / 1e3, device)
+    e2e_value = replicas.throughput(tokens, args.e2e_steps, e2e_sec, world)
+    h2d = sum(hx[k].numel() * hx[k].element_size() for k in ("q", "k", "v", "alpha", "beta"))
+    if hs_in is not None:
+        h2d += hs_in.numel() * hs_in.element_size()
+    d2h = h_out.numel() * h_out.element_size() + h_st.numel() * h_st.element_size()
+
+    # -------------------------------------------------------- CPU baseline
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_tok, dt, cores = cpu_baseline_run(w, x, w.F)
+        cpu = {"value": n_tok / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"full {w.name} workload ({n_tok} tokens x {w.H} heads, all outputs), one pass, fp64"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{w.name}: 60 s 720p latent sequence, B={w.B} H={w.H} F={w.F} N={w.N} "
+                                   f"dk={w.dk} dv={w.dv}, bf16 q/k/v/out, fp32 alpha/beta/state",
+                       "tokens_per_step_per_gpu": tokens,
+                       "l2": "inputs 1.31 GB per step > 126 MB L2; no flush",
+                       "parallelism": f"replicas x{world} (no data-path collective)"},
+            "roofline": roofline,
+            "phases": phases,
+            "path_roofline": {"floor_ms": floor_ms, "frac": floor_ms / ms_per_step,
+                              "ceiling_tokens_per_s": tokens / (floor_ms / 1e3) * world},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": args.e2e_steps},
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "gpu_launches": 3 * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    replicas.shutdown()
+
+
+if __name__ == "__main__":
+    main()

@@ -18,7 +18,8 @@ STATUS = {
     8: "GDN_ERR_ALIAS", 9: "GDN_ERR_NO_DEVICE",
 }
 EXPORTS = (
-    "gdn_frame_forward", "gdn_frame_step", "gdn_workspace_bytes", "gdn_step_workspace_bytes",
+    "gdn_frame_forward", "gdn_frame_step", "gdn_frame_forward_timed", "gdn_frame_forward_host",
+    "gdn_workspace_bytes", "gdn_step_workspace_bytes",
     "gdn_status_string", "gdn_sync_status", "gdn_set_wait_limit_ns", "gdn_selftest_wait_timeout",
     "gdn_version",
 )
@@ -48,6 +49,11 @@ def load(path: str | None = None):
     lib.gdn_frame_forward.restype = ctypes.c_int
     lib.gdn_frame_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, st]
     lib.gdn_frame_step.restype = ctypes.c_int
+    lib.gdn_frame_forward_timed.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, st,
+                                            ctypes.POINTER(ctypes.c_void_p)]
+    lib.gdn_frame_forward_timed.restype = ctypes.c_int
+    lib.gdn_frame_forward_host.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, st]
+    lib.gdn_frame_forward_host.restype = ctypes.c_int
     lib.gdn_workspace_bytes.argtypes = [i] * 6
     lib.gdn_workspace_bytes.restype = ctypes.c_size_t
     lib.gdn_step_workspace_bytes.argtypes = [i] * 5

@@ -11,6 +11,8 @@ the current device; calls run on torch's current CUDA stream.
 """
 from __future__ import annotations
 
+import ctypes
+
 import torch
 
 from ._lib import GDNError, check, load
@@ -82,23 +84,62 @@ def frame_step(q, k, v, alpha, beta, state_in=None, *, out=None, state_out=None,
     return out, state_out
 
 
-def frame_forward_host(q, k, v, alpha, beta, state_in=None, *, out=None, state_out=None, device=None):
-    """End-to-end call on HOST tensors: copies the inputs to the device, runs
-    gdn_frame_forward, copies out and the final state back (pinned host
-    tensors make the copies asynchronous).  Returns host tensors."""
-    device = device or torch.device("cuda", torch.cuda.current_device())
-    nb = q.is_pinned()
-    dq, dk_, dv_ = (t.to(device, non_blocking=nb) for t in (q, k, v))
-    da, db = alpha.to(device, non_blocking=nb), beta.to(device, non_blocking=nb)
-    ds = None if state_in is None else state_in.to(device, non_blocking=nb)
-    o, s = frame_forward(dq, dk_, dv_, da, db, ds)
+def frame_forward_timed(q, k, v, alpha, beta, state_in, out, state_out, events, stream=None):
+    """gdn_frame_forward that also records four torch.cuda.Event objects
+    (already recorded once, so their CUDA handles exist) before phase 1,
+    before phase 2, before phase 3 and after phase 3."""
+    lib = load()
+    B, F, N, H, dk = q.shape
+    dv = v.shape[-1]
+    handles = (ctypes.c_void_p * 4)(*[int(e.cuda_event) for e in events])
+    args = [
+        _dev(q, "q", torch.bfloat16, (B, F, N, H, dk)),
+        _dev(k, "k", torch.bfloat16, (B, F, N, H, dk)),
+        _dev(v, "v", torch.bfloat16, (B, F, N, H, dv)),
+        _dev(alpha, "alpha", torch.float32, (B, F, H)),
+        _dev(beta, "beta", torch.float32, (B, F, N, H)),
+        None if state_in is None else _dev(state_in, "state_in", torch.float32, (B, H, dv, dk)),
+        _dev(out, "out", torch.bfloat16, (B, F, N, H, dv)),
+        _dev(state_out, "state_out", torch.float32, (B, H, dv, dk)),
+    ]
+    check(lib.gdn_frame_forward_timed(*args, B, H, F, N, dk, dv, _stream_handle(stream), handles),
+          "gdn_frame_forward_timed")
+    return out, state_out
+
+
+def _host(t, name, dtype, shape):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)}")
+    return t.data_ptr()
+
+
+def frame_forward_host(q, k, v, alpha, beta, state_in=None, *, out=None, state_out=None, stream=None):
+    """End-to-end call on HOST tensors through gdn_frame_forward_host: the
+    library copies the inputs to the device, runs the forward and copies out
+    and the final state back before returning.  Page-locked (pinned) tensors
+    give full-speed copies.  Returns host tensors (out, state_out)."""
+    lib = load()
+    B, F, N, H, dk = q.shape
+    dv = v.shape[-1]
+    pin = q.is_pinned()
     if out is None:
-        out = torch.empty(o.shape, dtype=o.dtype, pin_memory=nb)
+        out = torch.empty((B, F, N, H, dv), dtype=torch.bfloat16, pin_memory=pin)
     if state_out is None:
-        state_out = torch.empty(s.shape, dtype=s.dtype, pin_memory=nb)
-    out.copy_(o, non_blocking=nb)
-    state_out.copy_(s, non_blocking=nb)
-    torch.cuda.current_stream().synchronize()
+        state_out = torch.empty((B, H, dv, dk), dtype=torch.float32, pin_memory=pin)
+    args = [
+        _host(q, "q", torch.bfloat16, (B, F, N, H, dk)),
+        _host(k, "k", torch.bfloat16, (B, F, N, H, dk)),
+        _host(v, "v", torch.bfloat16, (B, F, N, H, dv)),
+        _host(alpha, "alpha", torch.float32, (B, F, H)),
+        _host(beta, "beta", torch.float32, (B, F, N, H)),
+        None if state_in is None else _host(state_in, "state_in", torch.float32, (B, H, dv, dk)),
+        _host(out, "out", torch.bfloat16, (B, F, N, H, dv)),
+        _host(state_out, "state_out", torch.float32, (B, H, dv, dk)),
+    ]
+    check(lib.gdn_frame_forward_host(*args, B, H, F, N, dk, dv, _stream_handle(stream)),
+          "gdn_frame_forward_host")
     return out, state_out
 
 
@@ -126,6 +167,6 @@ def selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     return int(lib.gdn_sync_status(_stream_handle(stream)))
 
 
-__all__ = ["frame_forward", "frame_step", "frame_forward_host", "workspace_bytes",
+__all__ = ["frame_forward", "frame_step", "frame_forward_timed", "frame_forward_host", "workspace_bytes",
            "step_workspace_bytes", "sync_status", "set_wait_limit_ns", "selftest_wait_timeout",
            "GDNError"]

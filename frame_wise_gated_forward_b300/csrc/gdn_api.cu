@@ -210,7 +210,7 @@ bool encode_mats(CUtensorMap* m, const void* base, long long items, int rows_tot
 // ------------------------------------------------------------- the pass
 gdn_status run_pass(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
                     const float* state_in, void* out, float* state_out, int B, int H, int F, int N, int dk, int dv,
-                    bool step, cudaStream_t stream) {
+                    bool step, cudaStream_t stream, cudaEvent_t const* ev = nullptr) {
     int dev;
     DeviceState* ds;
     gdn_status st = device_ready(&dev, &ds);
@@ -263,6 +263,7 @@ gdn_status run_pass(const void* q, const void* k, const void* v, const float* al
         p1.work = static_cast<int>(items * nsplit);
         p1.wait_limit_ns = lim;
         const int g1 = std::min(p1.work, ds->sms);
+        if (ev) cudaEventRecord(ev[0], stream);
         gdn::k1::contract_kernel<<<g1, gdn::k1::THREADS, gdn::k1::SMEM_BYTES, stream>>>(tm_k, tm_v, p1);
         if (nsplit > 1) {
             const size_t total = static_cast<size_t>(items) * (dk * dk + dv * dk);
@@ -270,6 +271,7 @@ gdn_status run_pass(const void* q, const void* k, const void* v, const float* al
             gdn::k1::reduce_partials_kernel<<<blocks, 256, 0, stream>>>(partial, A_ws, U_ws, static_cast<int>(items),
                                                                        nsplit, dk, dv);
         }
+        if (ev) cudaEventRecord(ev[1], stream);
         // phase 2
         gdn::k2::Params p2;
         p2.alpha = alpha;
@@ -287,6 +289,7 @@ gdn_status run_pass(const void* q, const void* k, const void* v, const float* al
             gdn::k2::scan_kernel<32><<<g2, gdn::k2::THREADS, gdn::k2::Cfg<32>::SMEM_BYTES, stream>>>(tm_A, tm_S_store, p2);
         else
             gdn::k2::scan_kernel<16><<<g2, gdn::k2::THREADS, gdn::k2::Cfg<16>::SMEM_BYTES, stream>>>(tm_A, tm_S_store, p2);
+        if (ev) cudaEventRecord(ev[2], stream);
         // phase 3
         gdn::k3::Params p3;
         p3.H = H;
@@ -298,6 +301,7 @@ gdn_status run_pass(const void* q, const void* k, const void* v, const float* al
         p3.wait_limit_ns = lim;
         const int g3 = static_cast<int>(std::min<long long>(p3.total, ds->sms));
         gdn::k3::output_kernel<<<g3, gdn::k3::THREADS, gdn::k3::SMEM_BYTES, stream>>>(tm_q, tm_S_load, tm_out, p3);
+        if (ev) cudaEventRecord(ev[3], stream);
         if (cudaGetLastError() != cudaSuccess) result = GDN_ERR_LAUNCH;
     }
     cudaFreeAsync(ws, stream);
@@ -336,6 +340,62 @@ gdn_status gdn_frame_step(const void* q, const void* k, const void* v, const flo
     if (s != GDN_OK) return s;
     return run_pass(q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv, true,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_frame_forward_timed(const void* q, const void* k, const void* v, const float* alpha,
+                                   const float* beta, const float* state_in, void* out, float* state_out, int B,
+                                   int H, int F, int N, int dk, int dv, gdn_stream_t stream,
+                                   void* const* phase_events) {
+    if (phase_events == nullptr || !phase_events[0] || !phase_events[1] || !phase_events[2] || !phase_events[3])
+        return GDN_ERR_NULL_PTR;
+    gdn_status s = validate(q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv);
+    if (s != GDN_OK) return s;
+    cudaEvent_t ev[4];
+    for (int i = 0; i < 4; ++i) ev[i] = static_cast<cudaEvent_t>(phase_events[i]);
+    return run_pass(q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv, false,
+                    reinterpret_cast<cudaStream_t>(stream), ev);
+}
+
+gdn_status gdn_frame_forward_host(const void* q, const void* k, const void* v, const float* alpha,
+                                  const float* beta, const float* state_in, void* out, float* state_out, int B,
+                                  int H, int F, int N, int dk, int dv, gdn_stream_t stream) {
+    gdn_status s = validate(q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv);
+    if (s != GDN_OK) return s;
+    int dev;
+    DeviceState* ds;
+    s = device_ready(&dev, &ds);
+    if (s != GDN_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t tok = static_cast<size_t>(B) * F * N;
+    const size_t bq = tok * H * dk * 2, bv = tok * H * dv * 2, ba = static_cast<size_t>(B) * F * H * 4,
+                 bb = tok * H * 4, bs = static_cast<size_t>(B) * H * dv * dk * 4;
+    size_t off[8], total = 0;
+    const size_t sizes[8] = {bq, bq, bv, ba, bb, state_in ? bs : 0, bv, state_out ? bs : 0};
+    for (int i = 0; i < 8; ++i) { off[i] = total; total = align256(total + sizes[i]); }
+    uint8_t* d = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&d), total, ds->pool, st) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_ALLOC;
+    }
+    const void* src[6] = {q, k, v, alpha, beta, state_in};
+    bool ok = true;
+    for (int i = 0; i < 6 && ok; ++i)
+        if (sizes[i]) ok = cudaMemcpyAsync(d + off[i], src[i], sizes[i], cudaMemcpyHostToDevice, st) == cudaSuccess;
+    gdn_status r = ok ? GDN_OK : GDN_ERR_LAUNCH;
+    if (r == GDN_OK)
+        r = run_pass(d + off[0], d + off[1], d + off[2], reinterpret_cast<const float*>(d + off[3]),
+                     reinterpret_cast<const float*>(d + off[4]),
+                     state_in ? reinterpret_cast<const float*>(d + off[5]) : nullptr, d + off[6],
+                     state_out ? reinterpret_cast<float*>(d + off[7]) : nullptr, B, H, F, N, dk, dv, false, st);
+    if (r == GDN_OK) {
+        ok = cudaMemcpyAsync(out, d + off[6], bv, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+        if (ok && state_out) ok = cudaMemcpyAsync(state_out, d + off[7], bs, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+        if (!ok) r = GDN_ERR_LAUNCH;
+    }
+    cudaFreeAsync(d, st);
+    if (cudaStreamSynchronize(st) != cudaSuccess && r == GDN_OK) r = GDN_ERR_LAUNCH;
+    cudaGetLastError();
+    return r;
 }
 
 size_t gdn_workspace_bytes(int B, int H, int F, int N, int dk, int dv) {

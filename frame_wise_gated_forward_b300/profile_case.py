@@ -1,0 +1,55 @@
+"""Run the frame-wise GDN forward a few times on a 60 s-sequence-shaped case
+with a chosen number of latent frames, for profilers (ncu) to capture.
+
+    python -m frame_wise_gated_forward_b300.profile_case --frames 31 --iters 2
+
+Shapes are those of the 60 s 720p workload (H=16, N=880, d=128) with F
+frames; inputs come from the seeded generator.  Prints the event-timed
+milliseconds per call.
+"""
+import argparse
+import os
+import sys
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from frame_wise_gated_forward_b300 import api, build, inputs  # noqa: E402
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--frames", type=int, default=31)
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--heads", type=int, default=16)
+    ap.add_argument("--tokens", type=int, default=880)
+    ap.add_argument("--d", type=int, default=128)
+    ap.add_argument("--iters", type=int, default=2)
+    ap.add_argument("--step", action="store_true", help="profile gdn_frame_step instead (F ignored)")
+    a = ap.parse_args()
+    build.build()
+    F = 1 if a.step else a.frames
+    x = inputs.draw(a.batch, a.heads, F, a.tokens, a.d, a.d, seed=0, s0_std=0.0)
+    xd = {k: v.cuda() for k, v in x.items()}
+    if a.step:
+        args = [xd[k][:, 0].contiguous() for k in ("q", "k", "v", "alpha", "beta")]
+        call = lambda: api.frame_step(*args, xd["state_in"])  # noqa: E731
+    else:
+        call = lambda: api.frame_forward(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], None)  # noqa: E731
+    call()
+    api.sync_status()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.iters):
+        call()
+    e1.record()
+    api.sync_status()
+    print(f"{'step' if a.step else 'forward'} B={a.batch} H={a.heads} F={F} N={a.tokens} d={a.d}: "
+          f"{e0.elapsed_time(e1) / a.iters:.4f} ms/call")
+
+
+if __name__ == "__main__":
+    main()

@@ -99,6 +99,32 @@ gdn_status gdn_frame_step(const void* q, const void* k, const void* v,
                           int B, int H, int N, int dk, int dv,
                           gdn_stream_t stream);
 
+/*
+ * gdn_frame_forward with per-phase timing: records the caller's CUDA events
+ * phase_events[0..3] (cudaEvent_t handles, created by the caller) on `stream`
+ * before phase 1, before phase 2, before phase 3 and after phase 3, so that
+ * cudaEventElapsedTime gives each kernel's duration.  Same contract and
+ * results as gdn_frame_forward.  NULL events -> GDN_ERR_NULL_PTR.
+ */
+gdn_status gdn_frame_forward_timed(const void* q, const void* k, const void* v,
+                                   const float* alpha, const float* beta,
+                                   const float* state_in, void* out, float* state_out,
+                                   int B, int H, int F, int N, int dk, int dv,
+                                   gdn_stream_t stream, void* const* phase_events);
+
+/*
+ * gdn_frame_forward on HOST buffers (same layouts): copies the inputs to
+ * library-owned device memory on `stream`, runs the forward, copies `out` and
+ * (if not NULL) `state_out` back, and returns after synchronising `stream`.
+ * Page-locked host buffers make the copies run at full link speed.  The
+ * end-to-end cost of one call therefore includes both transfers.
+ */
+gdn_status gdn_frame_forward_host(const void* q, const void* k, const void* v,
+                                  const float* alpha, const float* beta,
+                                  const float* state_in, void* out, float* state_out,
+                                  int B, int H, int F, int N, int dk, int dv,
+                                  gdn_stream_t stream);
+
 /* Bytes of library workspace one gdn_frame_forward call of this shape takes
  * (0 for invalid shapes). */
 size_t gdn_workspace_bytes(int B, int H, int F, int N, int dk, int dv);
