@@ -15,13 +15,13 @@ from . import build as _build
 STATUS = {
     0: "GDN_OK", 1: "GDN_ERR_NULL_PTR", 2: "GDN_ERR_BAD_DIM", 3: "GDN_ERR_UNSUPPORTED",
     4: "GDN_ERR_MISALIGNED", 5: "GDN_ERR_ALLOC", 6: "GDN_ERR_LAUNCH", 7: "GDN_ERR_TIMEOUT",
-    8: "GDN_ERR_ALIAS", 9: "GDN_ERR_NO_DEVICE",
+    8: "GDN_ERR_ALIAS", 9: "GDN_ERR_NO_DEVICE", 10: "GDN_ERR_TOO_LARGE",
 }
 EXPORTS = (
     "gdn_frame_forward", "gdn_frame_step", "gdn_frame_forward_timed", "gdn_frame_forward_host",
     "gdn_workspace_bytes", "gdn_step_workspace_bytes",
     "gdn_status_string", "gdn_sync_status", "gdn_set_wait_limit_ns", "gdn_selftest_wait_timeout",
-    "gdn_version",
+    "gdn_version", "gdn_frame_step_noalloc",
 )
 
 
@@ -66,6 +66,8 @@ def load(path: str | None = None):
     lib.gdn_set_wait_limit_ns.restype = None
     lib.gdn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, st]
     lib.gdn_selftest_wait_timeout.restype = ctypes.c_int
+    lib.gdn_frame_step_noalloc.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, st]
+    lib.gdn_frame_step_noalloc.restype = ctypes.c_int
     lib.gdn_version.argtypes = []
     lib.gdn_version.restype = ctypes.c_char_p
     if path is None:

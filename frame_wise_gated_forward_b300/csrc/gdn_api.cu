@@ -427,6 +427,7 @@ const char* gdn_status_string(gdn_status s) {
         case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a device-side bounded wait ran out";
         case GDN_ERR_ALIAS: return "GDN_ERR_ALIAS: an output overlaps an input";
         case GDN_ERR_NO_DEVICE: return "GDN_ERR_NO_DEVICE: no usable sm_103 device is current";
+        case GDN_ERR_TOO_LARGE: return "GDN_ERR_TOO_LARGE: the step needs more scratch than GDN_STEP_NOALLOC_SCRATCH_BYTES";
     }
     return "GDN_ERR_UNKNOWN";
 }
@@ -466,3 +467,123 @@ gdn_status gdn_selftest_wait_timeout(unsigned long long limit_ns, gdn_stream_t s
 const char* gdn_version(void) { return "gdn-b300 0.1 (sm_103a, tcgen05)"; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free step (gdn_frame_step_noalloc).  For callers that cannot
+// allocate device memory while they advance a resident state.  The workspace
+// of the step path lives in one file-scope device array instead of a pool
+// allocation; the kernels and their launch shapes are those of gdn_frame_step.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kStepScratchBytes = GDN_STEP_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) uint8_t g_step_scratch[kStepScratchBytes];
+
+// Device address of g_step_scratch per device.  In host code the name
+// g_step_scratch is only a host-side stand-in for the symbol, never a device
+// address, so it is looked up once per device with that device current.
+uint8_t* g_step_scratch_dev[kMaxDevices] = {};
+std::mutex g_step_scratch_mu;
+
+gdn_status step_scratch_address(int dev, uint8_t** out) {
+    std::lock_guard<std::mutex> lk(g_step_scratch_mu);
+    if (g_step_scratch_dev[dev] == nullptr) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_step_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return GDN_ERR_LAUNCH;
+        }
+        g_step_scratch_dev[dev] = static_cast<uint8_t*>(p);
+    }
+    *out = g_step_scratch_dev[dev];
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" gdn_status gdn_frame_step_noalloc(const void* q, const void* k, const void* v, const float* alpha,
+                                             const float* beta, const float* state_in, void* out,
+                                             float* state_out, int B, int H, int N, int dk, int dv,
+                                             gdn_stream_t stream_handle) {
+    gdn_status st = validate(q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv);
+    if (st != GDN_OK) return st;
+    int dev;
+    DeviceState* ds;
+    st = device_ready(&dev, &ds);
+    if (st != GDN_OK) return st;
+    const long long items = static_cast<long long>(B) * H;
+    const int nsplit = step_nsplit(ds->sms, B, H, N);
+    const Layout L = layout_of(items, dk, dv, nsplit);
+    if (L.total > kStepScratchBytes) return GDN_ERR_TOO_LARGE;
+    if (!is_device_ptr(q) || !is_device_ptr(k) || !is_device_ptr(v) || !is_device_ptr(alpha) ||
+        !is_device_ptr(beta) || !is_device_ptr(state_in) || !is_device_ptr(out) || !is_device_ptr(state_out))
+        return GDN_ERR_NULL_PTR;
+    uint8_t* ws = nullptr;
+    st = step_scratch_address(dev, &ws);
+    if (st != GDN_OK) return st;
+
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+    __nv_bfloat16* A_ws = reinterpret_cast<__nv_bfloat16*>(ws + L.a_off);
+    float* U_ws = reinterpret_cast<float*>(ws + L.u_off);
+    __nv_bfloat16* S_all = reinterpret_cast<__nv_bfloat16*>(ws + L.s_off);
+    float* partial = nsplit > 1 ? reinterpret_cast<float*>(ws + L.p_off) : nullptr;
+    const int R = (dv % 32 == 0) ? 32 : 16;
+    CUtensorMap tm_k, tm_v, tm_q, tm_out, tm_A, tm_S_store, tm_S_load;
+    if (!(encode_tokens(&tm_k, k, B, N, H, dk, gdn::k1::CHUNK) && encode_tokens(&tm_v, v, B, N, H, dv, gdn::k1::CHUNK) &&
+          encode_tokens(&tm_q, q, B, N, H, dk, gdn::k3::TILE_M) && encode_tokens(&tm_out, out, B, N, H, dv, 32) &&
+          encode_mats(&tm_A, A_ws, items, dk, dk, 128) && encode_mats(&tm_S_store, S_all, items, dv, dk, R) &&
+          encode_mats(&tm_S_load, S_all, items, dv, dk, 128)))
+        return GDN_ERR_LAUNCH;
+    const unsigned long long lim = g_wait_limit_ns.load();
+
+    gdn::k1::Params p1;
+    p1.beta = beta;
+    p1.A_ws = A_ws;
+    p1.U_ws = U_ws;
+    p1.partial = partial;
+    p1.H = H;
+    p1.N = N;
+    p1.dk = dk;
+    p1.dv = dv;
+    p1.items = static_cast<int>(items);
+    p1.nsplit = nsplit;
+    p1.chunks = (N + gdn::k1::CHUNK - 1) / gdn::k1::CHUNK;
+    p1.work = static_cast<int>(items * nsplit);
+    p1.wait_limit_ns = lim;
+    gdn::k1::contract_kernel<<<std::min(p1.work, ds->sms), gdn::k1::THREADS, gdn::k1::SMEM_BYTES, stream>>>(tm_k, tm_v,
+                                                                                                        p1);
+    if (nsplit > 1) {
+        const size_t total = static_cast<size_t>(items) * (dk * dk + dv * dk);
+        const int blocks = static_cast<int>(std::min<size_t>((total + 255) / 256, 4 * ds->sms));
+        gdn::k1::reduce_partials_kernel<<<blocks, 256, 0, stream>>>(partial, A_ws, U_ws, static_cast<int>(items),
+                                                                   nsplit, dk, dv);
+    }
+    gdn::k2::Params p2;
+    p2.alpha = alpha;
+    p2.U_ws = U_ws;
+    p2.state_in = state_in;
+    p2.state_out = state_out;
+    p2.H = H;
+    p2.F = 1;
+    p2.dk = dk;
+    p2.dv = dv;
+    p2.rsplit = dv / R;
+    p2.wait_limit_ns = lim;
+    const int g2 = B * H * p2.rsplit;
+    if (R == 32)
+        gdn::k2::scan_kernel<32><<<g2, gdn::k2::THREADS, gdn::k2::Cfg<32>::SMEM_BYTES, stream>>>(tm_A, tm_S_store, p2);
+    else
+        gdn::k2::scan_kernel<16><<<g2, gdn::k2::THREADS, gdn::k2::Cfg<16>::SMEM_BYTES, stream>>>(tm_A, tm_S_store, p2);
+    gdn::k3::Params p3;
+    p3.H = H;
+    p3.N = N;
+    p3.dk = dk;
+    p3.dv = dv;
+    p3.ntile = (N + gdn::k3::TILE_M - 1) / gdn::k3::TILE_M;
+    p3.total = items * p3.ntile;
+    p3.wait_limit_ns = lim;
+    gdn::k3::output_kernel<<<static_cast<int>(std::min<long long>(p3.total, ds->sms)), gdn::k3::THREADS,
+                             gdn::k3::SMEM_BYTES, stream>>>(tm_q, tm_S_load, tm_out, p3);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}

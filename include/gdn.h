@@ -62,7 +62,8 @@ typedef enum gdn_status {
     GDN_ERR_LAUNCH = 6,       /* a kernel launch or CUDA runtime call failed       */
     GDN_ERR_TIMEOUT = 7,      /* a device-side bounded wait ran out (sync_status) */
     GDN_ERR_ALIAS = 8,        /* out overlaps an input                             */
-    GDN_ERR_NO_DEVICE = 9     /* no usable sm_103 device is current               */
+    GDN_ERR_NO_DEVICE = 9,    /* no usable sm_103 device is current               */
+    GDN_ERR_TOO_LARGE = 10    /* needs more than the fixed no-alloc scratch       */
 } gdn_status;
 
 /*
@@ -162,6 +163,37 @@ gdn_status gdn_selftest_wait_timeout(unsigned long long limit_ns, gdn_stream_t s
 
 /* Library version string. */
 const char* gdn_version(void);
+
+/*
+ * Allocation-free variant of gdn_frame_step.  No counterpart in the SANA-WM
+ * pages: it exists for callers that cannot allocate device memory when they
+ * advance the state -- for example a resident interactive rollout that
+ * reserved (nearly) all device memory up front for its models, or a runtime
+ * whose allocator must not be entered from this code path -- so the
+ * stream-ordered workspace allocation of gdn_frame_step is not an option.
+ *
+ * Same arguments, layouts, results and validation as gdn_frame_step.  The
+ * workspace lives instead in one fixed array of GDN_STEP_NOALLOC_SCRATCH_BYTES
+ * bytes in the library's device image: every GPU that loads the library
+ * holds it until the process exits.  No call allocates or frees memory.
+ *   - A shape whose workspace (gdn_step_workspace_bytes) exceeds the array
+ *     returns GDN_ERR_TOO_LARGE before anything is launched.  One frame of
+ *     B*H = 16 heads, N = 880 tokens, dk = dv = 128 needs about 21 MiB.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture starts.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents; each call writes every scratch byte it reads before reading
+ *     it, so nothing needs clearing.  Calls that may overlap on the GPU
+ *     (different streams, or unordered host threads) race on the array:
+ *     order them, for example by issuing them on one stream.
+ */
+#define GDN_STEP_NOALLOC_SCRATCH_BYTES (32u << 20)
+gdn_status gdn_frame_step_noalloc(const void* q, const void* k, const void* v,
+                                  const float* alpha, const float* beta,
+                                  const float* state_in, void* out, float* state_out,
+                                  int B, int H, int N, int dk, int dv,
+                                  gdn_stream_t stream);
 
 #ifdef __cplusplus
 }
