@@ -207,103 +207,134 @@ bool encode_mats(CUtensorMap* m, const void* base, long long items, int rows_tot
     return encode(m, const_cast<void*>(base), 3, dims, strides, box);
 }
 
+// per-item fp32 matrix [items, rows_total, cols], no swizzle, box (128, rows, 1)
+bool encode_mats_f32(CUtensorMap* m, const void* base, long long items, int rows_total, int cols, int rows) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows_total),
+                                static_cast<cuuint64_t>(items)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 4,
+                                   static_cast<cuuint64_t>(rows_total) * cols * 4};
+    const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(rows), 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------- the pass
-gdn_status run_pass(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
-                    const float* state_in, void* out, float* state_out, int B, int H, int F, int N, int dk, int dv,
-                    bool step, cudaStream_t stream, cudaEvent_t const* ev = nullptr) {
+struct PassArgs {
+    const void *q, *k, *v;
+    const float *alpha, *beta, *state_in;
+    void* out;
+    float* state_out;
+    int B, H, F, N, dk, dv;
+};
+
+int scan_rows(int dv) { return (dv % 32 == 0) ? 32 : 16; }
+
+// Launch the three phases (and the step path's partial reduction) on `stream`
+// with the workspace `ws` laid out as `L`.  Records ev[0..3] around the
+// phases when `ev` is not null.
+gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, int nsplit, const DeviceState* ds,
+                         cudaStream_t stream, cudaEvent_t const* ev) {
+    const long long items = static_cast<long long>(a.B) * a.F * a.H;
+    const int BF = a.B * a.F;
+    __nv_bfloat16* A_ws = reinterpret_cast<__nv_bfloat16*>(ws + L.a_off);
+    float* U_ws = reinterpret_cast<float*>(ws + L.u_off);
+    __nv_bfloat16* S_all = reinterpret_cast<__nv_bfloat16*>(ws + L.s_off);
+    float* partial = nsplit > 1 ? reinterpret_cast<float*>(ws + L.p_off) : nullptr;
+    const int R = scan_rows(a.dv);
+    CUtensorMap tm_k, tm_v, tm_q, tm_out, tm_A, tm_U, tm_S_store, tm_S_load;
+    const bool enc = encode_tokens(&tm_k, a.k, BF, a.N, a.H, a.dk, gdn::k1::CHUNK) &&
+                     encode_tokens(&tm_v, a.v, BF, a.N, a.H, a.dv, gdn::k1::CHUNK) &&
+                     encode_tokens(&tm_q, a.q, BF, a.N, a.H, a.dk, gdn::k3::TILE_M) &&
+                     encode_tokens(&tm_out, a.out, BF, a.N, a.H, a.dv, 32) &&
+                     encode_mats(&tm_A, A_ws, items, a.dk, a.dk, 128) &&
+                     encode_mats_f32(&tm_U, U_ws, items, a.dv, a.dk, R) &&
+                     encode_mats(&tm_S_store, S_all, items, a.dv, a.dk, R) &&
+                     encode_mats(&tm_S_load, S_all, items, a.dv, a.dk, 128);
+    if (!enc) return GDN_ERR_LAUNCH;
+    const unsigned long long lim = g_wait_limit_ns.load();
+
+    // phase 1
+    gdn::k1::Params p1;
+    p1.beta = a.beta;
+    p1.A_ws = A_ws;
+    p1.U_ws = U_ws;
+    p1.partial = partial;
+    p1.H = a.H;
+    p1.N = a.N;
+    p1.dk = a.dk;
+    p1.dv = a.dv;
+    p1.items = static_cast<int>(items);
+    p1.nsplit = nsplit;
+    p1.chunks = (a.N + gdn::k1::CHUNK - 1) / gdn::k1::CHUNK;
+    p1.work = static_cast<int>(items * nsplit);
+    p1.wait_limit_ns = lim;
+    if (ev) cudaEventRecord(ev[0], stream);
+    gdn::k1::contract_kernel<<<std::min(p1.work, ds->sms), gdn::k1::THREADS, gdn::k1::SMEM_BYTES, stream>>>(
+        tm_k, tm_v, p1);
+    if (nsplit > 1) {
+        const size_t total = static_cast<size_t>(items) * (a.dk * a.dk + a.dv * a.dk);
+        const int blocks = static_cast<int>(std::min<size_t>((total + 255) / 256, 4 * ds->sms));
+        gdn::k1::reduce_partials_kernel<<<blocks, 256, 0, stream>>>(partial, A_ws, U_ws, static_cast<int>(items),
+                                                                   nsplit, a.dk, a.dv);
+    }
+    // phase 2
+    if (ev) cudaEventRecord(ev[1], stream);
+    gdn::k2::Params p2;
+    p2.alpha = a.alpha;
+    p2.state_in = a.state_in;
+    p2.state_out = a.state_out;
+    p2.H = a.H;
+    p2.F = a.F;
+    p2.dk = a.dk;
+    p2.dv = a.dv;
+    p2.rsplit = a.dv / R;
+    p2.wait_limit_ns = lim;
+    const int g2 = a.B * a.H * p2.rsplit;
+    if (R == 32)
+        gdn::k2::scan_kernel<32><<<g2, gdn::k2::THREADS, gdn::k2::Cfg<32>::SMEM_BYTES, stream>>>(tm_A, tm_U,
+                                                                                               tm_S_store, p2);
+    else
+        gdn::k2::scan_kernel<16><<<g2, gdn::k2::THREADS, gdn::k2::Cfg<16>::SMEM_BYTES, stream>>>(tm_A, tm_U,
+                                                                                               tm_S_store, p2);
+    // phase 3
+    if (ev) cudaEventRecord(ev[2], stream);
+    gdn::k3::Params p3;
+    p3.H = a.H;
+    p3.N = a.N;
+    p3.dk = a.dk;
+    p3.dv = a.dv;
+    p3.ntile = (a.N + gdn::k3::TILE_M - 1) / gdn::k3::TILE_M;
+    p3.total = items * p3.ntile;
+    p3.wait_limit_ns = lim;
+    gdn::k3::output_kernel<<<static_cast<int>(std::min<long long>(p3.total, ds->sms)), gdn::k3::THREADS,
+                             gdn::k3::SMEM_BYTES, stream>>>(tm_q, tm_S_load, tm_out, p3);
+    if (ev) cudaEventRecord(ev[3], stream);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+
+bool all_device(const PassArgs& a) {
+    return is_device_ptr(a.q) && is_device_ptr(a.k) && is_device_ptr(a.v) && is_device_ptr(a.alpha) &&
+           is_device_ptr(a.beta) && is_device_ptr(a.state_in) && is_device_ptr(a.out) && is_device_ptr(a.state_out);
+}
+
+// Pooled-workspace pass: gdn_frame_forward (step = false) and gdn_frame_step.
+gdn_status run_pass(const PassArgs& a, bool step, cudaStream_t stream, cudaEvent_t const* ev = nullptr) {
     int dev;
     DeviceState* ds;
     gdn_status st = device_ready(&dev, &ds);
     if (st != GDN_OK) return st;
-    if (!is_device_ptr(q) || !is_device_ptr(k) || !is_device_ptr(v) || !is_device_ptr(alpha) ||
-        !is_device_ptr(beta) || !is_device_ptr(state_in) || !is_device_ptr(out) || !is_device_ptr(state_out))
-        return GDN_ERR_NULL_PTR;
-
-    const long long items = static_cast<long long>(B) * F * H;
-    const int BF = B * F;
-    const int chunks = (N + gdn::k1::CHUNK - 1) / gdn::k1::CHUNK;
-    const int nsplit = step ? step_nsplit(ds->sms, B, H, N) : 1;
-    const Layout L = layout_of(items, dk, dv, nsplit);
-
+    if (!all_device(a)) return GDN_ERR_NULL_PTR;
+    const long long items = static_cast<long long>(a.B) * a.F * a.H;
+    const int nsplit = step ? step_nsplit(ds->sms, a.B, a.H, a.N) : 1;
+    const Layout L = layout_of(items, a.dk, a.dv, nsplit);
     uint8_t* ws = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), L.total, ds->pool, stream) != cudaSuccess) {
         cudaGetLastError();
         return GDN_ERR_ALLOC;
     }
-    __nv_bfloat16* A_ws = reinterpret_cast<__nv_bfloat16*>(ws + L.a_off);
-    float* U_ws = reinterpret_cast<float*>(ws + L.u_off);
-    __nv_bfloat16* S_all = reinterpret_cast<__nv_bfloat16*>(ws + L.s_off);
-    float* partial = nsplit > 1 ? reinterpret_cast<float*>(ws + L.p_off) : nullptr;
-
-    const int R = (dv % 32 == 0) ? 32 : 16;
-    CUtensorMap tm_k, tm_v, tm_q, tm_out, tm_A, tm_S_store, tm_S_load;
-    bool enc = encode_tokens(&tm_k, k, BF, N, H, dk, gdn::k1::CHUNK) &&
-               encode_tokens(&tm_v, v, BF, N, H, dv, gdn::k1::CHUNK) &&
-               encode_tokens(&tm_q, q, BF, N, H, dk, gdn::k3::TILE_M) &&
-               encode_tokens(&tm_out, out, BF, N, H, dv, 32) && encode_mats(&tm_A, A_ws, items, dk, dk, 128) &&
-               encode_mats(&tm_S_store, S_all, items, dv, dk, R) && encode_mats(&tm_S_load, S_all, items, dv, dk, 128);
-    gdn_status result = GDN_OK;
-    if (!enc) {
-        result = GDN_ERR_LAUNCH;
-    } else {
-        const unsigned long long lim = g_wait_limit_ns.load();
-        // phase 1
-        gdn::k1::Params p1;
-        p1.beta = beta;
-        p1.A_ws = A_ws;
-        p1.U_ws = U_ws;
-        p1.partial = partial;
-        p1.H = H;
-        p1.N = N;
-        p1.dk = dk;
-        p1.dv = dv;
-        p1.items = static_cast<int>(items);
-        p1.nsplit = nsplit;
-        p1.chunks = chunks;
-        p1.work = static_cast<int>(items * nsplit);
-        p1.wait_limit_ns = lim;
-        const int g1 = std::min(p1.work, ds->sms);
-        if (ev) cudaEventRecord(ev[0], stream);
-        gdn::k1::contract_kernel<<<g1, gdn::k1::THREADS, gdn::k1::SMEM_BYTES, stream>>>(tm_k, tm_v, p1);
-        if (nsplit > 1) {
-            const size_t total = static_cast<size_t>(items) * (dk * dk + dv * dk);
-            const int blocks = static_cast<int>(std::min<size_t>((total + 255) / 256, 4 * ds->sms));
-            gdn::k1::reduce_partials_kernel<<<blocks, 256, 0, stream>>>(partial, A_ws, U_ws, static_cast<int>(items),
-                                                                       nsplit, dk, dv);
-        }
-        if (ev) cudaEventRecord(ev[1], stream);
-        // phase 2
-        gdn::k2::Params p2;
-        p2.alpha = alpha;
-        p2.U_ws = U_ws;
-        p2.state_in = state_in;
-        p2.state_out = state_out;
-        p2.H = H;
-        p2.F = F;
-        p2.dk = dk;
-        p2.dv = dv;
-        p2.rsplit = dv / R;
-        p2.wait_limit_ns = lim;
-        const int g2 = B * H * p2.rsplit;
-        if (R == 32)
-            gdn::k2::scan_kernel<32><<<g2, gdn::k2::THREADS, gdn::k2::Cfg<32>::SMEM_BYTES, stream>>>(tm_A, tm_S_store, p2);
-        else
-            gdn::k2::scan_kernel<16><<<g2, gdn::k2::THREADS, gdn::k2::Cfg<16>::SMEM_BYTES, stream>>>(tm_A, tm_S_store, p2);
-        if (ev) cudaEventRecord(ev[2], stream);
-        // phase 3
-        gdn::k3::Params p3;
-        p3.H = H;
-        p3.N = N;
-        p3.dk = dk;
-        p3.dv = dv;
-        p3.ntile = (N + gdn::k3::TILE_M - 1) / gdn::k3::TILE_M;
-        p3.total = items * p3.ntile;
-        p3.wait_limit_ns = lim;
-        const int g3 = static_cast<int>(std::min<long long>(p3.total, ds->sms));
-        gdn::k3::output_kernel<<<g3, gdn::k3::THREADS, gdn::k3::SMEM_BYTES, stream>>>(tm_q, tm_S_load, tm_out, p3);
-        if (ev) cudaEventRecord(ev[3], stream);
-        if (cudaGetLastError() != cudaSuccess) result = GDN_ERR_LAUNCH;
-    }
+    const gdn_status result = launch_phases(a, ws, L, nsplit, ds, stream, ev);
     cudaFreeAsync(ws, stream);
     return result;
 }
@@ -329,7 +360,7 @@ gdn_status gdn_frame_forward(const void* q, const void* k, const void* v, const 
                              int dv, gdn_stream_t stream) {
     gdn_status s = validate(q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv);
     if (s != GDN_OK) return s;
-    return run_pass(q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv, false,
+    return run_pass(PassArgs{q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv}, false,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -338,7 +369,7 @@ gdn_status gdn_frame_step(const void* q, const void* k, const void* v, const flo
                           gdn_stream_t stream) {
     gdn_status s = validate(q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv);
     if (s != GDN_OK) return s;
-    return run_pass(q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv, true,
+    return run_pass(PassArgs{q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv}, true,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -352,7 +383,7 @@ gdn_status gdn_frame_forward_timed(const void* q, const void* k, const void* v, 
     if (s != GDN_OK) return s;
     cudaEvent_t ev[4];
     for (int i = 0; i < 4; ++i) ev[i] = static_cast<cudaEvent_t>(phase_events[i]);
-    return run_pass(q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv, false,
+    return run_pass(PassArgs{q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv}, false,
                     reinterpret_cast<cudaStream_t>(stream), ev);
 }
 
@@ -383,10 +414,11 @@ gdn_status gdn_frame_forward_host(const void* q, const void* k, const void* v, c
         if (sizes[i]) ok = cudaMemcpyAsync(d + off[i], src[i], sizes[i], cudaMemcpyHostToDevice, st) == cudaSuccess;
     gdn_status r = ok ? GDN_OK : GDN_ERR_LAUNCH;
     if (r == GDN_OK)
-        r = run_pass(d + off[0], d + off[1], d + off[2], reinterpret_cast<const float*>(d + off[3]),
-                     reinterpret_cast<const float*>(d + off[4]),
-                     state_in ? reinterpret_cast<const float*>(d + off[5]) : nullptr, d + off[6],
-                     state_out ? reinterpret_cast<float*>(d + off[7]) : nullptr, B, H, F, N, dk, dv, false, st);
+        r = run_pass(PassArgs{d + off[0], d + off[1], d + off[2], reinterpret_cast<const float*>(d + off[3]),
+                              reinterpret_cast<const float*>(d + off[4]),
+                              state_in ? reinterpret_cast<const float*>(d + off[5]) : nullptr, d + off[6],
+                              state_out ? reinterpret_cast<float*>(d + off[7]) : nullptr, B, H, F, N, dk, dv},
+                     false, st);
     if (r == GDN_OK) {
         ok = cudaMemcpyAsync(out, d + off[6], bv, cudaMemcpyDeviceToHost, st) == cudaSuccess;
         if (ok && state_out) ok = cudaMemcpyAsync(state_out, d + off[7], bs, cudaMemcpyDeviceToHost, st) == cudaSuccess;
@@ -516,74 +548,10 @@ extern "C" gdn_status gdn_frame_step_noalloc(const void* q, const void* k, const
     const int nsplit = step_nsplit(ds->sms, B, H, N);
     const Layout L = layout_of(items, dk, dv, nsplit);
     if (L.total > kStepScratchBytes) return GDN_ERR_TOO_LARGE;
-    if (!is_device_ptr(q) || !is_device_ptr(k) || !is_device_ptr(v) || !is_device_ptr(alpha) ||
-        !is_device_ptr(beta) || !is_device_ptr(state_in) || !is_device_ptr(out) || !is_device_ptr(state_out))
-        return GDN_ERR_NULL_PTR;
+    const PassArgs a{q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv};
+    if (!all_device(a)) return GDN_ERR_NULL_PTR;
     uint8_t* ws = nullptr;
     st = step_scratch_address(dev, &ws);
     if (st != GDN_OK) return st;
-
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
-    __nv_bfloat16* A_ws = reinterpret_cast<__nv_bfloat16*>(ws + L.a_off);
-    float* U_ws = reinterpret_cast<float*>(ws + L.u_off);
-    __nv_bfloat16* S_all = reinterpret_cast<__nv_bfloat16*>(ws + L.s_off);
-    float* partial = nsplit > 1 ? reinterpret_cast<float*>(ws + L.p_off) : nullptr;
-    const int R = (dv % 32 == 0) ? 32 : 16;
-    CUtensorMap tm_k, tm_v, tm_q, tm_out, tm_A, tm_S_store, tm_S_load;
-    if (!(encode_tokens(&tm_k, k, B, N, H, dk, gdn::k1::CHUNK) && encode_tokens(&tm_v, v, B, N, H, dv, gdn::k1::CHUNK) &&
-          encode_tokens(&tm_q, q, B, N, H, dk, gdn::k3::TILE_M) && encode_tokens(&tm_out, out, B, N, H, dv, 32) &&
-          encode_mats(&tm_A, A_ws, items, dk, dk, 128) && encode_mats(&tm_S_store, S_all, items, dv, dk, R) &&
-          encode_mats(&tm_S_load, S_all, items, dv, dk, 128)))
-        return GDN_ERR_LAUNCH;
-    const unsigned long long lim = g_wait_limit_ns.load();
-
-    gdn::k1::Params p1;
-    p1.beta = beta;
-    p1.A_ws = A_ws;
-    p1.U_ws = U_ws;
-    p1.partial = partial;
-    p1.H = H;
-    p1.N = N;
-    p1.dk = dk;
-    p1.dv = dv;
-    p1.items = static_cast<int>(items);
-    p1.nsplit = nsplit;
-    p1.chunks = (N + gdn::k1::CHUNK - 1) / gdn::k1::CHUNK;
-    p1.work = static_cast<int>(items * nsplit);
-    p1.wait_limit_ns = lim;
-    gdn::k1::contract_kernel<<<std::min(p1.work, ds->sms), gdn::k1::THREADS, gdn::k1::SMEM_BYTES, stream>>>(tm_k, tm_v,
-                                                                                                        p1);
-    if (nsplit > 1) {
-        const size_t total = static_cast<size_t>(items) * (dk * dk + dv * dk);
-        const int blocks = static_cast<int>(std::min<size_t>((total + 255) / 256, 4 * ds->sms));
-        gdn::k1::reduce_partials_kernel<<<blocks, 256, 0, stream>>>(partial, A_ws, U_ws, static_cast<int>(items),
-                                                                   nsplit, dk, dv);
-    }
-    gdn::k2::Params p2;
-    p2.alpha = alpha;
-    p2.U_ws = U_ws;
-    p2.state_in = state_in;
-    p2.state_out = state_out;
-    p2.H = H;
-    p2.F = 1;
-    p2.dk = dk;
-    p2.dv = dv;
-    p2.rsplit = dv / R;
-    p2.wait_limit_ns = lim;
-    const int g2 = B * H * p2.rsplit;
-    if (R == 32)
-        gdn::k2::scan_kernel<32><<<g2, gdn::k2::THREADS, gdn::k2::Cfg<32>::SMEM_BYTES, stream>>>(tm_A, tm_S_store, p2);
-    else
-        gdn::k2::scan_kernel<16><<<g2, gdn::k2::THREADS, gdn::k2::Cfg<16>::SMEM_BYTES, stream>>>(tm_A, tm_S_store, p2);
-    gdn::k3::Params p3;
-    p3.H = H;
-    p3.N = N;
-    p3.dk = dk;
-    p3.dv = dv;
-    p3.ntile = (N + gdn::k3::TILE_M - 1) / gdn::k3::TILE_M;
-    p3.total = items * p3.ntile;
-    p3.wait_limit_ns = lim;
-    gdn::k3::output_kernel<<<static_cast<int>(std::min<long long>(p3.total, ds->sms)), gdn::k3::THREADS,
-                             gdn::k3::SMEM_BYTES, stream>>>(tm_q, tm_S_load, tm_out, p3);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+    return launch_phases(a, ws, L, nsplit, ds, reinterpret_cast<cudaStream_t>(stream_handle), nullptr);
 }

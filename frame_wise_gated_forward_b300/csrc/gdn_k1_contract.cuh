@@ -17,10 +17,13 @@
 // of q/k/v's natural token-major layout, i.e. MN-major in the MMA's terms.
 // beta is applied in fp32 to a copy of the K tile (rounded to bf16 once).
 //
-// Warp roles (256 threads): warp 0 TMA producer; warp 1 TMEM owner and MMA
-// issuer; warps 2-3 beta scalers (one token row per thread); warps 4-7
-// epilogue (TMEM lane quarter = warp % 4).  TMEM holds two 256-column
-// accumulators so one item's epilogue overlaps the next item's MMAs.
+// Warp roles (320 threads): warp 0 TMA producer; warp 1 TMEM owner and MMA
+// issuer; warps 2-5 beta scalers (one 64-column half row per thread); warps
+// 6-9 epilogue (TMEM lane quarter = warp % 4).  The K/V tiles stream through a
+// 6-deep TMA ring; the scaled copy of K has its own double buffer, so a ring
+// slot is released as soon as its MMAs retire and six 32 KB loads can be in
+// flight per SM.  TMEM holds two 256-column accumulators so one item's
+// epilogue overlaps the next item's MMAs.
 #pragma once
 
 #include "gdn_ptx.cuh"
@@ -29,11 +32,13 @@ namespace gdn {
 namespace k1 {
 
 constexpr int CHUNK = 64;                   // tokens per stage (MMA K extent per stage)
-constexpr int STAGES = 4;
+constexpr int STAGES = 6;                   // K/V ring depth
+constexpr int BK_BUFS = 2;                  // beta*K buffers
 constexpr int BOX_BYTES = CHUNK * 128;      // 64 token rows x 128 B (64 bf16)
 constexpr int TILE_BYTES = 2 * BOX_BYTES;   // d padded to 128 -> two 64-column boxes
-constexpr int STAGE_BYTES = 3 * TILE_BYTES; // K tile, V tile, beta*K tile
-constexpr int THREADS = 256;
+constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K tile, V tile
+constexpr int THREADS = 320;
+constexpr int SCALER_THREADS = 128;
 constexpr int TMEM_COLS = 512;
 constexpr int ACC_COLS = 256;
 // MN-major operand with 128-byte swizzle: 64 MN-elements per 128-byte row,
@@ -42,7 +47,7 @@ constexpr int ACC_COLS = 256;
 // groups.
 constexpr uint32_t MN_LBO = BOX_BYTES;
 constexpr uint32_t MN_SBO = 1024;
-constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
+constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + BK_BUFS * TILE_BYTES + 256 /*barriers*/;
 
 struct Params {
     const float* beta;     // [B, F, N, H]
@@ -74,15 +79,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* stage_base = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-    uint64_t* full = bars;                  // [STAGES]  TMA landed K and V
-    uint64_t* scaled = bars + STAGES;       // [STAGES]  beta*K written
-    uint64_t* empty = bars + 2 * STAGES;    // [STAGES]  MMA finished reading the stage
-    uint64_t* tfull = bars + 3 * STAGES;    // [2]       accumulator ready
-    uint64_t* tempty = bars + 3 * STAGES + 2; // [2]     accumulator drained
-    uint64_t* final_bar = bars + 3 * STAGES + 4; // [1]     every issued MMA retired
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
+    uint8_t* stage_base = smem;                                   // [STAGES][K tile | V tile]
+    uint8_t* bk_base = smem + STAGES * STAGE_BYTES;               // [BK_BUFS][beta*K tile]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(bk_base + BK_BUFS * TILE_BYTES);
+    uint64_t* full = bars;                          // [STAGES]  TMA landed K and V
+    uint64_t* empty = full + STAGES;                // [STAGES]  MMA finished reading the stage
+    uint64_t* bk_full = empty + STAGES;             // [BK_BUFS] beta*K written
+    uint64_t* bk_empty = bk_full + BK_BUFS;         // [BK_BUFS] MMA finished reading beta*K
+    uint64_t* tfull = bk_empty + BK_BUFS;           // [2]       accumulator ready
+    uint64_t* tempty = tfull + 2;                   // [2]       accumulator drained
+    uint64_t* final_bar = tempty + 2;               // [1]       every issued MMA retired
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32;
@@ -92,14 +99,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int kboxes = p.dk > 64 ? 2 : 1;
     const int vboxes = p.dv > 64 ? 2 : 1;
 
-    // Zero every stage once: boxes that are never loaded (d <= 64) must read as 0.
-    for (int i = threadIdx.x; i < STAGES * STAGE_BYTES / 16; i += THREADS)
-        reinterpret_cast<uint4*>(stage_base)[i] = make_uint4(0, 0, 0, 0);
+    // Zero every buffer once: boxes that are never loaded (d <= 64) must read as 0.
+    for (int i = threadIdx.x; i < (STAGES * STAGE_BYTES + BK_BUFS * TILE_BYTES) / 16; i += THREADS)
+        reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&scaled[s], 64);
             mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < BK_BUFS; ++b) {
+            mbar_init(&bk_full[b], SCALER_THREADS);
+            mbar_init(&bk_empty[b], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -152,8 +162,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t IDESC = idesc_bf16(128, 256, 1, 1);
-            int stage = 0;
-            uint32_t phase = 0;
+            int stage = 0, bk = 0;
+            uint32_t phase = 0, bk_phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             for (int w = w_begin; w < w_end && !*abort_flag; ++w) {
@@ -164,14 +174,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 bool ok = true;
                 for (int c = u.c_begin; c < u.c_end; ++c) {
                     if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag) ||
-                        !mbar_wait(&scaled[stage], phase, p.wait_limit_ns, abort_flag)) {
+                        !mbar_wait(&bk_full[bk], bk_phase, p.wait_limit_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t st = smem_u32(stage_base + stage * STAGE_BYTES);
-                    const uint32_t a_base = st + 2 * TILE_BYTES;  // beta*K
-                    const uint32_t b_base = st;                   // [K | V]
+                    const uint32_t a_base = smem_u32(bk_base + bk * TILE_BYTES);       // beta*K
+                    const uint32_t b_base = smem_u32(stage_base + stage * STAGE_BYTES); // [K | V]
 #pragma unroll
                     for (int kk = 0; kk < CHUNK / 16; ++kk) {
                         const uint64_t ad = smem_desc(a_base + kk * 2048, MN_LBO, MN_SBO);
@@ -179,7 +188,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         mma_bf16(d_tmem, ad, bd, IDESC, (c > u.c_begin || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(&empty[stage]);
+                    mma_commit(&bk_empty[bk]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    if (++bk == BK_BUFS) { bk = 0; bk_phase ^= 1; }
                 }
                 if (!ok) break;
                 mma_commit(&tfull[acc]);
@@ -188,11 +199,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             mma_commit(final_bar);
             mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
         }
-    } else if (warp < 4) {
+    } else if (warp < 6) {
         // ------------------------------------------------------ beta scalers
-        const int r = threadIdx.x - 64;  // token row within the stage, 0..63
-        int stage = 0;
-        uint32_t phase = 0;
+        const int t = threadIdx.x - 64;     // 0..127
+        const int r = t & 63;               // token row within the stage
+        const int bx = t >> 6;              // 64-column half of the row
+        int stage = 0, bk = 0;
+        uint32_t phase = 0, bk_phase = 0;
         for (int w = w_begin; w < w_end && !*abort_flag; ++w) {
             const Unit u = unit_of(p, w);
             const int frame = u.item / p.H, h = u.item % p.H;
@@ -201,11 +214,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int tok = c * CHUNK + r;
                 const float bval =
                     (tok < p.N) ? __ldg(p.beta + (static_cast<size_t>(frame) * p.N + tok) * p.H + h) : 0.0f;
-                if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag)) { ok = false; break; }
-                uint8_t* st = stage_base + stage * STAGE_BYTES;
-                for (int bx = 0; bx < kboxes; ++bx) {
-                    const uint8_t* src = st + bx * BOX_BYTES + r * 128;
-                    uint8_t* dst = st + 2 * TILE_BYTES + bx * BOX_BYTES + r * 128;
+                if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag) ||
+                    !mbar_wait(&bk_empty[bk], bk_phase ^ 1, p.wait_limit_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (bx < kboxes) {
+                    const uint8_t* src = stage_base + stage * STAGE_BYTES + bx * BOX_BYTES + r * 128;
+                    uint8_t* dst = bk_base + bk * TILE_BYTES + bx * BOX_BYTES + r * 128;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int ch = (i + r) & 7;  // rotate so 8 consecutive rows hit 8 distinct bank groups
@@ -221,8 +237,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&scaled[stage]);
+                mbar_arrive(&bk_full[bk]);
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                if (++bk == BK_BUFS) { bk = 0; bk_phase ^= 1; }
             }
             if (!ok) break;
         }
@@ -234,12 +251,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t acc_phase = 0;
         for (int w = w_begin; w < w_end && !*abort_flag; ++w) {
             const Unit u = unit_of(p, w);
-            if (!mbar_wait(&tfull[acc], acc_phase, p.wait_limit_ns, abort_flag)) break;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, p.wait_limit_ns, abort_flag));
+            if (!ok) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(quarter * 32) << 16);
             const bool jv = j < p.dk;
             if (p.nsplit == 1) {
-                __nv_bfloat16* Aout = p.A_ws + static_cast<size_t>(u.item) * p.dk * p.dk;
+                // A: row j of D holds A[j][0..dk); stored as row j (A is symmetric), 16-byte vectors
+                __nv_bfloat16* Arow = p.A_ws + (static_cast<size_t>(u.item) * p.dk + j) * p.dk;
                 float* Uout = p.U_ws + static_cast<size_t>(u.item) * p.dv * p.dk;
                 for (int c0 = 0; c0 < p.dk; c0 += 32) {
                     uint32_t r32[32];
@@ -247,12 +266,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tmem_wait_ld();
                     if (jv) {
 #pragma unroll
-                        for (int t = 0; t < 32; ++t)
-                            if (c0 + t < p.dk)
-                                Aout[static_cast<size_t>(c0 + t) * p.dk + j] =
-                                    __float2bfloat16_rn(__uint_as_float(r32[t]));
+                        for (int q8 = 0; q8 < 4; ++q8) {
+                            uint4 v4 = make_uint4(
+                                pack_bf16x2(__uint_as_float(r32[8 * q8 + 0]), __uint_as_float(r32[8 * q8 + 1])),
+                                pack_bf16x2(__uint_as_float(r32[8 * q8 + 2]), __uint_as_float(r32[8 * q8 + 3])),
+                                pack_bf16x2(__uint_as_float(r32[8 * q8 + 4]), __uint_as_float(r32[8 * q8 + 5])),
+                                pack_bf16x2(__uint_as_float(r32[8 * q8 + 6]), __uint_as_float(r32[8 * q8 + 7])));
+                            if (c0 + 8 * q8 < p.dk) *reinterpret_cast<uint4*>(Arow + c0 + 8 * q8) = v4;
+                        }
                     }
                 }
+                // U: row j of D holds U[0..dv)[j]; coalesced along j
                 for (int c0 = 0; c0 < p.dv; c0 += 32) {
                     uint32_t r32[32];
                     tmem_ld32(tbase + 128 + c0, r32);

@@ -11,8 +11,10 @@
 // the tensor core as C^T = A_f S_slice^T:
 //     M = 128 (dk index j, zero-padded), N = R (rows of the slice), K = dk
 // with both operands K-major in 128-byte-swizzled shared memory: A_f comes
-// from the bf16 workspace by TMA (4-deep prefetch ring), S_slice is the bf16
-// image of the state that the threads rewrite every frame.  The fp32 master
+// from the bf16 workspace by TMA together with the CTA's R rows of U_f
+// (fp32, unswizzled) through a 4-deep prefetch ring, so no global load sits
+// on the per-frame critical path; S_slice is the bf16 image of the state that
+// the threads rewrite every frame.  The fp32 master
 // state stays in registers: thread j (TMEM lane j) owns column j of the
 // slice, which is exactly the layout tcgen05.ld returns C in.  Each frame's
 // bf16 state image is also stored by TMA to the per-frame state buffer that
@@ -34,12 +36,13 @@ template <int R>
 struct Cfg {
     static constexpr int SBOX_BYTES = R * 128;
     static constexpr int STILE_BYTES = 2 * SBOX_BYTES;
-    static constexpr size_t SMEM_BYTES = 1024 + ASTAGES * ATILE_BYTES + 2 * STILE_BYTES + 256;
+    static constexpr int UTILE_BYTES = R * 128 * 4;            // R rows x 128 fp32 (dk padded)
+    static constexpr int STAGE_BYTES = ATILE_BYTES + UTILE_BYTES;
+    static constexpr size_t SMEM_BYTES = 1024 + ASTAGES * STAGE_BYTES + 2 * STILE_BYTES + 256;
 };
 
 struct Params {
     const float* alpha;     // [B, F, H]
-    const float* U_ws;      // [items][dv][dk] fp32, item = (b*F + f)*H + h
     const float* state_in;  // [B, H, dv, dk] or nullptr
     float* state_out;       // [B, H, dv, dk] or nullptr
     int H, F, dk, dv;
@@ -63,13 +66,13 @@ __device__ __forceinline__ uint32_t sop_offset(int r, int j) {
 
 template <int R>
 __global__ void __launch_bounds__(THREADS, 1)
-    scan_kernel(const __grid_constant__ CUtensorMap tm_A, const __grid_constant__ CUtensorMap tm_S,
-                const Params p) {
+    scan_kernel(const __grid_constant__ CUtensorMap tm_A, const __grid_constant__ CUtensorMap tm_U,
+                const __grid_constant__ CUtensorMap tm_S, const Params p) {
     using C = Cfg<R>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* aring = smem;                                  // [ASTAGES][ATILE_BYTES]
-    uint8_t* sop = smem + ASTAGES * ATILE_BYTES;            // [2][STILE_BYTES]
+    uint8_t* aring = smem;                                  // [ASTAGES][A tile | U rows]
+    uint8_t* sop = smem + ASTAGES * C::STAGE_BYTES;         // [2][STILE_BYTES]
     uint64_t* bars = reinterpret_cast<uint64_t*>(sop + 2 * C::STILE_BYTES);
     uint64_t* afull = bars;                                 // [ASTAGES]
     uint64_t* mma_done = bars + ASTAGES;                    // [1]
@@ -88,7 +91,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int nk = (p.dk + 15) / 16;
     const bool jv = j < p.dk;
 
-    for (int i = tid; i < (ASTAGES * ATILE_BYTES + 2 * C::STILE_BYTES) / 16; i += THREADS)
+    for (int i = tid; i < (ASTAGES * C::STAGE_BYTES + 2 * C::STILE_BYTES) / 16; i += THREADS)
         reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         for (int s = 0; s < ASTAGES; ++s) mbar_init(&afull[s], 1);
@@ -97,6 +100,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tm_A);
+        prefetch_tmap(&tm_U);
         prefetch_tmap(&tm_S);
     }
     if (warp == 0) {
@@ -120,19 +124,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         *reinterpret_cast<__nv_bfloat16*>(sop + sop_offset<R>(r, j)) = __float2bfloat16_rn(S[r]);
 
     auto item_of = [&](int f) { return (b * p.F + f) * p.H + h; };
-    int loaded = 0;  // frames whose A_f load has been issued
-    if (tid == 0) {
-        for (; loaded < ASTAGES && loaded < p.F; ++loaded) {
-            mbar_arrive_expect_tx(&afull[loaded], aboxes * ABOX_BYTES);
-            for (int bx = 0; bx < aboxes; ++bx)
-                tma_load_3d(aring + loaded * ATILE_BYTES + bx * ABOX_BYTES, &tm_A, &afull[loaded], 64 * bx, 0,
-                            item_of(loaded));
-        }
-    }
-    float u[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-        u[r] = jv ? __ldg(p.U_ws + (static_cast<size_t>(item_of(0)) * p.dv + r0 + r) * p.dk + j) : 0.0f;
+    // one ring slot = A_f (bf16, 128x128 swizzled) followed by U_f rows r0..r0+R-1 (fp32)
+    auto issue_load = [&](int frame, int slot) {
+        uint8_t* st = aring + slot * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&afull[slot], aboxes * ABOX_BYTES + C::UTILE_BYTES);
+        for (int bx = 0; bx < aboxes; ++bx)
+            tma_load_3d(st + bx * ABOX_BYTES, &tm_A, &afull[slot], 64 * bx, 0, item_of(frame));
+        tma_load_3d(st + ATILE_BYTES, &tm_U, &afull[slot], 0, r0, item_of(frame));
+    };
+    int loaded = 0;  // frames whose loads have been issued (thread 0 only)
+    if (tid == 0)
+        for (; loaded < ASTAGES && loaded < p.F; ++loaded) issue_load(loaded, loaded);
+    float a_next = __ldg(p.alpha + static_cast<size_t>(b * p.F) * p.H + h);
 
     fence_proxy_async_smem();
     __syncthreads();
@@ -147,7 +150,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (mbar_wait(&afull[slot], static_cast<uint32_t>((f / ASTAGES) & 1), p.wait_limit_ns, abort_flag)) {
                 ++consumed;
                 tc_fence_after();
-                const uint32_t a_base = smem_u32(aring + slot * ATILE_BYTES);
+                const uint32_t a_base = smem_u32(aring + slot * C::STAGE_BYTES);
                 const uint32_t b_base = smem_u32(sop + cur * C::STILE_BYTES);
                 for (int kk = 0; kk < nk; ++kk) {
                     const uint64_t ad = smem_desc(a_base + (kk >> 2) * ABOX_BYTES + (kk & 3) * 32, 16, 1024);
@@ -157,37 +160,27 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mma_commit(mma_done);
             }
         }
-        // Overlap the MMA with next frame's loads.
-        const float a_f = __ldg(p.alpha + static_cast<size_t>(b * p.F + f) * p.H + h);
-        float un[R];
-        const bool has_next = f + 1 < p.F;
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-            un[r] = (has_next && jv)
-                        ? __ldg(p.U_ws + (static_cast<size_t>(item_of(f + 1)) * p.dv + r0 + r) * p.dk + j)
-                        : 0.0f;
+        // alpha of the next frame is fetched one frame ahead
+        const float a_f = a_next;
+        if (f + 1 < p.F) a_next = __ldg(p.alpha + static_cast<size_t>(b * p.F + f + 1) * p.H + h);
 
-        bool ok = mbar_wait(mma_done, static_cast<uint32_t>(f & 1), p.wait_limit_ns, abort_flag);
+        bool ok = mbar_wait(&afull[slot], static_cast<uint32_t>((f / ASTAGES) & 1), p.wait_limit_ns, abort_flag) &&
+                  mbar_wait(mma_done, static_cast<uint32_t>(f & 1), p.wait_limit_ns, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             tc_fence_after();
             uint32_t c[R];
             tmem_ld_cols<R>(tmem, c);
+            const float* urow = reinterpret_cast<const float*>(aring + slot * C::STAGE_BYTES + ATILE_BYTES) + j;
+            float u[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) u[r] = urow[r * 128];
             tmem_wait_ld();
-            if (tid == 0 && loaded < p.F) {
-                // the MMA that read slot `slot` has retired: refill it with a later frame
-                mbar_arrive_expect_tx(&afull[slot], aboxes * ABOX_BYTES);
-                for (int bx = 0; bx < aboxes; ++bx)
-                    tma_load_3d(aring + slot * ATILE_BYTES + bx * ABOX_BYTES, &tm_A, &afull[slot], 64 * bx, 0,
-                                item_of(loaded));
-                ++loaded;
-            }
             uint8_t* nxt = sop + (cur ^ 1) * C::STILE_BYTES;
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 S[r] = a_f * (S[r] - __uint_as_float(c[r])) + u[r];
                 *reinterpret_cast<__nv_bfloat16*>(nxt + sop_offset<R>(r, j)) = __float2bfloat16_rn(S[r]);
-                u[r] = un[r];
             }
         }
         fence_proxy_async_smem();
@@ -196,6 +189,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         if (!ok) break;
         if (tid == 0) {
+            // every thread has read slot `slot` and its MMA has retired: refill it
+            if (loaded < p.F) {
+                issue_load(loaded, slot);
+                ++loaded;
+            }
             // publish the bf16 state after frame f for phase 3
             const uint8_t* nxt = sop + (cur ^ 1) * C::STILE_BYTES;
             for (int bx = 0; bx < sboxes; ++bx)
