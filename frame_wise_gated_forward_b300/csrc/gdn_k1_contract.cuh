@@ -20,10 +20,11 @@
 // Warp roles (320 threads): warp 0 TMA producer; warp 1 TMEM owner and MMA
 // issuer; warps 2-5 beta scalers (one 64-column half row per thread); warps
 // 6-9 epilogue (TMEM lane quarter = warp % 4).  The K/V tiles stream through a
-// 6-deep TMA ring; the scaled copy of K has its own double buffer, so a ring
-// slot is released as soon as its MMAs retire and six 32 KB loads can be in
-// flight per SM.  TMEM holds two 256-column accumulators so one item's
-// epilogue overlaps the next item's MMAs.
+// 5-deep TMA ring; the scaled copy of K has its own 3-deep ring, so a K/V slot
+// is released as soon as its MMAs retire.  beta reaches the scalers through a
+// small per-thread shared-memory ring filled by cp.async four chunks ahead.
+// TMEM holds two 256-column accumulators so one item's epilogue overlaps the
+// next item's MMAs.
 #pragma once
 
 #include "gdn_ptx.cuh"
@@ -31,14 +32,33 @@
 namespace gdn {
 namespace k1 {
 
+#ifndef GDN_K1_STAGES
+#define GDN_K1_STAGES 5
+#endif
+#ifndef GDN_K1_BK_BUFS
+#define GDN_K1_BK_BUFS 3
+#endif
+#ifndef GDN_K1_SCALER_WARPS
+#define GDN_K1_SCALER_WARPS 4
+#endif
 constexpr int CHUNK = 64;                   // tokens per stage (MMA K extent per stage)
-constexpr int STAGES = 6;                   // K/V ring depth
-constexpr int BK_BUFS = 2;                  // beta*K buffers
+constexpr int STAGES = GDN_K1_STAGES;       // K/V ring depth
+constexpr int BK_BUFS = GDN_K1_BK_BUFS;     // beta*K buffers
 constexpr int BOX_BYTES = CHUNK * 128;      // 64 token rows x 128 B (64 bf16)
 constexpr int TILE_BYTES = 2 * BOX_BYTES;   // d padded to 128 -> two 64-column boxes
 constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K tile, V tile
-constexpr int THREADS = 320;
-constexpr int SCALER_THREADS = 128;
+constexpr int SCALER_WARPS = GDN_K1_SCALER_WARPS;
+constexpr int SCALER_THREADS = SCALER_WARPS * 32;
+constexpr int EPI_WARP0 = 2 + SCALER_WARPS;  // four epilogue warps follow the scalers
+constexpr int THREADS = (EPI_WARP0 + 4) * 32;
+// each scaler thread owns one token row and CH16 of its sixteen 16-byte chunks
+constexpr int CH16 = 16 / (SCALER_THREADS / 64);
+static_assert(SCALER_THREADS % 64 == 0 && CH16 >= 1 && 16 % (SCALER_THREADS / 64) == 0, "scaler split");
+// beta is copied global -> shared by each scaler thread BETA_AHEAD chunks before
+// its use, into a per-thread ring of BETA_AHEAD + 1 slots
+constexpr int BETA_AHEAD = 4;
+constexpr int BETA_RING_BYTES = (BETA_AHEAD + 1) * SCALER_THREADS * 4;
+static_assert(1024 + STAGES * STAGE_BYTES + BK_BUFS * TILE_BYTES + BETA_RING_BYTES + 256 <= 232448, "shared memory");
 constexpr int TMEM_COLS = 512;
 constexpr int ACC_COLS = 256;
 // MN-major operand with 128-byte swizzle: 64 MN-elements per 128-byte row,
@@ -47,7 +67,8 @@ constexpr int ACC_COLS = 256;
 // groups.
 constexpr uint32_t MN_LBO = BOX_BYTES;
 constexpr uint32_t MN_SBO = 1024;
-constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + BK_BUFS * TILE_BYTES + 256 /*barriers*/;
+constexpr size_t SMEM_BYTES =
+    1024 /*align slack*/ + STAGES * STAGE_BYTES + BK_BUFS * TILE_BYTES + BETA_RING_BYTES + 256 /*barriers*/;
 
 struct Params {
     const float* beta;     // [B, F, N, H]
@@ -81,7 +102,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stage_base = smem;                                   // [STAGES][K tile | V tile]
     uint8_t* bk_base = smem + STAGES * STAGE_BYTES;               // [BK_BUFS][beta*K tile]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(bk_base + BK_BUFS * TILE_BYTES);
+    float* beta_ring = reinterpret_cast<float*>(bk_base + BK_BUFS * TILE_BYTES);  // [BETA_AHEAD+1][SCALER_THREADS]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(bk_base + BK_BUFS * TILE_BYTES + BETA_RING_BYTES);
     uint64_t* full = bars;                          // [STAGES]  TMA landed K and V
     uint64_t* empty = full + STAGES;                // [STAGES]  MMA finished reading the stage
     uint64_t* bk_full = empty + STAGES;             // [BK_BUFS] beta*K written
@@ -199,32 +221,63 @@ __global__ void __launch_bounds__(THREADS, 1)
             mma_commit(final_bar);
             mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
         }
-    } else if (warp < 6) {
+    } else if (warp < EPI_WARP0) {
         // ------------------------------------------------------ beta scalers
-        const int t = threadIdx.x - 64;     // 0..127
+        const int t = threadIdx.x - 64;     // 0..SCALER_THREADS-1
         const int r = t & 63;               // token row within the stage
-        const int bx = t >> 6;              // 64-column half of the row
+        const int c16 = (t >> 6) * CH16;    // first 16-byte chunk of the row this thread scales
+        // beta is copied to shared memory BETA_AHEAD chunks ahead of its use (a
+        // cursor walks the same unit/chunk sequence), so its global-load
+        // latency never sits between a landed K tile and its MMA.  Each thread
+        // reads back only the values it copied itself.
+        int pw = w_begin, pc = 0;
+        if (pw < w_end) pc = unit_of(p, pw).c_begin;
+        int pslot = 0;
+        auto beta_prefetch = [&]() {
+            float* dst = beta_ring + pslot * SCALER_THREADS + t;
+            if (pw < w_end) {
+                const Unit u = unit_of(p, pw);
+                const int tok = pc * CHUNK + r;
+                if (tok < p.N)
+                    cp_async_4(dst, p.beta + (static_cast<size_t>(u.item / p.H) * p.N + tok) * p.H + (u.item % p.H));
+                else
+                    *dst = 0.0f;
+                if (++pc >= u.c_end) {
+                    ++pw;
+                    if (pw < w_end) pc = unit_of(p, pw).c_begin;
+                }
+            }
+            cp_async_commit();
+            if (++pslot == BETA_AHEAD + 1) pslot = 0;
+        };
+        for (int i = 0; i < BETA_AHEAD; ++i) beta_prefetch();
+        int cslot = 0;
         int stage = 0, bk = 0;
         uint32_t phase = 0, bk_phase = 0;
         for (int w = w_begin; w < w_end && !*abort_flag; ++w) {
             const Unit u = unit_of(p, w);
-            const int frame = u.item / p.H, h = u.item % p.H;
             bool ok = true;
             for (int c = u.c_begin; c < u.c_end; ++c) {
-                const int tok = c * CHUNK + r;
-                const float bval =
-                    (tok < p.N) ? __ldg(p.beta + (static_cast<size_t>(frame) * p.N + tok) * p.H + h) : 0.0f;
+                beta_prefetch();                       // chunk BETA_AHEAD ahead
+                cp_async_wait<BETA_AHEAD>();           // this chunk's copy has landed
+                const float bval = beta_ring[cslot * SCALER_THREADS + t];
+                if (++cslot == BETA_AHEAD + 1) cslot = 0;
                 if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag) ||
                     !mbar_wait(&bk_empty[bk], bk_phase ^ 1, p.wait_limit_ns, abort_flag)) {
                     ok = false;
                     break;
                 }
-                if (bx < kboxes) {
-                    const uint8_t* src = stage_base + stage * STAGE_BYTES + bx * BOX_BYTES + r * 128;
-                    uint8_t* dst = bk_base + bk * TILE_BYTES + bx * BOX_BYTES + r * 128;
+                {
+                    const uint8_t* src = stage_base + stage * STAGE_BYTES + r * 128;
+                    uint8_t* dst = bk_base + bk * TILE_BYTES + r * 128;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int ch = (i + r) & 7;  // rotate so 8 consecutive rows hit 8 distinct bank groups
+                    for (int i = 0; i < CH16; ++i) {
+                        // global chunk g = box*8 + c8; rotate within the box so 8 consecutive
+                        // rows hit 8 distinct bank groups
+                        const int g = c16 + i;
+                        const int box = g >> 3;
+                        if (box >= kboxes) break;
+                        const int ch = box * (BOX_BYTES / 16) + (((g & 7) + r) & 7);
                         uint4 x = *reinterpret_cast<const uint4*>(src + ch * 16);
                         uint32_t* xs = reinterpret_cast<uint32_t*>(&x);
 #pragma unroll
@@ -243,9 +296,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok) break;
         }
+        cp_async_wait<0>();  // no copy into the beta ring may outlive the CTA
     } else {
         // ----------------------------------------------------------- epilogue
-        const int quarter = warp & 3;
+        const int quarter = warp & 3;       // warps EPI_WARP0..EPI_WARP0+3 cover the four lane quarters
         const int j = quarter * 32 + lane;  // TMEM lane = row j of (beta K)^T = dk index
         int acc = 0;
         uint32_t acc_phase = 0;
