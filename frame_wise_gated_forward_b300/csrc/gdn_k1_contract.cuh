@@ -268,25 +268,31 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 {
+                    // all loads first, then convert and store: the loads are independent of the
+                    // stores, and issuing them together keeps eight shared-memory reads in flight
                     const uint8_t* src = stage_base + stage * STAGE_BYTES + r * 128;
                     uint8_t* dst = bk_base + bk * TILE_BYTES + r * 128;
+                    uint4 x[CH16];
+                    int off[CH16];
 #pragma unroll
                     for (int i = 0; i < CH16; ++i) {
                         // global chunk g = box*8 + c8; rotate within the box so 8 consecutive
                         // rows hit 8 distinct bank groups
                         const int g = c16 + i;
-                        const int box = g >> 3;
-                        if (box >= kboxes) break;
-                        const int ch = box * (BOX_BYTES / 16) + (((g & 7) + r) & 7);
-                        uint4 x = *reinterpret_cast<const uint4*>(src + ch * 16);
-                        uint32_t* xs = reinterpret_cast<uint32_t*>(&x);
+                        off[i] = (g >> 3) * BOX_BYTES + ((((g & 7) + r) & 7) << 4);
+                        if ((g >> 3) < kboxes) x[i] = *reinterpret_cast<const uint4*>(src + off[i]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < CH16; ++i) {
+                        if (((c16 + i) >> 3) >= kboxes) continue;
+                        uint32_t* xs = reinterpret_cast<uint32_t*>(&x[i]);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             __nv_bfloat162 pr = *reinterpret_cast<__nv_bfloat162*>(&xs[e]);
                             float2 f2 = __bfloat1622float2(pr);
                             xs[e] = pack_bf16x2(f2.x * bval, f2.y * bval);
                         }
-                        *reinterpret_cast<uint4*>(dst + ch * 16) = x;
+                        *reinterpret_cast<uint4*>(dst + off[i]) = x[i];
                     }
                 }
                 fence_proxy_async_smem();
