@@ -80,6 +80,12 @@ def kernel_costs(w):
                     "flops": 2 * items * dv * dk * dk},
         "k3_output": {"bytes": T * H * dk * 2 + ws_s + T * H * dv * 2,
                       "flops": 2 * T * H * dk * dv},
+        # scan and output pass fused into one launch: the per-frame states stay
+        # inside the kernel (published through L2), so only A, U, q, alpha,
+        # the states in/out and out count
+        "k23_scan_output": {"bytes": ws_a + ws_u + w.B * w.F * H * 4 + 2 * state + T * H * dk * 2
+                            + T * H * dv * 2,
+                            "flops": 2 * items * dv * dk * dk + 2 * T * H * dk * dv},
     }
 
 
@@ -288,9 +294,13 @@ def main():
         api.frame_forward_timed(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], s_in, out, st, evs[i])
     torch.cuda.synchronize(device)
     api.sync_status()
-    names = ["k1_contract", "k2_scan", "k3_output"]
+    sched = api.scan_schedule(w.B, w.H, w.dv)
+    names = ["k1_contract", "k2_scan", "k3_output"] if sched <= 0 else ["k1_contract", "flags_reset",
+                                                                        "k23_scan_output"]
     phase_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(nk))
                 for j, n in enumerate(names)}
+    if sched > 0:
+        names = ["k1_contract", "k23_scan_output"]
     costs = kernel_costs(w)
     phases = {}
     for n in names:
@@ -346,7 +356,9 @@ def main():
                                    f"dk={w.dk} dv={w.dv}, bf16 q/k/v/out, fp32 alpha/beta/state",
                        "tokens_per_step_per_gpu": tokens,
                        "l2": "inputs 1.31 GB per step > 126 MB L2; no flush",
-                       "parallelism": f"replicas x{world} (no data-path collective)"},
+                       "parallelism": f"replicas x{world} (no data-path collective)",
+                       "scan_schedule": (f"fused scan+output, {sched} state rows per scan CTA" if sched > 0
+                                         else f"separate scan ({-sched} rows per CTA) and output launches")},
             "roofline": roofline,
             "phases": phases,
             "path_roofline": {"floor_ms": floor_ms, "frac": floor_ms / ms_per_step,
@@ -355,7 +367,7 @@ def main():
                     "steps": args.e2e_steps},
             "cpu_baseline": cpu,
             "clocks": clocks,
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": (3 if sched <= 0 else 2) * args.steps,
         }
         print(json.dumps(line), flush=True)
     replicas.shutdown()

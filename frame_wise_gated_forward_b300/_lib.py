@@ -21,7 +21,7 @@ EXPORTS = (
     "gdn_frame_forward", "gdn_frame_step", "gdn_frame_forward_timed", "gdn_frame_forward_host",
     "gdn_workspace_bytes", "gdn_step_workspace_bytes",
     "gdn_status_string", "gdn_sync_status", "gdn_set_wait_limit_ns", "gdn_selftest_wait_timeout",
-    "gdn_version", "gdn_frame_step_noalloc",
+    "gdn_version", "gdn_frame_step_noalloc", "gdn_set_fused_scan", "gdn_scan_schedule",
 )
 
 
@@ -68,6 +68,10 @@ def load(path: str | None = None):
     lib.gdn_selftest_wait_timeout.restype = ctypes.c_int
     lib.gdn_frame_step_noalloc.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, st]
     lib.gdn_frame_step_noalloc.restype = ctypes.c_int
+    lib.gdn_set_fused_scan.argtypes = [ctypes.c_int]
+    lib.gdn_set_fused_scan.restype = None
+    lib.gdn_scan_schedule.argtypes = [i, i, i]
+    lib.gdn_scan_schedule.restype = ctypes.c_int
     lib.gdn_version.argtypes = []
     lib.gdn_version.restype = ctypes.c_char_p
     if path is None:

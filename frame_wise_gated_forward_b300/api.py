@@ -156,6 +156,20 @@ def sync_status(stream=None) -> None:
     check(load().gdn_sync_status(_stream_handle(stream)), "gdn_sync_status")
 
 
+def set_fused_scan(mode) -> None:
+    """Run the scan and the output pass as one cooperative launch (True or 1,
+    the default; 16, 32 or 64 to force the state rows per scan CTA) or as two
+    launches (False or 0).  Results are identical."""
+    if mode is True:
+        mode = 1
+    load().gdn_set_fused_scan(int(mode))
+
+
+def scan_schedule(B, H, dv) -> int:
+    """+R: fused scan/output with R state rows per scan CTA; -R: two launches."""
+    return int(load().gdn_scan_schedule(B, H, dv))
+
+
 def set_wait_limit_ns(ns: int) -> None:
     load().gdn_set_wait_limit_ns(int(ns))
 
@@ -168,5 +182,5 @@ def selftest_wait_timeout(limit_ns: int, stream=None) -> int:
 
 
 __all__ = ["frame_forward", "frame_step", "frame_forward_timed", "frame_forward_host", "workspace_bytes",
-           "step_workspace_bytes", "sync_status", "set_wait_limit_ns", "selftest_wait_timeout",
+           "step_workspace_bytes", "sync_status", "set_fused_scan", "scan_schedule", "set_wait_limit_ns", "selftest_wait_timeout",
            "GDNError"]

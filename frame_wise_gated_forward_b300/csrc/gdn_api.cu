@@ -13,22 +13,22 @@
 
 #include "gdn.h"
 #include "gdn_k1_contract.cuh"
-#include "gdn_k2_scan.cuh"
-#include "gdn_k3_output.cuh"
+#include "gdn_k23_fused.cuh"
 
 namespace {
 
 
 constexpr int kMaxDevices = 64;
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ULL};
+std::atomic<int> g_fused_scan{1};
 
 // ------------------------------------------------------------------ devices
 struct DeviceState {
     bool probed = false;
     bool ok = false;
     int sms = 0;
+    bool coop = false;  // cooperative launches possible with one fused CTA per SM
     cudaMemPool_t pool = nullptr;
-    bool attrs_set = false;
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -73,17 +73,29 @@ gdn_status device_ready(int* dev_out, DeviceState** st_out) {
         if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) { cudaGetLastError(); return GDN_ERR_ALLOC; }
         unsigned long long keep = ~0ULL;  // keep freed workspace cached in the pool
         cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
-        if (cudaFuncSetAttribute(gdn::k1::contract_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(gdn::k1::SMEM_BYTES)) != cudaSuccess ||
-            cudaFuncSetAttribute(gdn::k2::scan_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(gdn::k2::Cfg<16>::SMEM_BYTES)) != cudaSuccess ||
-            cudaFuncSetAttribute(gdn::k2::scan_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(gdn::k2::Cfg<32>::SMEM_BYTES)) != cudaSuccess ||
-            cudaFuncSetAttribute(gdn::k3::output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(gdn::k3::SMEM_BYTES)) != cudaSuccess) {
+        auto smem_attr = [](const void* fn, size_t bytes) {
+            return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) ==
+                   cudaSuccess;
+        };
+        using namespace gdn;
+        if (!smem_attr(reinterpret_cast<const void*>(k1::contract_kernel), k1::SMEM_BYTES) ||
+            !smem_attr(reinterpret_cast<const void*>(k2::scan_kernel<16>), k2::Cfg<16>::SMEM_BYTES) ||
+            !smem_attr(reinterpret_cast<const void*>(k2::scan_kernel<32>), k2::Cfg<32>::SMEM_BYTES) ||
+            !smem_attr(reinterpret_cast<const void*>(k2::scan_kernel<64>), k2::Cfg<64>::SMEM_BYTES) ||
+            !smem_attr(reinterpret_cast<const void*>(k3::output_kernel), k3::SMEM_BYTES) ||
+            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<16>), k23::smem_bytes<16>()) ||
+            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<32>), k23::smem_bytes<32>()) ||
+            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<64>), k23::smem_bytes<64>())) {
             cudaGetLastError();
             return GDN_ERR_LAUNCH;
         }
+        int coop = 0, per_sm = 0;
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k23::scan_output_kernel<64>, k23::THREADS,
+                                                          k23::smem_bytes<64>()) != cudaSuccess)
+            per_sm = 0;
+        cudaGetLastError();
+        d.coop = coop != 0 && per_sm >= 1;
         d.ok = true;
     }
     if (!d.ok) return GDN_ERR_NO_DEVICE;
@@ -159,14 +171,15 @@ bool is_device_ptr(const void* p) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t a_off, u_off, s_off, p_off, total;
+    size_t a_off, u_off, s_off, f_off, p_off, total;
 };
 Layout layout_of(long long items, int dk, int dv, int nsplit) {
     Layout L;
     L.a_off = 0;
     L.u_off = align256(L.a_off + static_cast<size_t>(items) * dk * dk * 2);
     L.s_off = align256(L.u_off + static_cast<size_t>(items) * dv * dk * 4);
-    L.p_off = align256(L.s_off + static_cast<size_t>(items) * dv * dk * 2);
+    L.f_off = align256(L.s_off + static_cast<size_t>(items) * dv * dk * 2);   // per-item ready counts
+    L.p_off = align256(L.f_off + static_cast<size_t>(items) * 4);
     L.total = L.p_off;
     if (nsplit > 1) L.total = align256(L.p_off + static_cast<size_t>(nsplit) * items * (dk * dk + dv * dk) * 4);
     return L;
@@ -229,7 +242,23 @@ struct PassArgs {
     int B, H, F, N, dk, dv;
 };
 
-int scan_rows(int dv) { return (dv % 32 == 0) ? 32 : 16; }
+// Rows of S per scan CTA.  Standalone scan: the smallest slice that keeps
+// all scan CTAs in one wave.  Fused with the output pass: the smallest slice
+// that leaves most SMs to the output pass (0: do not fuse).
+int scan_rows_standalone(int B, int H, int dv, int sms) {
+    for (int R : {16, 32, 64})
+        if (dv % R == 0 && static_cast<long long>(B) * H * (dv / R) <= sms) return R;
+    return dv % 64 == 0 ? 64 : (dv % 32 == 0 ? 32 : 16);
+}
+int scan_rows_fused(int B, int H, int dv, int sms) {
+    const int forced = g_fused_scan.load();
+    if (forced == 16 || forced == 32 || forced == 64)
+        return (dv % forced == 0 && static_cast<long long>(B) * H * (dv / forced) < sms) ? forced : 0;
+    // at most half of the SMs scan; the rest run the output pass
+    for (int R : {16, 32, 64})
+        if (dv % R == 0 && static_cast<long long>(B) * H * (dv / R) <= sms / 2) return R;
+    return 0;
+}
 
 // Launch the three phases (and the step path's partial reduction) on `stream`
 // with the workspace `ws` laid out as `L`.  Records ev[0..3] around the
@@ -242,7 +271,9 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, int ns
     float* U_ws = reinterpret_cast<float*>(ws + L.u_off);
     __nv_bfloat16* S_all = reinterpret_cast<__nv_bfloat16*>(ws + L.s_off);
     float* partial = nsplit > 1 ? reinterpret_cast<float*>(ws + L.p_off) : nullptr;
-    const int R = scan_rows(a.dv);
+    const int Rf = (g_fused_scan.load() != 0 && ds->coop) ? scan_rows_fused(a.B, a.H, a.dv, ds->sms) : 0;
+    const int R = Rf != 0 ? Rf : scan_rows_standalone(a.B, a.H, a.dv, ds->sms);
+    int* flags = reinterpret_cast<int*>(ws + L.f_off);
     CUtensorMap tm_k, tm_v, tm_q, tm_out, tm_A, tm_U, tm_S_store, tm_S_load;
     const bool enc = encode_tokens(&tm_k, a.k, BF, a.N, a.H, a.dk, gdn::k1::CHUNK) &&
                      encode_tokens(&tm_v, a.v, BF, a.N, a.H, a.dv, gdn::k1::CHUNK) &&
@@ -279,7 +310,7 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, int ns
         gdn::k1::reduce_partials_kernel<<<blocks, 256, 0, stream>>>(partial, A_ws, U_ws, static_cast<int>(items),
                                                                    nsplit, a.dk, a.dv);
     }
-    // phase 2
+    // phases 2 and 3
     if (ev) cudaEventRecord(ev[1], stream);
     gdn::k2::Params p2;
     p2.alpha = a.alpha;
@@ -291,25 +322,49 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, int ns
     p2.dv = a.dv;
     p2.rsplit = a.dv / R;
     p2.wait_limit_ns = lim;
-    const int g2 = a.B * a.H * p2.rsplit;
-    if (R == 32)
-        gdn::k2::scan_kernel<32><<<g2, gdn::k2::THREADS, gdn::k2::Cfg<32>::SMEM_BYTES, stream>>>(tm_A, tm_U,
-                                                                                               tm_S_store, p2);
-    else
-        gdn::k2::scan_kernel<16><<<g2, gdn::k2::THREADS, gdn::k2::Cfg<16>::SMEM_BYTES, stream>>>(tm_A, tm_U,
-                                                                                               tm_S_store, p2);
-    // phase 3
-    if (ev) cudaEventRecord(ev[2], stream);
     gdn::k3::Params p3;
+    p3.B = a.B;
     p3.H = a.H;
+    p3.F = a.F;
     p3.N = a.N;
     p3.dk = a.dk;
     p3.dv = a.dv;
     p3.ntile = (a.N + gdn::k3::TILE_M - 1) / gdn::k3::TILE_M;
     p3.total = items * p3.ntile;
     p3.wait_limit_ns = lim;
-    gdn::k3::output_kernel<<<static_cast<int>(std::min<long long>(p3.total, ds->sms)), gdn::k3::THREADS,
-                             gdn::k3::SMEM_BYTES, stream>>>(tm_q, tm_S_load, tm_out, p3);
+    const int n_scan = a.B * a.H * p2.rsplit;
+    if (Rf != 0) {
+        // one cooperative launch: scan CTAs publish per-frame states, output CTAs follow them
+        if (cudaMemsetAsync(flags, 0, static_cast<size_t>(items) * sizeof(int), stream) != cudaSuccess)
+            return GDN_ERR_LAUNCH;
+        const long long workers = std::min<long long>(ds->sms - n_scan, std::max<long long>(1, items));
+        int grid = n_scan + static_cast<int>(workers);
+        int n_scan_arg = n_scan;
+        void* args[] = {&tm_A, &tm_U, &tm_S_store, &tm_q, &tm_S_load, &tm_out, &p2, &p3, &flags, &n_scan_arg};
+        const void* fn = Rf == 16   ? reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<16>)
+                         : Rf == 32 ? reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<32>)
+                                    : reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<64>);
+        const size_t smem = Rf == 16 ? gdn::k23::smem_bytes<16>()
+                             : Rf == 32 ? gdn::k23::smem_bytes<32>() : gdn::k23::smem_bytes<64>();
+        if (ev) cudaEventRecord(ev[2], stream);
+        if (cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(gdn::k23::THREADS), args, smem, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GDN_ERR_LAUNCH;
+        }
+    } else {
+        if (R == 16)
+            gdn::k2::scan_kernel<16><<<n_scan, gdn::k2::THREADS, gdn::k2::Cfg<16>::SMEM_BYTES, stream>>>(
+                tm_A, tm_U, tm_S_store, p2);
+        else if (R == 32)
+            gdn::k2::scan_kernel<32><<<n_scan, gdn::k2::THREADS, gdn::k2::Cfg<32>::SMEM_BYTES, stream>>>(
+                tm_A, tm_U, tm_S_store, p2);
+        else
+            gdn::k2::scan_kernel<64><<<n_scan, gdn::k2::THREADS, gdn::k2::Cfg<64>::SMEM_BYTES, stream>>>(
+                tm_A, tm_U, tm_S_store, p2);
+        if (ev) cudaEventRecord(ev[2], stream);
+        gdn::k3::output_kernel<<<static_cast<int>(std::min<long long>(p3.total, ds->sms)), gdn::k3::THREADS,
+                                 gdn::k3::SMEM_BYTES, stream>>>(tm_q, tm_S_load, tm_out, p3);
+    }
     if (ev) cudaEventRecord(ev[3], stream);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
@@ -479,6 +534,19 @@ gdn_status gdn_sync_status(gdn_stream_t stream) {
         return static_cast<gdn_status>(code);
     }
     return GDN_OK;
+}
+
+void gdn_set_fused_scan(int mode) {
+    g_fused_scan.store((mode == 16 || mode == 32 || mode == 64) ? mode : (mode != 0 ? 1 : 0));
+}
+
+int gdn_scan_schedule(int B, int H, int dv) {
+    if (B < 1 || H < 1 || !dim_ok(dv)) return 0;
+    int dev;
+    DeviceState* ds;
+    if (device_ready(&dev, &ds) != GDN_OK) return 0;
+    const int Rf = (g_fused_scan.load() != 0 && ds->coop) ? scan_rows_fused(B, H, dv, ds->sms) : 0;
+    return Rf != 0 ? Rf : -scan_rows_standalone(B, H, dv, ds->sms);
 }
 
 void gdn_set_wait_limit_ns(unsigned long long limit_ns) {

@@ -12,13 +12,21 @@
 //     M = 128 (dk index j, zero-padded), N = R (rows of the slice), K = dk
 // with both operands K-major in 128-byte-swizzled shared memory: A_f comes
 // from the bf16 workspace by TMA together with the CTA's R rows of U_f
-// (fp32, unswizzled) through a 4-deep prefetch ring, so no global load sits
-// on the per-frame critical path; S_slice is the bf16 image of the state that
-// the threads rewrite every frame.  The fp32 master
-// state stays in registers: thread j (TMEM lane j) owns column j of the
-// slice, which is exactly the layout tcgen05.ld returns C in.  Each frame's
-// bf16 state image is also stored by TMA to the per-frame state buffer that
-// phase 3 reads.
+// (fp32, unswizzled) through a prefetch ring, so no global load sits on the
+// per-frame critical path; S_slice is the bf16 image of the state that the
+// compute threads rewrite every frame.  The fp32 master state stays in
+// registers: thread j (TMEM lane j) owns column j of the slice, which is
+// exactly the layout tcgen05.ld returns C in.
+//
+// Warp roles (192 threads): warps 0-3 compute (thread 0 also issues the
+// MMAs); warp 4 publishes each frame's bf16 state image with a TMA store to the
+// per-frame state buffer that phase 3 reads (and, when the scan runs fused
+// with phase 3, then raises that item's ready count); warp 5 refills the
+// A_f/U_f ring.  Compute hands each image to the publisher through an
+// mbarrier and keeps up to NIMG images in flight, so neither store latency
+// nor load issue sits on the frame-to-frame chain.  The S A_f product is
+// split over NACC independent accumulators (halves of the dk reduction) that
+// the tensor core can work on concurrently.
 #pragma once
 
 #include "gdn_ptx.cuh"
@@ -26,19 +34,26 @@
 namespace gdn {
 namespace k2 {
 
-constexpr int THREADS = 128;
-constexpr int ASTAGES = 4;
+constexpr int COMPUTE_THREADS = 128;
+constexpr int THREADS = 192;                 // + publisher warp + loader warp
 constexpr int ABOX_BYTES = 128 * 128;        // 128 rows x 128 B
 constexpr int ATILE_BYTES = 2 * ABOX_BYTES;  // A_f, dk padded to 128
-constexpr int TMEM_COLS = 32;
+#ifndef GDN_SCAN_NACC
+#define GDN_SCAN_NACC 1
+#endif
+constexpr int NACC = GDN_SCAN_NACC;
 
 template <int R>
 struct Cfg {
+    static constexpr int ASTAGES = R >= 64 ? 3 : 4;
+    static constexpr int NIMG = R >= 64 ? 2 : 4;               // bf16 state images in flight
     static constexpr int SBOX_BYTES = R * 128;
     static constexpr int STILE_BYTES = 2 * SBOX_BYTES;
     static constexpr int UTILE_BYTES = R * 128 * 4;            // R rows x 128 fp32 (dk padded)
     static constexpr int STAGE_BYTES = ATILE_BYTES + UTILE_BYTES;
-    static constexpr size_t SMEM_BYTES = 1024 + ASTAGES * STAGE_BYTES + 2 * STILE_BYTES + 256;
+    static constexpr int TMEM_COLS = NACC * R < 32 ? 32 : NACC * R;
+    static constexpr size_t SMEM_BYTES = 1024 + ASTAGES * STAGE_BYTES + NIMG * STILE_BYTES + 512;
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
 struct Params {
@@ -50,13 +65,6 @@ struct Params {
     unsigned long long wait_limit_ns;
 };
 
-template <int R>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&c)[R]);
-template <>
-__device__ __forceinline__ void tmem_ld_cols<16>(uint32_t taddr, uint32_t (&c)[16]) { tmem_ld16(taddr, c); }
-template <>
-__device__ __forceinline__ void tmem_ld_cols<32>(uint32_t taddr, uint32_t (&c)[32]) { tmem_ld32(taddr, c); }
-
 // bf16 element (r, j) of a K-major, 128-byte-swizzled [R rows x 128 cols] tile
 template <int R>
 __device__ __forceinline__ uint32_t sop_offset(int r, int j) {
@@ -64,162 +72,234 @@ __device__ __forceinline__ uint32_t sop_offset(int r, int j) {
     return box * Cfg<R>::SBOX_BYTES + r * 128 + ((((col >> 3) ^ (r & 7))) << 4) + ((col & 7) << 1);
 }
 
+// The scan of one R-row slice of one head.  `cta` selects (b, h, slice);
+// `flags` (may be null) receives one increment per published frame state.
+// Needs THREADS threads.
 template <int R>
-__global__ void __launch_bounds__(THREADS, 1)
-    scan_kernel(const __grid_constant__ CUtensorMap tm_A, const __grid_constant__ CUtensorMap tm_U,
-                const __grid_constant__ CUtensorMap tm_S, const Params p) {
+__device__ __forceinline__ void scan_role(const CUtensorMap* tm_A, const CUtensorMap* tm_U, const CUtensorMap* tm_S,
+                                          const Params& p, int cta, int* flags, uint8_t* smem) {
     using C = Cfg<R>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* aring = smem;                                  // [ASTAGES][A tile | U rows]
-    uint8_t* sop = smem + ASTAGES * C::STAGE_BYTES;         // [2][STILE_BYTES]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sop + 2 * C::STILE_BYTES);
-    uint64_t* afull = bars;                                 // [ASTAGES]
-    uint64_t* mma_done = bars + ASTAGES;                    // [1]
-    uint64_t* final_bar = bars + ASTAGES + 1;               // [1]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + ASTAGES + 2);
+    constexpr int AS = C::ASTAGES;
+    constexpr int NI = C::NIMG;
+    uint8_t* aring = smem;                                  // [AS][A tile | U rows]
+    uint8_t* sop = smem + AS * C::STAGE_BYTES;              // [NI][STILE_BYTES] bf16 state images
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sop + NI * C::STILE_BYTES);
+    uint64_t* afull = bars;                                 // [AS] loader -> compute
+    uint64_t* slot_free = afull + AS;                       // [AS] compute -> loader
+    uint64_t* mma_done = slot_free + AS;                    // [1]
+    uint64_t* img_ready = mma_done + 1;                     // [NI] compute -> publisher, MMA
+    uint64_t* img_free = img_ready + NI;                    // [NI] publisher -> compute
+    uint64_t* final_bar = img_free + NI;                    // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
-    const int j = tid;  // TMEM lane = dk index = column of S owned by this thread
-    const int bh = blockIdx.x / p.rsplit;
-    const int r0 = (blockIdx.x % p.rsplit) * R;
+    const int j = tid;  // compute threads: TMEM lane = dk index = column of S owned by this thread
+    const int bh = cta / p.rsplit;
+    const int r0 = (cta % p.rsplit) * R;
     const int b = bh / p.H, h = bh % p.H;
     const int aboxes = p.dk > 64 ? 2 : 1;
     const int sboxes = aboxes;
     const int nk = (p.dk + 15) / 16;
+    const int nacc = nk < NACC ? nk : NACC;
     const bool jv = j < p.dk;
+    auto item_of = [&](int f) { return (b * p.F + f) * p.H + h; };
 
-    for (int i = tid; i < (ASTAGES * C::STAGE_BYTES + 2 * C::STILE_BYTES) / 16; i += THREADS)
+    for (int i = tid; i < (AS * C::STAGE_BYTES + NI * C::STILE_BYTES) / 16; i += blockDim.x)
         reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
-        for (int s = 0; s < ASTAGES; ++s) mbar_init(&afull[s], 1);
+        for (int s = 0; s < AS; ++s) {
+            mbar_init(&afull[s], 1);
+            mbar_init(&slot_free[s], COMPUTE_THREADS);
+        }
         mbar_init(mma_done, 1);
+        for (int x = 0; x < NI; ++x) {
+            mbar_init(&img_ready[x], COMPUTE_THREADS);
+            mbar_init(&img_free[x], 1);
+        }
         mbar_init(final_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tmap(&tm_A);
-        prefetch_tmap(&tm_U);
-        prefetch_tmap(&tm_S);
+        prefetch_tmap(tm_A);
+        prefetch_tmap(tm_U);
+        prefetch_tmap(tm_S);
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
-
-    // S_0 slice: thread j holds S[r0 + r][j] for r < R
-    float S[R];
-    const size_t state_off = (static_cast<size_t>(b) * p.H + h) * p.dv * p.dk;
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-        S[r] = (p.state_in != nullptr && jv) ? p.state_in[state_off + static_cast<size_t>(r0 + r) * p.dk + j] : 0.0f;
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();  // zero-fill done before the first state image is written
+    __syncthreads();  // zero-fill and barrier init done
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot + (static_cast<uint32_t>(warp * 32) << 16);
+
+    if (warp < 4) {
+        // ---------------------------------------------------------- compute
+        float S[R];
+        const size_t state_off = (static_cast<size_t>(b) * p.H + h) * p.dv * p.dk;
 #pragma unroll
-    for (int r = 0; r < R; ++r)
-        *reinterpret_cast<__nv_bfloat16*>(sop + sop_offset<R>(r, j)) = __float2bfloat16_rn(S[r]);
-
-    auto item_of = [&](int f) { return (b * p.F + f) * p.H + h; };
-    // one ring slot = A_f (bf16, 128x128 swizzled) followed by U_f rows r0..r0+R-1 (fp32)
-    auto issue_load = [&](int frame, int slot) {
-        uint8_t* st = aring + slot * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(&afull[slot], aboxes * ABOX_BYTES + C::UTILE_BYTES);
-        for (int bx = 0; bx < aboxes; ++bx)
-            tma_load_3d(st + bx * ABOX_BYTES, &tm_A, &afull[slot], 64 * bx, 0, item_of(frame));
-        tma_load_3d(st + ATILE_BYTES, &tm_U, &afull[slot], 0, r0, item_of(frame));
-    };
-    int loaded = 0;  // frames whose loads have been issued (thread 0 only)
-    if (tid == 0)
-        for (; loaded < ASTAGES && loaded < p.F; ++loaded) issue_load(loaded, loaded);
-    float a_next = __ldg(p.alpha + static_cast<size_t>(b * p.F) * p.H + h);
-
-    fence_proxy_async_smem();
-    __syncthreads();
-
-    constexpr uint32_t IDESC = idesc_bf16(128, R, 0, 0);
-    int consumed = 0;  // frames whose A_f has been waited for
-    int f = 0;
-    for (; f < p.F; ++f) {
-        const int cur = f & 1;
-        const int slot = f % ASTAGES;
-        if (tid == 0) {
-            if (mbar_wait(&afull[slot], static_cast<uint32_t>((f / ASTAGES) & 1), p.wait_limit_ns, abort_flag)) {
-                ++consumed;
-                tc_fence_after();
-                const uint32_t a_base = smem_u32(aring + slot * C::STAGE_BYTES);
-                const uint32_t b_base = smem_u32(sop + cur * C::STILE_BYTES);
-                for (int kk = 0; kk < nk; ++kk) {
-                    const uint64_t ad = smem_desc(a_base + (kk >> 2) * ABOX_BYTES + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = smem_desc(b_base + (kk >> 2) * C::SBOX_BYTES + (kk & 3) * 32, 16, 1024);
-                    mma_bf16(*tmem_slot, ad, bd, IDESC, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(mma_done);
-            }
-        }
-        // alpha of the next frame is fetched one frame ahead
-        const float a_f = a_next;
-        if (f + 1 < p.F) a_next = __ldg(p.alpha + static_cast<size_t>(b * p.F + f + 1) * p.H + h);
-
-        bool ok = mbar_wait(&afull[slot], static_cast<uint32_t>((f / ASTAGES) & 1), p.wait_limit_ns, abort_flag) &&
-                  mbar_wait(mma_done, static_cast<uint32_t>(f & 1), p.wait_limit_ns, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-            tc_fence_after();
-            uint32_t c[R];
-            tmem_ld_cols<R>(tmem, c);
-            const float* urow = reinterpret_cast<const float*>(aring + slot * C::STAGE_BYTES + ATILE_BYTES) + j;
-            float u[R];
+        for (int r = 0; r < R; ++r)
+            S[r] = (p.state_in != nullptr && jv) ? p.state_in[state_off + static_cast<size_t>(r0 + r) * p.dk + j]
+                                                 : 0.0f;
+        const uint32_t tmem_warp = *tmem_slot + (static_cast<uint32_t>(warp * 32) << 16);
+        // image of the state before frame 0 in buffer 0; the state after frame f goes to buffer (f + 1) % NI
 #pragma unroll
-            for (int r = 0; r < R; ++r) u[r] = urow[r * 128];
-            tmem_wait_ld();
-            uint8_t* nxt = sop + (cur ^ 1) * C::STILE_BYTES;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                S[r] = a_f * (S[r] - __uint_as_float(c[r])) + u[r];
-                *reinterpret_cast<__nv_bfloat16*>(nxt + sop_offset<R>(r, j)) = __float2bfloat16_rn(S[r]);
-            }
-        }
+        for (int r = 0; r < R; ++r)
+            *reinterpret_cast<__nv_bfloat16*>(sop + sop_offset<R>(r, j)) = __float2bfloat16_rn(S[r]);
         fence_proxy_async_smem();
-        tc_fence_before();
-        ok = __syncthreads_and(ok);
-        tc_fence_after();
-        if (!ok) break;
-        if (tid == 0) {
-            // every thread has read slot `slot` and its MMA has retired: refill it
-            if (loaded < p.F) {
-                issue_load(loaded, slot);
-                ++loaded;
+        mbar_arrive(&img_ready[0]);  // initial image (never stored: the publisher skips it)
+        float a_next = __ldg(p.alpha + static_cast<size_t>(b * p.F) * p.H + h);
+
+        constexpr uint32_t IDESC = idesc_bf16(128, R, 0, 0);
+        int f = 0;
+        for (; f < p.F; ++f) {
+            const int slot = f % AS;
+            const int cur = f % NI;        // image of the state after frame f - 1
+            const int nxt = (f + 1) % NI;  // image of the state after frame f
+            if (tid == 0) {
+                // the previous state's image is complete, and this frame's A_f has landed
+                const bool go = mbar_wait(&img_ready[cur], static_cast<uint32_t>((f / NI) & 1),
+                                          p.wait_limit_ns, abort_flag) &&
+                                mbar_wait(&afull[slot], static_cast<uint32_t>((f / AS) & 1), p.wait_limit_ns,
+                                          abort_flag);
+                if (go) {
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(aring + slot * C::STAGE_BYTES);
+                    const uint32_t b_base = smem_u32(sop + cur * C::STILE_BYTES);
+                    for (int kk = 0; kk < nk; ++kk) {
+                        const int acc = (kk * nacc) / nk;  // contiguous halves of the reduction
+                        const bool first = kk == (acc * nk + nacc - 1) / nacc;
+                        const uint64_t ad = smem_desc(a_base + (kk >> 2) * ABOX_BYTES + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd = smem_desc(b_base + (kk >> 2) * C::SBOX_BYTES + (kk & 3) * 32, 16, 1024);
+                        mma_bf16(*tmem_slot + acc * R, ad, bd, IDESC, first ? 0u : 1u);
+                    }
+                    mma_commit(mma_done);
+                }
             }
-            // publish the bf16 state after frame f for phase 3
-            const uint8_t* nxt = sop + (cur ^ 1) * C::STILE_BYTES;
-            for (int bx = 0; bx < sboxes; ++bx)
-                tma_store_3d(&tm_S, nxt + bx * C::SBOX_BYTES, 64 * bx, r0, item_of(f));
-            bulk_commit();
-            bulk_wait_read<1>();  // the store issued one frame ago no longer reads its buffer
+            const float a_f = a_next;
+            if (f + 1 < p.F) a_next = __ldg(p.alpha + static_cast<size_t>(b * p.F + f + 1) * p.H + h);
+
+            // the buffer this frame's image goes to was last stored NI frames ago
+            bool ok = f < NI || mbar_wait(&img_free[nxt], static_cast<uint32_t>(((f / NI) - 1) & 1),
+                                          p.wait_limit_ns, abort_flag);
+            ok = ok && mbar_wait(&afull[slot], static_cast<uint32_t>((f / AS) & 1), p.wait_limit_ns, abort_flag) &&
+                 mbar_wait(mma_done, static_cast<uint32_t>(f & 1), p.wait_limit_ns, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            // per chunk of RC rows: batch every read first (U rows, then the
+            // accumulators), then update the state and write its image
+            constexpr int RC = R < 32 ? R : 32;
+            const float* urow = reinterpret_cast<const float*>(aring + slot * C::STAGE_BYTES + ATILE_BYTES) + j;
+            uint8_t* img = sop + nxt * C::STILE_BYTES;
+#pragma unroll
+            for (int rc0 = 0; rc0 < R; rc0 += RC) {
+                float u[RC];
+#pragma unroll
+                for (int r = 0; r < RC; ++r) u[r] = urow[(rc0 + r) * 128];
+                uint32_t c[NACC][RC];
+#pragma unroll
+                for (int a = 0; a < NACC; ++a) {
+                    if (a < nacc) {
+#pragma unroll
+                        for (int rc = 0; rc < RC; rc += 16)
+                            tmem_ld16(tmem_warp + a * R + rc0 + rc, *reinterpret_cast<uint32_t(*)[16]>(&c[a][rc]));
+                    }
+                }
+                tmem_wait_ld();
+#pragma unroll
+                for (int r = 0; r < RC; ++r) {
+                    float cr = __uint_as_float(c[0][r]);
+#pragma unroll
+                    for (int a = 1; a < NACC; ++a)
+                        if (a < nacc) cr += __uint_as_float(c[a][r]);
+                    S[rc0 + r] = a_f * (S[rc0 + r] - cr) + u[r];
+                    *reinterpret_cast<__nv_bfloat16*>(img + sop_offset<R>(rc0 + r, j)) =
+                        __float2bfloat16_rn(S[rc0 + r]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&slot_free[slot]);  // U read, MMA that read A_f retired, accumulators drained
+            fence_proxy_async_smem();
+            mbar_arrive(&img_ready[nxt]);
+        }
+        if (f == p.F && p.state_out != nullptr && jv) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) p.state_out[state_off + static_cast<size_t>(r0 + r) * p.dk + j] = S[r];
+        }
+        if (tid == 0) {
+            mma_commit(final_bar);
+            mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
+        }
+    } else if (warp == 4) {
+        // -------------------------------------------------------- publisher
+        // Stores are pipelined: a frame's ready count is raised once at most
+        // two newer stores are still in flight.
+        if ((tid & 31) == 0) {
+            int published = 0;
+            auto publish_upto = [&](int f_end) {
+                if (flags == nullptr || published >= f_end) return;
+                fence_proxy_async_global();  // async-proxy writes ordered before the release below
+                for (; published < f_end; ++published) red_release_add(flags + item_of(published), 1);
+            };
+            int f = 0;
+            for (; f < p.F; ++f) {
+                const int x = (f + 1) % NI;  // buffer holding the image of the state after frame f
+                if (!mbar_wait(&img_ready[x], static_cast<uint32_t>(((f + 1) / NI) & 1), p.wait_limit_ns,
+                               abort_flag))
+                    break;
+                const uint8_t* img = sop + x * C::STILE_BYTES;
+                for (int bx = 0; bx < sboxes; ++bx)
+                    tma_store_3d(tm_S, img + bx * C::SBOX_BYTES, 64 * bx, r0, item_of(f));
+                bulk_commit();
+                bulk_wait_read<0>();
+                mbar_arrive(&img_free[x]);
+                bulk_wait<2>();  // stores of frames <= f - 2 are complete
+                publish_upto(f - 1);
+            }
+            bulk_wait<0>();
+            publish_upto(f);
+        }
+    } else if (warp == 5) {
+        // ----------------------------------------------------------- loader
+        if ((tid & 31) == 0) {
+            // one ring slot = A_f (bf16, 128x128 swizzled) followed by U_f rows r0..r0+R-1 (fp32)
+            int issued = 0;
+            for (int f = 0; f < p.F; ++f) {
+                const int slot = f % AS;
+                if (f >= AS && !mbar_wait(&slot_free[slot], static_cast<uint32_t>(((f / AS) - 1) & 1),
+                                          p.wait_limit_ns, abort_flag))
+                    break;
+                uint8_t* st = aring + slot * C::STAGE_BYTES;
+                mbar_arrive_expect_tx(&afull[slot], aboxes * ABOX_BYTES + C::UTILE_BYTES);
+                for (int bx = 0; bx < aboxes; ++bx)
+                    tma_load_3d(st + bx * ABOX_BYTES, tm_A, &afull[slot], 64 * bx, 0, item_of(f));
+                tma_load_3d(st + ATILE_BYTES, tm_U, &afull[slot], 0, r0, item_of(f));
+                ++issued;
+            }
+            // no copy may outlive the CTA (only matters when a wait gave up)
+            for (int k = (issued > AS ? issued - AS : 0); k < issued; ++k)
+                mbar_wait_drain(&afull[k % AS], static_cast<uint32_t>((k / AS) & 1), p.wait_limit_ns);
         }
     }
 
-    if (f == p.F && p.state_out != nullptr && jv) {
-#pragma unroll
-        for (int r = 0; r < R; ++r) p.state_out[state_off + static_cast<size_t>(r0 + r) * p.dk + j] = S[r];
-    }
-    if (tid == 0) {
-        bulk_wait<0>();
-        for (int fl = consumed; fl < loaded; ++fl)
-            mbar_wait_drain(&afull[fl % ASTAGES], static_cast<uint32_t>((fl / ASTAGES) & 1), p.wait_limit_ns);
-        mma_commit(final_bar);
-        mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
-    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(*tmem_slot, TMEM_COLS);
+        tmem_dealloc(*tmem_slot, C::TMEM_COLS);
     }
+}
+
+// Standalone phase 2: one CTA per R-row slice of each head.
+template <int R>
+__global__ void __launch_bounds__(THREADS, 1)
+    scan_kernel(const __grid_constant__ CUtensorMap tm_A, const __grid_constant__ CUtensorMap tm_U,
+                const __grid_constant__ CUtensorMap tm_S, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    scan_role<R>(&tm_A, &tm_U, &tm_S, p, blockIdx.x, nullptr, smem);
 }
 
 }  // namespace k2

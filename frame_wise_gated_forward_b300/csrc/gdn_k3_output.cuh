@@ -9,15 +9,21 @@
 //     M = 128 tokens, N = 128 (dv, zero-padded), K = dk (<= 128)
 // both operands K-major in 128-byte-swizzled shared memory, loaded by TMA
 // straight from q's token-major layout and from the bf16 per-frame states.
-// A persistent grid walks a contiguous range of tiles; S_f is loaded once per
-// item (2-deep ring), q through a 3-deep ring, four 128-column accumulators in
-// TMEM let the MMA run up to three tiles ahead of the epilogue.  Epilogue:
-// each of four warps drains its 32-lane quarter, rounds to bf16 (RNE), writes
-// a swizzled staging tile and stores it with its own TMA store (rows past N
-// are clipped by the tensor map).
+// S_f is loaded once per item (2-deep ring), q through a 3-deep ring, four
+// 128-column accumulators in TMEM let the MMA run up to three tiles ahead of
+// the epilogue.  Epilogue: each of four warps drains its 32-lane quarter,
+// rounds to bf16 (RNE), writes a swizzled staging tile and stores it with its
+// own TMA store (rows past N are clipped by the tensor map).
 //
 // Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
 // issuer, warps 2-5 epilogue (TMEM lane quarter = warp % 4).
+//
+// The role runs in two schedules:
+//  - standalone (output_kernel): a persistent grid, each CTA a contiguous
+//    range of tiles;
+//  - fused with the scan (gdn_k23_fused.cuh): each worker CTA takes whole
+//    items round-robin in frame-major order and, before loading S_f, waits
+//    (bounded) until the scan has published that item's state.
 #pragma once
 
 #include "gdn_ptx.cuh"
@@ -40,17 +46,69 @@ constexpr size_t SMEM_BYTES =
     1024 + QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES + 4 * 2 * OSTAGE_BYTES + 256;
 
 struct Params {
-    int H, N, dk, dv;
+    int B, H, F, N, dk, dv;
     int ntile;              // ceil(N / 128) tiles per item
     long long total;        // items * ntile
     unsigned long long wait_limit_ns;
 };
 
-__global__ void __launch_bounds__(THREADS, 1)
-    output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
-                  const __grid_constant__ CUtensorMap tm_out, const Params p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+// Which tiles a CTA processes, as a sequence of segments (item, nt_begin, nt_end).
+struct Sched {
+    // standalone: contiguous tile range [t0, t1)
+    long long t0, t1;
+    // fused: worker wi of nw takes frame-major item ranks wi, wi + nw, ...
+    int wi, nw;
+    bool fused;
+    const int* flags;       // fused: per-item count of published state slices
+    int flag_target;        // fused: slices per item
+
+    __device__ __forceinline__ bool segment(const Params& p, int k, long long& item, int& nb, int& ne) const {
+        if (!fused) {
+            // k-th segment of the contiguous range: walk items from t0
+            long long t = t0;
+            for (int i = 0; i < k && t < t1; ++i) t = (t / p.ntile + 1) * p.ntile;
+            if (t >= t1) return false;
+            item = t / p.ntile;
+            nb = static_cast<int>(t % p.ntile);
+            const long long end = (item + 1) * p.ntile < t1 ? (item + 1) * p.ntile : t1;
+            ne = static_cast<int>(end - item * p.ntile);
+            return true;
+        }
+        const long long rank = wi + static_cast<long long>(k) * nw;
+        const long long BH = static_cast<long long>(p.B) * p.H;
+        if (rank >= BH * p.F) return false;
+        const long long f = rank / BH, bh = rank % BH;
+        const long long b = bh / p.H, h = bh % p.H;
+        item = (b * p.F + f) * p.H + h;
+        nb = 0;
+        ne = p.ntile;
+        return true;
+    }
+};
+
+// Bounded wait until the scan has published all slices of `item`'s state.
+__device__ __forceinline__ bool wait_state_ready(const int* flags, long long item, int target, uint64_t limit_ns,
+                                                 volatile int* abort_flag) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flags + item) : "memory");
+    if (v >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(64);
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flags + item) : "memory");
+        if (v >= target) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            record_error(GDN_ERR_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUtensorMap* tm_s,
+                                            const CUtensorMap* tm_out, const Params& p, const Sched& sc,
+                                            uint8_t* smem) {
     uint8_t* qring = smem;
     uint8_t* sring = qring + QSTAGES * QTILE_BYTES;
     uint8_t* ostage = sring + SSTAGES * STILE_BYTES;   // [4 warps][2][OSTAGE_BYTES]
@@ -67,8 +125,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const long long t_begin = (static_cast<long long>(blockIdx.x) * p.total) / gridDim.x;
-    const long long t_end = (static_cast<long long>(blockIdx.x + 1) * p.total) / gridDim.x;
     const int kboxes = p.dk > 64 ? 2 : 1;
     const int vboxes = p.dv > 64 ? 2 : 1;
 
@@ -82,9 +138,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(final_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_s);
-        prefetch_tmap(&tm_out);
+        prefetch_tmap(tm_q);
+        prefetch_tmap(tm_s);
+        prefetch_tmap(tm_out);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -102,33 +158,36 @@ __global__ void __launch_bounds__(THREADS, 1)
             int qs = 0, ss = 0;
             uint32_t qph = 0, sph = 0;
             long long q_issued = 0, s_issued = 0;
-            long long prev_item = -1;
-            for (long long t = t_begin; t < t_end && !*abort_flag; ++t) {
-                const long long item = t / p.ntile;
-                const int nt = static_cast<int>(t % p.ntile);
+            long long item;
+            int nb, ne;
+            bool stop = false;
+            for (int k = 0; !stop && !*abort_flag && sc.segment(p, k, item, nb, ne); ++k) {
                 const int frame = static_cast<int>(item / p.H), h = static_cast<int>(item % p.H);
-                if (item != prev_item) {
-                    if (prev_item >= 0) { if (++ss == SSTAGES) { ss = 0; sph ^= 1; } }
-                    if (!mbar_wait(&sempty[ss], sph ^ 1, p.wait_limit_ns, abort_flag)) break;
-                    mbar_arrive_expect_tx(&sfull[ss], kboxes * BOX_BYTES);
-                    for (int bx = 0; bx < kboxes; ++bx)
-                        tma_load_3d(sring + ss * STILE_BYTES + bx * BOX_BYTES, &tm_s, &sfull[ss], 64 * bx, 0,
-                                    static_cast<int>(item));
-                    ++s_issued;
-                    prev_item = item;
+                if (k > 0) { if (++ss == SSTAGES) { ss = 0; sph ^= 1; } }
+                if (!mbar_wait(&sempty[ss], sph ^ 1, p.wait_limit_ns, abort_flag)) break;
+                if (sc.fused) {
+                    if (!wait_state_ready(sc.flags, item, sc.flag_target, p.wait_limit_ns, abort_flag)) break;
+                    fence_proxy_async_global();  // the published state is read through the async proxy
                 }
-                if (!mbar_wait(&qempty[qs], qph ^ 1, p.wait_limit_ns, abort_flag)) break;
-                mbar_arrive_expect_tx(&qfull[qs], kboxes * BOX_BYTES);
+                mbar_arrive_expect_tx(&sfull[ss], kboxes * BOX_BYTES);
                 for (int bx = 0; bx < kboxes; ++bx)
-                    tma_load_4d(qring + qs * QTILE_BYTES + bx * BOX_BYTES, &tm_q, &qfull[qs], 64 * bx, h,
-                                nt * TILE_M, frame);
-                ++q_issued;
-                if (++qs == QSTAGES) { qs = 0; qph ^= 1; }
+                    tma_load_3d(sring + ss * STILE_BYTES + bx * BOX_BYTES, tm_s, &sfull[ss], 64 * bx, 0,
+                                static_cast<int>(item));
+                ++s_issued;
+                for (int nt = nb; nt < ne; ++nt) {
+                    if (!mbar_wait(&qempty[qs], qph ^ 1, p.wait_limit_ns, abort_flag)) { stop = true; break; }
+                    mbar_arrive_expect_tx(&qfull[qs], kboxes * BOX_BYTES);
+                    for (int bx = 0; bx < kboxes; ++bx)
+                        tma_load_4d(qring + qs * QTILE_BYTES + bx * BOX_BYTES, tm_q, &qfull[qs], 64 * bx, h,
+                                    nt * TILE_M, frame);
+                    ++q_issued;
+                    if (++qs == QSTAGES) { qs = 0; qph ^= 1; }
+                }
             }
-            for (long long k = (q_issued > QSTAGES ? q_issued - QSTAGES : 0); k < q_issued; ++k)
-                mbar_wait_drain(&qfull[k % QSTAGES], static_cast<uint32_t>((k / QSTAGES) & 1), p.wait_limit_ns);
-            for (long long k = (s_issued > SSTAGES ? s_issued - SSTAGES : 0); k < s_issued; ++k)
-                mbar_wait_drain(&sfull[k % SSTAGES], static_cast<uint32_t>((k / SSTAGES) & 1), p.wait_limit_ns);
+            for (long long kq = (q_issued > QSTAGES ? q_issued - QSTAGES : 0); kq < q_issued; ++kq)
+                mbar_wait_drain(&qfull[kq % QSTAGES], static_cast<uint32_t>((kq / QSTAGES) & 1), p.wait_limit_ns);
+            for (long long ks = (s_issued > SSTAGES ? s_issued - SSTAGES : 0); ks < s_issued; ++ks)
+                mbar_wait_drain(&sfull[ks % SSTAGES], static_cast<uint32_t>((ks / SSTAGES) & 1), p.wait_limit_ns);
         }
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
@@ -137,31 +196,33 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int nk = (p.dk + 15) / 16;
             int qs = 0, ss = 0, acc = 0;
             uint32_t qph = 0, sph = 0, aph = 0;
-            long long prev_item = -1;
-            for (long long t = t_begin; t < t_end && !*abort_flag; ++t) {
-                const long long item = t / p.ntile;
-                const bool last_of_item = (t + 1 == t_end) || ((t + 1) / p.ntile != item);
-                if (item != prev_item) {
-                    if (prev_item >= 0) { if (++ss == SSTAGES) { ss = 0; sph ^= 1; } }
-                    if (!mbar_wait(&sfull[ss], sph, p.wait_limit_ns, abort_flag)) break;
-                    prev_item = item;
+            long long item;
+            int nb, ne;
+            bool stop = false;
+            for (int k = 0; !stop && !*abort_flag && sc.segment(p, k, item, nb, ne); ++k) {
+                if (k > 0) { if (++ss == SSTAGES) { ss = 0; sph ^= 1; } }
+                if (!mbar_wait(&sfull[ss], sph, p.wait_limit_ns, abort_flag)) break;
+                for (int nt = nb; nt < ne; ++nt) {
+                    if (!mbar_wait(&tempty[acc], aph ^ 1, p.wait_limit_ns, abort_flag) ||
+                        !mbar_wait(&qfull[qs], qph, p.wait_limit_ns, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(qring + qs * QTILE_BYTES);
+                    const uint32_t b_base = smem_u32(sring + ss * STILE_BYTES);
+                    const uint32_t d_tmem = tmem_base + acc * 128;
+                    for (int kk = 0; kk < nk; ++kk) {
+                        const uint64_t ad = smem_desc(a_base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd = smem_desc(b_base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
+                        mma_bf16(d_tmem, ad, bd, IDESC, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&qempty[qs]);
+                    mma_commit(&tfull[acc]);
+                    if (nt + 1 == ne) mma_commit(&sempty[ss]);
+                    if (++qs == QSTAGES) { qs = 0; qph ^= 1; }
+                    if (++acc == ACCS) { acc = 0; aph ^= 1; }
                 }
-                if (!mbar_wait(&tempty[acc], aph ^ 1, p.wait_limit_ns, abort_flag)) break;
-                if (!mbar_wait(&qfull[qs], qph, p.wait_limit_ns, abort_flag)) break;
-                tc_fence_after();
-                const uint32_t a_base = smem_u32(qring + qs * QTILE_BYTES);
-                const uint32_t b_base = smem_u32(sring + ss * STILE_BYTES);
-                const uint32_t d_tmem = tmem_base + acc * 128;
-                for (int kk = 0; kk < nk; ++kk) {
-                    const uint64_t ad = smem_desc(a_base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = smem_desc(b_base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
-                    mma_bf16(d_tmem, ad, bd, IDESC, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&qempty[qs]);
-                mma_commit(&tfull[acc]);
-                if (last_of_item) mma_commit(&sempty[ss]);
-                if (++qs == QSTAGES) { qs = 0; qph ^= 1; }
-                if (++acc == ACCS) { acc = 0; aph ^= 1; }
             }
             mma_commit(final_bar);
             mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
@@ -173,51 +234,60 @@ __global__ void __launch_bounds__(THREADS, 1)
         int acc = 0, ob = 0;
         uint32_t aph = 0;
         const int ncol32 = (p.dv + 31) / 32;
-        for (long long t = t_begin; t < t_end && !*abort_flag; ++t) {
-            const long long item = t / p.ntile;
-            const int nt = static_cast<int>(t % p.ntile);
+        long long item;
+        int nb, ne;
+        bool stop = false;
+        for (int k = 0; !stop && !*abort_flag && sc.segment(p, k, item, nb, ne); ++k) {
             const int frame = static_cast<int>(item / p.H), h = static_cast<int>(item % p.H);
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, p.wait_limit_ns, abort_flag));
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t tbase = tmem_base + acc * 128 + (static_cast<uint32_t>(quarter * 32) << 16);
-            uint32_t packed[64];
+            for (int nt = nb; nt < ne; ++nt) {
+                const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, p.wait_limit_ns, abort_flag));
+                if (!ok) { stop = true; break; }
+                tc_fence_after();
+                const uint32_t tbase = tmem_base + acc * 128 + (static_cast<uint32_t>(quarter * 32) << 16);
+                uint32_t packed[64];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (c < ncol32) {
-                    uint32_t r32[32];
-                    tmem_ld32(tbase + c * 32, r32);
-                    tmem_wait_ld();
+                for (int c = 0; c < 4; ++c) {
+                    if (c < ncol32) {
+                        uint32_t r32[32];
+                        tmem_ld32(tbase + c * 32, r32);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        packed[c * 16 + e] = pack_bf16x2(__uint_as_float(r32[2 * e]), __uint_as_float(r32[2 * e + 1]));
+                        for (int e = 0; e < 16; ++e)
+                            packed[c * 16 + e] =
+                                pack_bf16x2(__uint_as_float(r32[2 * e]), __uint_as_float(r32[2 * e + 1]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) packed[c * 16 + e] = 0u;
+                    }
                 }
-            }
-            tc_fence_before();
-            mbar_arrive(&tempty[acc]);
-            if (++acc == ACCS) { acc = 0; aph ^= 1; }
+                tc_fence_before();
+                mbar_arrive(&tempty[acc]);
+                if (++acc == ACCS) { acc = 0; aph ^= 1; }
 
-            // staging buffer `ob` was last read by the TMA store issued two tiles ago
-            if (lane == 0) bulk_wait_read<1>();
-            __syncwarp();
-            uint8_t* stg = my_stage + ob * OSTAGE_BYTES;
-            const int row = lane;  // token row within this warp's 32
+                // staging buffer `ob` was last read by the TMA store issued two tiles ago
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+                uint8_t* stg = my_stage + ob * OSTAGE_BYTES;
+                const int row = lane;  // token row within this warp's 32
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                const int box = ch >> 3, c8 = ch & 7;
-                if (box < vboxes) {
-                    uint4 v = make_uint4(packed[ch * 4 + 0], packed[ch * 4 + 1], packed[ch * 4 + 2], packed[ch * 4 + 3]);
-                    *reinterpret_cast<uint4*>(stg + box * OBOX_BYTES + row * 128 + ((c8 ^ (row & 7)) << 4)) = v;
+                for (int ch = 0; ch < 16; ++ch) {
+                    const int box = ch >> 3, c8 = ch & 7;
+                    if (box < vboxes) {
+                        uint4 v = make_uint4(packed[ch * 4 + 0], packed[ch * 4 + 1], packed[ch * 4 + 2],
+                                             packed[ch * 4 + 3]);
+                        *reinterpret_cast<uint4*>(stg + box * OBOX_BYTES + row * 128 + ((c8 ^ (row & 7)) << 4)) = v;
+                    }
                 }
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int row0 = nt * TILE_M + quarter * 32;
+                if (lane == 0 && row0 < p.N) {
+                    for (int bx = 0; bx < vboxes; ++bx)
+                        tma_store_4d(tm_out, stg + bx * OBOX_BYTES, 64 * bx, h, row0, frame);
+                }
+                if (lane == 0) bulk_commit();
+                ob ^= 1;
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                for (int bx = 0; bx < vboxes; ++bx)
-                    tma_store_4d(&tm_out, stg + bx * OBOX_BYTES, 64 * bx, h, nt * TILE_M + quarter * 32, frame);
-                bulk_commit();
-            }
-            ob ^= 1;
         }
         if (lane == 0) bulk_wait<0>();
     }
@@ -228,6 +298,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
+}
+
+// Standalone phase 3: persistent grid, contiguous tile ranges.
+__global__ void __launch_bounds__(THREADS, 1)
+    output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
+                  const __grid_constant__ CUtensorMap tm_out, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Sched sc;
+    sc.t0 = (static_cast<long long>(blockIdx.x) * p.total) / gridDim.x;
+    sc.t1 = (static_cast<long long>(blockIdx.x + 1) * p.total) / gridDim.x;
+    sc.wi = 0;
+    sc.nw = 1;
+    sc.fused = false;
+    sc.flags = nullptr;
+    sc.flag_target = 0;
+    output_role(&tm_q, &tm_s, &tm_out, p, sc, smem);
 }
 
 }  // namespace k3

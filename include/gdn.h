@@ -153,6 +153,24 @@ gdn_status gdn_sync_status(gdn_stream_t stream);
 void gdn_set_wait_limit_ns(unsigned long long limit_ns);
 
 /*
+ * Schedule of phases 2 and 3.  mode 1 (default): when the device supports
+ * cooperative launches and the heads leave most SMs free, the scan and the
+ * output pass run as one cooperative launch in which output CTAs consume each
+ * frame's state as soon as the scan CTAs publish it.  mode 16, 32 or 64: the
+ * same, with that many state rows per scan CTA (if dv allows it).  mode 0:
+ * the scan and the output pass run as two ordinary launches.  All schedules
+ * give identical results.  Applies to calls made after it returns.
+ */
+void gdn_set_fused_scan(int mode);
+
+/*
+ * Schedule phases 2 and 3 take for this shape on the current device: +R when
+ * they run as one cooperative launch with R rows of S per scan CTA, -R when
+ * they run as two launches, 0 for invalid shapes or no usable device.
+ */
+int gdn_scan_schedule(int B, int H, int dv);
+
+/*
  * Self-test of the bounded-wait machinery: launches one small kernel that
  * waits on a shared-memory barrier that nothing ever completes, with a wait
  * limit of `limit_ns`; the wait runs out, the kernel records GDN_ERR_TIMEOUT

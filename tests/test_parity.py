@@ -22,20 +22,28 @@ def _built():
     ensure_built()
 
 
+@pytest.fixture(params=["fused", "separate"])
+def schedule(request):
+    """Phases 2 and 3 as one cooperative launch, or as two launches."""
+    api.set_fused_scan(request.param == "fused")
+    yield request.param
+    api.set_fused_scan(True)
+
+
 @pytest.mark.parametrize("name", ["tiny", "window9"])
-def test_small_workloads_full_compare(name):
+def test_small_workloads_full_compare(name, schedule):
     w = inputs.WORKLOADS[name]
     x = inputs.workload_inputs(w)
     ref = oracle_run(x, w.B, w.H, w.F, w.N, w.dk, w.dv)
     out, st = gpu_forward(to_dev(x))
     eo = rel_err(out.float().cpu().numpy(), ref["out"])
     es = rel_err(st.cpu().numpy(), ref["state"])
-    print(f"{name}: err_O={eo:.3e} err_S={es:.3e}")
+    print(f"{name} [{schedule}]: err_O={eo:.3e} err_S={es:.3e}")
     assert eo <= TOL_OUT and es <= TOL_STATE
 
 
 @pytest.mark.parametrize("name", ["seq60s", "cfg2"])
-def test_full_size_workloads(name):
+def test_full_size_workloads(name, schedule):
     w = inputs.WORKLOADS[name]
     x = inputs.workload_inputs(w)
     toks = sample_tokens(w.B, w.F, w.N)
@@ -44,7 +52,8 @@ def test_full_size_workloads(name):
     flat = out.view(-1, w.H, w.dv)[torch.as_tensor(toks, device=out.device)].float().cpu().numpy()
     eo = rel_err(flat, ref["sample_out"])
     es = rel_err(st.cpu().numpy(), ref["state"])
-    print(f"{name}: err_O(sampled {toks.size})={eo:.3e} err_S={es:.3e}")
+    print(f"{name} [{schedule}, R={api.scan_schedule(w.B, w.H, w.dv)}]: "
+          f"err_O(sampled {toks.size})={eo:.3e} err_S={es:.3e}")
     assert np.isfinite(out.float().cpu().numpy()).all()
     assert eo <= TOL_OUT and es <= TOL_STATE
     if w.B == 2:  # each guidance stream on its own matches its rows of the batch
@@ -54,7 +63,7 @@ def test_full_size_workloads(name):
             assert torch.equal(ob, out[b:b + 1]) and torch.equal(sb, st[b:b + 1])
 
 
-def test_streaming_rollout_121_steps():
+def test_streaming_rollout_121_steps(schedule):
     w = inputs.WORKLOADS["stream121"]
     x = inputs.workload_inputs(w)
     toks = sample_tokens(1, w.F, w.N, n_random=500)
@@ -69,5 +78,17 @@ def test_streaming_rollout_121_steps():
     flat = outs.view(-1, w.H, w.dv)[torch.as_tensor(toks, device="cuda")].float().cpu().numpy()
     eo = rel_err(flat, ref["sample_out"])
     es = rel_err(state.cpu().numpy(), ref["state"])
-    print(f"stream121: err_O={eo:.3e} err_S={es:.3e}")
+    print(f"stream121 [{schedule}]: err_O={eo:.3e} err_S={es:.3e}")
     assert eo <= TOL_OUT and es <= TOL_STATE
+
+
+def test_schedules_agree_exactly():
+    """The fused and the two-launch schedules run the same arithmetic."""
+    w = inputs.WORKLOADS["seq60s"]
+    x = to_dev(inputs.workload_inputs(w))
+    res = {}
+    for fused in (True, False):
+        api.set_fused_scan(fused)
+        res[fused] = gpu_forward(x)
+    api.set_fused_scan(True)
+    assert torch.equal(res[True][0], res[False][0]) and torch.equal(res[True][1], res[False][1])
