@@ -32,11 +32,28 @@
 namespace gdn {
 namespace k1 {
 
+#ifndef GDN_K1_INPLACE
+#define GDN_K1_INPLACE 0
+#endif
+#if GDN_K1_INPLACE
+// K and V are scaled in place by sqrt(beta): A = K'^T K', U^T = K'^T V'
+#ifndef GDN_K1_STAGES
+#define GDN_K1_STAGES 7
+#endif
+#define GDN_K1_BK_BUFS 0
+#else
 #ifndef GDN_K1_STAGES
 #define GDN_K1_STAGES 5
 #endif
 #ifndef GDN_K1_BK_BUFS
 #define GDN_K1_BK_BUFS 3
+#endif
+#endif
+#ifndef GDN_K1_ROUND_ROBIN
+#define GDN_K1_ROUND_ROBIN 1
+#endif
+#ifndef GDN_K1_L2_AHEAD
+#define GDN_K1_L2_AHEAD 0
 #endif
 #ifndef GDN_K1_SCALER_WARPS
 #define GDN_K1_SCALER_WARPS 4
@@ -56,9 +73,10 @@ constexpr int CH16 = 16 / (SCALER_THREADS / 64);
 static_assert(SCALER_THREADS % 64 == 0 && CH16 >= 1 && 16 % (SCALER_THREADS / 64) == 0, "scaler split");
 // beta is copied global -> shared by each scaler thread BETA_AHEAD chunks before
 // its use, into a per-thread ring of BETA_AHEAD + 1 slots
-constexpr int BETA_AHEAD = 4;
+constexpr int BETA_AHEAD = GDN_K1_INPLACE ? 2 : 4;
 constexpr int BETA_RING_BYTES = (BETA_AHEAD + 1) * SCALER_THREADS * 4;
 static_assert(1024 + STAGES * STAGE_BYTES + BK_BUFS * TILE_BYTES + BETA_RING_BYTES + 256 <= 232448, "shared memory");
+static_assert(!GDN_K1_INPLACE || SCALER_THREADS == 128, "in-place scaling: one (row, tile) per scaler thread");
 constexpr int TMEM_COLS = 512;
 constexpr int ACC_COLS = 256;
 // MN-major operand with 128-byte swizzle: 64 MN-elements per 128-byte row,
@@ -108,7 +126,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t* empty = full + STAGES;                // [STAGES]  MMA finished reading the stage
     uint64_t* bk_full = empty + STAGES;             // [BK_BUFS] beta*K written
     uint64_t* bk_empty = bk_full + BK_BUFS;         // [BK_BUFS] MMA finished reading beta*K
-    uint64_t* tfull = bk_empty + BK_BUFS;           // [2]       accumulator ready
+    uint64_t* scaled = bk_empty + BK_BUFS;          // [STAGES]  (in place) stage scaled by sqrt(beta)
+    uint64_t* tfull = scaled + (GDN_K1_INPLACE ? STAGES : 0);  // [2] accumulator ready
     uint64_t* tempty = tfull + 2;                   // [2]       accumulator drained
     uint64_t* final_bar = tempty + 2;               // [1]       every issued MMA retired
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
@@ -116,8 +135,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+#if GDN_K1_ROUND_ROBIN
+    // work units round-robin over the grid: at any time the CTAs work on
+    // consecutive items, i.e. all heads of the same few frames, so together
+    // they read whole token rows (all heads) of k and v
+    const int w_begin = blockIdx.x, w_end = p.work, w_step = gridDim.x;
+#else
     const int w_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * p.work) / gridDim.x);
     const int w_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.work) / gridDim.x);
+    const int w_step = 1;
+#endif
     const int kboxes = p.dk > 64 ? 2 : 1;
     const int vboxes = p.dv > 64 ? 2 : 1;
 
@@ -133,6 +160,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&bk_full[b], SCALER_THREADS);
             mbar_init(&bk_empty[b], 1);
         }
+        if (GDN_K1_INPLACE)
+            for (int st = 0; st < STAGES; ++st) mbar_init(&scaled[st], SCALER_THREADS);
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], 128);
@@ -159,11 +188,29 @@ __global__ void __launch_bounds__(THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
-            for (int w = w_begin; w < w_end && !*abort_flag; ++w) {
+            // L2 prefetch cursor GDN_K1_L2_AHEAD chunks ahead of the loads: the
+            // loads into the ring then find their data in L2, which keeps more
+            // bytes in flight than the ring alone can hold
+            int lw = w_begin, lc = 0;
+            if (lw < w_end) lc = unit_of(p, lw).c_begin;
+            auto prefetch_next = [&]() {
+                if (lw >= w_end) return;
+                const Unit u = unit_of(p, lw);
+                const int fr = u.item / p.H, hh = u.item % p.H;
+                for (int bx = 0; bx < kboxes; ++bx) tma_prefetch_l2_4d(&tm_k, 64 * bx, hh, lc * CHUNK, fr);
+                for (int bx = 0; bx < vboxes; ++bx) tma_prefetch_l2_4d(&tm_v, 64 * bx, hh, lc * CHUNK, fr);
+                if (++lc >= u.c_end) {
+                    lw += w_step;
+                    if (lw < w_end) lc = unit_of(p, lw).c_begin;
+                }
+            };
+            for (int i = 0; i < STAGES + GDN_K1_L2_AHEAD; ++i) prefetch_next();
+            for (int w = w_begin; w < w_end && !*abort_flag; w += w_step) {
                 const Unit u = unit_of(p, w);
                 const int frame = u.item / p.H, h = u.item % p.H;
                 for (int c = u.c_begin; c < u.c_end; ++c) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, abort_flag)) break;
+                    if (GDN_K1_L2_AHEAD > 0) prefetch_next();
                     uint8_t* st = stage_base + stage * STAGE_BYTES;
                     mbar_arrive_expect_tx(&full[stage], (kboxes + vboxes) * BOX_BYTES);
                     for (int bx = 0; bx < kboxes; ++bx)
@@ -188,13 +235,22 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t phase = 0, bk_phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            for (int w = w_begin; w < w_end && !*abort_flag; ++w) {
+            for (int w = w_begin; w < w_end && !*abort_flag; w += w_step) {
                 const Unit u = unit_of(p, w);
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1, p.wait_limit_ns, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
                 bool ok = true;
                 for (int c = u.c_begin; c < u.c_end; ++c) {
+#if GDN_K1_INPLACE
+                    if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag) ||
+                        !mbar_wait(&scaled[stage], phase, p.wait_limit_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(stage_base + stage * STAGE_BYTES);  // sqrt(beta) K
+#else
                     if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag) ||
                         !mbar_wait(&bk_full[bk], bk_phase, p.wait_limit_ns, abort_flag)) {
                         ok = false;
@@ -202,6 +258,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t a_base = smem_u32(bk_base + bk * TILE_BYTES);       // beta*K
+#endif
                     const uint32_t b_base = smem_u32(stage_base + stage * STAGE_BYTES); // [K | V]
 #pragma unroll
                     for (int kk = 0; kk < CHUNK / 16; ++kk) {
@@ -210,9 +267,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                         mma_bf16(d_tmem, ad, bd, IDESC, (c > u.c_begin || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(&empty[stage]);
+#if !GDN_K1_INPLACE
                     mma_commit(&bk_empty[bk]);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
                     if (++bk == BK_BUFS) { bk = 0; bk_phase ^= 1; }
+#endif
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
                 mma_commit(&tfull[acc]);
@@ -243,7 +302,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 else
                     *dst = 0.0f;
                 if (++pc >= u.c_end) {
-                    ++pw;
+                    pw += w_step;
                     if (pw < w_end) pc = unit_of(p, pw).c_begin;
                 }
             }
@@ -254,7 +313,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int cslot = 0;
         int stage = 0, bk = 0;
         uint32_t phase = 0, bk_phase = 0;
-        for (int w = w_begin; w < w_end && !*abort_flag; ++w) {
+        for (int w = w_begin; w < w_end && !*abort_flag; w += w_step) {
             const Unit u = unit_of(p, w);
             bool ok = true;
             for (int c = u.c_begin; c < u.c_end; ++c) {
@@ -262,6 +321,40 @@ __global__ void __launch_bounds__(THREADS, 1)
                 cp_async_wait<BETA_AHEAD>();           // this chunk's copy has landed
                 const float bval = beta_ring[cslot * SCALER_THREADS + t];
                 if (++cslot == BETA_AHEAD + 1) cslot = 0;
+#if GDN_K1_INPLACE
+                if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                {
+                    // thread (row r, tile t>>6): scale row r of the K (0) or V (1) tile in place
+                    const int tile = t >> 6;
+                    const int nbx = tile == 0 ? kboxes : vboxes;
+                    const float sb = sqrtf(fmaxf(bval, 0.0f));
+                    uint8_t* row = stage_base + stage * STAGE_BYTES + tile * TILE_BYTES + r * 128;
+                    uint4 x[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int bx = i >> 3;
+                        if (bx < nbx) x[i] = *reinterpret_cast<const uint4*>(row + bx * BOX_BYTES + ((((i & 7) + r) & 7) << 4));
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int bx = i >> 3;
+                        if (bx >= nbx) continue;
+                        uint32_t* xs = reinterpret_cast<uint32_t*>(&x[i]);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            __nv_bfloat162 pr = *reinterpret_cast<__nv_bfloat162*>(&xs[e]);
+                            float2 f2 = __bfloat1622float2(pr);
+                            xs[e] = pack_bf16x2(f2.x * sb, f2.y * sb);
+                        }
+                        *reinterpret_cast<uint4*>(row + bx * BOX_BYTES + ((((i & 7) + r) & 7) << 4)) = x[i];
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&scaled[stage]);
+#else
                 if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag) ||
                     !mbar_wait(&bk_empty[bk], bk_phase ^ 1, p.wait_limit_ns, abort_flag)) {
                     ok = false;
@@ -282,23 +375,31 @@ __global__ void __launch_bounds__(THREADS, 1)
                         off[i] = (g >> 3) * BOX_BYTES + ((((g & 7) + r) & 7) << 4);
                         if ((g >> 3) < kboxes) x[i] = *reinterpret_cast<const uint4*>(src + off[i]);
                     }
+                    // beta = hi + lo with hi, lo in bf16; beta*k = fma(k, hi, k*lo) on packed
+                    // bf16 pairs: the small k*lo term carries the rest of beta, so the
+                    // product is rounded to bf16 essentially once, as an fp32 product would be
+                    const __nv_bfloat16 bhi = __float2bfloat16_rn(bval);
+                    const __nv_bfloat16 blo = __float2bfloat16_rn(bval - __bfloat162float(bhi));
+                    const __nv_bfloat162 hi2 = __halves2bfloat162(bhi, bhi);
+                    const __nv_bfloat162 lo2 = __halves2bfloat162(blo, blo);
 #pragma unroll
                     for (int i = 0; i < CH16; ++i) {
                         if (((c16 + i) >> 3) >= kboxes) continue;
                         uint32_t* xs = reinterpret_cast<uint32_t*>(&x[i]);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            __nv_bfloat162 pr = *reinterpret_cast<__nv_bfloat162*>(&xs[e]);
-                            float2 f2 = __bfloat1622float2(pr);
-                            xs[e] = pack_bf16x2(f2.x * bval, f2.y * bval);
+                            const __nv_bfloat162 kk2 = *reinterpret_cast<__nv_bfloat162*>(&xs[e]);
+                            const __nv_bfloat162 r2 = __hfma2(kk2, hi2, __hmul2(kk2, lo2));
+                            xs[e] = *reinterpret_cast<const uint32_t*>(&r2);
                         }
                         *reinterpret_cast<uint4*>(dst + off[i]) = x[i];
                     }
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&bk_full[bk]);
-                if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 if (++bk == BK_BUFS) { bk = 0; bk_phase ^= 1; }
+#endif
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
             if (!ok) break;
         }
@@ -309,7 +410,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int j = quarter * 32 + lane;  // TMEM lane = row j of (beta K)^T = dk index
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int w = w_begin; w < w_end && !*abort_flag; ++w) {
+        for (int w = w_begin; w < w_end && !*abort_flag; w += w_step) {
             const Unit u = unit_of(p, w);
             const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, p.wait_limit_ns, abort_flag));
             if (!ok) break;
