@@ -317,6 +317,29 @@ def main():
     ms_per_step = sec_max / args.steps * 1e3
     floor_ms = path_floor_bytes(w) / (peaks["hbm_gbs"] * 1e9) * 1e3
 
+    # ------------------------------------------- interactive step (one frame)
+    # the streaming rollout: F sequential gdn_frame_step calls on a resident state
+    step_state = torch.zeros((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=device)
+    step_out = torch.empty((w.B, w.N, w.H, w.dv), dtype=torch.bfloat16, device=device)
+    frames = [tuple(xd[k][:, f].contiguous() for k in ("q", "k", "v", "alpha", "beta")) for f in range(w.F)]
+    for f in range(3):
+        api.frame_step(*frames[f], step_state, out=step_out, state_out=step_state)
+    torch.cuda.synchronize(device)
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for f in range(w.F):
+        api.frame_step(*frames[f], step_state, out=step_out, state_out=step_state)
+    s1.record(stream)
+    torch.cuda.synchronize(device)
+    api.sync_status()
+    step_us = s0.elapsed_time(s1) * 1e3 / w.F
+    step_info = {"us_per_frame_step": step_us, "tokens_per_s": w.B * w.N / (step_us / 1e6),
+                 "launches_per_step": 4, "frames": w.F,
+                 "floor_us": (w.B * w.N * w.H * (2 * w.dk + 2 * w.dv) * 2 + 2 * w.B * w.H * w.dv * w.dk * 4)
+                 / (peaks["hbm_gbs"] * 1e9) * 1e6}
+    del frames
+
     # ---------------------------------------------------------------------- e2e
     hx = {k: v.pin_memory() for k, v in x.items()}
     h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
@@ -365,6 +388,7 @@ def main():
                               "ceiling_tokens_per_s": tokens / (floor_ms / 1e3) * world},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": args.e2e_steps},
+            "step": step_info,
             "cpu_baseline": cpu,
             "clocks": clocks,
             "gpu_launches": (3 if sched <= 0 else 2) * args.steps,
