@@ -317,6 +317,22 @@ def main():
     ms_per_step = sec_max / args.steps * 1e3
     floor_ms = path_floor_bytes(w) / (peaks["hbm_gbs"] * 1e9) * 1e3
 
+    # ------------------------------------- reverse direction (bidirectional stage)
+    nr = min(args.steps, 100)
+    r0 = torch.cuda.Event(enable_timing=True)
+    r1 = torch.cuda.Event(enable_timing=True)
+    api.frame_forward(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], s_in, out=out, state_out=st, reverse=True)
+    torch.cuda.synchronize(device)
+    r0.record(stream)
+    for _ in range(nr):
+        api.frame_forward(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], s_in, out=out, state_out=st,
+                          reverse=True)
+    r1.record(stream)
+    torch.cuda.synchronize(device)
+    api.sync_status()
+    rev_ms = r0.elapsed_time(r1) / nr
+    reverse_info = {"ms_per_step": rev_ms, "tokens_per_s": tokens / (rev_ms / 1e3), "steps": nr}
+
     # ------------------------------------------- interactive step (one frame)
     # the streaming rollout: F sequential gdn_frame_step calls on a resident state
     step_state = torch.zeros((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=device)
@@ -389,6 +405,7 @@ def main():
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": args.e2e_steps},
             "step": step_info,
+            "reverse_direction": reverse_info,
             "cpu_baseline": cpu,
             "clocks": clocks,
             "gpu_launches": (3 if sched <= 0 else 2) * args.steps,

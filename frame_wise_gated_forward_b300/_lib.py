@@ -18,7 +18,8 @@ STATUS = {
     8: "GDN_ERR_ALIAS", 9: "GDN_ERR_NO_DEVICE", 10: "GDN_ERR_TOO_LARGE",
 }
 EXPORTS = (
-    "gdn_frame_forward", "gdn_frame_step", "gdn_frame_forward_timed", "gdn_frame_forward_host",
+    "gdn_frame_forward", "gdn_frame_forward_reverse", "gdn_frame_step", "gdn_frame_forward_timed",
+    "gdn_frame_forward_host",
     "gdn_workspace_bytes", "gdn_step_workspace_bytes",
     "gdn_status_string", "gdn_sync_status", "gdn_set_wait_limit_ns", "gdn_selftest_wait_timeout",
     "gdn_version", "gdn_frame_step_noalloc", "gdn_set_fused_scan", "gdn_scan_schedule",
@@ -47,6 +48,8 @@ def load(path: str | None = None):
     vp, fp, i, st = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
     lib.gdn_frame_forward.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, st]
     lib.gdn_frame_forward.restype = ctypes.c_int
+    lib.gdn_frame_forward_reverse.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, st]
+    lib.gdn_frame_forward_reverse.restype = ctypes.c_int
     lib.gdn_frame_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, st]
     lib.gdn_frame_step.restype = ctypes.c_int
     lib.gdn_frame_forward_timed.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, st,

@@ -37,8 +37,10 @@ def _dev(t, name, dtype, shape):
     return t.data_ptr()
 
 
-def frame_forward(q, k, v, alpha, beta, state_in=None, *, out=None, state_out=None, stream=None):
-    """Whole-sequence forward.  Returns (out bf16 [B,F,N,H,dv], state_out fp32 [B,H,dv,dk])."""
+def frame_forward(q, k, v, alpha, beta, state_in=None, *, out=None, state_out=None, stream=None,
+                  reverse=False):
+    """Whole-sequence forward.  Returns (out bf16 [B,F,N,H,dv], state_out fp32 [B,H,dv,dk]).
+    reverse=True scans the frames from the last to the first (bidirectional stage)."""
     lib = load()
     B, F, N, H, dk = q.shape
     dv = v.shape[-1]
@@ -56,7 +58,8 @@ def frame_forward(q, k, v, alpha, beta, state_in=None, *, out=None, state_out=No
         _dev(out, "out", torch.bfloat16, (B, F, N, H, dv)),
         _dev(state_out, "state_out", torch.float32, (B, H, dv, dk)),
     ]
-    check(lib.gdn_frame_forward(*args, B, H, F, N, dk, dv, _stream_handle(stream)), "gdn_frame_forward")
+    fn = lib.gdn_frame_forward_reverse if reverse else lib.gdn_frame_forward
+    check(fn(*args, B, H, F, N, dk, dv, _stream_handle(stream)), "gdn_frame_forward")
     return out, state_out
 
 

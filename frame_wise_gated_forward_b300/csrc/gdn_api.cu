@@ -185,10 +185,16 @@ Layout layout_of(long long items, int dk, int dv, int nsplit) {
     return L;
 }
 
+#ifndef GDN_STEP_MAX_SPLIT
+#define GDN_STEP_MAX_SPLIT 4
+#endif
+// Token splits per head for the one-frame step: enough CTAs to stream the
+// frame, few enough that the fp32 partial sums stay small.
 int step_nsplit(int sms, int B, int H, int N) {
     const int items = B * H;
     const int chunks = (N + gdn::k1::CHUNK - 1) / gdn::k1::CHUNK;
     int ns = std::max(1, sms / std::max(items, 1));
+    ns = std::min(ns, GDN_STEP_MAX_SPLIT);
     return std::min(ns, chunks);
 }
 
@@ -240,6 +246,7 @@ struct PassArgs {
     void* out;
     float* state_out;
     int B, H, F, N, dk, dv;
+    int reverse = 0;
 };
 
 // Rows of S per scan CTA.  Standalone scan: the smallest slice that keeps
@@ -321,6 +328,7 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, int ns
     p2.dk = a.dk;
     p2.dv = a.dv;
     p2.rsplit = a.dv / R;
+    p2.reverse = a.reverse;
     p2.wait_limit_ns = lim;
     gdn::k3::Params p3;
     p3.B = a.B;
@@ -331,13 +339,14 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, int ns
     p3.dv = a.dv;
     p3.ntile = (a.N + gdn::k3::TILE_M - 1) / gdn::k3::TILE_M;
     p3.total = items * p3.ntile;
+    p3.reverse = a.reverse;
     p3.wait_limit_ns = lim;
     const int n_scan = a.B * a.H * p2.rsplit;
     if (Rf != 0) {
         // one cooperative launch: scan CTAs publish per-frame states, output CTAs follow them
         if (cudaMemsetAsync(flags, 0, static_cast<size_t>(items) * sizeof(int), stream) != cudaSuccess)
             return GDN_ERR_LAUNCH;
-        const long long workers = std::min<long long>(ds->sms - n_scan, std::max<long long>(1, items));
+        const long long workers = std::min<long long>(ds->sms - n_scan, std::max<long long>(1, items * p3.ntile));
         int grid = n_scan + static_cast<int>(workers);
         int n_scan_arg = n_scan;
         void* args[] = {&tm_A, &tm_U, &tm_S_store, &tm_q, &tm_S_load, &tm_out, &p2, &p3, &flags, &n_scan_arg};
@@ -426,6 +435,16 @@ gdn_status gdn_frame_step(const void* q, const void* k, const void* v, const flo
     if (s != GDN_OK) return s;
     return run_pass(PassArgs{q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv}, true,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_frame_forward_reverse(const void* q, const void* k, const void* v, const float* alpha,
+                                     const float* beta, const float* state_in, void* out, float* state_out, int B,
+                                     int H, int F, int N, int dk, int dv, gdn_stream_t stream) {
+    gdn_status s = validate(q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv);
+    if (s != GDN_OK) return s;
+    PassArgs a{q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv};
+    a.reverse = 1;
+    return run_pass(a, false, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gdn_status gdn_frame_forward_timed(const void* q, const void* k, const void* v, const float* alpha,

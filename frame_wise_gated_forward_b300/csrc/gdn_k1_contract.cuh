@@ -58,7 +58,10 @@ namespace k1 {
 #ifndef GDN_K1_SCALER_WARPS
 #define GDN_K1_SCALER_WARPS 4
 #endif
-constexpr int CHUNK = 64;                   // tokens per stage (MMA K extent per stage)
+#ifndef GDN_K1_CHUNK
+#define GDN_K1_CHUNK 64
+#endif
+constexpr int CHUNK = GDN_K1_CHUNK;         // tokens per stage (MMA K extent per stage)
 constexpr int STAGES = GDN_K1_STAGES;       // K/V ring depth
 constexpr int BK_BUFS = GDN_K1_BK_BUFS;     // beta*K buffers
 constexpr int BOX_BYTES = CHUNK * 128;      // 64 token rows x 128 B (64 bf16)
@@ -69,8 +72,9 @@ constexpr int SCALER_THREADS = SCALER_WARPS * 32;
 constexpr int EPI_WARP0 = 2 + SCALER_WARPS;  // four epilogue warps follow the scalers
 constexpr int THREADS = (EPI_WARP0 + 4) * 32;
 // each scaler thread owns one token row and CH16 of its sixteen 16-byte chunks
-constexpr int CH16 = 16 / (SCALER_THREADS / 64);
-static_assert(SCALER_THREADS % 64 == 0 && CH16 >= 1 && 16 % (SCALER_THREADS / 64) == 0, "scaler split");
+constexpr int TPR = SCALER_THREADS / CHUNK;   // scaler threads per token row
+constexpr int CH16 = 16 / TPR;
+static_assert(SCALER_THREADS % CHUNK == 0 && CH16 >= 1 && 16 % TPR == 0, "scaler split");
 // beta is copied global -> shared by each scaler thread BETA_AHEAD chunks before
 // its use, into a per-thread ring of BETA_AHEAD + 1 slots
 constexpr int BETA_AHEAD = GDN_K1_INPLACE ? 2 : 4;
@@ -148,9 +152,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int kboxes = p.dk > 64 ? 2 : 1;
     const int vboxes = p.dv > 64 ? 2 : 1;
 
-    // Zero every buffer once: boxes that are never loaded (d <= 64) must read as 0.
-    for (int i = threadIdx.x; i < (STAGES * STAGE_BYTES + BK_BUFS * TILE_BYTES) / 16; i += THREADS)
-        reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+    // Boxes that are never loaded (d <= 64) must read as 0; with d > 64 every
+    // byte is written before it is read.
+    if (kboxes < 2 || vboxes < 2)
+        for (int i = threadIdx.x; i < (STAGES * STAGE_BYTES + BK_BUFS * TILE_BYTES) / 16; i += THREADS)
+            reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -283,8 +289,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp < EPI_WARP0) {
         // ------------------------------------------------------ beta scalers
         const int t = threadIdx.x - 64;     // 0..SCALER_THREADS-1
-        const int r = t & 63;               // token row within the stage
-        const int c16 = (t >> 6) * CH16;    // first 16-byte chunk of the row this thread scales
+        const int r = t % CHUNK;            // token row within the stage
+        const int c16 = (t / CHUNK) * CH16; // first 16-byte chunk of the row this thread scales
         // beta is copied to shared memory BETA_AHEAD chunks ahead of its use (a
         // cursor walks the same unit/chunk sequence), so its global-load
         // latency never sits between a landed K tile and its MMA.  Each thread

@@ -62,6 +62,7 @@ struct Params {
     float* state_out;       // [B, H, dv, dk] or nullptr
     int H, F, dk, dv;
     int rsplit;             // dv / R CTAs per head
+    int reverse;            // nonzero: scan the frames from F-1 down to 0
     unsigned long long wait_limit_ns;
 };
 
@@ -104,10 +105,15 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_A, const CUtenso
     const int nk = (p.dk + 15) / 16;
     const int nacc = nk < NACC ? nk : NACC;
     const bool jv = j < p.dk;
-    auto item_of = [&](int f) { return (b * p.F + f) * p.H + h; };
+    // step f of the scan handles latent frame fr(f): f itself, or F-1-f when reversed
+    auto fr = [&](int f) { return p.reverse ? p.F - 1 - f : f; };
+    auto item_of = [&](int f) { return (b * p.F + fr(f)) * p.H + h; };
 
-    for (int i = tid; i < (AS * C::STAGE_BYTES + NI * C::STILE_BYTES) / 16; i += blockDim.x)
-        reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+    // A_f's second box is never loaded when dk <= 64 and must read as zero;
+    // everything else is written before it is read
+    if (aboxes < 2)
+        for (int i = tid; i < (AS * C::STAGE_BYTES + NI * C::STILE_BYTES) / 16; i += blockDim.x)
+            reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         for (int s = 0; s < AS; ++s) {
             mbar_init(&afull[s], 1);
@@ -149,7 +155,7 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_A, const CUtenso
             *reinterpret_cast<__nv_bfloat16*>(sop + sop_offset<R>(r, j)) = __float2bfloat16_rn(S[r]);
         fence_proxy_async_smem();
         mbar_arrive(&img_ready[0]);  // initial image (never stored: the publisher skips it)
-        float a_next = __ldg(p.alpha + static_cast<size_t>(b * p.F) * p.H + h);
+        float a_next = __ldg(p.alpha + static_cast<size_t>(b * p.F + fr(0)) * p.H + h);
 
         constexpr uint32_t IDESC = idesc_bf16(128, R, 0, 0);
         int f = 0;
@@ -178,7 +184,7 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_A, const CUtenso
                 }
             }
             const float a_f = a_next;
-            if (f + 1 < p.F) a_next = __ldg(p.alpha + static_cast<size_t>(b * p.F + f + 1) * p.H + h);
+            if (f + 1 < p.F) a_next = __ldg(p.alpha + static_cast<size_t>(b * p.F + fr(f + 1)) * p.H + h);
 
             // the buffer this frame's image goes to was last stored NI frames ago
             bool ok = f < NI || mbar_wait(&img_free[nxt], static_cast<uint32_t>(((f / NI) - 1) & 1),

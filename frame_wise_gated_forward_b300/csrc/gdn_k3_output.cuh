@@ -22,8 +22,9 @@
 //  - standalone (output_kernel): a persistent grid, each CTA a contiguous
 //    range of tiles;
 //  - fused with the scan (gdn_k23_fused.cuh): each worker CTA takes whole
-//    items round-robin in frame-major order and, before loading S_f, waits
-//    (bounded) until the scan has published that item's state.
+//    items (single tiles when there are fewer than two items per worker, as
+//    in a one-frame step) round-robin in frame-major order and, before loading
+//    S_f, waits (bounded) until the scan has published that item's state.
 #pragma once
 
 #include "gdn_ptx.cuh"
@@ -49,6 +50,7 @@ struct Params {
     int B, H, F, N, dk, dv;
     int ntile;              // ceil(N / 128) tiles per item
     long long total;        // items * ntile
+    int reverse;            // fused schedule: follow a scan that runs from frame F-1 down
     unsigned long long wait_limit_ns;
 };
 
@@ -76,12 +78,16 @@ struct Sched {
         }
         const long long rank = wi + static_cast<long long>(k) * nw;
         const long long BH = static_cast<long long>(p.B) * p.H;
-        if (rank >= BH * p.F) return false;
-        const long long f = rank / BH, bh = rank % BH;
+        const bool per_tile = BH * p.F < 2LL * nw;  // few items: spread single tiles instead
+        const long long units = per_tile ? BH * p.F * p.ntile : BH * p.F;
+        if (rank >= units) return false;
+        const long long ir = per_tile ? rank / p.ntile : rank;
+        const long long fs = ir / BH, bh = ir % BH;
+        const long long f = p.reverse ? p.F - 1 - fs : fs;
         const long long b = bh / p.H, h = bh % p.H;
         item = (b * p.F + f) * p.H + h;
-        nb = 0;
-        ne = p.ntile;
+        nb = per_tile ? static_cast<int>(rank % p.ntile) : 0;
+        ne = per_tile ? nb + 1 : p.ntile;
         return true;
     }
 };
@@ -128,9 +134,10 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
     const int kboxes = p.dk > 64 ? 2 : 1;
     const int vboxes = p.dv > 64 ? 2 : 1;
 
-    // never-loaded boxes (d <= 64) must read as zero
-    for (int i = threadIdx.x; i < (QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES) / 16; i += THREADS)
-        reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+    // never-loaded boxes (dk <= 64) must read as zero
+    if (kboxes < 2)
+        for (int i = threadIdx.x; i < (QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES) / 16; i += THREADS)
+            reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
         for (int s = 0; s < QSTAGES; ++s) { mbar_init(&qfull[s], 1); mbar_init(&qempty[s], 1); }
         for (int s = 0; s < SSTAGES; ++s) { mbar_init(&sfull[s], 1); mbar_init(&sempty[s], 1); }

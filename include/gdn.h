@@ -85,6 +85,23 @@ gdn_status gdn_frame_forward(const void* q, const void* k, const void* v,
                              gdn_stream_t stream);
 
 /*
+ * Reverse-direction forward for the bidirectional stage (WorldFoundry model
+ * card, "What it is for": the quality profile keeps a bidirectional stage):
+ * the same recurrence with the frames scanned from F-1 down to 0,
+ *     S_f = alpha_f * S_{f+1} * (I - K_f^T B_f K_f) + V_f^T B_f K_f,  S_F = state_in
+ *     O_f = Q_f * S_f^T
+ * so state_out holds the state after frame 0.  Same arguments, layouts,
+ * validation and results as gdn_frame_forward applied to the frame-reversed
+ * sequence; how the two directions of a bidirectional layer are combined is
+ * left to the caller.
+ */
+gdn_status gdn_frame_forward_reverse(const void* q, const void* k, const void* v,
+                                     const float* alpha, const float* beta,
+                                     const float* state_in, void* out, float* state_out,
+                                     int B, int H, int F, int N, int dk, int dv,
+                                     gdn_stream_t stream);
+
+/*
  * One-frame step for interactive rollout (WorldFoundry model card, "What it
  * is for": a resident pipeline that advances in native 8k+1 windows): the same
  * operation with F = 1 on a resident state.

@@ -92,3 +92,26 @@ def test_schedules_agree_exactly():
         res[fused] = gpu_forward(x)
     api.set_fused_scan(True)
     assert torch.equal(res[True][0], res[False][0]) and torch.equal(res[True][1], res[False][1])
+
+
+@pytest.mark.parametrize("name", ["tiny", "window9", "seq60s"])
+def test_reverse_direction(name, schedule):
+    """Reverse scan (bidirectional stage): frames F-1 .. 0, against the oracle's reverse mode."""
+    import oracle
+    w = inputs.WORKLOADS[name]
+    x = inputs.workload_inputs(w)
+    full = w.F * w.N <= 10000
+    toks = None if full else sample_tokens(w.B, w.F, w.N)
+    ref = oracle_run(x, w.B, w.H, w.F, w.N, w.dk, w.dv, mode=oracle.MODE_REVERSE, want_out=full,
+                     sample_tokens=toks)
+    xd = to_dev(x)
+    out, st = api.frame_forward(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], xd["state_in"], reverse=True)
+    api.sync_status()
+    if full:
+        eo = rel_err(out.float().cpu().numpy(), ref["out"])
+    else:
+        flat = out.view(-1, w.H, w.dv)[torch.as_tensor(toks, device=out.device)].float().cpu().numpy()
+        eo = rel_err(flat, ref["sample_out"])
+    es = rel_err(st.cpu().numpy(), ref["state"])
+    print(f"{name} reverse [{schedule}]: err_O={eo:.3e} err_S={es:.3e}")
+    assert eo <= TOL_OUT and es <= TOL_STATE
