@@ -333,6 +333,23 @@ def main():
     rev_ms = r0.elapsed_time(r1) / nr
     reverse_info = {"ms_per_step": rev_ms, "tokens_per_s": tokens / (rev_ms / 1e3), "steps": nr}
 
+    # ------------------------------- folded prologue (raw q, k and gate logits)
+    xr = {k: v.to(device) for k, v in inputs.draw_raw(w.B, w.H, w.F, w.N, w.dk, w.dv, seed=0).items()}
+    api.frame_forward_gated(xr["q"], xr["k"], xr["v"], xr["a_logit"], xr["b_logit"], 0.05, None,
+                            out=out, state_out=st)
+    torch.cuda.synchronize(device)
+    r0.record(stream)
+    for _ in range(nr):
+        api.frame_forward_gated(xr["q"], xr["k"], xr["v"], xr["a_logit"], xr["b_logit"], 0.05, None,
+                                out=out, state_out=st)
+    r1.record(stream)
+    torch.cuda.synchronize(device)
+    api.sync_status()
+    gated_ms = r0.elapsed_time(r1) / nr
+    gated_info = {"ms_per_step": gated_ms, "tokens_per_s": tokens / (gated_ms / 1e3), "steps": nr,
+                  "what": "raw q, k L2-normalized and sigmoid/softplus gates applied inside the kernels"}
+    del xr
+
     # ------------------------------------------- interactive step (one frame)
     # the streaming rollout: F sequential gdn_frame_step calls on a resident state
     step_state = torch.zeros((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=device)
@@ -406,6 +423,7 @@ def main():
                     "steps": args.e2e_steps},
             "step": step_info,
             "reverse_direction": reverse_info,
+            "gated_prologue": gated_info,
             "cpu_baseline": cpu,
             "clocks": clocks,
             "gpu_launches": (3 if sched <= 0 else 2) * args.steps,

@@ -19,7 +19,7 @@ STATUS = {
 }
 EXPORTS = (
     "gdn_frame_forward", "gdn_frame_forward_reverse", "gdn_frame_step", "gdn_frame_forward_timed",
-    "gdn_frame_forward_host",
+    "gdn_frame_forward_host", "gdn_frame_forward_gated", "gdn_frame_step_gated",
     "gdn_workspace_bytes", "gdn_step_workspace_bytes",
     "gdn_status_string", "gdn_sync_status", "gdn_set_wait_limit_ns", "gdn_selftest_wait_timeout",
     "gdn_version", "gdn_frame_step_noalloc", "gdn_set_fused_scan", "gdn_scan_schedule",
@@ -50,6 +50,11 @@ def load(path: str | None = None):
     lib.gdn_frame_forward.restype = ctypes.c_int
     lib.gdn_frame_forward_reverse.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, st]
     lib.gdn_frame_forward_reverse.restype = ctypes.c_int
+    fl = ctypes.c_float
+    lib.gdn_frame_forward_gated.argtypes = [vp, vp, vp, fp, fp, fl, fp, vp, fp, i, i, i, i, i, i, st]
+    lib.gdn_frame_forward_gated.restype = ctypes.c_int
+    lib.gdn_frame_step_gated.argtypes = [vp, vp, vp, fp, fp, fl, fp, vp, fp, i, i, i, i, i, st]
+    lib.gdn_frame_step_gated.restype = ctypes.c_int
     lib.gdn_frame_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, st]
     lib.gdn_frame_step.restype = ctypes.c_int
     lib.gdn_frame_forward_timed.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, st,

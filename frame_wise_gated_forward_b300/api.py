@@ -63,6 +63,59 @@ def frame_forward(q, k, v, alpha, beta, state_in=None, *, out=None, state_out=No
     return out, state_out
 
 
+def frame_forward_gated(q, k, v, a_logit, b_logit, alpha_scale, state_in=None, *, out=None, state_out=None,
+                        stream=None):
+    """Forward on raw q/k and gate logits: q and k are L2-normalized per (token,
+    head), beta = sigmoid(b_logit), alpha = exp(-softplus(a_logit) * alpha_scale),
+    all inside the kernels.  Shapes as frame_forward."""
+    lib = load()
+    B, F, N, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, F, N, H, dv), dtype=torch.bfloat16, device=q.device)
+    if state_out is None:
+        state_out = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
+    args = [
+        _dev(q, "q", torch.bfloat16, (B, F, N, H, dk)),
+        _dev(k, "k", torch.bfloat16, (B, F, N, H, dk)),
+        _dev(v, "v", torch.bfloat16, (B, F, N, H, dv)),
+        _dev(a_logit, "a_logit", torch.float32, (B, F, H)),
+        _dev(b_logit, "b_logit", torch.float32, (B, F, N, H)),
+    ]
+    rest = [None if state_in is None else _dev(state_in, "state_in", torch.float32, (B, H, dv, dk)),
+            _dev(out, "out", torch.bfloat16, (B, F, N, H, dv)),
+            _dev(state_out, "state_out", torch.float32, (B, H, dv, dk))]
+    check(lib.gdn_frame_forward_gated(*args, float(alpha_scale), *rest, B, H, F, N, dk, dv, _stream_handle(stream)),
+          "gdn_frame_forward_gated")
+    return out, state_out
+
+
+def frame_step_gated(q, k, v, a_logit, b_logit, alpha_scale, state_in=None, *, out=None, state_out=None,
+                     stream=None):
+    """One frame on a resident state with the folded prologue (see frame_forward_gated).
+    q, k [B,N,H,dk]; v [B,N,H,dv]; a_logit [B,H]; b_logit [B,N,H]."""
+    lib = load()
+    B, N, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=q.device)
+    if state_out is None:
+        state_out = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
+    args = [
+        _dev(q, "q", torch.bfloat16, (B, N, H, dk)),
+        _dev(k, "k", torch.bfloat16, (B, N, H, dk)),
+        _dev(v, "v", torch.bfloat16, (B, N, H, dv)),
+        _dev(a_logit, "a_logit", torch.float32, (B, H)),
+        _dev(b_logit, "b_logit", torch.float32, (B, N, H)),
+    ]
+    rest = [None if state_in is None else _dev(state_in, "state_in", torch.float32, (B, H, dv, dk)),
+            _dev(out, "out", torch.bfloat16, (B, N, H, dv)),
+            _dev(state_out, "state_out", torch.float32, (B, H, dv, dk))]
+    check(lib.gdn_frame_step_gated(*args, float(alpha_scale), *rest, B, H, N, dk, dv, _stream_handle(stream)),
+          "gdn_frame_step_gated")
+    return out, state_out
+
+
 def frame_step(q, k, v, alpha, beta, state_in=None, *, out=None, state_out=None, stream=None):
     """One latent frame on a resident state.  q, k [B,N,H,dk]; v [B,N,H,dv];
     alpha [B,H]; beta [B,N,H].  state_out may be the same tensor as state_in."""
@@ -184,6 +237,6 @@ def selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     return int(lib.gdn_sync_status(_stream_handle(stream)))
 
 
-__all__ = ["frame_forward", "frame_step", "frame_forward_timed", "frame_forward_host", "workspace_bytes",
+__all__ = ["frame_forward", "frame_forward_gated", "frame_step_gated", "frame_step", "frame_forward_timed", "frame_forward_host", "workspace_bytes",
            "step_workspace_bytes", "sync_status", "set_fused_scan", "scan_schedule", "set_wait_limit_ns", "selftest_wait_timeout",
            "GDNError"]

@@ -247,6 +247,8 @@ struct PassArgs {
     float* state_out;
     int B, H, F, N, dk, dv;
     int reverse = 0;
+    int prologue = 0;          // raw q, k and gate logits: normalize and apply the gates in the kernels
+    float alpha_scale = 0.0f;  // prologue: alpha = exp(-softplus(a) * alpha_scale)
 };
 
 // Rows of S per scan CTA.  Standalone scan: the smallest slice that keeps
@@ -307,6 +309,8 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, int ns
     p1.nsplit = nsplit;
     p1.chunks = (a.N + gdn::k1::CHUNK - 1) / gdn::k1::CHUNK;
     p1.work = static_cast<int>(items * nsplit);
+    p1.norm_k = a.prologue;
+    p1.beta_sigmoid = a.prologue;
     p1.wait_limit_ns = lim;
     if (ev) cudaEventRecord(ev[0], stream);
     gdn::k1::contract_kernel<<<std::min(p1.work, ds->sms), gdn::k1::THREADS, gdn::k1::SMEM_BYTES, stream>>>(
@@ -329,6 +333,8 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, int ns
     p2.dv = a.dv;
     p2.rsplit = a.dv / R;
     p2.reverse = a.reverse;
+    p2.alpha_gate = a.prologue;
+    p2.alpha_scale = a.alpha_scale;
     p2.wait_limit_ns = lim;
     gdn::k3::Params p3;
     p3.B = a.B;
@@ -340,6 +346,7 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, int ns
     p3.ntile = (a.N + gdn::k3::TILE_M - 1) / gdn::k3::TILE_M;
     p3.total = items * p3.ntile;
     p3.reverse = a.reverse;
+    p3.norm_q = a.prologue;
     p3.wait_limit_ns = lim;
     const int n_scan = a.B * a.H * p2.rsplit;
     if (Rf != 0) {
@@ -445,6 +452,29 @@ gdn_status gdn_frame_forward_reverse(const void* q, const void* k, const void* v
     PassArgs a{q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv};
     a.reverse = 1;
     return run_pass(a, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_frame_forward_gated(const void* q, const void* k, const void* v, const float* a_logit,
+                                   const float* b_logit, float alpha_scale, const float* state_in, void* out,
+                                   float* state_out, int B, int H, int F, int N, int dk, int dv,
+                                   gdn_stream_t stream) {
+    gdn_status s = validate(q, k, v, a_logit, b_logit, state_in, out, state_out, B, H, F, N, dk, dv);
+    if (s != GDN_OK) return s;
+    PassArgs a{q, k, v, a_logit, b_logit, state_in, out, state_out, B, H, F, N, dk, dv};
+    a.prologue = 1;
+    a.alpha_scale = alpha_scale;
+    return run_pass(a, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_frame_step_gated(const void* q, const void* k, const void* v, const float* a_logit,
+                                const float* b_logit, float alpha_scale, const float* state_in, void* out,
+                                float* state_out, int B, int H, int N, int dk, int dv, gdn_stream_t stream) {
+    gdn_status s = validate(q, k, v, a_logit, b_logit, state_in, out, state_out, B, H, 1, N, dk, dv);
+    if (s != GDN_OK) return s;
+    PassArgs a{q, k, v, a_logit, b_logit, state_in, out, state_out, B, H, 1, N, dk, dv};
+    a.prologue = 1;
+    a.alpha_scale = alpha_scale;
+    return run_pass(a, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gdn_status gdn_frame_forward_timed(const void* q, const void* k, const void* v, const float* alpha,

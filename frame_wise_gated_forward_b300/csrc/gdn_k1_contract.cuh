@@ -18,7 +18,7 @@
 // beta is applied in fp32 to a copy of the K tile (rounded to bf16 once).
 //
 // Warp roles (320 threads): warp 0 TMA producer; warp 1 TMEM owner and MMA
-// issuer; warps 2-5 beta scalers (one 64-column half row per thread); warps
+// issuer; warps 2-5 beta scalers (two adjacent lanes per token row); warps
 // 6-9 epilogue (TMEM lane quarter = warp % 4).  The K/V tiles stream through a
 // 5-deep TMA ring; the scaled copy of K has its own 3-deep ring, so a K/V slot
 // is released as soon as its MMAs retire.  beta reaches the scalers through a
@@ -32,22 +32,11 @@
 namespace gdn {
 namespace k1 {
 
-#ifndef GDN_K1_INPLACE
-#define GDN_K1_INPLACE 0
-#endif
-#if GDN_K1_INPLACE
-// K and V are scaled in place by sqrt(beta): A = K'^T K', U^T = K'^T V'
-#ifndef GDN_K1_STAGES
-#define GDN_K1_STAGES 7
-#endif
-#define GDN_K1_BK_BUFS 0
-#else
 #ifndef GDN_K1_STAGES
 #define GDN_K1_STAGES 5
 #endif
 #ifndef GDN_K1_BK_BUFS
 #define GDN_K1_BK_BUFS 3
-#endif
 #endif
 #ifndef GDN_K1_ROUND_ROBIN
 #define GDN_K1_ROUND_ROBIN 1
@@ -71,16 +60,13 @@ constexpr int SCALER_WARPS = GDN_K1_SCALER_WARPS;
 constexpr int SCALER_THREADS = SCALER_WARPS * 32;
 constexpr int EPI_WARP0 = 2 + SCALER_WARPS;  // four epilogue warps follow the scalers
 constexpr int THREADS = (EPI_WARP0 + 4) * 32;
-// each scaler thread owns one token row and CH16 of its sixteen 16-byte chunks
-constexpr int TPR = SCALER_THREADS / CHUNK;   // scaler threads per token row
-constexpr int CH16 = 16 / TPR;
-static_assert(SCALER_THREADS % CHUNK == 0 && CH16 >= 1 && 16 % TPR == 0, "scaler split");
+// a pair of adjacent scaler lanes owns one token row (one 64-column box each)
+static_assert(SCALER_THREADS == 2 * CHUNK, "two scaler threads per token row");
 // beta is copied global -> shared by each scaler thread BETA_AHEAD chunks before
 // its use, into a per-thread ring of BETA_AHEAD + 1 slots
-constexpr int BETA_AHEAD = GDN_K1_INPLACE ? 2 : 4;
+constexpr int BETA_AHEAD = 4;
 constexpr int BETA_RING_BYTES = (BETA_AHEAD + 1) * SCALER_THREADS * 4;
 static_assert(1024 + STAGES * STAGE_BYTES + BK_BUFS * TILE_BYTES + BETA_RING_BYTES + 256 <= 232448, "shared memory");
-static_assert(!GDN_K1_INPLACE || SCALER_THREADS == 128, "in-place scaling: one (row, tile) per scaler thread");
 constexpr int TMEM_COLS = 512;
 constexpr int ACC_COLS = 256;
 // MN-major operand with 128-byte swizzle: 64 MN-elements per 128-byte row,
@@ -102,8 +88,31 @@ struct Params {
     int nsplit;            // token splits per item
     int chunks;            // ceil(N / CHUNK)
     int work;              // items * nsplit
+    int norm_k;            // fused prologue: k <- k / max(|k|, 1e-12) per (token, head)
+    int beta_sigmoid;      // fused prologue: beta <- sigmoid(beta)
     unsigned long long wait_limit_ns;
 };
+
+// x * s on packed bf16 pairs with s = hi + lo split into two bf16: fma(x, hi, x*lo)
+// rounds the product essentially once, like an fp32 product rounded to bf16
+struct BSplit {
+    __nv_bfloat162 hi, lo;
+};
+__device__ __forceinline__ BSplit bsplit(float s) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(s);
+    const __nv_bfloat16 l = __float2bfloat16_rn(s - __bfloat162float(h));
+    return BSplit{__halves2bfloat162(h, h), __halves2bfloat162(l, l)};
+}
+__device__ __forceinline__ uint4 bscale(uint4 x, const BSplit& s) {
+    uint32_t* xs = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 k2 = *reinterpret_cast<const __nv_bfloat162*>(&xs[e]);
+        const __nv_bfloat162 r2 = __hfma2(k2, s.hi, __hmul2(k2, s.lo));
+        xs[e] = *reinterpret_cast<const uint32_t*>(&r2);
+    }
+    return x;
+}
 
 struct Unit {
     int item, split, c_begin, c_end;
@@ -130,8 +139,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t* empty = full + STAGES;                // [STAGES]  MMA finished reading the stage
     uint64_t* bk_full = empty + STAGES;             // [BK_BUFS] beta*K written
     uint64_t* bk_empty = bk_full + BK_BUFS;         // [BK_BUFS] MMA finished reading beta*K
-    uint64_t* scaled = bk_empty + BK_BUFS;          // [STAGES]  (in place) stage scaled by sqrt(beta)
-    uint64_t* tfull = scaled + (GDN_K1_INPLACE ? STAGES : 0);  // [2] accumulator ready
+    uint64_t* tfull = bk_empty + BK_BUFS;           // [2]       accumulator ready
     uint64_t* tempty = tfull + 2;                   // [2]       accumulator drained
     uint64_t* final_bar = tempty + 2;               // [1]       every issued MMA retired
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
@@ -166,8 +174,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&bk_full[b], SCALER_THREADS);
             mbar_init(&bk_empty[b], 1);
         }
-        if (GDN_K1_INPLACE)
-            for (int st = 0; st < STAGES; ++st) mbar_init(&scaled[st], SCALER_THREADS);
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], 128);
@@ -248,15 +254,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
                 bool ok = true;
                 for (int c = u.c_begin; c < u.c_end; ++c) {
-#if GDN_K1_INPLACE
-                    if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag) ||
-                        !mbar_wait(&scaled[stage], phase, p.wait_limit_ns, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_base = smem_u32(stage_base + stage * STAGE_BYTES);  // sqrt(beta) K
-#else
                     if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag) ||
                         !mbar_wait(&bk_full[bk], bk_phase, p.wait_limit_ns, abort_flag)) {
                         ok = false;
@@ -264,7 +261,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t a_base = smem_u32(bk_base + bk * TILE_BYTES);       // beta*K
-#endif
                     const uint32_t b_base = smem_u32(stage_base + stage * STAGE_BYTES); // [K | V]
 #pragma unroll
                     for (int kk = 0; kk < CHUNK / 16; ++kk) {
@@ -273,10 +269,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         mma_bf16(d_tmem, ad, bd, IDESC, (c > u.c_begin || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(&empty[stage]);
-#if !GDN_K1_INPLACE
                     mma_commit(&bk_empty[bk]);
                     if (++bk == BK_BUFS) { bk = 0; bk_phase ^= 1; }
-#endif
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
@@ -289,8 +283,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp < EPI_WARP0) {
         // ------------------------------------------------------ beta scalers
         const int t = threadIdx.x - 64;     // 0..SCALER_THREADS-1
-        const int r = t % CHUNK;            // token row within the stage
-        const int c16 = (t / CHUNK) * CH16; // first 16-byte chunk of the row this thread scales
+        const int r = t >> 1;               // token row within the stage
+        const int bx = t & 1;               // which 64-column box of the row
         // beta is copied to shared memory BETA_AHEAD chunks ahead of its use (a
         // cursor walks the same unit/chunk sequence), so its global-load
         // latency never sits between a landed K tile and its MMA.  Each thread
@@ -327,84 +321,60 @@ __global__ void __launch_bounds__(THREADS, 1)
                 cp_async_wait<BETA_AHEAD>();           // this chunk's copy has landed
                 const float bval = beta_ring[cslot * SCALER_THREADS + t];
                 if (++cslot == BETA_AHEAD + 1) cslot = 0;
-#if GDN_K1_INPLACE
-                if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                {
-                    // thread (row r, tile t>>6): scale row r of the K (0) or V (1) tile in place
-                    const int tile = t >> 6;
-                    const int nbx = tile == 0 ? kboxes : vboxes;
-                    const float sb = sqrtf(fmaxf(bval, 0.0f));
-                    uint8_t* row = stage_base + stage * STAGE_BYTES + tile * TILE_BYTES + r * 128;
-                    uint4 x[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int bx = i >> 3;
-                        if (bx < nbx) x[i] = *reinterpret_cast<const uint4*>(row + bx * BOX_BYTES + ((((i & 7) + r) & 7) << 4));
-                    }
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int bx = i >> 3;
-                        if (bx >= nbx) continue;
-                        uint32_t* xs = reinterpret_cast<uint32_t*>(&x[i]);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            __nv_bfloat162 pr = *reinterpret_cast<__nv_bfloat162*>(&xs[e]);
-                            float2 f2 = __bfloat1622float2(pr);
-                            xs[e] = pack_bf16x2(f2.x * sb, f2.y * sb);
-                        }
-                        *reinterpret_cast<uint4*>(row + bx * BOX_BYTES + ((((i & 7) + r) & 7) << 4)) = x[i];
-                    }
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&scaled[stage]);
-#else
                 if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag) ||
                     !mbar_wait(&bk_empty[bk], bk_phase ^ 1, p.wait_limit_ns, abort_flag)) {
                     ok = false;
                     break;
                 }
                 {
-                    // all loads first, then convert and store: the loads are independent of the
-                    // stores, and issuing them together keeps eight shared-memory reads in flight
-                    const uint8_t* src = stage_base + stage * STAGE_BYTES + r * 128;
-                    uint8_t* dst = bk_base + bk * TILE_BYTES + r * 128;
-                    uint4 x[CH16];
-                    int off[CH16];
+                    // thread pair (2r, 2r+1) owns token row r: box 0 and box 1 (64 columns each)
+                    uint8_t* src = stage_base + stage * STAGE_BYTES + bx * BOX_BYTES + r * 128;
+                    uint8_t* dst = bk_base + bk * TILE_BYTES + bx * BOX_BYTES + r * 128;
+                    const bool mine = bx < kboxes;
+                    uint4 x[8];
 #pragma unroll
-                    for (int i = 0; i < CH16; ++i) {
-                        // global chunk g = box*8 + c8; rotate within the box so 8 consecutive
-                        // rows hit 8 distinct bank groups
-                        const int g = c16 + i;
-                        off[i] = (g >> 3) * BOX_BYTES + ((((g & 7) + r) & 7) << 4);
-                        if ((g >> 3) < kboxes) x[i] = *reinterpret_cast<const uint4*>(src + off[i]);
+                    for (int i = 0; i < 8; ++i) {
+                        // rotate the 16-byte chunk order so 8 consecutive rows hit 8 distinct bank groups
+                        const int off = ((i + r) & 7) << 4;
+                        if (mine) x[i] = *reinterpret_cast<const uint4*>(src + off);
+                        else x[i] = make_uint4(0, 0, 0, 0);
                     }
-                    // beta = hi + lo with hi, lo in bf16; beta*k = fma(k, hi, k*lo) on packed
-                    // bf16 pairs: the small k*lo term carries the rest of beta, so the
-                    // product is rounded to bf16 essentially once, as an fp32 product would be
-                    const __nv_bfloat16 bhi = __float2bfloat16_rn(bval);
-                    const __nv_bfloat16 blo = __float2bfloat16_rn(bval - __bfloat162float(bhi));
-                    const __nv_bfloat162 hi2 = __halves2bfloat162(bhi, bhi);
-                    const __nv_bfloat162 lo2 = __halves2bfloat162(blo, blo);
+                    float sb = p.beta_sigmoid ? 1.0f / (1.0f + expf(-bval)) : bval;
+                    if (p.norm_k) {
+                        // k <- k / max(|k|, eps): the row's sum of squares over both halves
+                        float ss = 0.0f;
 #pragma unroll
-                    for (int i = 0; i < CH16; ++i) {
-                        if (((c16 + i) >> 3) >= kboxes) continue;
-                        uint32_t* xs = reinterpret_cast<uint32_t*>(&x[i]);
+                        for (int i = 0; i < 8; ++i) {
+                            const uint32_t* xs = reinterpret_cast<const uint32_t*>(&x[i]);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const __nv_bfloat162 kk2 = *reinterpret_cast<__nv_bfloat162*>(&xs[e]);
-                            const __nv_bfloat162 r2 = __hfma2(kk2, hi2, __hmul2(kk2, lo2));
-                            xs[e] = *reinterpret_cast<const uint32_t*>(&r2);
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[e]));
+                                ss = fmaf(f2.x, f2.x, fmaf(f2.y, f2.y, ss));
+                            }
                         }
-                        *reinterpret_cast<uint4*>(dst + off[i]) = x[i];
+                        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                        const float inv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+                        sb *= inv;
+                        if (mine) {
+                            const BSplit n2 = bsplit(inv);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const uint4 y = bscale(x[i], n2);   // normalized k, the B operand
+                                *reinterpret_cast<uint4*>(src + (((i + r) & 7) << 4)) = y;
+                            }
+                        }
+                    }
+                    if (mine) {
+                        // beta*k = fma(k, hi, k*lo) with beta = hi + lo split into two bf16
+                        const BSplit b2 = bsplit(sb);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            *reinterpret_cast<uint4*>(dst + (((i + r) & 7) << 4)) = bscale(x[i], b2);
                     }
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&bk_full[bk]);
                 if (++bk == BK_BUFS) { bk = 0; bk_phase ^= 1; }
-#endif
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
             if (!ok) break;

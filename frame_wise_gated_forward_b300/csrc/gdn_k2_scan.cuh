@@ -63,8 +63,16 @@ struct Params {
     int H, F, dk, dv;
     int rsplit;             // dv / R CTAs per head
     int reverse;            // nonzero: scan the frames from F-1 down to 0
+    int alpha_gate;         // fused prologue: alpha <- exp(-softplus(alpha) * alpha_scale)
+    float alpha_scale;
     unsigned long long wait_limit_ns;
 };
+
+__device__ __forceinline__ float decay_gate(const Params& p, float x) {
+    if (!p.alpha_gate) return x;
+    const float sp = x > 20.0f ? x : log1pf(expf(x));  // softplus
+    return expf(-sp * p.alpha_scale);
+}
 
 // bf16 element (r, j) of a K-major, 128-byte-swizzled [R rows x 128 cols] tile
 template <int R>
@@ -155,7 +163,7 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_A, const CUtenso
             *reinterpret_cast<__nv_bfloat16*>(sop + sop_offset<R>(r, j)) = __float2bfloat16_rn(S[r]);
         fence_proxy_async_smem();
         mbar_arrive(&img_ready[0]);  // initial image (never stored: the publisher skips it)
-        float a_next = __ldg(p.alpha + static_cast<size_t>(b * p.F + fr(0)) * p.H + h);
+        float a_next = decay_gate(p, __ldg(p.alpha + static_cast<size_t>(b * p.F + fr(0)) * p.H + h));
 
         constexpr uint32_t IDESC = idesc_bf16(128, R, 0, 0);
         int f = 0;
@@ -184,7 +192,7 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_A, const CUtenso
                 }
             }
             const float a_f = a_next;
-            if (f + 1 < p.F) a_next = __ldg(p.alpha + static_cast<size_t>(b * p.F + fr(f + 1)) * p.H + h);
+            if (f + 1 < p.F) a_next = decay_gate(p, __ldg(p.alpha + static_cast<size_t>(b * p.F + fr(f + 1)) * p.H + h));
 
             // the buffer this frame's image goes to was last stored NI frames ago
             bool ok = f < NI || mbar_wait(&img_free[nxt], static_cast<uint32_t>(((f / NI) - 1) & 1),

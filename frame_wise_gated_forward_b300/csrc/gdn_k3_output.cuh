@@ -15,8 +15,11 @@
 // rounds to bf16 (RNE), writes a swizzled staging tile and stores it with its
 // own TMA store (rows past N are clipped by the tensor map).
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
-// issuer, warps 2-5 epilogue (TMEM lane quarter = warp % 4).
+// Warp roles (256 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
+// issuer, warps 2-5 epilogue (TMEM lane quarter = warp % 4), warps 6-7 row
+// norms of q for the folded prologue (idle otherwise): they read each q tile
+// from shared memory as soon as it lands, hand 1/max(|q_n|, eps) per row to
+// the epilogue and co-sign the release of the ring slot.
 //
 // The role runs in two schedules:
 //  - standalone (output_kernel): a persistent grid, each CTA a contiguous
@@ -32,7 +35,8 @@
 namespace gdn {
 namespace k3 {
 
-constexpr int THREADS = 192;
+constexpr int THREADS = 256;
+constexpr int NORM_THREADS = 64;
 constexpr int TILE_M = 128;                  // tokens per tile
 constexpr int QSTAGES = 3;
 constexpr int SSTAGES = 2;
@@ -43,14 +47,18 @@ constexpr int STILE_BYTES = 2 * BOX_BYTES;   // S_f: 128 rows (dv) x dk
 constexpr int OBOX_BYTES = 32 * 128;         // one warp's 32 rows x 64 columns
 constexpr int OSTAGE_BYTES = 2 * OBOX_BYTES; // 32 rows x 128 columns
 constexpr int TMEM_COLS = 512;
+constexpr int NSLOTS = 2;                    // row-norm buffers (folded prologue)
+constexpr int BAR_BYTES = 256;
 constexpr size_t SMEM_BYTES =
-    1024 + QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES + 4 * 2 * OSTAGE_BYTES + 256;
+    1024 + QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES + 4 * 2 * OSTAGE_BYTES + BAR_BYTES + NSLOTS * TILE_M * 4;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct Params {
     int B, H, F, N, dk, dv;
     int ntile;              // ceil(N / 128) tiles per item
     long long total;        // items * ntile
     int reverse;            // fused schedule: follow a scan that runs from frame F-1 down
+    int norm_q;             // fused prologue: scale each output row by 1/max(|q_n|, eps)
     unsigned long long wait_limit_ns;
 };
 
@@ -126,8 +134,12 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
     uint64_t* tfull = sempty + SSTAGES;
     uint64_t* tempty = tfull + ACCS;
     uint64_t* final_bar = tempty + ACCS;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
+    uint64_t* nready = final_bar + 1;                 // [NSLOTS] row norms of a tile written
+    uint64_t* nfree = nready + NSLOTS;                // [NSLOTS] epilogue has read them
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(nfree + NSLOTS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* rnorm = reinterpret_cast<float*>(smem + QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES +
+                                            4 * 2 * OSTAGE_BYTES + BAR_BYTES);   // [NSLOTS][TILE_M]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -139,9 +151,20 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
         for (int i = threadIdx.x; i < (QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES) / 16; i += THREADS)
             reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < QSTAGES; ++s) { mbar_init(&qfull[s], 1); mbar_init(&qempty[s], 1); }
+        // a q slot is released by the MMA commit and, with the folded prologue, by the norm threads
+        for (int s = 0; s < QSTAGES; ++s) {
+            mbar_init(&qfull[s], 1);
+            mbar_init(&qempty[s], 1 + (p.norm_q ? NORM_THREADS : 0));
+        }
         for (int s = 0; s < SSTAGES; ++s) { mbar_init(&sfull[s], 1); mbar_init(&sempty[s], 1); }
-        for (int a = 0; a < ACCS; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 128); }
+        for (int a = 0; a < ACCS; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
+        for (int n = 0; n < NSLOTS; ++n) {
+            mbar_init(&nready[n], NORM_THREADS);
+            mbar_init(&nfree[n], 128);
+        }
         mbar_init(final_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -234,12 +257,58 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
             mma_commit(final_bar);
             mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
         }
+    } else if (warp >= 6) {
+        // ---------------------------------------------------------- q row norms
+        if (p.norm_q) {
+            const int t = threadIdx.x - 192;  // 0..63: rows t and t + 64 of each tile
+            int qs = 0, ns = 0;
+            uint32_t qph = 0, nph = 0;
+            long long item;
+            int nb, ne;
+            bool stop = false;
+            for (int k = 0; !stop && !*abort_flag && sc.segment(p, k, item, nb, ne); ++k) {
+                for (int nt = nb; nt < ne; ++nt) {
+                    // the tile has landed, and the epilogue has read this norm slot's last contents
+                    if (!mbar_wait(&qfull[qs], qph, p.wait_limit_ns, abort_flag) ||
+                        !mbar_wait(&nfree[ns], nph ^ 1, p.wait_limit_ns, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    const uint8_t* tile = qring + qs * QTILE_BYTES;
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int row = t + 64 * h2;
+                        float ss = 0.0f;
+                        for (int bx = 0; bx < kboxes; ++bx) {
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                // any chunk order sums the same row; rotate for distinct bank groups
+                                const uint4 v4 = *reinterpret_cast<const uint4*>(
+                                    tile + bx * BOX_BYTES + row * 128 + (((c + row) & 7) << 4));
+                                const uint32_t* vs = reinterpret_cast<const uint32_t*>(&v4);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 f2 =
+                                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vs[e]));
+                                    ss = fmaf(f2.x, f2.x, fmaf(f2.y, f2.y, ss));
+                                }
+                            }
+                        }
+                        rnorm[ns * TILE_M + row] = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+                    }
+                    mbar_arrive(&nready[ns]);
+                    mbar_arrive(&qempty[qs]);
+                    if (++qs == QSTAGES) { qs = 0; qph ^= 1; }
+                    if (++ns == NSLOTS) { ns = 0; nph ^= 1; }
+                }
+            }
+        }
     } else {
         // ----------------------------------------------------------- epilogue
         const int quarter = warp & 3;
         uint8_t* my_stage = ostage + quarter * 2 * OSTAGE_BYTES;
-        int acc = 0, ob = 0;
-        uint32_t aph = 0;
+        int acc = 0, ob = 0, ns = 0;
+        uint32_t aph = 0, nph = 0;
         const int ncol32 = (p.dv + 31) / 32;
         long long item;
         int nb, ne;
@@ -247,6 +316,16 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
         for (int k = 0; !stop && !*abort_flag && sc.segment(p, k, item, nb, ne); ++k) {
             const int frame = static_cast<int>(item / p.H), h = static_cast<int>(item % p.H);
             for (int nt = nb; nt < ne; ++nt) {
+                // fused prologue: o_n = S q_n / max(|q_n|, eps), norms from the norm warps
+                float rs = 1.0f;
+                if (p.norm_q) {
+                    const bool okn =
+                        __all_sync(0xffffffffu, mbar_wait(&nready[ns], nph, p.wait_limit_ns, abort_flag));
+                    if (!okn) { stop = true; break; }
+                    rs = rnorm[ns * TILE_M + quarter * 32 + lane];
+                    mbar_arrive(&nfree[ns]);
+                    if (++ns == NSLOTS) { ns = 0; nph ^= 1; }
+                }
                 const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, p.wait_limit_ns, abort_flag));
                 if (!ok) { stop = true; break; }
                 tc_fence_after();
@@ -260,8 +339,8 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
-                            packed[c * 16 + e] =
-                                pack_bf16x2(__uint_as_float(r32[2 * e]), __uint_as_float(r32[2 * e + 1]));
+                            packed[c * 16 + e] = pack_bf16x2(__uint_as_float(r32[2 * e]) * rs,
+                                                             __uint_as_float(r32[2 * e + 1]) * rs);
                     } else {
 #pragma unroll
                         for (int e = 0; e < 16; ++e) packed[c * 16 + e] = 0u;

@@ -110,3 +110,25 @@ def workload_inputs(w: Workload) -> dict:
 
 def has_zero_state(w: Workload) -> bool:
     return all(std == 0.0 for _, std in w.streams)
+
+
+def draw_raw(B: int, H: int, F: int, N: int, dk: int, dv: int, seed: int,
+             qk_std: float = 1.0, s0_std: float = 0.0) -> dict:
+    """Raw inputs for the folded-prologue entry points: unnormalized q, k
+    ~ N(0, qk_std^2) (bf16), v ~ N(0, 1) (bf16), decay logits a ~ N(0, 1)
+    [B, F, H] and write-strength logits b ~ N(0, 1) - ln N [B, F, N, H], so that
+    sigmoid(b) is about 1/N per token, as in the normalized workloads."""
+    import math
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = (torch.randn((B, F, N, H, dk), generator=g) * qk_std).to(torch.bfloat16)
+    k = (torch.randn((B, F, N, H, dk), generator=g) * qk_std).to(torch.bfloat16)
+    v = torch.randn((B, F, N, H, dv), generator=g).to(torch.bfloat16)
+    b = torch.randn((B, F, N, H), generator=g) - math.log(max(N, 1))
+    a = torch.randn((B, F, H), generator=g)
+    if s0_std > 0.0:
+        s0 = torch.randn((B, H, dv, dk), generator=g) * s0_std
+    else:
+        s0 = torch.zeros((B, H, dv, dk))
+    return {"q": q, "k": k, "v": v, "a_logit": a.contiguous(), "b_logit": b.contiguous(),
+            "state_in": s0.contiguous()}

@@ -102,6 +102,31 @@ gdn_status gdn_frame_forward_reverse(const void* q, const void* k, const void* v
                                      gdn_stream_t stream);
 
 /*
+ * Forward with the per-token prologue of a GDN block folded into the kernels,
+ * for callers whose projections emit raw queries, keys and gate logits:
+ *     q <- q / max(|q|, 1e-12),  k <- k / max(|k|, 1e-12)   per (token, head)
+ *     beta  = sigmoid(b_logit)                               [B, F, N, H]
+ *     alpha = exp(-softplus(a_logit) * alpha_scale)          [B, F, H]
+ * followed by exactly the gdn_frame_forward recurrence.  q and k are read
+ * once: the contraction kernel normalizes k rows as it scales them by beta,
+ * the output kernel divides each output row by |q_n|, and the scan applies the
+ * decay gate.  Same layouts, validation and ownership as gdn_frame_forward
+ * (a_logit and b_logit take the places of alpha and beta).
+ */
+gdn_status gdn_frame_forward_gated(const void* q, const void* k, const void* v,
+                                   const float* a_logit, const float* b_logit, float alpha_scale,
+                                   const float* state_in, void* out, float* state_out,
+                                   int B, int H, int F, int N, int dk, int dv,
+                                   gdn_stream_t stream);
+
+/* gdn_frame_step with the same folded prologue as gdn_frame_forward_gated. */
+gdn_status gdn_frame_step_gated(const void* q, const void* k, const void* v,
+                                const float* a_logit, const float* b_logit, float alpha_scale,
+                                const float* state_in, void* out, float* state_out,
+                                int B, int H, int N, int dk, int dv,
+                                gdn_stream_t stream);
+
+/*
  * One-frame step for interactive rollout (WorldFoundry model card, "What it
  * is for": a resident pipeline that advances in native 8k+1 windows): the same
  * operation with F = 1 on a resident state.

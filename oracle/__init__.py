@@ -63,6 +63,10 @@ def _load():
             p, p, p, p, p, p, p, p, p, p, ctypes.c_int64, p,
             i, i, i, i, i, i, i, i]
         lib.oracle_gdn_frame_forward.restype = ctypes.c_int
+        lib.oracle_gdn_frame_forward_f64.argtypes = [
+            p, p, p, p, p, p, p, p, p, p, ctypes.c_int64, p,
+            i, i, i, i, i, i, i, i]
+        lib.oracle_gdn_frame_forward_f64.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -143,6 +147,79 @@ def frame_forward(q, k, v, alpha, beta, state_in=None, *, B, H, F, N, dk, dv,
         B, H, F, N, dk, dv, int(mode), int(n_threads))
     if rc != 0:
         raise RuntimeError(f"oracle_gdn_frame_forward failed with code {rc}")
+    res = {"state": state}
+    if out is not None:
+        res["out"] = out
+    if states is not None:
+        res["states"] = states
+    if sout is not None:
+        res["sample_out"] = sout
+    return res
+
+
+def prologue(q_raw, k_raw, a_logit, b_logit, alpha_scale):
+    """The per-token prologue that gdn_frame_forward_gated folds into its
+    kernels, in fp64 by its definition:
+        q / max(|q|, 1e-12),  k / max(|k|, 1e-12)   (norm over the head dim)
+        beta  = sigmoid(b_logit) = 1 / (1 + exp(-b))
+        alpha = exp(-softplus(a_logit) * alpha_scale),  softplus(a) = log(1 + exp(a))
+    Takes bf16 torch tensors (or fp64 arrays) for q/k and fp32 logits; returns
+    fp64 numpy arrays (q, k, alpha, beta)."""
+    def f64(x):
+        try:
+            import torch
+            if isinstance(x, torch.Tensor):
+                return x.detach().cpu().to(torch.float64).numpy()
+        except ImportError:  # pragma: no cover
+            pass
+        return np.asarray(x, dtype=np.float64)
+    q, k = f64(q_raw), f64(k_raw)
+    qn = q / np.maximum(np.sqrt((q * q).sum(-1, keepdims=True)), 1e-12)
+    kn = k / np.maximum(np.sqrt((k * k).sum(-1, keepdims=True)), 1e-12)
+    b = f64(b_logit)
+    a = f64(a_logit)
+    beta = 1.0 / (1.0 + np.exp(-b))
+    softplus = np.logaddexp(0.0, a)
+    alpha = np.exp(-softplus * float(alpha_scale))
+    return qn, kn, alpha, beta
+
+
+def frame_forward_f64(q, k, v, alpha, beta, state_in=None, *, B, H, F, N, dk, dv,
+                      want_out=True, want_states=False, sample_tokens=None,
+                      mode=MODE_GDN, n_threads=0):
+    """frame_forward on fp64 inputs (any array-likes; v may be a bf16 torch tensor)."""
+    lib = _load()
+
+    def f64(x):
+        if x is None:
+            return None
+        try:
+            import torch
+            if isinstance(x, torch.Tensor):
+                return x.detach().cpu().to(torch.float64).contiguous().numpy()
+        except ImportError:  # pragma: no cover
+            pass
+        return np.ascontiguousarray(x, dtype=np.float64)
+    qa, ka, va, al, be, s0 = (f64(t) for t in (q, k, v, alpha, beta, state_in))
+    if ka.size != B * F * N * H * dk or va.size != B * F * N * H * dv or al.size != B * F * H \
+            or be.size != B * F * N * H or (qa is not None and qa.size != B * F * N * H * dk) \
+            or (s0 is not None and s0.size != B * H * dv * dk):
+        raise ValueError("input sizes do not match B,F,N,H,dk,dv")
+    state = np.empty((B, H, dv, dk), dtype=np.float64)
+    out = np.empty((B, F, N, H, dv), dtype=np.float64) if want_out else None
+    states = np.empty((B, H, F, dv, dk), dtype=np.float64) if want_states else None
+    if sample_tokens is not None:
+        st = np.ascontiguousarray(sample_tokens, dtype=np.int64)
+        sout = np.zeros((st.size, H, dv), dtype=np.float64)
+    else:
+        st, sout = None, None
+    rc = lib.oracle_gdn_frame_forward_f64(
+        _ptr(qa), _ptr(ka), _ptr(va), _ptr(al), _ptr(be), _ptr(s0),
+        _ptr(out), _ptr(state), _ptr(states),
+        _ptr(st), 0 if st is None else int(st.size), _ptr(sout),
+        B, H, F, N, dk, dv, int(mode), int(n_threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gdn_frame_forward_f64 failed with code {rc}")
     res = {"state": state}
     if out is not None:
         res["out"] = out

@@ -60,10 +60,27 @@ static double bf16_to_f64(uint16_t bits)
     return (double)c.f;
 }
 
+/* Inputs come either as bf16 bit patterns with fp32 gates and state (the
+ * values the GPU library receives) or as fp64 arrays (used to state the
+ * folded prologue exactly). */
+typedef struct {
+    const uint16_t *q16, *k16, *v16;
+    const double *q64, *k64, *v64;
+    const float *alpha32, *beta32, *s0_32;
+    const double *alpha64, *beta64, *s0_64;
+} Inputs;
+
+static double in_q(const Inputs* in, size_t i) { return in->q64 ? in->q64[i] : bf16_to_f64(in->q16[i]); }
+static double in_k(const Inputs* in, size_t i) { return in->k64 ? in->k64[i] : bf16_to_f64(in->k16[i]); }
+static double in_v(const Inputs* in, size_t i) { return in->v64 ? in->v64[i] : bf16_to_f64(in->v16[i]); }
+static double in_alpha(const Inputs* in, size_t i) { return in->alpha64 ? in->alpha64[i] : (double)in->alpha32[i]; }
+static double in_beta(const Inputs* in, size_t i) { return in->beta64 ? in->beta64[i] : (double)in->beta32[i]; }
+static int has_s0(const Inputs* in) { return in->s0_64 != NULL || in->s0_32 != NULL; }
+static double in_s0(const Inputs* in, size_t i) { return in->s0_64 ? in->s0_64[i] : (double)in->s0_32[i]; }
+
 /* One (b, h) sequence.  Work arrays are allocated per call so that (b, h)
  * pairs can run on separate threads. */
-static int run_head(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                    const float* alpha, const float* beta, const float* state_in,
+static int run_head(const Inputs* in,
                     double* out, double* state_out, double* states_all,
                     const int64_t* sample_tok, int64_t n_samples, double* sample_out,
                     int b, int h, int B, int H, int F, int N, int dk, int dv, int mode)
@@ -82,9 +99,9 @@ static int run_head(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     }
 
     /* S_0 */
-    if (state_in) {
-        const float* s0 = state_in + ((size_t)b * H + h) * dv * dk;
-        for (size_t e = 0; e < (size_t)dv * dk; ++e) S[e] = (double)s0[e];
+    if (has_s0(in)) {
+        const size_t s0 = ((size_t)b * H + h) * dv * dk;
+        for (size_t e = 0; e < (size_t)dv * dk; ++e) S[e] = in_s0(in, s0 + e);
     }
 
     for (int step = 0; step < F; ++step) {
@@ -96,11 +113,9 @@ static int run_head(const uint16_t* q, const uint16_t* k, const uint16_t* v,
         memset(U, 0, (size_t)dv * dk * sizeof(double));
         for (int n = 0; n < N; ++n) {
             const size_t tok = frame * N + n;
-            const double bn = (double)beta[tok * H + h];
-            const uint16_t* kp = k + (tok * H + h) * dk;
-            const uint16_t* vp = v + (tok * H + h) * dv;
-            for (int j = 0; j < dk; ++j) kn[j] = bf16_to_f64(kp[j]);
-            for (int i = 0; i < dv; ++i) vn[i] = bf16_to_f64(vp[i]);
+            const double bn = in_beta(in, tok * H + h);
+            for (int j = 0; j < dk; ++j) kn[j] = in_k(in, (tok * H + h) * dk + j);
+            for (int i = 0; i < dv; ++i) vn[i] = in_v(in, (tok * H + h) * dv + i);
             for (int i = 0; i < dk; ++i) {
                 const double w = bn * kn[i];
                 double* row = A + (size_t)i * dk;
@@ -114,7 +129,7 @@ static int run_head(const uint16_t* q, const uint16_t* k, const uint16_t* v,
         }
 
         /* S_f = alpha_f (S_{f-1} - S_{f-1} A_f) + U_f */
-        const double af = (double)alpha[frame * H + h];
+        const double af = in_alpha(in, frame * H + h);
         if (mode == ORACLE_MODE_NODELTA) {
             for (size_t e = 0; e < (size_t)dv * dk; ++e) S[e] = af * S[e] + U[e];
         } else {
@@ -140,8 +155,7 @@ static int run_head(const uint16_t* q, const uint16_t* k, const uint16_t* v,
         if (out) {
             for (int n = 0; n < N; ++n) {
                 const size_t tok = frame * N + n;
-                const uint16_t* qp = q + (tok * H + h) * dk;
-                for (int j = 0; j < dk; ++j) qn[j] = bf16_to_f64(qp[j]);
+                for (int j = 0; j < dk; ++j) qn[j] = in_q(in, (tok * H + h) * dk + j);
                 double* op = out + (tok * H + h) * dv;
                 for (int i = 0; i < dv; ++i) {
                     const double* srow = S + (size_t)i * dk;
@@ -155,8 +169,7 @@ static int run_head(const uint16_t* q, const uint16_t* k, const uint16_t* v,
             for (int64_t s = 0; s < n_samples; ++s) {
                 const int64_t tok = sample_tok[s];
                 if (tok / N != (int64_t)frame) continue;
-                const uint16_t* qp = q + ((size_t)tok * H + h) * dk;
-                for (int j = 0; j < dk; ++j) qn[j] = bf16_to_f64(qp[j]);
+                for (int j = 0; j < dk; ++j) qn[j] = in_q(in, ((size_t)tok * H + h) * dk + j);
                 double* op = sample_out + ((size_t)s * H + h) * dv;
                 for (int i = 0; i < dv; ++i) {
                     const double* srow = S + (size_t)i * dk;
@@ -186,15 +199,12 @@ static int run_head(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  *   n_threads   OpenMP threads over the (b, h) pairs (<= 0: library default).
  * Returns 0 on success, 1 on allocation failure, 2 on bad arguments.
  */
-int oracle_gdn_frame_forward(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                             const float* alpha, const float* beta, const float* state_in,
-                             double* out, double* state_out, double* states_all,
-                             const int64_t* sample_tok, int64_t n_samples, double* sample_out,
-                             int B, int H, int F, int N, int dk, int dv, int mode, int n_threads)
+static int forward(const Inputs* in, int need_q, double* out, double* state_out, double* states_all,
+                   const int64_t* sample_tok, int64_t n_samples, double* sample_out,
+                   int B, int H, int F, int N, int dk, int dv, int mode, int n_threads)
 {
     if (B < 1 || H < 1 || F < 0 || N < 0 || dk < 1 || dv < 1) return 2;
-    if (!alpha || !beta || !k || !v) return 2;
-    if ((out || sample_out) && !q) return 2;
+    if ((out || sample_out) && !need_q) return 2;
     if (mode < 0 || mode > 2) return 2;
     for (int64_t s = 0; s < n_samples; ++s)
         if (sample_tok[s] < 0 || sample_tok[s] >= (int64_t)B * F * N) return 2;
@@ -207,10 +217,48 @@ int oracle_gdn_frame_forward(const uint16_t* q, const uint16_t* k, const uint16_
 #endif
     for (int p = 0; p < pairs; ++p) {
         const int b = p / H, h = p % H;
-        failed |= run_head(q, k, v, alpha, beta, state_in, out, state_out, states_all,
-                           sample_tok, n_samples, sample_out, b, h, B, H, F, N, dk, dv, mode);
+        failed |= run_head(in, out, state_out, states_all, sample_tok, n_samples, sample_out,
+                           b, h, B, H, F, N, dk, dv, mode);
     }
     return failed ? 1 : 0;
+}
+
+/*
+ * Full frame-wise forward on the GPU library's input types (bf16 q/k/v,
+ * fp32 alpha/beta/state_in).
+ *   out         fp64 [B,F,N,H,dv]   every output, or NULL
+ *   state_out   fp64 [B,H,dv,dk]    final state S_F, or NULL
+ *   states_all  fp64 [B,H,F,dv,dk]  state after every frame, or NULL
+ *   sample_tok / n_samples / sample_out: outputs of selected tokens only;
+ *               sample_tok holds flat token indices (b*F + f)*N + n and
+ *               sample_out is fp64 [n_samples, H, dv].  May be NULL / 0.
+ *   n_threads   OpenMP threads over the (b, h) pairs (<= 0: library default).
+ * Returns 0 on success, 1 on allocation failure, 2 on bad arguments.
+ */
+int oracle_gdn_frame_forward(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                             const float* alpha, const float* beta, const float* state_in,
+                             double* out, double* state_out, double* states_all,
+                             const int64_t* sample_tok, int64_t n_samples, double* sample_out,
+                             int B, int H, int F, int N, int dk, int dv, int mode, int n_threads)
+{
+    if (!alpha || !beta || !k || !v) return 2;
+    Inputs in = {q, k, v, NULL, NULL, NULL, alpha, beta, state_in, NULL, NULL, NULL};
+    return forward(&in, q != NULL, out, state_out, states_all, sample_tok, n_samples, sample_out,
+                   B, H, F, N, dk, dv, mode, n_threads);
+}
+
+/* The same forward on fp64 inputs of the same layouts (q, k, v, alpha, beta,
+ * state_in all fp64; state_in may be NULL). */
+int oracle_gdn_frame_forward_f64(const double* q, const double* k, const double* v,
+                                 const double* alpha, const double* beta, const double* state_in,
+                                 double* out, double* state_out, double* states_all,
+                                 const int64_t* sample_tok, int64_t n_samples, double* sample_out,
+                                 int B, int H, int F, int N, int dk, int dv, int mode, int n_threads)
+{
+    if (!alpha || !beta || !k || !v) return 2;
+    Inputs in = {NULL, NULL, NULL, q, k, v, NULL, NULL, NULL, alpha, beta, state_in};
+    return forward(&in, q != NULL, out, state_out, states_all, sample_tok, n_samples, sample_out,
+                   B, H, F, N, dk, dv, mode, n_threads);
 }
 
 int oracle_max_threads(void)

@@ -311,3 +311,39 @@ def test_oracle_rejects_bad_arguments():
         oracle.frame_forward(x["q"], x["k"], x["v"], x["alpha"], x["beta"], None,
                              B=w.B, H=w.H, F=w.F, N=w.N, dk=w.dk, dv=w.dv,
                              want_out=False, sample_tokens=np.array([10 ** 9]))
+
+
+# ------------------------------------------------ folded prologue (gated entry)
+def test_prologue_definition_pins():
+    g = torch.Generator().manual_seed(31)
+    q = (torch.randn((1, 3, 5, 2, 16), generator=g) * 3).to(torch.bfloat16)
+    k = (torch.randn((1, 3, 5, 2, 16), generator=g) * 0.2).to(torch.bfloat16)
+    a = torch.tensor([[[-30.0, 0.0], [1.0, 40.0], [-1.0, 2.0]]])
+    b = torch.tensor([0.0, 2.0, -2.0, 50.0, -50.0]).repeat(1, 3, 2, 1).permute(0, 1, 3, 2).contiguous()
+    qn, kn, alpha, beta = oracle.prologue(q, k, a, b, 0.05)
+    np.testing.assert_allclose(np.linalg.norm(qn, axis=-1), 1.0, atol=1e-14)
+    np.testing.assert_allclose(np.linalg.norm(kn, axis=-1), 1.0, atol=1e-14)
+    # sigmoid fixed points: sigma(0) = 1/2, sigma(2) + sigma(-2) = 1, tails
+    assert beta[0, 0, 0, 0] == 0.5
+    np.testing.assert_allclose(beta[0, 0, 1, 0] + beta[0, 0, 2, 0], 1.0, atol=1e-15)
+    np.testing.assert_allclose(beta[0, 0, 1, 0], 1 / (1 + np.exp(-2.0)), rtol=1e-15)
+    assert beta[0, 0, 3, 0] == 1.0 and 0 < beta[0, 0, 4, 0] < 1e-21   # sigma(50) rounds to 1 in fp64
+    # softplus(0) = ln 2; softplus(x) ~ x for large x, ~ exp(x) for very negative x
+    np.testing.assert_allclose(alpha[0, 0, 1], np.exp(-np.log(2.0) * 0.05), rtol=1e-15)
+    np.testing.assert_allclose(alpha[0, 1, 1], np.exp(-40.0 * 0.05), rtol=1e-12)
+    np.testing.assert_allclose(alpha[0, 0, 0], np.exp(-np.exp(-30.0) * 0.05), rtol=1e-15)
+    # positive rescaling of raw q, k does not change the normalized values
+    qn2, kn2, _, _ = oracle.prologue((q.float() * 4).to(torch.bfloat16), (k.float() * 0.5).to(torch.bfloat16),
+                                     a, b, 0.05)
+    np.testing.assert_allclose(qn2, qn, atol=1e-15)
+    np.testing.assert_allclose(kn2, kn, atol=1e-15)
+
+
+def test_f64_entry_equals_bf16_entry():
+    B, H, F, N, dk, dv = 2, 2, 4, 6, 8, 8
+    q, k, v, alpha, beta, s0 = rand_inputs(B, H, F, N, dk, dv, seed=41)
+    r16 = run(q, k, v, alpha, beta, s0)
+    r64 = oracle.frame_forward_f64(f64(q), f64(k), f64(v), alpha.double().numpy(), beta.double().numpy(),
+                                   s0.double().numpy(), B=B, H=H, F=F, N=N, dk=dk, dv=dv)
+    np.testing.assert_array_equal(r64["out"], r16["out"])
+    np.testing.assert_array_equal(r64["state"], r16["state"])
