@@ -27,7 +27,8 @@ struct DeviceState {
     bool probed = false;
     bool ok = false;
     int sms = 0;
-    bool coop = false;  // cooperative launches possible with one fused CTA per SM
+    bool coop = false;     // cooperative launches possible with one fused CTA per SM
+    bool coop_k1 = false;  // the same for the contraction kernel (needed to split items)
     cudaMemPool_t pool = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
@@ -96,6 +97,12 @@ gdn_status device_ready(int* dev_out, DeviceState** st_out) {
             per_sm = 0;
         cudaGetLastError();
         d.coop = coop != 0 && per_sm >= 1;
+        int per_sm_k1 = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_k1, k1::contract_kernel, k1::THREADS,
+                                                          k1::SMEM_BYTES) != cudaSuccess)
+            per_sm_k1 = 0;
+        cudaGetLastError();
+        d.coop_k1 = coop != 0 && per_sm_k1 >= 1;
         d.ok = true;
     }
     if (!d.ok) return GDN_ERR_NO_DEVICE;
@@ -170,33 +177,41 @@ bool is_device_ptr(const void* p) {
 // ------------------------------------------------------------- workspace
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-struct Layout {
-    size_t a_off, u_off, s_off, f_off, p_off, total;
+// Work plan of the contraction kernel on a grid of `grid` CTAs: whole items
+// for as many full rounds as fit, the remaining items split into token ranges
+// so the last round is as long as the others (see gdn::k1::unit_of).
+struct SplitPlan {
+    int whole, rem, split_per, work;
 };
-Layout layout_of(long long items, int dk, int dv, int nsplit) {
+SplitPlan plan_split(long long items, int chunks, int grid, bool allow_split) {
+    SplitPlan sp;
+    sp.whole = static_cast<int>(items >= grid ? (items / grid) * grid : 0);
+    sp.rem = static_cast<int>(items - sp.whole);
+    sp.split_per = (sp.rem > 0 && allow_split) ? std::max(1, std::min(chunks, grid / sp.rem)) : 1;
+    if (sp.split_per == 1) {  // nothing to gain from splitting: every item whole
+        sp.whole = static_cast<int>(items);
+        sp.rem = 0;
+    }
+    sp.work = sp.whole + sp.rem * sp.split_per;
+    return sp;
+}
+
+struct Layout {
+    size_t a_off, u_off, s_off, f_off, c_off, p_off, total;
+};
+Layout layout_of(long long items, int dk, int dv, const SplitPlan& sp) {
     Layout L;
     L.a_off = 0;
     L.u_off = align256(L.a_off + static_cast<size_t>(items) * dk * dk * 2);
     L.s_off = align256(L.u_off + static_cast<size_t>(items) * dv * dk * 4);
     L.f_off = align256(L.s_off + static_cast<size_t>(items) * dv * dk * 2);   // per-item ready counts
-    L.p_off = align256(L.f_off + static_cast<size_t>(items) * 4);
-    L.total = L.p_off;
-    if (nsplit > 1) L.total = align256(L.p_off + static_cast<size_t>(nsplit) * items * (dk * dk + dv * dk) * 4);
+    L.c_off = L.f_off + static_cast<size_t>(items) * 4;                        // split-item counters
+    L.p_off = align256(L.c_off + static_cast<size_t>(items) * 4);             // split partial sums
+    L.total = align256(L.p_off + static_cast<size_t>(sp.rem) * sp.split_per * (dk * dk + dv * dk) * 4);
     return L;
 }
 
-#ifndef GDN_STEP_MAX_SPLIT
-#define GDN_STEP_MAX_SPLIT 4
-#endif
-// Token splits per head for the one-frame step: enough CTAs to stream the
-// frame, few enough that the fp32 partial sums stay small.
-int step_nsplit(int sms, int B, int H, int N) {
-    const int items = B * H;
-    const int chunks = (N + gdn::k1::CHUNK - 1) / gdn::k1::CHUNK;
-    int ns = std::max(1, sms / std::max(items, 1));
-    ns = std::min(ns, GDN_STEP_MAX_SPLIT);
-    return std::min(ns, chunks);
-}
+int chunks_of(int N) { return (N + gdn::k1::CHUNK - 1) / gdn::k1::CHUNK; }
 
 // ------------------------------------------------------------ tensor maps
 bool encode(CUtensorMap* m, void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
@@ -272,14 +287,14 @@ int scan_rows_fused(int B, int H, int dv, int sms) {
 // Launch the three phases (and the step path's partial reduction) on `stream`
 // with the workspace `ws` laid out as `L`.  Records ev[0..3] around the
 // phases when `ev` is not null.
-gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, int nsplit, const DeviceState* ds,
-                         cudaStream_t stream, cudaEvent_t const* ev) {
+gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const SplitPlan& sp,
+                         const DeviceState* ds, cudaStream_t stream, cudaEvent_t const* ev) {
     const long long items = static_cast<long long>(a.B) * a.F * a.H;
     const int BF = a.B * a.F;
     __nv_bfloat16* A_ws = reinterpret_cast<__nv_bfloat16*>(ws + L.a_off);
     float* U_ws = reinterpret_cast<float*>(ws + L.u_off);
     __nv_bfloat16* S_all = reinterpret_cast<__nv_bfloat16*>(ws + L.s_off);
-    float* partial = nsplit > 1 ? reinterpret_cast<float*>(ws + L.p_off) : nullptr;
+    float* partial = reinterpret_cast<float*>(ws + L.p_off);
     const int Rf = (g_fused_scan.load() != 0 && ds->coop) ? scan_rows_fused(a.B, a.H, a.dv, ds->sms) : 0;
     const int R = Rf != 0 ? Rf : scan_rows_standalone(a.B, a.H, a.dv, ds->sms);
     int* flags = reinterpret_cast<int*>(ws + L.f_off);
@@ -295,31 +310,40 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, int ns
     if (!enc) return GDN_ERR_LAUNCH;
     const unsigned long long lim = g_wait_limit_ns.load();
 
+    // ready counts of the fused scan/output launch and the split-item counters start at zero
+    if (cudaMemsetAsync(ws + L.f_off, 0, static_cast<size_t>(items) * 8, stream) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
     // phase 1
     gdn::k1::Params p1;
     p1.beta = a.beta;
     p1.A_ws = A_ws;
     p1.U_ws = U_ws;
     p1.partial = partial;
+    p1.counters = reinterpret_cast<int*>(ws + L.c_off);
     p1.H = a.H;
     p1.N = a.N;
     p1.dk = a.dk;
     p1.dv = a.dv;
     p1.items = static_cast<int>(items);
-    p1.nsplit = nsplit;
-    p1.chunks = (a.N + gdn::k1::CHUNK - 1) / gdn::k1::CHUNK;
-    p1.work = static_cast<int>(items * nsplit);
+    p1.whole = sp.whole;
+    p1.split_per = sp.split_per;
+    p1.chunks = chunks_of(a.N);
+    p1.work = sp.work;
     p1.norm_k = a.prologue;
     p1.beta_sigmoid = a.prologue;
     p1.wait_limit_ns = lim;
     if (ev) cudaEventRecord(ev[0], stream);
-    gdn::k1::contract_kernel<<<std::min(p1.work, ds->sms), gdn::k1::THREADS, gdn::k1::SMEM_BYTES, stream>>>(
-        tm_k, tm_v, p1);
-    if (nsplit > 1) {
-        const size_t total = static_cast<size_t>(items) * (a.dk * a.dk + a.dv * a.dk);
-        const int blocks = static_cast<int>(std::min<size_t>((total + 255) / 256, 4 * ds->sms));
-        gdn::k1::reduce_partials_kernel<<<blocks, 256, 0, stream>>>(partial, A_ws, U_ws, static_cast<int>(items),
-                                                                   nsplit, a.dk, a.dv);
+    const int grid1 = std::min(p1.work, ds->sms);
+    if (sp.rem > 0) {
+        // split items wait for each other's partial sums: all CTAs must be resident
+        void* args1[] = {&tm_k, &tm_v, &p1};
+        if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(gdn::k1::contract_kernel), dim3(grid1),
+                                        dim3(gdn::k1::THREADS), args1, gdn::k1::SMEM_BYTES, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GDN_ERR_LAUNCH;
+        }
+    } else {
+        gdn::k1::contract_kernel<<<grid1, gdn::k1::THREADS, gdn::k1::SMEM_BYTES, stream>>>(tm_k, tm_v, p1);
     }
     // phases 2 and 3
     if (ev) cudaEventRecord(ev[1], stream);
@@ -351,8 +375,6 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, int ns
     const int n_scan = a.B * a.H * p2.rsplit;
     if (Rf != 0) {
         // one cooperative launch: scan CTAs publish per-frame states, output CTAs follow them
-        if (cudaMemsetAsync(flags, 0, static_cast<size_t>(items) * sizeof(int), stream) != cudaSuccess)
-            return GDN_ERR_LAUNCH;
         const long long workers = std::min<long long>(ds->sms - n_scan, std::max<long long>(1, items * p3.ntile));
         int grid = n_scan + static_cast<int>(workers);
         int n_scan_arg = n_scan;
@@ -398,14 +420,15 @@ gdn_status run_pass(const PassArgs& a, bool step, cudaStream_t stream, cudaEvent
     if (st != GDN_OK) return st;
     if (!all_device(a)) return GDN_ERR_NULL_PTR;
     const long long items = static_cast<long long>(a.B) * a.F * a.H;
-    const int nsplit = step ? step_nsplit(ds->sms, a.B, a.H, a.N) : 1;
-    const Layout L = layout_of(items, a.dk, a.dv, nsplit);
+    (void)step;
+    const SplitPlan sp = plan_split(items, chunks_of(a.N), ds->sms, ds->coop_k1);
+    const Layout L = layout_of(items, a.dk, a.dv, sp);
     uint8_t* ws = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), L.total, ds->pool, stream) != cudaSuccess) {
         cudaGetLastError();
         return GDN_ERR_ALLOC;
     }
-    const gdn_status result = launch_phases(a, ws, L, nsplit, ds, stream, ev);
+    const gdn_status result = launch_phases(a, ws, L, sp, ds, stream, ev);
     cudaFreeAsync(ws, stream);
     return result;
 }
@@ -534,13 +557,10 @@ gdn_status gdn_frame_forward_host(const void* q, const void* k, const void* v, c
     return r;
 }
 
-size_t gdn_workspace_bytes(int B, int H, int F, int N, int dk, int dv) {
-    if (B < 1 || H < 1 || F < 1 || N < 1 || !dim_ok(dk) || !dim_ok(dv)) return 0;
-    return layout_of(static_cast<long long>(B) * F * H, dk, dv, 1).total;
-}
+}  // extern "C"
 
-size_t gdn_step_workspace_bytes(int B, int H, int N, int dk, int dv) {
-    if (B < 1 || H < 1 || N < 1 || !dim_ok(dk) || !dim_ok(dv)) return 0;
+namespace {
+int current_sms() {
     int sms = 148;
     int dev = -1;
     if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0) {
@@ -548,7 +568,20 @@ size_t gdn_step_workspace_bytes(int B, int H, int N, int dk, int dv) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) sms = n;
     }
     cudaGetLastError();
-    return layout_of(static_cast<long long>(B) * H, dk, dv, step_nsplit(sms, B, H, N)).total;
+    return sms;
+}
+}  // namespace
+
+extern "C" {
+
+size_t gdn_workspace_bytes(int B, int H, int F, int N, int dk, int dv) {
+    if (B < 1 || H < 1 || F < 1 || N < 1 || !dim_ok(dk) || !dim_ok(dv)) return 0;
+    const long long items = static_cast<long long>(B) * F * H;
+    return layout_of(items, dk, dv, plan_split(items, chunks_of(N), current_sms(), true)).total;
+}
+
+size_t gdn_step_workspace_bytes(int B, int H, int N, int dk, int dv) {
+    return gdn_workspace_bytes(B, H, 1, N, dk, dv);
 }
 
 const char* gdn_status_string(gdn_status s) {
@@ -662,13 +695,13 @@ extern "C" gdn_status gdn_frame_step_noalloc(const void* q, const void* k, const
     st = device_ready(&dev, &ds);
     if (st != GDN_OK) return st;
     const long long items = static_cast<long long>(B) * H;
-    const int nsplit = step_nsplit(ds->sms, B, H, N);
-    const Layout L = layout_of(items, dk, dv, nsplit);
+    const SplitPlan sp = plan_split(items, chunks_of(N), ds->sms, ds->coop_k1);
+    const Layout L = layout_of(items, dk, dv, sp);
     if (L.total > kStepScratchBytes) return GDN_ERR_TOO_LARGE;
     const PassArgs a{q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv};
     if (!all_device(a)) return GDN_ERR_NULL_PTR;
     uint8_t* ws = nullptr;
     st = step_scratch_address(dev, &ws);
     if (st != GDN_OK) return st;
-    return launch_phases(a, ws, L, nsplit, ds, reinterpret_cast<cudaStream_t>(stream_handle), nullptr);
+    return launch_phases(a, ws, L, sp, ds, reinterpret_cast<cudaStream_t>(stream_handle), nullptr);
 }

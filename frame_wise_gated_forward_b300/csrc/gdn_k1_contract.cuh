@@ -38,9 +38,6 @@ namespace k1 {
 #ifndef GDN_K1_BK_BUFS
 #define GDN_K1_BK_BUFS 3
 #endif
-#ifndef GDN_K1_ROUND_ROBIN
-#define GDN_K1_ROUND_ROBIN 1
-#endif
 #ifndef GDN_K1_L2_AHEAD
 #define GDN_K1_L2_AHEAD 0
 #endif
@@ -80,14 +77,16 @@ constexpr size_t SMEM_BYTES =
 
 struct Params {
     const float* beta;     // [B, F, N, H]
-    __nv_bfloat16* A_ws;   // [items][dk][dk]  (nsplit == 1)
-    float* U_ws;           // [items][dv][dk]  (nsplit == 1)
-    float* partial;        // [nsplit][items][dk*dk + dv*dk]  (nsplit > 1)
+    __nv_bfloat16* A_ws;   // [items][dk][dk]
+    float* U_ws;           // [items][dv][dk]
+    float* partial;        // [items - whole][split_per][dk*dk + dv*dk] fp32 partial sums
+    int* counters;         // [items - whole] finished splits per split item (zero on entry)
     int H, N, dk, dv;
     int items;             // B * F * H, item = (b*F + f)*H + h
-    int nsplit;            // token splits per item
+    int whole;             // items 0..whole-1 are processed whole (full rounds of the grid)
+    int split_per;         // each remaining item is split into this many token ranges
     int chunks;            // ceil(N / CHUNK)
-    int work;              // items * nsplit
+    int work;              // whole + (items - whole) * split_per
     int norm_k;            // fused prologue: k <- k / max(|k|, 1e-12) per (token, head)
     int beta_sigmoid;      // fused prologue: beta <- sigmoid(beta)
     unsigned long long wait_limit_ns;
@@ -114,15 +113,26 @@ __device__ __forceinline__ uint4 bscale(uint4 x, const BSplit& s) {
     return x;
 }
 
+// Work units: the first `whole` items whole, then every remaining item split
+// into `split_per` contiguous token ranges (so the last round of the grid is
+// as long as the others); split == -1 marks a whole item.
 struct Unit {
     int item, split, c_begin, c_end;
 };
 __device__ __forceinline__ Unit unit_of(const Params& p, int w) {
     Unit u;
-    u.item = w / p.nsplit;
-    u.split = w % p.nsplit;
-    u.c_begin = static_cast<int>((static_cast<long long>(u.split) * p.chunks) / p.nsplit);
-    u.c_end = static_cast<int>((static_cast<long long>(u.split + 1) * p.chunks) / p.nsplit);
+    if (w < p.whole) {
+        u.item = w;
+        u.split = -1;
+        u.c_begin = 0;
+        u.c_end = p.chunks;
+        return u;
+    }
+    const int r = w - p.whole;
+    u.item = p.whole + r / p.split_per;
+    u.split = r % p.split_per;
+    u.c_begin = static_cast<int>((static_cast<long long>(u.split) * p.chunks) / p.split_per);
+    u.c_end = static_cast<int>((static_cast<long long>(u.split + 1) * p.chunks) / p.split_per);
     return u;
 }
 
@@ -147,16 +157,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-#if GDN_K1_ROUND_ROBIN
-    // work units round-robin over the grid: at any time the CTAs work on
+    // Work units round-robin over the grid: at any time the CTAs work on
     // consecutive items, i.e. all heads of the same few frames, so together
-    // they read whole token rows (all heads) of k and v
+    // they read whole token rows (all heads) of k and v.  The split units come
+    // last and number at most gridDim.x, so each CTA holds at most one.
     const int w_begin = blockIdx.x, w_end = p.work, w_step = gridDim.x;
-#else
-    const int w_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * p.work) / gridDim.x);
-    const int w_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.work) / gridDim.x);
-    const int w_step = 1;
-#endif
     const int kboxes = p.dk > 64 ? 2 : 1;
     const int vboxes = p.dv > 64 ? 2 : 1;
 
@@ -386,22 +391,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int j = quarter * 32 + lane;  // TMEM lane = row j of (beta K)^T = dk index
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int w = w_begin; w < w_end && !*abort_flag; w += w_step) {
+        // The four epilogue warps take every decision together (the AND barrier), so
+        // the named barriers of the split-item fixup below can never be left waiting.
+        for (int w = w_begin; w < w_end; w += w_step) {
             const Unit u = unit_of(p, w);
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, p.wait_limit_ns, abort_flag));
+            const bool ok = bar_and(1, 128, mbar_wait(&tfull[acc], acc_phase, p.wait_limit_ns, abort_flag));
             if (!ok) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(quarter * 32) << 16);
             const bool jv = j < p.dk;
-            if (p.nsplit == 1) {
-                // A: row j of D holds A[j][0..dk); stored as row j (A is symmetric), 16-byte vectors
-                __nv_bfloat16* Arow = p.A_ws + (static_cast<size_t>(u.item) * p.dk + j) * p.dk;
-                float* Uout = p.U_ws + static_cast<size_t>(u.item) * p.dv * p.dk;
+            const size_t per = static_cast<size_t>(p.dk) * p.dk + static_cast<size_t>(p.dv) * p.dk;
+            // whole item: A (bf16) and U (fp32) straight to the workspace; split item: fp32
+            // partial sums in the same element order
+            float* part = u.split < 0 ? nullptr
+                                      : p.partial + (static_cast<size_t>(u.item - p.whole) * p.split_per + u.split) * per;
+            {
+                // A: row j of D holds A[j][0..dk); stored as row j (A is symmetric)
                 for (int c0 = 0; c0 < p.dk; c0 += 32) {
                     uint32_t r32[32];
                     tmem_ld32(tbase + c0, r32);
                     tmem_wait_ld();
-                    if (jv) {
+                    if (!jv) continue;
+                    if (part == nullptr) {
+                        __nv_bfloat16* Arow = p.A_ws + (static_cast<size_t>(u.item) * p.dk + j) * p.dk;
 #pragma unroll
                         for (int q8 = 0; q8 < 4; ++q8) {
                             uint4 v4 = make_uint4(
@@ -411,9 +423,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 pack_bf16x2(__uint_as_float(r32[8 * q8 + 6]), __uint_as_float(r32[8 * q8 + 7])));
                             if (c0 + 8 * q8 < p.dk) *reinterpret_cast<uint4*>(Arow + c0 + 8 * q8) = v4;
                         }
+                    } else {
+                        float* prow = part + static_cast<size_t>(j) * p.dk;
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            if (c0 + 4 * q4 < p.dk)
+                                *reinterpret_cast<uint4*>(prow + c0 + 4 * q4) =
+                                    make_uint4(r32[4 * q4], r32[4 * q4 + 1], r32[4 * q4 + 2], r32[4 * q4 + 3]);
                     }
                 }
                 // U: row j of D holds U[0..dv)[j]; coalesced along j
+                float* Uout = part == nullptr ? p.U_ws + static_cast<size_t>(u.item) * p.dv * p.dk
+                                              : part + static_cast<size_t>(p.dk) * p.dk;
                 for (int c0 = 0; c0 < p.dv; c0 += 32) {
                     uint32_t r32[32];
                     tmem_ld32(tbase + 128 + c0, r32);
@@ -424,34 +445,51 @@ __global__ void __launch_bounds__(THREADS, 1)
                             if (c0 + t < p.dv) Uout[static_cast<size_t>(c0 + t) * p.dk + j] = __uint_as_float(r32[t]);
                     }
                 }
-            } else {
-                const size_t per = static_cast<size_t>(p.dk) * p.dk + static_cast<size_t>(p.dv) * p.dk;
-                float* out = p.partial + (static_cast<size_t>(u.split) * p.items + u.item) * per;
-                for (int c0 = 0; c0 < p.dk; c0 += 32) {
-                    uint32_t r32[32];
-                    tmem_ld32(tbase + c0, r32);
-                    tmem_wait_ld();
-                    if (jv) {
-#pragma unroll
-                        for (int t = 0; t < 32; ++t)
-                            if (c0 + t < p.dk) out[static_cast<size_t>(c0 + t) * p.dk + j] = __uint_as_float(r32[t]);
-                    }
-                }
-                float* outU = out + static_cast<size_t>(p.dk) * p.dk;
-                for (int c0 = 0; c0 < p.dv; c0 += 32) {
-                    uint32_t r32[32];
-                    tmem_ld32(tbase + 128 + c0, r32);
-                    tmem_wait_ld();
-                    if (jv) {
-#pragma unroll
-                        for (int t = 0; t < 32; ++t)
-                            if (c0 + t < p.dv) outU[static_cast<size_t>(c0 + t) * p.dk + j] = __uint_as_float(r32[t]);
-                    }
-                }
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            if (part != nullptr) {
+                // Split item: once every split of the item has written its
+                // partial sums, each split reduces its own share of the
+                // elements, adding the partials in split order (deterministic).
+                // The splits of an item are consecutive units, so they run on
+                // distinct CTAs, each as its CTA's last unit, and the
+                // cooperative launch keeps all of them resident: the wait ends.
+                __threadfence();
+                named_bar_sync(1, 128);
+                const int r_item = u.item - p.whole;
+                bool ready = true;
+                if (j == 0) {
+                    red_release_add(p.counters + r_item, 1);
+                    ready = wait_count_geq(p.counters + r_item, p.split_per, p.wait_limit_ns, abort_flag);
+                }
+                if (!bar_and(1, 128, ready)) break;
+                __threadfence();
+                const float4* base = reinterpret_cast<const float4*>(
+                    p.partial + static_cast<size_t>(r_item) * p.split_per * per);
+                const size_t per4 = per / 4;                                   // dk, dv are multiples of 16
+                const size_t a4 = static_cast<size_t>(p.dk) * p.dk / 4;        // A occupies [0, a4)
+                const size_t e_begin = per4 * u.split / p.split_per;
+                const size_t e_end = per4 * (u.split + 1) / p.split_per;
+                for (size_t e = e_begin + j; e < e_end; e += 128) {
+                    float4 acc4 = __ldcg(base + e);
+                    for (int sp = 1; sp < p.split_per; ++sp) {
+                        const float4 t4 = __ldcg(base + static_cast<size_t>(sp) * per4 + e);
+                        acc4.x += t4.x;
+                        acc4.y += t4.y;
+                        acc4.z += t4.z;
+                        acc4.w += t4.w;
+                    }
+                    if (e < a4) {
+                        *reinterpret_cast<uint2*>(p.A_ws + static_cast<size_t>(u.item) * p.dk * p.dk + 4 * e) =
+                            make_uint2(pack_bf16x2(acc4.x, acc4.y), pack_bf16x2(acc4.z, acc4.w));
+                    } else {
+                        *reinterpret_cast<float4*>(p.U_ws + static_cast<size_t>(u.item) * p.dv * p.dk +
+                                                   4 * (e - a4)) = acc4;
+                    }
+                }
+            }
         }
     }
 
@@ -461,24 +499,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
-    }
-}
-
-// Step path: sum the per-split fp32 partials in split order (deterministic)
-// and write A (bf16) and U (fp32) in the layout phase 2 reads.
-__global__ void reduce_partials_kernel(const float* __restrict__ partial, __nv_bfloat16* __restrict__ A_ws,
-                                       float* __restrict__ U_ws, int items, int nsplit, int dk, int dv) {
-    const size_t per = static_cast<size_t>(dk) * dk + static_cast<size_t>(dv) * dk;
-    const size_t total = per * items;
-    for (size_t e = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; e < total;
-         e += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const size_t item = e / per, off = e % per;
-        float s = 0.0f;
-        for (int sp = 0; sp < nsplit; ++sp) s += partial[(static_cast<size_t>(sp) * items + item) * per + off];
-        if (off < static_cast<size_t>(dk) * dk)
-            A_ws[item * dk * dk + off] = __float2bfloat16_rn(s);
-        else
-            U_ws[item * dv * dk + (off - static_cast<size_t>(dk) * dk)] = s;
     }
 }
 

@@ -101,25 +101,6 @@ struct Sched {
 };
 
 // Bounded wait until the scan has published all slices of `item`'s state.
-__device__ __forceinline__ bool wait_state_ready(const int* flags, long long item, int target, uint64_t limit_ns,
-                                                 volatile int* abort_flag) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flags + item) : "memory");
-    if (v >= target) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        __nanosleep(64);
-        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flags + item) : "memory");
-        if (v >= target) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > limit_ns) {
-            record_error(GDN_ERR_TIMEOUT);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
 __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUtensorMap* tm_s,
                                             const CUtensorMap* tm_out, const Params& p, const Sched& sc,
                                             uint8_t* smem) {
@@ -196,7 +177,7 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
                 if (k > 0) { if (++ss == SSTAGES) { ss = 0; sph ^= 1; } }
                 if (!mbar_wait(&sempty[ss], sph ^ 1, p.wait_limit_ns, abort_flag)) break;
                 if (sc.fused) {
-                    if (!wait_state_ready(sc.flags, item, sc.flag_target, p.wait_limit_ns, abort_flag)) break;
+                    if (!wait_count_geq(sc.flags + item, sc.flag_target, p.wait_limit_ns, abort_flag)) break;
                     fence_proxy_async_global();  // the published state is read through the async proxy
                 }
                 mbar_arrive_expect_tx(&sfull[ss], kboxes * BOX_BYTES);

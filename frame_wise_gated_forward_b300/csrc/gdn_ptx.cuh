@@ -88,6 +88,26 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
     }
 }
 
+// Named barrier `id` over the first `nthreads` threads of the CTA (multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// AND-reduction over named barrier `id` among `nthreads` threads: every
+// participant gets true only if all passed true.
+__device__ __forceinline__ bool bar_and(int id, int nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -163,6 +183,29 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // release-ordered atomic add at GPU scope (publishes everything written before it)
 __device__ __forceinline__ void red_release_add(int* p, int v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait (bounded) until the counter at `p` reaches `target`, with acquire
+// ordering: whatever the other CTAs wrote before their release-add is then
+// visible.  Gives up after limit_ns, or when `abort_flag` is raised, recording
+// GDN_ERR_TIMEOUT and raising the flag itself on a timeout.
+__device__ __forceinline__ bool wait_count_geq(const int* p, int target, uint64_t limit_ns,
+                                               volatile int* abort_flag) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(64);
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v >= target) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            record_error(GDN_ERR_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+    }
 }
 
 // generic-proxy shared-memory writes -> visible to the async proxy (TMA, tensor core)
