@@ -221,6 +221,14 @@ def set_fused_scan(mode) -> None:
     load().gdn_set_fused_scan(int(mode))
 
 
+def set_contract_split(max_split: int) -> None:
+    """Phase-1 work plan: 0 (default) splits the items left over after the
+    last full round of the grid into token ranges only when they have at
+    least 32 chunks of 64 tokens; 1 never splits; k > 1 always splits them
+    into up to k ranges."""
+    load().gdn_set_contract_split(int(max_split))
+
+
 def scan_schedule(B, H, dv) -> int:
     """+R: fused scan/output with R state rows per scan CTA; -R: two launches."""
     return int(load().gdn_scan_schedule(B, H, dv))

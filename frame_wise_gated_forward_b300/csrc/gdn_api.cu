@@ -21,6 +21,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ULL};
 std::atomic<int> g_fused_scan{1};
+std::atomic<int> g_max_split{0};  // 0: automatic; 1: never split; k > 1: up to k token ranges per item
 
 // ------------------------------------------------------------------ devices
 struct DeviceState {
@@ -178,8 +179,13 @@ bool is_device_ptr(const void* p) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Work plan of the contraction kernel on a grid of `grid` CTAs: whole items
-// for as many full rounds as fit, the remaining items split into token ranges
-// so the last round is as long as the others (see gdn::k1::unit_of).
+// for as many full rounds as fit, then the remaining items, either whole or
+// split into token ranges so that the last round is about as long as the
+// others (see gdn::k1::unit_of).  A split costs a fixed few microseconds (the
+// fp32 partial sums go through L2 and the splits wait for each other), which
+// measured on B300 about what it saves at 14 chunks per item; so the automatic
+// plan splits only items of at least kMinSplitChunks 64-token chunks.
+constexpr int kMinSplitChunks = 32;
 struct SplitPlan {
     int whole, rem, split_per, work;
 };
@@ -187,8 +193,10 @@ SplitPlan plan_split(long long items, int chunks, int grid, bool allow_split) {
     SplitPlan sp;
     sp.whole = static_cast<int>(items >= grid ? (items / grid) * grid : 0);
     sp.rem = static_cast<int>(items - sp.whole);
-    sp.split_per = (sp.rem > 0 && allow_split) ? std::max(1, std::min(chunks, grid / sp.rem)) : 1;
-    if (sp.split_per == 1) {  // nothing to gain from splitting: every item whole
+    const int mode = g_max_split.load();
+    int cap = mode == 0 ? (chunks >= kMinSplitChunks ? chunks : 1) : mode;
+    sp.split_per = (sp.rem > 0 && allow_split) ? std::max(1, std::min({cap, chunks, grid / sp.rem})) : 1;
+    if (sp.split_per == 1) {  // every item whole
         sp.whole = static_cast<int>(items);
         sp.rem = 0;
     }
@@ -617,6 +625,8 @@ gdn_status gdn_sync_status(gdn_stream_t stream) {
     }
     return GDN_OK;
 }
+
+void gdn_set_contract_split(int max_split) { g_max_split.store(max_split > 0 ? max_split : 0); }
 
 void gdn_set_fused_scan(int mode) {
     g_fused_scan.store((mode == 16 || mode == 32 || mode == 64) ? mode : (mode != 0 ? 1 : 0));

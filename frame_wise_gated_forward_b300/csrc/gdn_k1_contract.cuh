@@ -38,9 +38,6 @@ namespace k1 {
 #ifndef GDN_K1_BK_BUFS
 #define GDN_K1_BK_BUFS 3
 #endif
-#ifndef GDN_K1_L2_AHEAD
-#define GDN_K1_L2_AHEAD 0
-#endif
 #ifndef GDN_K1_SCALER_WARPS
 #define GDN_K1_SCALER_WARPS 4
 #endif
@@ -205,29 +202,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
-            // L2 prefetch cursor GDN_K1_L2_AHEAD chunks ahead of the loads: the
-            // loads into the ring then find their data in L2, which keeps more
-            // bytes in flight than the ring alone can hold
-            int lw = w_begin, lc = 0;
-            if (lw < w_end) lc = unit_of(p, lw).c_begin;
-            auto prefetch_next = [&]() {
-                if (lw >= w_end) return;
-                const Unit u = unit_of(p, lw);
-                const int fr = u.item / p.H, hh = u.item % p.H;
-                for (int bx = 0; bx < kboxes; ++bx) tma_prefetch_l2_4d(&tm_k, 64 * bx, hh, lc * CHUNK, fr);
-                for (int bx = 0; bx < vboxes; ++bx) tma_prefetch_l2_4d(&tm_v, 64 * bx, hh, lc * CHUNK, fr);
-                if (++lc >= u.c_end) {
-                    lw += w_step;
-                    if (lw < w_end) lc = unit_of(p, lw).c_begin;
-                }
-            };
-            for (int i = 0; i < STAGES + GDN_K1_L2_AHEAD; ++i) prefetch_next();
             for (int w = w_begin; w < w_end && !*abort_flag; w += w_step) {
                 const Unit u = unit_of(p, w);
                 const int frame = u.item / p.H, h = u.item % p.H;
                 for (int c = u.c_begin; c < u.c_end; ++c) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, abort_flag)) break;
-                    if (GDN_K1_L2_AHEAD > 0) prefetch_next();
                     uint8_t* st = stage_base + stage * STAGE_BYTES;
                     mbar_arrive_expect_tx(&full[stage], (kboxes + vboxes) * BOX_BYTES);
                     for (int bx = 0; bx < kboxes; ++bx)
@@ -472,22 +451,41 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const size_t a4 = static_cast<size_t>(p.dk) * p.dk / 4;        // A occupies [0, a4)
                 const size_t e_begin = per4 * u.split / p.split_per;
                 const size_t e_end = per4 * (u.split + 1) / p.split_per;
-                for (size_t e = e_begin + j; e < e_end; e += 128) {
-                    float4 acc4 = __ldcg(base + e);
-                    for (int sp = 1; sp < p.split_per; ++sp) {
-                        const float4 t4 = __ldcg(base + static_cast<size_t>(sp) * per4 + e);
-                        acc4.x += t4.x;
-                        acc4.y += t4.y;
-                        acc4.z += t4.z;
-                        acc4.w += t4.w;
-                    }
+                // two elements per thread and up to eight splits per batch of
+                // loads, all issued before the adds: 16 L2 reads in flight per thread
+                const int S = p.split_per;
+                auto store4 = [&](size_t e, const float4& v) {
                     if (e < a4) {
                         *reinterpret_cast<uint2*>(p.A_ws + static_cast<size_t>(u.item) * p.dk * p.dk + 4 * e) =
-                            make_uint2(pack_bf16x2(acc4.x, acc4.y), pack_bf16x2(acc4.z, acc4.w));
+                            make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
                     } else {
                         *reinterpret_cast<float4*>(p.U_ws + static_cast<size_t>(u.item) * p.dv * p.dk +
-                                                   4 * (e - a4)) = acc4;
+                                                   4 * (e - a4)) = v;
                     }
+                };
+                for (size_t e0 = e_begin + j; e0 < e_end; e0 += 256) {
+                    const size_t e1 = e0 + 128;
+                    const bool has1 = e1 < e_end;
+                    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+                    for (int sb = 0; sb < S; sb += 8) {
+                        float4 t0[8], t1[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            if (sb + i < S) {
+                                t0[i] = __ldcg(base + static_cast<size_t>(sb + i) * per4 + e0);
+                                if (has1) t1[i] = __ldcg(base + static_cast<size_t>(sb + i) * per4 + e1);
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            if (sb + i < S) {  // splits added in order
+                                s0.x += t0[i].x; s0.y += t0[i].y; s0.z += t0[i].z; s0.w += t0[i].w;
+                                if (has1) { s1.x += t1[i].x; s1.y += t1[i].y; s1.z += t1[i].z; s1.w += t1[i].w; }
+                            }
+                        }
+                    }
+                    store4(e0, s0);
+                    if (has1) store4(e1, s1);
                 }
             }
         }

@@ -206,6 +206,20 @@ void gdn_set_wait_limit_ns(unsigned long long limit_ns);
 void gdn_set_fused_scan(int mode);
 
 /*
+ * Work plan of phase 1.  Phase 1 runs (b, f, h) items round-robin over one CTA
+ * per SM.  The items left over after the last full round can be split into
+ * token ranges, one CTA each, whose fp32 partial sums are then added in split
+ * order (the launch is then cooperative).  max_split 0 (default): split only
+ * items of at least 32 chunks of 64 tokens, into as many ranges as the free
+ * CTAs and the chunks allow; 1: never split; k > 1: split the leftover items
+ * into up to k ranges whatever their length.  Results are deterministic for
+ * every setting; different settings round the split items' sums in a
+ * different order.  Applies to calls made after it returns.  A scheduling
+ * control of this library; the pages have no counterpart.
+ */
+void gdn_set_contract_split(int max_split);
+
+/*
  * Schedule phases 2 and 3 take for this shape on the current device: +R when
  * they run as one cooperative launch with R rows of S per scan CTA, -R when
  * they run as two launches, 0 for invalid shapes or no usable device.

@@ -45,22 +45,22 @@ def test_status_strings(lib):
 
 def test_workspace_bytes(lib):
     # A bf16 + U fp32 + per-frame states bf16 for 121*16 items of 128x128,
-    # one ready count and one split counter per item, and fp32 partial sums
-    # of the items left over after full rounds of 148 CTAs (no GPU here, so
-    # the library plans for 148 SMs): 1936 = 13*148 + 12 items, each of the
-    # last 12 split into min(14 chunks, 148 // 12) = 12 token ranges.
+    # plus one ready count and one split counter per item.  At N = 880 (14
+    # chunks of 64 tokens per item) the automatic plan splits nothing.
     items = 121 * 16
-    partial = 12 * 12 * (128 * 128 + 128 * 128) * 4
-    want = items * 128 * 128 * (2 + 4 + 2) + items * 8 + partial
+    want = items * 128 * 128 * (2 + 4 + 2) + items * 8
     got = lib.gdn_workspace_bytes(1, 16, 121, 880, 128, 128)
     assert want <= got <= want + 4 * 256
-    # 2 * 148 items fill two rounds exactly: nothing is split
-    items = 2 * 148
-    want = items * 128 * 128 * 8 + items * 8
-    assert want <= lib.gdn_workspace_bytes(1, 2, 148, 880, 128, 128) <= want + 4 * 256
-    # the one-frame step of 16 heads: every head split into 148 // 16 = 9 ranges
+    assert lib.gdn_step_workspace_bytes(1, 16, 880, 128, 128) == lib.gdn_workspace_bytes(1, 16, 1, 880, 128, 128)
+    # N = 8800 (138 chunks): 1936 = 13*148 + 12 items, the last 12 split into
+    # min(138, 148 // 12) = 12 token ranges with fp32 partial sums (no GPU
+    # here, so the library plans for 148 SMs)
+    partial = 12 * 12 * (128 * 128 + 128 * 128) * 4
+    want = items * 128 * 128 * 8 + items * 8 + partial
+    assert want <= lib.gdn_workspace_bytes(1, 16, 121, 8800, 128, 128) <= want + 4 * 256
+    # the one-frame step of 16 heads at N = 8800: 148 // 16 = 9 ranges per head
     want = 16 * 128 * 128 * 8 + 16 * 8 + 16 * 9 * 2 * 128 * 128 * 4
-    assert want <= lib.gdn_step_workspace_bytes(1, 16, 880, 128, 128) <= want + 4 * 256
+    assert want <= lib.gdn_step_workspace_bytes(1, 16, 8800, 128, 128) <= want + 4 * 256
     assert lib.gdn_workspace_bytes(0, 16, 121, 880, 128, 128) == 0
     assert lib.gdn_workspace_bytes(1, 16, 121, 880, 96 + 8, 128) == 0
 
