@@ -89,10 +89,11 @@ def kernel_costs(w):
     }
 
 
-def path_floor_bytes(w):
-    """Compulsory HBM bytes of the whole forward: q, k, v read, out written, beta, alpha, state."""
+def path_floor_bytes(w, in_bytes=2):
+    """Compulsory HBM bytes of the whole forward: q, k, v read (in_bytes per
+    element: 2 bf16, 1 fp8), out written (bf16), beta, alpha, state."""
     T = w.B * w.F * w.N
-    return (T * w.H * (2 * w.dk + w.dv) * 2 + T * w.H * w.dv * 2 + T * w.H * 4 + w.B * w.F * w.H * 4
+    return (T * w.H * (2 * w.dk + w.dv) * in_bytes + T * w.H * w.dv * 2 + T * w.H * 4 + w.B * w.F * w.H * 4
             + w.B * w.H * w.dv * w.dk * 4)
 
 
@@ -350,6 +351,29 @@ def main():
                   "what": "raw q, k L2-normalized and sigmoid/softplus gates applied inside the kernels"}
     del xr
 
+    # ------------------------------------------ 8-bit inputs (e4m3 q, k, v)
+    x8 = {k: (v.to(device) if torch.is_tensor(v) else v)
+          for k, v in inputs.draw_fp8(w.B, w.H, w.F, w.N, w.dk, w.dv, seed=0).items()}
+
+    def step8():
+        api.frame_forward_fp8(x8["q8"], x8["k8"], x8["v8"], x8["q_scale"], x8["k_scale"], x8["v_scale"],
+                              x8["alpha"], x8["beta"], None, out=out, state_out=st)
+    step8()
+    torch.cuda.synchronize(device)
+    r0.record(stream)
+    for _ in range(nr):
+        step8()
+    r1.record(stream)
+    torch.cuda.synchronize(device)
+    api.sync_status()
+    fp8_ms = r0.elapsed_time(r1) / nr
+    fp8_floor_ms = path_floor_bytes(w, in_bytes=1) / (peaks["hbm_gbs"] * 1e9) * 1e3
+    fp8_info = {"ms_per_step": fp8_ms, "tokens_per_s": tokens / (fp8_ms / 1e3), "steps": nr,
+                "path_floor_ms": fp8_floor_ms, "path_frac": fp8_floor_ms / fp8_ms,
+                "what": "q, k, v as per-tensor-scaled OCP FP8 E4M3 (1 byte each), decoded in shared memory; "
+                        "out bf16, state fp32"}
+    del x8
+
     # ------------------------------------------- interactive step (one frame)
     # the streaming rollout: F sequential gdn_frame_step calls on a resident state
     step_state = torch.zeros((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=device)
@@ -368,7 +392,7 @@ def main():
     api.sync_status()
     step_us = s0.elapsed_time(s1) * 1e3 / w.F
     step_info = {"us_per_frame_step": step_us, "tokens_per_s": w.B * w.N / (step_us / 1e6),
-                 "launches_per_step": 4, "frames": w.F,
+                 "launches_per_step": 2, "memsets_per_step": 1, "frames": w.F,
                  "floor_us": (w.B * w.N * w.H * (2 * w.dk + 2 * w.dv) * 2 + 2 * w.B * w.H * w.dv * w.dk * 4)
                  / (peaks["hbm_gbs"] * 1e9) * 1e6}
     del frames
@@ -424,6 +448,7 @@ def main():
             "step": step_info,
             "reverse_direction": reverse_info,
             "gated_prologue": gated_info,
+            "fp8_inputs": fp8_info,
             "cpu_baseline": cpu,
             "clocks": clocks,
             "gpu_launches": (3 if sched <= 0 else 2) * args.steps,

@@ -116,6 +116,68 @@ def frame_step_gated(q, k, v, a_logit, b_logit, alpha_scale, state_in=None, *, o
     return out, state_out
 
 
+def _bytes8(t):
+    """e4m3 tensors are passed as their bytes (torch.float8_e4m3fn or uint8)."""
+    if isinstance(t, torch.Tensor) and t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8)
+    return t
+
+
+def frame_forward_fp8(q, k, v, q_scale, k_scale, v_scale, alpha, beta, state_in=None, *, out=None,
+                      state_out=None, stream=None):
+    """Forward on 8-bit inputs: q, k [B,F,N,H,dk] and v [B,F,N,H,dv] as OCP
+    FP8 E4M3 (torch.float8_e4m3fn, or uint8 holding the codes), each with one
+    fp32 scale (value = scale * e4m3).  out bf16, state fp32 as frame_forward."""
+    lib = load()
+    q, k, v = _bytes8(q), _bytes8(k), _bytes8(v)
+    B, F, N, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, F, N, H, dv), dtype=torch.bfloat16, device=q.device)
+    if state_out is None:
+        state_out = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
+    args = [
+        _dev(q, "q", torch.uint8, (B, F, N, H, dk)),
+        _dev(k, "k", torch.uint8, (B, F, N, H, dk)),
+        _dev(v, "v", torch.uint8, (B, F, N, H, dv)),
+        float(q_scale), float(k_scale), float(v_scale),
+        _dev(alpha, "alpha", torch.float32, (B, F, H)),
+        _dev(beta, "beta", torch.float32, (B, F, N, H)),
+        None if state_in is None else _dev(state_in, "state_in", torch.float32, (B, H, dv, dk)),
+        _dev(out, "out", torch.bfloat16, (B, F, N, H, dv)),
+        _dev(state_out, "state_out", torch.float32, (B, H, dv, dk)),
+    ]
+    check(lib.gdn_frame_forward_fp8(*args, B, H, F, N, dk, dv, _stream_handle(stream)), "gdn_frame_forward_fp8")
+    return out, state_out
+
+
+def frame_step_fp8(q, k, v, q_scale, k_scale, v_scale, alpha, beta, state_in=None, *, out=None, state_out=None,
+                   stream=None):
+    """One frame on a resident state with 8-bit inputs (see frame_forward_fp8).
+    q, k [B,N,H,dk]; v [B,N,H,dv]; alpha [B,H]; beta [B,N,H]."""
+    lib = load()
+    q, k, v = _bytes8(q), _bytes8(k), _bytes8(v)
+    B, N, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=q.device)
+    if state_out is None:
+        state_out = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
+    args = [
+        _dev(q, "q", torch.uint8, (B, N, H, dk)),
+        _dev(k, "k", torch.uint8, (B, N, H, dk)),
+        _dev(v, "v", torch.uint8, (B, N, H, dv)),
+        float(q_scale), float(k_scale), float(v_scale),
+        _dev(alpha, "alpha", torch.float32, (B, H)),
+        _dev(beta, "beta", torch.float32, (B, N, H)),
+        None if state_in is None else _dev(state_in, "state_in", torch.float32, (B, H, dv, dk)),
+        _dev(out, "out", torch.bfloat16, (B, N, H, dv)),
+        _dev(state_out, "state_out", torch.float32, (B, H, dv, dk)),
+    ]
+    check(lib.gdn_frame_step_fp8(*args, B, H, N, dk, dv, _stream_handle(stream)), "gdn_frame_step_fp8")
+    return out, state_out
+
+
 def frame_step(q, k, v, alpha, beta, state_in=None, *, out=None, state_out=None, stream=None):
     """One latent frame on a resident state.  q, k [B,N,H,dk]; v [B,N,H,dv];
     alpha [B,H]; beta [B,N,H].  state_out may be the same tensor as state_in."""

@@ -80,26 +80,31 @@ gdn_status device_ready(int* dev_out, DeviceState** st_out) {
                    cudaSuccess;
         };
         using namespace gdn;
-        if (!smem_attr(reinterpret_cast<const void*>(k1::contract_kernel), k1::SMEM_BYTES) ||
+        if (!smem_attr(reinterpret_cast<const void*>(k1::contract_kernel<false>), k1::SMEM_BYTES) ||
+            !smem_attr(reinterpret_cast<const void*>(k1::contract_kernel<true>), k1::SMEM_BYTES_FP8) ||
             !smem_attr(reinterpret_cast<const void*>(k2::scan_kernel<16>), k2::Cfg<16>::SMEM_BYTES) ||
             !smem_attr(reinterpret_cast<const void*>(k2::scan_kernel<32>), k2::Cfg<32>::SMEM_BYTES) ||
             !smem_attr(reinterpret_cast<const void*>(k2::scan_kernel<64>), k2::Cfg<64>::SMEM_BYTES) ||
-            !smem_attr(reinterpret_cast<const void*>(k3::output_kernel), k3::SMEM_BYTES) ||
-            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<16>), k23::smem_bytes<16>()) ||
-            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<32>), k23::smem_bytes<32>()) ||
-            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<64>), k23::smem_bytes<64>())) {
+            !smem_attr(reinterpret_cast<const void*>(k3::output_kernel<false>), k3::SMEM_BYTES) ||
+            !smem_attr(reinterpret_cast<const void*>(k3::output_kernel<true>), k3::SMEM_BYTES) ||
+            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<16, false>), k23::smem_bytes<16>()) ||
+            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<32, false>), k23::smem_bytes<32>()) ||
+            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<64, false>), k23::smem_bytes<64>()) ||
+            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<16, true>), k23::smem_bytes<16>()) ||
+            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<32, true>), k23::smem_bytes<32>()) ||
+            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<64, true>), k23::smem_bytes<64>())) {
             cudaGetLastError();
             return GDN_ERR_LAUNCH;
         }
         int coop = 0, per_sm = 0;
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k23::scan_output_kernel<64>, k23::THREADS,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k23::scan_output_kernel<64, false>, k23::THREADS,
                                                           k23::smem_bytes<64>()) != cudaSuccess)
             per_sm = 0;
         cudaGetLastError();
         d.coop = coop != 0 && per_sm >= 1;
         int per_sm_k1 = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_k1, k1::contract_kernel, k1::THREADS,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_k1, k1::contract_kernel<false>, k1::THREADS,
                                                           k1::SMEM_BYTES) != cudaSuccess)
             per_sm_k1 = 0;
         cudaGetLastError();
@@ -120,9 +125,10 @@ struct Range {
 };
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
+// in_bytes: bytes per q/k/v element (2: bf16, 1: fp8); out is always bf16
 gdn_status validate(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
                     const float* state_in, const void* out, const float* state_out, int B, int H, int F, int N,
-                    int dk, int dv) {
+                    int dk, int dv, int in_bytes = 2) {
     if (!q || !k || !v || !alpha || !beta || !out) return GDN_ERR_NULL_PTR;
     if (B < 1 || H < 1 || F < 1 || N < 1) return GDN_ERR_BAD_DIM;
     if (!dim_ok(dk) || !dim_ok(dv)) return GDN_ERR_UNSUPPORTED;
@@ -136,9 +142,9 @@ gdn_status validate(const void* q, const void* k, const void* v, const float* al
         return GDN_ERR_MISALIGNED;
     const uintptr_t qb = reinterpret_cast<uintptr_t>(q), kb = reinterpret_cast<uintptr_t>(k),
                     vb = reinterpret_cast<uintptr_t>(v), ob = reinterpret_cast<uintptr_t>(out);
-    const Range rq{qb, qb + static_cast<uintptr_t>(tok * H * dk * 2)};
-    const Range rk{kb, kb + static_cast<uintptr_t>(tok * H * dk * 2)};
-    const Range rv{vb, vb + static_cast<uintptr_t>(tok * H * dv * 2)};
+    const Range rq{qb, qb + static_cast<uintptr_t>(tok * H * dk * in_bytes)};
+    const Range rk{kb, kb + static_cast<uintptr_t>(tok * H * dk * in_bytes)};
+    const Range rv{vb, vb + static_cast<uintptr_t>(tok * H * dv * in_bytes)};
     const Range ro{ob, ob + static_cast<uintptr_t>(tok * H * dv * 2)};
     const uintptr_t ab = reinterpret_cast<uintptr_t>(alpha), bb = reinterpret_cast<uintptr_t>(beta);
     const Range ra{ab, ab + static_cast<uintptr_t>(static_cast<long long>(B) * F * H * 4)};
@@ -239,6 +245,19 @@ bool encode_tokens(CUtensorMap* m, const void* base, int BF, int N, int H, int d
     const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(rows), 1};
     return encode(m, const_cast<void*>(base), 4, dims, strides, box);
 }
+// fp8 token tensor [BF, N, H, d] bytes, box (128, 1, rows, 1): one 128-byte
+// row per token, columns past d zero-filled
+bool encode_tokens8(CUtensorMap* m, const void* base, int BF, int N, int H, int d, int rows) {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BF)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H) * d,
+                                   static_cast<cuuint64_t>(N) * H * d};
+    const cuuint32_t box[4] = {128, 1, static_cast<cuuint32_t>(rows), 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 // per-item matrix [items, rows_total, cols] bf16, box (64, rows, 1)
 bool encode_mats(CUtensorMap* m, const void* base, long long items, int rows_total, int cols, int rows) {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows_total),
@@ -272,6 +291,8 @@ struct PassArgs {
     int reverse = 0;
     int prologue = 0;          // raw q, k and gate logits: normalize and apply the gates in the kernels
     float alpha_scale = 0.0f;  // prologue: alpha = exp(-softplus(a) * alpha_scale)
+    int fp8 = 0;               // q, k, v are e4m3 bytes; real value = scale * e4m3
+    float q_scale = 1.0f, k_scale = 1.0f, v_scale = 1.0f;
 };
 
 // Rows of S per scan CTA.  Standalone scan: the smallest slice that keeps
@@ -307,9 +328,14 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
     const int R = Rf != 0 ? Rf : scan_rows_standalone(a.B, a.H, a.dv, ds->sms);
     int* flags = reinterpret_cast<int*>(ws + L.f_off);
     CUtensorMap tm_k, tm_v, tm_q, tm_out, tm_A, tm_U, tm_S_store, tm_S_load;
-    const bool enc = encode_tokens(&tm_k, a.k, BF, a.N, a.H, a.dk, gdn::k1::CHUNK) &&
-                     encode_tokens(&tm_v, a.v, BF, a.N, a.H, a.dv, gdn::k1::CHUNK) &&
-                     encode_tokens(&tm_q, a.q, BF, a.N, a.H, a.dk, gdn::k3::TILE_M) &&
+    const bool enc_in =
+        a.fp8 ? (encode_tokens8(&tm_k, a.k, BF, a.N, a.H, a.dk, gdn::k1::CHUNK) &&
+                 encode_tokens8(&tm_v, a.v, BF, a.N, a.H, a.dv, gdn::k1::CHUNK) &&
+                 encode_tokens8(&tm_q, a.q, BF, a.N, a.H, a.dk, gdn::k3::TILE_M))
+              : (encode_tokens(&tm_k, a.k, BF, a.N, a.H, a.dk, gdn::k1::CHUNK) &&
+                 encode_tokens(&tm_v, a.v, BF, a.N, a.H, a.dv, gdn::k1::CHUNK) &&
+                 encode_tokens(&tm_q, a.q, BF, a.N, a.H, a.dk, gdn::k3::TILE_M));
+    const bool enc = enc_in &&
                      encode_tokens(&tm_out, a.out, BF, a.N, a.H, a.dv, 32) &&
                      encode_mats(&tm_A, A_ws, items, a.dk, a.dk, 128) &&
                      encode_mats_f32(&tm_U, U_ws, items, a.dv, a.dk, R) &&
@@ -339,19 +365,22 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
     p1.work = sp.work;
     p1.norm_k = a.prologue;
     p1.beta_sigmoid = a.prologue;
+    p1.a_scale = a.fp8 ? a.k_scale * a.k_scale : 1.0f;
+    p1.u_scale = a.fp8 ? a.k_scale * a.v_scale : 1.0f;
     p1.wait_limit_ns = lim;
     if (ev) cudaEventRecord(ev[0], stream);
     const int grid1 = std::min(p1.work, ds->sms);
-    if (sp.rem > 0) {
-        // split items wait for each other's partial sums: all CTAs must be resident
-        void* args1[] = {&tm_k, &tm_v, &p1};
-        if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(gdn::k1::contract_kernel), dim3(grid1),
-                                        dim3(gdn::k1::THREADS), args1, gdn::k1::SMEM_BYTES, stream) != cudaSuccess) {
-            cudaGetLastError();
-            return GDN_ERR_LAUNCH;
-        }
-    } else {
-        gdn::k1::contract_kernel<<<grid1, gdn::k1::THREADS, gdn::k1::SMEM_BYTES, stream>>>(tm_k, tm_v, p1);
+    const void* fn1 = a.fp8 ? reinterpret_cast<const void*>(gdn::k1::contract_kernel<true>)
+                            : reinterpret_cast<const void*>(gdn::k1::contract_kernel<false>);
+    const size_t smem1 = a.fp8 ? gdn::k1::SMEM_BYTES_FP8 : gdn::k1::SMEM_BYTES;
+    void* args1[] = {&tm_k, &tm_v, &p1};
+    // split items wait for each other's partial sums: then all CTAs must be resident
+    const cudaError_t e1 =
+        sp.rem > 0 ? cudaLaunchCooperativeKernel(fn1, dim3(grid1), dim3(gdn::k1::THREADS), args1, smem1, stream)
+                   : cudaLaunchKernel(fn1, dim3(grid1), dim3(gdn::k1::THREADS), args1, smem1, stream);
+    if (e1 != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_LAUNCH;
     }
     // phases 2 and 3
     if (ev) cudaEventRecord(ev[1], stream);
@@ -379,6 +408,7 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
     p3.total = items * p3.ntile;
     p3.reverse = a.reverse;
     p3.norm_q = a.prologue;
+    p3.q_scale = a.fp8 ? a.q_scale : 1.0f;
     p3.wait_limit_ns = lim;
     const int n_scan = a.B * a.H * p2.rsplit;
     if (Rf != 0) {
@@ -387,9 +417,13 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
         int grid = n_scan + static_cast<int>(workers);
         int n_scan_arg = n_scan;
         void* args[] = {&tm_A, &tm_U, &tm_S_store, &tm_q, &tm_S_load, &tm_out, &p2, &p3, &flags, &n_scan_arg};
-        const void* fn = Rf == 16   ? reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<16>)
-                         : Rf == 32 ? reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<32>)
-                                    : reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<64>);
+        const void* fn =
+            a.fp8 ? (Rf == 16   ? reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<16, true>)
+                     : Rf == 32 ? reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<32, true>)
+                                : reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<64, true>))
+                  : (Rf == 16   ? reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<16, false>)
+                     : Rf == 32 ? reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<32, false>)
+                                : reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<64, false>));
         const size_t smem = Rf == 16 ? gdn::k23::smem_bytes<16>()
                              : Rf == 32 ? gdn::k23::smem_bytes<32>() : gdn::k23::smem_bytes<64>();
         if (ev) cudaEventRecord(ev[2], stream);
@@ -408,8 +442,13 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
             gdn::k2::scan_kernel<64><<<n_scan, gdn::k2::THREADS, gdn::k2::Cfg<64>::SMEM_BYTES, stream>>>(
                 tm_A, tm_U, tm_S_store, p2);
         if (ev) cudaEventRecord(ev[2], stream);
-        gdn::k3::output_kernel<<<static_cast<int>(std::min<long long>(p3.total, ds->sms)), gdn::k3::THREADS,
-                                 gdn::k3::SMEM_BYTES, stream>>>(tm_q, tm_S_load, tm_out, p3);
+        const int grid3 = static_cast<int>(std::min<long long>(p3.total, ds->sms));
+        if (a.fp8)
+            gdn::k3::output_kernel<true><<<grid3, gdn::k3::THREADS, gdn::k3::SMEM_BYTES, stream>>>(tm_q, tm_S_load,
+                                                                                                 tm_out, p3);
+        else
+            gdn::k3::output_kernel<false><<<grid3, gdn::k3::THREADS, gdn::k3::SMEM_BYTES, stream>>>(tm_q, tm_S_load,
+                                                                                                  tm_out, p3);
     }
     if (ev) cudaEventRecord(ev[3], stream);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
@@ -505,6 +544,33 @@ gdn_status gdn_frame_step_gated(const void* q, const void* k, const void* v, con
     PassArgs a{q, k, v, a_logit, b_logit, state_in, out, state_out, B, H, 1, N, dk, dv};
     a.prologue = 1;
     a.alpha_scale = alpha_scale;
+    return run_pass(a, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_frame_forward_fp8(const void* q, const void* k, const void* v, float q_scale, float k_scale,
+                                 float v_scale, const float* alpha, const float* beta, const float* state_in,
+                                 void* out, float* state_out, int B, int H, int F, int N, int dk, int dv,
+                                 gdn_stream_t stream) {
+    gdn_status s = validate(q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv, 1);
+    if (s != GDN_OK) return s;
+    PassArgs a{q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv};
+    a.fp8 = 1;
+    a.q_scale = q_scale;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    return run_pass(a, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_frame_step_fp8(const void* q, const void* k, const void* v, float q_scale, float k_scale,
+                              float v_scale, const float* alpha, const float* beta, const float* state_in, void* out,
+                              float* state_out, int B, int H, int N, int dk, int dv, gdn_stream_t stream) {
+    gdn_status s = validate(q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv, 1);
+    if (s != GDN_OK) return s;
+    PassArgs a{q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv};
+    a.fp8 = 1;
+    a.q_scale = q_scale;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     return run_pass(a, true, reinterpret_cast<cudaStream_t>(stream));
 }
 

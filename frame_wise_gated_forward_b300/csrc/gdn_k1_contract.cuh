@@ -69,8 +69,27 @@ constexpr int ACC_COLS = 256;
 // groups.
 constexpr uint32_t MN_LBO = BOX_BYTES;
 constexpr uint32_t MN_SBO = 1024;
-constexpr size_t SMEM_BYTES =
-    1024 /*align slack*/ + STAGES * STAGE_BYTES + BK_BUFS * TILE_BYTES + BETA_RING_BYTES + 256 /*barriers*/;
+// fp8 (e4m3) k and v: one 128-byte box (128 columns, zero-filled past d) per
+// token row and input, STAGES8-deep; the scalers decode each stage into a bf16
+// buffer [beta*K | K | V] that the MMA reads instead of the TMA tiles.
+constexpr int STAGES8 = 6;
+constexpr int BOX8_BYTES = CHUNK * 128;        // 64 token rows x 128 fp8
+constexpr int STAGE8_BYTES = 2 * BOX8_BYTES;   // K, V
+constexpr int CBUFS8 = 2;
+constexpr int CBUF8_BYTES = 3 * TILE_BYTES;    // beta*K | K | V, bf16
+template <bool FP8>
+struct Lay {
+    static constexpr int NST = FP8 ? STAGES8 : STAGES;              // TMA ring slots
+    static constexpr int ST_BYTES = FP8 ? STAGE8_BYTES : STAGE_BYTES;
+    static constexpr int NBK = FP8 ? CBUFS8 : BK_BUFS;              // MMA operand buffers
+    static constexpr int BK_BYTES = FP8 ? CBUF8_BYTES : TILE_BYTES;
+    static constexpr size_t SMEM =
+        1024 /*align slack*/ + NST * ST_BYTES + NBK * BK_BYTES + BETA_RING_BYTES + 256 /*barriers*/;
+    static_assert(SMEM <= 232448, "shared memory");
+    static_assert((2 * NST + 2 * NBK + 5) * 8 + 8 <= 256, "barrier area");
+};
+constexpr size_t SMEM_BYTES = Lay<false>::SMEM;
+constexpr size_t SMEM_BYTES_FP8 = Lay<true>::SMEM;
 
 struct Params {
     const float* beta;     // [B, F, N, H]
@@ -86,6 +105,8 @@ struct Params {
     int work;              // whole + (items - whole) * split_per
     int norm_k;            // fused prologue: k <- k / max(|k|, 1e-12) per (token, head)
     int beta_sigmoid;      // fused prologue: beta <- sigmoid(beta)
+    float a_scale;         // A = a_scale * D[:, :dk]  (fp8 inputs: k_scale^2; else 1)
+    float u_scale;         // U = u_scale * D[:, 128:] (fp8 inputs: k_scale * v_scale; else 1)
     unsigned long long wait_limit_ns;
 };
 
@@ -133,20 +154,23 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int w) {
     return u;
 }
 
+template <bool FP8>
 __global__ void __launch_bounds__(THREADS, 1)
     contract_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const Params p) {
+    using L = Lay<FP8>;
+    constexpr int NST = L::NST, NBK = L::NBK;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* stage_base = smem;                                   // [STAGES][K tile | V tile]
-    uint8_t* bk_base = smem + STAGES * STAGE_BYTES;               // [BK_BUFS][beta*K tile]
-    float* beta_ring = reinterpret_cast<float*>(bk_base + BK_BUFS * TILE_BYTES);  // [BETA_AHEAD+1][SCALER_THREADS]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(bk_base + BK_BUFS * TILE_BYTES + BETA_RING_BYTES);
-    uint64_t* full = bars;                          // [STAGES]  TMA landed K and V
-    uint64_t* empty = full + STAGES;                // [STAGES]  MMA finished reading the stage
-    uint64_t* bk_full = empty + STAGES;             // [BK_BUFS] beta*K written
-    uint64_t* bk_empty = bk_full + BK_BUFS;         // [BK_BUFS] MMA finished reading beta*K
-    uint64_t* tfull = bk_empty + BK_BUFS;           // [2]       accumulator ready
+    uint8_t* stage_base = smem;                                   // [NST][K tile | V tile]
+    uint8_t* bk_base = smem + NST * L::ST_BYTES;                  // [NBK][beta*K tile (| K | V when FP8)]
+    float* beta_ring = reinterpret_cast<float*>(bk_base + NBK * L::BK_BYTES);  // [BETA_AHEAD+1][SCALER_THREADS]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(bk_base + NBK * L::BK_BYTES + BETA_RING_BYTES);
+    uint64_t* full = bars;                          // [NST]  TMA landed K and V
+    uint64_t* empty = full + NST;                   // [NST]  stage consumed (MMA, or FP8 decoders)
+    uint64_t* bk_full = empty + NST;                // [NBK]  MMA operand buffer written
+    uint64_t* bk_empty = bk_full + NBK;             // [NBK]  MMA finished reading it
+    uint64_t* tfull = bk_empty + NBK;               // [2]       accumulator ready
     uint64_t* tempty = tfull + 2;                   // [2]       accumulator drained
     uint64_t* final_bar = tempty + 2;               // [1]       every issued MMA retired
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
@@ -164,15 +188,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     // Boxes that are never loaded (d <= 64) must read as 0; with d > 64 every
     // byte is written before it is read.
-    if (kboxes < 2 || vboxes < 2)
-        for (int i = threadIdx.x; i < (STAGES * STAGE_BYTES + BK_BUFS * TILE_BYTES) / 16; i += THREADS)
+    // (FP8: the decoders write every byte of every operand buffer.)
+    if (!FP8 && (kboxes < 2 || vboxes < 2))
+        for (int i = threadIdx.x; i < (NST * L::ST_BYTES + NBK * L::BK_BYTES) / 16; i += THREADS)
             reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], FP8 ? SCALER_THREADS : 1);
         }
-        for (int b = 0; b < BK_BUFS; ++b) {
+        for (int b = 0; b < NBK; ++b) {
             mbar_init(&bk_full[b], SCALER_THREADS);
             mbar_init(&bk_empty[b], 1);
         }
@@ -207,21 +232,27 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int frame = u.item / p.H, h = u.item % p.H;
                 for (int c = u.c_begin; c < u.c_end; ++c) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_limit_ns, abort_flag)) break;
-                    uint8_t* st = stage_base + stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full[stage], (kboxes + vboxes) * BOX_BYTES);
-                    for (int bx = 0; bx < kboxes; ++bx)
-                        tma_load_4d(st + bx * BOX_BYTES, &tm_k, &full[stage], 64 * bx, h, c * CHUNK, frame);
-                    for (int bx = 0; bx < vboxes; ++bx)
-                        tma_load_4d(st + TILE_BYTES + bx * BOX_BYTES, &tm_v, &full[stage], 64 * bx, h,
-                                    c * CHUNK, frame);
+                    uint8_t* st = stage_base + stage * L::ST_BYTES;
+                    if constexpr (FP8) {
+                        mbar_arrive_expect_tx(&full[stage], STAGE8_BYTES);
+                        tma_load_4d(st, &tm_k, &full[stage], 0, h, c * CHUNK, frame);
+                        tma_load_4d(st + BOX8_BYTES, &tm_v, &full[stage], 0, h, c * CHUNK, frame);
+                    } else {
+                        mbar_arrive_expect_tx(&full[stage], (kboxes + vboxes) * BOX_BYTES);
+                        for (int bx = 0; bx < kboxes; ++bx)
+                            tma_load_4d(st + bx * BOX_BYTES, &tm_k, &full[stage], 64 * bx, h, c * CHUNK, frame);
+                        for (int bx = 0; bx < vboxes; ++bx)
+                            tma_load_4d(st + TILE_BYTES + bx * BOX_BYTES, &tm_v, &full[stage], 64 * bx, h,
+                                        c * CHUNK, frame);
+                    }
                     ++issued;
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    if (++stage == NST) { stage = 0; phase ^= 1; }
                 }
             }
             // Drain: the most recent fill of every stage must have landed before exit
             // (only matters when a wait gave up; otherwise the MMA issuer consumed all).
-            for (long long kf = (issued > STAGES ? issued - STAGES : 0); kf < issued; ++kf)
-                mbar_wait_drain(&full[kf % STAGES], static_cast<uint32_t>((kf / STAGES) & 1), p.wait_limit_ns);
+            for (long long kf = (issued > NST ? issued - NST : 0); kf < issued; ++kf)
+                mbar_wait_drain(&full[kf % NST], static_cast<uint32_t>((kf / NST) & 1), p.wait_limit_ns);
         }
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
@@ -238,24 +269,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
                 bool ok = true;
                 for (int c = u.c_begin; c < u.c_end; ++c) {
-                    if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag) ||
+                    if ((!FP8 && !mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag)) ||
                         !mbar_wait(&bk_full[bk], bk_phase, p.wait_limit_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(bk_base + bk * TILE_BYTES);       // beta*K
-                    const uint32_t b_base = smem_u32(stage_base + stage * STAGE_BYTES); // [K | V]
+                    const uint32_t a_base = smem_u32(bk_base + bk * L::BK_BYTES);       // beta*K
+                    // [K | V]: the TMA stage, or (FP8) the decoded copy after beta*K
+                    const uint32_t b_base = FP8 ? a_base + TILE_BYTES : smem_u32(stage_base + stage * L::ST_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < CHUNK / 16; ++kk) {
                         const uint64_t ad = smem_desc(a_base + kk * 2048, MN_LBO, MN_SBO);
                         const uint64_t bd = smem_desc(b_base + kk * 2048, MN_LBO, MN_SBO);
                         mma_bf16(d_tmem, ad, bd, IDESC, (c > u.c_begin || kk > 0) ? 1u : 0u);
                     }
-                    mma_commit(&empty[stage]);
+                    if (!FP8) mma_commit(&empty[stage]);
                     mma_commit(&bk_empty[bk]);
-                    if (++bk == BK_BUFS) { bk = 0; bk_phase ^= 1; }
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    if (++bk == NBK) { bk = 0; bk_phase ^= 1; }
+                    if (++stage == NST) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
                 mma_commit(&tfull[acc]);
@@ -310,10 +342,49 @@ __global__ void __launch_bounds__(THREADS, 1)
                     ok = false;
                     break;
                 }
-                {
+                if constexpr (FP8) {
+                    // Thread pair (2r, 2r+1) owns token row r; this thread decodes the
+                    // row's 64 columns of box bx (fp8 chunks 4bx..4bx+3, 16 columns
+                    // each) of K and V to bf16 (exact: e4m3 has 3 mantissa bits) and
+                    // forms beta*k in fp32, rounded to bf16 once.
+                    const uint8_t* src = stage_base + stage * L::ST_BYTES + r * 128;
+                    uint8_t* dst = bk_base + bk * L::BK_BYTES + bx * BOX_BYTES + r * 128;
+                    const float sb = bval;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int c = 4 * bx + i;                    // fp8 chunk: columns 16c..16c+15
+                        const int so = (c ^ (r & 7)) << 4;           // 128-byte swizzle of the TMA box
+                        const uint4 k16 = *reinterpret_cast<const uint4*>(src + so);
+                        const uint4 v16 = *reinterpret_cast<const uint4*>(src + BOX8_BYTES + so);
+                        const uint32_t* kw = reinterpret_cast<const uint32_t*>(&k16);
+                        const uint32_t* vw = reinterpret_cast<const uint32_t*>(&v16);
+                        uint32_t kb[8], bkb[8], vb[8];
+#pragma unroll
+                        for (int wd = 0; wd < 4; ++wd) {
+                            const float2 k0 = e4m3x2_to_float2(static_cast<uint16_t>(kw[wd] & 0xffffu));
+                            const float2 k1 = e4m3x2_to_float2(static_cast<uint16_t>(kw[wd] >> 16));
+                            const float2 v0 = e4m3x2_to_float2(static_cast<uint16_t>(vw[wd] & 0xffffu));
+                            const float2 v1 = e4m3x2_to_float2(static_cast<uint16_t>(vw[wd] >> 16));
+                            kb[2 * wd] = pack_bf16x2(k0.x, k0.y);
+                            kb[2 * wd + 1] = pack_bf16x2(k1.x, k1.y);
+                            bkb[2 * wd] = pack_bf16x2(k0.x * sb, k0.y * sb);
+                            bkb[2 * wd + 1] = pack_bf16x2(k1.x * sb, k1.y * sb);
+                            vb[2 * wd] = pack_bf16x2(v0.x, v0.y);
+                            vb[2 * wd + 1] = pack_bf16x2(v1.x, v1.y);
+                        }
+                        // columns 16i..16i+15 of box bx = its bf16 chunks 2i and 2i+1
+                        const int o0 = ((2 * i) ^ (r & 7)) << 4, o1 = ((2 * i + 1) ^ (r & 7)) << 4;
+                        *reinterpret_cast<uint4*>(dst + o0) = make_uint4(bkb[0], bkb[1], bkb[2], bkb[3]);
+                        *reinterpret_cast<uint4*>(dst + o1) = make_uint4(bkb[4], bkb[5], bkb[6], bkb[7]);
+                        *reinterpret_cast<uint4*>(dst + TILE_BYTES + o0) = make_uint4(kb[0], kb[1], kb[2], kb[3]);
+                        *reinterpret_cast<uint4*>(dst + TILE_BYTES + o1) = make_uint4(kb[4], kb[5], kb[6], kb[7]);
+                        *reinterpret_cast<uint4*>(dst + 2 * TILE_BYTES + o0) = make_uint4(vb[0], vb[1], vb[2], vb[3]);
+                        *reinterpret_cast<uint4*>(dst + 2 * TILE_BYTES + o1) = make_uint4(vb[4], vb[5], vb[6], vb[7]);
+                    }
+                } else {
                     // thread pair (2r, 2r+1) owns token row r: box 0 and box 1 (64 columns each)
-                    uint8_t* src = stage_base + stage * STAGE_BYTES + bx * BOX_BYTES + r * 128;
-                    uint8_t* dst = bk_base + bk * TILE_BYTES + bx * BOX_BYTES + r * 128;
+                    uint8_t* src = stage_base + stage * L::ST_BYTES + bx * BOX_BYTES + r * 128;
+                    uint8_t* dst = bk_base + bk * L::BK_BYTES + bx * BOX_BYTES + r * 128;
                     const bool mine = bx < kboxes;
                     uint4 x[8];
 #pragma unroll
@@ -358,8 +429,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&bk_full[bk]);
-                if (++bk == BK_BUFS) { bk = 0; bk_phase ^= 1; }
-                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                if (FP8) mbar_arrive(&empty[stage]);   // the decoders were the stage's last readers
+                if (++bk == NBK) { bk = 0; bk_phase ^= 1; }
+                if (++stage == NST) { stage = 0; phase ^= 1; }
             }
             if (!ok) break;
         }
@@ -391,6 +463,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tmem_ld32(tbase + c0, r32);
                     tmem_wait_ld();
                     if (!jv) continue;
+                    if (FP8) {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) r32[t] = __float_as_uint(__uint_as_float(r32[t]) * p.a_scale);
+                    }
                     if (part == nullptr) {
                         __nv_bfloat16* Arow = p.A_ws + (static_cast<size_t>(u.item) * p.dk + j) * p.dk;
 #pragma unroll
@@ -418,6 +494,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint32_t r32[32];
                     tmem_ld32(tbase + 128 + c0, r32);
                     tmem_wait_ld();
+                    if (FP8) {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) r32[t] = __float_as_uint(__uint_as_float(r32[t]) * p.u_scale);
+                    }
                     if (jv) {
 #pragma unroll
                         for (int t = 0; t < 32; ++t)

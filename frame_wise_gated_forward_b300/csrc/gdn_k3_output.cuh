@@ -49,6 +49,13 @@ constexpr int OSTAGE_BYTES = 2 * OBOX_BYTES; // 32 rows x 128 columns
 constexpr int TMEM_COLS = 512;
 constexpr int NSLOTS = 2;                    // row-norm buffers (folded prologue)
 constexpr int BAR_BYTES = 256;
+// fp8 (e4m3) q: the third q slot's 32 KB hold two raw 128x128-byte TMA
+// tiles; warps 6-7 decode each into one of the two remaining bf16 slots.
+constexpr int RAW_BYTES = TILE_M * 128;
+constexpr int RSTAGES = 2;
+static_assert(RSTAGES * RAW_BYTES <= QTILE_BYTES, "raw fp8 tiles fit in one q slot");
+static_assert((2 * QSTAGES + 2 * SSTAGES + 2 * ACCS + 1 + 2 * NSLOTS + 2 * RSTAGES) * 8 + 8 <= BAR_BYTES,
+              "barrier area");
 constexpr size_t SMEM_BYTES =
     1024 + QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES + 4 * 2 * OSTAGE_BYTES + BAR_BYTES + NSLOTS * TILE_M * 4;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -59,6 +66,7 @@ struct Params {
     long long total;        // items * ntile
     int reverse;            // fused schedule: follow a scan that runs from frame F-1 down
     int norm_q;             // fused prologue: scale each output row by 1/max(|q_n|, eps)
+    float q_scale;          // fp8 q: o_n = q_scale * S q8_n  (1 otherwise)
     unsigned long long wait_limit_ns;
 };
 
@@ -100,11 +108,14 @@ struct Sched {
     }
 };
 
-// Bounded wait until the scan has published all slices of `item`'s state.
+// FP8: q is e4m3 (tm_q maps bytes, one 128-column box per token row).
+template <bool FP8>
 __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUtensorMap* tm_s,
                                             const CUtensorMap* tm_out, const Params& p, const Sched& sc,
                                             uint8_t* smem) {
+    constexpr int QS = FP8 ? 2 : QSTAGES;             // bf16 q slots the MMA reads
     uint8_t* qring = smem;
+    uint8_t* rawring = smem + 2 * QTILE_BYTES;        // FP8: [RSTAGES][RAW_BYTES] in the third slot
     uint8_t* sring = qring + QSTAGES * QTILE_BYTES;
     uint8_t* ostage = sring + SSTAGES * STILE_BYTES;   // [4 warps][2][OSTAGE_BYTES]
     uint64_t* bars = reinterpret_cast<uint64_t*>(ostage + 4 * 2 * OSTAGE_BYTES);
@@ -117,7 +128,9 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
     uint64_t* final_bar = tempty + ACCS;
     uint64_t* nready = final_bar + 1;                 // [NSLOTS] row norms of a tile written
     uint64_t* nfree = nready + NSLOTS;                // [NSLOTS] epilogue has read them
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(nfree + NSLOTS);
+    uint64_t* rfull = nfree + NSLOTS;                 // [RSTAGES] FP8: raw q tile landed
+    uint64_t* rempty = rfull + RSTAGES;               // [RSTAGES] FP8: raw q tile decoded
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rempty + RSTAGES);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     float* rnorm = reinterpret_cast<float*>(smem + QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES +
                                             4 * 2 * OSTAGE_BYTES + BAR_BYTES);   // [NSLOTS][TILE_M]
@@ -128,14 +141,19 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
     const int vboxes = p.dv > 64 ? 2 : 1;
 
     // never-loaded boxes (dk <= 64) must read as zero
-    if (kboxes < 2)
+    if (!FP8 && kboxes < 2)
         for (int i = threadIdx.x; i < (QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES) / 16; i += THREADS)
             reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
         // a q slot is released by the MMA commit and, with the folded prologue, by the norm threads
-        for (int s = 0; s < QSTAGES; ++s) {
-            mbar_init(&qfull[s], 1);
-            mbar_init(&qempty[s], 1 + (p.norm_q ? NORM_THREADS : 0));
+        // (FP8: a q slot is filled by the decoder threads, released by the MMA commit)
+        for (int s = 0; s < QS; ++s) {
+            mbar_init(&qfull[s], FP8 ? NORM_THREADS : 1);
+            mbar_init(&qempty[s], 1 + ((!FP8 && p.norm_q) ? NORM_THREADS : 0));
+        }
+        for (int s = 0; s < RSTAGES; ++s) {
+            mbar_init(&rfull[s], 1);
+            mbar_init(&rempty[s], NORM_THREADS);
         }
         for (int s = 0; s < SSTAGES; ++s) { mbar_init(&sfull[s], 1); mbar_init(&sempty[s], 1); }
         for (int a = 0; a < ACCS; ++a) {
@@ -186,17 +204,30 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
                                 static_cast<int>(item));
                 ++s_issued;
                 for (int nt = nb; nt < ne; ++nt) {
-                    if (!mbar_wait(&qempty[qs], qph ^ 1, p.wait_limit_ns, abort_flag)) { stop = true; break; }
-                    mbar_arrive_expect_tx(&qfull[qs], kboxes * BOX_BYTES);
-                    for (int bx = 0; bx < kboxes; ++bx)
-                        tma_load_4d(qring + qs * QTILE_BYTES + bx * BOX_BYTES, tm_q, &qfull[qs], 64 * bx, h,
-                                    nt * TILE_M, frame);
-                    ++q_issued;
-                    if (++qs == QSTAGES) { qs = 0; qph ^= 1; }
+                    if constexpr (FP8) {
+                        // raw e4m3 tile into the raw ring (qs/qph walk it here)
+                        if (!mbar_wait(&rempty[qs], qph ^ 1, p.wait_limit_ns, abort_flag)) { stop = true; break; }
+                        mbar_arrive_expect_tx(&rfull[qs], RAW_BYTES);
+                        tma_load_4d(rawring + qs * RAW_BYTES, tm_q, &rfull[qs], 0, h, nt * TILE_M, frame);
+                        ++q_issued;
+                        if (++qs == RSTAGES) { qs = 0; qph ^= 1; }
+                    } else {
+                        if (!mbar_wait(&qempty[qs], qph ^ 1, p.wait_limit_ns, abort_flag)) { stop = true; break; }
+                        mbar_arrive_expect_tx(&qfull[qs], kboxes * BOX_BYTES);
+                        for (int bx = 0; bx < kboxes; ++bx)
+                            tma_load_4d(qring + qs * QTILE_BYTES + bx * BOX_BYTES, tm_q, &qfull[qs], 64 * bx, h,
+                                        nt * TILE_M, frame);
+                        ++q_issued;
+                        if (++qs == QSTAGES) { qs = 0; qph ^= 1; }
+                    }
                 }
             }
-            for (long long kq = (q_issued > QSTAGES ? q_issued - QSTAGES : 0); kq < q_issued; ++kq)
-                mbar_wait_drain(&qfull[kq % QSTAGES], static_cast<uint32_t>((kq / QSTAGES) & 1), p.wait_limit_ns);
+            {
+                constexpr int NQ = FP8 ? RSTAGES : QSTAGES;
+                uint64_t* qf = FP8 ? rfull : qfull;
+                for (long long kq = (q_issued > NQ ? q_issued - NQ : 0); kq < q_issued; ++kq)
+                    mbar_wait_drain(&qf[kq % NQ], static_cast<uint32_t>((kq / NQ) & 1), p.wait_limit_ns);
+            }
             for (long long ks = (s_issued > SSTAGES ? s_issued - SSTAGES : 0); ks < s_issued; ++ks)
                 mbar_wait_drain(&sfull[ks % SSTAGES], static_cast<uint32_t>((ks / SSTAGES) & 1), p.wait_limit_ns);
         }
@@ -231,7 +262,7 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
                     mma_commit(&qempty[qs]);
                     mma_commit(&tfull[acc]);
                     if (nt + 1 == ne) mma_commit(&sempty[ss]);
-                    if (++qs == QSTAGES) { qs = 0; qph ^= 1; }
+                    if (++qs == QS) { qs = 0; qph ^= 1; }
                     if (++acc == ACCS) { acc = 0; aph ^= 1; }
                 }
             }
@@ -239,8 +270,59 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
             mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
         }
     } else if (warp >= 6) {
-        // ---------------------------------------------------------- q row norms
-        if (p.norm_q) {
+        if constexpr (FP8) {
+            // ------------------------------------------------ e4m3 q decoders
+            // rows t and t + 64 of each raw tile: 8 chunks of 16 columns each,
+            // decoded exactly to bf16 into the K-major, 128-byte-swizzled slot
+            const int t = threadIdx.x - 192;
+            int qs = 0, rs = 0;
+            uint32_t qph = 0, rph = 0;
+            long long item;
+            int nb, ne;
+            bool stop = false;
+            for (int k = 0; !stop && !*abort_flag && sc.segment(p, k, item, nb, ne); ++k) {
+                for (int nt = nb; nt < ne; ++nt) {
+                    if (!mbar_wait(&rfull[rs], rph, p.wait_limit_ns, abort_flag) ||
+                        !mbar_wait(&qempty[qs], qph ^ 1, p.wait_limit_ns, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    const uint8_t* raw = rawring + rs * RAW_BYTES;
+                    uint8_t* tile = qring + qs * QTILE_BYTES;
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int row = t + 64 * h2;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 q16 =
+                                *reinterpret_cast<const uint4*>(raw + row * 128 + ((c ^ (row & 7)) << 4));
+                            const uint32_t* qw = reinterpret_cast<const uint32_t*>(&q16);
+                            uint32_t qb[8];
+#pragma unroll
+                            for (int wd = 0; wd < 4; ++wd) {
+                                const float2 a = e4m3x2_to_float2(static_cast<uint16_t>(qw[wd] & 0xffffu));
+                                const float2 b = e4m3x2_to_float2(static_cast<uint16_t>(qw[wd] >> 16));
+                                qb[2 * wd] = pack_bf16x2(a.x, a.y);
+                                qb[2 * wd + 1] = pack_bf16x2(b.x, b.y);
+                            }
+                            // columns 16c..16c+15 = bf16 box c/4, chunks 2(c%4) and 2(c%4)+1
+                            uint8_t* rowp = tile + (c >> 2) * BOX_BYTES + row * 128;
+                            const int c8 = 2 * (c & 3);
+                            *reinterpret_cast<uint4*>(rowp + ((c8 ^ (row & 7)) << 4)) =
+                                make_uint4(qb[0], qb[1], qb[2], qb[3]);
+                            *reinterpret_cast<uint4*>(rowp + (((c8 + 1) ^ (row & 7)) << 4)) =
+                                make_uint4(qb[4], qb[5], qb[6], qb[7]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&qfull[qs]);
+                    mbar_arrive(&rempty[rs]);
+                    if (++qs == QS) { qs = 0; qph ^= 1; }
+                    if (++rs == RSTAGES) { rs = 0; rph ^= 1; }
+                }
+            }
+        } else if (p.norm_q) {
+            // ---------------------------------------------------------- q row norms
             const int t = threadIdx.x - 192;  // 0..63: rows t and t + 64 of each tile
             int qs = 0, ns = 0;
             uint32_t qph = 0, nph = 0;
@@ -298,8 +380,8 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
             const int frame = static_cast<int>(item / p.H), h = static_cast<int>(item % p.H);
             for (int nt = nb; nt < ne; ++nt) {
                 // fused prologue: o_n = S q_n / max(|q_n|, eps), norms from the norm warps
-                float rs = 1.0f;
-                if (p.norm_q) {
+                float rs = FP8 ? p.q_scale : 1.0f;
+                if (!FP8 && p.norm_q) {
                     const bool okn =
                         __all_sync(0xffffffffu, mbar_wait(&nready[ns], nph, p.wait_limit_ns, abort_flag));
                     if (!okn) { stop = true; break; }
@@ -368,6 +450,7 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
 }
 
 // Standalone phase 3: persistent grid, contiguous tile ranges.
+template <bool FP8>
 __global__ void __launch_bounds__(THREADS, 1)
     output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
                   const __grid_constant__ CUtensorMap tm_out, const Params p) {
@@ -381,7 +464,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     sc.fused = false;
     sc.flags = nullptr;
     sc.flag_target = 0;
-    output_role(&tm_q, &tm_s, &tm_out, p, sc, smem);
+    output_role<FP8>(&tm_q, &tm_s, &tm_out, p, sc, smem);
 }
 
 }  // namespace k3

@@ -19,6 +19,9 @@ is fixed as q, k, v, beta, alpha, S_0):
   beta  = sigmoid(N(0, 1)) / N                      fp32 [B, F, N, H]
   alpha = exp(-softplus(N(0, 1)) * 0.05)            fp32 [B, F, H]  (no clamp)
   S_0   = 0, or N(0, 0.01) read as variance 0.01 (std 0.1), fp32 [B, H, dv, dk]
+For the 8-bit entry points (draw_fp8) q, k and v are instead quantized to
+OCP FP8 E4M3 with one fp32 scale per tensor (amax / 448, round to nearest
+even).
 """
 from __future__ import annotations
 
@@ -61,9 +64,8 @@ WORKLOADS = {
 }
 
 
-def draw(B: int, H: int, F: int, N: int, dk: int, dv: int, seed: int,
-         s0_std: float = 0.0) -> dict:
-    """Draw one set of inputs (all batch rows from one generator)."""
+def _draw_f32(B, H, F, N, dk, dv, seed, s0_std):
+    """The fp32 draws shared by draw() and draw_fp8(): q, k L2-normalised."""
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
     q = torch.randn((B, F, N, H, dk), generator=g, dtype=torch.float32)
@@ -75,13 +77,45 @@ def draw(B: int, H: int, F: int, N: int, dk: int, dv: int, seed: int,
         s0 = torch.randn((B, H, dv, dk), generator=g, dtype=torch.float32) * s0_std
     else:
         s0 = torch.zeros((B, H, dv, dk), dtype=torch.float32)
-    q = torch.nn.functional.normalize(q, dim=-1).to(torch.bfloat16)
-    k = torch.nn.functional.normalize(k, dim=-1).to(torch.bfloat16)
-    v = v.to(torch.bfloat16)
+    q = torch.nn.functional.normalize(q, dim=-1)
+    k = torch.nn.functional.normalize(k, dim=-1)
     beta = torch.sigmoid(braw) / float(max(N, 1))
     alpha = torch.exp(-torch.nn.functional.softplus(araw) * 0.05)
-    return {"q": q, "k": k, "v": v, "alpha": alpha.contiguous(),
-            "beta": beta.contiguous(), "state_in": s0.contiguous()}
+    return q, k, v, alpha.contiguous(), beta.contiguous(), s0.contiguous()
+
+
+def draw(B: int, H: int, F: int, N: int, dk: int, dv: int, seed: int,
+         s0_std: float = 0.0) -> dict:
+    """Draw one set of inputs (all batch rows from one generator)."""
+    q, k, v, alpha, beta, s0 = _draw_f32(B, H, F, N, dk, dv, seed, s0_std)
+    return {"q": q.to(torch.bfloat16), "k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16),
+            "alpha": alpha, "beta": beta, "state_in": s0}
+
+
+E4M3_MAX = 448.0
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor scaled OCP FP8 E4M3: scale = amax / 448 (fp32), codes =
+    round-to-nearest-even(x / scale) as torch.float8_e4m3fn, returned as
+    their uint8 bytes.  Input preparation only: the method itself never
+    quantizes."""
+    amax = float(x.abs().max())
+    scale = amax / E4M3_MAX if amax > 0.0 else 1.0
+    codes = (x / scale).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+    return codes, float(scale)
+
+
+def draw_fp8(B: int, H: int, F: int, N: int, dk: int, dv: int, seed: int,
+             s0_std: float = 0.0) -> dict:
+    """The draws of draw() with q, k and v quantized to per-tensor-scaled
+    e4m3 instead of rounded to bf16 (same generator sequence)."""
+    q, k, v, alpha, beta, s0 = _draw_f32(B, H, F, N, dk, dv, seed, s0_std)
+    q8, sq = quantize_e4m3(q)
+    k8, sk = quantize_e4m3(k)
+    v8, sv = quantize_e4m3(v)
+    return {"q8": q8, "k8": k8, "v8": v8, "q_scale": sq, "k_scale": sk, "v_scale": sv,
+            "alpha": alpha, "beta": beta, "state_in": s0}
 
 
 def workload_inputs(w: Workload) -> dict:

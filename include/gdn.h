@@ -127,6 +127,35 @@ gdn_status gdn_frame_step_gated(const void* q, const void* k, const void* v,
                                 gdn_stream_t stream);
 
 /*
+ * Forward with 8-bit inputs.  The SANA-WM article ("NVIDIA's New 2.6B World
+ * Model...", intro) deploys a distilled variant with NVFP4 quantization; the
+ * pages do not say which tensors are quantized or how.  This entry point
+ * takes q, k and v as OCP FP8 E4M3 bytes (1 sign, 4 exponent bits with bias
+ * 7, 3 mantissa bits; code 0x7F/0xFF is NaN) with one fp32 scale per tensor:
+ * the value of element x is scale * e4m3(x).  Layouts as gdn_frame_forward
+ * with one byte per element (q, k: [B, F, N, H, dk]; v: [B, F, N, H, dv]);
+ * out stays bf16 and the state fp32.  The recurrence is exactly that of
+ * gdn_frame_forward on the decoded values.  The kernels decode in shared
+ * memory (exactly, to bf16) and fold the scales into A, U and out, so HBM
+ * carries one byte per input element.  Validation and errors as
+ * gdn_frame_forward (q, k, v, out 16-byte aligned).
+ */
+gdn_status gdn_frame_forward_fp8(const void* q, const void* k, const void* v,
+                                 float q_scale, float k_scale, float v_scale,
+                                 const float* alpha, const float* beta,
+                                 const float* state_in, void* out, float* state_out,
+                                 int B, int H, int F, int N, int dk, int dv,
+                                 gdn_stream_t stream);
+
+/* gdn_frame_step with the 8-bit inputs of gdn_frame_forward_fp8. */
+gdn_status gdn_frame_step_fp8(const void* q, const void* k, const void* v,
+                              float q_scale, float k_scale, float v_scale,
+                              const float* alpha, const float* beta,
+                              const float* state_in, void* out, float* state_out,
+                              int B, int H, int N, int dk, int dv,
+                              gdn_stream_t stream);
+
+/*
  * One-frame step for interactive rollout (WorldFoundry model card, "What it
  * is for": a resident pipeline that advances in native 8k+1 windows): the same
  * operation with F = 1 on a resident state.

@@ -184,6 +184,42 @@ def prologue(q_raw, k_raw, a_logit, b_logit, alpha_scale):
     return qn, kn, alpha, beta
 
 
+def decode_e4m3(codes) -> np.ndarray:
+    """OCP FP8 E4M3 codes (uint8) -> fp64 values, from the format's definition:
+    bit 7 sign s, bits 6..3 exponent e (bias 7), bits 2..0 mantissa m;
+        e == 0:              (-1)^s * (m / 8) * 2^-6        (zero and subnormals)
+        e == 15 and m == 7:  NaN                             (no infinities)
+        otherwise:           (-1)^s * (1 + m / 8) * 2^(e - 7)
+    Accepts a uint8 numpy array or torch tensor (uint8 or float8_e4m3fn)."""
+    try:
+        import torch
+        if isinstance(codes, torch.Tensor):
+            t = codes.detach().cpu()
+            if t.dtype != torch.uint8:
+                t = t.view(torch.uint8)
+            codes = t.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    s = (c >> 7) & 1
+    e = (c >> 3) & 15
+    m = c & 7
+    sign = np.where(s == 1, -1.0, 1.0)
+    val = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    val = sign * val
+    return np.where((e == 15) & (m == 7), np.nan, val)
+
+
+def frame_forward_fp8(q8, k8, v8, q_scale, k_scale, v_scale, alpha, beta, state_in=None, *, B, H, F, N,
+                      dk, dv, **kw):
+    """The forward on 8-bit inputs: every element's value is scale * e4m3(code)
+    (one fp32 scale per tensor), then exactly frame_forward_f64 on those values."""
+    q = None if q8 is None else decode_e4m3(q8) * float(q_scale)
+    k = decode_e4m3(k8) * float(k_scale)
+    v = decode_e4m3(v8) * float(v_scale)
+    return frame_forward_f64(q, k, v, alpha, beta, state_in, B=B, H=H, F=F, N=N, dk=dk, dv=dv, **kw)
+
+
 def frame_forward_f64(q, k, v, alpha, beta, state_in=None, *, B, H, F, N, dk, dv,
                       want_out=True, want_states=False, sample_tokens=None,
                       mode=MODE_GDN, n_threads=0):

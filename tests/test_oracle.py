@@ -347,3 +347,49 @@ def test_f64_entry_equals_bf16_entry():
                                    s0.double().numpy(), B=B, H=H, F=F, N=N, dk=dk, dv=dv)
     np.testing.assert_array_equal(r64["out"], r16["out"])
     np.testing.assert_array_equal(r64["state"], r16["state"])
+
+
+def test_e4m3_decoder_pins():
+    """The oracle's e4m3 decoder against values the OCP FP8 format fixes, and
+    against torch's own float8_e4m3fn conversion for all 256 codes."""
+    spot = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x30: 0.5, 0x38: 1.0,
+            0x39: 1.125, 0x40: 2.0, 0x7E: 448.0, 0x80: -0.0, 0xB8: -1.0, 0xFE: -448.0}
+    codes = np.array(list(spot), dtype=np.uint8)
+    np.testing.assert_array_equal(oracle.decode_e4m3(codes), np.array(list(spot.values())))
+    assert np.isnan(oracle.decode_e4m3(np.array([0x7F, 0xFF], dtype=np.uint8))).all()
+    every = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(every.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.decode_e4m3(every)
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[ok], ref[ok])
+    # positive codes increase strictly; the sign bit only flips the sign
+    pos = got[:0x7F]
+    assert (np.diff(pos) > 0).all()
+    np.testing.assert_array_equal(got[0x80:0xFF], -got[:0x7F])
+
+
+def test_fp8_forward_equals_bf16_forward_on_shared_values():
+    """Every e4m3 value times a power-of-two scale is a bf16 value, so the fp8
+    entry (e4m3 decoder) and the bf16 entry (bf16 decoder) see the same
+    numbers and must agree exactly."""
+    B, H, F, N, dk, dv = 1, 2, 3, 7, 16, 16
+    g = torch.Generator().manual_seed(77)
+    q8 = torch.randint(0, 0x7F, (B, F, N, H, dk), generator=g, dtype=torch.uint8) | \
+        (torch.randint(0, 2, (B, F, N, H, dk), generator=g, dtype=torch.uint8) << 7)
+    k8 = torch.randint(0x20, 0x50, (B, F, N, H, dk), generator=g, dtype=torch.uint8)
+    v8 = torch.randint(0, 0x7F, (B, F, N, H, dv), generator=g, dtype=torch.uint8)
+    sq, sk, sv = 2.0 ** -3, 2.0 ** -6, 0.5
+    beta = torch.rand((B, F, N, H), generator=g) / N
+    alpha = 0.8 + 0.2 * torch.rand((B, F, H), generator=g)
+    s0 = torch.randn((B, H, dv, dk), generator=g) * 0.3
+    r8 = oracle.frame_forward_fp8(q8, k8, v8, sq, sk, sv, alpha, beta, s0, B=B, H=H, F=F, N=N, dk=dk, dv=dv)
+
+    def as_bf16(c, s):
+        t = c.view(torch.float8_e4m3fn).to(torch.float32) * s
+        b = t.to(torch.bfloat16)
+        assert torch.equal(b.to(torch.float32), t)  # exactly representable
+        return b
+    r16 = run(as_bf16(q8, sq), as_bf16(k8, sk), as_bf16(v8, sv), alpha, beta, s0)
+    np.testing.assert_array_equal(r8["out"], r16["out"])
+    np.testing.assert_array_equal(r8["state"], r16["state"])
