@@ -16,6 +16,7 @@ STATUS = {
     0: "GDN_OK", 1: "GDN_ERR_NULL_PTR", 2: "GDN_ERR_BAD_DIM", 3: "GDN_ERR_UNSUPPORTED",
     4: "GDN_ERR_MISALIGNED", 5: "GDN_ERR_ALLOC", 6: "GDN_ERR_LAUNCH", 7: "GDN_ERR_TIMEOUT",
     8: "GDN_ERR_ALIAS", 9: "GDN_ERR_NO_DEVICE", 10: "GDN_ERR_TOO_LARGE",
+    11: "GDN_ERR_RANGE",
 }
 EXPORTS = (
     "gdn_frame_forward", "gdn_frame_forward_reverse", "gdn_frame_step", "gdn_frame_forward_timed",

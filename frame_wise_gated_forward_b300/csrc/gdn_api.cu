@@ -427,7 +427,8 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
         const size_t smem = Rf == 16 ? gdn::k23::smem_bytes<16>()
                              : Rf == 32 ? gdn::k23::smem_bytes<32>() : gdn::k23::smem_bytes<64>();
         if (ev) cudaEventRecord(ev[2], stream);
-        if (cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(gdn::k23::THREADS), args, smem, stream) != cudaSuccess) {
+        const int threads = a.fp8 ? gdn::k3::threads<true>() : gdn::k3::threads<false>();
+        if (cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(threads), args, smem, stream) != cudaSuccess) {
             cudaGetLastError();
             return GDN_ERR_LAUNCH;
         }
@@ -444,8 +445,8 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
         if (ev) cudaEventRecord(ev[2], stream);
         const int grid3 = static_cast<int>(std::min<long long>(p3.total, ds->sms));
         if (a.fp8)
-            gdn::k3::output_kernel<true><<<grid3, gdn::k3::THREADS, gdn::k3::SMEM_BYTES, stream>>>(tm_q, tm_S_load,
-                                                                                                 tm_out, p3);
+            gdn::k3::output_kernel<true><<<grid3, gdn::k3::threads<true>(), gdn::k3::SMEM_BYTES, stream>>>(
+                tm_q, tm_S_load, tm_out, p3);
         else
             gdn::k3::output_kernel<false><<<grid3, gdn::k3::THREADS, gdn::k3::SMEM_BYTES, stream>>>(tm_q, tm_S_load,
                                                                                                   tm_out, p3);
@@ -671,6 +672,7 @@ const char* gdn_status_string(gdn_status s) {
         case GDN_ERR_ALIAS: return "GDN_ERR_ALIAS: an output overlaps an input";
         case GDN_ERR_NO_DEVICE: return "GDN_ERR_NO_DEVICE: no usable sm_103 device is current";
         case GDN_ERR_TOO_LARGE: return "GDN_ERR_TOO_LARGE: the step needs more scratch than GDN_STEP_NOALLOC_SCRATCH_BYTES";
+        case GDN_ERR_RANGE: return "GDN_ERR_RANGE: an input value is outside the entry point's range";
     }
     return "GDN_ERR_UNKNOWN";
 }

@@ -70,13 +70,18 @@ constexpr int ACC_COLS = 256;
 constexpr uint32_t MN_LBO = BOX_BYTES;
 constexpr uint32_t MN_SBO = 1024;
 // fp8 (e4m3) k and v: one 128-byte box (128 columns, zero-filled past d) per
-// token row and input, STAGES8-deep; the scalers decode each stage into a bf16
-// buffer [beta*K | K | V] that the MMA reads instead of the TMA tiles.
+// token row and input, STAGES8-deep; the scalers decode each stage into an f16
+// buffer [beta*K | K | V] that the MMA (kind::f16 with f16 operands) reads
+// instead of the TMA tiles.  e4m3 -> f16 is exact and takes one conversion
+// per pair; beta*k is formed in f16 arithmetic, which needs |beta| * 448 to
+// stay below the f16 maximum: |beta| > FP8_BETA_MAX is reported as
+// GDN_ERR_RANGE.
 constexpr int STAGES8 = 6;
 constexpr int BOX8_BYTES = CHUNK * 128;        // 64 token rows x 128 fp8
 constexpr int STAGE8_BYTES = 2 * BOX8_BYTES;   // K, V
 constexpr int CBUFS8 = 2;
-constexpr int CBUF8_BYTES = 3 * TILE_BYTES;    // beta*K | K | V, bf16
+constexpr int CBUF8_BYTES = 3 * TILE_BYTES;    // beta*K | K | V, f16
+constexpr float FP8_BETA_MAX = 128.0f;
 template <bool FP8>
 struct Lay {
     static constexpr int NST = FP8 ? STAGES8 : STAGES;              // TMA ring slots
@@ -129,6 +134,21 @@ __device__ __forceinline__ uint4 bscale(uint4 x, const BSplit& s) {
         xs[e] = *reinterpret_cast<const uint32_t*>(&r2);
     }
     return x;
+}
+
+// The same split product on packed f16 pairs (fp8 inputs).
+struct HSplit {
+    __half2 hi, lo;
+};
+__device__ __forceinline__ HSplit hsplit(float s) {
+    const __half h = __float2half_rn(s);
+    const __half l = __float2half_rn(s - __half2float(h));
+    return HSplit{__halves2half2(h, h), __halves2half2(l, l)};
+}
+__device__ __forceinline__ uint32_t hscale(uint32_t x, const HSplit& s) {
+    const __half2 k2 = *reinterpret_cast<const __half2*>(&x);
+    const __half2 r2 = __hfma2(k2, s.hi, __hmul2(k2, s.lo));
+    return *reinterpret_cast<const uint32_t*>(&r2);
 }
 
 // Work units: the first `whole` items whole, then every remaining item split
@@ -257,7 +277,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t IDESC = idesc_bf16(128, 256, 1, 1);
+            constexpr uint32_t IDESC = FP8 ? idesc_f16(128, 256, 1, 1) : idesc_bf16(128, 256, 1, 1);
             int stage = 0, bk = 0;
             uint32_t phase = 0, bk_phase = 0;
             int acc = 0;
@@ -345,41 +365,41 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if constexpr (FP8) {
                     // Thread pair (2r, 2r+1) owns token row r; this thread decodes the
                     // row's 64 columns of box bx (fp8 chunks 4bx..4bx+3, 16 columns
-                    // each) of K and V to bf16 (exact: e4m3 has 3 mantissa bits) and
-                    // forms beta*k in fp32, rounded to bf16 once.
+                    // each) of K and V to f16 and forms beta*k = fma(k, hi, k*lo)
+                    // with beta = hi + lo split into two f16.
+                    if (!(fabsf(bval) <= FP8_BETA_MAX)) record_error(GDN_ERR_RANGE);
                     const uint8_t* src = stage_base + stage * L::ST_BYTES + r * 128;
                     uint8_t* dst = bk_base + bk * L::BK_BYTES + bx * BOX_BYTES + r * 128;
-                    const float sb = bval;
+                    const HSplit b2 = hsplit(bval);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i0 = 0; i0 < 4; ++i0) {
+                        // box 1 walks its chunks in the order 2,3,0,1 so that the 8 threads of
+                        // a quarter warp (4 rows x 2 boxes) hit 8 distinct bank groups
+                        const int i = bx ? (i0 ^ 2) : i0;
                         const int c = 4 * bx + i;                    // fp8 chunk: columns 16c..16c+15
                         const int so = (c ^ (r & 7)) << 4;           // 128-byte swizzle of the TMA box
                         const uint4 k16 = *reinterpret_cast<const uint4*>(src + so);
                         const uint4 v16 = *reinterpret_cast<const uint4*>(src + BOX8_BYTES + so);
                         const uint32_t* kw = reinterpret_cast<const uint32_t*>(&k16);
                         const uint32_t* vw = reinterpret_cast<const uint32_t*>(&v16);
-                        uint32_t kb[8], bkb[8], vb[8];
+                        uint32_t kh[8], bkh[8], vh[8];
 #pragma unroll
                         for (int wd = 0; wd < 4; ++wd) {
-                            const float2 k0 = e4m3x2_to_float2(static_cast<uint16_t>(kw[wd] & 0xffffu));
-                            const float2 k1 = e4m3x2_to_float2(static_cast<uint16_t>(kw[wd] >> 16));
-                            const float2 v0 = e4m3x2_to_float2(static_cast<uint16_t>(vw[wd] & 0xffffu));
-                            const float2 v1 = e4m3x2_to_float2(static_cast<uint16_t>(vw[wd] >> 16));
-                            kb[2 * wd] = pack_bf16x2(k0.x, k0.y);
-                            kb[2 * wd + 1] = pack_bf16x2(k1.x, k1.y);
-                            bkb[2 * wd] = pack_bf16x2(k0.x * sb, k0.y * sb);
-                            bkb[2 * wd + 1] = pack_bf16x2(k1.x * sb, k1.y * sb);
-                            vb[2 * wd] = pack_bf16x2(v0.x, v0.y);
-                            vb[2 * wd + 1] = pack_bf16x2(v1.x, v1.y);
+                            kh[2 * wd] = e4m3x2_to_f16x2(static_cast<uint16_t>(kw[wd] & 0xffffu));
+                            kh[2 * wd + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(kw[wd] >> 16));
+                            vh[2 * wd] = e4m3x2_to_f16x2(static_cast<uint16_t>(vw[wd] & 0xffffu));
+                            vh[2 * wd + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(vw[wd] >> 16));
+                            bkh[2 * wd] = hscale(kh[2 * wd], b2);
+                            bkh[2 * wd + 1] = hscale(kh[2 * wd + 1], b2);
                         }
-                        // columns 16i..16i+15 of box bx = its bf16 chunks 2i and 2i+1
+                        // columns 16i..16i+15 of box bx = its 16-bit chunks 2i and 2i+1
                         const int o0 = ((2 * i) ^ (r & 7)) << 4, o1 = ((2 * i + 1) ^ (r & 7)) << 4;
-                        *reinterpret_cast<uint4*>(dst + o0) = make_uint4(bkb[0], bkb[1], bkb[2], bkb[3]);
-                        *reinterpret_cast<uint4*>(dst + o1) = make_uint4(bkb[4], bkb[5], bkb[6], bkb[7]);
-                        *reinterpret_cast<uint4*>(dst + TILE_BYTES + o0) = make_uint4(kb[0], kb[1], kb[2], kb[3]);
-                        *reinterpret_cast<uint4*>(dst + TILE_BYTES + o1) = make_uint4(kb[4], kb[5], kb[6], kb[7]);
-                        *reinterpret_cast<uint4*>(dst + 2 * TILE_BYTES + o0) = make_uint4(vb[0], vb[1], vb[2], vb[3]);
-                        *reinterpret_cast<uint4*>(dst + 2 * TILE_BYTES + o1) = make_uint4(vb[4], vb[5], vb[6], vb[7]);
+                        *reinterpret_cast<uint4*>(dst + o0) = make_uint4(bkh[0], bkh[1], bkh[2], bkh[3]);
+                        *reinterpret_cast<uint4*>(dst + o1) = make_uint4(bkh[4], bkh[5], bkh[6], bkh[7]);
+                        *reinterpret_cast<uint4*>(dst + TILE_BYTES + o0) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
+                        *reinterpret_cast<uint4*>(dst + TILE_BYTES + o1) = make_uint4(kh[4], kh[5], kh[6], kh[7]);
+                        *reinterpret_cast<uint4*>(dst + 2 * TILE_BYTES + o0) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
+                        *reinterpret_cast<uint4*>(dst + 2 * TILE_BYTES + o1) = make_uint4(vh[4], vh[5], vh[6], vh[7]);
                     }
                 } else {
                     // thread pair (2r, 2r+1) owns token row r: box 0 and box 1 (64 columns each)
@@ -389,8 +409,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint4 x[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        // rotate the 16-byte chunk order so 8 consecutive rows hit 8 distinct bank groups
-                        const int off = ((i + r) & 7) << 4;
+                        // rotate the 16-byte chunk order by row, and by 4 more for box 1, so
+                        // the 8 threads of a quarter warp (4 rows x 2 boxes) hit 8 distinct
+                        // bank groups
+                        const int off = ((i + r + 4 * bx) & 7) << 4;
                         if (mine) x[i] = *reinterpret_cast<const uint4*>(src + off);
                         else x[i] = make_uint4(0, 0, 0, 0);
                     }
@@ -415,7 +437,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                             for (int i = 0; i < 8; ++i) {
                                 const uint4 y = bscale(x[i], n2);   // normalized k, the B operand
-                                *reinterpret_cast<uint4*>(src + (((i + r) & 7) << 4)) = y;
+                                *reinterpret_cast<uint4*>(src + (((i + r + 4 * bx) & 7) << 4)) = y;
                             }
                         }
                     }
@@ -424,7 +446,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const BSplit b2 = bsplit(sb);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            *reinterpret_cast<uint4*>(dst + (((i + r) & 7) << 4)) = bscale(x[i], b2);
+                            *reinterpret_cast<uint4*>(dst + (((i + r + 4 * bx) & 7) << 4)) = bscale(x[i], b2);
                     }
                 }
                 fence_proxy_async_smem();

@@ -31,7 +31,7 @@ constexpr size_t smem_bytes() {
 }
 
 template <int R, bool FP8>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(k3::threads<FP8>(), 1)
     scan_output_kernel(const __grid_constant__ CUtensorMap tm_A, const __grid_constant__ CUtensorMap tm_U,
                        const __grid_constant__ CUtensorMap tm_S_store, const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_S_load, const __grid_constant__ CUtensorMap tm_out,

@@ -50,7 +50,11 @@ constexpr int TMEM_COLS = 512;
 constexpr int NSLOTS = 2;                    // row-norm buffers (folded prologue)
 constexpr int BAR_BYTES = 256;
 // fp8 (e4m3) q: the third q slot's 32 KB hold two raw 128x128-byte TMA
-// tiles; warps 6-7 decode each into one of the two remaining bf16 slots.
+// tiles; four decoder warps (6-9, so the block has 320 threads) decode each
+// into one of the two remaining bf16 slots.
+constexpr int DEC_THREADS = 128;
+template <bool FP8>
+constexpr int threads() { return FP8 ? 192 + DEC_THREADS : THREADS; }
 constexpr int RAW_BYTES = TILE_M * 128;
 constexpr int RSTAGES = 2;
 static_assert(RSTAGES * RAW_BYTES <= QTILE_BYTES, "raw fp8 tiles fit in one q slot");
@@ -148,12 +152,12 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
         // a q slot is released by the MMA commit and, with the folded prologue, by the norm threads
         // (FP8: a q slot is filled by the decoder threads, released by the MMA commit)
         for (int s = 0; s < QS; ++s) {
-            mbar_init(&qfull[s], FP8 ? NORM_THREADS : 1);
+            mbar_init(&qfull[s], FP8 ? DEC_THREADS : 1);
             mbar_init(&qempty[s], 1 + ((!FP8 && p.norm_q) ? NORM_THREADS : 0));
         }
         for (int s = 0; s < RSTAGES; ++s) {
             mbar_init(&rfull[s], 1);
-            mbar_init(&rempty[s], NORM_THREADS);
+            mbar_init(&rempty[s], DEC_THREADS);
         }
         for (int s = 0; s < SSTAGES; ++s) { mbar_init(&sfull[s], 1); mbar_init(&sempty[s], 1); }
         for (int a = 0; a < ACCS; ++a) {
@@ -272,8 +276,8 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
     } else if (warp >= 6) {
         if constexpr (FP8) {
             // ------------------------------------------------ e4m3 q decoders
-            // rows t and t + 64 of each raw tile: 8 chunks of 16 columns each,
-            // decoded exactly to bf16 into the K-major, 128-byte-swizzled slot
+            // row t of each raw tile: 8 chunks of 16 columns each, decoded
+            // exactly to bf16 into the K-major, 128-byte-swizzled slot
             const int t = threadIdx.x - 192;
             int qs = 0, rs = 0;
             uint32_t qph = 0, rph = 0;
@@ -289,9 +293,8 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
                     }
                     const uint8_t* raw = rawring + rs * RAW_BYTES;
                     uint8_t* tile = qring + qs * QTILE_BYTES;
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int row = t + 64 * h2;
+                    {
+                        const int row = t;
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             const uint4 q16 =
@@ -300,10 +303,8 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
                             uint32_t qb[8];
 #pragma unroll
                             for (int wd = 0; wd < 4; ++wd) {
-                                const float2 a = e4m3x2_to_float2(static_cast<uint16_t>(qw[wd] & 0xffffu));
-                                const float2 b = e4m3x2_to_float2(static_cast<uint16_t>(qw[wd] >> 16));
-                                qb[2 * wd] = pack_bf16x2(a.x, a.y);
-                                qb[2 * wd + 1] = pack_bf16x2(b.x, b.y);
+                                qb[2 * wd] = e4m3x2_to_bf16x2(static_cast<uint16_t>(qw[wd] & 0xffffu));
+                                qb[2 * wd + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(qw[wd] >> 16));
                             }
                             // columns 16c..16c+15 = bf16 box c/4, chunks 2(c%4) and 2(c%4)+1
                             uint8_t* rowp = tile + (c >> 2) * BOX_BYTES + row * 128;
@@ -451,7 +452,7 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
 
 // Standalone phase 3: persistent grid, contiguous tile ranges.
 template <bool FP8>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(threads<FP8>(), 1)
     output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
                   const __grid_constant__ CUtensorMap tm_out, const Params p) {
     extern __shared__ uint8_t smem_raw[];

@@ -286,13 +286,31 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Two OCP FP8 E4M3 values (low byte first) -> two floats, exactly: the
-// hardware conversion to f16x2 is exact (every e4m3 value, subnormals
-// included, is an f16 value), and f16 -> f32 is exact.
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
+// Instruction descriptor, kind::f16 with f16 A/B and fp32 D, dense.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Two OCP FP8 E4M3 codes (low byte first) -> f16x2, exactly: every e4m3
+// value, subnormals included, is an f16 value (one conversion instruction).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
     uint32_t h2;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
-    return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+    return h2;
+}
+
+// Two OCP FP8 E4M3 codes -> bf16x2, exactly.  After the f16 conversion every
+// nonzero value is a normal f16 (the smallest e4m3 value, 2^-9, is above the
+// f16 normal range's 2^-14) with at most 3 mantissa bits, so per 16-bit half
+//     bf16 = sign | ((f16 & 0x7fff) >> 3) + (nonzero ? (127 - 15) << 7 : 0)
+// (exponent rebiased, mantissa truncated without loss).  Integer arithmetic
+// only, so the conversion unit is used once per pair.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
+    const uint32_t x = e4m3x2_to_f16x2(two);
+    const uint32_t y = (x >> 3) & 0x0fff0fffu;                      // exponent and mantissa per half
+    const uint32_t nz = ((y + 0x0fff0fffu) >> 12) & 0x00010001u;    // 1 in each nonzero half
+    return (y + nz * 0x3800u) | (x & 0x80008000u);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -63,7 +63,9 @@ typedef enum gdn_status {
     GDN_ERR_TIMEOUT = 7,      /* a device-side bounded wait ran out (sync_status) */
     GDN_ERR_ALIAS = 8,        /* out overlaps an input                             */
     GDN_ERR_NO_DEVICE = 9,    /* no usable sm_103 device is current               */
-    GDN_ERR_TOO_LARGE = 10    /* needs more than the fixed no-alloc scratch       */
+    GDN_ERR_TOO_LARGE = 10,   /* needs more than the fixed no-alloc scratch       */
+    GDN_ERR_RANGE = 11        /* an input value outside the entry point's range
+                                 (device-reported, via gdn_sync_status)           */
 } gdn_status;
 
 /*
