@@ -70,18 +70,21 @@ constexpr int ACC_COLS = 256;
 constexpr uint32_t MN_LBO = BOX_BYTES;
 constexpr uint32_t MN_SBO = 1024;
 // fp8 (e4m3) k and v: one 128-byte box (128 columns, zero-filled past d) per
-// token row and input, STAGES8-deep; the scalers decode each stage into an f16
-// buffer [beta*K | K | V] that the MMA (kind::f16 with f16 operands) reads
-// instead of the TMA tiles.  e4m3 -> f16 is exact and takes one conversion
-// per pair; beta*k is formed in f16 arithmetic, which needs |beta| * 448 to
-// stay below the f16 maximum: |beta| > FP8_BETA_MAX is reported as
-// GDN_ERR_RANGE.
-constexpr int STAGES8 = 6;
+// token row and input, STAGES8-deep.  The scalers decode each stage into one
+// f16 buffer [sqrt(beta) K | sqrt(beta) V] and the MMA (kind::f16, f16
+// operands) reads it as both operands,
+//     D = (sqrt(B) K)^T [sqrt(B) K | sqrt(B) V] = [K^T B K | (V^T B K)^T],
+// which writes a third less shared memory than separate beta*K, K and V
+// copies (the fp8 path is bound by shared-memory traffic, not HBM).  e4m3 ->
+// f16 is exact (one conversion per pair); the sqrt(beta) product is formed in
+// f16 arithmetic, so beta must lie in [0, FP8_BETA_MAX] (sqrt(beta) * 448 below
+// the f16 maximum); anything else is reported as GDN_ERR_RANGE.
+constexpr int STAGES8 = 7;
 constexpr int BOX8_BYTES = CHUNK * 128;        // 64 token rows x 128 fp8
 constexpr int STAGE8_BYTES = 2 * BOX8_BYTES;   // K, V
-constexpr int CBUFS8 = 2;
-constexpr int CBUF8_BYTES = 3 * TILE_BYTES;    // beta*K | K | V, f16
-constexpr float FP8_BETA_MAX = 128.0f;
+constexpr int CBUFS8 = 3;
+constexpr int CBUF8_BYTES = 2 * TILE_BYTES;    // sqrt(beta) K | sqrt(beta) V, f16
+constexpr float FP8_BETA_MAX = 16384.0f;
 template <bool FP8>
 struct Lay {
     static constexpr int NST = FP8 ? STAGES8 : STAGES;              // TMA ring slots
@@ -295,9 +298,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(bk_base + bk * L::BK_BYTES);       // beta*K
-                    // [K | V]: the TMA stage, or (FP8) the decoded copy after beta*K
-                    const uint32_t b_base = FP8 ? a_base + TILE_BYTES : smem_u32(stage_base + stage * L::ST_BYTES);
+                    // A = beta*K (FP8: sqrt(beta) K); B = [K | V] from the TMA stage, or (FP8)
+                    // [sqrt(beta) K | sqrt(beta) V], the same buffer as A
+                    const uint32_t a_base = smem_u32(bk_base + bk * L::BK_BYTES);
+                    const uint32_t b_base = FP8 ? a_base : smem_u32(stage_base + stage * L::ST_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < CHUNK / 16; ++kk) {
                         const uint64_t ad = smem_desc(a_base + kk * 2048, MN_LBO, MN_SBO);
@@ -365,12 +369,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if constexpr (FP8) {
                     // Thread pair (2r, 2r+1) owns token row r; this thread decodes the
                     // row's 64 columns of box bx (fp8 chunks 4bx..4bx+3, 16 columns
-                    // each) of K and V to f16 and forms beta*k = fma(k, hi, k*lo)
-                    // with beta = hi + lo split into two f16.
-                    if (!(fabsf(bval) <= FP8_BETA_MAX)) record_error(GDN_ERR_RANGE);
+                    // each) of K and V to f16 and scales them by sqrt(beta) =
+                    // hi + lo split into two f16: fma(x, hi, x*lo).
+                    if (!(bval >= 0.0f && bval <= FP8_BETA_MAX)) record_error(GDN_ERR_RANGE);
                     const uint8_t* src = stage_base + stage * L::ST_BYTES + r * 128;
                     uint8_t* dst = bk_base + bk * L::BK_BYTES + bx * BOX_BYTES + r * 128;
-                    const HSplit b2 = hsplit(bval);
+                    const HSplit b2 = hsplit(sqrtf(fmaxf(bval, 0.0f)));
 #pragma unroll
                     for (int i0 = 0; i0 < 4; ++i0) {
                         // box 1 walks its chunks in the order 2,3,0,1 so that the 8 threads of
@@ -382,24 +386,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const uint4 v16 = *reinterpret_cast<const uint4*>(src + BOX8_BYTES + so);
                         const uint32_t* kw = reinterpret_cast<const uint32_t*>(&k16);
                         const uint32_t* vw = reinterpret_cast<const uint32_t*>(&v16);
-                        uint32_t kh[8], bkh[8], vh[8];
+                        uint32_t kh[8], vh[8];
 #pragma unroll
                         for (int wd = 0; wd < 4; ++wd) {
-                            kh[2 * wd] = e4m3x2_to_f16x2(static_cast<uint16_t>(kw[wd] & 0xffffu));
-                            kh[2 * wd + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(kw[wd] >> 16));
-                            vh[2 * wd] = e4m3x2_to_f16x2(static_cast<uint16_t>(vw[wd] & 0xffffu));
-                            vh[2 * wd + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(vw[wd] >> 16));
-                            bkh[2 * wd] = hscale(kh[2 * wd], b2);
-                            bkh[2 * wd + 1] = hscale(kh[2 * wd + 1], b2);
+                            kh[2 * wd] = hscale(e4m3x2_to_f16x2(static_cast<uint16_t>(kw[wd] & 0xffffu)), b2);
+                            kh[2 * wd + 1] = hscale(e4m3x2_to_f16x2(static_cast<uint16_t>(kw[wd] >> 16)), b2);
+                            vh[2 * wd] = hscale(e4m3x2_to_f16x2(static_cast<uint16_t>(vw[wd] & 0xffffu)), b2);
+                            vh[2 * wd + 1] = hscale(e4m3x2_to_f16x2(static_cast<uint16_t>(vw[wd] >> 16)), b2);
                         }
                         // columns 16i..16i+15 of box bx = its 16-bit chunks 2i and 2i+1
                         const int o0 = ((2 * i) ^ (r & 7)) << 4, o1 = ((2 * i + 1) ^ (r & 7)) << 4;
-                        *reinterpret_cast<uint4*>(dst + o0) = make_uint4(bkh[0], bkh[1], bkh[2], bkh[3]);
-                        *reinterpret_cast<uint4*>(dst + o1) = make_uint4(bkh[4], bkh[5], bkh[6], bkh[7]);
-                        *reinterpret_cast<uint4*>(dst + TILE_BYTES + o0) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
-                        *reinterpret_cast<uint4*>(dst + TILE_BYTES + o1) = make_uint4(kh[4], kh[5], kh[6], kh[7]);
-                        *reinterpret_cast<uint4*>(dst + 2 * TILE_BYTES + o0) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
-                        *reinterpret_cast<uint4*>(dst + 2 * TILE_BYTES + o1) = make_uint4(vh[4], vh[5], vh[6], vh[7]);
+                        *reinterpret_cast<uint4*>(dst + o0) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
+                        *reinterpret_cast<uint4*>(dst + o1) = make_uint4(kh[4], kh[5], kh[6], kh[7]);
+                        *reinterpret_cast<uint4*>(dst + TILE_BYTES + o0) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
+                        *reinterpret_cast<uint4*>(dst + TILE_BYTES + o1) = make_uint4(vh[4], vh[5], vh[6], vh[7]);
                     }
                 } else {
                     // thread pair (2r, 2r+1) owns token row r: box 0 and box 1 (64 columns each)

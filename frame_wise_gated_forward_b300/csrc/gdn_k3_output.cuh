@@ -49,17 +49,17 @@ constexpr int OSTAGE_BYTES = 2 * OBOX_BYTES; // 32 rows x 128 columns
 constexpr int TMEM_COLS = 512;
 constexpr int NSLOTS = 2;                    // row-norm buffers (folded prologue)
 constexpr int BAR_BYTES = 256;
-// fp8 (e4m3) q: the third q slot's 32 KB hold two raw 128x128-byte TMA
-// tiles; four decoder warps (6-9, so the block has 320 threads) decode each
-// into one of the two remaining bf16 slots.
+// fp8 (e4m3) q: TMA loads the raw 128x128-byte tile into the upper half of a
+// q slot, and four decoder warps (6-9, so the block has 320 threads) decode
+// it in place into the slot's two bf16 boxes: each thread owns one token row,
+// reads its raw row whole before writing, and box 1's row is exactly the raw
+// row it came from, so no thread overwrites bytes another one still reads.
 constexpr int DEC_THREADS = 128;
 template <bool FP8>
 constexpr int threads() { return FP8 ? 192 + DEC_THREADS : THREADS; }
 constexpr int RAW_BYTES = TILE_M * 128;
-constexpr int RSTAGES = 2;
-static_assert(RSTAGES * RAW_BYTES <= QTILE_BYTES, "raw fp8 tiles fit in one q slot");
-static_assert((2 * QSTAGES + 2 * SSTAGES + 2 * ACCS + 1 + 2 * NSLOTS + 2 * RSTAGES) * 8 + 8 <= BAR_BYTES,
-              "barrier area");
+static_assert(RAW_BYTES == BOX_BYTES, "a raw fp8 tile fills box 1 of a q slot");
+static_assert((3 * QSTAGES + 2 * SSTAGES + 2 * ACCS + 1 + 2 * NSLOTS) * 8 + 8 <= BAR_BYTES, "barrier area");
 constexpr size_t SMEM_BYTES =
     1024 + QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES + 4 * 2 * OSTAGE_BYTES + BAR_BYTES + NSLOTS * TILE_M * 4;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -117,9 +117,8 @@ template <bool FP8>
 __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUtensorMap* tm_s,
                                             const CUtensorMap* tm_out, const Params& p, const Sched& sc,
                                             uint8_t* smem) {
-    constexpr int QS = FP8 ? 2 : QSTAGES;             // bf16 q slots the MMA reads
+    constexpr int QS = QSTAGES;
     uint8_t* qring = smem;
-    uint8_t* rawring = smem + 2 * QTILE_BYTES;        // FP8: [RSTAGES][RAW_BYTES] in the third slot
     uint8_t* sring = qring + QSTAGES * QTILE_BYTES;
     uint8_t* ostage = sring + SSTAGES * STILE_BYTES;   // [4 warps][2][OSTAGE_BYTES]
     uint64_t* bars = reinterpret_cast<uint64_t*>(ostage + 4 * 2 * OSTAGE_BYTES);
@@ -132,9 +131,8 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
     uint64_t* final_bar = tempty + ACCS;
     uint64_t* nready = final_bar + 1;                 // [NSLOTS] row norms of a tile written
     uint64_t* nfree = nready + NSLOTS;                // [NSLOTS] epilogue has read them
-    uint64_t* rfull = nfree + NSLOTS;                 // [RSTAGES] FP8: raw q tile landed
-    uint64_t* rempty = rfull + RSTAGES;               // [RSTAGES] FP8: raw q tile decoded
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rempty + RSTAGES);
+    uint64_t* qdec = nfree + NSLOTS;                  // [QSTAGES] FP8: q slot decoded (qfull: raw landed)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qdec + QSTAGES);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     float* rnorm = reinterpret_cast<float*>(smem + QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES +
                                             4 * 2 * OSTAGE_BYTES + BAR_BYTES);   // [NSLOTS][TILE_M]
@@ -150,14 +148,10 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
             reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
         // a q slot is released by the MMA commit and, with the folded prologue, by the norm threads
-        // (FP8: a q slot is filled by the decoder threads, released by the MMA commit)
         for (int s = 0; s < QS; ++s) {
-            mbar_init(&qfull[s], FP8 ? DEC_THREADS : 1);
+            mbar_init(&qfull[s], 1);
             mbar_init(&qempty[s], 1 + ((!FP8 && p.norm_q) ? NORM_THREADS : 0));
-        }
-        for (int s = 0; s < RSTAGES; ++s) {
-            mbar_init(&rfull[s], 1);
-            mbar_init(&rempty[s], DEC_THREADS);
+            mbar_init(&qdec[s], DEC_THREADS);
         }
         for (int s = 0; s < SSTAGES; ++s) { mbar_init(&sfull[s], 1); mbar_init(&sempty[s], 1); }
         for (int a = 0; a < ACCS; ++a) {
@@ -209,12 +203,13 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
                 ++s_issued;
                 for (int nt = nb; nt < ne; ++nt) {
                     if constexpr (FP8) {
-                        // raw e4m3 tile into the raw ring (qs/qph walk it here)
-                        if (!mbar_wait(&rempty[qs], qph ^ 1, p.wait_limit_ns, abort_flag)) { stop = true; break; }
-                        mbar_arrive_expect_tx(&rfull[qs], RAW_BYTES);
-                        tma_load_4d(rawring + qs * RAW_BYTES, tm_q, &rfull[qs], 0, h, nt * TILE_M, frame);
+                        // raw e4m3 tile into box 1 of the slot, decoded there in place
+                        if (!mbar_wait(&qempty[qs], qph ^ 1, p.wait_limit_ns, abort_flag)) { stop = true; break; }
+                        mbar_arrive_expect_tx(&qfull[qs], RAW_BYTES);
+                        tma_load_4d(qring + qs * QTILE_BYTES + BOX_BYTES, tm_q, &qfull[qs], 0, h, nt * TILE_M,
+                                    frame);
                         ++q_issued;
-                        if (++qs == RSTAGES) { qs = 0; qph ^= 1; }
+                        if (++qs == QS) { qs = 0; qph ^= 1; }
                     } else {
                         if (!mbar_wait(&qempty[qs], qph ^ 1, p.wait_limit_ns, abort_flag)) { stop = true; break; }
                         mbar_arrive_expect_tx(&qfull[qs], kboxes * BOX_BYTES);
@@ -226,12 +221,8 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
                     }
                 }
             }
-            {
-                constexpr int NQ = FP8 ? RSTAGES : QSTAGES;
-                uint64_t* qf = FP8 ? rfull : qfull;
-                for (long long kq = (q_issued > NQ ? q_issued - NQ : 0); kq < q_issued; ++kq)
-                    mbar_wait_drain(&qf[kq % NQ], static_cast<uint32_t>((kq / NQ) & 1), p.wait_limit_ns);
-            }
+            for (long long kq = (q_issued > QS ? q_issued - QS : 0); kq < q_issued; ++kq)
+                mbar_wait_drain(&qfull[kq % QS], static_cast<uint32_t>((kq / QS) & 1), p.wait_limit_ns);
             for (long long ks = (s_issued > SSTAGES ? s_issued - SSTAGES : 0); ks < s_issued; ++ks)
                 mbar_wait_drain(&sfull[ks % SSTAGES], static_cast<uint32_t>((ks / SSTAGES) & 1), p.wait_limit_ns);
         }
@@ -250,7 +241,7 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
                 if (!mbar_wait(&sfull[ss], sph, p.wait_limit_ns, abort_flag)) break;
                 for (int nt = nb; nt < ne; ++nt) {
                     if (!mbar_wait(&tempty[acc], aph ^ 1, p.wait_limit_ns, abort_flag) ||
-                        !mbar_wait(&qfull[qs], qph, p.wait_limit_ns, abort_flag)) {
+                        !mbar_wait(FP8 ? &qdec[qs] : &qfull[qs], qph, p.wait_limit_ns, abort_flag)) {
                         stop = true;
                         break;
                     }
@@ -276,50 +267,46 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
     } else if (warp >= 6) {
         if constexpr (FP8) {
             // ------------------------------------------------ e4m3 q decoders
-            // row t of each raw tile: 8 chunks of 16 columns each, decoded
-            // exactly to bf16 into the K-major, 128-byte-swizzled slot
+            // row t of each raw tile (box 1 of the slot): 8 chunks of 16 columns,
+            // all read first, then decoded exactly to bf16 into row t of the
+            // slot's K-major, 128-byte-swizzled boxes 0 and 1
             const int t = threadIdx.x - 192;
-            int qs = 0, rs = 0;
-            uint32_t qph = 0, rph = 0;
+            int qs = 0;
+            uint32_t qph = 0;
             long long item;
             int nb, ne;
             bool stop = false;
             for (int k = 0; !stop && !*abort_flag && sc.segment(p, k, item, nb, ne); ++k) {
                 for (int nt = nb; nt < ne; ++nt) {
-                    if (!mbar_wait(&rfull[rs], rph, p.wait_limit_ns, abort_flag) ||
-                        !mbar_wait(&qempty[qs], qph ^ 1, p.wait_limit_ns, abort_flag)) {
+                    if (!mbar_wait(&qfull[qs], qph, p.wait_limit_ns, abort_flag)) {
                         stop = true;
                         break;
                     }
-                    const uint8_t* raw = rawring + rs * RAW_BYTES;
                     uint8_t* tile = qring + qs * QTILE_BYTES;
-                    {
-                        const int row = t;
+                    const int row = t;
+                    uint4 q16[8];
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const uint4 q16 =
-                                *reinterpret_cast<const uint4*>(raw + row * 128 + ((c ^ (row & 7)) << 4));
-                            const uint32_t* qw = reinterpret_cast<const uint32_t*>(&q16);
-                            uint32_t qb[8];
+                    for (int c = 0; c < 8; ++c)
+                        q16[c] = *reinterpret_cast<const uint4*>(tile + BOX_BYTES + row * 128 + ((c ^ (row & 7)) << 4));
 #pragma unroll
-                            for (int wd = 0; wd < 4; ++wd) {
-                                qb[2 * wd] = e4m3x2_to_bf16x2(static_cast<uint16_t>(qw[wd] & 0xffffu));
-                                qb[2 * wd + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(qw[wd] >> 16));
-                            }
-                            // columns 16c..16c+15 = bf16 box c/4, chunks 2(c%4) and 2(c%4)+1
-                            uint8_t* rowp = tile + (c >> 2) * BOX_BYTES + row * 128;
-                            const int c8 = 2 * (c & 3);
-                            *reinterpret_cast<uint4*>(rowp + ((c8 ^ (row & 7)) << 4)) =
-                                make_uint4(qb[0], qb[1], qb[2], qb[3]);
-                            *reinterpret_cast<uint4*>(rowp + (((c8 + 1) ^ (row & 7)) << 4)) =
-                                make_uint4(qb[4], qb[5], qb[6], qb[7]);
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t* qw = reinterpret_cast<const uint32_t*>(&q16[c]);
+                        uint32_t qb[8];
+#pragma unroll
+                        for (int wd = 0; wd < 4; ++wd) {
+                            qb[2 * wd] = e4m3x2_to_bf16x2(static_cast<uint16_t>(qw[wd] & 0xffffu));
+                            qb[2 * wd + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(qw[wd] >> 16));
                         }
+                        // columns 16c..16c+15 = bf16 box c/4, chunks 2(c%4) and 2(c%4)+1
+                        uint8_t* rowp = tile + (c >> 2) * BOX_BYTES + row * 128;
+                        const int c8 = 2 * (c & 3);
+                        *reinterpret_cast<uint4*>(rowp + ((c8 ^ (row & 7)) << 4)) = make_uint4(qb[0], qb[1], qb[2], qb[3]);
+                        *reinterpret_cast<uint4*>(rowp + (((c8 + 1) ^ (row & 7)) << 4)) =
+                            make_uint4(qb[4], qb[5], qb[6], qb[7]);
                     }
                     fence_proxy_async_smem();
-                    mbar_arrive(&qfull[qs]);
-                    mbar_arrive(&rempty[rs]);
+                    mbar_arrive(&qdec[qs]);
                     if (++qs == QS) { qs = 0; qph ^= 1; }
-                    if (++rs == RSTAGES) { rs = 0; rph ^= 1; }
                 }
             }
         } else if (p.norm_q) {

@@ -138,9 +138,11 @@ gdn_status gdn_frame_step_gated(const void* q, const void* k, const void* v,
  * with one byte per element (q, k: [B, F, N, H, dk]; v: [B, F, N, H, dv]);
  * out stays bf16 and the state fp32.  The recurrence is exactly that of
  * gdn_frame_forward on the decoded values.  The kernels decode in shared
- * memory (exactly, to bf16) and fold the scales into A, U and out, so HBM
- * carries one byte per input element.  Validation and errors as
- * gdn_frame_forward (q, k, v, out 16-byte aligned).
+ * memory (exactly) and fold the scales into A, U and out, so HBM carries one
+ * byte per input element.  The contraction scales k and v by sqrt(beta) in
+ * f16 arithmetic, so every beta must lie in [0, 16384]; a value outside (or
+ * NaN) is reported as GDN_ERR_RANGE by gdn_sync_status.  Validation and
+ * other errors as gdn_frame_forward (q, k, v, out 16-byte aligned).
  */
 gdn_status gdn_frame_forward_fp8(const void* q, const void* k, const void* v,
                                  float q_scale, float k_scale, float v_scale,

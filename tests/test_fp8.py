@@ -105,3 +105,20 @@ def test_fp8_accepts_float8_tensors_and_rejects_bf16():
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
     with pytest.raises(TypeError):
         api.frame_forward_fp8(x["q8"].to(torch.bfloat16), x["k8"], x["v8"], 1.0, 1.0, 1.0, x["alpha"], x["beta"])
+
+
+@pytest.mark.parametrize("bad", [-0.25, 20000.0, float("nan")])
+def test_fp8_reports_beta_out_of_range(bad):
+    """The 8-bit contraction scales k and v by sqrt(beta) in f16, so it takes
+    beta in [0, 16384]; one value outside is reported as GDN_ERR_RANGE (11)
+    by gdn_sync_status, and the next call runs clean."""
+    B, H, F, N, d = 1, 2, 2, 64, 64
+    x = dev(inputs.draw_fp8(B, H, F, N, d, d, seed=4))
+    beta = x["beta"].clone()
+    beta[0, 1, 5, 1] = bad
+    api.frame_forward_fp8(x["q8"], x["k8"], x["v8"], x["q_scale"], x["k_scale"], x["v_scale"],
+                          x["alpha"], beta, x["state_in"])
+    with pytest.raises(api.GDNError) as e:
+        api.sync_status()
+    assert e.value.code == 11
+    gpu_fp8(x)  # clean inputs: no error left behind
