@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the frame-wise Gated DeltaNet forward.
+"""fp64 CPU oracle for the frame-wise Gated DeltaNet forward and its backward.
 
 TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg may import this package.  It shares no code with
@@ -67,6 +67,8 @@ def _load():
             p, p, p, p, p, p, p, p, p, p, ctypes.c_int64, p,
             i, i, i, i, i, i, i, i]
         lib.oracle_gdn_frame_forward_f64.restype = ctypes.c_int
+        lib.oracle_gdn_frame_backward_f64.argtypes = [p] * 14 + [i] * 7
+        lib.oracle_gdn_frame_backward_f64.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -263,4 +265,42 @@ def frame_forward_f64(q, k, v, alpha, beta, state_in=None, *, B, H, F, N, dk, dv
         res["states"] = states
     if sout is not None:
         res["sample_out"] = sout
+    return res
+
+
+def frame_backward(q, k, v, alpha, beta, state_in, d_out, d_state_out=None, *, B, H, F, N, dk, dv,
+                   n_threads=0):
+    """Reverse-mode derivatives of the forward (fp64; gdn_oracle.c,
+    backward_head).  Inputs are any arrays (bf16/fp32 torch tensors or
+    numpy), converted to fp64 exactly; d_out [B,F,N,H,dv]; d_state_out
+    [B,H,dv,dk] or None (zero).  Returns a dict of fp64 arrays: dq, dk, dv,
+    d_alpha [B,F,H], d_beta [B,F,N,H], d_state_in [B,H,dv,dk]."""
+    lib = _load()
+
+    def f64(x):
+        if x is None:
+            return None
+        try:
+            import torch
+            if isinstance(x, torch.Tensor):
+                return x.detach().cpu().to(torch.float64).contiguous().numpy()
+        except ImportError:  # pragma: no cover
+            pass
+        return np.ascontiguousarray(x, dtype=np.float64)
+    qa, ka, va, al, be, s0, do, dsf = (f64(t) for t in (q, k, v, alpha, beta, state_in, d_out, d_state_out))
+    T = B * F * N
+    if (qa.size != T * H * dk or ka.size != T * H * dk or va.size != T * H * dv or al.size != B * F * H
+            or be.size != T * H or do.size != T * H * dv
+            or (s0 is not None and s0.size != B * H * dv * dk)
+            or (dsf is not None and dsf.size != B * H * dv * dk)):
+        raise ValueError("input sizes do not match B,F,N,H,dk,dv")
+    res = {"dq": np.empty((B, F, N, H, dk)), "dk": np.empty((B, F, N, H, dk)), "dv": np.empty((B, F, N, H, dv)),
+           "d_alpha": np.empty((B, F, H)), "d_beta": np.empty((B, F, N, H)),
+           "d_state_in": np.empty((B, H, dv, dk))}
+    rc = lib.oracle_gdn_frame_backward_f64(
+        _ptr(qa), _ptr(ka), _ptr(va), _ptr(al), _ptr(be), _ptr(s0), _ptr(do), _ptr(dsf),
+        _ptr(res["dq"]), _ptr(res["dk"]), _ptr(res["dv"]), _ptr(res["d_alpha"]), _ptr(res["d_beta"]),
+        _ptr(res["d_state_in"]), B, H, F, N, dk, dv, int(n_threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gdn_frame_backward_f64 failed with code {rc}")
     return res

@@ -1,5 +1,5 @@
 /*
- * Frame-wise Gated DeltaNet forward -- fp64 CPU ORACLE.
+ * Frame-wise Gated DeltaNet forward and backward -- fp64 CPU ORACLE.
  *
  * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
  * statement of what the GPU path must compute.  Only the tests, the package's
@@ -259,6 +259,157 @@ int oracle_gdn_frame_forward_f64(const double* q, const double* k, const double*
     Inputs in = {NULL, NULL, NULL, q, k, v, NULL, NULL, NULL, alpha, beta, state_in};
     return forward(&in, q != NULL, out, state_out, states_all, sample_tok, n_samples, sample_out,
                    B, H, F, N, dk, dv, mode, n_threads);
+}
+
+/*
+ * Backward of the forward above (reverse-mode derivatives), fp64, all arrays
+ * fp64 in the forward's layouts.
+ *
+ * Given dL/dO (d_out, [B,F,N,H,dv]) and dL/dS_F (d_state_out, [B,H,dv,dk], or
+ * NULL for zero), returns dL/dq, dL/dk, dL/dv (token layouts), dL/dalpha
+ * [B,F,H], dL/dbeta [B,F,N,H] and dL/dS_0 [B,H,dv,dk] (d_state_in, may be
+ * NULL).  The chain rule applied to the forward's steps, per (b, h):
+ *
+ *   G_f = dL/dS_f (everything that depends on S_f):
+ *       G_{F-1} = dS_F + M_{F-1},   G_{f-1} = M_{f-1} + alpha_f G_f (I - A_f)
+ *       with M_f = sum_n do_n q_n^T over frame f's tokens (o_n = S_f q_n),
+ *       and dL/dS_0 = alpha_0 G_0 (I - A_0)       (A is symmetric)
+ *   from S_f = alpha_f (S_{f-1} - S_{f-1} A_f) + U_f, with P_f = S_{f-1}^T G_f:
+ *       dU_f = G_f,   dA_f = -alpha_f P_f,   dalpha_f = tr(P_f) - <P_f, A_f>
+ *   from A_f = sum_n beta_n k_n k_n^T and U_f = sum_n beta_n v_n k_n^T:
+ *       dk_n = beta_n ((dA_f + dA_f^T) k_n + G_f^T v_n),   dv_n = beta_n G_f k_n,
+ *       dbeta_n = k_n^T dA_f k_n + v_n^T G_f k_n
+ *   from o_n = S_f q_n:  dq_n = S_f^T do_n.
+ * Returns 0 on success, 1 on allocation failure, 2 on bad arguments.
+ */
+static int backward_head(const double* q, const double* k, const double* v, const double* alpha,
+                         const double* beta, const double* state_in, const double* d_out,
+                         const double* d_state_out, double* dq, double* dkv_k, double* dkv_v,
+                         double* d_alpha, double* d_beta, double* d_state_in,
+                         int b, int h, int H, int F, int N, int dk, int dv)
+{
+    const size_t SD = (size_t)dv * dk, AD = (size_t)dk * dk;
+    double* Sprev = (double*)malloc((size_t)(F + 1) * SD * sizeof(double)); /* Sprev[f] = S before frame f; Sprev[F] = S_F */
+    double* Af = (double*)malloc((size_t)(F > 0 ? F : 1) * AD * sizeof(double));
+    double* G = (double*)malloc(SD * sizeof(double));
+    double* T = (double*)malloc(SD * sizeof(double));
+    double* P = (double*)malloc(AD * sizeof(double));
+    double* W = (double*)malloc(AD * sizeof(double));
+    if (!Sprev || !Af || !G || !T || !P || !W) {
+        free(Sprev); free(Af); free(G); free(T); free(P); free(W);
+        return 1;
+    }
+    /* forward, keeping every state and every A_f */
+    for (size_t e = 0; e < SD; ++e) Sprev[e] = state_in ? state_in[((size_t)b * H + h) * SD + e] : 0.0;
+    for (int f = 0; f < F; ++f) {
+        const size_t frame = (size_t)b * F + f;
+        double* A = Af + (size_t)f * AD;
+        double* S = Sprev + (size_t)(f + 1) * SD;
+        const double* S0 = Sprev + (size_t)f * SD;
+        memset(A, 0, AD * sizeof(double));
+        memset(T, 0, SD * sizeof(double));       /* T = U_f */
+        for (int n = 0; n < N; ++n) {
+            const size_t th = (frame * N + n) * H + h;
+            const double bn = beta[th];
+            for (int i = 0; i < dk; ++i)
+                for (int j = 0; j < dk; ++j) A[(size_t)i * dk + j] += bn * k[th * dk + i] * k[th * dk + j];
+            for (int i = 0; i < dv; ++i)
+                for (int j = 0; j < dk; ++j) T[(size_t)i * dk + j] += bn * v[th * dv + i] * k[th * dk + j];
+        }
+        const double af = alpha[frame * H + h];
+        for (int i = 0; i < dv; ++i)
+            for (int j = 0; j < dk; ++j) {
+                double sa = 0.0;
+                for (int m = 0; m < dk; ++m) sa += S0[(size_t)i * dk + m] * A[(size_t)m * dk + j];
+                S[(size_t)i * dk + j] = af * (S0[(size_t)i * dk + j] - sa) + T[(size_t)i * dk + j];
+            }
+    }
+    /* reverse */
+    for (size_t e = 0; e < SD; ++e) G[e] = d_state_out ? d_state_out[((size_t)b * H + h) * SD + e] : 0.0;
+    for (int f = F - 1; f >= 0; --f) {
+        const size_t frame = (size_t)b * F + f;
+        const double* A = Af + (size_t)f * AD;
+        const double* Sf = Sprev + (size_t)(f + 1) * SD;
+        const double* S0 = Sprev + (size_t)f * SD;
+        /* G_f = G (carried from frame f+1) + M_f;  dq_n = S_f^T do_n */
+        for (int n = 0; n < N; ++n) {
+            const size_t th = (frame * N + n) * H + h;
+            for (int i = 0; i < dv; ++i)
+                for (int j = 0; j < dk; ++j) G[(size_t)i * dk + j] += d_out[th * dv + i] * q[th * dk + j];
+            for (int j = 0; j < dk; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < dv; ++i) acc += Sf[(size_t)i * dk + j] * d_out[th * dv + i];
+                dq[th * dk + j] = acc;
+            }
+        }
+        /* P_f = S_{f-1}^T G_f, dalpha_f, dA_f = -alpha_f P_f, W = dA_f + dA_f^T */
+        const double af = alpha[frame * H + h];
+        double tr = 0.0, pa = 0.0;
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dk; ++j) {
+                double acc = 0.0;
+                for (int m = 0; m < dv; ++m) acc += S0[(size_t)m * dk + i] * G[(size_t)m * dk + j];
+                P[(size_t)i * dk + j] = acc;
+            }
+        for (int i = 0; i < dk; ++i) {
+            tr += P[(size_t)i * dk + i];
+            for (int j = 0; j < dk; ++j) pa += P[(size_t)i * dk + j] * A[(size_t)i * dk + j];
+        }
+        d_alpha[frame * H + h] = tr - pa;
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dk; ++j) W[(size_t)i * dk + j] = -af * (P[(size_t)i * dk + j] + P[(size_t)j * dk + i]);
+        /* token gradients of frame f */
+        for (int n = 0; n < N; ++n) {
+            const size_t th = (frame * N + n) * H + h;
+            const double bn = beta[th];
+            double kdak = 0.0, vgk = 0.0;
+            for (int j = 0; j < dk; ++j) {
+                double wk = 0.0, gv = 0.0;
+                for (int m = 0; m < dk; ++m) wk += W[(size_t)j * dk + m] * k[th * dk + m];
+                for (int i = 0; i < dv; ++i) gv += G[(size_t)i * dk + j] * v[th * dv + i];
+                dkv_k[th * dk + j] = bn * (wk + gv);
+                kdak += 0.5 * k[th * dk + j] * wk;   /* k^T dA k = k^T W k / 2 */
+            }
+            for (int i = 0; i < dv; ++i) {
+                double gk = 0.0;
+                for (int j = 0; j < dk; ++j) gk += G[(size_t)i * dk + j] * k[th * dk + j];
+                dkv_v[th * dv + i] = bn * gk;
+                vgk += v[th * dv + i] * gk;
+            }
+            d_beta[th] = kdak + vgk;
+        }
+        /* carry to S_{f-1}: alpha_f G_f (I - A_f) */
+        for (int i = 0; i < dv; ++i)
+            for (int j = 0; j < dk; ++j) {
+                double ga = 0.0;
+                for (int m = 0; m < dk; ++m) ga += G[(size_t)i * dk + m] * A[(size_t)m * dk + j];
+                T[(size_t)i * dk + j] = af * (G[(size_t)i * dk + j] - ga);
+            }
+        memcpy(G, T, SD * sizeof(double));
+    }
+    if (d_state_in) memcpy(d_state_in + ((size_t)b * H + h) * SD, G, SD * sizeof(double));
+    free(Sprev); free(Af); free(G); free(T); free(P); free(W);
+    return 0;
+}
+
+int oracle_gdn_frame_backward_f64(const double* q, const double* k, const double* v,
+                                  const double* alpha, const double* beta, const double* state_in,
+                                  const double* d_out, const double* d_state_out,
+                                  double* dq, double* dk_out, double* dv_out, double* d_alpha, double* d_beta,
+                                  double* d_state_in, int B, int H, int F, int N, int dk, int dv, int n_threads)
+{
+    if (!q || !k || !v || !alpha || !beta || !d_out || !dq || !dk_out || !dv_out || !d_alpha || !d_beta) return 2;
+    if (B < 1 || H < 1 || F < 0 || N < 0 || dk < 1 || dv < 1) return 2;
+    const int pairs = B * H;
+    int failed = 0;
+#ifdef _OPENMP
+    #pragma omp parallel for schedule(dynamic, 1) reduction(|:failed) num_threads(n_threads > 0 ? n_threads : omp_get_max_threads())
+#endif
+    for (int p = 0; p < pairs; ++p)
+        failed |= backward_head(q, k, v, alpha, beta, state_in, d_out, d_state_out, dq, dk_out, dv_out,
+                                d_alpha, d_beta, d_state_in, p / H, p % H, H, F, N, dk, dv);
+    (void)n_threads;
+    return failed ? 1 : 0;
 }
 
 int oracle_max_threads(void)

@@ -393,3 +393,92 @@ def test_fp8_forward_equals_bf16_forward_on_shared_values():
     r16 = run(as_bf16(q8, sq), as_bf16(k8, sk), as_bf16(v8, sv), alpha, beta, s0)
     np.testing.assert_array_equal(r8["out"], r16["out"])
     np.testing.assert_array_equal(r8["state"], r16["state"])
+
+
+def _f64_problem(B, H, F, N, dk, dv, seed):
+    g = np.random.default_rng(seed)
+    x = {"q": g.standard_normal((B, F, N, H, dk)), "k": g.standard_normal((B, F, N, H, dk)) * 0.5,
+         "v": g.standard_normal((B, F, N, H, dv)), "alpha": 0.6 + 0.4 * g.random((B, F, H)),
+         "beta": g.random((B, F, N, H)) / N, "state_in": g.standard_normal((B, H, dv, dk)) * 0.3}
+    w = {"d_out": g.standard_normal((B, F, N, H, dv)), "d_state_out": g.standard_normal((B, H, dv, dk))}
+    return x, w
+
+
+def _loss(x, w, dims):
+    r = oracle.frame_forward_f64(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["state_in"], **dims)
+    return float((r["out"] * w["d_out"]).sum() + (r["state"] * w["d_state_out"]).sum())
+
+
+def test_backward_matches_central_differences():
+    """Every gradient of the backward oracle against central differences of
+    the forward oracle, along random directions (L = <W_o, O> + <W_s, S_F>)."""
+    B, H, F, N, dk, dv = 1, 2, 3, 4, 3, 2
+    dims = dict(B=B, H=H, F=F, N=N, dk=dk, dv=dv)
+    x, w = _f64_problem(B, H, F, N, dk, dv, seed=5)
+    gr = oracle.frame_backward(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["state_in"], w["d_out"],
+                               w["d_state_out"], **dims)
+    names = {"q": "dq", "k": "dk", "v": "dv", "alpha": "d_alpha", "beta": "d_beta", "state_in": "d_state_in"}
+    rng = np.random.default_rng(9)
+    eps = 1e-6
+    for name, gname in names.items():
+        for _ in range(3):
+            d = rng.standard_normal(x[name].shape)
+            xp = dict(x); xp[name] = x[name] + eps * d
+            xm = dict(x); xm[name] = x[name] - eps * d
+            fd = (_loss(xp, w, dims) - _loss(xm, w, dims)) / (2 * eps)
+            an = float((gr[gname] * d).sum())
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, fd, an)
+
+
+def _torch_forward(q, k, v, alpha, beta, s0):
+    """The forward written as torch operations, differentiated by autograd."""
+    B, F, N, H, dk = q.shape
+    outs, states = [], []
+    for b in range(B):
+        ob, sb = [], []
+        for h in range(H):
+            S = s0[b, h]
+            frames = []
+            for f in range(F):
+                K, V, Q = k[b, f, :, h], v[b, f, :, h], q[b, f, :, h]
+                bt = beta[b, f, :, h]
+                A = (K * bt[:, None]).T @ K
+                U = (V * bt[:, None]).T @ K
+                S = alpha[b, f, h] * (S - S @ A) + U
+                frames.append(Q @ S.T)
+            ob.append(torch.stack(frames))
+            sb.append(S)
+        outs.append(torch.stack(ob, dim=2))
+        states.append(torch.stack(sb))
+    return torch.stack(outs), torch.stack(states)
+
+
+def test_backward_matches_autograd():
+    B, H, F, N, dk, dv = 2, 2, 3, 5, 4, 3
+    x, w = _f64_problem(B, H, F, N, dk, dv, seed=6)
+    t = {n: torch.tensor(a, requires_grad=True) for n, a in x.items()}
+    out, st = _torch_forward(t["q"], t["k"], t["v"], t["alpha"], t["beta"], t["state_in"])
+    loss = (out * torch.tensor(w["d_out"])).sum() + (st * torch.tensor(w["d_state_out"])).sum()
+    loss.backward()
+    gr = oracle.frame_backward(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["state_in"], w["d_out"],
+                               w["d_state_out"], B=B, H=H, F=F, N=N, dk=dk, dv=dv)
+    for name, gname in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("alpha", "d_alpha"), ("beta", "d_beta"),
+                        ("state_in", "d_state_in")):
+        np.testing.assert_allclose(gr[gname], t[name].grad.numpy(), rtol=1e-10, atol=1e-12, err_msg=name)
+
+
+def test_backward_special_cases():
+    """alpha = 0 cuts the chain: nothing flows back to S_0, and with no
+    upstream state gradient the last frame's beta gradient only sees the
+    outputs.  A zero d_state_out equals passing None."""
+    B, H, F, N, dk, dv = 1, 1, 2, 3, 3, 3
+    dims = dict(B=B, H=H, F=F, N=N, dk=dk, dv=dv)
+    x, w = _f64_problem(B, H, F, N, dk, dv, seed=7)
+    x["alpha"][:] = 0.0
+    gr = oracle.frame_backward(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["state_in"], w["d_out"], None,
+                               **dims)
+    assert np.all(gr["d_state_in"] == 0.0)
+    gz = oracle.frame_backward(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["state_in"], w["d_out"],
+                               np.zeros((B, H, dv, dk)), **dims)
+    for n in gr:
+        np.testing.assert_array_equal(gr[n], gz[n])
