@@ -24,7 +24,7 @@ EXPORTS = (
     "gdn_workspace_bytes", "gdn_step_workspace_bytes",
     "gdn_status_string", "gdn_sync_status", "gdn_set_wait_limit_ns", "gdn_selftest_wait_timeout",
     "gdn_version", "gdn_frame_step_noalloc", "gdn_set_fused_scan", "gdn_scan_schedule",
-    "gdn_set_contract_split", "gdn_frame_forward_fp8", "gdn_frame_step_fp8",
+    "gdn_set_contract_split", "gdn_frame_forward_fp8", "gdn_frame_step_fp8", "gdn_frame_backward",
 )
 
 
@@ -61,6 +61,9 @@ def load(path: str | None = None):
     lib.gdn_frame_forward_fp8.restype = ctypes.c_int
     lib.gdn_frame_step_fp8.argtypes = [vp, vp, vp, fl, fl, fl, fp, fp, fp, vp, fp, i, i, i, i, i, st]
     lib.gdn_frame_step_fp8.restype = ctypes.c_int
+    lib.gdn_frame_backward.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, vp, vp, vp, fp, fp, fp,
+                                       i, i, i, i, i, i, st]
+    lib.gdn_frame_backward.restype = ctypes.c_int
     lib.gdn_frame_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, st]
     lib.gdn_frame_step.restype = ctypes.c_int
     lib.gdn_frame_forward_timed.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, st,

@@ -116,6 +116,37 @@ def frame_step_gated(q, k, v, a_logit, b_logit, alpha_scale, state_in=None, *, o
     return out, state_out
 
 
+def frame_backward(q, k, v, alpha, beta, state_in, d_out, d_state_out=None, *, want_d_state_in=True,
+                   stream=None):
+    """Gradients of frame_forward: returns (dq, dk, dv, d_alpha, d_beta,
+    d_state_in) for upstream d_out [B,F,N,H,dv] (bf16) and d_state_out
+    [B,H,dv,dk] (fp32, None = 0).  Shapes and dtypes as the inputs."""
+    lib = load()
+    B, F, N, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    dq = torch.empty((B, F, N, H, dk), dtype=torch.bfloat16, device=dev)
+    dkk = torch.empty((B, F, N, H, dk), dtype=torch.bfloat16, device=dev)
+    dvv = torch.empty((B, F, N, H, dv), dtype=torch.bfloat16, device=dev)
+    d_alpha = torch.empty((B, F, H), dtype=torch.float32, device=dev)
+    d_beta = torch.empty((B, F, N, H), dtype=torch.float32, device=dev)
+    d_s0 = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev) if want_d_state_in else None
+    args = [
+        _dev(q, "q", torch.bfloat16, (B, F, N, H, dk)),
+        _dev(k, "k", torch.bfloat16, (B, F, N, H, dk)),
+        _dev(v, "v", torch.bfloat16, (B, F, N, H, dv)),
+        _dev(alpha, "alpha", torch.float32, (B, F, H)),
+        _dev(beta, "beta", torch.float32, (B, F, N, H)),
+        None if state_in is None else _dev(state_in, "state_in", torch.float32, (B, H, dv, dk)),
+        _dev(d_out, "d_out", torch.bfloat16, (B, F, N, H, dv)),
+        None if d_state_out is None else _dev(d_state_out, "d_state_out", torch.float32, (B, H, dv, dk)),
+        dq.data_ptr(), dkk.data_ptr(), dvv.data_ptr(), d_alpha.data_ptr(), d_beta.data_ptr(),
+        None if d_s0 is None else d_s0.data_ptr(),
+    ]
+    check(lib.gdn_frame_backward(*args, B, H, F, N, dk, dv, _stream_handle(stream)), "gdn_frame_backward")
+    return dq, dkk, dvv, d_alpha, d_beta, d_s0
+
+
 def _bytes8(t):
     """e4m3 tensors are passed as their bytes (torch.float8_e4m3fn or uint8)."""
     if isinstance(t, torch.Tensor) and t.dtype == torch.float8_e4m3fn:

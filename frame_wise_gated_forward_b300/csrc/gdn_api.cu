@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "gdn.h"
+#include "gdn_bwd.cuh"
 #include "gdn_k1_contract.cuh"
 #include "gdn_k23_fused.cuh"
 
@@ -92,7 +93,9 @@ gdn_status device_ready(int* dev_out, DeviceState** st_out) {
             !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<64, false>), k23::smem_bytes<64>()) ||
             !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<16, true>), k23::smem_bytes<16>()) ||
             !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<32, true>), k23::smem_bytes<32>()) ||
-            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<64, true>), k23::smem_bytes<64>())) {
+            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<64, true>), k23::smem_bytes<64>()) ||
+            !smem_attr(reinterpret_cast<const void*>(bwd::frame_grad_kernel), bwd::FRAME_SMEM) ||
+            !smem_attr(reinterpret_cast<const void*>(bwd::token_grad_kernel), bwd::TOKEN_SMEM)) {
             cudaGetLastError();
             return GDN_ERR_LAUNCH;
         }
@@ -481,6 +484,210 @@ gdn_status run_pass(const PassArgs& a, bool step, cudaStream_t stream, cudaEvent
     return result;
 }
 
+// ---------------------------------------------------------------- backward
+__global__ void fill_f32_kernel(float* dst, long long n, float v) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x)
+        dst[i] = v;
+}
+__global__ void f32_to_bf16_kernel(const float* src, __nv_bfloat16* dst, long long n) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x)
+        dst[i] = __float2bfloat16_rn(src[i]);
+}
+
+struct BwdArgs {
+    const void *q, *k, *v;
+    const float *alpha, *beta, *state_in;
+    const void* d_out;
+    const float* d_state_out;
+    void *dq, *dk, *dv;
+    float *d_alpha, *d_beta, *d_state_in;
+    int B, H, F, N, dk_, dv_;
+};
+
+// Workspace of one batch row (reused row after row); F1 = F + 1 frame slots.
+struct BwdLayout {
+    size_t a_off, u_off, u2_off, sx_off, gx_off, w_off, al_off, one_off, c_off, total;
+};
+BwdLayout bwd_layout(int H, int F, int N, int dk, int dv) {
+    const size_t F1 = static_cast<size_t>(F) + 1;
+    BwdLayout L;
+    L.a_off = 0;                                                               // A_f, bf16, slot F zero
+    L.u_off = align256(L.a_off + F1 * H * dk * dk * 2);                        // U_f, fp32
+    L.u2_off = align256(L.u_off + static_cast<size_t>(F) * H * dv * dk * 4);   // M_{f-1} in slot f, fp32
+    L.sx_off = align256(L.u2_off + F1 * H * dv * dk * 4);                      // S_{f-1} in slot f, bf16
+    L.gx_off = align256(L.sx_off + F1 * H * dv * dk * 2);                      // G_{f-1} in slot f, bf16
+    L.w_off = align256(L.gx_off + F1 * H * dv * dk * 2);                       // W_f, bf16
+    L.al_off = align256(L.w_off + static_cast<size_t>(F) * H * dk * dk * 2);   // alpha', fp32
+    L.one_off = align256(L.al_off + F1 * H * 4);                               // ones [F, N, H]
+    L.c_off = align256(L.one_off + static_cast<size_t>(F) * N * H * 4);        // phase-1 counters
+    L.total = align256(L.c_off + F1 * H * 8);
+    return L;
+}
+
+// Phase 1 on one batch row: A_f, U_f of (k, v, beta) for F frames, whole items.
+gdn_status bwd_contract(const void* k, const void* v, const float* beta, __nv_bfloat16* A_out, float* U_out,
+                        int* counters, int H, int F, int N, int dk, int dv, const DeviceState* ds, cudaStream_t st) {
+    CUtensorMap tm_k, tm_v;
+    if (!encode_tokens(&tm_k, k, F, N, H, dk, gdn::k1::CHUNK) || !encode_tokens(&tm_v, v, F, N, H, dv, gdn::k1::CHUNK))
+        return GDN_ERR_LAUNCH;
+    const long long items = static_cast<long long>(F) * H;
+    gdn::k1::Params p1;
+    p1.beta = beta;
+    p1.A_ws = A_out;
+    p1.U_ws = U_out;
+    p1.partial = nullptr;
+    p1.counters = counters;
+    p1.H = H;
+    p1.N = N;
+    p1.dk = dk;
+    p1.dv = dv;
+    p1.items = static_cast<int>(items);
+    p1.whole = static_cast<int>(items);
+    p1.split_per = 1;
+    p1.chunks = chunks_of(N);
+    p1.work = static_cast<int>(items);
+    p1.norm_k = 0;
+    p1.beta_sigmoid = 0;
+    p1.a_scale = 1.0f;
+    p1.u_scale = 1.0f;
+    p1.wait_limit_ns = g_wait_limit_ns.load();
+    gdn::k1::contract_kernel<false><<<std::min(p1.work, ds->sms), gdn::k1::THREADS, gdn::k1::SMEM_BYTES, st>>>(
+        tm_k, tm_v, p1);
+    return GDN_OK;
+}
+
+// The scan over `F` frames on one batch row (standalone kernel), state images
+// stored through tm_S_store.
+gdn_status bwd_scan(const __nv_bfloat16* A, const float* U, __nv_bfloat16* S_store, const float* alpha,
+                    const float* state_in, float* state_out, int H, int F, int dk, int dv, int reverse,
+                    const DeviceState* ds, cudaStream_t st) {
+    const int R = scan_rows_standalone(1, H, dv, ds->sms);
+    CUtensorMap tm_A, tm_U, tm_S;
+    const long long items = static_cast<long long>(F) * H;
+    if (!encode_mats(&tm_A, A, items, dk, dk, 128) || !encode_mats_f32(&tm_U, U, items, dv, dk, R) ||
+        !encode_mats(&tm_S, S_store, items, dv, dk, R))
+        return GDN_ERR_LAUNCH;
+    gdn::k2::Params p2;
+    p2.alpha = alpha;
+    p2.state_in = state_in;
+    p2.state_out = state_out;
+    p2.H = H;
+    p2.F = F;
+    p2.dk = dk;
+    p2.dv = dv;
+    p2.rsplit = dv / R;
+    p2.reverse = reverse;
+    p2.alpha_gate = 0;
+    p2.alpha_scale = 0.0f;
+    p2.wait_limit_ns = g_wait_limit_ns.load();
+    const int n_scan = H * p2.rsplit;
+    if (R == 16)
+        gdn::k2::scan_kernel<16><<<n_scan, gdn::k2::THREADS, gdn::k2::Cfg<16>::SMEM_BYTES, st>>>(tm_A, tm_U, tm_S, p2);
+    else if (R == 32)
+        gdn::k2::scan_kernel<32><<<n_scan, gdn::k2::THREADS, gdn::k2::Cfg<32>::SMEM_BYTES, st>>>(tm_A, tm_U, tm_S, p2);
+    else
+        gdn::k2::scan_kernel<64><<<n_scan, gdn::k2::THREADS, gdn::k2::Cfg<64>::SMEM_BYTES, st>>>(tm_A, tm_U, tm_S, p2);
+    return GDN_OK;
+}
+
+// The backward of one batch row b (B = 1 views of every array).
+gdn_status bwd_row(const BwdArgs& a, int b, uint8_t* ws, const BwdLayout& L, const DeviceState* ds,
+                   cudaStream_t st) {
+    const int H = a.H, F = a.F, N = a.N, dk = a.dk_, dv = a.dv_;
+    const size_t tokH = static_cast<size_t>(F) * N * H;
+    const size_t sd = static_cast<size_t>(dv) * dk, ad = static_cast<size_t>(dk) * dk;
+    auto bf = [](const void* p, size_t elems) {
+        return reinterpret_cast<const __nv_bfloat16*>(p) + elems;
+    };
+    const void* q = bf(a.q, b * tokH * dk);
+    const void* k = bf(a.k, b * tokH * dk);
+    const void* v = bf(a.v, b * tokH * dv);
+    const void* dO = bf(a.d_out, b * tokH * dv);
+    const float* alpha = a.alpha + static_cast<size_t>(b) * F * H;
+    const float* beta = a.beta + b * tokH;
+    const float* s0 = a.state_in ? a.state_in + static_cast<size_t>(b) * H * sd : nullptr;
+    const float* dSF = a.d_state_out ? a.d_state_out + static_cast<size_t>(b) * H * sd : nullptr;
+    __nv_bfloat16* A1 = reinterpret_cast<__nv_bfloat16*>(ws + L.a_off);
+    float* U = reinterpret_cast<float*>(ws + L.u_off);
+    float* U2 = reinterpret_cast<float*>(ws + L.u2_off);
+    __nv_bfloat16* Sx = reinterpret_cast<__nv_bfloat16*>(ws + L.sx_off);
+    __nv_bfloat16* Gx = reinterpret_cast<__nv_bfloat16*>(ws + L.gx_off);
+    __nv_bfloat16* Wb = reinterpret_cast<__nv_bfloat16*>(ws + L.w_off);
+    float* al = reinterpret_cast<float*>(ws + L.al_off);
+    const float* ones = reinterpret_cast<const float*>(ws + L.one_off);
+    int* counters = reinterpret_cast<int*>(ws + L.c_off);
+    const int fill_grid = 2 * ds->sms;
+    gdn_status r;
+
+    // slots that no kernel writes: A_F = 0, M_{-1} = 0, S_{-1} image = S_0; alpha' = [alpha, 1]
+    if (cudaMemsetAsync(A1 + static_cast<size_t>(F) * H * ad, 0, H * ad * 2, st) != cudaSuccess ||
+        cudaMemsetAsync(U2, 0, H * sd * 4, st) != cudaSuccess ||
+        cudaMemcpyAsync(al, alpha, static_cast<size_t>(F) * H * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
+    fill_f32_kernel<<<1, 128, 0, st>>>(al + static_cast<size_t>(F) * H, H, 1.0f);
+    if (s0)
+        f32_to_bf16_kernel<<<fill_grid, 256, 0, st>>>(s0, Sx, static_cast<long long>(H) * sd);
+    else if (cudaMemsetAsync(Sx, 0, H * sd * 2, st) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
+    // forward recompute: A_f, U_f, and the states S_0..S_{F-1} into slots 1..F
+    if ((r = bwd_contract(k, v, beta, A1, U, counters, H, F, N, dk, dv, ds, st)) != GDN_OK) return r;
+    if ((r = bwd_scan(A1, U, Sx + H * sd, alpha, s0, nullptr, H, F, dk, dv, 0, ds, st)) != GDN_OK) return r;
+    // M_f = dO_f^T Q_f into slots 1..F (the contraction with beta = 1; its A output is scratch)
+    if ((r = bwd_contract(q, dO, ones, Wb, U2 + H * sd, counters, H, F, N, dk, dv, ds, st)) != GDN_OK) return r;
+    // reverse scan over F + 1 slots: slot j >= 1 receives G_{j-1}, slot 0 dL/dS_0
+    if ((r = bwd_scan(A1, U2, Gx, al, dSF, a.d_state_in ? a.d_state_in + static_cast<size_t>(b) * H * sd : nullptr,
+                      H, F + 1, dk, dv, 1, ds, st)) != GDN_OK)
+        return r;
+    // per-frame gradients
+    {
+        CUtensorMap tm_Sx, tm_Gx, tm_A;
+        const long long slots = static_cast<long long>(F + 1) * H;
+        if (!encode_mats(&tm_Sx, Sx, slots, dv, dk, 128) || !encode_mats(&tm_Gx, Gx, slots, dv, dk, 128) ||
+            !encode_mats(&tm_A, A1, slots, dk, dk, 128))
+            return GDN_ERR_LAUNCH;
+        gdn::bwd::FrameParams pf;
+        pf.alpha = alpha;
+        pf.d_alpha = a.d_alpha + static_cast<size_t>(b) * F * H;
+        pf.W = Wb;
+        pf.H = H;
+        pf.F = F;
+        pf.dk = dk;
+        pf.dv = dv;
+        pf.wait_limit_ns = g_wait_limit_ns.load();
+        gdn::bwd::frame_grad_kernel<<<std::min(F * H, ds->sms), gdn::bwd::THREADS, gdn::bwd::FRAME_SMEM, st>>>(
+            tm_Sx, tm_Gx, tm_A, pf);
+    }
+    // per-token gradients
+    {
+        CUtensorMap tm_k, tm_v, tm_do, tm_Sx, tm_Gx, tm_W;
+        const long long slots = static_cast<long long>(F + 1) * H;
+        if (!encode_tokens(&tm_k, k, F, N, H, dk, 128) || !encode_tokens(&tm_v, v, F, N, H, dv, 128) ||
+            !encode_tokens(&tm_do, dO, F, N, H, dv, 128) || !encode_mats(&tm_Sx, Sx, slots, dv, dk, 128) ||
+            !encode_mats(&tm_Gx, Gx, slots, dv, dk, 128) ||
+            !encode_mats(&tm_W, Wb, static_cast<long long>(F) * H, dk, dk, 128))
+            return GDN_ERR_LAUNCH;
+        gdn::bwd::TokenParams pt;
+        pt.beta = beta;
+        pt.dq_out = reinterpret_cast<__nv_bfloat16*>(a.dq) + b * tokH * dk;
+        pt.dk_out = reinterpret_cast<__nv_bfloat16*>(a.dk) + b * tokH * dk;
+        pt.dv_out = reinterpret_cast<__nv_bfloat16*>(a.dv) + b * tokH * dv;
+        pt.d_beta = a.d_beta + b * tokH;
+        pt.H = H;
+        pt.F = F;
+        pt.N = N;
+        pt.dk = dk;
+        pt.dv = dv;
+        pt.ntile = (N + 127) / 128;
+        pt.units = static_cast<long long>(F) * H * pt.ntile;
+        pt.wait_limit_ns = g_wait_limit_ns.load();
+        gdn::bwd::token_grad_kernel<<<static_cast<int>(std::min<long long>(pt.units, ds->sms)), gdn::bwd::THREADS,
+                                      gdn::bwd::TOKEN_SMEM, st>>>(tm_k, tm_v, tm_do, tm_Sx, tm_Gx, tm_W, pt);
+    }
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+
 __global__ void selftest_timeout_kernel(unsigned long long limit_ns) {
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
@@ -573,6 +780,62 @@ gdn_status gdn_frame_step_fp8(const void* q, const void* k, const void* v, float
     a.k_scale = k_scale;
     a.v_scale = v_scale;
     return run_pass(a, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_frame_backward(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
+                              const float* state_in, const void* d_out, const float* d_state_out, void* dq_out,
+                              void* dk_out, void* dv_out, float* d_alpha, float* d_beta, float* d_state_in, int B,
+                              int H, int F, int N, int dk, int dv, gdn_stream_t stream) {
+    if (!q || !k || !v || !alpha || !beta || !d_out || !dq_out || !dk_out || !dv_out || !d_alpha || !d_beta)
+        return GDN_ERR_NULL_PTR;
+    gdn_status s = validate(q, k, v, alpha, beta, state_in, d_out, nullptr, B, H, F, N, dk, dv);
+    if (s != GDN_OK) return s;
+    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+    if (!a16(dq_out) || !a16(dk_out) || !a16(dv_out) || !a4(d_alpha) || !a4(d_beta) || (d_state_in && !a4(d_state_in)) ||
+        (d_state_out && !a4(d_state_out)))
+        return GDN_ERR_MISALIGNED;
+    // every gradient output must stay clear of every input
+    {
+        const long long tok = static_cast<long long>(B) * F * N;
+        const uintptr_t sb = static_cast<uintptr_t>(static_cast<long long>(B) * H * dv * dk * 4);
+        auto R = [](const void* p, uintptr_t n) { return Range{reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p) + n}; };
+        const Range ins[8] = {R(q, tok * H * dk * 2), R(k, tok * H * dk * 2), R(v, tok * H * dv * 2),
+                              R(alpha, static_cast<uintptr_t>(B) * F * H * 4), R(beta, tok * H * 4),
+                              R(d_out, tok * H * dv * 2), state_in ? R(state_in, sb) : Range{0, 0},
+                              d_state_out ? R(d_state_out, sb) : Range{0, 0}};
+        const Range outs[6] = {R(dq_out, tok * H * dk * 2), R(dk_out, tok * H * dk * 2), R(dv_out, tok * H * dv * 2),
+                               R(d_alpha, static_cast<uintptr_t>(B) * F * H * 4), R(d_beta, tok * H * 4),
+                               d_state_in ? R(d_state_in, sb) : Range{0, 0}};
+        for (const Range& o : outs)
+            for (const Range& i : ins)
+                if (o.hi > o.lo && i.hi > i.lo && overlap(o, i)) return GDN_ERR_ALIAS;
+        for (int x = 0; x < 6; ++x)
+            for (int y = x + 1; y < 6; ++y)
+                if (outs[x].hi > outs[x].lo && outs[y].hi > outs[y].lo && overlap(outs[x], outs[y])) return GDN_ERR_ALIAS;
+    }
+    int dev;
+    DeviceState* ds;
+    s = device_ready(&dev, &ds);
+    if (s != GDN_OK) return s;
+    const void* ptrs[14] = {q, k, v, alpha, beta, state_in, d_out, d_state_out, dq_out, dk_out, dv_out, d_alpha, d_beta, d_state_in};
+    for (const void* p : ptrs)
+        if (!is_device_ptr(p)) return GDN_ERR_NULL_PTR;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const BwdLayout L = bwd_layout(H, F, N, dk, dv);
+    uint8_t* ws = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), L.total, ds->pool, st) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_ALLOC;
+    }
+    BwdArgs a{q, k, v, alpha, beta, state_in, d_out, d_state_out, dq_out, dk_out, dv_out, d_alpha, d_beta,
+              d_state_in, B, H, F, N, dk, dv};
+    fill_f32_kernel<<<2 * ds->sms, 256, 0, st>>>(reinterpret_cast<float*>(ws + L.one_off),
+                                                 static_cast<long long>(F) * N * H, 1.0f);
+    gdn_status r = GDN_OK;
+    for (int b = 0; b < B && r == GDN_OK; ++b) r = bwd_row(a, b, ws, L, ds, st);
+    cudaFreeAsync(ws, st);
+    return r;
 }
 
 gdn_status gdn_frame_forward_timed(const void* q, const void* k, const void* v, const float* alpha,

@@ -1,0 +1,397 @@
+// gdn_bwd.cuh -- the backward pass of the frame-wise GDN forward: the two
+// frame-parallel gradient kernels.  The reverse recurrence of the state
+// gradient runs on the forward's scan kernel (see gdn_frame_backward in
+// gdn_api.cu); these kernels turn its per-frame results into the gradients.
+//
+// Per (b, f, h) with S_{f-1} the state before frame f, G_f = dL/dS_f, and the
+// forward S_f = alpha_f (S_{f-1} - S_{f-1} A_f) + U_f, o_n = S_f q_n
+// (SANA-WM article, "The Architecture": a decay gate and a delta-rule
+// correction of a fixed-size state, one latent frame per step), the chain
+// rule gives
+//     P_f = S_{f-1}^T G_f,  dalpha_f = tr P_f - <P_f, A_f>,
+//     W_f = dA_f + dA_f^T = -alpha_f (P_f + P_f^T)
+// (frame_grad_kernel) and, per token n of frame f,
+//     dq_n = S_f^T do_n,  dk_n = beta_n (W_f k_n + G_f^T v_n),
+//     dv_n = beta_n G_f k_n,  dbeta_n = k_n^T W_f k_n / 2 + v_n^T G_f k_n
+// (token_grad_kernel).  Both are tcgen05 MMAs on operands TMA-loaded into
+// 128-byte-swizzled shared memory; the bf16 per-frame states S and G are read
+// MN-major or K-major from the same tile as each product needs.
+//
+// Both kernels take one batch row (items f*H + h) and run one work unit at a
+// time per CTA (load, MMA, epilogue), with bounded waits throughout.
+#pragma once
+
+#include "gdn_ptx.cuh"
+
+namespace gdn {
+namespace bwd {
+
+constexpr int THREADS = 128;                 // four warps: TMEM lane quarters
+constexpr int BOX = 128 * 128;               // 128 rows x 64 bf16 columns
+constexpr int TILE = 2 * BOX;                // 128 x 128 bf16, two 64-column boxes
+constexpr uint32_t MN_LBO = BOX;             // MN-major: distance between 64-column blocks
+constexpr uint32_t SBO = 1024;               // 8 rows x 128 B
+constexpr int PT_STRIDE = 129;               // fp32 staging of P^T, padded against bank conflicts
+
+// ------------------------------------------------------------ frame grads
+constexpr size_t FRAME_SMEM = 1024 + 3 * TILE + 128 * PT_STRIDE * 4 + 256;
+static_assert(FRAME_SMEM <= 232448, "shared memory");
+
+struct FrameParams {
+    const float* alpha;       // [F, H] forward decay
+    float* d_alpha;           // [F, H] out
+    __nv_bfloat16* W;         // [F*H][dk][dk] out: -alpha (P + P^T)
+    int H, F, dk, dv;
+    unsigned long long wait_limit_ns;
+};
+
+// One CTA per SM; item f*H + h: P = S_{f-1}^T G_f with M = dk, N = dk, K = dv,
+// both operands MN-major straight from the [dv][dk] state images.
+//   tm_Sx: per-frame states, slot f holds S_{f-1} (slot 0 = S_0)
+//   tm_Gx: state gradients, slot f + 1 holds G_f
+//   tm_A:  A_f (bf16 [dk][dk])
+__global__ void __launch_bounds__(THREADS, 1)
+    frame_grad_kernel(const __grid_constant__ CUtensorMap tm_Sx, const __grid_constant__ CUtensorMap tm_Gx,
+                      const __grid_constant__ CUtensorMap tm_A, const FrameParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sS = smem;
+    uint8_t* sG = sS + TILE;
+    uint8_t* sA = sG + TILE;
+    float* Pt = reinterpret_cast<float*>(sA + TILE);                   // Pt[c * 129 + j] = P[j][c]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(Pt + 128 * PT_STRIDE);
+    uint64_t* load_bar = bars;
+    uint64_t* mma_bar = bars + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* red = reinterpret_cast<float*>(tmem_slot + 2);               // [4] per-warp partial sums
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kboxes = p.dk > 64 ? 2 : 1;
+    const int items = p.F * p.H;
+    if (kboxes < 2)  // box 1 of every tile is never loaded and must read as zero
+        for (int i = tid; i < 3 * TILE / 16; i += THREADS) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+    if (tid == 0) {
+        mbar_init(load_bar, 1);
+        mbar_init(mma_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tm_Sx);
+        prefetch_tmap(&tm_Gx);
+        prefetch_tmap(&tm_A);
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 128);
+        tmem_relinquish();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    uint32_t phase = 0;
+    bool load_pending = false, mma_pending = false;
+
+    for (int it = blockIdx.x; it < items; it += gridDim.x) {
+        const int f = it / p.H, h = it % p.H;
+        if (tid == 0) {
+            mbar_arrive_expect_tx(load_bar, 3 * kboxes * BOX);
+            for (int bx = 0; bx < kboxes; ++bx) {
+                tma_load_3d(sS + bx * BOX, &tm_Sx, load_bar, 64 * bx, 0, f * p.H + h);
+                tma_load_3d(sG + bx * BOX, &tm_Gx, load_bar, 64 * bx, 0, (f + 1) * p.H + h);
+                tma_load_3d(sA + bx * BOX, &tm_A, load_bar, 64 * bx, 0, it);
+            }
+        }
+        load_pending = true;
+        bool ok = mbar_wait(load_bar, phase, p.wait_limit_ns, abort_flag);
+        if (!__syncthreads_and(ok)) break;
+        load_pending = false;
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t IDESC = idesc_bf16(128, 128, 1, 1);
+            const int nk = (p.dv + 15) / 16;
+            for (int kk = 0; kk < nk; ++kk) {
+                const uint64_t ad = smem_desc(smem_u32(sS) + kk * 2048, MN_LBO, SBO);
+                const uint64_t bd = smem_desc(smem_u32(sG) + kk * 2048, MN_LBO, SBO);
+                mma_bf16(tmem_base, ad, bd, IDESC, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(mma_bar);
+        }
+        mma_pending = true;
+        ok = mbar_wait(mma_bar, phase, p.wait_limit_ns, abort_flag);
+        if (!__syncthreads_and(ok)) break;
+        mma_pending = false;
+        phase ^= 1;
+        tc_fence_after();
+
+        // thread j holds row j of P (TMEM lane j): the trace term, <P, A> with
+        // row j of A from shared memory, and P^T staged for the transpose
+        const int j = tid;
+        const uint32_t trow = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+        float part = 0.0f;
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t r32[32];
+            tmem_ld32(trow + c0, r32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                const int c = c0 + t;
+                const float pv = __uint_as_float(r32[t]);
+                Pt[c * PT_STRIDE + j] = pv;
+                if (j < p.dk && c < p.dk) {
+                    // A[j][c] in the swizzled K-major tile: box c/64, 16-byte chunk (c%64)/8
+                    const int cc = c & 63;
+                    const __nv_bfloat16* ap = reinterpret_cast<const __nv_bfloat16*>(
+                        sA + (c >> 6) * BOX + j * 128 + ((((cc >> 3) ^ (j & 7))) << 4)) + (cc & 7);
+                    part += (c == j ? pv : 0.0f) - pv * __bfloat162float(*ap);
+                }
+            }
+        }
+        tc_fence_before();
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) red[warp] = part;
+        __syncthreads();
+        const float af = p.alpha[it];
+        if (tid == 0) p.d_alpha[it] = (red[0] + red[1]) + (red[2] + red[3]);
+        if (j < p.dk) {
+            __nv_bfloat16* wrow = p.W + (static_cast<size_t>(it) * p.dk + j) * p.dk;
+            for (int c0 = 0; c0 < p.dk; c0 += 8) {
+                float w[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t)
+                    w[t] = -af * (Pt[(c0 + t) * PT_STRIDE + j] + Pt[j * PT_STRIDE + c0 + t]);
+                *reinterpret_cast<uint4*>(wrow + c0) =
+                    make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
+                               pack_bf16x2(w[6], w[7]));
+            }
+        }
+        __syncthreads();  // tiles, Pt and red are reused by the next item
+    }
+    // an abandoned item's copies or MMAs must land before the CTA leaves
+    if (tid == 0) {
+        if (load_pending) mbar_wait_drain(load_bar, phase, p.wait_limit_ns);
+        if (mma_pending) mbar_wait_drain(mma_bar, phase, p.wait_limit_ns);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 128);
+    }
+}
+
+// ------------------------------------------------------------ token grads
+constexpr size_t TOKEN_SMEM = 1024 + 6 * TILE + 256;
+static_assert(TOKEN_SMEM <= 232448, "shared memory");
+
+struct TokenParams {
+    const float* beta;         // [F, N, H]
+    __nv_bfloat16 *dq_out, *dk_out, *dv_out;  // [F, N, H, d] out
+    float* d_beta;             // [F, N, H] out
+    int H, F, N, dk, dv;
+    int ntile;                 // ceil(N / 128)
+    long long units;           // F * H * ntile
+    unsigned long long wait_limit_ns;
+};
+
+// Unit u: item u / ntile = f*H + h, token tile u % ntile.  Four accumulators
+// of 128 columns, M = 128 tokens each:
+//     T1 = K W_f   T2 = V G_f   T3 = K G_f^T   T4 = dO S_f
+// token tiles (k, v, dO) K-major; W_f (symmetric) and G_f as K-major B for
+// T1 / T3; G_f and S_f MN-major for T2 / T4.
+__global__ void __launch_bounds__(THREADS, 1)
+    token_grad_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_Sx,
+                      const __grid_constant__ CUtensorMap tm_Gx, const __grid_constant__ CUtensorMap tm_W,
+                      const TokenParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sK = smem;
+    uint8_t* sV = sK + TILE;
+    uint8_t* sO = sV + TILE;
+    uint8_t* sS = sO + TILE;
+    uint8_t* sG = sS + TILE;
+    uint8_t* sW = sG + TILE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sW + TILE);
+    uint64_t* load_bar = bars;
+    uint64_t* mma_bar = bars + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int kb = p.dk > 64 ? 2 : 1, vb = p.dv > 64 ? 2 : 1;
+    if (kb < 2 || vb < 2)  // boxes that are never loaded must read as zero
+        for (int i = tid; i < 6 * TILE / 16; i += THREADS) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+    if (tid == 0) {
+        mbar_init(load_bar, 1);
+        mbar_init(mma_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_do);
+        prefetch_tmap(&tm_Sx);
+        prefetch_tmap(&tm_Gx);
+        prefetch_tmap(&tm_W);
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    uint32_t phase = 0;
+    bool load_pending = false, mma_pending = false;
+    int loaded_item = -1;
+
+    // contiguous unit ranges: a CTA's consecutive tiles mostly share an item,
+    // whose S_f, G_f and W_f stay in shared memory
+    const long long u_begin = (static_cast<long long>(blockIdx.x) * p.units) / gridDim.x;
+    const long long u_end = (static_cast<long long>(blockIdx.x + 1) * p.units) / gridDim.x;
+    for (long long u = u_begin; u < u_end; ++u) {
+        const int item = static_cast<int>(u / p.ntile), tile = static_cast<int>(u % p.ntile);
+        const int f = item / p.H, h = item % p.H;
+        if (tid == 0) {
+            const bool new_item = item != loaded_item;
+            const uint32_t bytes = (kb + 2 * vb) * BOX + (new_item ? 3 * kb * BOX : 0);
+            mbar_arrive_expect_tx(load_bar, bytes);
+            for (int bx = 0; bx < kb; ++bx) tma_load_4d(sK + bx * BOX, &tm_k, load_bar, 64 * bx, h, tile * 128, f);
+            for (int bx = 0; bx < vb; ++bx) {
+                tma_load_4d(sV + bx * BOX, &tm_v, load_bar, 64 * bx, h, tile * 128, f);
+                tma_load_4d(sO + bx * BOX, &tm_do, load_bar, 64 * bx, h, tile * 128, f);
+            }
+            if (new_item)
+                for (int bx = 0; bx < kb; ++bx) {
+                    tma_load_3d(sS + bx * BOX, &tm_Sx, load_bar, 64 * bx, 0, (f + 1) * p.H + h);  // S_f
+                    tma_load_3d(sG + bx * BOX, &tm_Gx, load_bar, 64 * bx, 0, (f + 1) * p.H + h);  // G_f
+                    tma_load_3d(sW + bx * BOX, &tm_W, load_bar, 64 * bx, 0, item);
+                }
+        }
+        loaded_item = item;
+        load_pending = true;
+        bool ok = mbar_wait(load_bar, phase, p.wait_limit_ns, abort_flag);
+        if (!__syncthreads_and(ok)) break;
+        load_pending = false;
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t ID_KK = idesc_bf16(128, 128, 0, 0);   // A K-major, B K-major
+            constexpr uint32_t ID_KM = idesc_bf16(128, 128, 0, 1);   // A K-major, B MN-major
+            const int nkk = (p.dk + 15) / 16, nkv = (p.dv + 15) / 16;
+            const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aO = smem_u32(sO);
+            const uint32_t bS = smem_u32(sS), bG = smem_u32(sG), bW = smem_u32(sW);
+            for (int kk = 0; kk < nkk; ++kk) {   // K-steps over dk
+                const uint32_t ko = (kk >> 2) * BOX + (kk & 3) * 32;
+                const uint64_t ad = smem_desc(aK + ko, 16, SBO);
+                mma_bf16(tmem_base + 0, ad, smem_desc(bW + ko, 16, SBO), ID_KK, kk > 0 ? 1u : 0u);    // T1
+                mma_bf16(tmem_base + 256, ad, smem_desc(bG + ko, 16, SBO), ID_KK, kk > 0 ? 1u : 0u);  // T3
+            }
+            for (int kk = 0; kk < nkv; ++kk) {   // K-steps over dv
+                const uint32_t ko = (kk >> 2) * BOX + (kk & 3) * 32;
+                mma_bf16(tmem_base + 128, smem_desc(aV + ko, 16, SBO), smem_desc(bG + kk * 2048, MN_LBO, SBO), ID_KM,
+                         kk > 0 ? 1u : 0u);  // T2
+                mma_bf16(tmem_base + 384, smem_desc(aO + ko, 16, SBO), smem_desc(bS + kk * 2048, MN_LBO, SBO), ID_KM,
+                         kk > 0 ? 1u : 0u);  // T4
+            }
+            mma_commit(mma_bar);
+        }
+        mma_pending = true;
+        ok = mbar_wait(mma_bar, phase, p.wait_limit_ns, abort_flag);
+        if (!__syncthreads_and(ok)) break;
+        mma_pending = false;
+        phase ^= 1;
+        tc_fence_after();
+
+        // thread n: token row n of the tile (TMEM lane n)
+        const int n = tid;
+        const int token = tile * 128 + n;
+        const bool valid = token < p.N;
+        const size_t th = (static_cast<size_t>(f) * p.N + (valid ? token : 0)) * p.H + h;
+        const float bn = valid ? p.beta[th] : 0.0f;
+        const uint32_t trow = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+        float dbeta = 0.0f;
+        // dk = beta (T1 + T2), dbeta += (T1 . k) / 2 ; dq = T4
+        for (int c0 = 0; c0 < p.dk; c0 += 32) {
+            uint32_t t1[32], t2[32];
+            tmem_ld32(trow + 0 + c0, t1);
+            tmem_ld32(trow + 128 + c0, t2);
+            tmem_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int t = 0; t < 32; t += 2) {
+                const int c = c0 + t;
+                const int cc = c & 63;
+                const __nv_bfloat162 k2 = *reinterpret_cast<const __nv_bfloat162*>(
+                    sK + (c >> 6) * BOX + n * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2);
+                const float2 kf = __bfloat1622float2(k2);
+                const float a0 = __uint_as_float(t1[t]), a1 = __uint_as_float(t1[t + 1]);
+                dbeta += 0.5f * (a0 * kf.x + a1 * kf.y);
+                pk[t / 2] = pack_bf16x2(bn * (a0 + __uint_as_float(t2[t])), bn * (a1 + __uint_as_float(t2[t + 1])));
+            }
+            if (valid) {
+                __nv_bfloat16* dst = p.dk_out + th * p.dk + c0;
+                for (int q4 = 0; q4 < 4; ++q4)
+                    if (c0 + 8 * q4 < p.dk)
+                        *reinterpret_cast<uint4*>(dst + 8 * q4) =
+                            make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+            }
+            uint32_t t4[32];
+            tmem_ld32(trow + 384 + c0, t4);
+            tmem_wait_ld();
+            if (valid) {
+                __nv_bfloat16* dst = p.dq_out + th * p.dk + c0;
+                for (int q4 = 0; q4 < 4; ++q4)
+                    if (c0 + 8 * q4 < p.dk)
+                        *reinterpret_cast<uint4*>(dst + 8 * q4) = make_uint4(
+                            pack_bf16x2(__uint_as_float(t4[8 * q4 + 0]), __uint_as_float(t4[8 * q4 + 1])),
+                            pack_bf16x2(__uint_as_float(t4[8 * q4 + 2]), __uint_as_float(t4[8 * q4 + 3])),
+                            pack_bf16x2(__uint_as_float(t4[8 * q4 + 4]), __uint_as_float(t4[8 * q4 + 5])),
+                            pack_bf16x2(__uint_as_float(t4[8 * q4 + 6]), __uint_as_float(t4[8 * q4 + 7])));
+            }
+        }
+        // dv = beta T3, dbeta += T3 . v
+        for (int c0 = 0; c0 < p.dv; c0 += 32) {
+            uint32_t t3[32];
+            tmem_ld32(trow + 256 + c0, t3);
+            tmem_wait_ld();
+            uint32_t pv[16];
+#pragma unroll
+            for (int t = 0; t < 32; t += 2) {
+                const int c = c0 + t;
+                const int cc = c & 63;
+                const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(
+                    sV + (c >> 6) * BOX + n * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2);
+                const float2 vf = __bfloat1622float2(v2);
+                const float a0 = __uint_as_float(t3[t]), a1 = __uint_as_float(t3[t + 1]);
+                dbeta += a0 * vf.x + a1 * vf.y;
+                pv[t / 2] = pack_bf16x2(bn * a0, bn * a1);
+            }
+            if (valid) {
+                __nv_bfloat16* dst = p.dv_out + th * p.dv + c0;
+                for (int q4 = 0; q4 < 4; ++q4)
+                    if (c0 + 8 * q4 < p.dv)
+                        *reinterpret_cast<uint4*>(dst + 8 * q4) =
+                            make_uint4(pv[4 * q4], pv[4 * q4 + 1], pv[4 * q4 + 2], pv[4 * q4 + 3]);
+            }
+        }
+        if (valid) p.d_beta[th] = dbeta;
+        tc_fence_before();
+        __syncthreads();  // tiles and accumulators are reused by the next unit
+    }
+    if (tid == 0) {
+        if (load_pending) mbar_wait_drain(load_bar, phase, p.wait_limit_ns);
+        if (mma_pending) mbar_wait_drain(mma_bar, phase, p.wait_limit_ns);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+}  // namespace bwd
+}  // namespace gdn

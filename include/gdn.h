@@ -151,6 +151,34 @@ gdn_status gdn_frame_forward_fp8(const void* q, const void* k, const void* v,
                                  int B, int H, int F, int N, int dk, int dv,
                                  gdn_stream_t stream);
 
+/*
+ * Backward of gdn_frame_forward, for training (the SANA-WM pages train the
+ * model, wispaper "Methodology"; they give no gradient formulas).  Given the
+ * forward's inputs and the upstream gradients d_out = dL/dout [B, F, N, H, dv]
+ * (bf16) and d_state_out = dL/dstate_out [B, H, dv, dk] (fp32, NULL = 0), it
+ * writes dq, dk [B, F, N, H, dk] and dv [B, F, N, H, dv] (bf16), d_alpha
+ * [B, F, H] and d_beta [B, F, N, H] (fp32), and d_state_in [B, H, dv, dk]
+ * (fp32, may be NULL).  The chain rule of the forward's steps:
+ *     G_{f-1} = M_{f-1} + alpha_f G_f (I - A_f),  G_{F-1} = dS_F + M_{F-1},
+ *     M_f = dO_f^T Q_f,  P_f = S_{f-1}^T G_f,  dA_f = -alpha_f P_f,
+ *     dalpha_f = tr P_f - <P_f, A_f>,  dS_0 = alpha_0 G_0 (I - A_0),
+ *     dq_n = S_f^T do_n,  dk_n = beta_n ((dA_f + dA_f^T) k_n + G_f^T v_n),
+ *     dv_n = beta_n G_f k_n,  dbeta_n = k_n^T dA_f k_n + v_n^T G_f k_n.
+ * It recomputes the forward states (phase 1 and the scan), runs the state
+ * gradient recurrence on the same scan kernel in reverse, then two
+ * frame-parallel tcgen05 kernels form the gradients.  Outputs must not
+ * overlap inputs or each other (GDN_ERR_ALIAS); otherwise validation and
+ * errors as gdn_frame_forward.  Batch rows run one after another on the
+ * stream with one workspace of about (F + 1) * H * (2 dk^2 + 12 dv dk) bytes.
+ */
+gdn_status gdn_frame_backward(const void* q, const void* k, const void* v,
+                              const float* alpha, const float* beta, const float* state_in,
+                              const void* d_out, const float* d_state_out,
+                              void* dq_out, void* dk_out, void* dv_out, float* d_alpha, float* d_beta,
+                              float* d_state_in,
+                              int B, int H, int F, int N, int dk, int dv,
+                              gdn_stream_t stream);
+
 /* gdn_frame_step with the 8-bit inputs of gdn_frame_forward_fp8. */
 gdn_status gdn_frame_step_fp8(const void* q, const void* k, const void* v,
                               float q_scale, float k_scale, float v_scale,
