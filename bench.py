@@ -374,6 +374,27 @@ def main():
                         "out bf16, state fp32"}
     del x8
 
+    # ------------------------------------------------------- backward (training)
+    g = torch.Generator().manual_seed(1)
+    d_out = torch.randn(out.shape, generator=g).to(torch.bfloat16).to(device)
+    api.frame_backward(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], s_in, d_out)
+    torch.cuda.synchronize(device)
+    nb = min(args.steps, 20)
+    r0.record(stream)
+    for _ in range(nb):
+        api.frame_backward(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], s_in, d_out)
+    r1.record(stream)
+    torch.cuda.synchronize(device)
+    api.sync_status()
+    bwd_ms = r0.elapsed_time(r1) / nb
+    # compulsory bytes: q, k, v, d_out, beta read; dq, dk, dv, d_beta written (bf16 / fp32)
+    bwd_bytes = tokens * w.H * ((2 * w.dk + 2 * w.dv) * 2 + (2 * w.dk + w.dv) * 2 + 8)
+    backward_info = {"ms_per_step": bwd_ms, "tokens_per_s": tokens / (bwd_ms / 1e3), "steps": nb,
+                     "path_floor_ms": bwd_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3,
+                     "what": "gdn_frame_backward: dq, dk, dv, dalpha, dbeta, dS0 for upstream dO (forward states "
+                             "recomputed)"}
+    del d_out
+
     # ------------------------------------------- interactive step (one frame)
     # the streaming rollout: F sequential gdn_frame_step calls on a resident state
     step_state = torch.zeros((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=device)
@@ -449,6 +470,7 @@ def main():
             "reverse_direction": reverse_info,
             "gated_prologue": gated_info,
             "fp8_inputs": fp8_info,
+            "backward": backward_info,
             "cpu_baseline": cpu,
             "clocks": clocks,
             "gpu_launches": (3 if sched <= 0 else 2) * args.steps,

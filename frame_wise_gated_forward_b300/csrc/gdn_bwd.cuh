@@ -34,7 +34,7 @@ constexpr uint32_t SBO = 1024;               // 8 rows x 128 B
 constexpr int PT_STRIDE = 129;               // fp32 staging of P^T, padded against bank conflicts
 
 // ------------------------------------------------------------ frame grads
-constexpr size_t FRAME_SMEM = 1024 + 3 * TILE + 128 * PT_STRIDE * 4 + 256;
+constexpr size_t FRAME_SMEM = 1024 + 4 * TILE + 128 * PT_STRIDE * 4 + 256;
 static_assert(FRAME_SMEM <= 232448, "shared memory");
 
 struct FrameParams {
@@ -57,8 +57,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sS = smem;
     uint8_t* sG = sS + TILE;
-    uint8_t* sA = sG + TILE;
-    float* Pt = reinterpret_cast<float*>(sA + TILE);                   // Pt[c * 129 + j] = P[j][c]
+    uint8_t* sA2 = sG + TILE;                                          // [2]: A_f is read by the epilogue
+    float* Pt = reinterpret_cast<float*>(sA2 + 2 * TILE);              // Pt[c * 129 + j] = P[j][c]
     uint64_t* bars = reinterpret_cast<uint64_t*>(Pt + 128 * PT_STRIDE);
     uint64_t* load_bar = bars;
     uint64_t* mma_bar = bars + 1;
@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int kboxes = p.dk > 64 ? 2 : 1;
     const int items = p.F * p.H;
     if (kboxes < 2)  // box 1 of every tile is never loaded and must read as zero
-        for (int i = tid; i < 3 * TILE / 16; i += THREADS) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < 4 * TILE / 16; i += THREADS) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         mbar_init(load_bar, 1);
         mbar_init(mma_bar, 1);
@@ -92,17 +92,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t phase = 0;
     bool load_pending = false, mma_pending = false;
 
-    for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    // thread 0: copies of item `it` (S_{f-1}, G_f, and A_f into buffer `ab`); the
+    // next item's copies are issued as soon as this item's MMAs have completed
+    auto issue_loads = [&](int it, int ab) {
         const int f = it / p.H, h = it % p.H;
-        if (tid == 0) {
-            mbar_arrive_expect_tx(load_bar, 3 * kboxes * BOX);
-            for (int bx = 0; bx < kboxes; ++bx) {
-                tma_load_3d(sS + bx * BOX, &tm_Sx, load_bar, 64 * bx, 0, f * p.H + h);
-                tma_load_3d(sG + bx * BOX, &tm_Gx, load_bar, 64 * bx, 0, (f + 1) * p.H + h);
-                tma_load_3d(sA + bx * BOX, &tm_A, load_bar, 64 * bx, 0, it);
-            }
+        mbar_arrive_expect_tx(load_bar, 3 * kboxes * BOX);
+        for (int bx = 0; bx < kboxes; ++bx) {
+            tma_load_3d(sS + bx * BOX, &tm_Sx, load_bar, 64 * bx, 0, f * p.H + h);
+            tma_load_3d(sG + bx * BOX, &tm_Gx, load_bar, 64 * bx, 0, (f + 1) * p.H + h);
+            tma_load_3d(sA2 + ab * TILE + bx * BOX, &tm_A, load_bar, 64 * bx, 0, it);
         }
-        load_pending = true;
+    };
+    if (tid == 0 && static_cast<int>(blockIdx.x) < items) issue_loads(blockIdx.x, 0);
+    load_pending = static_cast<int>(blockIdx.x) < items;
+    int ab = 0;
+    for (int it = blockIdx.x; it < items; it += gridDim.x, ab ^= 1) {
+        uint8_t* sA = sA2 + ab * TILE;
         bool ok = mbar_wait(load_bar, phase, p.wait_limit_ns, abort_flag);
         if (!__syncthreads_and(ok)) break;
         load_pending = false;
@@ -123,6 +128,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         mma_pending = false;
         phase ^= 1;
         tc_fence_after();
+        if (it + static_cast<int>(gridDim.x) < items) {
+            if (tid == 0) issue_loads(it + gridDim.x, ab ^ 1);
+            load_pending = true;
+        }
 
         // thread j holds row j of P (TMEM lane j): the trace term, <P, A> with
         // row j of A from shared memory, and P^T staged for the transpose
@@ -252,27 +261,32 @@ __global__ void __launch_bounds__(THREADS, 1)
     // whose S_f, G_f and W_f stay in shared memory
     const long long u_begin = (static_cast<long long>(blockIdx.x) * p.units) / gridDim.x;
     const long long u_end = (static_cast<long long>(blockIdx.x + 1) * p.units) / gridDim.x;
+    // thread 0: TMA loads of unit u (the tiles of the previous unit are no longer read:
+    // its MMAs have completed and its epilogue reads only TMEM and global memory)
+    auto issue_loads = [&](long long u) {
+        const int item = static_cast<int>(u / p.ntile), tile = static_cast<int>(u % p.ntile);
+        const int f = item / p.H, h = item % p.H;
+        const bool new_item = item != loaded_item;
+        const uint32_t bytes = (kb + 2 * vb) * BOX + (new_item ? 3 * kb * BOX : 0);
+        mbar_arrive_expect_tx(load_bar, bytes);
+        for (int bx = 0; bx < kb; ++bx) tma_load_4d(sK + bx * BOX, &tm_k, load_bar, 64 * bx, h, tile * 128, f);
+        for (int bx = 0; bx < vb; ++bx) {
+            tma_load_4d(sV + bx * BOX, &tm_v, load_bar, 64 * bx, h, tile * 128, f);
+            tma_load_4d(sO + bx * BOX, &tm_do, load_bar, 64 * bx, h, tile * 128, f);
+        }
+        if (new_item)
+            for (int bx = 0; bx < kb; ++bx) {
+                tma_load_3d(sS + bx * BOX, &tm_Sx, load_bar, 64 * bx, 0, (f + 1) * p.H + h);  // S_f
+                tma_load_3d(sG + bx * BOX, &tm_Gx, load_bar, 64 * bx, 0, (f + 1) * p.H + h);  // G_f
+                tma_load_3d(sW + bx * BOX, &tm_W, load_bar, 64 * bx, 0, item);
+            }
+        loaded_item = item;
+    };
+    if (tid == 0 && u_begin < u_end) issue_loads(u_begin);
+    load_pending = u_begin < u_end;
     for (long long u = u_begin; u < u_end; ++u) {
         const int item = static_cast<int>(u / p.ntile), tile = static_cast<int>(u % p.ntile);
         const int f = item / p.H, h = item % p.H;
-        if (tid == 0) {
-            const bool new_item = item != loaded_item;
-            const uint32_t bytes = (kb + 2 * vb) * BOX + (new_item ? 3 * kb * BOX : 0);
-            mbar_arrive_expect_tx(load_bar, bytes);
-            for (int bx = 0; bx < kb; ++bx) tma_load_4d(sK + bx * BOX, &tm_k, load_bar, 64 * bx, h, tile * 128, f);
-            for (int bx = 0; bx < vb; ++bx) {
-                tma_load_4d(sV + bx * BOX, &tm_v, load_bar, 64 * bx, h, tile * 128, f);
-                tma_load_4d(sO + bx * BOX, &tm_do, load_bar, 64 * bx, h, tile * 128, f);
-            }
-            if (new_item)
-                for (int bx = 0; bx < kb; ++bx) {
-                    tma_load_3d(sS + bx * BOX, &tm_Sx, load_bar, 64 * bx, 0, (f + 1) * p.H + h);  // S_f
-                    tma_load_3d(sG + bx * BOX, &tm_Gx, load_bar, 64 * bx, 0, (f + 1) * p.H + h);  // G_f
-                    tma_load_3d(sW + bx * BOX, &tm_W, load_bar, 64 * bx, 0, item);
-                }
-        }
-        loaded_item = item;
-        load_pending = true;
         bool ok = mbar_wait(load_bar, phase, p.wait_limit_ns, abort_flag);
         if (!__syncthreads_and(ok)) break;
         load_pending = false;
@@ -304,7 +318,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         mma_pending = false;
         phase ^= 1;
         tc_fence_after();
-
         // thread n: token row n of the tile (TMEM lane n)
         const int n = tid;
         const int token = tile * 128 + n;
@@ -312,8 +325,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         const size_t th = (static_cast<size_t>(f) * p.N + (valid ? token : 0)) * p.H + h;
         const float bn = valid ? p.beta[th] : 0.0f;
         const uint32_t trow = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+        // 8 bf16 of row n of a K-major token tile, columns c..c+7 (c % 8 == 0)
+        auto row8 = [&](const uint8_t* tilep, int c, float* x) {
+            const int cc = c & 63;
+            const uint4 w = *reinterpret_cast<const uint4*>(tilep + (c >> 6) * BOX + n * 128 +
+                                                            (((cc >> 3) ^ (n & 7)) << 4));
+            const uint32_t* ws = reinterpret_cast<const uint32_t*>(&w);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e]));
+                x[2 * e] = f2.x;
+                x[2 * e + 1] = f2.y;
+            }
+        };
         float dbeta = 0.0f;
-        // dk = beta (T1 + T2), dbeta += (T1 . k) / 2 ; dq = T4
+        // dk = beta (T1 + T2), dbeta += (T1 . k) / 2
         for (int c0 = 0; c0 < p.dk; c0 += 32) {
             uint32_t t1[32], t2[32];
             tmem_ld32(trow + 0 + c0, t1);
@@ -321,15 +347,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_wait_ld();
             uint32_t pk[16];
 #pragma unroll
-            for (int t = 0; t < 32; t += 2) {
-                const int c = c0 + t;
-                const int cc = c & 63;
-                const __nv_bfloat162 k2 = *reinterpret_cast<const __nv_bfloat162*>(
-                    sK + (c >> 6) * BOX + n * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2);
-                const float2 kf = __bfloat1622float2(k2);
-                const float a0 = __uint_as_float(t1[t]), a1 = __uint_as_float(t1[t + 1]);
-                dbeta += 0.5f * (a0 * kf.x + a1 * kf.y);
-                pk[t / 2] = pack_bf16x2(bn * (a0 + __uint_as_float(t2[t])), bn * (a1 + __uint_as_float(t2[t + 1])));
+            for (int q8 = 0; q8 < 4; ++q8) {
+                float kx[8];
+                row8(sK, c0 + 8 * q8, kx);
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    const int t = 8 * q8 + e;
+                    const float a0 = __uint_as_float(t1[t]), a1 = __uint_as_float(t1[t + 1]);
+                    dbeta += 0.5f * (a0 * kx[e] + a1 * kx[e + 1]);
+                    pk[t / 2] = pack_bf16x2(bn * (a0 + __uint_as_float(t2[t])), bn * (a1 + __uint_as_float(t2[t + 1])));
+                }
             }
             if (valid) {
                 __nv_bfloat16* dst = p.dk_out + th * p.dk + c0;
@@ -338,6 +365,42 @@ __global__ void __launch_bounds__(THREADS, 1)
                         *reinterpret_cast<uint4*>(dst + 8 * q4) =
                             make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
             }
+        }
+        // dv = beta T3, dbeta += T3 . v
+        for (int c0 = 0; c0 < p.dv; c0 += 32) {
+            uint32_t t3[32];
+            tmem_ld32(trow + 256 + c0, t3);
+            tmem_wait_ld();
+            uint32_t pv[16];
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {
+                float vx[8];
+                row8(sV, c0 + 8 * q8, vx);
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    const int t = 8 * q8 + e;
+                    const float a0 = __uint_as_float(t3[t]), a1 = __uint_as_float(t3[t + 1]);
+                    dbeta += a0 * vx[e] + a1 * vx[e + 1];
+                    pv[t / 2] = pack_bf16x2(bn * a0, bn * a1);
+                }
+            }
+            if (valid) {
+                __nv_bfloat16* dst = p.dv_out + th * p.dv + c0;
+                for (int q4 = 0; q4 < 4; ++q4)
+                    if (c0 + 8 * q4 < p.dv)
+                        *reinterpret_cast<uint4*>(dst + 8 * q4) =
+                            make_uint4(pv[4 * q4], pv[4 * q4 + 1], pv[4 * q4 + 2], pv[4 * q4 + 3]);
+            }
+        }
+        if (valid) p.d_beta[th] = dbeta;
+        // the token tiles are no longer read: the next unit's copies overlap the dq part
+        __syncthreads();
+        if (u + 1 < u_end) {
+            if (tid == 0) issue_loads(u + 1);
+            load_pending = true;
+        }
+        // dq = T4
+        for (int c0 = 0; c0 < p.dk; c0 += 32) {
             uint32_t t4[32];
             tmem_ld32(trow + 384 + c0, t4);
             tmem_wait_ld();
@@ -352,32 +415,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                             pack_bf16x2(__uint_as_float(t4[8 * q4 + 6]), __uint_as_float(t4[8 * q4 + 7])));
             }
         }
-        // dv = beta T3, dbeta += T3 . v
-        for (int c0 = 0; c0 < p.dv; c0 += 32) {
-            uint32_t t3[32];
-            tmem_ld32(trow + 256 + c0, t3);
-            tmem_wait_ld();
-            uint32_t pv[16];
-#pragma unroll
-            for (int t = 0; t < 32; t += 2) {
-                const int c = c0 + t;
-                const int cc = c & 63;
-                const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(
-                    sV + (c >> 6) * BOX + n * 128 + (((cc >> 3) ^ (n & 7)) << 4) + (cc & 7) * 2);
-                const float2 vf = __bfloat1622float2(v2);
-                const float a0 = __uint_as_float(t3[t]), a1 = __uint_as_float(t3[t + 1]);
-                dbeta += a0 * vf.x + a1 * vf.y;
-                pv[t / 2] = pack_bf16x2(bn * a0, bn * a1);
-            }
-            if (valid) {
-                __nv_bfloat16* dst = p.dv_out + th * p.dv + c0;
-                for (int q4 = 0; q4 < 4; ++q4)
-                    if (c0 + 8 * q4 < p.dv)
-                        *reinterpret_cast<uint4*>(dst + 8 * q4) =
-                            make_uint4(pv[4 * q4], pv[4 * q4 + 1], pv[4 * q4 + 2], pv[4 * q4 + 3]);
-            }
-        }
-        if (valid) p.d_beta[th] = dbeta;
         tc_fence_before();
         __syncthreads();  // tiles and accumulators are reused by the next unit
     }
