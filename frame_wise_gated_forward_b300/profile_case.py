@@ -1,5 +1,6 @@
-"""Run the frame-wise GDN forward a few times on a 60 s-sequence-shaped case
-with a chosen number of latent frames, for profilers (ncu) to capture.
+"""Run the frame-wise GDN forward (or the step, the 8-bit-input forward or the
+backward) a few times on a 60 s-sequence-shaped case with a chosen number of
+latent frames, for profilers (ncu) to capture.
 
     python -m frame_wise_gated_forward_b300.profile_case --frames 31 --iters 2
 
@@ -28,17 +29,32 @@ def main():
     ap.add_argument("--tokens", type=int, default=880)
     ap.add_argument("--d", type=int, default=128)
     ap.add_argument("--iters", type=int, default=2)
-    ap.add_argument("--step", action="store_true", help="profile gdn_frame_step instead (F ignored)")
+    ap.add_argument("--mode", choices=["forward", "step", "fp8", "backward"], default="forward",
+                    help="gdn_frame_forward, gdn_frame_step (F ignored), gdn_frame_forward_fp8 or "
+                         "gdn_frame_backward")
+    ap.add_argument("--step", action="store_true", help="same as --mode step")
     a = ap.parse_args()
+    mode = "step" if a.step else a.mode
     build.build()
-    F = 1 if a.step else a.frames
-    x = inputs.draw(a.batch, a.heads, F, a.tokens, a.d, a.d, seed=0, s0_std=0.0)
-    xd = {k: v.cuda() for k, v in x.items()}
-    if a.step:
-        args = [xd[k][:, 0].contiguous() for k in ("q", "k", "v", "alpha", "beta")]
-        call = lambda: api.frame_step(*args, xd["state_in"])  # noqa: E731
+    F = 1 if mode == "step" else a.frames
+    B, H, N, d = a.batch, a.heads, a.tokens, a.d
+    if mode == "fp8":
+        x8 = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inputs.draw_fp8(B, H, F, N, d, d, seed=0).items()}
+        call = lambda: api.frame_forward_fp8(x8["q8"], x8["k8"], x8["v8"], x8["q_scale"], x8["k_scale"],  # noqa: E731
+                                             x8["v_scale"], x8["alpha"], x8["beta"], None)
     else:
-        call = lambda: api.frame_forward(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], None)  # noqa: E731
+        x = inputs.draw(B, H, F, N, d, d, seed=0, s0_std=0.0)
+        xd = {k: v.cuda() for k, v in x.items()}
+        if mode == "step":
+            args = [xd[k][:, 0].contiguous() for k in ("q", "k", "v", "alpha", "beta")]
+            call = lambda: api.frame_step(*args, xd["state_in"])  # noqa: E731
+        elif mode == "backward":
+            g = torch.Generator().manual_seed(1)
+            d_out = torch.randn((B, F, N, H, d), generator=g).to(torch.bfloat16).cuda()
+            call = lambda: api.frame_backward(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], None,  # noqa: E731
+                                              d_out)
+        else:
+            call = lambda: api.frame_forward(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], None)  # noqa: E731
     call()
     api.sync_status()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -47,8 +63,7 @@ def main():
         call()
     e1.record()
     api.sync_status()
-    print(f"{'step' if a.step else 'forward'} B={a.batch} H={a.heads} F={F} N={a.tokens} d={a.d}: "
-          f"{e0.elapsed_time(e1) / a.iters:.4f} ms/call")
+    print(f"{mode} B={B} H={H} F={F} N={N} d={d}: {e0.elapsed_time(e1) / a.iters:.4f} ms/call")
 
 
 if __name__ == "__main__":
