@@ -9,7 +9,7 @@
 // all of A_f), so the dv rows of each head are split over CTAs, R rows each,
 // with no communication.  Per frame one CTA computes its slice of S A_f on
 // the tensor core as C^T = A_f S_slice^T:
-//     M = 128 (dk index j, zero-padded), N = R (rows of the slice), K = dk
+//     M = 128 (dk index j, zero-padded), N = rows of the slice, K = dk
 // with both operands K-major in 128-byte-swizzled shared memory: A_f comes
 // from the bf16 workspace by TMA together with the CTA's R rows of U_f
 // (fp32, unswizzled) through a prefetch ring, so no global load sits on the
@@ -18,15 +18,17 @@
 // registers: thread j (TMEM lane j) owns column j of the slice, which is
 // exactly the layout tcgen05.ld returns C in.
 //
-// Warp roles (192 threads): warps 0-3 compute (thread 0 also issues the
-// MMAs); warp 4 publishes each frame's bf16 state image with a TMA store to the
-// per-frame state buffer that phase 3 reads (and, when the scan runs fused
-// with phase 3, then raises that item's ready count); warp 5 refills the
-// A_f/U_f ring.  Compute hands each image to the publisher through an
-// mbarrier and keeps up to NIMG images in flight, so neither store latency
-// nor load issue sits on the frame-to-frame chain.  The S A_f product is
-// split over NACC independent accumulators (halves of the dk reduction) that
-// the tensor core can work on concurrently.
+// A slice of more than 32 rows is split into independent chains of 32 rows,
+// each with its own MMA (N = 32), accumulator columns and image-ready
+// barrier: while one chain's MMA runs, the compute threads update another.
+//
+// Warp roles (224 threads): warps 0-3 compute; warp 4 publishes each frame's
+// bf16 state image with a TMA store to the per-frame state buffer that phase
+// 3 reads (and, when the scan runs fused with phase 3, then raises that item's
+// ready count); warp 5 refills the A_f/U_f ring; warp 6 issues the MMAs.
+// Compute hands each image to the publisher and the MMA issuer through
+// mbarriers and keeps up to NIMG images in flight, so neither store latency
+// nor load issue sits on the frame-to-frame chain.
 #pragma once
 
 #include "gdn_ptx.cuh"
@@ -35,25 +37,25 @@ namespace gdn {
 namespace k2 {
 
 constexpr int COMPUTE_THREADS = 128;
-constexpr int THREADS = 192;                 // + publisher warp + loader warp
+constexpr int THREADS = 224;                 // + publisher, loader and MMA-issuer warps
 constexpr int ABOX_BYTES = 128 * 128;        // 128 rows x 128 B
 constexpr int ATILE_BYTES = 2 * ABOX_BYTES;  // A_f, dk padded to 128
-#ifndef GDN_SCAN_NACC
-#define GDN_SCAN_NACC 1
-#endif
-constexpr int NACC = GDN_SCAN_NACC;
 
 template <int R>
 struct Cfg {
-    static constexpr int ASTAGES = R >= 64 ? 3 : 4;
-    static constexpr int NIMG = R >= 64 ? 2 : 4;               // bf16 state images in flight
+    static constexpr int RS = R < 32 ? R : 32;                 // rows per independent chain (MMA N)
+    static constexpr int NC = R / RS;                          // chains per slice
+    static constexpr int ASTAGES = R >= 64 ? 2 : 4;
+    static constexpr int NIMG = 4;                             // bf16 state images in flight
     static constexpr int SBOX_BYTES = R * 128;
     static constexpr int STILE_BYTES = 2 * SBOX_BYTES;
     static constexpr int UTILE_BYTES = R * 128 * 4;            // R rows x 128 fp32 (dk padded)
     static constexpr int STAGE_BYTES = ATILE_BYTES + UTILE_BYTES;
-    static constexpr int TMEM_COLS = NACC * R < 32 ? 32 : NACC * R;
+    static constexpr int TMEM_COLS = R < 32 ? 32 : R;
     static constexpr size_t SMEM_BYTES = 1024 + ASTAGES * STAGE_BYTES + NIMG * STILE_BYTES + 512;
+    static_assert(R % RS == 0, "whole chains");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
+    static_assert((2 * ASTAGES + NC + NIMG * NC + NIMG + 1) * 8 + 8 <= 512, "barrier area");
 };
 
 struct Params {
@@ -90,14 +92,16 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_A, const CUtenso
     using C = Cfg<R>;
     constexpr int AS = C::ASTAGES;
     constexpr int NI = C::NIMG;
+    constexpr int NC = C::NC;
+    constexpr int RS = C::RS;
     uint8_t* aring = smem;                                  // [AS][A tile | U rows]
     uint8_t* sop = smem + AS * C::STAGE_BYTES;              // [NI][STILE_BYTES] bf16 state images
     uint64_t* bars = reinterpret_cast<uint64_t*>(sop + NI * C::STILE_BYTES);
-    uint64_t* afull = bars;                                 // [AS] loader -> compute
+    uint64_t* afull = bars;                                 // [AS] loader -> compute, MMA
     uint64_t* slot_free = afull + AS;                       // [AS] compute -> loader
-    uint64_t* mma_done = slot_free + AS;                    // [1]
-    uint64_t* img_ready = mma_done + 1;                     // [NI] compute -> publisher, MMA
-    uint64_t* img_free = img_ready + NI;                    // [NI] publisher -> compute
+    uint64_t* mma_done = slot_free + AS;                    // [NC] MMA -> compute
+    uint64_t* img_ready = mma_done + NC;                    // [NI][NC] compute -> MMA, publisher
+    uint64_t* img_free = img_ready + NI * NC;               // [NI] publisher -> compute
     uint64_t* final_bar = img_free + NI;                    // [1]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -111,7 +115,6 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_A, const CUtenso
     const int aboxes = p.dk > 64 ? 2 : 1;
     const int sboxes = aboxes;
     const int nk = (p.dk + 15) / 16;
-    const int nacc = nk < NACC ? nk : NACC;
     const bool jv = j < p.dk;
     // step f of the scan handles latent frame fr(f): f itself, or F-1-f when reversed
     auto fr = [&](int f) { return p.reverse ? p.F - 1 - f : f; };
@@ -127,9 +130,9 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_A, const CUtenso
             mbar_init(&afull[s], 1);
             mbar_init(&slot_free[s], COMPUTE_THREADS);
         }
-        mbar_init(mma_done, 1);
+        for (int c = 0; c < NC; ++c) mbar_init(&mma_done[c], 1);
         for (int x = 0; x < NI; ++x) {
-            mbar_init(&img_ready[x], COMPUTE_THREADS);
+            for (int c = 0; c < NC; ++c) mbar_init(&img_ready[x * NC + c], COMPUTE_THREADS);
             mbar_init(&img_free[x], 1);
         }
         mbar_init(final_bar, 1);
@@ -162,87 +165,84 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_A, const CUtenso
         for (int r = 0; r < R; ++r)
             *reinterpret_cast<__nv_bfloat16*>(sop + sop_offset<R>(r, j)) = __float2bfloat16_rn(S[r]);
         fence_proxy_async_smem();
-        mbar_arrive(&img_ready[0]);  // initial image (never stored: the publisher skips it)
+        for (int c = 0; c < NC; ++c) mbar_arrive(&img_ready[c]);  // initial image (never stored)
         float a_next = decay_gate(p, __ldg(p.alpha + static_cast<size_t>(b * p.F + fr(0)) * p.H + h));
 
-        constexpr uint32_t IDESC = idesc_bf16(128, R, 0, 0);
         int f = 0;
         for (; f < p.F; ++f) {
             const int slot = f % AS;
-            const int cur = f % NI;        // image of the state after frame f - 1
             const int nxt = (f + 1) % NI;  // image of the state after frame f
-            if (tid == 0) {
-                // the previous state's image is complete, and this frame's A_f has landed
-                const bool go = mbar_wait(&img_ready[cur], static_cast<uint32_t>((f / NI) & 1),
-                                          p.wait_limit_ns, abort_flag) &&
-                                mbar_wait(&afull[slot], static_cast<uint32_t>((f / AS) & 1), p.wait_limit_ns,
-                                          abort_flag);
-                if (go) {
-                    tc_fence_after();
-                    const uint32_t a_base = smem_u32(aring + slot * C::STAGE_BYTES);
-                    const uint32_t b_base = smem_u32(sop + cur * C::STILE_BYTES);
-                    for (int kk = 0; kk < nk; ++kk) {
-                        const int acc = (kk * nacc) / nk;  // contiguous halves of the reduction
-                        const bool first = kk == (acc * nk + nacc - 1) / nacc;
-                        const uint64_t ad = smem_desc(a_base + (kk >> 2) * ABOX_BYTES + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = smem_desc(b_base + (kk >> 2) * C::SBOX_BYTES + (kk & 3) * 32, 16, 1024);
-                        mma_bf16(*tmem_slot + acc * R, ad, bd, IDESC, first ? 0u : 1u);
-                    }
-                    mma_commit(mma_done);
-                }
-            }
             const float a_f = a_next;
             if (f + 1 < p.F) a_next = decay_gate(p, __ldg(p.alpha + static_cast<size_t>(b * p.F + fr(f + 1)) * p.H + h));
 
             // the buffer this frame's image goes to was last stored NI frames ago
             bool ok = f < NI || mbar_wait(&img_free[nxt], static_cast<uint32_t>(((f / NI) - 1) & 1),
                                           p.wait_limit_ns, abort_flag);
-            ok = ok && mbar_wait(&afull[slot], static_cast<uint32_t>((f / AS) & 1), p.wait_limit_ns, abort_flag) &&
-                 mbar_wait(mma_done, static_cast<uint32_t>(f & 1), p.wait_limit_ns, abort_flag);
+            ok = ok && mbar_wait(&afull[slot], static_cast<uint32_t>((f / AS) & 1), p.wait_limit_ns, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
-            tc_fence_after();
-            // per chunk of RC rows: batch every read first (U rows, then the
-            // accumulators), then update the state and write its image
-            constexpr int RC = R < 32 ? R : 32;
             const float* urow = reinterpret_cast<const float*>(aring + slot * C::STAGE_BYTES + ATILE_BYTES) + j;
             uint8_t* img = sop + nxt * C::STILE_BYTES;
+            // chain by chain: read the chain's U rows and accumulator, update its
+            // rows of the state, write them to the image and hand the chain on
 #pragma unroll
-            for (int rc0 = 0; rc0 < R; rc0 += RC) {
-                float u[RC];
+            for (int c = 0; c < NC; ++c) {
+                float u[RS];
 #pragma unroll
-                for (int r = 0; r < RC; ++r) u[r] = urow[(rc0 + r) * 128];
-                uint32_t c[NACC][RC];
+                for (int r = 0; r < RS; ++r) u[r] = urow[(c * RS + r) * 128];
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&mma_done[c], static_cast<uint32_t>(f & 1), p.wait_limit_ns, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t cc[RS];
 #pragma unroll
-                for (int a = 0; a < NACC; ++a) {
-                    if (a < nacc) {
-#pragma unroll
-                        for (int rc = 0; rc < RC; rc += 16)
-                            tmem_ld16(tmem_warp + a * R + rc0 + rc, *reinterpret_cast<uint32_t(*)[16]>(&c[a][rc]));
-                    }
-                }
+                for (int q = 0; q < RS; q += 16)
+                    tmem_ld16(tmem_warp + c * RS + q, *reinterpret_cast<uint32_t(*)[16]>(&cc[q]));
                 tmem_wait_ld();
 #pragma unroll
-                for (int r = 0; r < RC; ++r) {
-                    float cr = __uint_as_float(c[0][r]);
-#pragma unroll
-                    for (int a = 1; a < NACC; ++a)
-                        if (a < nacc) cr += __uint_as_float(c[a][r]);
-                    S[rc0 + r] = a_f * (S[rc0 + r] - cr) + u[r];
-                    *reinterpret_cast<__nv_bfloat16*>(img + sop_offset<R>(rc0 + r, j)) =
-                        __float2bfloat16_rn(S[rc0 + r]);
+                for (int r = 0; r < RS; ++r) {
+                    const int row = c * RS + r;
+                    S[row] = a_f * (S[row] - __uint_as_float(cc[r])) + u[r];
+                    *reinterpret_cast<__nv_bfloat16*>(img + sop_offset<R>(row, j)) = __float2bfloat16_rn(S[row]);
                 }
+                tc_fence_before();
+                fence_proxy_async_smem();
+                mbar_arrive(&img_ready[nxt * NC + c]);
             }
-            tc_fence_before();
-            mbar_arrive(&slot_free[slot]);  // U read, MMA that read A_f retired, accumulators drained
-            fence_proxy_async_smem();
-            mbar_arrive(&img_ready[nxt]);
+            if (!ok) break;
+            mbar_arrive(&slot_free[slot]);  // U read, the MMAs that read A_f retired
         }
         if (f == p.F && p.state_out != nullptr && jv) {
 #pragma unroll
             for (int r = 0; r < R; ++r) p.state_out[state_off + static_cast<size_t>(r0 + r) * p.dk + j] = S[r];
         }
-        if (tid == 0) {
+    } else if (warp == 6) {
+        // -------------------------------------------------------- MMA issuer
+        if ((tid & 31) == 0) {
+            constexpr uint32_t IDESC = idesc_bf16(128, RS, 0, 0);
+            bool stop = false;
+            for (int f = 0; f < p.F && !stop; ++f) {
+                const int slot = f % AS;
+                const int cur = f % NI;  // image of the state after frame f - 1
+                if (!mbar_wait(&afull[slot], static_cast<uint32_t>((f / AS) & 1), p.wait_limit_ns, abort_flag))
+                    break;
+                for (int c = 0; c < NC; ++c) {
+                    if (!mbar_wait(&img_ready[cur * NC + c], static_cast<uint32_t>((f / NI) & 1), p.wait_limit_ns,
+                                   abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(aring + slot * C::STAGE_BYTES);
+                    const uint32_t b_base = smem_u32(sop + cur * C::STILE_BYTES) + c * RS * 128;
+                    for (int kk = 0; kk < nk; ++kk) {
+                        const uint64_t ad = smem_desc(a_base + (kk >> 2) * ABOX_BYTES + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd = smem_desc(b_base + (kk >> 2) * C::SBOX_BYTES + (kk & 3) * 32, 16, 1024);
+                        mma_bf16(*tmem_slot + c * RS, ad, bd, IDESC, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&mma_done[c]);
+                }
+            }
             mma_commit(final_bar);
             mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
         }
@@ -258,11 +258,13 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_A, const CUtenso
                 for (; published < f_end; ++published) red_release_add(flags + item_of(published), 1);
             };
             int f = 0;
+            bool stop = false;
             for (; f < p.F; ++f) {
                 const int x = (f + 1) % NI;  // buffer holding the image of the state after frame f
-                if (!mbar_wait(&img_ready[x], static_cast<uint32_t>(((f + 1) / NI) & 1), p.wait_limit_ns,
-                               abort_flag))
-                    break;
+                for (int c = 0; c < NC && !stop; ++c)
+                    stop = !mbar_wait(&img_ready[x * NC + c], static_cast<uint32_t>(((f + 1) / NI) & 1),
+                                      p.wait_limit_ns, abort_flag);
+                if (stop) break;
                 const uint8_t* img = sop + x * C::STILE_BYTES;
                 for (int bx = 0; bx < sboxes; ++bx)
                     tma_store_3d(tm_S, img + bx * C::SBOX_BYTES, 64 * bx, r0, item_of(f));
