@@ -412,6 +412,7 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
     p3.reverse = a.reverse;
     p3.norm_q = a.prologue;
     p3.q_scale = a.fp8 ? a.q_scale : 1.0f;
+    p3.b_mn = 0;
     p3.wait_limit_ns = lim;
     const int n_scan = a.B * a.H * p2.rsplit;
     if (Rf != 0) {
@@ -659,18 +660,40 @@ gdn_status bwd_row(const BwdArgs& a, int b, uint8_t* ws, const BwdLayout& L, con
         gdn::bwd::frame_grad_kernel<<<std::min(F * H, ds->sms), gdn::bwd::THREADS, gdn::bwd::FRAME_SMEM, st>>>(
             tm_Sx, tm_Gx, tm_A, pf);
     }
-    // per-token gradients
+    // dq = dO S_f: the output kernel with the state read MN-major (A = dO, width dv; out width dk)
     {
-        CUtensorMap tm_k, tm_v, tm_do, tm_Sx, tm_Gx, tm_W;
+        CUtensorMap tm_do, tm_S, tm_dq;
+        if (!encode_tokens(&tm_do, dO, F, N, H, dv, gdn::k3::TILE_M) ||
+            !encode_mats(&tm_S, Sx + H * sd, static_cast<long long>(F) * H, dv, dk, 128) ||
+            !encode_tokens(&tm_dq, reinterpret_cast<__nv_bfloat16*>(a.dq) + b * tokH * dk, F, N, H, dk, 32))
+            return GDN_ERR_LAUNCH;
+        gdn::k3::Params p3;
+        p3.B = 1;
+        p3.H = H;
+        p3.F = F;
+        p3.N = N;
+        p3.dk = dv;   // the A operand's (dO's) width
+        p3.dv = dk;   // the output's (dq's) width
+        p3.ntile = (N + gdn::k3::TILE_M - 1) / gdn::k3::TILE_M;
+        p3.total = static_cast<long long>(F) * H * p3.ntile;
+        p3.reverse = 0;
+        p3.norm_q = 0;
+        p3.q_scale = 1.0f;
+        p3.b_mn = 1;
+        p3.wait_limit_ns = g_wait_limit_ns.load();
+        gdn::k3::output_kernel<false><<<static_cast<int>(std::min<long long>(p3.total, ds->sms)),
+                                        gdn::k3::threads<false>(), gdn::k3::SMEM_BYTES, st>>>(tm_do, tm_S, tm_dq, p3);
+    }
+    // dk, dv, dbeta
+    {
+        CUtensorMap tm_k, tm_v, tm_Gx, tm_W;
         const long long slots = static_cast<long long>(F + 1) * H;
         if (!encode_tokens(&tm_k, k, F, N, H, dk, 128) || !encode_tokens(&tm_v, v, F, N, H, dv, 128) ||
-            !encode_tokens(&tm_do, dO, F, N, H, dv, 128) || !encode_mats(&tm_Sx, Sx, slots, dv, dk, 128) ||
             !encode_mats(&tm_Gx, Gx, slots, dv, dk, 128) ||
             !encode_mats(&tm_W, Wb, static_cast<long long>(F) * H, dk, dk, 128))
             return GDN_ERR_LAUNCH;
         gdn::bwd::TokenParams pt;
         pt.beta = beta;
-        pt.dq_out = reinterpret_cast<__nv_bfloat16*>(a.dq) + b * tokH * dk;
         pt.dk_out = reinterpret_cast<__nv_bfloat16*>(a.dk) + b * tokH * dk;
         pt.dv_out = reinterpret_cast<__nv_bfloat16*>(a.dv) + b * tokH * dv;
         pt.d_beta = a.d_beta + b * tokH;
@@ -682,8 +705,8 @@ gdn_status bwd_row(const BwdArgs& a, int b, uint8_t* ws, const BwdLayout& L, con
         pt.ntile = (N + 127) / 128;
         pt.units = static_cast<long long>(F) * H * pt.ntile;
         pt.wait_limit_ns = g_wait_limit_ns.load();
-        gdn::bwd::token_grad_kernel<<<static_cast<int>(std::min<long long>(pt.units, ds->sms)), gdn::bwd::THREADS,
-                                      gdn::bwd::TOKEN_SMEM, st>>>(tm_k, tm_v, tm_do, tm_Sx, tm_Gx, tm_W, pt);
+        gdn::bwd::token_grad_kernel<<<static_cast<int>(std::min<long long>(pt.units, ds->sms)),
+                                      gdn::bwd::TOKEN_THREADS, gdn::bwd::TOKEN_SMEM, st>>>(tm_k, tm_v, tm_Gx, tm_W, pt);
     }
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }

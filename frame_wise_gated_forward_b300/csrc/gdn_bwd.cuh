@@ -11,14 +11,15 @@
 //     P_f = S_{f-1}^T G_f,  dalpha_f = tr P_f - <P_f, A_f>,
 //     W_f = dA_f + dA_f^T = -alpha_f (P_f + P_f^T)
 // (frame_grad_kernel) and, per token n of frame f,
-//     dq_n = S_f^T do_n,  dk_n = beta_n (W_f k_n + G_f^T v_n),
-//     dv_n = beta_n G_f k_n,  dbeta_n = k_n^T W_f k_n / 2 + v_n^T G_f k_n
-// (token_grad_kernel).  Both are tcgen05 MMAs on operands TMA-loaded into
+//     dk_n = beta_n (W_f k_n + G_f^T v_n),  dv_n = beta_n G_f k_n,
+//     dbeta_n = k_n^T W_f k_n / 2 + v_n^T G_f k_n       (token_grad_kernel)
+//     dq_n = S_f^T do_n           (the forward's output kernel, S_f MN-major).  Both are tcgen05 MMAs on operands TMA-loaded into
 // 128-byte-swizzled shared memory; the bf16 per-frame states S and G are read
 // MN-major or K-major from the same tile as each product needs.
 //
-// Both kernels take one batch row (items f*H + h) and run one work unit at a
-// time per CTA (load, MMA, epilogue), with bounded waits throughout.
+// Both kernels take one batch row (items f*H + h); each CTA runs one work
+// unit's MMAs and epilogue at a time while the next unit's copies are in
+// flight.  Every wait is bounded.
 #pragma once
 
 #include "gdn_ptx.cuh"
@@ -191,12 +192,29 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ------------------------------------------------------------ token grads
-constexpr size_t TOKEN_SMEM = 1024 + 6 * TILE + 256;
+// dq = dO S_f runs on the forward's output kernel with the state read
+// MN-major (k3::Params::b_mn); this kernel forms dk, dv and dbeta from two
+// accumulators per 128-token tile, M = 128 tokens each:
+//     T12 = K W_f + V G_f     T3 = K G_f^T
+// so dk = beta T12, dv = beta T3, and, since T12 . k_n = k_n^T W_f k_n +
+// v_n^T G_f k_n and T3 . v_n = v_n^T G_f k_n,
+//     dbeta_n = (T12 . k_n + T3 . v_n) / 2.
+// Two accumulator pairs fill TMEM's 512 columns, so one tile's MMAs run while
+// the previous tile's epilogue drains.  Warp roles (320 threads): warp 0 TMA
+// producer, warp 1 TMEM owner and MMA issuer, warps 2-9 epilogue (two warps
+// per TMEM lane quarter, one per half of the columns).  Token tiles (k, v)
+// stream through a 2-deep ring; a slot is released when the epilogue has read
+// its k and v rows.  G_f (K-major for T3, MN-major for T12) and W_f (K-major,
+// symmetric) are reloaded when the item changes.
+constexpr int TOKEN_THREADS = 320;
+constexpr int TOKEN_EPI = 256;
+constexpr int KV_STAGES = 2;
+constexpr size_t TOKEN_SMEM = 1024 + (2 * KV_STAGES + 2) * TILE + 256 + 2 * 128 * 4;
 static_assert(TOKEN_SMEM <= 232448, "shared memory");
 
 struct TokenParams {
     const float* beta;         // [F, N, H]
-    __nv_bfloat16 *dq_out, *dk_out, *dv_out;  // [F, N, H, d] out
+    __nv_bfloat16 *dk_out, *dv_out;  // [F, N, H, d] out
     float* d_beta;             // [F, N, H] out
     int H, F, N, dk, dv;
     int ntile;                 // ceil(N / 128)
@@ -204,47 +222,52 @@ struct TokenParams {
     unsigned long long wait_limit_ns;
 };
 
-// Unit u: item u / ntile = f*H + h, token tile u % ntile.  Four accumulators
-// of 128 columns, M = 128 tokens each:
-//     T1 = K W_f   T2 = V G_f   T3 = K G_f^T   T4 = dO S_f
-// token tiles (k, v, dO) K-major; W_f (symmetric) and G_f as K-major B for
-// T1 / T3; G_f and S_f MN-major for T2 / T4.
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(TOKEN_THREADS, 1)
     token_grad_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_Sx,
                       const __grid_constant__ CUtensorMap tm_Gx, const __grid_constant__ CUtensorMap tm_W,
                       const TokenParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sK = smem;
-    uint8_t* sV = sK + TILE;
-    uint8_t* sO = sV + TILE;
-    uint8_t* sS = sO + TILE;
-    uint8_t* sG = sS + TILE;
+    uint8_t* ring = smem;                              // [KV_STAGES][K tile | V tile]
+    uint8_t* sG = ring + KV_STAGES * 2 * TILE;
     uint8_t* sW = sG + TILE;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sW + TILE);
-    uint64_t* load_bar = bars;
-    uint64_t* mma_bar = bars + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
+    uint64_t* kfull = bars;                            // [2] TMA landed k, v
+    uint64_t* kempty = kfull + KV_STAGES;              // [2] epilogue read the rows
+    uint64_t* tfull = kempty + KV_STAGES;              // [2] accumulator pair ready
+    uint64_t* tempty = tfull + 2;                      // [2] accumulator pair drained
+    uint64_t* gw_full = tempty + 2;                    // G_f, W_f landed
+    uint64_t* gw_empty = gw_full + 1;                  // the item's last MMAs retired
+    uint64_t* final_bar = gw_empty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* dbh = reinterpret_cast<float*>(sW + TILE + 256);   // [2][128] upper column half's dbeta part
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int kb = p.dk > 64 ? 2 : 1, vb = p.dv > 64 ? 2 : 1;
     if (kb < 2 || vb < 2)  // boxes that are never loaded must read as zero
-        for (int i = tid; i < 6 * TILE / 16; i += THREADS) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < (2 * KV_STAGES + 2) * TILE / 16; i += TOKEN_THREADS)
+            reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
-        mbar_init(load_bar, 1);
-        mbar_init(mma_bar, 1);
+        for (int s = 0; s < KV_STAGES; ++s) {
+            mbar_init(&kfull[s], 1);
+            mbar_init(&kempty[s], TOKEN_EPI);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], TOKEN_EPI);
+        }
+        mbar_init(gw_full, 1);
+        mbar_init(gw_empty, 1);
+        mbar_init(final_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
-        prefetch_tmap(&tm_do);
-        prefetch_tmap(&tm_Sx);
         prefetch_tmap(&tm_Gx);
         prefetch_tmap(&tm_W);
     }
-    if (warp == 0) {
+    if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
@@ -253,78 +276,94 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    uint32_t phase = 0;
-    bool load_pending = false, mma_pending = false;
-    int loaded_item = -1;
 
-    // contiguous unit ranges: a CTA's consecutive tiles mostly share an item,
-    // whose S_f, G_f and W_f stay in shared memory
+    // contiguous unit ranges: a CTA's consecutive tiles mostly share an item
     const long long u_begin = (static_cast<long long>(blockIdx.x) * p.units) / gridDim.x;
     const long long u_end = (static_cast<long long>(blockIdx.x + 1) * p.units) / gridDim.x;
-    // thread 0: TMA loads of unit u (the tiles of the previous unit are no longer read:
-    // its MMAs have completed and its epilogue reads only TMEM and global memory)
-    auto issue_loads = [&](long long u) {
-        const int item = static_cast<int>(u / p.ntile), tile = static_cast<int>(u % p.ntile);
-        const int f = item / p.H, h = item % p.H;
-        const bool new_item = item != loaded_item;
-        const uint32_t bytes = (kb + 2 * vb) * BOX + (new_item ? 3 * kb * BOX : 0);
-        mbar_arrive_expect_tx(load_bar, bytes);
-        for (int bx = 0; bx < kb; ++bx) tma_load_4d(sK + bx * BOX, &tm_k, load_bar, 64 * bx, h, tile * 128, f);
-        for (int bx = 0; bx < vb; ++bx) {
-            tma_load_4d(sV + bx * BOX, &tm_v, load_bar, 64 * bx, h, tile * 128, f);
-            tma_load_4d(sO + bx * BOX, &tm_do, load_bar, 64 * bx, h, tile * 128, f);
-        }
-        if (new_item)
-            for (int bx = 0; bx < kb; ++bx) {
-                tma_load_3d(sS + bx * BOX, &tm_Sx, load_bar, 64 * bx, 0, (f + 1) * p.H + h);  // S_f
-                tma_load_3d(sG + bx * BOX, &tm_Gx, load_bar, 64 * bx, 0, (f + 1) * p.H + h);  // G_f
-                tma_load_3d(sW + bx * BOX, &tm_W, load_bar, 64 * bx, 0, item);
+    auto item_of = [&](long long u) { return static_cast<int>(u / p.ntile); };
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int gw_item = -1, gw_loads = 0;
+            long long issued = 0;
+            for (long long u = u_begin; u < u_end; ++u) {
+                const long long i = u - u_begin;
+                const int s = static_cast<int>(i % KV_STAGES);
+                const int item = item_of(u), tile = static_cast<int>(u % p.ntile);
+                const int f = item / p.H, h = item % p.H;
+                if (!mbar_wait(&kempty[s], static_cast<uint32_t>(((i / KV_STAGES) & 1) ^ 1), p.wait_limit_ns,
+                               abort_flag))
+                    break;
+                if (item != gw_item) {
+                    if (!mbar_wait(gw_empty, static_cast<uint32_t>((gw_loads & 1) ^ 1), p.wait_limit_ns, abort_flag))
+                        break;
+                    mbar_arrive_expect_tx(gw_full, 2 * kb * BOX);
+                    for (int bx = 0; bx < kb; ++bx) {
+                        tma_load_3d(sG + bx * BOX, &tm_Gx, gw_full, 64 * bx, 0, (f + 1) * p.H + h);  // G_f
+                        tma_load_3d(sW + bx * BOX, &tm_W, gw_full, 64 * bx, 0, item);
+                    }
+                    gw_item = item;
+                    ++gw_loads;
+                }
+                uint8_t* dst = ring + s * 2 * TILE;
+                mbar_arrive_expect_tx(&kfull[s], (kb + vb) * BOX);
+                for (int bx = 0; bx < kb; ++bx) tma_load_4d(dst + bx * BOX, &tm_k, &kfull[s], 64 * bx, h, tile * 128, f);
+                for (int bx = 0; bx < vb; ++bx)
+                    tma_load_4d(dst + TILE + bx * BOX, &tm_v, &kfull[s], 64 * bx, h, tile * 128, f);
+                ++issued;
             }
-        loaded_item = item;
-    };
-    if (tid == 0 && u_begin < u_end) issue_loads(u_begin);
-    load_pending = u_begin < u_end;
-    for (long long u = u_begin; u < u_end; ++u) {
-        const int item = static_cast<int>(u / p.ntile), tile = static_cast<int>(u % p.ntile);
-        const int f = item / p.H, h = item % p.H;
-        bool ok = mbar_wait(load_bar, phase, p.wait_limit_ns, abort_flag);
-        if (!__syncthreads_and(ok)) break;
-        load_pending = false;
-        if (tid == 0) {
-            tc_fence_after();
+            // copies in flight must land before the CTA leaves (only when a wait gave up)
+            for (long long kq = (issued > KV_STAGES ? issued - KV_STAGES : 0); kq < issued; ++kq)
+                mbar_wait_drain(&kfull[kq % KV_STAGES], static_cast<uint32_t>((kq / KV_STAGES) & 1), p.wait_limit_ns);
+            if (gw_loads > 0) mbar_wait_drain(gw_full, static_cast<uint32_t>((gw_loads - 1) & 1), p.wait_limit_ns);
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
             constexpr uint32_t ID_KK = idesc_bf16(128, 128, 0, 0);   // A K-major, B K-major
             constexpr uint32_t ID_KM = idesc_bf16(128, 128, 0, 1);   // A K-major, B MN-major
             const int nkk = (p.dk + 15) / 16, nkv = (p.dv + 15) / 16;
-            const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aO = smem_u32(sO);
-            const uint32_t bS = smem_u32(sS), bG = smem_u32(sG), bW = smem_u32(sW);
-            for (int kk = 0; kk < nkk; ++kk) {   // K-steps over dk
-                const uint32_t ko = (kk >> 2) * BOX + (kk & 3) * 32;
-                const uint64_t ad = smem_desc(aK + ko, 16, SBO);
-                mma_bf16(tmem_base + 0, ad, smem_desc(bW + ko, 16, SBO), ID_KK, kk > 0 ? 1u : 0u);    // T1
-                mma_bf16(tmem_base + 256, ad, smem_desc(bG + ko, 16, SBO), ID_KK, kk > 0 ? 1u : 0u);  // T3
+            const uint32_t bG = smem_u32(sG), bW = smem_u32(sW);
+            int gw_item = -1, gw_used = 0;
+            for (long long u = u_begin; u < u_end; ++u) {
+                const long long i = u - u_begin;
+                const int s = static_cast<int>(i % KV_STAGES), a = static_cast<int>(i & 1);
+                const int item = item_of(u);
+                if (!mbar_wait(&tempty[a], static_cast<uint32_t>(((i >> 1) & 1) ^ 1), p.wait_limit_ns, abort_flag) ||
+                    !mbar_wait(&kfull[s], static_cast<uint32_t>((i / KV_STAGES) & 1), p.wait_limit_ns, abort_flag))
+                    break;
+                if (item != gw_item) {
+                    if (!mbar_wait(gw_full, static_cast<uint32_t>(gw_used & 1), p.wait_limit_ns, abort_flag)) break;
+                    gw_item = item;
+                    ++gw_used;
+                }
+                tc_fence_after();
+                const uint32_t aK = smem_u32(ring + s * 2 * TILE), aV = aK + TILE;
+                const uint32_t t12 = tmem_base + a * 256, t3 = t12 + 128;
+                for (int kk = 0; kk < nkk; ++kk) {   // K W and K G^T: K-steps over dk
+                    const uint32_t ko = (kk >> 2) * BOX + (kk & 3) * 32;
+                    const uint64_t ad = smem_desc(aK + ko, 16, SBO);
+                    mma_bf16(t12, ad, smem_desc(bW + ko, 16, SBO), ID_KK, kk > 0 ? 1u : 0u);
+                    mma_bf16(t3, ad, smem_desc(bG + ko, 16, SBO), ID_KK, kk > 0 ? 1u : 0u);
+                }
+                for (int kk = 0; kk < nkv; ++kk) {   // + V G: K-steps over dv, into the same accumulator
+                    const uint32_t ko = (kk >> 2) * BOX + (kk & 3) * 32;
+                    mma_bf16(t12, smem_desc(aV + ko, 16, SBO), smem_desc(bG + kk * 2048, MN_LBO, SBO), ID_KM, 1u);
+                }
+                mma_commit(&tfull[a]);
+                if (u + 1 == u_end || item_of(u + 1) != item) mma_commit(gw_empty);
             }
-            for (int kk = 0; kk < nkv; ++kk) {   // K-steps over dv
-                const uint32_t ko = (kk >> 2) * BOX + (kk & 3) * 32;
-                mma_bf16(tmem_base + 128, smem_desc(aV + ko, 16, SBO), smem_desc(bG + kk * 2048, MN_LBO, SBO), ID_KM,
-                         kk > 0 ? 1u : 0u);  // T2
-                mma_bf16(tmem_base + 384, smem_desc(aO + ko, 16, SBO), smem_desc(bS + kk * 2048, MN_LBO, SBO), ID_KM,
-                         kk > 0 ? 1u : 0u);  // T4
-            }
-            mma_commit(mma_bar);
+            mma_commit(final_bar);
+            mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
         }
-        mma_pending = true;
-        ok = mbar_wait(mma_bar, phase, p.wait_limit_ns, abort_flag);
-        if (!__syncthreads_and(ok)) break;
-        mma_pending = false;
-        phase ^= 1;
-        tc_fence_after();
-        // thread n: token row n of the tile (TMEM lane n)
-        const int n = tid;
-        const int token = tile * 128 + n;
-        const bool valid = token < p.N;
-        const size_t th = (static_cast<size_t>(f) * p.N + (valid ? token : 0)) * p.H + h;
-        const float bn = valid ? p.beta[th] : 0.0f;
-        const uint32_t trow = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+    } else {
+        // ----------------------------------------------------------- epilogue
+        // thread (n, half): token row n (TMEM lane n), columns [64 half, 64 half + 64)
+        const int et = tid - 64;                 // 0..255
+        const int half = et >> 7;
+        const int n = (warp & 3) * 32 + lane;
+        const uint32_t trow_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         // 8 bf16 of row n of a K-major token tile, columns c..c+7 (c % 8 == 0)
         auto row8 = [&](const uint8_t* tilep, int c, float* x) {
             const int cc = c & 63;
@@ -338,93 +377,86 @@ __global__ void __launch_bounds__(THREADS, 1)
                 x[2 * e + 1] = f2.y;
             }
         };
-        float dbeta = 0.0f;
-        // dk = beta (T1 + T2), dbeta += (T1 . k) / 2
-        for (int c0 = 0; c0 < p.dk; c0 += 32) {
-            uint32_t t1[32], t2[32];
-            tmem_ld32(trow + 0 + c0, t1);
-            tmem_ld32(trow + 128 + c0, t2);
-            tmem_wait_ld();
-            uint32_t pk[16];
+        for (long long u = u_begin; u < u_end; ++u) {
+            const long long i = u - u_begin;
+            const int s = static_cast<int>(i % KV_STAGES), a = static_cast<int>(i & 1);
+            const int item = item_of(u), tile = static_cast<int>(u % p.ntile);
+            const int f = item / p.H, h = item % p.H;
+            // both halves decide together: the named barrier below is never left waiting
+            const bool ok = bar_and(1, TOKEN_EPI,
+                                    mbar_wait(&tfull[a], static_cast<uint32_t>((i >> 1) & 1), p.wait_limit_ns,
+                                              abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            const uint8_t* sK = ring + s * 2 * TILE;
+            const uint8_t* sV = sK + TILE;
+            const int token = tile * 128 + n;
+            const bool valid = token < p.N;
+            const size_t th = (static_cast<size_t>(f) * p.N + (valid ? token : 0)) * p.H + h;
+            const float bn = valid ? p.beta[th] : 0.0f;
+            const uint32_t trow = tmem_base + a * 256 + trow_off;
+            float dbeta = 0.0f;
+            // dk = beta T12, dbeta += T12 . k / 2
+            for (int c0 = 64 * half; c0 < p.dk && c0 < 64 * half + 64; c0 += 32) {
+                uint32_t t[32];
+                tmem_ld32(trow + c0, t);
+                tmem_wait_ld();
+                uint32_t pk[16];
 #pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-                float kx[8];
-                row8(sK, c0 + 8 * q8, kx);
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    float kx[8];
+                    row8(sK, c0 + 8 * q8, kx);
 #pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const int t = 8 * q8 + e;
-                    const float a0 = __uint_as_float(t1[t]), a1 = __uint_as_float(t1[t + 1]);
-                    dbeta += 0.5f * (a0 * kx[e] + a1 * kx[e + 1]);
-                    pk[t / 2] = pack_bf16x2(bn * (a0 + __uint_as_float(t2[t])), bn * (a1 + __uint_as_float(t2[t + 1])));
+                    for (int e = 0; e < 8; e += 2) {
+                        const float a0 = __uint_as_float(t[8 * q8 + e]), a1 = __uint_as_float(t[8 * q8 + e + 1]);
+                        dbeta += 0.5f * (a0 * kx[e] + a1 * kx[e + 1]);
+                        pk[(8 * q8 + e) / 2] = pack_bf16x2(bn * a0, bn * a1);
+                    }
+                }
+                if (valid) {
+                    __nv_bfloat16* dst = p.dk_out + th * p.dk + c0;
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        if (c0 + 8 * q4 < p.dk)
+                            *reinterpret_cast<uint4*>(dst + 8 * q4) =
+                                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
                 }
             }
-            if (valid) {
-                __nv_bfloat16* dst = p.dk_out + th * p.dk + c0;
-                for (int q4 = 0; q4 < 4; ++q4)
-                    if (c0 + 8 * q4 < p.dk)
-                        *reinterpret_cast<uint4*>(dst + 8 * q4) =
-                            make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-            }
-        }
-        // dv = beta T3, dbeta += T3 . v
-        for (int c0 = 0; c0 < p.dv; c0 += 32) {
-            uint32_t t3[32];
-            tmem_ld32(trow + 256 + c0, t3);
-            tmem_wait_ld();
-            uint32_t pv[16];
+            // dv = beta T3, dbeta += T3 . v / 2
+            for (int c0 = 64 * half; c0 < p.dv && c0 < 64 * half + 64; c0 += 32) {
+                uint32_t t[32];
+                tmem_ld32(trow + 128 + c0, t);
+                tmem_wait_ld();
+                uint32_t pv[16];
 #pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-                float vx[8];
-                row8(sV, c0 + 8 * q8, vx);
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    float vx[8];
+                    row8(sV, c0 + 8 * q8, vx);
 #pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const int t = 8 * q8 + e;
-                    const float a0 = __uint_as_float(t3[t]), a1 = __uint_as_float(t3[t + 1]);
-                    dbeta += a0 * vx[e] + a1 * vx[e + 1];
-                    pv[t / 2] = pack_bf16x2(bn * a0, bn * a1);
+                    for (int e = 0; e < 8; e += 2) {
+                        const float a0 = __uint_as_float(t[8 * q8 + e]), a1 = __uint_as_float(t[8 * q8 + e + 1]);
+                        dbeta += 0.5f * (a0 * vx[e] + a1 * vx[e + 1]);
+                        pv[(8 * q8 + e) / 2] = pack_bf16x2(bn * a0, bn * a1);
+                    }
+                }
+                if (valid) {
+                    __nv_bfloat16* dst = p.dv_out + th * p.dv + c0;
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        if (c0 + 8 * q4 < p.dv)
+                            *reinterpret_cast<uint4*>(dst + 8 * q4) =
+                                make_uint4(pv[4 * q4], pv[4 * q4 + 1], pv[4 * q4 + 2], pv[4 * q4 + 3]);
                 }
             }
-            if (valid) {
-                __nv_bfloat16* dst = p.dv_out + th * p.dv + c0;
-                for (int q4 = 0; q4 < 4; ++q4)
-                    if (c0 + 8 * q4 < p.dv)
-                        *reinterpret_cast<uint4*>(dst + 8 * q4) =
-                            make_uint4(pv[4 * q4], pv[4 * q4 + 1], pv[4 * q4 + 2], pv[4 * q4 + 3]);
-            }
+            tc_fence_before();
+            mbar_arrive(&tempty[a]);
+            mbar_arrive(&kempty[s]);
+            if (half == 1) dbh[a * 128 + n] = dbeta;
+            named_bar_sync(1, TOKEN_EPI);
+            if (half == 0 && valid) p.d_beta[th] = dbeta + dbh[a * 128 + n];
         }
-        if (valid) p.d_beta[th] = dbeta;
-        // the token tiles are no longer read: the next unit's copies overlap the dq part
-        __syncthreads();
-        if (u + 1 < u_end) {
-            if (tid == 0) issue_loads(u + 1);
-            load_pending = true;
-        }
-        // dq = T4
-        for (int c0 = 0; c0 < p.dk; c0 += 32) {
-            uint32_t t4[32];
-            tmem_ld32(trow + 384 + c0, t4);
-            tmem_wait_ld();
-            if (valid) {
-                __nv_bfloat16* dst = p.dq_out + th * p.dk + c0;
-                for (int q4 = 0; q4 < 4; ++q4)
-                    if (c0 + 8 * q4 < p.dk)
-                        *reinterpret_cast<uint4*>(dst + 8 * q4) = make_uint4(
-                            pack_bf16x2(__uint_as_float(t4[8 * q4 + 0]), __uint_as_float(t4[8 * q4 + 1])),
-                            pack_bf16x2(__uint_as_float(t4[8 * q4 + 2]), __uint_as_float(t4[8 * q4 + 3])),
-                            pack_bf16x2(__uint_as_float(t4[8 * q4 + 4]), __uint_as_float(t4[8 * q4 + 5])),
-                            pack_bf16x2(__uint_as_float(t4[8 * q4 + 6]), __uint_as_float(t4[8 * q4 + 7])));
-            }
-        }
-        tc_fence_before();
-        __syncthreads();  // tiles and accumulators are reused by the next unit
-    }
-    if (tid == 0) {
-        if (load_pending) mbar_wait_drain(load_bar, phase, p.wait_limit_ns);
-        if (mma_pending) mbar_wait_drain(mma_bar, phase, p.wait_limit_ns);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, 512);
     }

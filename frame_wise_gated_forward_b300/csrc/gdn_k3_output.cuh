@@ -71,6 +71,9 @@ struct Params {
     int reverse;            // fused schedule: follow a scan that runs from frame F-1 down
     int norm_q;             // fused prologue: scale each output row by 1/max(|q_n|, eps)
     float q_scale;          // fp8 q: o_n = q_scale * S q8_n  (1 otherwise)
+    int b_mn;               // 0: O = Q S^T (S K-major).  1: O = Q S with S read MN-major, for the
+                            // backward's dq = dO S_f: then dk is dO's width (dv of S) and dv the
+                            // output width (dk of S)
     unsigned long long wait_limit_ns;
 };
 
@@ -141,9 +144,10 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
     const int lane = threadIdx.x & 31;
     const int kboxes = p.dk > 64 ? 2 : 1;
     const int vboxes = p.dv > 64 ? 2 : 1;
+    const int sboxes = p.b_mn ? vboxes : kboxes;   // 64-column boxes of the state tile
 
     // never-loaded boxes (dk <= 64) must read as zero
-    if (!FP8 && kboxes < 2)
+    if (!FP8 && (kboxes < 2 || sboxes < 2))
         for (int i = threadIdx.x; i < (QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES) / 16; i += THREADS)
             reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
@@ -196,8 +200,8 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
                     if (!wait_count_geq(sc.flags + item, sc.flag_target, p.wait_limit_ns, abort_flag)) break;
                     fence_proxy_async_global();  // the published state is read through the async proxy
                 }
-                mbar_arrive_expect_tx(&sfull[ss], kboxes * BOX_BYTES);
-                for (int bx = 0; bx < kboxes; ++bx)
+                mbar_arrive_expect_tx(&sfull[ss], sboxes * BOX_BYTES);
+                for (int bx = 0; bx < sboxes; ++bx)
                     tma_load_3d(sring + ss * STILE_BYTES + bx * BOX_BYTES, tm_s, &sfull[ss], 64 * bx, 0,
                                 static_cast<int>(item));
                 ++s_issued;
@@ -229,7 +233,7 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t IDESC = idesc_bf16(128, 128, 0, 0);
+            const uint32_t IDESC = p.b_mn ? idesc_bf16(128, 128, 0, 1) : idesc_bf16(128, 128, 0, 0);
             const int nk = (p.dk + 15) / 16;
             int qs = 0, ss = 0, acc = 0;
             uint32_t qph = 0, sph = 0, aph = 0;
@@ -251,7 +255,8 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
                     const uint32_t d_tmem = tmem_base + acc * 128;
                     for (int kk = 0; kk < nk; ++kk) {
                         const uint64_t ad = smem_desc(a_base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = smem_desc(b_base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd = p.b_mn ? smem_desc(b_base + kk * 2048, BOX_BYTES, 1024)
+                                                   : smem_desc(b_base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
                         mma_bf16(d_tmem, ad, bd, IDESC, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(&qempty[qs]);
