@@ -25,6 +25,7 @@ EXPORTS = (
     "gdn_status_string", "gdn_sync_status", "gdn_set_wait_limit_ns", "gdn_selftest_wait_timeout",
     "gdn_version", "gdn_frame_step_noalloc", "gdn_set_fused_scan", "gdn_scan_schedule",
     "gdn_set_contract_split", "gdn_frame_forward_fp8", "gdn_frame_step_fp8", "gdn_frame_backward",
+    "gdn_set_fused_step",
 )
 
 
@@ -87,6 +88,8 @@ def load(path: str | None = None):
     lib.gdn_frame_step_noalloc.restype = ctypes.c_int
     lib.gdn_set_fused_scan.argtypes = [ctypes.c_int]
     lib.gdn_set_fused_scan.restype = None
+    lib.gdn_set_fused_step.argtypes = [ctypes.c_int]
+    lib.gdn_set_fused_step.restype = None
     lib.gdn_set_contract_split.argtypes = [ctypes.c_int]
     lib.gdn_set_contract_split.restype = None
     lib.gdn_scan_schedule.argtypes = [i, i, i]

@@ -322,6 +322,12 @@ def set_contract_split(max_split: int) -> None:
     load().gdn_set_contract_split(int(max_split))
 
 
+def set_fused_step(on: bool) -> None:
+    """One-launch step for frames of up to 1024 tokens (True, the default) or
+    the three-phase path (False)."""
+    load().gdn_set_fused_step(1 if on else 0)
+
+
 def scan_schedule(B, H, dv) -> int:
     """+R: fused scan/output with R state rows per scan CTA; -R: two launches."""
     return int(load().gdn_scan_schedule(B, H, dv))

@@ -15,6 +15,7 @@
 #include "gdn_bwd.cuh"
 #include "gdn_k1_contract.cuh"
 #include "gdn_k23_fused.cuh"
+#include "gdn_step_fused.cuh"
 
 namespace {
 
@@ -22,7 +23,8 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ULL};
 std::atomic<int> g_fused_scan{1};
-std::atomic<int> g_max_split{0};  // 0: automatic; 1: never split; k > 1: up to k token ranges per item
+std::atomic<int> g_max_split{0};
+std::atomic<int> g_fused_step{1};  // one-launch step (gdn_step_fused.cuh) where it applies  // 0: automatic; 1: never split; k > 1: up to k token ranges per item
 
 // ------------------------------------------------------------------ devices
 struct DeviceState {
@@ -94,6 +96,7 @@ gdn_status device_ready(int* dev_out, DeviceState** st_out) {
             !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<16, true>), k23::smem_bytes<16>()) ||
             !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<32, true>), k23::smem_bytes<32>()) ||
             !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<64, true>), k23::smem_bytes<64>()) ||
+            !smem_attr(reinterpret_cast<const void*>(step::step_kernel), step::SMEM_BYTES) ||
             !smem_attr(reinterpret_cast<const void*>(bwd::frame_grad_kernel), bwd::FRAME_SMEM) ||
             !smem_attr(reinterpret_cast<const void*>(bwd::token_grad_kernel), bwd::TOKEN_SMEM)) {
             cudaGetLastError();
@@ -464,6 +467,35 @@ bool all_device(const PassArgs& a) {
            is_device_ptr(a.beta) && is_device_ptr(a.state_in) && is_device_ptr(a.out) && is_device_ptr(a.state_out);
 }
 
+// The one-launch step: a plain bf16 frame (no folded prologue, no 8-bit
+// inputs) of at most step::MAX_CHUNKS chunks of 64 tokens.
+bool fused_step_applies(const PassArgs& a) {
+    return g_fused_step.load() != 0 && a.F == 1 && !a.fp8 && !a.prologue &&
+           (a.N + gdn::step::CHUNK - 1) / gdn::step::CHUNK <= gdn::step::MAX_CHUNKS;
+}
+gdn_status launch_step_fused(const PassArgs& a, cudaStream_t stream) {
+    CUtensorMap tm_k, tm_v, tm_q;
+    if (!encode_tokens(&tm_k, a.k, a.B, a.N, a.H, a.dk, gdn::step::CHUNK) ||
+        !encode_tokens(&tm_v, a.v, a.B, a.N, a.H, a.dv, gdn::step::CHUNK) ||
+        !encode_tokens(&tm_q, a.q, a.B, a.N, a.H, a.dk, 128))
+        return GDN_ERR_LAUNCH;
+    gdn::step::Params ps;
+    ps.alpha = a.alpha;
+    ps.beta = a.beta;
+    ps.state_in = a.state_in;
+    ps.state_out = a.state_out;
+    ps.out = reinterpret_cast<__nv_bfloat16*>(a.out);
+    ps.H = a.H;
+    ps.N = a.N;
+    ps.dk = a.dk;
+    ps.dv = a.dv;
+    ps.chunks = (a.N + gdn::step::CHUNK - 1) / gdn::step::CHUNK;
+    ps.wait_limit_ns = g_wait_limit_ns.load();
+    gdn::step::step_kernel<<<a.B * a.H * gdn::step::CS, gdn::step::THREADS, gdn::step::SMEM_BYTES, stream>>>(
+        tm_k, tm_v, tm_q, ps);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+
 // Pooled-workspace pass: gdn_frame_forward (step = false) and gdn_frame_step.
 gdn_status run_pass(const PassArgs& a, bool step, cudaStream_t stream, cudaEvent_t const* ev = nullptr) {
     int dev;
@@ -471,8 +503,8 @@ gdn_status run_pass(const PassArgs& a, bool step, cudaStream_t stream, cudaEvent
     gdn_status st = device_ready(&dev, &ds);
     if (st != GDN_OK) return st;
     if (!all_device(a)) return GDN_ERR_NULL_PTR;
+    if (step && fused_step_applies(a) && ev == nullptr) return launch_step_fused(a, stream);
     const long long items = static_cast<long long>(a.B) * a.F * a.H;
-    (void)step;
     const SplitPlan sp = plan_split(items, chunks_of(a.N), ds->sms, ds->coop_k1);
     const Layout L = layout_of(items, a.dk, a.dv, sp);
     uint8_t* ws = nullptr;
@@ -982,6 +1014,8 @@ gdn_status gdn_sync_status(gdn_stream_t stream) {
 
 void gdn_set_contract_split(int max_split) { g_max_split.store(max_split > 0 ? max_split : 0); }
 
+void gdn_set_fused_step(int on) { g_fused_step.store(on != 0 ? 1 : 0); }
+
 void gdn_set_fused_scan(int mode) {
     g_fused_scan.store((mode == 16 || mode == 32 || mode == 64) ? mode : (mode != 0 ? 1 : 0));
 }
@@ -1058,11 +1092,15 @@ extern "C" gdn_status gdn_frame_step_noalloc(const void* q, const void* k, const
     DeviceState* ds;
     st = device_ready(&dev, &ds);
     if (st != GDN_OK) return st;
+    const PassArgs a{q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv};
+    if (fused_step_applies(a)) {  // the one-launch step keeps everything on chip: no scratch at all
+        if (!all_device(a)) return GDN_ERR_NULL_PTR;
+        return launch_step_fused(a, reinterpret_cast<cudaStream_t>(stream_handle));
+    }
     const long long items = static_cast<long long>(B) * H;
     const SplitPlan sp = plan_split(items, chunks_of(N), ds->sms, ds->coop_k1);
     const Layout L = layout_of(items, dk, dv, sp);
     if (L.total > kStepScratchBytes) return GDN_ERR_TOO_LARGE;
-    const PassArgs a{q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv};
     if (!all_device(a)) return GDN_ERR_NULL_PTR;
     uint8_t* ws = nullptr;
     st = step_scratch_address(dev, &ws);

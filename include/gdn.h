@@ -281,6 +281,20 @@ void gdn_set_fused_scan(int mode);
 void gdn_set_contract_split(int max_split);
 
 /*
+ * The one-launch step.  on != 0 (default): gdn_frame_step and
+ * gdn_frame_step_noalloc run a frame of at most 1024 tokens (bf16 inputs) as
+ * one kernel: one thread-block cluster of 8 CTAs per head computes the
+ * frame's contractions on its tokens, reduces them through distributed shared
+ * memory in a fixed order, advances its rows of the state and writes the
+ * frame's outputs, with no workspace in HBM.  on = 0: the three-phase path
+ * (two launches and a workspace).  Results agree to rounding (the partial
+ * sums are added in a different order).  Applies to calls made after it
+ * returns.  A scheduling control of this library; the pages have no
+ * counterpart.
+ */
+void gdn_set_fused_step(int on);
+
+/*
  * Schedule phases 2 and 3 take for this shape on the current device: +R when
  * they run as one cooperative launch with R rows of S per scan CTA, -R when
  * they run as two launches, 0 for invalid shapes or no usable device.
@@ -311,9 +325,10 @@ const char* gdn_version(void);
  * workspace lives instead in one fixed array of GDN_STEP_NOALLOC_SCRATCH_BYTES
  * bytes in the library's device image: every GPU that loads the library
  * holds it until the process exits.  No call allocates or frees memory.
- *   - A shape whose workspace (gdn_step_workspace_bytes) exceeds the array
- *     returns GDN_ERR_TOO_LARGE before anything is launched.  One frame of
- *     B*H = 16 heads, N = 880 tokens, dk = dv = 128 needs about 21 MiB.
+ *   - Frames of at most 1024 tokens run as the one-launch step (see
+ *     gdn_set_fused_step) and use no scratch at all.  Longer frames use the
+ *     array: a shape whose workspace (gdn_step_workspace_bytes) exceeds it
+ *     returns GDN_ERR_TOO_LARGE before anything is launched.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture starts.

@@ -1,0 +1,75 @@
+"""GPU parity of the one-launch step (one 8-CTA cluster per head) against the
+fp64 oracle and against the three-phase step path.
+
+Shapes cover one token, tokens fewer than the cluster's CTAs have chunks
+(CTAs with no tokens), a ragged last chunk, the largest frame the fused step
+takes (1024 tokens, two chunks per CTA), head sizes 32 / 64 / 128 with
+dk != dv, more clusters than SMs, a NULL state_in and an in-place state.
+"""
+import numpy as np
+import pytest
+import torch
+
+from frame_wise_gated_forward_b300 import api, inputs
+from gpu_util import TOL_OUT, TOL_STATE, ensure_built, oracle_run, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def step_args(x):
+    return [x[k][:, 0].contiguous() for k in ("q", "k", "v", "alpha", "beta")]
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 2, 1, 64, 64),       # one token
+    (1, 4, 100, 128, 128),   # 2 chunks: six of the eight CTAs have no tokens
+    (1, 3, 448, 64, 128),    # 7 chunks, dk != dv
+    (1, 16, 880, 128, 128),  # the 60 s shape's frame
+    (2, 3, 1000, 32, 32),    # ragged last chunk, d = 32
+    (1, 2, 1024, 128, 48),   # the largest fused frame: two chunks per CTA
+    (2, 40, 200, 64, 64),    # 80 clusters: more CTAs than SMs
+])
+def test_fused_step_matches_oracle_and_three_phase_step(shape):
+    B, H, N, dk, dv = shape
+    x = inputs.draw(B, H, 1, N, dk, dv, seed=31, s0_std=0.1)
+    ref = oracle_run(x, B, H, 1, N, dk, dv)
+    xd = {k: v.cuda() for k, v in x.items()}
+    api.set_fused_step(True)
+    o1, s1 = api.frame_step(*step_args(xd), xd["state_in"])
+    api.sync_status()
+    api.set_fused_step(False)
+    try:
+        o3, s3 = api.frame_step(*step_args(xd), xd["state_in"])
+        api.sync_status()
+    finally:
+        api.set_fused_step(True)
+    eo = rel_err(o1.float().cpu().numpy(), ref["out"][:, 0])
+    es = rel_err(s1.cpu().numpy(), ref["state"])
+    print(f"fused step {shape}: err_O={eo:.3e} err_S={es:.3e}")
+    assert np.isfinite(o1.float().cpu().numpy()).all()
+    assert eo <= TOL_OUT and es <= TOL_STATE
+    # the two paths differ only in the order the partial sums are added
+    assert rel_err(o1.float().cpu().numpy(), o3.float().cpu().numpy()) <= 5e-3
+    assert rel_err(s1.cpu().numpy(), s3.cpu().numpy()) <= 2e-3
+
+
+def test_fused_step_null_and_in_place_state_and_determinism():
+    B, H, N, d = 1, 4, 300, 128
+    x = inputs.draw(B, H, 1, N, d, d, seed=32, s0_std=0.0)
+    xd = {k: v.cuda() for k, v in x.items()}
+    o_null, s_null = api.frame_step(*step_args(xd), None)
+    zero = torch.zeros((B, H, d, d), device="cuda")
+    o_zero, s_zero = api.frame_step(*step_args(xd), zero)
+    st = torch.zeros((B, H, d, d), device="cuda")
+    o_ip, _ = api.frame_step(*step_args(xd), st, state_out=st)
+    api.sync_status()
+    assert torch.equal(o_null, o_zero) and torch.equal(s_null, s_zero)
+    assert torch.equal(o_ip, o_zero) and torch.equal(st, s_zero)
+    o2, s2 = api.frame_step(*step_args(xd), None)
+    api.sync_status()
+    assert torch.equal(o2, o_null) and torch.equal(s2, s_null)
