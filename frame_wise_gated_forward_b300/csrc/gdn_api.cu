@@ -24,7 +24,7 @@ constexpr int kMaxDevices = 64;
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ULL};
 std::atomic<int> g_fused_scan{1};
 std::atomic<int> g_max_split{0};
-std::atomic<int> g_fused_step{1};  // one-launch step (gdn_step_fused.cuh) where it applies  // 0: automatic; 1: never split; k > 1: up to k token ranges per item
+std::atomic<int> g_fused_step{0};  // one-launch step (gdn_step_fused.cuh) where it applies  // 0: automatic; 1: never split; k > 1: up to k token ranges per item
 
 // ------------------------------------------------------------------ devices
 struct DeviceState {

@@ -213,17 +213,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
     return d;
 }
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
+// Load from another CTA's shared memory.  Volatile, so it stays in program
+// order with cluster_sync() (also volatile), but without a memory clobber, so
+// that a run of independent loads is issued back to back.
 __device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
+                 : "r"(addr));
     return v;
 }
 __device__ __forceinline__ void st_dsmem_v4(uint32_t addr, uint4 v) {

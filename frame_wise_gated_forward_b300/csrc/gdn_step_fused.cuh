@@ -198,7 +198,8 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(THREADS, 1)
         good = __syncthreads_and(good);
         tc_fence_after();
     }
-    // the A part of D (row j = TMEM lane j) -> fp32 partials [j][c] (zeros without tokens)
+    // the A part of D (row j = TMEM lane j) -> fp32 partials part[c][j] = A_r[j][c]
+    // (column-major: consecutive threads write consecutive words); zeros without tokens
     float* part = reinterpret_cast<float*>(smem + OFF_KV);
     for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t v[32];
@@ -210,41 +211,51 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(THREADS, 1)
             for (int t = 0; t < 32; ++t) v[t] = 0u;
         }
 #pragma unroll
-        for (int t = 0; t < 32; t += 4)
-            *reinterpret_cast<uint4*>(part + j * 128 + c0 + t) = make_uint4(v[t], v[t + 1], v[t + 2], v[t + 3]);
+        for (int t = 0; t < 32; ++t) part[(c0 + t) * 128 + j] = __uint_as_float(v[t]);
     }
     cluster_sync();  // ---------------------------------------------- (1)
 
     // ---------------------------------------- 2a. A: reduce rows, share them
+    // rows of the CTA's 16-row block are written to a local bf16 staging block,
+    // then sent to every CTA's copy of A in 16-byte pieces
+    __nv_bfloat16* blk = reinterpret_cast<__nv_bfloat16*>(smem + OFF_SROW);   // [16][128]
+    auto send_rows = [&](uint32_t dst_off) {
+        for (int k = tid; k < SROWS * 16; k += THREADS) {
+            const int rr = k / 16, ch = k % 16;   // 16 pieces of 8 columns per row
+            const uint4 w = *reinterpret_cast<const uint4*>(blk + rr * 128 + ch * 8);
+            const uint32_t o = sbase + dst_off + kmaj(i0 + rr, ch * 8, QBOX);
+            for (int q = 0; q < CS; ++q) st_dsmem_v4(mapa_shared(o, q), w);
+        }
+    };
     {
-        // thread t: row i0 + t / 8, columns 16 (t % 8) .. + 15, summed over ranks in order
-        const int row = i0 + tid / 8, col0 = (tid % 8) * 16;
-        float acc[16];
+        // thread c: column c of rows i0 .. i0 + 15, i.e. part[c][i0 .. i0 + 15] of every rank, summed in order
+        const int c = tid;
+        float acc[SROWS];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) acc[e] = 0.0f;
-        const uint32_t local = sbase + OFF_KV + static_cast<uint32_t>(row * 128 + col0) * 4;
+        for (int e = 0; e < SROWS; ++e) acc[e] = 0.0f;
+        const uint32_t local = sbase + OFF_KV + static_cast<uint32_t>(c * 128 + i0) * 4;
+        // all 32 loads in flight at once, then the adds in rank order
+        float4 x[CS][4];
+#pragma unroll
         for (int q = 0; q < CS; ++q) {
             const uint32_t remote = mapa_shared(local, q);
 #pragma unroll
-            for (int e = 0; e < 16; e += 4) {
-                const float4 x = ld_dsmem_f32x4(remote + e * 4);
-                acc[e] += x.x;
-                acc[e + 1] += x.y;
-                acc[e + 2] += x.z;
-                acc[e + 3] += x.w;
+            for (int e = 0; e < 4; ++e) x[q][e] = ld_dsmem_f32x4(remote + e * 16);
+        }
+#pragma unroll
+        for (int q = 0; q < CS; ++q)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc[4 * e] += x[q][e].x;
+                acc[4 * e + 1] += x[q][e].y;
+                acc[4 * e + 2] += x[q][e].z;
+                acc[4 * e + 3] += x[q][e].w;
             }
-        }
-        uint4 w0, w1;
-        w0 = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                        pack_bf16x2(acc[6], acc[7]));
-        w1 = make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]), pack_bf16x2(acc[12], acc[13]),
-                        pack_bf16x2(acc[14], acc[15]));
-        const uint32_t o0 = sbase + OFF_A + kmaj(row, col0, QBOX), o1 = sbase + OFF_A + kmaj(row, col0 + 8, QBOX);
-        for (int q = 0; q < CS; ++q) {
-            st_dsmem_v4(mapa_shared(o0, q), w0);
-            st_dsmem_v4(mapa_shared(o1, q), w1);
-        }
+#pragma unroll
+        for (int e = 0; e < SROWS; ++e) blk[e * 128 + c] = __float2bfloat16_rn(acc[e]);
     }
+    __syncthreads();
+    send_rows(OFF_A);
     // the U part of D -> fp32 partials [i][j] (U[i][j] = D[j][128 + i]); the A
     // partials it overwrites have been read by every CTA only after barrier (2)
     fence_proxy_async_cluster();
@@ -264,14 +275,39 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(THREADS, 1)
     cluster_sync();  // ---------------------------------------------- (3)
 
     // ------------------------------- 2b. U: this CTA's rows, summed in rank order
+    // thread t sums row t / 8, columns 16 (t % 8) .. + 15 (16-byte remote loads)
+    // into a local fp32 block; thread j then takes column j of it
+    float* ured = reinterpret_cast<float*>(smem + OFF_BK);   // [16][128] (the beta*K tiles are done)
+    {
+        const int rr = tid / 8, col0 = (tid % 8) * 16;
+        float acc[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] = 0.0f;
+        const uint32_t local = sbase + OFF_KV + static_cast<uint32_t>((i0 + rr) * 128 + col0) * 4;
+        float4 x[CS][4];
+#pragma unroll
+        for (int q = 0; q < CS; ++q) {
+            const uint32_t remote = mapa_shared(local, q);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[q][e] = ld_dsmem_f32x4(remote + e * 16);
+        }
+#pragma unroll
+        for (int q = 0; q < CS; ++q)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc[4 * e] += x[q][e].x;
+                acc[4 * e + 1] += x[q][e].y;
+                acc[4 * e + 2] += x[q][e].z;
+                acc[4 * e + 3] += x[q][e].w;
+            }
+#pragma unroll
+        for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(ured + rr * 128 + col0 + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+    }
+    __syncthreads();
     float U[SROWS];
 #pragma unroll
-    for (int rr = 0; rr < SROWS; ++rr) U[rr] = 0.0f;
-    for (int q = 0; q < CS; ++q) {
-        const uint32_t remote = mapa_shared(sbase + OFF_KV + static_cast<uint32_t>(i0 * 128 + j) * 4, q);
-#pragma unroll
-        for (int rr = 0; rr < SROWS; ++rr) U[rr] += ld_dsmem_f32(remote + rr * 128 * 4);
-    }
+    for (int rr = 0; rr < SROWS; ++rr) U[rr] = ured[rr * 128 + j];
 
     // ------------------------------------------ 3. the state rows of this CTA
     fence_proxy_async_smem();
@@ -308,26 +344,16 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int t = 0; t < 16; ++t) c16[t] = 0u;
         }
-        __nv_bfloat16* srow = reinterpret_cast<__nv_bfloat16*>(smem + OFF_SROW);
 #pragma unroll
         for (int rr = 0; rr < SROWS; ++rr) {
             const float sn = af * (S[rr] - __uint_as_float(c16[rr])) + U[rr];
             if (good && p.state_out != nullptr && j < p.dk && i0 + rr < p.dv)
                 p.state_out[soff + static_cast<size_t>(i0 + rr) * p.dk + j] = sn;
-            srow[rr * 128 + j] = __float2bfloat16_rn(j < p.dk && i0 + rr < p.dv ? sn : 0.0f);
+            blk[rr * 128 + j] = __float2bfloat16_rn(j < p.dk && i0 + rr < p.dv ? sn : 0.0f);
         }
     }
     __syncthreads();
-    {
-        // send this CTA's 16 rows of the bf16 state into every CTA's copy of S
-        const __nv_bfloat16* srow = reinterpret_cast<const __nv_bfloat16*>(smem + OFF_SROW);
-        for (int k = tid; k < SROWS * 16; k += THREADS) {
-            const int rr = k / 16, ch = k % 16;   // 16 chunks of 8 columns per row
-            const uint4 w = *reinterpret_cast<const uint4*>(srow + rr * 128 + ch * 8);
-            const uint32_t o = sbase + OFF_S + kmaj(i0 + rr, ch * 8, QBOX);
-            for (int q = 0; q < CS; ++q) st_dsmem_v4(mapa_shared(o, q), w);
-        }
-    }
+    send_rows(OFF_S);   // this CTA's 16 rows of the bf16 state into every CTA's copy of S
     fence_proxy_async_cluster();
     cluster_sync();  // ---------------------------------------------- (4)
     fence_proxy_async_smem();

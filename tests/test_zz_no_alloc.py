@@ -53,7 +53,7 @@ def test_noalloc_step_matches_step_on_two_calls_in_a_row():
 def test_noalloc_step_rejects_shapes_beyond_its_scratch():
     ensure_built()
     lib = load()
-    B, H, N, d = 4, 72, 1100, 128        # 288 heads, frames past the one-launch step: 36+ MiB of workspace
+    B, H, N, d = 4, 72, 1100, 128        # 288 heads: 36+ MiB of workspace
     q = torch.zeros((B, N, H, d), dtype=torch.bfloat16, device="cuda")
     k, v, out = torch.zeros_like(q), torch.zeros_like(q), torch.zeros_like(q)
     alpha = torch.ones((B, H), device="cuda")
