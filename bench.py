@@ -413,7 +413,8 @@ def main():
     api.sync_status()
     step_us = s0.elapsed_time(s1) * 1e3 / w.F
     step_info = {"us_per_frame_step": step_us, "tokens_per_s": w.B * w.N / (step_us / 1e6),
-                 "launches_per_step": 2, "memsets_per_step": 1, "frames": w.F,
+                 "launches_per_step": 1, "memsets_per_step": 0, "frames": w.F,
+                 "kernel": "one-launch step (one 4-CTA cluster per head, default)",
                  "floor_us": (w.B * w.N * w.H * (2 * w.dk + 2 * w.dv) * 2 + 2 * w.B * w.H * w.dv * w.dk * 4)
                  / (peaks["hbm_gbs"] * 1e9) * 1e6}
     del frames

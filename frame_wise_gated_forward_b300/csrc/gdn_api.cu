@@ -23,8 +23,8 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ULL};
 std::atomic<int> g_fused_scan{1};
-std::atomic<int> g_max_split{0};
-std::atomic<int> g_fused_step{0};  // one-launch step (gdn_step_fused.cuh) where it applies  // 0: automatic; 1: never split; k > 1: up to k token ranges per item
+std::atomic<int> g_max_split{0};  // 0: automatic; 1: never split; k > 1: up to k token ranges per item
+std::atomic<int> g_fused_step{1};  // one-launch step (gdn_step_fused.cuh) where it applies
 
 // ------------------------------------------------------------------ devices
 struct DeviceState {
@@ -467,32 +467,34 @@ bool all_device(const PassArgs& a) {
            is_device_ptr(a.beta) && is_device_ptr(a.state_in) && is_device_ptr(a.out) && is_device_ptr(a.state_out);
 }
 
-// The one-launch step: a plain bf16 frame (no folded prologue, no 8-bit
-// inputs) of at most step::MAX_CHUNKS chunks of 64 tokens.
+// The one-launch step: a plain bf16 frame (no folded prologue, no 8-bit inputs).
 bool fused_step_applies(const PassArgs& a) {
-    return g_fused_step.load() != 0 && a.F == 1 && !a.fp8 && !a.prologue &&
-           (a.N + gdn::step::CHUNK - 1) / gdn::step::CHUNK <= gdn::step::MAX_CHUNKS;
+    return g_fused_step.load() != 0 && a.F == 1 && !a.fp8 && !a.prologue;
 }
 gdn_status launch_step_fused(const PassArgs& a, cudaStream_t stream) {
-    CUtensorMap tm_k, tm_v, tm_q;
+    CUtensorMap tm_k, tm_v, tm_q, tm_o;
     if (!encode_tokens(&tm_k, a.k, a.B, a.N, a.H, a.dk, gdn::step::CHUNK) ||
         !encode_tokens(&tm_v, a.v, a.B, a.N, a.H, a.dv, gdn::step::CHUNK) ||
-        !encode_tokens(&tm_q, a.q, a.B, a.N, a.H, a.dk, 128))
+        !encode_tokens(&tm_q, a.q, a.B, a.N, a.H, a.dk, 128) ||
+        !encode_tokens(&tm_o, a.out, a.B, a.N, a.H, a.dv, 128))
+        return GDN_ERR_LAUNCH;
+    CUtensorMap tm_s;
+    std::memset(&tm_s, 0, sizeof(tm_s));
+    if (a.state_out != nullptr &&
+        !encode_mats_f32(&tm_s, a.state_out, static_cast<long long>(a.B) * a.H, a.dv, a.dk, gdn::step::SR))
         return GDN_ERR_LAUNCH;
     gdn::step::Params ps;
     ps.alpha = a.alpha;
     ps.beta = a.beta;
     ps.state_in = a.state_in;
     ps.state_out = a.state_out;
-    ps.out = reinterpret_cast<__nv_bfloat16*>(a.out);
     ps.H = a.H;
     ps.N = a.N;
     ps.dk = a.dk;
     ps.dv = a.dv;
-    ps.chunks = (a.N + gdn::step::CHUNK - 1) / gdn::step::CHUNK;
     ps.wait_limit_ns = g_wait_limit_ns.load();
     gdn::step::step_kernel<<<a.B * a.H * gdn::step::CS, gdn::step::THREADS, gdn::step::SMEM_BYTES, stream>>>(
-        tm_k, tm_v, tm_q, ps);
+        tm_k, tm_v, tm_q, tm_o, tm_s, ps);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 

@@ -2,24 +2,33 @@
 // state in a single launch (the interactive step: the pipeline advances by
 // one latent frame at a time, WorldFoundry model card "What it is for").
 //
-// One thread-block cluster of CS CTAs per (b, h) head; CTA r of the
-// cluster owns token chunks [r C / CS, (r + 1) C / CS) of the frame (C chunks
-// of 64 tokens, at most two per CTA) and state rows [16 r, 16 r + 16).
-//   1. D_r = (beta K)^T [K | V] over its tokens on tcgen05 (TMEM, fp32), as
-//      phase 1 does for a whole frame;
-//   2. the CTAs reduce the partial sums through distributed shared memory in
-//      a fixed rank order: CTA r sums rows [16 r, 16 r + 16) of A and sends
-//      them (bf16) into every CTA's copy of A; then it sums its rows of U;
-//   3. its state rows: S_r <- alpha (S_r - S_r A) + U_r (one tcgen05 MMA,
-//      M = 128, N = 16), written to state_out and, as bf16, into every CTA's
-//      copy of S;
-//   4. o_n = S q_n for its tokens (tcgen05, M = 128 tokens, N = dv), bf16.
-// No workspace: nothing but the inputs, state and outputs touches HBM.
+// One thread-block cluster of CS = 4 CTAs per (b, h) head.  The frame's
+// contraction D = K^T B [K | V] (dk x (dk + dv)) is split by its columns, not
+// by tokens, so no CTA ever adds another CTA's partial sums:
+//   CTA 0, 1: columns [64 r, 64 r + 64) of A = K^T B K   (B operand: K box r)
+//   CTA 2, 3: rows [64 (r-2), + 64) of U = V^T B K        (B operand: V box r-2)
+// each over all N tokens of the frame (a ring of 64-token chunks).  The MMA's
+// A operand is the raw K tile; each CTA scales only its own 64 B-operand
+// columns by beta (the fp32 product rounded once to bf16), so the rounding
+// sits on the other factor than in phase 1 -- the same sum to bf16 accuracy.
+// Then
+//   - CTAs 0 and 1 write their columns of A (bf16) into CTAs 2 and 3's copy of
+//     A through distributed shared memory (A is symmetric: row = column);
+//   - CTAs 2 and 3 advance their 64 state rows, S <- alpha (S - S A) + U, with
+//     one tcgen05 MMA (M = 128, N = 64), write state_out, and send the rows
+//     (bf16) into every CTA's copy of S;
+//   - every CTA computes o_n = S q_n for a quarter of the frame's 128-token
+//     tiles, staged in shared memory and written by a TMA store.
+// Nothing but the inputs, the state and the outputs touches HBM, and every
+// sum is taken in one accumulator in token order, as in phase 1.
 //
 // The cluster barriers are executed by every thread of every CTA exactly the
 // same number of times on every path: a bounded wait that gives up only marks
 // the CTA as failed (GDN_ERR_TIMEOUT is recorded) and skips the work that
-// depended on it.  128 threads; thread j is TMEM lane j.
+// depends on it.  160 threads: warps 0-3 (thread j is TMEM lane j) scale the
+// B operand and run every later phase; warp 4's first lane issues the
+// contraction's ring loads and MMAs, so a chunk's MMAs and the refill of its
+// stage overlap the scaling of the next chunk (mbarriers, no block barrier).
 #pragma once
 
 #include "gdn_ptx.cuh"
@@ -27,41 +36,50 @@
 namespace gdn {
 namespace step {
 
-constexpr int CS = 8;                       // CTAs per cluster (one head)
-constexpr int THREADS = 128;
-constexpr int CHUNK = 64;                   // tokens per contraction chunk
-constexpr int MAX_CHUNKS = 2 * CS;          // frames of up to 1024 tokens
-constexpr int KBOX = CHUNK * 128;           // 64 rows x 128 B
-constexpr int KTILE = 2 * KBOX;             // 64 tokens x 128 columns, bf16
+constexpr int CS = 4;                       // CTAs per cluster (one head)
+constexpr int NWORK = 128;                  // warps 0-3
+constexpr int THREADS = NWORK + 32;         // + the contraction's issuer warp
+constexpr int CHUNK = 64;                   // tokens per ring stage
+constexpr int NST = 4;                      // ring depth
+constexpr int NBK = 4;                      // scaled B boxes in flight (workers run up to NBK chunks ahead of the MMAs)
+constexpr int KBOX = CHUNK * 128;           // 64 token rows x 128 B
+constexpr int STAGE = 3 * KBOX;             // K box 0 | K box 1 | this CTA's V box
 constexpr int QBOX = 128 * 128;             // 128 rows x 128 B
-constexpr int QTILE = 2 * QBOX;             // 128 x 128 bf16
-constexpr int SROWS = 16;                   // state rows per CTA
-constexpr int SBOX = SROWS * 128;
-// shared memory, in order
-constexpr int OFF_KV = 0;                               // [2][K tile | V tile]; then fp32 partials [128][128]
-constexpr int OFF_BK = OFF_KV + 4 * KTILE;              // [2] beta*K tiles
-constexpr int OFF_Q = OFF_BK + 2 * KTILE;               // q tile, K-major (128 tokens)
-constexpr int OFF_A = OFF_Q + QTILE;                    // A, K-major (128 x 128)
-constexpr int OFF_S = OFF_A + QTILE;                    // S after the frame, K-major (128 x 128)
-constexpr int OFF_SIMG = OFF_S + QTILE;                 // this CTA's rows of S before the frame, K-major
-constexpr int OFF_SROW = OFF_SIMG + 2 * SBOX;           // this CTA's rows of S after the frame, row-major bf16
-constexpr int OFF_BAR = OFF_SROW + SROWS * 128 * 2;
-constexpr size_t SMEM_BYTES = 1024 + OFF_BAR + 64;
-static_assert(4 * KTILE >= 128 * 128 * 4, "the partial sums fit in the K/V region");
+constexpr int TILE = 2 * QBOX;              // 128 x 128 bf16, K-major
+constexpr int SR = 64;                      // state rows per scan CTA
+constexpr int SRBOX = SR * 128;
+// shared memory, in order (1024-byte aligned pieces)
+constexpr int OFF_RING = 0;                              // [NST] stages; later two q tiles
+constexpr int OFF_OSTG = OFF_RING + 2 * TILE;            // (after the contraction) output staging tile;
+                                                         // before it, the scan CTA's fp32 state rows
+constexpr int OFF_BK = OFF_RING + NST * STAGE;           // [NBK] beta-scaled B boxes (64 rows x 64 columns)
+constexpr int OFF_A = OFF_BK + NBK * KBOX;               // A, K-major 128 x 128 (scan CTAs)
+constexpr int OFF_S = OFF_A + TILE;                      // S after the frame, K-major 128 x 128
+constexpr int OFF_SIMG = OFF_S + TILE;                   // scan CTA's 64 rows of S before the frame, K-major
+constexpr int OFF_BETA = OFF_SIMG + 2 * SRBOX;           // per-thread beta rings of the contraction
+constexpr int BETA_BYTES = 4096;
+constexpr int OFF_BAR = OFF_BETA + BETA_BYTES;
+constexpr int NBARS = 2 * NST + 2 + 2 * 2 + 2 * NBK;     // full, empty; d, c; qfull, o_bar; bk_empty, scaled
+constexpr int BAR_BYTES = 256;                           // the barriers, the TMEM address and the abort flag
+static_assert(NBARS * 8 + 8 <= BAR_BYTES, "barrier area");
+constexpr size_t SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES;
+static_assert(NST * STAGE >= 3 * TILE, "two q tiles and the output staging tile fit in the ring");
+static_assert(SR * 128 * 4 <= TILE, "the fp32 state rows fit in the output staging tile");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 // TMEM columns
-constexpr uint32_t T_D = 0;                 // 256: A part [0, 128), U part [128, 256)
-constexpr uint32_t T_C = 256;               // 16: S_r A
-constexpr uint32_t T_O = 384;               // 128: Q S^T
+constexpr uint32_t T_D = 0;                 // 64: this CTA's columns of D
+constexpr uint32_t T_C = 64;                // 64: S_rows A (scan CTAs)
+constexpr int BETA_AHEAD = 4;               // beta copies in flight per thread
+static_assert((BETA_AHEAD + 1) * NWORK * 4 <= BETA_BYTES, "beta rings");
+constexpr uint32_t T_S = 128;               // 64: the scan CTA's fp32 state rows before the frame
+constexpr uint32_t T_O = 256;               // [2] x 128: Q S^T
 
 struct Params {
     const float* alpha;     // [B, H]
     const float* beta;      // [B, N, H]
     const float* state_in;  // [B, H, dv, dk] or nullptr
     float* state_out;       // [B, H, dv, dk] or nullptr
-    __nv_bfloat16* out;     // [B, N, H, dv]
     int H, N, dk, dv;
-    int chunks;             // ceil(N / 64) <= MAX_CHUNKS
     unsigned long long wait_limit_ns;
 };
 
@@ -71,41 +89,67 @@ __device__ __forceinline__ uint32_t kmaj(int row, int col, int box_bytes) {
     return (col >> 6) * box_bytes + row * 128 + (((((col & 63) >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1);
 }
 
-// tm_k, tm_v: [B, N, H, d] token tensors, box (64, 1, 64, 1); tm_q: box (64, 1, 128, 1)
+// tm_k, tm_v: [B, N, H, d] token tensors, box (64, 1, 64, 1); tm_q, tm_o: box (64, 1, 128, 1);
+// tm_s: state_out as [B H, dv, dk] fp32, box (128, 64, 1), unswizzled (unused when state_out is null)
 __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(THREADS, 1)
     step_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                const __grid_constant__ CUtensorMap tm_q, const Params p) {
+                const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
+                const __grid_constant__ CUtensorMap tm_s, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    uint64_t* ld_bar = bars;
-    uint64_t* mma_bar = bars + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
+    uint64_t* full = bars;                  // [NST] stage landed
+    uint64_t* empty = full + NST;           // [NST] the stage's MMAs retired
+    uint64_t* bk_empty = empty + NST;       // [NBK] the scaled box's MMAs retired
+    uint64_t* d_bar = bk_empty + NBK;       // every contraction MMA retired
+    uint64_t* c_bar = d_bar + 1;            // scan MMA retired
+    uint64_t* qfull = c_bar + 1;            // [2] q tile landed
+    uint64_t* o_bar = qfull + 2;            // [2] output MMA retired
+    uint64_t* scaled = o_bar + 2;           // [NBK] every worker has written its part of the scaled box
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(scaled + NBK);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5;
+    const bool worker = tid < NWORK;   // owns TMEM lane tid
+    const bool issuer = tid == NWORK;  // contraction loads and MMAs
     const int rank = static_cast<int>(cluster_ctarank());
+    const bool scan_cta = rank >= 2;
     const int bh = blockIdx.x / CS;
     const int b = bh / p.H, h = bh % p.H;
-    const int c_begin = (rank * p.chunks) / CS, c_end = ((rank + 1) * p.chunks) / CS;
-    const int nch = c_end - c_begin;                       // 0, 1 or 2
-    const int t0 = c_begin * CHUNK;
-    const int t1 = min(c_end * CHUNK, p.N);
+    const int C = (p.N + CHUNK - 1) / CHUNK;
     const int kb = p.dk > 64 ? 2 : 1, vb = p.dv > 64 ? 2 : 1;
+    const bool vload = scan_cta && rank - 2 < vb;          // this CTA's V box exists
     const uint32_t sbase = smem_u32(smem);
+    const int j = tid;
+    const int i0 = (rank - 2) * SR;                        // scan CTAs: first state row
+    const size_t soff = (static_cast<size_t>(b) * p.H + h) * p.dv * p.dk;
+    const float af = p.alpha[static_cast<size_t>(b) * p.H + h];
 
-    // boxes that are never loaded (d <= 64) must read as zero in the contraction's
-    // operands; the A, S and S-row tiles are written whole before they are read
-    if (kb < 2 || vb < 2)
-        for (int i = tid; i < OFF_Q / 16; i += THREADS) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+    // boxes that are never loaded must read as zero (the whole ring and the
+    // scaled boxes once; A, S and the state images are written whole)
+    for (int i = tid; i < OFF_A / 16; i += THREADS) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
-        mbar_init(ld_bar, 1);
-        mbar_init(mma_bar, 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&qfull[x], 1);
+            mbar_init(&o_bar[x], 1);
+        }
+        for (int x = 0; x < NBK; ++x) {
+            mbar_init(&bk_empty[x], 1);
+            mbar_init(&scaled[x], NWORK);
+        }
+        mbar_init(d_bar, 1);
+        mbar_init(c_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_o);
+        if (p.state_out != nullptr) prefetch_tmap(&tm_s);
     }
     if (warp == 0) {
         tmem_alloc(tmem_slot, 512);
@@ -116,295 +160,302 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tlane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t tlane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);   // workers only
     bool good = true;
-    uint32_t mma_phase = 0;
-    bool mma_pending = false;   // thread 0: a commit not yet waited for
+    int loads_issued = 0;   // issuer: ring loads issued (for the drain)
 
-    // ------------------------------------------------------------- loads
-    if (tid == 0 && nch > 0) {
-        mbar_arrive_expect_tx(ld_bar, nch * (kb + vb) * KBOX + kb * QBOX);
-        for (int c = 0; c < nch; ++c) {
-            uint8_t* kv = smem + OFF_KV + c * 2 * KTILE;
-            const int tok = (c_begin + c) * CHUNK;
-            for (int bx = 0; bx < kb; ++bx) tma_load_4d(kv + bx * KBOX, &tm_k, ld_bar, 64 * bx, h, tok, b);
-            for (int bx = 0; bx < vb; ++bx) tma_load_4d(kv + KTILE + bx * KBOX, &tm_v, ld_bar, 64 * bx, h, tok, b);
+    auto load_chunk = [&](int c) {   // issuer
+        const int s = c % NST;
+        uint8_t* st = smem + OFF_RING + s * STAGE;
+        mbar_arrive_expect_tx(&full[s], (kb + (vload ? 1 : 0)) * KBOX);
+        for (int bx = 0; bx < kb; ++bx) tma_load_4d(st + bx * KBOX, &tm_k, &full[s], 64 * bx, h, c * CHUNK, b);
+        if (vload) tma_load_4d(st + 2 * KBOX, &tm_v, &full[s], 64 * (rank - 2), h, c * CHUNK, b);
+        ++loads_issued;
+    };
+    if (issuer)
+        for (int c = 0; c < NST && c < C; ++c) load_chunk(c);
+
+    // scan CTAs: their state rows before the frame -- fp32 into TMEM (lane j,
+    // column T_S + r) for the update, bf16 image in shared memory for S A
+    if (scan_cta && worker) {
+        uint32_t sv[SR];
+#pragma unroll
+        for (int t = 0; t < SR; ++t) {   // all 64 loads in flight at once: one memory latency
+            const bool v = p.state_in != nullptr && j < p.dk && i0 + t < p.dv;
+            sv[t] = v ? __float_as_uint(p.state_in[soff + static_cast<size_t>(i0 + t) * p.dk + j]) : 0u;
         }
-        for (int bx = 0; bx < kb; ++bx) tma_load_4d(smem + OFF_Q + bx * QBOX, &tm_q, ld_bar, 64 * bx, h, t0, b);
+#pragma unroll
+        for (int r0 = 0; r0 < SR; r0 += 16) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+                *reinterpret_cast<__nv_bfloat16*>(smem + OFF_SIMG + kmaj(r0 + t, j, SRBOX)) =
+                    __float2bfloat16_rn(__uint_as_float(sv[r0 + t]));
+            tmem_st16(tlane + T_S + r0, *reinterpret_cast<const uint32_t(*)[16]>(&sv[r0]));
+        }
+        tmem_wait_st();
     }
-    // thread r: token t0 + r (beta), and column j = tid of this CTA's state rows
-    const int r = tid;
-    const bool tok_ok = nch > 0 && t0 + r < t1;
-    const float bval = tok_ok ? p.beta[(static_cast<size_t>(b) * p.N + t0 + r) * p.H + h] : 0.0f;
-    const float af = p.alpha[static_cast<size_t>(b) * p.H + h];
-    const int j = tid;
-    const int i0 = rank * SROWS;                            // this CTA's state rows
-    const size_t soff = (static_cast<size_t>(b) * p.H + h) * p.dv * p.dk;
-    float S[SROWS];
-#pragma unroll
-    for (int rr = 0; rr < SROWS; ++rr) {
-        const bool v = p.state_in != nullptr && j < p.dk && i0 + rr < p.dv;
-        S[rr] = v ? p.state_in[soff + static_cast<size_t>(i0 + rr) * p.dk + j] : 0.0f;
-    }
-    // image of this CTA's rows of S (before the frame): B operand of S_r A
-#pragma unroll
-    for (int rr = 0; rr < SROWS; ++rr)
-        *reinterpret_cast<__nv_bfloat16*>(smem + OFF_SIMG + kmaj(rr, j, SBOX)) = __float2bfloat16_rn(S[rr]);
 
-    if (nch > 0) good = mbar_wait(ld_bar, 0, p.wait_limit_ns, abort_flag);
-    good = __syncthreads_and(good);
-
-    // ------------------------------------------------- 1. partial contraction
-    if (good && nch > 0) {
-        // thread r scales token row r (chunk r / 64, row r % 64) by beta into the beta*K tile
-        if (r < nch * CHUNK) {
-            const int c = r / CHUNK, rw = r % CHUNK;
-            const uint8_t* src = smem + OFF_KV + c * 2 * KTILE + rw * 128;
-            uint8_t* dst = smem + OFF_BK + c * KTILE + rw * 128;
-            for (int bx = 0; bx < kb; ++bx)
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(src + bx * KBOX + ch * 16);
-                    const uint32_t* xs = reinterpret_cast<const uint32_t*>(&x);
-                    uint32_t y[4];
+    // ------------------------------------------------ 1. the contraction slice
+    constexpr uint32_t ID_D = idesc_bf16(128, 64, 1, 1);
+    int c_done = 0;          // workers: chunks scaled; issuer: chunks whose MMAs were issued
+    bool d_issued = false;   // issuer: the final commit of the contraction
+    if (worker) {
+        // thread pair (2 row, 2 row + 1): token row `row` of the chunk, 16-byte
+        // pieces 4 half .. 4 half + 3 of this CTA's B box
+        const int row = tid >> 1, half = tid & 1;
+        // beta of this thread's token row: a per-thread ring in shared memory
+        // filled by cp.async BETA_AHEAD chunks ahead (each thread reads back
+        // only what it copied), so no global-load latency sits inside a chunk
+        float* beta_ring = reinterpret_cast<float*>(smem + OFF_BETA);
+        int pslot = 0, cslot = 0;
+        auto beta_prefetch = [&](int c) {
+            float* dst = beta_ring + pslot * NWORK + tid;
+            const int tok = c * CHUNK + row;
+            if (c < C && tok < p.N)
+                cp_async_4(dst, p.beta + (static_cast<size_t>(b) * p.N + tok) * p.H + h);
+            else
+                *dst = 0.0f;
+            cp_async_commit();
+            if (++pslot == BETA_AHEAD + 1) pslot = 0;
+        };
+        for (int c = 0; c < BETA_AHEAD; ++c) beta_prefetch(c);
+        for (int c = 0; c < C; ++c) {
+            const int s = c % NST, bkb = c % NBK;
+            beta_prefetch(c + BETA_AHEAD);
+            cp_async_wait<BETA_AHEAD>();   // this chunk's copy has landed
+            const float bval = beta_ring[cslot * NWORK + tid];
+            if (++cslot == BETA_AHEAD + 1) cslot = 0;
+            if (!mbar_wait(&full[s], static_cast<uint32_t>((c / NST) & 1), p.wait_limit_ns, abort_flag) ||
+                (c >= NBK &&
+                 !mbar_wait(&bk_empty[bkb], static_cast<uint32_t>(((c / NBK) - 1) & 1), p.wait_limit_ns, abort_flag))) {
+                good = false;
+                break;
+            }
+            c_done = c + 1;
+            // B box of this CTA: K box `rank` or its V box (a box never loaded is zero)
+            const uint8_t* src = smem + OFF_RING + s * STAGE + (scan_cta ? 2 : rank) * KBOX + row * 128;
+            uint8_t* dst = smem + OFF_BK + bkb * KBOX + row * 128;
+            // pieces rotated by the row: the 8 threads of a quarter-warp touch 8
+            // different 16-byte bank groups; all loads issue before any store
+            uint4 x[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[e]));
-                        y[e] = pack_bf16x2(f2.x * bval, f2.y * bval);   // fp32 product rounded once
-                    }
-                    *reinterpret_cast<uint4*>(dst + bx * KBOX + ch * 16) = make_uint4(y[0], y[1], y[2], y[3]);
+            for (int c4 = 0; c4 < 4; ++c4) x[c4] = *reinterpret_cast<const uint4*>(src + (((c4 + 4 * half + row) & 7) << 4));
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const uint32_t* xs = reinterpret_cast<const uint32_t*>(&x[c4]);
+                uint32_t y[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[e]));
+                    y[e] = pack_bf16x2(f2.x * bval, f2.y * bval);   // fp32 product rounded once
                 }
+                *reinterpret_cast<uint4*>(dst + (((c4 + 4 * half + row) & 7) << 4)) = make_uint4(y[0], y[1], y[2], y[3]);
+            }
+            fence_proxy_async_smem();   // the scaled pieces are visible to the MMA
+            mbar_arrive(&scaled[bkb]);
         }
+        cp_async_wait<0>();   // no beta copy outlives the loop
+    } else if (issuer) {
+        for (int c = 0; c < C; ++c) {
+            const int s = c % NST, bkb = c % NBK;
+            if (!mbar_wait(&scaled[bkb], static_cast<uint32_t>((c / NBK) & 1), p.wait_limit_ns, abort_flag)) {
+                good = false;
+                break;
+            }
+            tc_fence_after();
+            // A: the raw K tile (both boxes); B: this CTA's scaled 64 columns
+            const uint32_t a_base = sbase + OFF_RING + s * STAGE;
+            const uint32_t b_base = sbase + OFF_BK + bkb * KBOX;
+            for (int kk = 0; kk < CHUNK / 16; ++kk)
+                mma_bf16(tmem + T_D, smem_desc(a_base + kk * 2048, KBOX, 1024), smem_desc(b_base + kk * 2048, KBOX, 1024),
+                         ID_D, (c > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&empty[s]);
+            mma_commit(&bk_empty[bkb]);
+            c_done = c + 1;
+            // refill the previous chunk's stage (its MMAs have most likely retired by now)
+            if (c >= 1 && c - 1 + NST < C) {
+                if (!mbar_wait(&empty[(c - 1) % NST], static_cast<uint32_t>(((c - 1) / NST) & 1), p.wait_limit_ns,
+                               abort_flag)) {
+                    good = false;
+                    break;
+                }
+                load_chunk(c - 1 + NST);
+            }
+        }
+        mma_commit(d_bar);   // tracks every contraction MMA issued, also after a given-up wait
+        d_issued = true;
+    }
+    good = good && mbar_wait(d_bar, 0, p.wait_limit_ns, abort_flag);
+    good = __syncthreads_and(good);
+    tc_fence_after();
+
+    // q tiles of this CTA's quarter of the tokens into the (now idle) ring
+    const int ntiles = (p.N + 127) / 128;
+    const int tile0 = (rank * ntiles) / CS, nq = ((rank + 1) * ntiles) / CS - tile0;
+    int q_issued = 0;   // thread 0
+    if (tid == 0 && good)
+        for (int t = 0; t < nq && t < 2; ++t) {
+            mbar_arrive_expect_tx(&qfull[t], kb * QBOX);
+            for (int bx = 0; bx < kb; ++bx)
+                tma_load_4d(smem + OFF_RING + t * TILE + bx * QBOX, &tm_q, &qfull[t], 64 * bx, h, (tile0 + t) * 128, b);
+            ++q_issued;
+        }
+
+    // ------------------------------------------ 2. A columns to the scan CTAs
+    if (!scan_cta && worker) {
+        // thread j: row j of D = A[j][64 rank .. + 63] = A[64 rank .. + 63][j] (A symmetric);
+        // both TMEM loads in flight before the one wait (a TMEM load's latency
+        // is long next to the work between loads)
+        uint32_t v[64];
+        if (good) {
+            tmem_ld32(tlane + T_D, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(tlane + T_D + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_wait_ld();
+        } else {
+#pragma unroll
+            for (int t = 0; t < 64; ++t) v[t] = 0u;
+        }
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+            const uint4 w = make_uint4(
+                pack_bf16x2(__uint_as_float(v[8 * q8 + 0]), __uint_as_float(v[8 * q8 + 1])),
+                pack_bf16x2(__uint_as_float(v[8 * q8 + 2]), __uint_as_float(v[8 * q8 + 3])),
+                pack_bf16x2(__uint_as_float(v[8 * q8 + 4]), __uint_as_float(v[8 * q8 + 5])),
+                pack_bf16x2(__uint_as_float(v[8 * q8 + 6]), __uint_as_float(v[8 * q8 + 7])));
+            const uint32_t o = sbase + OFF_A + kmaj(j, 64 * rank + 8 * q8, QBOX);
+            st_dsmem_v4(mapa_shared(o, 2), w);
+            st_dsmem_v4(mapa_shared(o, 3), w);
+        }
+    }
+    fence_proxy_async_cluster();
+    cluster_sync();  // ---------------------------------------------- (1) A complete in CTAs 2, 3
+
+    // -------------------------------------------------- 3. the state rows
+    if (scan_cta) {
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == 0 && good) {
             tc_fence_after();
-            constexpr uint32_t ID = idesc_bf16(128, 256, 1, 1);
-            for (int c = 0; c < nch; ++c) {
-                const uint32_t a_base = sbase + OFF_BK + c * KTILE;
-                const uint32_t b_base = sbase + OFF_KV + c * 2 * KTILE;
-                for (int kk = 0; kk < CHUNK / 16; ++kk)
-                    mma_bf16(tmem + T_D, smem_desc(a_base + kk * 2048, KBOX, 1024),
-                             smem_desc(b_base + kk * 2048, KBOX, 1024), ID, (c > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(mma_bar);
-            mma_pending = true;
+            constexpr uint32_t ID_C = idesc_bf16(128, SR, 0, 0);
+            const int nk = (p.dk + 15) / 16;
+            for (int kk = 0; kk < nk; ++kk)
+                mma_bf16(tmem + T_C, smem_desc(sbase + OFF_A + (kk >> 2) * QBOX + (kk & 3) * 32, 16, 1024),
+                         smem_desc(sbase + OFF_SIMG + (kk >> 2) * SRBOX + (kk & 3) * 32, 16, 1024), ID_C,
+                         kk > 0 ? 1u : 0u);
+            mma_commit(c_bar);
         }
-        good = mbar_wait(mma_bar, mma_phase, p.wait_limit_ns, abort_flag);
-        if (good) {
-            mma_phase ^= 1;
-            mma_pending = false;
-        }
+        if (good) good = mbar_wait(c_bar, 0, p.wait_limit_ns, abort_flag);
         good = __syncthreads_and(good);
         tc_fence_after();
-    }
-    // the A part of D (row j = TMEM lane j) -> fp32 partials part[c][j] = A_r[j][c]
-    // (column-major: consecutive threads write consecutive words); zeros without tokens
-    float* part = reinterpret_cast<float*>(smem + OFF_KV);
-    for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t v[32];
-        if (good && nch > 0) {
-            tmem_ld32(tlane + T_D + c0, v);
+        // thread j, rows i0 + r: S' = alpha (S - C[j][r]) + U[r][j], U = D column r,
+        // into fp32 staging rows (zero outside dv x dk); state_out by one TMA store
+        float* fstg = reinterpret_cast<float*>(smem + OFF_OSTG);
+        const bool col_ok = j < p.dk;
+        for (int r0 = 0; r0 < SR && worker; r0 += 32) {   // 32 rows: three TMEM loads, one wait
+            uint32_t cc[32], uu[32], so[32];
+            tmem_ld32(tlane + T_S + r0, so);
+            if (good) {
+                tmem_ld32(tlane + T_C + r0, cc);
+                tmem_ld32(tlane + T_D + r0, uu);
+            } else {
+#pragma unroll
+                for (int t = 0; t < 32; ++t) cc[t] = uu[t] = 0u;
+            }
             tmem_wait_ld();
-        } else {
 #pragma unroll
-            for (int t = 0; t < 32; ++t) v[t] = 0u;
+            for (int t = 0; t < 32; ++t) {
+                const float sn = af * (__uint_as_float(so[t]) - __uint_as_float(cc[t])) + __uint_as_float(uu[t]);
+                fstg[(r0 + t) * 128 + j] = (col_ok && i0 + r0 + t < p.dv) ? sn : 0.0f;
+            }
         }
-#pragma unroll
-        for (int t = 0; t < 32; ++t) part[(c0 + t) * 128 + j] = __uint_as_float(v[t]);
-    }
-    cluster_sync();  // ---------------------------------------------- (1)
-
-    // ---------------------------------------- 2a. A: reduce rows, share them
-    // rows of the CTA's 16-row block are written to a local bf16 staging block,
-    // then sent to every CTA's copy of A in 16-byte pieces
-    __nv_bfloat16* blk = reinterpret_cast<__nv_bfloat16*>(smem + OFF_SROW);   // [16][128]
-    auto send_rows = [&](uint32_t dst_off) {
-        for (int k = tid; k < SROWS * 16; k += THREADS) {
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0 && good && p.state_out != nullptr && i0 < p.dv) {   // rows past dv, columns past dk clipped
+            tma_store_3d(&tm_s, fstg, 0, i0, b * p.H + h);
+            bulk_commit();
+        }
+        // this CTA's 64 rows of the state, rounded to bf16, into every CTA's copy of S
+        for (int k = tid; k < SR * 16; k += THREADS) {
             const int rr = k / 16, ch = k % 16;   // 16 pieces of 8 columns per row
-            const uint4 w = *reinterpret_cast<const uint4*>(blk + rr * 128 + ch * 8);
-            const uint32_t o = sbase + dst_off + kmaj(i0 + rr, ch * 8, QBOX);
+            const float4 f0 = *reinterpret_cast<const float4*>(fstg + rr * 128 + ch * 8);
+            const float4 f1 = *reinterpret_cast<const float4*>(fstg + rr * 128 + ch * 8 + 4);
+            const uint4 w = make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f0.z, f0.w), pack_bf16x2(f1.x, f1.y),
+                                       pack_bf16x2(f1.z, f1.w));
+            const uint32_t o = sbase + OFF_S + kmaj(i0 + rr, ch * 8, QBOX);
             for (int q = 0; q < CS; ++q) st_dsmem_v4(mapa_shared(o, q), w);
         }
-    };
-    {
-        // thread c: column c of rows i0 .. i0 + 15, i.e. part[c][i0 .. i0 + 15] of every rank, summed in order
-        const int c = tid;
-        float acc[SROWS];
-#pragma unroll
-        for (int e = 0; e < SROWS; ++e) acc[e] = 0.0f;
-        const uint32_t local = sbase + OFF_KV + static_cast<uint32_t>(c * 128 + i0) * 4;
-        // all 32 loads in flight at once, then the adds in rank order
-        float4 x[CS][4];
-#pragma unroll
-        for (int q = 0; q < CS; ++q) {
-            const uint32_t remote = mapa_shared(local, q);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) x[q][e] = ld_dsmem_f32x4(remote + e * 16);
-        }
-#pragma unroll
-        for (int q = 0; q < CS; ++q)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                acc[4 * e] += x[q][e].x;
-                acc[4 * e + 1] += x[q][e].y;
-                acc[4 * e + 2] += x[q][e].z;
-                acc[4 * e + 3] += x[q][e].w;
-            }
-#pragma unroll
-        for (int e = 0; e < SROWS; ++e) blk[e * 128 + c] = __float2bfloat16_rn(acc[e]);
     }
-    __syncthreads();
-    send_rows(OFF_A);
-    // the U part of D -> fp32 partials [i][j] (U[i][j] = D[j][128 + i]); the A
-    // partials it overwrites have been read by every CTA only after barrier (2)
     fence_proxy_async_cluster();
-    cluster_sync();  // ---------------------------------------------- (2)
-    for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t v[32];
-        if (good && nch > 0) {
-            tmem_ld32(tlane + T_D + 128 + c0, v);
-            tmem_wait_ld();
-        } else {
-#pragma unroll
-            for (int t = 0; t < 32; ++t) v[t] = 0u;
-        }
-#pragma unroll
-        for (int t = 0; t < 32; ++t) part[(c0 + t) * 128 + j] = __uint_as_float(v[t]);
-    }
-    cluster_sync();  // ---------------------------------------------- (3)
-
-    // ------------------------------- 2b. U: this CTA's rows, summed in rank order
-    // thread t sums row t / 8, columns 16 (t % 8) .. + 15 (16-byte remote loads)
-    // into a local fp32 block; thread j then takes column j of it
-    float* ured = reinterpret_cast<float*>(smem + OFF_BK);   // [16][128] (the beta*K tiles are done)
-    {
-        const int rr = tid / 8, col0 = (tid % 8) * 16;
-        float acc[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) acc[e] = 0.0f;
-        const uint32_t local = sbase + OFF_KV + static_cast<uint32_t>((i0 + rr) * 128 + col0) * 4;
-        float4 x[CS][4];
-#pragma unroll
-        for (int q = 0; q < CS; ++q) {
-            const uint32_t remote = mapa_shared(local, q);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) x[q][e] = ld_dsmem_f32x4(remote + e * 16);
-        }
-#pragma unroll
-        for (int q = 0; q < CS; ++q)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                acc[4 * e] += x[q][e].x;
-                acc[4 * e + 1] += x[q][e].y;
-                acc[4 * e + 2] += x[q][e].z;
-                acc[4 * e + 3] += x[q][e].w;
-            }
-#pragma unroll
-        for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(ured + rr * 128 + col0 + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
-    }
-    __syncthreads();
-    float U[SROWS];
-#pragma unroll
-    for (int rr = 0; rr < SROWS; ++rr) U[rr] = ured[rr * 128 + j];
-
-    // ------------------------------------------ 3. the state rows of this CTA
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && good) {
-        tc_fence_after();
-        constexpr uint32_t ID = idesc_bf16(128, SROWS, 0, 0);
-        const int nk = (p.dk + 15) / 16;
-        for (int kk = 0; kk < nk; ++kk) {
-            const uint32_t ko = (kk >> 2) * QBOX + (kk & 3) * 32;
-            const uint32_t so = (kk >> 2) * SBOX + (kk & 3) * 32;
-            mma_bf16(tmem + T_C, smem_desc(sbase + OFF_A + ko, 16, 1024), smem_desc(sbase + OFF_SIMG + so, 16, 1024),
-                     ID, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(mma_bar);
-        mma_pending = true;
-    }
-    if (good) {
-        good = mbar_wait(mma_bar, mma_phase, p.wait_limit_ns, abort_flag);
-        if (good) {
-            mma_phase ^= 1;
-            mma_pending = false;
-        }
-    }
-    good = __syncthreads_and(good);
-    tc_fence_after();
-    {
-        uint32_t c16[16];
-        if (good) {
-            tmem_ld16(tlane + T_C, c16);
-            tmem_wait_ld();
-        } else {
-#pragma unroll
-            for (int t = 0; t < 16; ++t) c16[t] = 0u;
-        }
-#pragma unroll
-        for (int rr = 0; rr < SROWS; ++rr) {
-            const float sn = af * (S[rr] - __uint_as_float(c16[rr])) + U[rr];
-            if (good && p.state_out != nullptr && j < p.dk && i0 + rr < p.dv)
-                p.state_out[soff + static_cast<size_t>(i0 + rr) * p.dk + j] = sn;
-            blk[rr * 128 + j] = __float2bfloat16_rn(j < p.dk && i0 + rr < p.dv ? sn : 0.0f);
-        }
-    }
-    __syncthreads();
-    send_rows(OFF_S);   // this CTA's 16 rows of the bf16 state into every CTA's copy of S
-    fence_proxy_async_cluster();
-    cluster_sync();  // ---------------------------------------------- (4)
+    cluster_sync();  // ---------------------------------------------- (2) S complete everywhere
     fence_proxy_async_smem();
 
-    // --------------------------------------------- 4. outputs of this CTA's tokens
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && good && nch > 0) {
-        tc_fence_after();
-        constexpr uint32_t ID = idesc_bf16(128, 128, 0, 0);
-        const int nk = (p.dk + 15) / 16;
-        for (int kk = 0; kk < nk; ++kk) {
-            const uint32_t ko = (kk >> 2) * QBOX + (kk & 3) * 32;
-            mma_bf16(tmem + T_O, smem_desc(sbase + OFF_Q + ko, 16, 1024), smem_desc(sbase + OFF_S + ko, 16, 1024), ID,
-                     kk > 0 ? 1u : 0u);
+    // ------------------------------------------------------- 4. the outputs
+    int q_done = 0;
+    for (int t = 0; t < nq; ++t) {
+        const int x = t & 1;
+        if (t >= 2 && tid == 0 && good) {  // the tile two back has been consumed: refill its buffer
+            mbar_arrive_expect_tx(&qfull[x], kb * QBOX);
+            for (int bx = 0; bx < kb; ++bx)
+                tma_load_4d(smem + OFF_RING + x * TILE + bx * QBOX, &tm_q, &qfull[x], 64 * bx, h, (tile0 + t) * 128, b);
+            ++q_issued;
         }
-        mma_commit(mma_bar);
-        mma_pending = true;
-    }
-    if (good && nch > 0) {
-        good = mbar_wait(mma_bar, mma_phase, p.wait_limit_ns, abort_flag);
-        if (good) {
-            mma_phase ^= 1;
-            mma_pending = false;
-        }
-    }
-    good = __syncthreads_and(good);
-    tc_fence_after();
-    if (good && nch > 0) {
-        // thread r: output row of token t0 + r
-        __nv_bfloat16* orow = p.out + ((static_cast<size_t>(b) * p.N + (tok_ok ? t0 + r : 0)) * p.H + h) * p.dv;
-        for (int c0 = 0; c0 < p.dv; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tlane + T_O + c0, v);
-            tmem_wait_ld();
-            if (tok_ok) {
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8)
-                    if (c0 + 8 * q8 < p.dv)
-                        *reinterpret_cast<uint4*>(orow + c0 + 8 * q8) = make_uint4(
-                            pack_bf16x2(__uint_as_float(v[8 * q8 + 0]), __uint_as_float(v[8 * q8 + 1])),
-                            pack_bf16x2(__uint_as_float(v[8 * q8 + 2]), __uint_as_float(v[8 * q8 + 3])),
-                            pack_bf16x2(__uint_as_float(v[8 * q8 + 4]), __uint_as_float(v[8 * q8 + 5])),
-                            pack_bf16x2(__uint_as_float(v[8 * q8 + 6]), __uint_as_float(v[8 * q8 + 7])));
+        if (good) good = mbar_wait(&qfull[x], static_cast<uint32_t>((t >> 1) & 1), p.wait_limit_ns, abort_flag);
+        good = __syncthreads_and(good);
+        if (!good) break;
+        q_done = t + 1;
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t ID_O = idesc_bf16(128, 128, 0, 0);
+            const int nk = (p.dk + 15) / 16;
+            for (int kk = 0; kk < nk; ++kk) {
+                const uint32_t ko = (kk >> 2) * QBOX + (kk & 3) * 32;
+                mma_bf16(tmem + T_O + x * 128, smem_desc(sbase + OFF_RING + x * TILE + ko, 16, 1024),
+                         smem_desc(sbase + OFF_S + ko, 16, 1024), ID_O, kk > 0 ? 1u : 0u);
             }
+            mma_commit(&o_bar[x]);
+        }
+        good = mbar_wait(&o_bar[x], static_cast<uint32_t>((t >> 1) & 1), p.wait_limit_ns, abort_flag);
+        good = __syncthreads_and(good);
+        if (!good) break;
+        tc_fence_after();
+        // the previous store out of the staging tile (a tile's outputs, or the
+        // state rows) has finished reading it
+        if (tid == 0) bulk_wait_read<0>();
+        __syncthreads();
+        // thread j: token row j of the tile, bf16, into the swizzled staging boxes
+        for (int c0 = 0; c0 < p.dv && worker; c0 += 64) {   // 64 columns: two TMEM loads, one wait
+            uint32_t v[64];
+            tmem_ld32(tlane + T_O + x * 128 + c0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(tlane + T_O + x * 128 + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_wait_ld();
+#pragma unroll
+            for (int q8 = 0; q8 < 8; ++q8)
+                *reinterpret_cast<uint4*>(smem + OFF_OSTG + kmaj(j, c0 + 8 * q8, QBOX)) = make_uint4(
+                    pack_bf16x2(__uint_as_float(v[8 * q8 + 0]), __uint_as_float(v[8 * q8 + 1])),
+                    pack_bf16x2(__uint_as_float(v[8 * q8 + 2]), __uint_as_float(v[8 * q8 + 3])),
+                    pack_bf16x2(__uint_as_float(v[8 * q8 + 4]), __uint_as_float(v[8 * q8 + 5])),
+                    pack_bf16x2(__uint_as_float(v[8 * q8 + 6]), __uint_as_float(v[8 * q8 + 7])));
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();  // buffer x and its accumulator are reused two tiles on
+        if (tid == 0) {   // tokens past N and columns past dv are clipped by the store
+            for (int bx = 0; bx < vb; ++bx)
+                tma_store_4d(&tm_o, smem + OFF_OSTG + bx * QBOX, 64 * bx, h, (tile0 + t) * 128, b);
+            bulk_commit();
         }
     }
-    // a copy or MMA of a given-up wait must land before the CTA leaves
+    if (tid == 0) bulk_wait<0>();   // the output stores are complete before the CTA leaves
+    // copies or MMAs of a given-up wait must land before the CTA leaves
+    if (issuer && !good) {
+        for (int k = c_done; k < loads_issued; ++k)
+            mbar_wait_drain(&full[k % NST], static_cast<uint32_t>((k / NST) & 1), p.wait_limit_ns);
+        if (d_issued) mbar_wait_drain(d_bar, 0, p.wait_limit_ns);
+    }
     if (tid == 0 && !good) {
-        if (nch > 0) mbar_wait_drain(ld_bar, 0, p.wait_limit_ns);
-        if (mma_pending) mbar_wait_drain(mma_bar, mma_phase, p.wait_limit_ns);
+        for (int k = q_done; k < q_issued; ++k)
+            mbar_wait_drain(&qfull[k & 1], static_cast<uint32_t>((k >> 1) & 1), p.wait_limit_ns);
     }
     tc_fence_before();
     __syncthreads();

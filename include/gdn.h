@@ -282,13 +282,15 @@ void gdn_set_contract_split(int max_split);
 
 /*
  * The one-launch step.  on != 0 (default): gdn_frame_step and
- * gdn_frame_step_noalloc run a frame of at most 1024 tokens (bf16 inputs) as
- * one kernel: one thread-block cluster of 8 CTAs per head computes the
- * frame's contractions on its tokens, reduces them through distributed shared
- * memory in a fixed order, advances its rows of the state and writes the
- * frame's outputs, with no workspace in HBM.  on = 0: the three-phase path
- * (two launches and a workspace).  Results agree to rounding (the partial
- * sums are added in a different order).  Applies to calls made after it
+ * gdn_frame_step_noalloc run a frame with bf16 inputs as one kernel: one
+ * thread-block cluster of 4 CTAs per head splits the frame's contraction by
+ * its columns (two CTAs form A, two form U, each over all tokens), the U CTAs
+ * advance the state rows with A received through distributed shared memory,
+ * and all four write outputs for a quarter of the frame's 128-token tiles,
+ * with no workspace in HBM and no cross-CTA sums.  on = 0: the three-phase
+ * path (two launches and a workspace).  The two agree to bf16 rounding: the
+ * one-launch step rounds the product beta k (or beta v) on the other factor
+ * of each contraction term than phase 1 does.  Applies to calls made after it
  * returns.  A scheduling control of this library; the pages have no
  * counterpart.
  */
@@ -325,10 +327,10 @@ const char* gdn_version(void);
  * workspace lives instead in one fixed array of GDN_STEP_NOALLOC_SCRATCH_BYTES
  * bytes in the library's device image: every GPU that loads the library
  * holds it until the process exits.  No call allocates or frees memory.
- *   - Frames of at most 1024 tokens run as the one-launch step (see
- *     gdn_set_fused_step) and use no scratch at all.  Longer frames use the
- *     array: a shape whose workspace (gdn_step_workspace_bytes) exceeds it
- *     returns GDN_ERR_TOO_LARGE before anything is launched.
+ *   - With the one-launch step on (gdn_set_fused_step, the default) the call
+ *     uses no scratch at all.  Otherwise it uses the array: a shape whose
+ *     workspace (gdn_step_workspace_bytes) exceeds it returns
+ *     GDN_ERR_TOO_LARGE before anything is launched.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture starts.

@@ -1,10 +1,11 @@
-"""GPU parity of the one-launch step (one 8-CTA cluster per head) against the
-fp64 oracle and against the three-phase step path.
+"""GPU parity of the one-launch step (one 4-CTA cluster per head, the frame's
+contraction split by columns) against the fp64 oracle and against the
+three-phase step path.
 
-Shapes cover one token, tokens fewer than the cluster's CTAs have chunks
-(CTAs with no tokens), a ragged last chunk, the largest frame the fused step
-takes (1024 tokens, two chunks per CTA), head sizes 32 / 64 / 128 with
-dk != dv, more clusters than SMs, a NULL state_in and an in-place state.
+Shapes cover one token, a single chunk, ragged last chunks, frames longer
+than the ring (up to 8800 tokens), head sizes 32 / 64 / 128 with dk != dv
+(CTAs whose 64 columns are all padding), more clusters than fit at once, a
+NULL state_in and an in-place state.
 """
 import numpy as np
 import pytest
@@ -27,11 +28,12 @@ def step_args(x):
 
 @pytest.mark.parametrize("shape", [
     (1, 2, 1, 64, 64),       # one token
-    (1, 4, 100, 128, 128),   # 2 chunks: six of the eight CTAs have no tokens
-    (1, 3, 448, 64, 128),    # 7 chunks, dk != dv
+    (1, 4, 100, 128, 128),   # 2 chunks, ragged
+    (1, 3, 448, 64, 128),    # dk != dv: the second A CTA's columns are padding
     (1, 16, 880, 128, 128),  # the 60 s shape's frame
-    (2, 3, 1000, 32, 32),    # ragged last chunk, d = 32
-    (1, 2, 1024, 128, 48),   # the largest fused frame: two chunks per CTA
+    (2, 3, 1000, 32, 32),    # d = 32
+    (1, 2, 1024, 128, 48),   # dv = 48: the second U CTA's rows are padding
+    (1, 4, 8800, 128, 128),  # 138 chunks through the 4-deep ring
     (2, 40, 200, 64, 64),    # 80 clusters: more CTAs than SMs
 ])
 def test_fused_step_matches_oracle_and_three_phase_step(shape):
@@ -53,9 +55,11 @@ def test_fused_step_matches_oracle_and_three_phase_step(shape):
     print(f"fused step {shape}: err_O={eo:.3e} err_S={es:.3e}")
     assert np.isfinite(o1.float().cpu().numpy()).all()
     assert eo <= TOL_OUT and es <= TOL_STATE
-    # the two paths differ only in the order the partial sums are added
-    assert rel_err(o1.float().cpu().numpy(), o3.float().cpu().numpy()) <= 5e-3
-    assert rel_err(s1.cpu().numpy(), s3.cpu().numpy()) <= 2e-3
+    # the two paths take the same sums in another order, and round the beta
+    # product on the other factor (beta v / beta k on the B operand here,
+    # beta k on the A operand in phase 1): bf16-level differences only
+    assert rel_err(o1.float().cpu().numpy(), o3.float().cpu().numpy()) <= TOL_OUT / 2
+    assert rel_err(s1.cpu().numpy(), s3.cpu().numpy()) <= TOL_STATE
 
 
 def test_fused_step_null_and_in_place_state_and_determinism():

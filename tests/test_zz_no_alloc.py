@@ -51,8 +51,11 @@ def test_noalloc_step_matches_step_on_two_calls_in_a_row():
 
 
 def test_noalloc_step_rejects_shapes_beyond_its_scratch():
+    """With the one-launch step off the call runs on the fixed scratch array,
+    and a shape whose workspace exceeds it is refused before any launch."""
     ensure_built()
     lib = load()
+    lib.gdn_set_fused_step(0)
     B, H, N, d = 4, 72, 1100, 128        # 288 heads: 36+ MiB of workspace
     q = torch.zeros((B, N, H, d), dtype=torch.bfloat16, device="cuda")
     k, v, out = torch.zeros_like(q), torch.zeros_like(q), torch.zeros_like(q)
@@ -61,5 +64,10 @@ def test_noalloc_step_rejects_shapes_beyond_its_scratch():
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     rc = lib.gdn_frame_step_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), None, _ptr(out), None,
                                     B, H, N, d, d, stream)
+    lib.gdn_set_fused_step(1)
     assert rc == 10  # GDN_ERR_TOO_LARGE, nothing launched
     assert lib.gdn_step_workspace_bytes(B, H, N, d, d) > (32 << 20)
+    # the one-launch step needs no scratch: the same shape runs
+    rc = lib.gdn_frame_step_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), None, _ptr(out), None,
+                                    B, H, N, d, d, stream)
+    assert rc == 0 and lib.gdn_sync_status(stream) == 0
