@@ -97,12 +97,17 @@ def path_floor_bytes(w, in_bytes=2):
             + w.B * w.H * w.dv * w.dk * 4)
 
 
+# the sources the forward pass's kernels (phase 1, phases 2+3) are built from;
+# the step and backward kernels live in files of their own
+FORWARD_SOURCES = ("gdn_api.cu", "gdn_k1_contract.cuh", "gdn_k23_fused.cuh", "gdn_k2_scan.cuh", "gdn_k3_output.cuh",
+                   "gdn_ptx.cuh")
+
+
 def kernel_source_sha():
     h = hashlib.sha256()
     d = os.path.join(ROOT, "frame_wise_gated_forward_b300", "csrc")
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(d, f), "rb").read())
+    for f in FORWARD_SOURCES:
+        h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
 
