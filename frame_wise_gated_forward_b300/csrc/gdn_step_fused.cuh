@@ -125,9 +125,11 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(THREADS, 1)
     const size_t soff = (static_cast<size_t>(b) * p.H + h) * p.dv * p.dk;
     const float af = p.alpha[static_cast<size_t>(b) * p.H + h];
 
-    // boxes that are never loaded must read as zero (the whole ring and the
-    // scaled boxes once; A, S and the state images are written whole)
-    for (int i = tid; i < OFF_A / 16; i += THREADS) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+    // ring boxes that are never loaded must read as zero: with dk <= 64 (no k
+    // box 1) or a U CTA without a v box, clear the ring and the scaled boxes
+    // once (A, S and the state images are always written whole)
+    if (kb == 1 || (scan_cta && !vload))
+        for (int i = tid; i < OFF_A / 16; i += THREADS) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 1);
@@ -175,24 +177,18 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(THREADS, 1)
     if (issuer)
         for (int c = 0; c < NST && c < C; ++c) load_chunk(c);
 
-    // scan CTAs: their state rows before the frame -- fp32 into TMEM (lane j,
-    // column T_S + r) for the update, bf16 image in shared memory for S A
-    if (scan_cta && worker) {
-        uint32_t sv[SR];
+    // scan CTAs: their state rows before the frame, loaded now (all 64 loads in
+    // flight, addresses clamped into the matrix) and used after the
+    // contraction, so the loads' latency hides behind it
+    const bool load_state = scan_cta && worker && p.state_in != nullptr;
+    uint32_t sv[SR];
+    if (load_state) {
+        const int jc = j < p.dk ? j : p.dk - 1;
 #pragma unroll
-        for (int t = 0; t < SR; ++t) {   // all 64 loads in flight at once: one memory latency
-            const bool v = p.state_in != nullptr && j < p.dk && i0 + t < p.dv;
-            sv[t] = v ? __float_as_uint(p.state_in[soff + static_cast<size_t>(i0 + t) * p.dk + j]) : 0u;
+        for (int t = 0; t < SR; ++t) {
+            const int ic = i0 + t < p.dv ? i0 + t : p.dv - 1;
+            sv[t] = __float_as_uint(p.state_in[soff + static_cast<size_t>(ic) * p.dk + jc]);
         }
-#pragma unroll
-        for (int r0 = 0; r0 < SR; r0 += 16) {
-#pragma unroll
-            for (int t = 0; t < 16; ++t)
-                *reinterpret_cast<__nv_bfloat16*>(smem + OFF_SIMG + kmaj(r0 + t, j, SRBOX)) =
-                    __float2bfloat16_rn(__uint_as_float(sv[r0 + t]));
-            tmem_st16(tlane + T_S + r0, *reinterpret_cast<const uint32_t(*)[16]>(&sv[r0]));
-        }
-        tmem_wait_st();
     }
 
     // ------------------------------------------------ 1. the contraction slice
@@ -255,6 +251,23 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(THREADS, 1)
             mbar_arrive(&scaled[bkb]);
         }
         cp_async_wait<0>();   // no beta copy outlives the loop
+        // scan CTAs: the state rows -- fp32 into TMEM (lane j, column T_S + r)
+        // for the update, bf16 image in shared memory for S A (zero outside
+        // dv x dk, and for a null state_in)
+        if (scan_cta) {
+#pragma unroll
+            for (int r0 = 0; r0 < SR; r0 += 16) {
+                uint32_t w[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    w[t] = (load_state && j < p.dk && i0 + r0 + t < p.dv) ? sv[r0 + t] : 0u;
+                    *reinterpret_cast<__nv_bfloat16*>(smem + OFF_SIMG + kmaj(r0 + t, j, SRBOX)) =
+                        __float2bfloat16_rn(__uint_as_float(w[t]));
+                }
+                tmem_st16(tlane + T_S + r0, w);
+            }
+            tmem_wait_st();
+        }
     } else if (issuer) {
         for (int c = 0; c < C; ++c) {
             const int s = c % NST, bkb = c % NBK;
