@@ -41,7 +41,7 @@ constexpr int NWORK = 128;                  // warps 0-3
 constexpr int THREADS = NWORK + 32;         // + the contraction's issuer warp
 constexpr int CHUNK = 64;                   // tokens per ring stage
 constexpr int NST = 4;                      // ring depth
-constexpr int NBK = 4;                      // scaled B boxes in flight (workers run up to NBK chunks ahead of the MMAs)
+constexpr int NBK = 2;                      // scaled B boxes in flight (workers run up to NBK chunks ahead of the MMAs)
 constexpr int KBOX = CHUNK * 128;           // 64 token rows x 128 B
 constexpr int STAGE = 3 * KBOX;             // K box 0 | K box 1 | this CTA's V box
 constexpr int QBOX = 128 * 128;             // 128 rows x 128 B
