@@ -7,7 +7,8 @@
 // by tokens, so no CTA ever adds another CTA's partial sums:
 //   CTA 0, 1: columns [64 r, 64 r + 64) of A = K^T B K   (B operand: K box r)
 //   CTA 2, 3: rows [64 (r-2), + 64) of U = V^T B K        (B operand: V box r-2)
-// each over all N tokens of the frame (a ring of 64-token chunks).  The MMA's
+// each over all N tokens of the frame (a 4-deep ring of 64-token chunks; the
+// U CTAs' state-row loads are issued before it and used after it).  The MMA's
 // A operand is the raw K tile; each CTA scales only its own 64 B-operand
 // columns by beta (the fp32 product rounded once to bf16), so the rounding
 // sits on the other factor than in phase 1 -- the same sum to bf16 accuracy.
@@ -58,6 +59,8 @@ constexpr int OFF_S = OFF_A + TILE;                      // S after the frame, K
 constexpr int OFF_SIMG = OFF_S + TILE;                   // scan CTA's 64 rows of S before the frame, K-major
 constexpr int OFF_BETA = OFF_SIMG + 2 * SRBOX;           // per-thread beta rings of the contraction
 constexpr int BETA_BYTES = 4096;
+constexpr int BETA_AHEAD = 4;                            // beta copies in flight per thread
+static_assert((BETA_AHEAD + 1) * NWORK * 4 <= BETA_BYTES, "beta rings");
 constexpr int OFF_BAR = OFF_BETA + BETA_BYTES;
 constexpr int NBARS = 2 * NST + 2 + 2 * 2 + 2 * NBK;     // full, empty; d, c; qfull, o_bar; bk_empty, scaled
 constexpr int BAR_BYTES = 256;                           // the barriers, the TMEM address and the abort flag
@@ -69,8 +72,6 @@ static_assert(SMEM_BYTES <= 232448, "shared memory");
 // TMEM columns
 constexpr uint32_t T_D = 0;                 // 64: this CTA's columns of D
 constexpr uint32_t T_C = 64;                // 64: S_rows A (scan CTAs)
-constexpr int BETA_AHEAD = 4;               // beta copies in flight per thread
-static_assert((BETA_AHEAD + 1) * NWORK * 4 <= BETA_BYTES, "beta rings");
 constexpr uint32_t T_S = 128;               // 64: the scan CTA's fp32 state rows before the frame
 constexpr uint32_t T_O = 256;               // [2] x 128: Q S^T
 
