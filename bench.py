@@ -98,16 +98,29 @@ def path_floor_bytes(w, in_bytes=2):
 
 
 # the sources the forward pass's kernels (phase 1, phases 2+3) are built from;
-# the step and backward kernels live in files of their own
+# the step and backward kernels live in files of their own, and the one-launch
+# step's host launcher is cut out of gdn_api.cu before hashing
 FORWARD_SOURCES = ("gdn_api.cu", "gdn_k1_contract.cuh", "gdn_k23_fused.cuh", "gdn_k2_scan.cuh", "gdn_k3_output.cuh",
                    "gdn_ptx.cuh")
 
 
-def kernel_source_sha():
-    h = hashlib.sha256()
+def forward_part(name, text):
+    if name == "gdn_api.cu":
+        i = text.find(b"gdn_status launch_step_fused(")
+        j = text.find(b"\n}\n", i) if i >= 0 else -1
+        if i >= 0 and j >= 0:
+            text = text[:i] + text[j + 3:]
+    return text
+
+
+def kernel_source_sha(read=None):
+    """Hash of the forward kernels' sources; `read(name)` returns a file's
+    bytes (default: the working tree)."""
     d = os.path.join(ROOT, "frame_wise_gated_forward_b300", "csrc")
+    read = read or (lambda f: open(os.path.join(d, f), "rb").read())
+    h = hashlib.sha256()
     for f in FORWARD_SOURCES:
-        h.update(open(os.path.join(d, f), "rb").read())
+        h.update(forward_part(f, read(f)))
     return h.hexdigest()[:16]
 
 

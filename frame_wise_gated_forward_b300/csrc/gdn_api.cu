@@ -493,9 +493,25 @@ gdn_status launch_step_fused(const PassArgs& a, cudaStream_t stream) {
     ps.dk = a.dk;
     ps.dv = a.dv;
     ps.wait_limit_ns = g_wait_limit_ns.load();
-    gdn::step::step_kernel<<<a.B * a.H * gdn::step::CS, gdn::step::THREADS, gdn::step::SMEM_BYTES, stream>>>(
-        tm_k, tm_v, tm_q, tm_o, tm_s, ps);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+    // programmatic dependent launch: the kernel's prologue (barriers, TMEM,
+    // tensor-map prefetch) overlaps the end of the previous grid in the
+    // stream; the kernel waits for that grid before its first global access
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.H * gdn::step::CS));
+    cfg.blockDim = dim3(gdn::step::THREADS);
+    cfg.dynamicSmemBytes = gdn::step::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, gdn::step::step_kernel, tm_k, tm_v, tm_q, tm_o, tm_s, ps) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_LAUNCH;
+    }
+    return GDN_OK;
 }
 
 // Pooled-workspace pass: gdn_frame_forward (step = false) and gdn_frame_step.

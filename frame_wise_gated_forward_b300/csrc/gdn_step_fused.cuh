@@ -37,6 +37,15 @@
 namespace gdn {
 namespace step {
 
+// Programmatic dependent launch: wait until the grids this one depends on in
+// the stream have completed and their memory is visible (a no-op for a grid
+// launched without the programmatic-serialization attribute), and let the
+// next such grid in the stream be scheduled before this one ends.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 constexpr int CS = 4;                       // CTAs per cluster (one head)
 constexpr int NWORK = 128;                  // warps 0-3
 constexpr int THREADS = NWORK + 32;         // + the contraction's issuer warp
@@ -124,7 +133,6 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(THREADS, 1)
     const int j = tid;
     const int i0 = (rank - 2) * SR;                        // scan CTAs: first state row
     const size_t soff = (static_cast<size_t>(b) * p.H + h) * p.dv * p.dk;
-    const float af = p.alpha[static_cast<size_t>(b) * p.H + h];
 
     // ring boxes that are never loaded must read as zero: with dk <= 64 (no k
     // box 1) or a U CTA without a v box, clear the ring and the scaled boxes
@@ -162,6 +170,12 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Everything above touches no global memory, so with programmatic launch
+    // it overlaps the end of the previous step; every global access comes
+    // after the wait (the previous grid may have written this step's inputs).
+    griddep_wait();
+    griddep_launch_dependents();
+    const float af = p.alpha[static_cast<size_t>(b) * p.H + h];
     const uint32_t tmem = *tmem_slot;
     const uint32_t tlane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);   // workers only
     bool good = true;

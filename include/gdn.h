@@ -194,8 +194,11 @@ gdn_status gdn_frame_step_fp8(const void* q, const void* k, const void* v,
  *   q, k   bf16 [B, N, H, dk];  v, out bf16 [B, N, H, dv];
  *   alpha  fp32 [B, H];         beta fp32 [B, N, H];
  *   state_in / state_out fp32 [B, H, dv, dk]; state_out may equal state_in.
- * The frame's tokens are split across CTAs; the per-split partial sums are
- * added in a fixed order, so the result is deterministic.
+ * By default (gdn_set_fused_step) the frame runs as one kernel, launched with
+ * programmatic dependent launch: its prologue (barriers, tensor memory) may
+ * overlap the end of the previous kernel in the stream, and it touches no
+ * global memory before that kernel has completed.  Every sum is taken in a
+ * fixed order, so the result is deterministic.
  */
 gdn_status gdn_frame_step(const void* q, const void* k, const void* v,
                           const float* alpha, const float* beta,
