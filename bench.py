@@ -207,6 +207,12 @@ def cpu_baseline_run(w, x, frames):
     return w.B * frames * w.N, dt, oracle.max_threads()
 
 
+def workload_desc(w):
+    """The workload's name and shape, the same string on both arms."""
+    return (f"{w.name}: 60 s 720p latent sequence, B={w.B} H={w.H} F={w.F} N={w.N} "
+            f"dk={w.dk} dv={w.dv}, bf16 q/k/v/out, fp32 alpha/beta/state")
+
+
 def run_reference(args, w):
     """--impl reference: the fp64 CPU oracle on a bounded sample of the workload per step."""
     from frame_wise_gated_forward_b300 import inputs, replicas
@@ -232,7 +238,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": f"{w.name}: B={w.B} H={w.H} F={w.F} N={w.N} dk={w.dk} dv={w.dv}",
+        "data": "synthetic", "config": {"workload": workload_desc(w), "tokens_per_step_per_gpu": w.B * w.F * w.N,
                                         "sample": sample},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -472,8 +478,7 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"{w.name}: 60 s 720p latent sequence, B={w.B} H={w.H} F={w.F} N={w.N} "
-                                   f"dk={w.dk} dv={w.dv}, bf16 q/k/v/out, fp32 alpha/beta/state",
+            "config": {"workload": workload_desc(w),
                        "tokens_per_step_per_gpu": tokens,
                        "l2": "inputs 1.31 GB per step > 126 MB L2; no flush",
                        "parallelism": f"replicas x{world} (no data-path collective)",
