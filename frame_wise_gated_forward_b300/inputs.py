@@ -118,6 +118,54 @@ def draw_fp8(B: int, H: int, F: int, N: int, dk: int, dv: int, seed: int,
             "alpha": alpha, "beta": beta, "state_in": s0}
 
 
+E2M1_MAX = 6.0
+# the eight non-negative E2M1 magnitudes, in code order (codes 0..7)
+E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def quantize_nvfp4(x: torch.Tensor):
+    """NVFP4 with 16-element blocks along the last dimension: one fp32 tensor
+    scale gs = amax / (6 * 448), one E4M3 block scale per 16 elements
+    (round-to-nearest-even of block amax / (6 gs)), and E2M1 codes, each the
+    nearest E2M1 value to x / (gs * block scale) (ties to the even code).
+    Returns (packed uint8 [..., d/2] with element 2i in the low nibble, block
+    scale codes uint8 [..., d/16], gs).  Input preparation only: the method
+    itself never quantizes."""
+    d = x.shape[-1]
+    if d % 16:
+        raise ValueError("the last dimension must be a multiple of 16")
+    x = x.to(torch.float32)
+    amax = float(x.abs().max())
+    gs = amax / (E2M1_MAX * E4M3_MAX) if amax > 0.0 else 1.0
+    xb = x.reshape(*x.shape[:-1], d // 16, 16)
+    sc = (xb.abs().amax(dim=-1) / (E2M1_MAX * gs)).to(torch.float8_e4m3fn)
+    den = (sc.to(torch.float32) * gs).unsqueeze(-1)
+    y = torch.where(den > 0, xb / torch.where(den > 0, den, torch.ones_like(den)), torch.zeros_like(xb))
+    mags = torch.tensor(E2M1_MAGNITUDES, dtype=torch.float32)
+    a = y.abs().clamp(max=E2M1_MAX)
+    dist = (a.unsqueeze(-1) - mags).abs()                 # [..., 16, 8]
+    best = dist.min(dim=-1, keepdim=True).values
+    idx = torch.arange(8)
+    # among the nearest magnitudes, the even code (mantissa bit 0) wins a tie
+    key = torch.where(dist == best, (idx % 2) * 8 + idx, torch.full_like(idx, 99))
+    code = key.argmin(dim=-1).to(torch.uint8)
+    code = code | ((y < 0).to(torch.uint8) << 3)
+    code = code.reshape(*x.shape[:-1], d)
+    packed = (code[..., 0::2] | (code[..., 1::2] << 4)).contiguous()
+    return packed, sc.view(torch.uint8).contiguous(), float(gs)
+
+
+def draw_nvfp4(B: int, H: int, F: int, N: int, dk: int, dv: int, seed: int,
+               s0_std: float = 0.0) -> dict:
+    """The draws of draw() with q, k and v quantized to NVFP4 (same generator
+    sequence)."""
+    q, k, v, alpha, beta, s0 = _draw_f32(B, H, F, N, dk, dv, seed, s0_std)
+    out = {"alpha": alpha, "beta": beta, "state_in": s0}
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        out[name + "4"], out[name + "_sf"], out[name + "_gs"] = quantize_nvfp4(t)
+    return out
+
+
 def workload_inputs(w: Workload) -> dict:
     """Inputs of a named workload, concatenated over its batch streams.
 

@@ -222,6 +222,60 @@ def frame_forward_fp8(q8, k8, v8, q_scale, k_scale, v_scale, alpha, beta, state_
     return frame_forward_f64(q, k, v, alpha, beta, state_in, B=B, H=H, F=F, N=N, dk=dk, dv=dv, **kw)
 
 
+def decode_e2m1(codes) -> np.ndarray:
+    """FP4 E2M1 codes (0..15, the low 4 bits of each value) -> fp64 values,
+    from the format's definition: bit 3 sign s, bits 2..1 exponent e (bias 1),
+    bit 0 mantissa m;
+        e == 0:     (-1)^s * (m / 2)                  (zero and the one subnormal)
+        otherwise:  (-1)^s * (1 + m / 2) * 2^(e - 1)
+    No infinities and no NaN (the largest magnitude is 6)."""
+    c = np.asarray(codes).astype(np.int64) & 15
+    s = (c >> 3) & 1
+    e = (c >> 1) & 3
+    m = c & 1
+    val = np.where(e == 0, m / 2.0, (1.0 + m / 2.0) * np.exp2(e.astype(np.float64) - 1.0))
+    return np.where(s == 1, -val, val)
+
+
+def _bytes(x) -> np.ndarray:
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            t = x.detach().cpu()
+            if t.dtype != torch.uint8:
+                t = t.view(torch.uint8)
+            return t.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(x, dtype=np.uint8)
+
+
+def decode_nvfp4(packed, scales, global_scale) -> np.ndarray:
+    """NVFP4 tensor -> fp64 values [..., d].
+
+    packed: uint8 [..., d/2], element 2i in the low nibble of byte i and element
+    2i+1 in the high nibble (E2M1 codes); scales: E4M3 codes [..., d/16], one
+    per 16 consecutive elements; global_scale: one fp32 per tensor.
+        x[..., i] = global_scale * e4m3(scales[..., i // 16]) * e2m1(code i)"""
+    p = _bytes(packed).astype(np.int64)
+    codes = np.stack([p & 15, p >> 4], axis=-1).reshape(*p.shape[:-1], 2 * p.shape[-1])
+    sc = decode_e4m3(_bytes(scales))
+    if sc.shape[-1] * 16 != codes.shape[-1]:
+        raise ValueError("one scale per 16 elements")
+    return decode_e2m1(codes) * np.repeat(sc, 16, axis=-1) * float(global_scale)
+
+
+def frame_forward_nvfp4(q4, k4, v4, q_sf, k_sf, v_sf, q_gs, k_gs, v_gs, alpha, beta, state_in=None, *,
+                        B, H, F, N, dk, dv, **kw):
+    """The forward on NVFP4 inputs: each of q, k, v decoded by decode_nvfp4
+    (E2M1 elements, E4M3 scales per 16 elements along the head dimension, one
+    fp32 scale per tensor), then exactly frame_forward_f64 on those values."""
+    q = None if q4 is None else decode_nvfp4(q4, q_sf, q_gs)
+    k = decode_nvfp4(k4, k_sf, k_gs)
+    v = decode_nvfp4(v4, v_sf, v_gs)
+    return frame_forward_f64(q, k, v, alpha, beta, state_in, B=B, H=H, F=F, N=N, dk=dk, dv=dv, **kw)
+
+
 def frame_forward_f64(q, k, v, alpha, beta, state_in=None, *, B, H, F, N, dk, dv,
                       want_out=True, want_states=False, sample_tokens=None,
                       mode=MODE_GDN, n_threads=0):

@@ -395,6 +395,77 @@ def test_fp8_forward_equals_bf16_forward_on_shared_values():
     np.testing.assert_array_equal(r8["state"], r16["state"])
 
 
+def test_e2m1_decoder_pins():
+    """The oracle's E2M1 decoder against what a binary floating-point format
+    with one sign bit, a 2-bit exponent of bias 1 and a 1-bit mantissa (no
+    infinities, no NaN) fixes: exponent field 1 is the binade [1, 2); each
+    binade holds two values, the second 1.5 times the first; each next binade
+    doubles; the subnormal step equals the first binade's step; the sign bit
+    only flips the sign.  Every value is also an exact E4M3 value (torch's
+    float8_e4m3fn conversion as the check)."""
+    v = oracle.decode_e2m1(np.arange(16))
+
+    def val(e, m):
+        return v[(e << 1) | m]
+    assert val(0, 0) == 0.0 and val(1, 0) == 1.0
+    for e in (1, 2, 3):
+        assert val(e, 1) == 1.5 * val(e, 0)
+    for e in (1, 2):
+        assert val(e + 1, 0) == 2.0 * val(e, 0)
+    assert val(0, 1) - val(0, 0) == (val(1, 1) - val(1, 0))
+    assert val(3, 1) == 6.0                       # (2 - 2^-1) * 2^(3 - 1): the largest magnitude
+    assert (np.diff(v[:8]) > 0).all()
+    np.testing.assert_array_equal(v[8:], -v[:8])
+    as_e4m3 = torch.from_numpy(v.copy()).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(as_e4m3, v)
+
+
+def test_nvfp4_layout_worked_example():
+    """A hand-decoded 32-element row: nibble order (element 2i low, 2i+1 high),
+    one E4M3 scale per 16 elements, the tensor scale on top."""
+    packed = np.zeros((1, 16), dtype=np.uint8)
+    packed[0, 0] = 0x21          # element 0: code 1 (0.5), element 1: code 2 (1.0)
+    packed[0, 7] = 0xF7          # element 14: code 7 (6.0), element 15: code 15 (-6.0)
+    packed[0, 8] = 0x9B          # element 16: code 11 (-1.5), element 17: code 9 (-0.5)
+    scales = np.array([[0x40, 0x30]], dtype=np.uint8)   # e4m3 2.0 for elements 0-15, 0.5 for 16-31
+    x = oracle.decode_nvfp4(packed, scales, 3.0)
+    want = np.zeros((1, 32))
+    want[0, 0], want[0, 1] = 0.5 * 2.0 * 3.0, 1.0 * 2.0 * 3.0
+    want[0, 14], want[0, 15] = 6.0 * 2.0 * 3.0, -6.0 * 2.0 * 3.0
+    want[0, 16], want[0, 17] = -1.5 * 0.5 * 3.0, -0.5 * 0.5 * 3.0
+    np.testing.assert_array_equal(x, want)
+
+
+def test_nvfp4_quantizer_picks_the_nearest_value():
+    """Brute force over all 15 E2M1 values of each element's block: the input
+    generator's codes are nearest to x / (tensor scale * block scale)."""
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn((4, 3, 64), generator=g) * torch.tensor([0.01, 1.0, 30.0]).view(1, 3, 1)
+    packed, sc, gs = inputs.quantize_nvfp4(x)
+    xd = oracle.decode_nvfp4(packed, sc, gs)
+    s = np.repeat(oracle.decode_e4m3(sc.numpy()), 16, axis=-1) * gs
+    cand = oracle.decode_e2m1(np.arange(16))[None, None, None, :] * s[..., None]   # [..., 64, 16]
+    best = np.abs(cand - x.double().numpy()[..., None]).min(axis=-1)
+    np.testing.assert_allclose(np.abs(xd - x.double().numpy()), best, rtol=0, atol=1e-12)
+    # the block scale never clips: every |x| fits under 6 * block scale (to E4M3 rounding)
+    assert (np.abs(x.double().numpy()) <= 6.0 * s * (1 + 2.0 ** -3) + 1e-30).all()
+
+
+def test_nvfp4_forward_is_the_f64_forward_on_decoded_values():
+    B, H, F, N, dk, dv = 1, 2, 2, 5, 16, 32
+    x = inputs.draw_nvfp4(B, H, F, N, dk, dv, seed=9, s0_std=0.1)
+    r4 = oracle.frame_forward_nvfp4(x["q4"], x["k4"], x["v4"], x["q_sf"], x["k_sf"], x["v_sf"],
+                                    x["q_gs"], x["k_gs"], x["v_gs"], x["alpha"], x["beta"], x["state_in"],
+                                    B=B, H=H, F=F, N=N, dk=dk, dv=dv)
+    dec = {n: oracle.decode_nvfp4(x[n + "4"], x[n + "_sf"], x[n + "_gs"]) for n in ("q", "k", "v")}
+    r64 = oracle.frame_forward_f64(dec["q"], dec["k"], dec["v"], x["alpha"].double().numpy(),
+                                   x["beta"].double().numpy(), x["state_in"].double().numpy(),
+                                   B=B, H=H, F=F, N=N, dk=dk, dv=dv)
+    np.testing.assert_array_equal(r4["out"], r64["out"])
+    np.testing.assert_array_equal(r4["state"], r64["state"])
+    assert dec["k"].shape == (B, F, N, H, dk) and dec["v"].shape == (B, F, N, H, dv)
+
+
 def _f64_problem(B, H, F, N, dk, dv, seed):
     g = np.random.default_rng(seed)
     x = {"q": g.standard_normal((B, F, N, H, dk)), "k": g.standard_normal((B, F, N, H, dk)) * 0.5,
