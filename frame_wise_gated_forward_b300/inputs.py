@@ -214,3 +214,53 @@ def draw_raw(B: int, H: int, F: int, N: int, dk: int, dv: int, seed: int,
         s0 = torch.zeros((B, H, dv, dk))
     return {"q": q, "k": k, "v": v, "a_logit": a.contiguous(), "b_logit": b.contiguous(),
             "state_in": s0.contiguous()}
+
+
+def draw_delta(B: int, H: int, F: int, N: int, dk: int, dv: int, seed: int,
+               s0_std: float = 0.0, keys: str = "shared", mass=(0.5, 0.95),
+               noise: float = 0.3) -> dict:
+    """Inputs in the regime where the delta-rule correction dominates the
+    update (SANA-WM article, "The Architecture": the state is corrected by a
+    delta rule, not only accumulated): |K_f^T B_f K_f| is close to 1 in every
+    frame, so S (I - A_f) differs from S by a large term instead of the ~0.4 %
+    of the spec's beta = sigmoid(x)/N workloads.
+
+    keys = "shared": per (b, f, h) one unit direction u; token keys
+        k_n = normalize(u + noise * g_n / sqrt(dk)), g_n ~ N(0, I), so the
+        keys of a frame are strongly correlated; beta_n = m * w_n / sum(w)
+        with w_n = sigmoid(N(0, 1)) and m ~ U(mass) per (b, f, h), i.e.
+        sum_n beta_n |k_n|^2 = m before the bf16 rounding of k.
+    keys = "orthonormal" (needs N <= dk): the keys of a frame are the first N
+        rows of a random orthogonal matrix and beta_n ~ U(0.5, 1), so A_f has
+        eigenvalues beta_n up to 1 (a near-projection: exact delta writes).
+    q ~ N(0, 1) L2-normalised, v ~ N(0, 1), alpha as in draw(); q, k, v rounded
+    to bf16.  Input preparation only: no arithmetic of the method."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = torch.nn.functional.normalize(torch.randn((B, F, N, H, dk), generator=g), dim=-1)
+    v = torch.randn((B, F, N, H, dv), generator=g)
+    araw = torch.randn((B, F, H), generator=g)
+    alpha = torch.exp(-torch.nn.functional.softplus(araw) * 0.05)
+    if keys == "shared":
+        u = torch.nn.functional.normalize(torch.randn((B, F, 1, H, dk), generator=g), dim=-1)
+        gk = torch.randn((B, F, N, H, dk), generator=g)
+        k = torch.nn.functional.normalize(u + noise * gk / float(dk) ** 0.5, dim=-1)
+        w = torch.sigmoid(torch.randn((B, F, N, H), generator=g))
+        m = mass[0] + (mass[1] - mass[0]) * torch.rand((B, F, 1, H), generator=g)
+        beta = m * w / w.sum(dim=2, keepdim=True)
+    elif keys == "orthonormal":
+        if N > dk:
+            raise ValueError("orthonormal keys need N <= dk")
+        z = torch.randn((B, F, H, dk, dk), generator=g, dtype=torch.float64)
+        qm, _ = torch.linalg.qr(z)                          # columns orthonormal
+        k = qm.transpose(-1, -2)[..., :N, :].permute(0, 1, 3, 2, 4).to(torch.float32)   # [B, F, N, H, dk]
+        beta = 0.5 + 0.5 * torch.rand((B, F, N, H), generator=g)
+    else:
+        raise ValueError(f"unknown key mode {keys!r}")
+    if s0_std > 0.0:
+        s0 = torch.randn((B, H, dv, dk), generator=g) * s0_std
+    else:
+        s0 = torch.zeros((B, H, dv, dk))
+    return {"q": q.to(torch.bfloat16).contiguous(), "k": k.to(torch.bfloat16).contiguous(),
+            "v": v.to(torch.bfloat16).contiguous(), "alpha": alpha.contiguous(),
+            "beta": beta.to(torch.float32).contiguous(), "state_in": s0.contiguous()}
