@@ -988,6 +988,12 @@ extern "C" {
 size_t gdn_workspace_bytes(int B, int H, int F, int N, int dk, int dv) {
     if (B < 1 || H < 1 || F < 1 || N < 1 || !dim_ok(dk) || !dim_ok(dv)) return 0;
     const long long items = static_cast<long long>(B) * F * H;
+    // on a usable device: exactly the plan a call would launch; otherwise the
+    // plan with splitting allowed (an upper bound)
+    int dev;
+    DeviceState* ds;
+    if (device_ready(&dev, &ds) == GDN_OK)
+        return layout_of(items, dk, dv, plan_split(items, chunks_of(N), ds->sms, ds->coop_k1)).total;
     return layout_of(items, dk, dv, plan_split(items, chunks_of(N), current_sms(), true)).total;
 }
 
@@ -1110,6 +1116,11 @@ extern "C" gdn_status gdn_frame_step_noalloc(const void* q, const void* k, const
     DeviceState* ds;
     st = device_ready(&dev, &ds);
     if (st != GDN_OK) return st;
+    // the array's device address, looked up on the first call on this device
+    // whichever step path the call takes
+    uint8_t* ws = nullptr;
+    st = step_scratch_address(dev, &ws);
+    if (st != GDN_OK) return st;
     const PassArgs a{q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv};
     if (fused_step_applies(a)) {  // the one-launch step keeps everything on chip: no scratch at all
         if (!all_device(a)) return GDN_ERR_NULL_PTR;
@@ -1120,8 +1131,5 @@ extern "C" gdn_status gdn_frame_step_noalloc(const void* q, const void* k, const
     const Layout L = layout_of(items, dk, dv, sp);
     if (L.total > kStepScratchBytes) return GDN_ERR_TOO_LARGE;
     if (!all_device(a)) return GDN_ERR_NULL_PTR;
-    uint8_t* ws = nullptr;
-    st = step_scratch_address(dev, &ws);
-    if (st != GDN_OK) return st;
     return launch_phases(a, ws, L, sp, ds, reinterpret_cast<cudaStream_t>(stream_handle), nullptr);
 }

@@ -233,10 +233,14 @@ gdn_status gdn_frame_forward_host(const void* q, const void* k, const void* v,
                                   gdn_stream_t stream);
 
 /* Bytes of library workspace one gdn_frame_forward call of this shape takes
- * (0 for invalid shapes). */
+ * on the current device (0 for invalid shapes; with no usable device, an
+ * upper bound). */
 size_t gdn_workspace_bytes(int B, int H, int F, int N, int dk, int dv);
 
-/* Bytes of library workspace one gdn_frame_step call of this shape takes. */
+/* Bytes of library workspace one gdn_frame_step call of this shape takes on
+ * the three-phase step path (gdn_set_fused_step(0)), computed with the work
+ * plan that call would launch on the current device (with no usable device:
+ * an upper bound). */
 size_t gdn_step_workspace_bytes(int B, int H, int N, int dk, int dv);
 
 /* Static, human-readable name of a status code. */
@@ -332,16 +336,20 @@ const char* gdn_version(void);
  * holds it until the process exits.  No call allocates or frees memory.
  *   - With the one-launch step on (gdn_set_fused_step, the default) the call
  *     uses no scratch at all.  Otherwise it uses the array: a shape whose
- *     workspace (gdn_step_workspace_bytes) exceeds it returns
- *     GDN_ERR_TOO_LARGE before anything is launched.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture starts.
+ *     workspace (gdn_step_workspace_bytes, the same work plan) exceeds it
+ *     returns GDN_ERR_TOO_LARGE before anything is launched.
+ *   - The first call on each device, whichever step path it takes, looks up
+ *     the array's device address (cudaGetSymbolAddress) with that device
+ *     current; make that first call before any stream capture starts.
  *   - All calls on a device share the one array and it keeps the last call's
- *     contents; each call writes every scratch byte it reads before reading
- *     it, so nothing needs clearing.  Calls that may overlap on the GPU
- *     (different streams, or unordered host threads) race on the array:
- *     order them, for example by issuing them on one stream.
+ *     contents; each call clears the counters it uses with a stream-ordered
+ *     memset and writes every other scratch byte before reading it.  Calls
+ *     that may overlap on the GPU (different streams, or unordered host
+ *     threads) race on the array: order them, for example by issuing them on
+ *     one stream.
+ *   - The looked-up address (like the library's other per-device state) is
+ *     kept for the life of the process: resetting a device
+ *     (cudaDeviceReset) while the library is loaded is not supported.
  */
 #define GDN_STEP_NOALLOC_SCRATCH_BYTES (32u << 20)
 gdn_status gdn_frame_step_noalloc(const void* q, const void* k, const void* v,
