@@ -11,7 +11,8 @@ HBM).  Prints ONE JSON line (rank 0):
   e2e         the same metric through gdn_frame_forward_host on pinned host
               buffers, host<->device copies inside the timed region
   cpu_baseline  the fp64 CPU oracle on the host cores (rank 0, N=1 only)
-  clocks      nvidia-smi samples taken during the timed region
+  clocks      NVML samples (SM clock, throttle reasons) taken during the
+              timed region
 
 --impl reference times the fp64 CPU oracle on the same workload instead
 (a bounded sample of frames per step).
@@ -65,7 +66,16 @@ def load_peaks():
 
 
 def kernel_costs(w):
-    """Algorithmic bytes and FLOPs of one launch of each phase."""
+    """Bytes and FLOPs of one launch of each kernel of the forward.
+
+    "bytes" are the algorithmic bytes: what the layer itself must move for the
+    part of the work the kernel does (q, k, v, beta and alpha read, out
+    written, the initial and final state), 16,468 B per token at H = 16,
+    d = 128 over the whole path.  The per-frame workspace that a multi-launch
+    schedule adds (A_f, U_f written by the contraction and read back, the bf16
+    per-frame states) is reported apart as "overhead_bytes": it is a cost of
+    the schedule, not work of the layer.
+    """
     T = w.B * w.F * w.N            # tokens
     items = w.B * w.F * w.H        # (b, f, h) items
     dk, dv, H = w.dk, w.dv, w.H
@@ -73,19 +83,23 @@ def kernel_costs(w):
     ws_u = items * dv * dk * 4     # U_f fp32
     ws_s = items * dv * dk * 2     # S_f bf16
     state = w.B * H * dv * dk * 4
+    alpha = w.B * w.F * H * 4
+    kvb = T * H * (dk + dv) * 2 + T * H * 4        # k, v, beta
+    qo = T * H * dk * 2 + T * H * dv * 2           # q in, out
+    f_contract = 2 * T * H * dk * (dk + dv)
+    f_scan = 2 * items * dv * dk * dk
+    f_out = 2 * T * H * dk * dv
     return {
-        "k1_contract": {"bytes": T * H * (dk + dv) * 2 + T * H * 4 + ws_a + ws_u,
-                        "flops": 2 * T * H * dk * (dk + dv)},
-        "k2_scan": {"bytes": ws_a + ws_u + ws_s + w.B * w.F * H * 4 + 2 * state,
-                    "flops": 2 * items * dv * dk * dk},
-        "k3_output": {"bytes": T * H * dk * 2 + ws_s + T * H * dv * 2,
-                      "flops": 2 * T * H * dk * dv},
-        # scan and output pass fused into one launch: the per-frame states stay
-        # inside the kernel (published through L2), so only A, U, q, alpha,
-        # the states in/out and out count
-        "k23_scan_output": {"bytes": ws_a + ws_u + w.B * w.F * H * 4 + 2 * state + T * H * dk * 2
-                            + T * H * dv * 2,
-                            "flops": 2 * items * dv * dk * dk + 2 * T * H * dk * dv},
+        "k1_contract": {"bytes": kvb, "overhead_bytes": ws_a + ws_u, "flops": f_contract},
+        "k2_scan": {"bytes": alpha + 2 * state, "overhead_bytes": ws_a + ws_u + ws_s, "flops": f_scan},
+        "k3_output": {"bytes": qo, "overhead_bytes": ws_s, "flops": f_out},
+        # scan and output pass in one launch: the per-frame states stay on
+        # chip / in L2; A_f and U_f are read back from the workspace
+        "k23_scan_output": {"bytes": qo + alpha + 2 * state, "overhead_bytes": ws_a + ws_u,
+                            "flops": f_scan + f_out},
+        # the whole pass in one launch: every byte is compulsory
+        "fwd_single_pass": {"bytes": kvb + qo + alpha + 2 * state, "overhead_bytes": 0,
+                            "flops": f_contract + f_scan + f_out},
     }
 
 
@@ -137,35 +151,86 @@ def ncu_traffic(kernel):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock, max clock, power and throttle reasons."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock, max clock, power and throttle reasons of one GPU, polled
+    through NVML (read-only queries) about every millisecond in a background
+    thread, so that even a timed region of a few milliseconds holds samples.
+    Falls back to nvidia-smi at 100 ms when NVML is missing."""
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, gpu_index):
-        self.gpu_index = gpu_index
-        self.samples = []
-        self.proc = None
+    def __init__(self, gpu_index, pci_bus_id=None):
+        self.pci_bus_id = pci_bus_id
+        self.error = None
+        g = str(gpu_index).strip()
+        self.uuid = g if g.startswith(("GPU-", "MIG-")) else None   # CUDA_VISIBLE_DEVICES may hold UUIDs
+        self.gpu_index = int(g) if g.isdigit() else 0
+        self.samples = []          # (time, sm_mhz, max_mhz, power_w, set of reasons)
+        self._stop = threading.Event()
         self.thread = None
+        self.proc = None
+        self.source = None
 
     def start(self):
         try:
+            import pynvml
+            pynvml.nvmlInit()
+            h = None
+            if self.pci_bus_id is not None:   # the CUDA device's own PCI address: unambiguous
+                try:
+                    h = pynvml.nvmlDeviceGetHandleByPciBusId(self.pci_bus_id)
+                except pynvml.NVMLError:
+                    h = None
+            if h is None and self.uuid is not None:
+                h = pynvml.nvmlDeviceGetHandleByUUID(self.uuid)
+            if h is None:
+                h = pynvml.nvmlDeviceGetHandleByIndex(self.gpu_index)
+            bits = {"hw_slowdown": pynvml.nvmlClocksEventReasonHwSlowdown,
+                    "hw_thermal_slowdown": pynvml.nvmlClocksEventReasonHwThermalSlowdown,
+                    "sw_thermal_slowdown": pynvml.nvmlClocksEventReasonSwThermalSlowdown,
+                    "sw_power_cap": pynvml.nvmlClocksEventReasonSwPowerCap}
+            mx = float(pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM))
+
+            def poll():
+                while not self._stop.is_set():
+                    try:
+                        sm = float(pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM))
+                        r = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
+                        pw = pynvml.nvmlDeviceGetPowerUsage(h) / 1000.0
+                    except pynvml.NVMLError:
+                        break
+                    self.samples.append((time.perf_counter(), sm, mx, pw,
+                                         {n for n, b in bits.items() if r & b}))
+                    time.sleep(0.0005)
+            self.source = "nvml, ~1 ms"
+            self.thread = threading.Thread(target=poll, daemon=True)
+            self.thread.start()
+            return
+        except Exception as e:  # NVML unavailable: nvidia-smi every 100 ms
+            self.error = f"{type(e).__name__}: {e}"
+        fields = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
+        try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                ["nvidia-smi", f"--query-gpu={fields}", "--format=csv,noheader,nounits", "-lms", "100",
                  "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
-            self.proc = None
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.source = "nvidia-smi, 100 ms"
+
+        def read():
+            for line in self.proc.stdout:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) == 7:
+                    try:
+                        self.samples.append((time.perf_counter(), float(p[0]), float(p[1]), float(p[2]),
+                                             {n for n, x in zip(self.NAMES, p[3:]) if x.lower() == "active"}))
+                    except ValueError:
+                        pass
+        self.thread = threading.Thread(target=read, daemon=True)
         self.thread.start()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) == 9:
-                self.samples.append((time.perf_counter(), parts))
-
     def stop(self):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -176,24 +241,17 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self, t0, t1):
-        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
-        used = inside if inside else [p for (t, p) in self.samples]
-        if not used:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-        sm = [num(p[1]) for p in used if num(p[1]) is not None]
-        mx = [num(p[2]) for p in used if num(p[2]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for p in used for i in range(4) if p[5 + i].lower() == "active"})
-        pw = [num(p[3]) for p in used if num(p[3]) is not None]
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(used), "samples_in_region": len(inside),
-                "power_w_max": max(pw) if pw else None}
+        """Samples taken inside [t0, t1] only; says so when there are none."""
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:
+            r = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples_in_region": 0,
+                 "source": self.source, "note": "no clock sample fell inside the timed region"}
+            if self.error:
+                r["nvml_error"] = self.error
+            return r
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": sorted(set().union(*(s[4] for s in inside))), "samples_in_region": len(inside),
+                "power_w_max": max(s[3] for s in inside), "source": self.source}
 
 
 def cpu_baseline_run(w, x, frames):
@@ -238,7 +296,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": workload_desc(w), "tokens_per_step_per_gpu": w.B * w.F * w.N,
+        "data": "synthetic", "config": {"workload": workload_desc(w), "tokens_per_step_per_gpu": tokens,
                                         "sample": sample},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -283,7 +341,11 @@ def main():
 
     # ---------------------------------------------------------------- timed region
     cvd = [c for c in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if c.strip()]
-    sampler = ClockSampler(cvd[local_rank].strip() if local_rank < len(cvd) else local_rank)
+    props = torch.cuda.get_device_properties(device)
+    pci = None
+    if hasattr(props, "pci_bus_id"):
+        pci = f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:{getattr(props, 'pci_device_id', 0):02X}.0"
+    sampler = ClockSampler(cvd[local_rank].strip() if local_rank < len(cvd) else local_rank, pci)
     sampler.start()
     time.sleep(0.3)
     torch.cuda.synchronize(device)
@@ -331,6 +393,7 @@ def main():
     for n in names:
         t = phase_ms[n] / 1e3
         phases[n] = {"ms": phase_ms[n], "GB/s": costs[n]["bytes"] / t / 1e9,
+                     "overhead_bytes": costs[n]["overhead_bytes"],
                      "hbm_frac": costs[n]["bytes"] / t / 1e9 / peaks["hbm_gbs"],
                      "TFLOP/s": costs[n]["flops"] / t / 1e12,
                      "tensor_frac": costs[n]["flops"] / t / 1e12 / peaks["bf16_tflops"]}
@@ -338,7 +401,8 @@ def main():
     achieved = costs[dom]["bytes"] / (phase_ms[dom] / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(dom), "kernel": dom,
-                "peak_source": peaks["source"], "algorithmic_bytes": costs[dom]["bytes"]}
+                "peak_source": peaks["source"], "algorithmic_bytes": costs[dom]["bytes"],
+                "overhead_bytes": costs[dom]["overhead_bytes"]}
     ms_per_step = sec_max / args.steps * 1e3
     floor_ms = path_floor_bytes(w) / (peaks["hbm_gbs"] * 1e9) * 1e3
 
