@@ -150,18 +150,54 @@ def ncu_traffic(kernel):
     return None if k is None else k.get("dram_bytes_per_launch")
 
 
+class _Nvml:
+    """The few read-only NVML queries the clock sampler needs, through ctypes
+    on the driver's libnvidia-ml (no Python NVML package required)."""
+    SM = 1              # NVML_CLOCK_SM
+    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+               "sw_power_cap": 0x4}
+
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+
+    def handle(self, pci_bus_id=None, index=0):
+        ct = self.ct
+        h = ct.c_void_p()
+        if pci_bus_id is not None and self.lib.nvmlDeviceGetHandleByPciBusId_v2(
+                ct.c_char_p(pci_bus_id.encode()), ct.byref(h)) == 0:
+            return h
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ct.c_uint(index), ct.byref(h)) != 0:
+            raise RuntimeError("no NVML handle")
+        return h
+
+    def sample(self, h):
+        ct = self.ct
+        sm, mx, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if (self.lib.nvmlDeviceGetClockInfo(h, self.SM, ct.byref(sm)) != 0
+                or self.lib.nvmlDeviceGetMaxClockInfo(h, self.SM, ct.byref(mx)) != 0
+                or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons(h, ct.byref(rs)) != 0):
+            return None
+        if self.lib.nvmlDeviceGetPowerUsage(h, ct.byref(pw)) != 0:
+            pw.value = 0
+        return (float(sm.value), float(mx.value), pw.value / 1000.0,
+                {n for n, b in self.REASONS.items() if rs.value & b})
+
+
 class ClockSampler:
     """SM clock, max clock, power and throttle reasons of one GPU, polled
     through NVML (read-only queries) about every millisecond in a background
     thread, so that even a timed region of a few milliseconds holds samples.
-    Falls back to nvidia-smi at 100 ms when NVML is missing."""
+    Falls back to nvidia-smi at 100 ms when NVML cannot be loaded."""
     NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index, pci_bus_id=None):
         self.pci_bus_id = pci_bus_id
         self.error = None
         g = str(gpu_index).strip()
-        self.uuid = g if g.startswith(("GPU-", "MIG-")) else None   # CUDA_VISIBLE_DEVICES may hold UUIDs
         self.gpu_index = int(g) if g.isdigit() else 0
         self.samples = []          # (time, sm_mhz, max_mhz, power_w, set of reasons)
         self._stop = threading.Event()
@@ -171,34 +207,15 @@ class ClockSampler:
 
     def start(self):
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            h = None
-            if self.pci_bus_id is not None:   # the CUDA device's own PCI address: unambiguous
-                try:
-                    h = pynvml.nvmlDeviceGetHandleByPciBusId(self.pci_bus_id)
-                except pynvml.NVMLError:
-                    h = None
-            if h is None and self.uuid is not None:
-                h = pynvml.nvmlDeviceGetHandleByUUID(self.uuid)
-            if h is None:
-                h = pynvml.nvmlDeviceGetHandleByIndex(self.gpu_index)
-            bits = {"hw_slowdown": pynvml.nvmlClocksEventReasonHwSlowdown,
-                    "hw_thermal_slowdown": pynvml.nvmlClocksEventReasonHwThermalSlowdown,
-                    "sw_thermal_slowdown": pynvml.nvmlClocksEventReasonSwThermalSlowdown,
-                    "sw_power_cap": pynvml.nvmlClocksEventReasonSwPowerCap}
-            mx = float(pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM))
+            nv = _Nvml()
+            h = nv.handle(self.pci_bus_id, self.gpu_index)
 
             def poll():
                 while not self._stop.is_set():
-                    try:
-                        sm = float(pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM))
-                        r = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
-                        pw = pynvml.nvmlDeviceGetPowerUsage(h) / 1000.0
-                    except pynvml.NVMLError:
+                    s = nv.sample(h)
+                    if s is None:
                         break
-                    self.samples.append((time.perf_counter(), sm, mx, pw,
-                                         {n for n, b in bits.items() if r & b}))
+                    self.samples.append((time.perf_counter(),) + s)
                     time.sleep(0.0005)
             self.source = "nvml, ~1 ms"
             self.thread = threading.Thread(target=poll, daemon=True)
@@ -381,14 +398,14 @@ def main():
         api.frame_forward_timed(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], s_in, out, st, evs[i])
     torch.cuda.synchronize(device)
     api.sync_status()
+    fsched = api.forward_schedule(w.B, w.H, w.F, w.N, w.dk, w.dv)
     sched = api.scan_schedule(w.B, w.H, w.dv)
-    names = ["k1_contract", "k2_scan", "k3_output"] if sched <= 0 else ["k1_contract", "flags_reset",
-                                                                        "k23_scan_output"]
+    names = {2: ["counters_reset", "none", "fwd_single_pass"],
+             1: ["k1_contract", "flags_reset", "k23_scan_output"]}.get(fsched, ["k1_contract", "k2_scan", "k3_output"])
     phase_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(nk))
                 for j, n in enumerate(names)}
-    if sched > 0:
-        names = ["k1_contract", "k23_scan_output"]
     costs = kernel_costs(w)
+    names = [n for n in names if n in costs]
     phases = {}
     for n in names:
         t = phase_ms[n] / 1e3
@@ -406,10 +423,28 @@ def main():
     ms_per_step = sec_max / args.steps * 1e3
     floor_ms = path_floor_bytes(w) / (peaks["hbm_gbs"] * 1e9) * 1e3
 
-    # ------------------------------------- reverse direction (bidirectional stage)
+    # ------------------------ the same pass in the multi-launch schedule (context)
     nr = min(args.steps, 100)
     r0 = torch.cuda.Event(enable_timing=True)
     r1 = torch.cuda.Event(enable_timing=True)
+    api.set_single_pass(False)
+    try:
+        step()
+        torch.cuda.synchronize(device)
+        r0.record(stream)
+        for _ in range(nr):
+            step()
+        r1.record(stream)
+        torch.cuda.synchronize(device)
+        api.sync_status()
+    finally:
+        api.set_single_pass(True)
+    multi_ms = r0.elapsed_time(r1) / nr
+    multi_info = {"ms_per_step": multi_ms, "tokens_per_s": tokens / (multi_ms / 1e3), "steps": nr,
+                  "what": "phase 1, then scan and output in one cooperative launch (A_f, U_f and the "
+                          "per-frame states through HBM)"}
+
+    # ------------------------------------- reverse direction (bidirectional stage)
     api.frame_forward(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], s_in, out=out, state_out=st, reverse=True)
     torch.cuda.synchronize(device)
     r0.record(stream)
@@ -461,6 +496,31 @@ def main():
                 "what": "q, k, v as per-tensor-scaled OCP FP8 E4M3 (1 byte each), decoded in shared memory; "
                         "out bf16, state fp32"}
     del x8
+
+    # ---------------------------------------------------------- NVFP4 inputs
+    x4 = {k: (v.to(device) if torch.is_tensor(v) else v)
+          for k, v in inputs.draw_nvfp4(w.B, w.H, w.F, w.N, w.dk, w.dv, seed=0).items()}
+
+    def step4():
+        api.frame_forward_nvfp4(x4["q4"], x4["k4"], x4["v4"], x4["q_sf"], x4["k_sf"], x4["v_sf"], x4["q_gs"],
+                                x4["k_gs"], x4["v_gs"], x4["alpha"], x4["beta"], None, out=out, state_out=st)
+    step4()
+    torch.cuda.synchronize(device)
+    r0.record(stream)
+    for _ in range(nr):
+        step4()
+    r1.record(stream)
+    torch.cuda.synchronize(device)
+    api.sync_status()
+    fp4_ms = r0.elapsed_time(r1) / nr
+    T = w.B * w.F * w.N
+    fp4_floor_ms = (T * w.H * (2 * w.dk + w.dv) * (0.5 + 1.0 / 16) + T * w.H * w.dv * 2 + T * w.H * 4
+                    + w.B * w.F * w.H * 4 + w.B * w.H * w.dv * w.dk * 4) / (peaks["hbm_gbs"] * 1e9) * 1e3
+    fp4_info = {"ms_per_step": fp4_ms, "tokens_per_s": tokens / (fp4_ms / 1e3), "steps": nr,
+                "path_floor_ms": fp4_floor_ms, "path_frac": fp4_floor_ms / fp4_ms,
+                "what": "q, k, v as NVFP4 (E2M1 codes, E4M3 scale per 16, fp32 scale per tensor), decoded in "
+                        "shared memory; out bf16, state fp32"}
+    del x4
 
     # ------------------------------------------------------- backward (training)
     g = torch.Generator().manual_seed(1)
@@ -546,22 +606,26 @@ def main():
                        "tokens_per_step_per_gpu": tokens,
                        "l2": "inputs 1.31 GB per step > 126 MB L2; no flush",
                        "parallelism": f"replicas x{world} (no data-path collective)",
-                       "scan_schedule": (f"fused scan+output, {sched} state rows per scan CTA" if sched > 0
-                                         else f"separate scan ({-sched} rows per CTA) and output launches")},
+                       "schedule": ("single pass: contraction, scan (one CTA per head) and output in one "
+                                    "cooperative launch, L2-resident rings" if fsched == 2 else
+                                    f"phase 1, then fused scan+output ({sched} state rows per scan CTA)" if fsched == 1
+                                    else f"three launches ({-sched} state rows per scan CTA)")},
             "roofline": roofline,
             "phases": phases,
             "path_roofline": {"floor_ms": floor_ms, "frac": floor_ms / ms_per_step,
                               "ceiling_tokens_per_s": tokens / (floor_ms / 1e3) * world},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": args.e2e_steps},
+            "multi_launch_schedule": multi_info,
             "step": step_info,
             "reverse_direction": reverse_info,
             "gated_prologue": gated_info,
             "fp8_inputs": fp8_info,
+            "nvfp4_inputs": fp4_info,
             "backward": backward_info,
             "cpu_baseline": cpu,
             "clocks": clocks,
-            "gpu_launches": (3 if sched <= 0 else 2) * args.steps,
+            "gpu_launches": {2: 1, 1: 2}.get(fsched, 3) * args.steps,
         }
         print(json.dumps(line), flush=True)
     replicas.shutdown()

@@ -25,7 +25,8 @@ EXPORTS = (
     "gdn_status_string", "gdn_sync_status", "gdn_set_wait_limit_ns", "gdn_selftest_wait_timeout",
     "gdn_version", "gdn_frame_step_noalloc", "gdn_set_fused_scan", "gdn_scan_schedule",
     "gdn_set_contract_split", "gdn_frame_forward_fp8", "gdn_frame_step_fp8", "gdn_frame_backward",
-    "gdn_set_fused_step",
+    "gdn_set_fused_step", "gdn_set_single_pass", "gdn_forward_schedule", "gdn_debug_last_timeout",
+    "gdn_frame_forward_nvfp4", "gdn_frame_step_nvfp4",
 )
 
 
@@ -62,6 +63,11 @@ def load(path: str | None = None):
     lib.gdn_frame_forward_fp8.restype = ctypes.c_int
     lib.gdn_frame_step_fp8.argtypes = [vp, vp, vp, fl, fl, fl, fp, fp, fp, vp, fp, i, i, i, i, i, st]
     lib.gdn_frame_step_fp8.restype = ctypes.c_int
+    lib.gdn_frame_forward_nvfp4.argtypes = [vp, vp, vp, vp, vp, vp, fl, fl, fl, fp, fp, fp, vp, fp,
+                                            i, i, i, i, i, i, st]
+    lib.gdn_frame_forward_nvfp4.restype = ctypes.c_int
+    lib.gdn_frame_step_nvfp4.argtypes = [vp, vp, vp, vp, vp, vp, fl, fl, fl, fp, fp, fp, vp, fp, i, i, i, i, i, st]
+    lib.gdn_frame_step_nvfp4.restype = ctypes.c_int
     lib.gdn_frame_backward.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, vp, vp, vp, fp, fp, fp,
                                        i, i, i, i, i, i, st]
     lib.gdn_frame_backward.restype = ctypes.c_int
@@ -92,8 +98,14 @@ def load(path: str | None = None):
     lib.gdn_set_fused_step.restype = None
     lib.gdn_set_contract_split.argtypes = [ctypes.c_int]
     lib.gdn_set_contract_split.restype = None
+    lib.gdn_set_single_pass.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.gdn_set_single_pass.restype = None
+    lib.gdn_forward_schedule.argtypes = [i] * 6
+    lib.gdn_forward_schedule.restype = ctypes.c_int
     lib.gdn_scan_schedule.argtypes = [i, i, i]
     lib.gdn_scan_schedule.restype = ctypes.c_int
+    lib.gdn_debug_last_timeout.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.gdn_debug_last_timeout.restype = ctypes.c_int
     lib.gdn_version.argtypes = []
     lib.gdn_version.restype = ctypes.c_char_p
     if path is None:

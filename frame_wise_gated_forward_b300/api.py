@@ -209,6 +209,66 @@ def frame_step_fp8(q, k, v, q_scale, k_scale, v_scale, alpha, beta, state_in=Non
     return out, state_out
 
 
+def frame_forward_nvfp4(q4, k4, v4, q_sf, k_sf, v_sf, q_gs, k_gs, v_gs, alpha, beta, state_in=None, *,
+                        out=None, state_out=None, stream=None):
+    """Forward on NVFP4 inputs: q4, k4 uint8 [B,F,N,H,dk/2] and v4 [B,F,N,H,dv/2]
+    (two E2M1 codes per byte, lower-indexed element in the low nibble), block
+    scales q_sf, k_sf uint8 [B,F,N,H,dk/16] and v_sf [B,F,N,H,dv/16] (E4M3),
+    per-tensor fp32 scales q_gs, k_gs, v_gs.  dk, dv in {64, 128}."""
+    lib = load()
+    B, F, N, H, hk = q4.shape
+    dk, dv = 2 * hk, 2 * v4.shape[-1]
+    if out is None:
+        out = torch.empty((B, F, N, H, dv), dtype=torch.bfloat16, device=q4.device)
+    if state_out is None:
+        state_out = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q4.device)
+    args = [
+        _dev(q4, "q4", torch.uint8, (B, F, N, H, dk // 2)),
+        _dev(k4, "k4", torch.uint8, (B, F, N, H, dk // 2)),
+        _dev(v4, "v4", torch.uint8, (B, F, N, H, dv // 2)),
+        _dev(q_sf, "q_sf", torch.uint8, (B, F, N, H, dk // 16)),
+        _dev(k_sf, "k_sf", torch.uint8, (B, F, N, H, dk // 16)),
+        _dev(v_sf, "v_sf", torch.uint8, (B, F, N, H, dv // 16)),
+        float(q_gs), float(k_gs), float(v_gs),
+        _dev(alpha, "alpha", torch.float32, (B, F, H)),
+        _dev(beta, "beta", torch.float32, (B, F, N, H)),
+        None if state_in is None else _dev(state_in, "state_in", torch.float32, (B, H, dv, dk)),
+        _dev(out, "out", torch.bfloat16, (B, F, N, H, dv)),
+        _dev(state_out, "state_out", torch.float32, (B, H, dv, dk)),
+    ]
+    check(lib.gdn_frame_forward_nvfp4(*args, B, H, F, N, dk, dv, _stream_handle(stream)), "gdn_frame_forward_nvfp4")
+    return out, state_out
+
+
+def frame_step_nvfp4(q4, k4, v4, q_sf, k_sf, v_sf, q_gs, k_gs, v_gs, alpha, beta, state_in=None, *, out=None,
+                     state_out=None, stream=None):
+    """One frame on a resident state with NVFP4 inputs (see frame_forward_nvfp4).
+    q4, k4 [B,N,H,dk/2]; v4 [B,N,H,dv/2]; scales [B,N,H,d/16]; alpha [B,H]; beta [B,N,H]."""
+    lib = load()
+    B, N, H, hk = q4.shape
+    dk, dv = 2 * hk, 2 * v4.shape[-1]
+    if out is None:
+        out = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=q4.device)
+    if state_out is None:
+        state_out = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q4.device)
+    args = [
+        _dev(q4, "q4", torch.uint8, (B, N, H, dk // 2)),
+        _dev(k4, "k4", torch.uint8, (B, N, H, dk // 2)),
+        _dev(v4, "v4", torch.uint8, (B, N, H, dv // 2)),
+        _dev(q_sf, "q_sf", torch.uint8, (B, N, H, dk // 16)),
+        _dev(k_sf, "k_sf", torch.uint8, (B, N, H, dk // 16)),
+        _dev(v_sf, "v_sf", torch.uint8, (B, N, H, dv // 16)),
+        float(q_gs), float(k_gs), float(v_gs),
+        _dev(alpha, "alpha", torch.float32, (B, H)),
+        _dev(beta, "beta", torch.float32, (B, N, H)),
+        None if state_in is None else _dev(state_in, "state_in", torch.float32, (B, H, dv, dk)),
+        _dev(out, "out", torch.bfloat16, (B, N, H, dv)),
+        _dev(state_out, "state_out", torch.float32, (B, H, dv, dk)),
+    ]
+    check(lib.gdn_frame_step_nvfp4(*args, B, H, N, dk, dv, _stream_handle(stream)), "gdn_frame_step_nvfp4")
+    return out, state_out
+
+
 def frame_step(q, k, v, alpha, beta, state_in=None, *, out=None, state_out=None, stream=None):
     """One latent frame on a resident state.  q, k [B,N,H,dk]; v [B,N,H,dv];
     alpha [B,H]; beta [B,N,H].  state_out may be the same tensor as state_in."""
@@ -328,9 +388,31 @@ def set_fused_step(on: bool) -> None:
     load().gdn_set_fused_step(1 if on else 0)
 
 
+def set_single_pass(on: bool, contract_ctas: int = 0, ring_frames: int = 0) -> None:
+    """Whole forward as one launch (True, the default: one scan CTA per head,
+    contraction and output CTAs on the other SMs, frames handed on through
+    L2-resident rings) or phase 1 then phases 2+3 (False).  contract_ctas and
+    ring_frames > 0 fix the contraction CTA count and the ring depth."""
+    load().gdn_set_single_pass(1 if on else 0, int(contract_ctas), int(ring_frames))
+
+
+def forward_schedule(B, H, F, N, dk, dv) -> int:
+    """2: single pass; 1: phase 1 then fused scan/output; 0: three launches."""
+    return int(load().gdn_forward_schedule(B, H, F, N, dk, dv))
+
+
 def scan_schedule(B, H, dv) -> int:
     """+R: fused scan/output with R state rows per scan CTA; -R: two launches."""
     return int(load().gdn_scan_schedule(B, H, dv))
+
+
+def last_timeout() -> dict:
+    """Where the first bounded wait that ran out gave up (and clear it):
+    site code, block, thread, value seen, value awaited (site 0: none)."""
+    import ctypes
+    info = (ctypes.c_int * 5)()
+    check(load().gdn_debug_last_timeout(info), "gdn_debug_last_timeout")
+    return dict(zip(("site", "block", "thread", "seen", "awaited"), list(info)))
 
 
 def set_wait_limit_ns(ns: int) -> None:
@@ -344,6 +426,7 @@ def selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     return int(lib.gdn_sync_status(_stream_handle(stream)))
 
 
-__all__ = ["frame_forward", "frame_forward_gated", "frame_step_gated", "frame_step", "frame_forward_timed", "frame_forward_host", "workspace_bytes",
-           "step_workspace_bytes", "sync_status", "set_fused_scan", "scan_schedule", "set_wait_limit_ns", "selftest_wait_timeout",
+__all__ = ["frame_forward", "frame_forward_nvfp4", "frame_step_nvfp4", "frame_forward_gated", "frame_step_gated", "frame_step", "frame_forward_timed", "frame_forward_host", "workspace_bytes",
+           "step_workspace_bytes", "sync_status", "set_fused_scan", "scan_schedule", "set_single_pass",
+           "forward_schedule", "set_wait_limit_ns", "selftest_wait_timeout",
            "GDNError"]

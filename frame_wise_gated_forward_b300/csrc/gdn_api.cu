@@ -13,6 +13,7 @@
 
 #include "gdn.h"
 #include "gdn_bwd.cuh"
+#include "gdn_fwd_single.cuh"
 #include "gdn_k1_contract.cuh"
 #include "gdn_k23_fused.cuh"
 #include "gdn_step_fused.cuh"
@@ -25,6 +26,48 @@ std::atomic<unsigned long long> g_wait_limit_ns{2000000000ULL};
 std::atomic<int> g_fused_scan{1};
 std::atomic<int> g_max_split{0};  // 0: automatic; 1: never split; k > 1: up to k token ranges per item
 std::atomic<int> g_fused_step{1};  // one-launch step (gdn_step_fused.cuh) where it applies
+std::atomic<int> g_single_pass{1};     // whole forward in one launch (gdn_fwd_single.cuh) where it applies
+std::atomic<int> g_single_contract{0}; // contraction CTAs of the single pass (0: automatic)
+std::atomic<int> g_single_ring{0};     // ring frames of the single pass (0: automatic)
+
+// Kernels of each element format (gdn::FMT_BF16, FMT_FP8, FMT_FP4).
+using gdn::FMT_BF16;
+using gdn::FMT_FP4;
+using gdn::FMT_FP8;
+const void* k1_fn(int fmt) {
+    return fmt == FMT_FP8   ? reinterpret_cast<const void*>(gdn::k1::contract_kernel<FMT_FP8>)
+           : fmt == FMT_FP4 ? reinterpret_cast<const void*>(gdn::k1::contract_kernel<FMT_FP4>)
+                            : reinterpret_cast<const void*>(gdn::k1::contract_kernel<FMT_BF16>);
+}
+size_t k1_smem(int fmt) {
+    return fmt == FMT_FP8 ? gdn::k1::SMEM_BYTES_FP8 : fmt == FMT_FP4 ? gdn::k1::SMEM_BYTES_FP4 : gdn::k1::SMEM_BYTES;
+}
+const void* k3_fn(int fmt) {
+    return fmt == FMT_FP8   ? reinterpret_cast<const void*>(gdn::k3::output_kernel<FMT_FP8>)
+           : fmt == FMT_FP4 ? reinterpret_cast<const void*>(gdn::k3::output_kernel<FMT_FP4>)
+                            : reinterpret_cast<const void*>(gdn::k3::output_kernel<FMT_BF16>);
+}
+int k3_threads(int fmt) { return fmt == FMT_BF16 ? gdn::k3::threads<FMT_BF16>() : gdn::k3::threads<FMT_FP8>(); }
+template <int R>
+const void* k23_fn_r(int fmt) {
+    return fmt == FMT_FP8   ? reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<R, FMT_FP8>)
+           : fmt == FMT_FP4 ? reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<R, FMT_FP4>)
+                            : reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<R, FMT_BF16>);
+}
+const void* k23_fn(int R, int fmt) { return R == 16 ? k23_fn_r<16>(fmt) : R == 32 ? k23_fn_r<32>(fmt) : k23_fn_r<64>(fmt); }
+size_t k23_smem(int R) {
+    return R == 16 ? gdn::k23::smem_bytes<16>() : R == 32 ? gdn::k23::smem_bytes<32>() : gdn::k23::smem_bytes<64>();
+}
+const void* fwd_fn(int fmt) {
+    return fmt == FMT_FP8   ? reinterpret_cast<const void*>(gdn::fwd::forward_kernel<FMT_FP8>)
+           : fmt == FMT_FP4 ? reinterpret_cast<const void*>(gdn::fwd::forward_kernel<FMT_FP4>)
+                            : reinterpret_cast<const void*>(gdn::fwd::forward_kernel<FMT_BF16>);
+}
+size_t fwd_smem(int fmt) {
+    return fmt == FMT_FP8   ? gdn::fwd::smem_bytes<FMT_FP8>()
+           : fmt == FMT_FP4 ? gdn::fwd::smem_bytes<FMT_FP4>()
+                            : gdn::fwd::smem_bytes<FMT_BF16>();
+}
 
 // ------------------------------------------------------------------ devices
 struct DeviceState {
@@ -33,6 +76,7 @@ struct DeviceState {
     int sms = 0;
     bool coop = false;     // cooperative launches possible with one fused CTA per SM
     bool coop_k1 = false;  // the same for the contraction kernel (needed to split items)
+    bool coop_single = false;  // the same for the single-pass forward kernel
     cudaMemPool_t pool = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
@@ -83,19 +127,17 @@ gdn_status device_ready(int* dev_out, DeviceState** st_out) {
                    cudaSuccess;
         };
         using namespace gdn;
-        if (!smem_attr(reinterpret_cast<const void*>(k1::contract_kernel<false>), k1::SMEM_BYTES) ||
-            !smem_attr(reinterpret_cast<const void*>(k1::contract_kernel<true>), k1::SMEM_BYTES_FP8) ||
+        bool fmt_ok = true;
+        for (int fmt : {FMT_BF16, FMT_FP8, FMT_FP4}) {
+            fmt_ok = fmt_ok && smem_attr(k1_fn(fmt), k1_smem(fmt)) && smem_attr(k3_fn(fmt), k3::SMEM_BYTES) &&
+                     smem_attr(fwd_fn(fmt), fwd_smem(fmt));
+            for (int R : {16, 32, 64}) fmt_ok = fmt_ok && smem_attr(k23_fn(R, fmt), k23_smem(R));
+        }
+        if (!fmt_ok ||
             !smem_attr(reinterpret_cast<const void*>(k2::scan_kernel<16>), k2::Cfg<16>::SMEM_BYTES) ||
             !smem_attr(reinterpret_cast<const void*>(k2::scan_kernel<32>), k2::Cfg<32>::SMEM_BYTES) ||
             !smem_attr(reinterpret_cast<const void*>(k2::scan_kernel<64>), k2::Cfg<64>::SMEM_BYTES) ||
-            !smem_attr(reinterpret_cast<const void*>(k3::output_kernel<false>), k3::SMEM_BYTES) ||
-            !smem_attr(reinterpret_cast<const void*>(k3::output_kernel<true>), k3::SMEM_BYTES) ||
-            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<16, false>), k23::smem_bytes<16>()) ||
-            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<32, false>), k23::smem_bytes<32>()) ||
-            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<64, false>), k23::smem_bytes<64>()) ||
-            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<16, true>), k23::smem_bytes<16>()) ||
-            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<32, true>), k23::smem_bytes<32>()) ||
-            !smem_attr(reinterpret_cast<const void*>(k23::scan_output_kernel<64, true>), k23::smem_bytes<64>()) ||
+
             !smem_attr(reinterpret_cast<const void*>(step::step_kernel), step::SMEM_BYTES) ||
             !smem_attr(reinterpret_cast<const void*>(bwd::frame_grad_kernel), bwd::FRAME_SMEM) ||
             !smem_attr(reinterpret_cast<const void*>(bwd::token_grad_kernel), bwd::TOKEN_SMEM)) {
@@ -104,17 +146,27 @@ gdn_status device_ready(int* dev_out, DeviceState** st_out) {
         }
         int coop = 0, per_sm = 0;
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k23::scan_output_kernel<64, false>, k23::THREADS,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k23::scan_output_kernel<64, FMT_BF16>, k23::THREADS,
                                                           k23::smem_bytes<64>()) != cudaSuccess)
             per_sm = 0;
         cudaGetLastError();
         d.coop = coop != 0 && per_sm >= 1;
         int per_sm_k1 = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_k1, k1::contract_kernel<false>, k1::THREADS,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_k1, k1::contract_kernel<FMT_BF16>, k1::THREADS,
                                                           k1::SMEM_BYTES) != cudaSuccess)
             per_sm_k1 = 0;
         cudaGetLastError();
         d.coop_k1 = coop != 0 && per_sm_k1 >= 1;
+        int per_sm_single = 1;
+        for (int fmt : {FMT_BF16, FMT_FP8, FMT_FP4}) {
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_fn(fmt), fwd::THREADS, fwd_smem(fmt)) !=
+                cudaSuccess)
+                n = 0;
+            per_sm_single = std::min(per_sm_single, n);
+        }
+        cudaGetLastError();
+        d.coop_single = coop != 0 && per_sm_single >= 1;
         d.ok = true;
     }
     if (!d.ok) return GDN_ERR_NO_DEVICE;
@@ -131,10 +183,10 @@ struct Range {
 };
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
-// in_bytes: bytes per q/k/v element (2: bf16, 1: fp8); out is always bf16
+// in_bits: bits per q/k/v element (16: bf16, 8: fp8, 4: NVFP4 codes); out is always bf16
 gdn_status validate(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
                     const float* state_in, const void* out, const float* state_out, int B, int H, int F, int N,
-                    int dk, int dv, int in_bytes = 2) {
+                    int dk, int dv, int in_bits = 16) {
     if (!q || !k || !v || !alpha || !beta || !out) return GDN_ERR_NULL_PTR;
     if (B < 1 || H < 1 || F < 1 || N < 1) return GDN_ERR_BAD_DIM;
     if (!dim_ok(dk) || !dim_ok(dv)) return GDN_ERR_UNSUPPORTED;
@@ -148,9 +200,9 @@ gdn_status validate(const void* q, const void* k, const void* v, const float* al
         return GDN_ERR_MISALIGNED;
     const uintptr_t qb = reinterpret_cast<uintptr_t>(q), kb = reinterpret_cast<uintptr_t>(k),
                     vb = reinterpret_cast<uintptr_t>(v), ob = reinterpret_cast<uintptr_t>(out);
-    const Range rq{qb, qb + static_cast<uintptr_t>(tok * H * dk * in_bytes)};
-    const Range rk{kb, kb + static_cast<uintptr_t>(tok * H * dk * in_bytes)};
-    const Range rv{vb, vb + static_cast<uintptr_t>(tok * H * dv * in_bytes)};
+    const Range rq{qb, qb + static_cast<uintptr_t>(tok * H * dk * in_bits / 8)};
+    const Range rk{kb, kb + static_cast<uintptr_t>(tok * H * dk * in_bits / 8)};
+    const Range rv{vb, vb + static_cast<uintptr_t>(tok * H * dv * in_bits / 8)};
     const Range ro{ob, ob + static_cast<uintptr_t>(tok * H * dv * 2)};
     const uintptr_t ab = reinterpret_cast<uintptr_t>(alpha), bb = reinterpret_cast<uintptr_t>(beta);
     const Range ra{ab, ab + static_cast<uintptr_t>(static_cast<long long>(B) * F * H * 4)};
@@ -264,6 +316,23 @@ bool encode_tokens8(CUtensorMap* m, const void* base, int BF, int N, int H, int 
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+// NVFP4 token tensor [BF, N, H, d/2] bytes (two codes per byte), box (d/2, 1,
+// rows, 1): one unswizzled row of d/2 bytes per token (d = 64 or 128)
+bool encode_tokens4(CUtensorMap* m, const void* base, int BF, int N, int H, int d, int rows) {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d / 2), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BF)};
+    const cuuint64_t st[3] = {static_cast<cuuint64_t>(d / 2), static_cast<cuuint64_t>(H) * d / 2,
+                              static_cast<cuuint64_t>(N) * H * d / 2};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(d / 2), 1, static_cast<cuuint32_t>(rows), 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, st, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// q, k, v token maps in the call's element format; rows_k: token rows per box of k and v
+bool encode_inputs(CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tq, const void* q, const void* k, const void* v,
+                   int fmt, int BF, int N, int H, int dk, int dv, int rows_k, int rows_q);
+
 // per-item matrix [items, rows_total, cols] bf16, box (64, rows, 1)
 bool encode_mats(CUtensorMap* m, const void* base, long long items, int rows_total, int cols, int rows) {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows_total),
@@ -287,6 +356,31 @@ bool encode_mats_f32(CUtensorMap* m, const void* base, long long items, int rows
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_inputs(CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tq, const void* q, const void* k, const void* v,
+                   int fmt, int BF, int N, int H, int dk, int dv, int rows_k, int rows_q) {
+    if (fmt == FMT_FP8)
+        return encode_tokens8(tk, k, BF, N, H, dk, rows_k) && encode_tokens8(tv, v, BF, N, H, dv, rows_k) &&
+               encode_tokens8(tq, q, BF, N, H, dk, rows_q);
+    if (fmt == FMT_FP4)
+        return encode_tokens4(tk, k, BF, N, H, dk, rows_k) && encode_tokens4(tv, v, BF, N, H, dv, rows_k) &&
+               encode_tokens4(tq, q, BF, N, H, dk, rows_q);
+    return encode_tokens(tk, k, BF, N, H, dk, rows_k) && encode_tokens(tv, v, BF, N, H, dv, rows_k) &&
+           encode_tokens(tq, q, BF, N, H, dk, rows_q);
+}
+
+// per-item fp32 matrix [items, rows_total, cols], 128-byte swizzle, box (32, rows, 1)
+bool encode_mats_f32_sw(CUtensorMap* m, const void* base, long long items, int rows_total, int cols, int rows) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows_total),
+                                static_cast<cuuint64_t>(items)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 4,
+                                   static_cast<cuuint64_t>(rows_total) * cols * 4};
+    const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(rows), 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------- the pass
 struct PassArgs {
     const void *q, *k, *v;
@@ -297,7 +391,8 @@ struct PassArgs {
     int reverse = 0;
     int prologue = 0;          // raw q, k and gate logits: normalize and apply the gates in the kernels
     float alpha_scale = 0.0f;  // prologue: alpha = exp(-softplus(a) * alpha_scale)
-    int fp8 = 0;               // q, k, v are e4m3 bytes; real value = scale * e4m3
+    int fmt = gdn::FMT_BF16;   // q, k, v element format (FMT_FP8: value = scale * e4m3; FMT_FP4: NVFP4)
+    const uint8_t *q_sf = nullptr, *k_sf = nullptr, *v_sf = nullptr;   // NVFP4 block scales
     float q_scale = 1.0f, k_scale = 1.0f, v_scale = 1.0f;
 };
 
@@ -334,13 +429,8 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
     const int R = Rf != 0 ? Rf : scan_rows_standalone(a.B, a.H, a.dv, ds->sms);
     int* flags = reinterpret_cast<int*>(ws + L.f_off);
     CUtensorMap tm_k, tm_v, tm_q, tm_out, tm_A, tm_U, tm_S_store, tm_S_load;
-    const bool enc_in =
-        a.fp8 ? (encode_tokens8(&tm_k, a.k, BF, a.N, a.H, a.dk, gdn::k1::CHUNK) &&
-                 encode_tokens8(&tm_v, a.v, BF, a.N, a.H, a.dv, gdn::k1::CHUNK) &&
-                 encode_tokens8(&tm_q, a.q, BF, a.N, a.H, a.dk, gdn::k3::TILE_M))
-              : (encode_tokens(&tm_k, a.k, BF, a.N, a.H, a.dk, gdn::k1::CHUNK) &&
-                 encode_tokens(&tm_v, a.v, BF, a.N, a.H, a.dv, gdn::k1::CHUNK) &&
-                 encode_tokens(&tm_q, a.q, BF, a.N, a.H, a.dk, gdn::k3::TILE_M));
+    const bool enc_in = encode_inputs(&tm_k, &tm_v, &tm_q, a.q, a.k, a.v, a.fmt, BF, a.N, a.H, a.dk, a.dv,
+                                      gdn::k1::CHUNK, gdn::k3::TILE_M);
     const bool enc = enc_in &&
                      encode_tokens(&tm_out, a.out, BF, a.N, a.H, a.dv, 32) &&
                      encode_mats(&tm_A, A_ws, items, a.dk, a.dk, 128) &&
@@ -355,6 +445,7 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
         return GDN_ERR_LAUNCH;
     // phase 1
     gdn::k1::Params p1;
+    std::memset(&p1, 0, sizeof(p1));   // ring mode off
     p1.beta = a.beta;
     p1.A_ws = A_ws;
     p1.U_ws = U_ws;
@@ -371,14 +462,15 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
     p1.work = sp.work;
     p1.norm_k = a.prologue;
     p1.beta_sigmoid = a.prologue;
-    p1.a_scale = a.fp8 ? a.k_scale * a.k_scale : 1.0f;
-    p1.u_scale = a.fp8 ? a.k_scale * a.v_scale : 1.0f;
+    p1.a_scale = a.fmt != gdn::FMT_BF16 ? a.k_scale * a.k_scale : 1.0f;
+    p1.u_scale = a.fmt != gdn::FMT_BF16 ? a.k_scale * a.v_scale : 1.0f;
+    p1.k_sf = a.k_sf;
+    p1.v_sf = a.v_sf;
     p1.wait_limit_ns = lim;
     if (ev) cudaEventRecord(ev[0], stream);
     const int grid1 = std::min(p1.work, ds->sms);
-    const void* fn1 = a.fp8 ? reinterpret_cast<const void*>(gdn::k1::contract_kernel<true>)
-                            : reinterpret_cast<const void*>(gdn::k1::contract_kernel<false>);
-    const size_t smem1 = a.fp8 ? gdn::k1::SMEM_BYTES_FP8 : gdn::k1::SMEM_BYTES;
+    const void* fn1 = k1_fn(a.fmt);
+    const size_t smem1 = k1_smem(a.fmt);
     void* args1[] = {&tm_k, &tm_v, &p1};
     // split items wait for each other's partial sums: then all CTAs must be resident
     const cudaError_t e1 =
@@ -414,7 +506,8 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
     p3.total = items * p3.ntile;
     p3.reverse = a.reverse;
     p3.norm_q = a.prologue;
-    p3.q_scale = a.fp8 ? a.q_scale : 1.0f;
+    p3.q_scale = a.fmt != gdn::FMT_BF16 ? a.q_scale : 1.0f;
+    p3.q_sf = a.q_sf;
     p3.b_mn = 0;
     p3.wait_limit_ns = lim;
     const int n_scan = a.B * a.H * p2.rsplit;
@@ -424,17 +517,10 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
         int grid = n_scan + static_cast<int>(workers);
         int n_scan_arg = n_scan;
         void* args[] = {&tm_A, &tm_U, &tm_S_store, &tm_q, &tm_S_load, &tm_out, &p2, &p3, &flags, &n_scan_arg};
-        const void* fn =
-            a.fp8 ? (Rf == 16   ? reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<16, true>)
-                     : Rf == 32 ? reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<32, true>)
-                                : reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<64, true>))
-                  : (Rf == 16   ? reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<16, false>)
-                     : Rf == 32 ? reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<32, false>)
-                                : reinterpret_cast<const void*>(gdn::k23::scan_output_kernel<64, false>));
-        const size_t smem = Rf == 16 ? gdn::k23::smem_bytes<16>()
-                             : Rf == 32 ? gdn::k23::smem_bytes<32>() : gdn::k23::smem_bytes<64>();
+        const void* fn = k23_fn(Rf, a.fmt);
+        const size_t smem = k23_smem(Rf);
         if (ev) cudaEventRecord(ev[2], stream);
-        const int threads = a.fp8 ? gdn::k3::threads<true>() : gdn::k3::threads<false>();
+        const int threads = k3_threads(a.fmt);
         if (cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(threads), args, smem, stream) != cudaSuccess) {
             cudaGetLastError();
             return GDN_ERR_LAUNCH;
@@ -451,12 +537,170 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
                 tm_A, tm_U, tm_S_store, p2);
         if (ev) cudaEventRecord(ev[2], stream);
         const int grid3 = static_cast<int>(std::min<long long>(p3.total, ds->sms));
-        if (a.fp8)
-            gdn::k3::output_kernel<true><<<grid3, gdn::k3::threads<true>(), gdn::k3::SMEM_BYTES, stream>>>(
-                tm_q, tm_S_load, tm_out, p3);
-        else
-            gdn::k3::output_kernel<false><<<grid3, gdn::k3::THREADS, gdn::k3::SMEM_BYTES, stream>>>(tm_q, tm_S_load,
-                                                                                                  tm_out, p3);
+        void* args3[] = {&tm_q, &tm_S_load, &tm_out, &p3};
+        if (cudaLaunchKernel(k3_fn(a.fmt), dim3(grid3), dim3(k3_threads(a.fmt)), args3, gdn::k3::SMEM_BYTES, stream) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return GDN_ERR_LAUNCH;
+        }
+    }
+    if (ev) cudaEventRecord(ev[3], stream);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+
+// ------------------------------------------------ the single-pass forward
+// Scan CTAs of the single pass for this shape (one per head), or 0 when the
+// whole forward does not run as one launch: switched off, a one-frame call,
+// no cooperative launch at one CTA per SM, or so many heads that fewer than
+// three quarters of the SMs would be left to the contraction and the output.
+int single_pass_heads(const PassArgs& a, const DeviceState* ds) {
+    if (g_single_pass.load() == 0 || !ds->coop_single || a.F < 2) return 0;
+    const long long heads = static_cast<long long>(a.B) * a.H;
+    return heads * 4 <= ds->sms ? static_cast<int>(heads) : 0;
+}
+
+// Ring frames: as many as keep the three rings within ~24 MiB (so they stay
+// in L2 next to the streaming inputs), at least 4, at most F.
+int single_pass_ring(const PassArgs& a) {
+    const int forced = g_single_ring.load();
+    if (forced > 0) return std::min(forced, a.F);
+    const size_t per_frame = static_cast<size_t>(a.B) * a.H *
+                             (static_cast<size_t>(a.dk) * a.dk * 2 + static_cast<size_t>(a.dv) * a.dk * 6);
+    const int w = static_cast<int>(std::max<size_t>(4, (size_t(24) << 20) / per_frame));
+    return std::min(w, a.F);
+}
+
+struct SingleLayout {
+    int ring;
+    long long slots;
+    size_t a_off, u_off, s_off, c_off, total;
+};
+SingleLayout single_layout(const PassArgs& a) {
+    SingleLayout L;
+    L.ring = single_pass_ring(a);
+    L.slots = static_cast<long long>(a.B) * L.ring * a.H;
+    L.a_off = 0;
+    L.u_off = align256(L.a_off + static_cast<size_t>(L.slots) * a.dk * a.dk * 2);
+    L.s_off = align256(L.u_off + static_cast<size_t>(L.slots) * a.dv * a.dk * 4);
+    L.c_off = align256(L.s_off + static_cast<size_t>(L.slots) * a.dv * a.dk * 2);
+    L.total = align256(L.c_off + static_cast<size_t>(L.slots) * 4 * 4);
+    return L;
+}
+
+gdn_status launch_single(const PassArgs& a, uint8_t* ws, const SingleLayout& L, const DeviceState* ds,
+                         cudaStream_t stream, cudaEvent_t const* ev) {
+    using namespace gdn;
+    const int BF = a.B * a.F;
+    const long long items = static_cast<long long>(a.B) * a.F * a.H;
+    __nv_bfloat16* A_r = reinterpret_cast<__nv_bfloat16*>(ws + L.a_off);
+    float* U_r = reinterpret_cast<float*>(ws + L.u_off);
+    __nv_bfloat16* S_r = reinterpret_cast<__nv_bfloat16*>(ws + L.s_off);
+    int* cnt = reinterpret_cast<int*>(ws + L.c_off);
+    int* au_ready = cnt;
+    int* au_free = cnt + L.slots;
+    int* s_ready = cnt + 2 * L.slots;
+    int* s_free = cnt + 3 * L.slots;
+    CUtensorMap tm_k, tm_v, tm_q, tm_out, tm_A, tm_U, tm_S;
+    const bool enc_in =
+        encode_inputs(&tm_k, &tm_v, &tm_q, a.q, a.k, a.v, a.fmt, BF, a.N, a.H, a.dk, a.dv, k1::CHUNK, k3::TILE_M);
+    if (!enc_in || !encode_tokens(&tm_out, a.out, BF, a.N, a.H, a.dv, 32) ||
+        !encode_mats(&tm_A, A_r, L.slots, a.dk, a.dk, 128) || !encode_mats_f32_sw(&tm_U, U_r, L.slots, a.dv, a.dk, 128) ||
+        !encode_mats(&tm_S, S_r, L.slots, a.dv, a.dk, 128))
+        return GDN_ERR_LAUNCH;
+    const unsigned long long lim = g_wait_limit_ns.load();
+    if (ev) cudaEventRecord(ev[0], stream);
+    if (cudaMemsetAsync(cnt, 0, static_cast<size_t>(L.slots) * 16, stream) != cudaSuccess) return GDN_ERR_LAUNCH;
+    if (ev) {
+        cudaEventRecord(ev[1], stream);
+        cudaEventRecord(ev[2], stream);
+    }
+    // roles: one scan CTA per head, the other SMs split between contraction and output
+    fwd::Counts c;
+    c.s_ready = s_ready;
+    c.s_free = s_free;
+    c.n_scan = a.B * a.H;
+    const int rest = ds->sms - c.n_scan;
+    const int forced = g_single_contract.load();
+    // automatic: 60 % of the free SMs contract (a contraction CTA streams k and v
+    // at about two thirds of an output CTA's rate of q in plus out; measured on
+    // B300 at the 60 s shape: 50 % 0.417 ms, 55 % 0.385 ms, 60 % 0.378 ms, 68 % 0.407 ms)
+    c.n_contract = forced > 0 ? std::min(forced, rest - 1) : (rest * 3 + 2) / 5;
+    const int n_out = rest - c.n_contract;
+    if (c.n_contract < 1 || n_out < 1) return GDN_ERR_LAUNCH;
+
+    k1::Params p1;
+    std::memset(&p1, 0, sizeof(p1));
+    p1.beta = a.beta;
+    p1.A_ws = A_r;
+    p1.U_ws = U_r;
+    p1.H = a.H;
+    p1.N = a.N;
+    p1.dk = a.dk;
+    p1.dv = a.dv;
+    p1.items = static_cast<int>(items);
+    p1.whole = static_cast<int>(items);
+    p1.split_per = 1;
+    p1.chunks = chunks_of(a.N);
+    p1.work = static_cast<int>(items);
+    p1.norm_k = a.prologue;
+    p1.beta_sigmoid = a.prologue;
+    p1.a_scale = a.fmt != FMT_BF16 ? a.k_scale * a.k_scale : 1.0f;
+    p1.u_scale = a.fmt != FMT_BF16 ? a.k_scale * a.v_scale : 1.0f;
+    p1.k_sf = a.k_sf;
+    p1.v_sf = a.v_sf;
+    p1.ring = L.ring;
+    p1.B = a.B;
+    p1.F = a.F;
+    p1.reverse = a.reverse;
+    p1.au_ready = au_ready;
+    p1.au_free = au_free;
+    p1.wait_limit_ns = lim;
+
+    k3::Params p3;
+    p3.B = a.B;
+    p3.H = a.H;
+    p3.F = a.F;
+    p3.N = a.N;
+    p3.dk = a.dk;
+    p3.dv = a.dv;
+    p3.ntile = (a.N + k3::TILE_M - 1) / k3::TILE_M;
+    p3.total = items * p3.ntile;
+    p3.reverse = a.reverse;
+    p3.norm_q = a.prologue;
+    p3.q_scale = a.fmt != FMT_BF16 ? a.q_scale : 1.0f;
+    p3.q_sf = a.q_sf;
+    p3.b_mn = 0;
+    p3.wait_limit_ns = lim;
+
+    k2h::Params p2;
+    p2.alpha = a.alpha;
+    p2.state_in = a.state_in;
+    p2.state_out = a.state_out;
+    p2.B = a.B;
+    p2.H = a.H;
+    p2.F = a.F;
+    p2.dk = a.dk;
+    p2.dv = a.dv;
+    p2.reverse = a.reverse;
+    p2.alpha_gate = a.prologue;
+    p2.alpha_scale = a.alpha_scale;
+    p2.ring = L.ring;
+    p2.au_ready = au_ready;
+    p2.au_free = au_free;
+    p2.s_ready = s_ready;
+    p2.s_free = s_free;
+    // the output role loads an item's state once per item, or once per tile when
+    // items are fewer than two per output CTA (k3::Sched)
+    p2.s_units = items < 2LL * n_out ? p3.ntile : 1;
+    p2.wait_limit_ns = lim;
+
+    const int grid = c.n_scan + c.n_contract + n_out;
+    void* args[] = {&tm_k, &tm_v, &tm_A, &tm_U, &tm_S, &tm_q, &tm_out, &p1, &p2, &p3, &c};
+    const void* fn = fwd_fn(a.fmt);
+    const size_t smem = fwd_smem(a.fmt);
+    if (cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(fwd::THREADS), args, smem, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_LAUNCH;
     }
     if (ev) cudaEventRecord(ev[3], stream);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
@@ -469,7 +713,7 @@ bool all_device(const PassArgs& a) {
 
 // The one-launch step: a plain bf16 frame (no folded prologue, no 8-bit inputs).
 bool fused_step_applies(const PassArgs& a) {
-    return g_fused_step.load() != 0 && a.F == 1 && !a.fp8 && !a.prologue;
+    return g_fused_step.load() != 0 && a.F == 1 && a.fmt == gdn::FMT_BF16 && !a.prologue;
 }
 gdn_status launch_step_fused(const PassArgs& a, cudaStream_t stream) {
     CUtensorMap tm_k, tm_v, tm_q, tm_o;
@@ -522,6 +766,17 @@ gdn_status run_pass(const PassArgs& a, bool step, cudaStream_t stream, cudaEvent
     if (st != GDN_OK) return st;
     if (!all_device(a)) return GDN_ERR_NULL_PTR;
     if (step && fused_step_applies(a) && ev == nullptr) return launch_step_fused(a, stream);
+    if (!step && single_pass_heads(a, ds) > 0) {
+        const SingleLayout L = single_layout(a);
+        uint8_t* ws = nullptr;
+        if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), L.total, ds->pool, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GDN_ERR_ALLOC;
+        }
+        const gdn_status result = launch_single(a, ws, L, ds, stream, ev);
+        cudaFreeAsync(ws, stream);
+        return result;
+    }
     const long long items = static_cast<long long>(a.B) * a.F * a.H;
     const SplitPlan sp = plan_split(items, chunks_of(a.N), ds->sms, ds->coop_k1);
     const Layout L = layout_of(items, a.dk, a.dv, sp);
@@ -585,6 +840,7 @@ gdn_status bwd_contract(const void* k, const void* v, const float* beta, __nv_bf
         return GDN_ERR_LAUNCH;
     const long long items = static_cast<long long>(F) * H;
     gdn::k1::Params p1;
+    std::memset(&p1, 0, sizeof(p1));   // ring mode off
     p1.beta = beta;
     p1.A_ws = A_out;
     p1.U_ws = U_out;
@@ -604,7 +860,7 @@ gdn_status bwd_contract(const void* k, const void* v, const float* beta, __nv_bf
     p1.a_scale = 1.0f;
     p1.u_scale = 1.0f;
     p1.wait_limit_ns = g_wait_limit_ns.load();
-    gdn::k1::contract_kernel<false><<<std::min(p1.work, ds->sms), gdn::k1::THREADS, gdn::k1::SMEM_BYTES, st>>>(
+    gdn::k1::contract_kernel<gdn::FMT_BF16><<<std::min(p1.work, ds->sms), gdn::k1::THREADS, gdn::k1::SMEM_BYTES, st>>>(
         tm_k, tm_v, p1);
     return GDN_OK;
 }
@@ -731,8 +987,9 @@ gdn_status bwd_row(const BwdArgs& a, int b, uint8_t* ws, const BwdLayout& L, con
         p3.q_scale = 1.0f;
         p3.b_mn = 1;
         p3.wait_limit_ns = g_wait_limit_ns.load();
-        gdn::k3::output_kernel<false><<<static_cast<int>(std::min<long long>(p3.total, ds->sms)),
-                                        gdn::k3::threads<false>(), gdn::k3::SMEM_BYTES, st>>>(tm_do, tm_S, tm_dq, p3);
+        gdn::k3::output_kernel<gdn::FMT_BF16><<<static_cast<int>(std::min<long long>(p3.total, ds->sms)),
+                                                gdn::k3::threads<gdn::FMT_BF16>(), gdn::k3::SMEM_BYTES, st>>>(
+            tm_do, tm_S, tm_dq, p3);
     }
     // dk, dv, dbeta
     {
@@ -832,10 +1089,10 @@ gdn_status gdn_frame_forward_fp8(const void* q, const void* k, const void* v, fl
                                  float v_scale, const float* alpha, const float* beta, const float* state_in,
                                  void* out, float* state_out, int B, int H, int F, int N, int dk, int dv,
                                  gdn_stream_t stream) {
-    gdn_status s = validate(q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv, 1);
+    gdn_status s = validate(q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv, 8);
     if (s != GDN_OK) return s;
     PassArgs a{q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv};
-    a.fp8 = 1;
+    a.fmt = gdn::FMT_FP8;
     a.q_scale = q_scale;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
@@ -845,13 +1102,81 @@ gdn_status gdn_frame_forward_fp8(const void* q, const void* k, const void* v, fl
 gdn_status gdn_frame_step_fp8(const void* q, const void* k, const void* v, float q_scale, float k_scale,
                               float v_scale, const float* alpha, const float* beta, const float* state_in, void* out,
                               float* state_out, int B, int H, int N, int dk, int dv, gdn_stream_t stream) {
-    gdn_status s = validate(q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv, 1);
+    gdn_status s = validate(q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv, 8);
     if (s != GDN_OK) return s;
     PassArgs a{q, k, v, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv};
-    a.fp8 = 1;
+    a.fmt = gdn::FMT_FP8;
     a.q_scale = q_scale;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
+    return run_pass(a, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+namespace {
+// NVFP4 arguments: the common checks with 4 bits per element, then head sizes
+// 64 or 128, the three block-scale arrays (device memory, 16-byte aligned,
+// clear of every output).
+gdn_status validate_nvfp4(const void* q4, const void* k4, const void* v4, const void* q_sf, const void* k_sf,
+                          const void* v_sf, const float* alpha, const float* beta, const float* state_in,
+                          const void* out, const float* state_out, int B, int H, int F, int N, int dk, int dv) {
+    gdn_status s = validate(q4, k4, v4, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv, 4);
+    if (s != GDN_OK) return s;
+    if (!q_sf || !k_sf || !v_sf) return GDN_ERR_NULL_PTR;
+    if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128)) return GDN_ERR_UNSUPPORTED;
+    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!a16(q_sf) || !a16(k_sf) || !a16(v_sf)) return GDN_ERR_MISALIGNED;
+    const long long tok = static_cast<long long>(B) * F * N;
+    auto R = [](const void* p, long long n) {
+        return Range{reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(n)};
+    };
+    const Range sf[3] = {R(q_sf, tok * H * dk / 16), R(k_sf, tok * H * dk / 16), R(v_sf, tok * H * dv / 16)};
+    const Range ro = R(out, tok * H * dv * 2);
+    const Range rso = state_out ? R(state_out, static_cast<long long>(B) * H * dv * dk * 4) : Range{0, 0};
+    for (const Range& r : sf)
+        if (overlap(r, ro) || (state_out && overlap(r, rso))) return GDN_ERR_ALIAS;
+    if (!is_device_ptr(q_sf) || !is_device_ptr(k_sf) || !is_device_ptr(v_sf)) return GDN_ERR_NULL_PTR;
+    return GDN_OK;
+}
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_frame_forward_nvfp4(const void* q4, const void* k4, const void* v4, const void* q_sf,
+                                   const void* k_sf, const void* v_sf, float q_gs, float k_gs, float v_gs,
+                                   const float* alpha, const float* beta, const float* state_in, void* out,
+                                   float* state_out, int B, int H, int F, int N, int dk, int dv,
+                                   gdn_stream_t stream) {
+    gdn_status s = validate_nvfp4(q4, k4, v4, q_sf, k_sf, v_sf, alpha, beta, state_in, out, state_out, B, H, F, N,
+                                  dk, dv);
+    if (s != GDN_OK) return s;
+    PassArgs a{q4, k4, v4, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv};
+    a.fmt = gdn::FMT_FP4;
+    a.q_sf = static_cast<const uint8_t*>(q_sf);
+    a.k_sf = static_cast<const uint8_t*>(k_sf);
+    a.v_sf = static_cast<const uint8_t*>(v_sf);
+    a.q_scale = q_gs;
+    a.k_scale = k_gs;
+    a.v_scale = v_gs;
+    return run_pass(a, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_frame_step_nvfp4(const void* q4, const void* k4, const void* v4, const void* q_sf, const void* k_sf,
+                                const void* v_sf, float q_gs, float k_gs, float v_gs, const float* alpha,
+                                const float* beta, const float* state_in, void* out, float* state_out, int B, int H,
+                                int N, int dk, int dv, gdn_stream_t stream) {
+    gdn_status s = validate_nvfp4(q4, k4, v4, q_sf, k_sf, v_sf, alpha, beta, state_in, out, state_out, B, H, 1, N,
+                                  dk, dv);
+    if (s != GDN_OK) return s;
+    PassArgs a{q4, k4, v4, alpha, beta, state_in, out, state_out, B, H, 1, N, dk, dv};
+    a.fmt = gdn::FMT_FP4;
+    a.q_sf = static_cast<const uint8_t*>(q_sf);
+    a.k_sf = static_cast<const uint8_t*>(k_sf);
+    a.v_sf = static_cast<const uint8_t*>(v_sf);
+    a.q_scale = q_gs;
+    a.k_scale = k_gs;
+    a.v_scale = v_gs;
     return run_pass(a, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -992,13 +1317,16 @@ size_t gdn_workspace_bytes(int B, int H, int F, int N, int dk, int dv) {
     // plan with splitting allowed (an upper bound)
     int dev;
     DeviceState* ds;
-    if (device_ready(&dev, &ds) == GDN_OK)
+    if (device_ready(&dev, &ds) == GDN_OK) {
+        const PassArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, B, H, F, N, dk, dv};
+        if (single_pass_heads(a, ds) > 0) return single_layout(a).total;
         return layout_of(items, dk, dv, plan_split(items, chunks_of(N), ds->sms, ds->coop_k1)).total;
+    }
     return layout_of(items, dk, dv, plan_split(items, chunks_of(N), current_sms(), true)).total;
 }
 
 size_t gdn_step_workspace_bytes(int B, int H, int N, int dk, int dv) {
-    return gdn_workspace_bytes(B, H, 1, N, dk, dv);
+    return gdn_workspace_bytes(B, H, 1, N, dk, dv);   // a one-frame call never takes the single pass
 }
 
 const char* gdn_status_string(gdn_status s) {
@@ -1036,9 +1364,40 @@ gdn_status gdn_sync_status(gdn_stream_t stream) {
     return GDN_OK;
 }
 
+gdn_status gdn_debug_last_timeout(int* info) {
+    if (info == nullptr) return GDN_ERR_NULL_PTR;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return GDN_ERR_NO_DEVICE; }
+    int zero[5] = {0, 0, 0, 0, 0};
+    int taken = 0;
+    if (cudaMemcpyFromSymbol(info, gdn::g_timeout_info, sizeof(zero)) != cudaSuccess ||
+        cudaMemcpyToSymbol(gdn::g_timeout_info, zero, sizeof(zero)) != cudaSuccess ||
+        cudaMemcpyToSymbol(gdn::g_timeout_taken, &taken, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN_ERR_LAUNCH;
+    }
+    return GDN_OK;
+}
+
 void gdn_set_contract_split(int max_split) { g_max_split.store(max_split > 0 ? max_split : 0); }
 
 void gdn_set_fused_step(int on) { g_fused_step.store(on != 0 ? 1 : 0); }
+
+void gdn_set_single_pass(int on, int contract_ctas, int ring_frames) {
+    g_single_pass.store(on != 0 ? 1 : 0);
+    g_single_contract.store(contract_ctas > 0 ? contract_ctas : 0);
+    g_single_ring.store(ring_frames > 0 ? ring_frames : 0);
+}
+
+int gdn_forward_schedule(int B, int H, int F, int N, int dk, int dv) {
+    if (B < 1 || H < 1 || F < 1 || N < 1 || !dim_ok(dk) || !dim_ok(dv)) return -1;
+    int dev;
+    DeviceState* ds;
+    if (device_ready(&dev, &ds) != GDN_OK) return -1;
+    const PassArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, B, H, F, N, dk, dv};
+    if (single_pass_heads(a, ds) > 0) return 2;
+    return (g_fused_scan.load() != 0 && ds->coop && scan_rows_fused(B, H, dv, ds->sms) != 0) ? 1 : 0;
+}
 
 void gdn_set_fused_scan(int mode) {
     g_fused_scan.store((mode == 16 || mode == 32 || mode == 64) ? mode : (mode != 0 ? 1 : 0));

@@ -85,19 +85,33 @@ constexpr int STAGE8_BYTES = 2 * BOX8_BYTES;   // K, V
 constexpr int CBUFS8 = 3;
 constexpr int CBUF8_BYTES = 2 * TILE_BYTES;    // sqrt(beta) K | sqrt(beta) V, f16
 constexpr float FP8_BETA_MAX = 16384.0f;
-template <bool FP8>
+// NVFP4 k and v: one box of d/2 bytes (64 codes of a 128-column row: at most
+// 64 bytes, d = 64 or 128) per token row and input, unswizzled, STAGES4-deep;
+// their E4M3 block scales (d/16 per row) reach the decoders like beta, by
+// cp.async a few chunks ahead.  The decoders form e2m1 * scale exactly in
+// f16, then scale by sqrt(beta) like the 8-bit path; with values up to
+// 6 * 448 = 2688, beta must lie in [0, FP4_BETA_MAX] for sqrt(beta) * 2688 to
+// stay below the f16 maximum.
+constexpr int STAGES4 = 8;
+constexpr int RAW4_BYTES = CHUNK * 64;          // 64 token rows x up to 64 B
+constexpr int STAGE4_BYTES = 2 * RAW4_BYTES;    // K, V
+constexpr float FP4_BETA_MAX = 512.0f;
+constexpr int SF_RING_BYTES = (BETA_AHEAD + 1) * SCALER_THREADS * 8;   // two scale words per thread
+template <int FMT>
 struct Lay {
-    static constexpr int NST = FP8 ? STAGES8 : STAGES;              // TMA ring slots
-    static constexpr int ST_BYTES = FP8 ? STAGE8_BYTES : STAGE_BYTES;
-    static constexpr int NBK = FP8 ? CBUFS8 : BK_BUFS;              // MMA operand buffers
-    static constexpr int BK_BYTES = FP8 ? CBUF8_BYTES : TILE_BYTES;
+    static constexpr int NST = FMT == FMT_FP8 ? STAGES8 : FMT == FMT_FP4 ? STAGES4 : STAGES;   // TMA ring slots
+    static constexpr int ST_BYTES = FMT == FMT_FP8 ? STAGE8_BYTES : FMT == FMT_FP4 ? STAGE4_BYTES : STAGE_BYTES;
+    static constexpr int NBK = FMT != FMT_BF16 ? CBUFS8 : BK_BUFS;              // MMA operand buffers
+    static constexpr int BK_BYTES = FMT != FMT_BF16 ? CBUF8_BYTES : TILE_BYTES;
+    static constexpr int SF_BYTES = FMT == FMT_FP4 ? SF_RING_BYTES : 0;
     static constexpr size_t SMEM =
-        1024 /*align slack*/ + NST * ST_BYTES + NBK * BK_BYTES + BETA_RING_BYTES + 256 /*barriers*/;
+        1024 /*align slack*/ + NST * ST_BYTES + NBK * BK_BYTES + BETA_RING_BYTES + SF_BYTES + 256 /*barriers*/;
     static_assert(SMEM <= 232448, "shared memory");
     static_assert((2 * NST + 2 * NBK + 5) * 8 + 8 <= 256, "barrier area");
 };
-constexpr size_t SMEM_BYTES = Lay<false>::SMEM;
-constexpr size_t SMEM_BYTES_FP8 = Lay<true>::SMEM;
+constexpr size_t SMEM_BYTES = Lay<FMT_BF16>::SMEM;
+constexpr size_t SMEM_BYTES_FP8 = Lay<FMT_FP8>::SMEM;
+constexpr size_t SMEM_BYTES_FP4 = Lay<FMT_FP4>::SMEM;
 
 struct Params {
     const float* beta;     // [B, F, N, H]
@@ -115,6 +129,18 @@ struct Params {
     int beta_sigmoid;      // fused prologue: beta <- sigmoid(beta)
     float a_scale;         // A = a_scale * D[:, :dk]  (fp8 inputs: k_scale^2; else 1)
     float u_scale;         // U = u_scale * D[:, 128:] (fp8 inputs: k_scale * v_scale; else 1)
+    const uint8_t* k_sf;   // NVFP4: E4M3 block scales of k [B, F, N, H, dk/16]
+    const uint8_t* v_sf;   //        and of v [B, F, N, H, dv/16]
+    // Ring mode (single-pass forward; 0 = off): units are whole items in scan
+    // order -- step s of the scan (frame s, or F-1-s when reversed) for every
+    // (b, h) -- and A_f, U_f go to ring slot (b * ring + s % ring) * H + h of
+    // A_ws / U_ws instead of the item's own place.  Before a slot is
+    // rewritten the scan must have read its previous frame (au_free counts
+    // frames read per slot); after the stores au_ready counts one more frame.
+    int ring;
+    int B, F, reverse;
+    int* au_ready;
+    const int* au_free;
     unsigned long long wait_limit_ns;
 };
 
@@ -156,12 +182,28 @@ __device__ __forceinline__ uint32_t hscale(uint32_t x, const HSplit& s) {
 
 // Work units: the first `whole` items whole, then every remaining item split
 // into `split_per` contiguous token ranges (so the last round of the grid is
-// as long as the others); split == -1 marks a whole item.
+// as long as the others); split == -1 marks a whole item.  In ring mode every
+// unit is a whole item in scan order; `slot` is where its A and U go and
+// `use` how many frames went through that slot before it.
 struct Unit {
-    int item, split, c_begin, c_end;
+    int item, split, c_begin, c_end, slot, use;
 };
 __device__ __forceinline__ Unit unit_of(const Params& p, int w) {
     Unit u;
+    if (p.ring > 0) {
+        const int BH = p.B * p.H;
+        const int st = w / BH, r = w % BH, b = r / p.H, h = r % p.H;
+        const int f = p.reverse ? p.F - 1 - st : st;
+        u.item = (b * p.F + f) * p.H + h;
+        u.split = -1;
+        u.c_begin = 0;
+        u.c_end = p.chunks;
+        u.slot = (b * p.ring + st % p.ring) * p.H + h;
+        u.use = st / p.ring;
+        return u;
+    }
+    u.slot = -1;
+    u.use = 0;
     if (w < p.whole) {
         u.item = w;
         u.split = -1;
@@ -177,18 +219,21 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int w) {
     return u;
 }
 
-template <bool FP8>
-__global__ void __launch_bounds__(THREADS, 1)
-    contract_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                    const Params p) {
-    using L = Lay<FP8>;
+// The contraction of work units w_begin, w_begin + w_step, ... < p.work, in
+// a block of at least THREADS threads (warps past the epilogue stay idle).
+template <int FMT>
+__device__ __forceinline__ void contract_role(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const Params& p,
+                                              int w_begin, int w_step, uint8_t* smem) {
+    constexpr bool FP8 = FMT == FMT_FP8;
+    constexpr bool FP4 = FMT == FMT_FP4;
+    constexpr bool LP = FMT != FMT_BF16;   // decoded into one f16 operand buffer [sqrt(beta) K | sqrt(beta) V]
+    using L = Lay<FMT>;
     constexpr int NST = L::NST, NBK = L::NBK;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stage_base = smem;                                   // [NST][K tile | V tile]
     uint8_t* bk_base = smem + NST * L::ST_BYTES;                  // [NBK][beta*K tile (| K | V when FP8)]
     float* beta_ring = reinterpret_cast<float*>(bk_base + NBK * L::BK_BYTES);  // [BETA_AHEAD+1][SCALER_THREADS]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(bk_base + NBK * L::BK_BYTES + BETA_RING_BYTES);
+    uint32_t* sf_ring = reinterpret_cast<uint32_t*>(bk_base + NBK * L::BK_BYTES + BETA_RING_BYTES);  // FP4: [..][2]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(bk_base + NBK * L::BK_BYTES + BETA_RING_BYTES + L::SF_BYTES);
     uint64_t* full = bars;                          // [NST]  TMA landed K and V
     uint64_t* empty = full + NST;                   // [NST]  stage consumed (MMA, or FP8 decoders)
     uint64_t* bk_full = empty + NST;                // [NBK]  MMA operand buffer written
@@ -205,20 +250,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     // consecutive items, i.e. all heads of the same few frames, so together
     // they read whole token rows (all heads) of k and v.  The split units come
     // last and number at most gridDim.x, so each CTA holds at most one.
-    const int w_begin = blockIdx.x, w_end = p.work, w_step = gridDim.x;
+    const int w_end = p.work;
     const int kboxes = p.dk > 64 ? 2 : 1;
     const int vboxes = p.dv > 64 ? 2 : 1;
 
     // Boxes that are never loaded (d <= 64) must read as 0; with d > 64 every
     // byte is written before it is read.
     // (FP8: the decoders write every byte of every operand buffer.)
-    if (!FP8 && (kboxes < 2 || vboxes < 2))
-        for (int i = threadIdx.x; i < (NST * L::ST_BYTES + NBK * L::BK_BYTES) / 16; i += THREADS)
+    if (!LP && (kboxes < 2 || vboxes < 2))
+        for (int i = threadIdx.x; i < (NST * L::ST_BYTES + NBK * L::BK_BYTES) / 16; i += blockDim.x)
             reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], FP8 ? SCALER_THREADS : 1);
+            mbar_init(&empty[s], LP ? SCALER_THREADS : 1);
         }
         for (int b = 0; b < NBK; ++b) {
             mbar_init(&bk_full[b], SCALER_THREADS);
@@ -260,6 +305,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                         mbar_arrive_expect_tx(&full[stage], STAGE8_BYTES);
                         tma_load_4d(st, &tm_k, &full[stage], 0, h, c * CHUNK, frame);
                         tma_load_4d(st + BOX8_BYTES, &tm_v, &full[stage], 0, h, c * CHUNK, frame);
+                    } else if constexpr (FP4) {
+                        mbar_arrive_expect_tx(&full[stage], CHUNK * (p.dk / 2 + p.dv / 2));
+                        tma_load_4d(st, &tm_k, &full[stage], 0, h, c * CHUNK, frame);
+                        tma_load_4d(st + RAW4_BYTES, &tm_v, &full[stage], 0, h, c * CHUNK, frame);
                     } else {
                         mbar_arrive_expect_tx(&full[stage], (kboxes + vboxes) * BOX_BYTES);
                         for (int bx = 0; bx < kboxes; ++bx)
@@ -280,7 +329,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t IDESC = FP8 ? idesc_f16(128, 256, 1, 1) : idesc_bf16(128, 256, 1, 1);
+            constexpr uint32_t IDESC = LP ? idesc_f16(128, 256, 1, 1) : idesc_bf16(128, 256, 1, 1);
             int stage = 0, bk = 0;
             uint32_t phase = 0, bk_phase = 0;
             int acc = 0;
@@ -292,7 +341,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
                 bool ok = true;
                 for (int c = u.c_begin; c < u.c_end; ++c) {
-                    if ((!FP8 && !mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag)) ||
+                    if ((!LP && !mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag)) ||
                         !mbar_wait(&bk_full[bk], bk_phase, p.wait_limit_ns, abort_flag)) {
                         ok = false;
                         break;
@@ -301,14 +350,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // A = beta*K (FP8: sqrt(beta) K); B = [K | V] from the TMA stage, or (FP8)
                     // [sqrt(beta) K | sqrt(beta) V], the same buffer as A
                     const uint32_t a_base = smem_u32(bk_base + bk * L::BK_BYTES);
-                    const uint32_t b_base = FP8 ? a_base : smem_u32(stage_base + stage * L::ST_BYTES);
+                    const uint32_t b_base = LP ? a_base : smem_u32(stage_base + stage * L::ST_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < CHUNK / 16; ++kk) {
                         const uint64_t ad = smem_desc(a_base + kk * 2048, MN_LBO, MN_SBO);
                         const uint64_t bd = smem_desc(b_base + kk * 2048, MN_LBO, MN_SBO);
                         mma_bf16(d_tmem, ad, bd, IDESC, (c > u.c_begin || kk > 0) ? 1u : 0u);
                     }
-                    if (!FP8) mma_commit(&empty[stage]);
+                    if (!LP) mma_commit(&empty[stage]);
                     mma_commit(&bk_empty[bk]);
                     if (++bk == NBK) { bk = 0; bk_phase ^= 1; }
                     if (++stage == NST) { stage = 0; phase ^= 1; }
@@ -334,13 +383,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         int pslot = 0;
         auto beta_prefetch = [&]() {
             float* dst = beta_ring + pslot * SCALER_THREADS + t;
+            uint32_t* sdst = sf_ring + (pslot * SCALER_THREADS + t) * 2;
             if (pw < w_end) {
                 const Unit u = unit_of(p, pw);
                 const int tok = pc * CHUNK + r;
+                const size_t row = (static_cast<size_t>(u.item / p.H) * p.N + tok) * p.H + (u.item % p.H);
                 if (tok < p.N)
-                    cp_async_4(dst, p.beta + (static_cast<size_t>(u.item / p.H) * p.N + tok) * p.H + (u.item % p.H));
+                    cp_async_4(dst, p.beta + row);
                 else
                     *dst = 0.0f;
+                if constexpr (FP4) {
+                    // scale word of this thread's 64 columns (4 scales of 16), if they exist
+                    if (tok < p.N && 64 * bx < p.dk) cp_async_4(sdst, p.k_sf + row * (p.dk / 16) + 4 * bx);
+                    else sdst[0] = 0u;
+                    if (tok < p.N && 64 * bx < p.dv) cp_async_4(sdst + 1, p.v_sf + row * (p.dv / 16) + 4 * bx);
+                    else sdst[1] = 0u;
+                }
                 if (++pc >= u.c_end) {
                     pw += w_step;
                     if (pw < w_end) pc = unit_of(p, pw).c_begin;
@@ -360,6 +418,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 beta_prefetch();                       // chunk BETA_AHEAD ahead
                 cp_async_wait<BETA_AHEAD>();           // this chunk's copy has landed
                 const float bval = beta_ring[cslot * SCALER_THREADS + t];
+                uint32_t ksf = 0, vsf = 0;
+                if constexpr (FP4) {
+                    ksf = sf_ring[(cslot * SCALER_THREADS + t) * 2];
+                    vsf = sf_ring[(cslot * SCALER_THREADS + t) * 2 + 1];
+                }
                 if (++cslot == BETA_AHEAD + 1) cslot = 0;
                 if (!mbar_wait(&full[stage], phase, p.wait_limit_ns, abort_flag) ||
                     !mbar_wait(&bk_empty[bk], bk_phase ^ 1, p.wait_limit_ns, abort_flag)) {
@@ -395,6 +458,48 @@ __global__ void __launch_bounds__(THREADS, 1)
                             vh[2 * wd + 1] = hscale(e4m3x2_to_f16x2(static_cast<uint16_t>(vw[wd] >> 16)), b2);
                         }
                         // columns 16i..16i+15 of box bx = its 16-bit chunks 2i and 2i+1
+                        const int o0 = ((2 * i) ^ (r & 7)) << 4, o1 = ((2 * i + 1) ^ (r & 7)) << 4;
+                        *reinterpret_cast<uint4*>(dst + o0) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
+                        *reinterpret_cast<uint4*>(dst + o1) = make_uint4(kh[4], kh[5], kh[6], kh[7]);
+                        *reinterpret_cast<uint4*>(dst + TILE_BYTES + o0) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
+                        *reinterpret_cast<uint4*>(dst + TILE_BYTES + o1) = make_uint4(vh[4], vh[5], vh[6], vh[7]);
+                    }
+                } else if constexpr (FP4) {
+                    // Thread pair (2r, 2r+1) owns token row r; this thread decodes the
+                    // row's 64 columns of box bx: e2m1 codes (bytes 32bx..32bx+31 of
+                    // the row, two per byte) times their E4M3 block scale (one per 16
+                    // columns), exactly in f16, then times sqrt(beta) split hi + lo.
+                    if (!(bval >= 0.0f && bval <= FP4_BETA_MAX)) record_error(GDN_ERR_RANGE);
+                    const uint8_t* st = stage_base + stage * L::ST_BYTES;
+                    uint8_t* dst = bk_base + bk * L::BK_BYTES + bx * BOX_BYTES + r * 128;
+                    const HSplit b2 = hsplit(sqrtf(fmaxf(bval, 0.0f)));
+                    const bool kin = 64 * bx < p.dk, vin = 64 * bx < p.dv;
+                    uint32_t kw[8], vw[8];
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const uint4 kx = kin ? *reinterpret_cast<const uint4*>(st + r * (p.dk / 2) + 32 * bx + 16 * q)
+                                             : make_uint4(0, 0, 0, 0);
+                        const uint4 vx = vin ? *reinterpret_cast<const uint4*>(st + RAW4_BYTES + r * (p.dv / 2) +
+                                                                                 32 * bx + 16 * q)
+                                             : make_uint4(0, 0, 0, 0);
+                        kw[4 * q] = kx.x; kw[4 * q + 1] = kx.y; kw[4 * q + 2] = kx.z; kw[4 * q + 3] = kx.w;
+                        vw[4 * q] = vx.x; vw[4 * q + 1] = vx.y; vw[4 * q + 2] = vx.z; vw[4 * q + 3] = vx.w;
+                    }
+#pragma unroll
+                    for (int i0 = 0; i0 < 4; ++i0) {
+                        const int i = bx ? (i0 ^ 2) : i0;    // columns 16i..16i+15 of box bx
+                        const uint32_t ks2 = e4m3_to_f16x2_bcast(ksf >> (8 * i));
+                        const uint32_t vs2 = e4m3_to_f16x2_bcast(vsf >> (8 * i));
+                        uint32_t kh[8], vh[8];
+                        fp4x8_to_f16(kw[2 * i], ks2, *reinterpret_cast<uint32_t(*)[4]>(&kh[0]));
+                        fp4x8_to_f16(kw[2 * i + 1], ks2, *reinterpret_cast<uint32_t(*)[4]>(&kh[4]));
+                        fp4x8_to_f16(vw[2 * i], vs2, *reinterpret_cast<uint32_t(*)[4]>(&vh[0]));
+                        fp4x8_to_f16(vw[2 * i + 1], vs2, *reinterpret_cast<uint32_t(*)[4]>(&vh[4]));
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            kh[e] = hscale(kh[e], b2);
+                            vh[e] = hscale(vh[e], b2);
+                        }
                         const int o0 = ((2 * i) ^ (r & 7)) << 4, o1 = ((2 * i + 1) ^ (r & 7)) << 4;
                         *reinterpret_cast<uint4*>(dst + o0) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
                         *reinterpret_cast<uint4*>(dst + o1) = make_uint4(kh[4], kh[5], kh[6], kh[7]);
@@ -451,14 +556,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&bk_full[bk]);
-                if (FP8) mbar_arrive(&empty[stage]);   // the decoders were the stage's last readers
+                if (LP) mbar_arrive(&empty[stage]);    // the decoders were the stage's last readers
                 if (++bk == NBK) { bk = 0; bk_phase ^= 1; }
                 if (++stage == NST) { stage = 0; phase ^= 1; }
             }
             if (!ok) break;
         }
         cp_async_wait<0>();  // no copy into the beta ring may outlive the CTA
-    } else {
+    } else if (warp < EPI_WARP0 + 4) {
         // ----------------------------------------------------------- epilogue
         const int quarter = warp & 3;       // warps EPI_WARP0..EPI_WARP0+3 cover the four lane quarters
         const int j = quarter * 32 + lane;  // TMEM lane = row j of (beta K)^T = dk index
@@ -468,8 +573,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         // the named barriers of the split-item fixup below can never be left waiting.
         for (int w = w_begin; w < w_end; w += w_step) {
             const Unit u = unit_of(p, w);
-            const bool ok = bar_and(1, 128, mbar_wait(&tfull[acc], acc_phase, p.wait_limit_ns, abort_flag));
-            if (!ok) break;
+            bool ok = mbar_wait(&tfull[acc], acc_phase, p.wait_limit_ns, abort_flag, 2010000 + (w & 0xffff));
+            // ring mode: the scan has read the slot's previous frame (one scan CTA per head)
+            if (ok && u.slot >= 0 && u.use > 0 && j == 0)
+                ok = wait_count_geq(p.au_free + u.slot, u.use, p.wait_limit_ns, abort_flag, 2020000 + (w & 0xffff));
+            if (!bar_and(1, 128, ok)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(quarter * 32) << 16);
             const bool jv = j < p.dk;
@@ -478,6 +586,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // partial sums in the same element order
             float* part = u.split < 0 ? nullptr
                                       : p.partial + (static_cast<size_t>(u.item - p.whole) * p.split_per + u.split) * per;
+            const size_t dst = static_cast<size_t>(u.slot >= 0 ? u.slot : u.item);   // A/U destination
             {
                 // A: row j of D holds A[j][0..dk); stored as row j (A is symmetric)
                 for (int c0 = 0; c0 < p.dk; c0 += 32) {
@@ -485,12 +594,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tmem_ld32(tbase + c0, r32);
                     tmem_wait_ld();
                     if (!jv) continue;
-                    if (FP8) {
+                    if (LP) {
 #pragma unroll
                         for (int t = 0; t < 32; ++t) r32[t] = __float_as_uint(__uint_as_float(r32[t]) * p.a_scale);
                     }
                     if (part == nullptr) {
-                        __nv_bfloat16* Arow = p.A_ws + (static_cast<size_t>(u.item) * p.dk + j) * p.dk;
+                        __nv_bfloat16* Arow = p.A_ws + (dst * p.dk + j) * p.dk;
 #pragma unroll
                         for (int q8 = 0; q8 < 4; ++q8) {
                             uint4 v4 = make_uint4(
@@ -510,13 +619,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
                 // U: row j of D holds U[0..dv)[j]; coalesced along j
-                float* Uout = part == nullptr ? p.U_ws + static_cast<size_t>(u.item) * p.dv * p.dk
+                float* Uout = part == nullptr ? p.U_ws + dst * p.dv * p.dk
                                               : part + static_cast<size_t>(p.dk) * p.dk;
                 for (int c0 = 0; c0 < p.dv; c0 += 32) {
                     uint32_t r32[32];
                     tmem_ld32(tbase + 128 + c0, r32);
                     tmem_wait_ld();
-                    if (FP8) {
+                    if (LP) {
 #pragma unroll
                         for (int t = 0; t < 32; ++t) r32[t] = __float_as_uint(__uint_as_float(r32[t]) * p.u_scale);
                     }
@@ -530,6 +639,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            if (u.slot >= 0) {
+                // ring mode: every epilogue thread's stores, then one release (read
+                // by the scan's copies through the async proxy after its acquire)
+                fence_proxy_async_global();
+                __threadfence();
+                named_bar_sync(1, 128);
+                if (j == 0) red_release_add(p.au_ready + u.slot, 1);
+            }
             if (part != nullptr) {
                 // Split item: once every split of the item has written its
                 // partial sums, each split reduces its own share of the
@@ -600,6 +717,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
+}
+
+// Standalone phase 1: a persistent grid, work units round-robin.
+template <int FMT>
+__global__ void __launch_bounds__(THREADS, 1)
+    contract_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    contract_role<FMT>(tm_k, tm_v, p, blockIdx.x, gridDim.x, smem);
 }
 
 }  // namespace k1

@@ -30,8 +30,8 @@ constexpr size_t smem_bytes() {
     return k2::Cfg<R>::SMEM_BYTES > k3::SMEM_BYTES ? k2::Cfg<R>::SMEM_BYTES : k3::SMEM_BYTES;
 }
 
-template <int R, bool FP8>
-__global__ void __launch_bounds__(k3::threads<FP8>(), 1)
+template <int R, int FMT>
+__global__ void __launch_bounds__(k3::threads<FMT>(), 1)
     scan_output_kernel(const __grid_constant__ CUtensorMap tm_A, const __grid_constant__ CUtensorMap tm_U,
                        const __grid_constant__ CUtensorMap tm_S_store, const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_S_load, const __grid_constant__ CUtensorMap tm_out,
@@ -49,7 +49,9 @@ __global__ void __launch_bounds__(k3::threads<FP8>(), 1)
         sc.fused = true;
         sc.flags = flags;
         sc.flag_target = p2.rsplit;
-        k3::output_role<FP8>(&tm_q, &tm_S_load, &tm_out, p3, sc, smem);
+        sc.ring = 0;
+        sc.s_free = nullptr;
+        k3::output_role<FMT>(&tm_q, &tm_S_load, &tm_out, p3, sc, smem);
     }
 }
 

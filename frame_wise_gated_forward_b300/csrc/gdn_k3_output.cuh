@@ -55,8 +55,8 @@ constexpr int BAR_BYTES = 256;
 // reads its raw row whole before writing, and box 1's row is exactly the raw
 // row it came from, so no thread overwrites bytes another one still reads.
 constexpr int DEC_THREADS = 128;
-template <bool FP8>
-constexpr int threads() { return FP8 ? 192 + DEC_THREADS : THREADS; }
+template <int FMT>
+__host__ __device__ constexpr int threads() { return FMT != FMT_BF16 ? 192 + DEC_THREADS : THREADS; }
 constexpr int RAW_BYTES = TILE_M * 128;
 static_assert(RAW_BYTES == BOX_BYTES, "a raw fp8 tile fills box 1 of a q slot");
 static_assert((3 * QSTAGES + 2 * SSTAGES + 2 * ACCS + 1 + 2 * NSLOTS) * 8 + 8 <= BAR_BYTES, "barrier area");
@@ -70,7 +70,8 @@ struct Params {
     long long total;        // items * ntile
     int reverse;            // fused schedule: follow a scan that runs from frame F-1 down
     int norm_q;             // fused prologue: scale each output row by 1/max(|q_n|, eps)
-    float q_scale;          // fp8 q: o_n = q_scale * S q8_n  (1 otherwise)
+    float q_scale;          // fp8 / NVFP4 q: o_n = q_scale * S q_n (q decoded without it; 1 otherwise)
+    const uint8_t* q_sf;    // NVFP4 q: E4M3 block scales [B, F, N, H, dk/16]
     int b_mn;               // 0: O = Q S^T (S K-major).  1: O = Q S with S read MN-major, for the
                             // backward's dq = dO S_f: then dk is dO's width (dv of S) and dv the
                             // output width (dk of S)
@@ -84,10 +85,23 @@ struct Sched {
     // fused: worker wi of nw takes frame-major item ranks wi, wi + nw, ...
     int wi, nw;
     bool fused;
-    const int* flags;       // fused: per-item count of published state slices
+    const int* flags;       // fused: per-item (ring: per-slot) count of published state slices
     int flag_target;        // fused: slices per item
+    // ring mode (single-pass forward, 0 = off): the state of scan step s of
+    // head (b, h) sits in slot (b * ring + s % ring) * H + h, which holds frames
+    // s, s + ring, ... in turn; flags count published slices per slot, and
+    // s_free counts this role's loads of each slot's image
+    int ring;
+    int* s_free;
 
     __device__ __forceinline__ bool segment(const Params& p, int k, long long& item, int& nb, int& ne) const {
+        long long slot;
+        int use;
+        return segment(p, k, item, nb, ne, slot, use);
+    }
+    __device__ __forceinline__ bool segment(const Params& p, int k, long long& item, int& nb, int& ne,
+                                            long long& slot, int& use) const {
+        use = 0;
         if (!fused) {
             // k-th segment of the contiguous range: walk items from t0
             long long t = t0;
@@ -97,6 +111,7 @@ struct Sched {
             nb = static_cast<int>(t % p.ntile);
             const long long end = (item + 1) * p.ntile < t1 ? (item + 1) * p.ntile : t1;
             ne = static_cast<int>(end - item * p.ntile);
+            slot = item;
             return true;
         }
         const long long rank = wi + static_cast<long long>(k) * nw;
@@ -111,15 +126,26 @@ struct Sched {
         item = (b * p.F + f) * p.H + h;
         nb = per_tile ? static_cast<int>(rank % p.ntile) : 0;
         ne = per_tile ? nb + 1 : p.ntile;
+        if (ring > 0) {
+            slot = (b * ring + fs % ring) * p.H + h;
+            use = static_cast<int>(fs / ring);
+        } else {
+            slot = item;
+        }
         return true;
     }
 };
 
-// FP8: q is e4m3 (tm_q maps bytes, one 128-column box per token row).
-template <bool FP8>
+// FMT_FP8: q is e4m3 (tm_q maps bytes, one 128-column box per token row).
+// FMT_FP4: q is NVFP4 (tm_q maps the packed codes, one box of dk/2 bytes per
+// token row, unswizzled; dk = 64 or 128).
+template <int FMT>
 __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUtensorMap* tm_s,
                                             const CUtensorMap* tm_out, const Params& p, const Sched& sc,
                                             uint8_t* smem) {
+    constexpr bool FP8 = FMT == FMT_FP8;
+    constexpr bool FP4 = FMT == FMT_FP4;
+    constexpr bool LP = FMT != FMT_BF16;
     constexpr int QS = QSTAGES;
     uint8_t* qring = smem;
     uint8_t* sring = qring + QSTAGES * QTILE_BYTES;
@@ -147,14 +173,14 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
     const int sboxes = p.b_mn ? vboxes : kboxes;   // 64-column boxes of the state tile
 
     // never-loaded boxes (dk <= 64) must read as zero
-    if (!FP8 && (kboxes < 2 || sboxes < 2))
-        for (int i = threadIdx.x; i < (QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES) / 16; i += THREADS)
+    if (!LP && (kboxes < 2 || sboxes < 2))
+        for (int i = threadIdx.x; i < (QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES) / 16; i += blockDim.x)
             reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
         // a q slot is released by the MMA commit and, with the folded prologue, by the norm threads
         for (int s = 0; s < QS; ++s) {
             mbar_init(&qfull[s], 1);
-            mbar_init(&qempty[s], 1 + ((!FP8 && p.norm_q) ? NORM_THREADS : 0));
+            mbar_init(&qempty[s], 1 + ((!LP && p.norm_q) ? NORM_THREADS : 0));
             mbar_init(&qdec[s], DEC_THREADS);
         }
         for (int s = 0; s < SSTAGES; ++s) { mbar_init(&sfull[s], 1); mbar_init(&sempty[s], 1); }
@@ -189,27 +215,29 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
             int qs = 0, ss = 0;
             uint32_t qph = 0, sph = 0;
             long long q_issued = 0, s_issued = 0;
-            long long item;
-            int nb, ne;
+            long long item, slot;
+            int nb, ne, use;
             bool stop = false;
-            for (int k = 0; !stop && !*abort_flag && sc.segment(p, k, item, nb, ne); ++k) {
+            for (int k = 0; !stop && !*abort_flag && sc.segment(p, k, item, nb, ne, slot, use); ++k) {
                 const int frame = static_cast<int>(item / p.H), h = static_cast<int>(item % p.H);
                 if (k > 0) { if (++ss == SSTAGES) { ss = 0; sph ^= 1; } }
-                if (!mbar_wait(&sempty[ss], sph ^ 1, p.wait_limit_ns, abort_flag)) break;
+                if (!mbar_wait(&sempty[ss], sph ^ 1, p.wait_limit_ns, abort_flag, 3010000 + (k & 0xffff))) break;
                 if (sc.fused) {
-                    if (!wait_count_geq(sc.flags + item, sc.flag_target, p.wait_limit_ns, abort_flag)) break;
+                    if (!wait_count_geq(sc.flags + slot, (use + 1) * sc.flag_target, p.wait_limit_ns, abort_flag,
+                                        3020000 + (k & 0xffff)))
+                        break;
                     fence_proxy_async_global();  // the published state is read through the async proxy
                 }
                 mbar_arrive_expect_tx(&sfull[ss], sboxes * BOX_BYTES);
                 for (int bx = 0; bx < sboxes; ++bx)
                     tma_load_3d(sring + ss * STILE_BYTES + bx * BOX_BYTES, tm_s, &sfull[ss], 64 * bx, 0,
-                                static_cast<int>(item));
+                                static_cast<int>(slot));
                 ++s_issued;
                 for (int nt = nb; nt < ne; ++nt) {
-                    if constexpr (FP8) {
-                        // raw e4m3 tile into box 1 of the slot, decoded there in place
+                    if constexpr (LP) {
+                        // raw e4m3 / NVFP4 tile into box 1 of the slot, decoded there in place
                         if (!mbar_wait(&qempty[qs], qph ^ 1, p.wait_limit_ns, abort_flag)) { stop = true; break; }
-                        mbar_arrive_expect_tx(&qfull[qs], RAW_BYTES);
+                        mbar_arrive_expect_tx(&qfull[qs], FP8 ? RAW_BYTES : TILE_M * (p.dk / 2));
                         tma_load_4d(qring + qs * QTILE_BYTES + BOX_BYTES, tm_q, &qfull[qs], 0, h, nt * TILE_M,
                                     frame);
                         ++q_issued;
@@ -240,12 +268,16 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
             long long item;
             int nb, ne;
             bool stop = false;
-            for (int k = 0; !stop && !*abort_flag && sc.segment(p, k, item, nb, ne); ++k) {
+            long long slot;
+            int use;
+            for (int k = 0; !stop && !*abort_flag && sc.segment(p, k, item, nb, ne, slot, use); ++k) {
                 if (k > 0) { if (++ss == SSTAGES) { ss = 0; sph ^= 1; } }
-                if (!mbar_wait(&sfull[ss], sph, p.wait_limit_ns, abort_flag)) break;
+                if (!mbar_wait(&sfull[ss], sph, p.wait_limit_ns, abort_flag, 3110000 + (k & 0xffff))) break;
+                // ring mode: the image is in shared memory, the scan may reuse its slot
+                if (sc.ring > 0) red_release_add(sc.s_free + slot, 1);
                 for (int nt = nb; nt < ne; ++nt) {
                     if (!mbar_wait(&tempty[acc], aph ^ 1, p.wait_limit_ns, abort_flag) ||
-                        !mbar_wait(FP8 ? &qdec[qs] : &qfull[qs], qph, p.wait_limit_ns, abort_flag)) {
+                        !mbar_wait(LP ? &qdec[qs] : &qfull[qs], qph, p.wait_limit_ns, abort_flag)) {
                         stop = true;
                         break;
                     }
@@ -269,8 +301,76 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
             mma_commit(final_bar);
             mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
         }
-    } else if (warp >= 6) {
-        if constexpr (FP8) {
+    } else if (warp >= 6 && warp < threads<FMT>() / 32) {
+        if constexpr (FP4) {
+            // --------------------------------------------- NVFP4 q decoders
+            // Thread t owns token row t of each tile: its dk/2 raw bytes sit in
+            // box 1 of the slot, packed (row pitch dk/2), so rows of different
+            // threads overlap the decoded rows: every decoder reads its raw row
+            // into registers, all meet at a named barrier, then each writes row t
+            // of boxes 0 and 1 (bf16, K-major, 128-byte swizzle).  e2m1 times the
+            // E4M3 block scale is exact in f16 and in bf16.  The row's block
+            // scales (dk/16 bytes) are loaded one tile ahead.
+            const int t = threadIdx.x - 192;
+            const int nsc = p.dk / 16;                 // 4 or 8 scales per row
+            int qs = 0;
+            uint32_t qph = 0;
+            long long item;
+            int nb, ne;
+            int k = 0;
+            bool have = sc.segment(p, 0, item, nb, ne);
+            int nt = nb;
+            auto load_sf = [&](long long it, int ntile) -> uint2 {
+                const int tok = ntile * TILE_M + t;
+                if (tok >= p.N) return make_uint2(0u, 0u);
+                const size_t row = (static_cast<size_t>(it / p.H) * p.N + tok) * p.H + (it % p.H);
+                if (nsc == 8) return __ldg(reinterpret_cast<const uint2*>(p.q_sf + row * 8));
+                return make_uint2(__ldg(reinterpret_cast<const uint32_t*>(p.q_sf + row * 4)), 0u);
+            };
+            uint2 sf_cur = have ? load_sf(item, nt) : make_uint2(0u, 0u);
+            while (have && !*abort_flag) {
+                // the next tile of this CTA, and its scales (consumed next round)
+                long long item2 = item;
+                int nt2 = nt + 1, nb2 = nb, ne2 = ne, k2 = k;
+                bool have2 = true;
+                if (nt2 >= ne) {
+                    k2 = k + 1;
+                    have2 = sc.segment(p, k2, item2, nb2, ne2);
+                    nt2 = nb2;
+                }
+                const uint2 sf_next = have2 ? load_sf(item2, nt2) : make_uint2(0u, 0u);
+                if (!bar_and(2, DEC_THREADS, mbar_wait(&qfull[qs], qph, p.wait_limit_ns, abort_flag))) break;
+                uint8_t* tile = qring + qs * QTILE_BYTES;
+                uint32_t w[16];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    if (q4 * 32 < p.dk) {
+                        const uint4 x = *reinterpret_cast<const uint4*>(tile + BOX_BYTES + t * (p.dk / 2) + 16 * q4);
+                        w[4 * q4] = x.x; w[4 * q4 + 1] = x.y; w[4 * q4 + 2] = x.z; w[4 * q4 + 3] = x.w;
+                    }
+                }
+                named_bar_sync(2, DEC_THREADS);   // every raw row has been read
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {     // 16 columns 16g..16g+15: raw words 2g, 2g+1
+                    if (g < nsc) {
+                        const uint32_t s2 = e4m3_to_f16x2_bcast((g < 4 ? sf_cur.x : sf_cur.y) >> (8 * (g & 3)));
+                        uint32_t h[8];
+                        fp4x8_to_f16(w[2 * g], s2, *reinterpret_cast<uint32_t(*)[4]>(&h[0]));
+                        fp4x8_to_f16(w[2 * g + 1], s2, *reinterpret_cast<uint32_t(*)[4]>(&h[4]));
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) h[e] = f16x2_to_bf16x2_exact(h[e]);
+                        uint8_t* rowp = tile + (g >> 2) * BOX_BYTES + t * 128;
+                        const int c8 = 2 * (g & 3);
+                        *reinterpret_cast<uint4*>(rowp + ((c8 ^ (t & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+                        *reinterpret_cast<uint4*>(rowp + (((c8 + 1) ^ (t & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&qdec[qs]);
+                if (++qs == QS) { qs = 0; qph ^= 1; }
+                item = item2; nt = nt2; nb = nb2; ne = ne2; k = k2; have = have2; sf_cur = sf_next;
+            }
+        } else if constexpr (FP8) {
             // ------------------------------------------------ e4m3 q decoders
             // row t of each raw tile (box 1 of the slot): 8 chunks of 16 columns,
             // all read first, then decoded exactly to bf16 into row t of the
@@ -359,7 +459,7 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
                 }
             }
         }
-    } else {
+    } else if (warp >= 2 && warp < 6) {
         // ----------------------------------------------------------- epilogue
         const int quarter = warp & 3;
         uint8_t* my_stage = ostage + quarter * 2 * OSTAGE_BYTES;
@@ -373,8 +473,8 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
             const int frame = static_cast<int>(item / p.H), h = static_cast<int>(item % p.H);
             for (int nt = nb; nt < ne; ++nt) {
                 // fused prologue: o_n = S q_n / max(|q_n|, eps), norms from the norm warps
-                float rs = FP8 ? p.q_scale : 1.0f;
-                if (!FP8 && p.norm_q) {
+                float rs = LP ? p.q_scale : 1.0f;
+                if (!LP && p.norm_q) {
                     const bool okn =
                         __all_sync(0xffffffffu, mbar_wait(&nready[ns], nph, p.wait_limit_ns, abort_flag));
                     if (!okn) { stop = true; break; }
@@ -443,8 +543,8 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
 }
 
 // Standalone phase 3: persistent grid, contiguous tile ranges.
-template <bool FP8>
-__global__ void __launch_bounds__(threads<FP8>(), 1)
+template <int FMT>
+__global__ void __launch_bounds__(threads<FMT>(), 1)
     output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
                   const __grid_constant__ CUtensorMap tm_out, const Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -457,7 +557,9 @@ __global__ void __launch_bounds__(threads<FP8>(), 1)
     sc.fused = false;
     sc.flags = nullptr;
     sc.flag_target = 0;
-    output_role<FP8>(&tm_q, &tm_s, &tm_out, p, sc, smem);
+    sc.ring = 0;
+    sc.s_free = nullptr;
+    output_role<FMT>(&tm_q, &tm_s, &tm_out, p, sc, smem);
 }
 
 }  // namespace k3

@@ -13,12 +13,33 @@
 
 namespace gdn {
 
+// Element formats of q, k and v: bf16; OCP FP8 E4M3 with one scale per tensor;
+// NVFP4 (E2M1 elements, one E4M3 scale per 16 along the head dimension, one
+// fp32 scale per tensor).
+enum : int { FMT_BF16 = 0, FMT_FP8 = 1, FMT_FP4 = 2 };
+
 // First error any kernel recorded on this device (0 = none).  Read and
 // cleared by gdn_sync_status().  The library is one translation unit
 // (gdn_api.cu includes every kernel header), so this is its only definition.
 __device__ int g_error = 0;
 
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_error, 0, code); }
+
+// Where the first bounded wait that ran out gave up: {site, block, thread,
+// value seen, value awaited} (site 0 = a wait without a site number).  Read
+// and cleared by gdn_debug_last_timeout().
+__device__ int g_timeout_info[5] = {0, 0, 0, 0, 0};
+__device__ int g_timeout_taken = 0;
+__device__ __forceinline__ void record_timeout(int site, int seen, int awaited) {
+    if (atomicCAS(&g_timeout_taken, 0, 1) == 0) {
+        g_timeout_info[0] = site;
+        g_timeout_info[1] = static_cast<int>(blockIdx.x);
+        g_timeout_info[2] = static_cast<int>(threadIdx.x);
+        g_timeout_info[3] = seen;
+        g_timeout_info[4] = awaited;
+    }
+    record_error(GDN_ERR_TIMEOUT);
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -61,14 +82,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // exceeds `limit_ns`; in the latter case GDN_ERR_TIMEOUT is recorded and the
 // abort flag is raised so that every other role of the CTA drains quickly.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag, int site = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
-            record_error(GDN_ERR_TIMEOUT);
+            record_timeout(site, -1, static_cast<int>(parity));
             *abort_flag = 1;
             return false;
         }
@@ -83,7 +104,7 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
         if (globaltimer_ns() - t0 > limit_ns) {
-            record_error(GDN_ERR_TIMEOUT);
+            record_timeout(-1, -1, static_cast<int>(parity));
             return;
         }
     }
@@ -178,7 +199,7 @@ __device__ __forceinline__ void red_release_add(int* p, int v) {
 // visible.  Gives up after limit_ns, or when `abort_flag` is raised, recording
 // GDN_ERR_TIMEOUT and raising the flag itself on a timeout.
 __device__ __forceinline__ bool wait_count_geq(const int* p, int target, uint64_t limit_ns,
-                                               volatile int* abort_flag) {
+                                               volatile int* abort_flag, int site = 0) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     if (v >= target) return true;
@@ -189,7 +210,7 @@ __device__ __forceinline__ bool wait_count_geq(const int* p, int target, uint64_
         if (v >= target) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
-            record_error(GDN_ERR_TIMEOUT);
+            record_timeout(site, v, target);
             *abort_flag = 1;
             return false;
         }
@@ -308,6 +329,18 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
+// 32 lanes x 32 consecutive 32-bit columns, the store counterpart of tmem_ld32
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading /
@@ -357,6 +390,43 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
     const uint32_t x = e4m3x2_to_f16x2(two);
     const uint32_t y = (x >> 3) & 0x0fff0fffu;                      // exponent and mantissa per half
     const uint32_t nz = ((y + 0x0fff0fffu) >> 12) & 0x00010001u;    // 1 in each nonzero half
+    return (y + nz * 0x3800u) | (x & 0x80008000u);
+}
+
+// Two FP4 E2M1 codes in one byte (the lower-indexed element in the low
+// nibble) -> f16x2 (that element in the low half), exactly: every e2m1 value
+// is an f16 value.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+    uint32_t h2;
+    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(h2) : "r"(byte));
+    return h2;
+}
+
+// One E4M3 code -> the f16x2 holding its value in both halves (exact).
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_bcast(uint32_t code) {
+    return e4m3x2_to_f16x2(static_cast<uint16_t>((code & 0xffu) * 0x0101u));
+}
+
+// Four consecutive bytes of NVFP4 codes (8 elements) times their block scale
+// (f16x2, both halves equal) -> four f16x2 words, elements in order.  The
+// product of an e2m1 value (at most 2 significant bits) and an e4m3 scale (at
+// most 4) has at most 6 significant bits and lies in [2^-10, 2688]: exact in
+// f16 (and in bf16).
+__device__ __forceinline__ void fp4x8_to_f16(uint32_t word, uint32_t scale2, uint32_t (&h)[4]) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const uint32_t x = e2m1x2_to_f16x2((word >> (8 * b)) & 0xffu);
+        const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&x), *reinterpret_cast<const __half2*>(&scale2));
+        h[b] = *reinterpret_cast<const uint32_t*>(&r);
+    }
+}
+
+// f16x2 -> bf16x2 by integer rebiasing, exact for values with at most 8
+// significant bits that are zero or normal in f16 (|x| >= 2^-14): per half
+//     bf16 = sign | ((f16 & 0x7fff) >> 3) + (nonzero ? (127 - 15) << 7 : 0)
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2_exact(uint32_t x) {
+    const uint32_t y = (x >> 3) & 0x0fff0fffu;
+    const uint32_t nz = ((y + 0x0fff0fffu) >> 12) & 0x00010001u;
     return (y + nz * 0x3800u) | (x & 0x80008000u);
 }
 

@@ -1,0 +1,342 @@
+// gdn_scan_head.cuh -- the sequential scan of the frame-wise GDN forward with
+// one CTA per (b, h) head, for the single-pass forward (gdn_fwd_single.cuh):
+//     S_f = alpha_f * (S_{f-1} - S_{f-1} A_f) + U_f
+// (SANA-WM article, "The Architecture": a fixed-size state matrix updated
+// once per latent frame by a decay gate and a delta-rule correction; wispaper
+// summary, "Methodology" 1: frames scanned one by one).
+//
+// The state's rows live in tensor-memory lanes: lane i holds row i of the
+// fp32 master state (columns [128, 256)) and row i of C = S_img A_f (columns
+// [0, 128)), where S_img is the bf16 image of the state before the frame.
+// Per frame one MMA chain on the tensor core
+//     D[i][j] = sum_k S_img[i][k] A_f[k][j]      M = 128 (i), N = 128 (j), K = dk
+// reads S_img (K-major: row i, k contiguous) and A_f (row j of the symmetric
+// A_f, also K-major) from 128-byte-swizzled shared memory.  Eight compute
+// warps update the state: warp w owns the lanes (rows) of quarter w % 4 and
+// the 64 columns of half w / 4, so each thread reads its row of C and S from
+// tensor memory, its row of U_f from the TMA-loaded tile, writes the new fp32
+// row back to tensor memory and its bf16 row into the image with 16-byte
+// stores.  One image buffer suffices: the image is rewritten only after the
+// MMA that reads it has retired and the TMA store that publishes it has read
+// it.
+//
+// A_f and U_f come from ring slots of the workspace that contraction CTAs of
+// the same launch fill (a per-slot count of frames written, raised with
+// release semantics after the slot's stores); the loader warp waits (bounded,
+// acquire) for the count, then copies the slot by TMA.  Once the copy has
+// landed the MMA warp hands the slot back (a count of frames read).  The
+// publisher warp stores each frame's image into the ring slot of the output
+// CTAs, after they have loaded the slot's previous occupant, and raises the
+// slot's ready count once the store has completed.
+//
+// Warp roles (352 threads): warps 0-7 compute, warp 8 loads A_f / U_f, warp 9
+// issues the MMAs, warp 10 publishes the images.  The image of the initial
+// state has a barrier of its own, so the publisher's phase count starts with
+// the image after frame 0.
+#pragma once
+
+#include "gdn_ptx.cuh"
+
+namespace gdn {
+namespace k2h {
+
+constexpr int COMPUTE_THREADS = 256;
+constexpr int LOADER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr int PUB_WARP = 10;
+constexpr int THREADS = 352;
+constexpr int AS = 2;                      // A_f / U_f stages
+constexpr int ABOX = 128 * 128;            // 128 rows x 128 B (64 bf16)
+constexpr int ATILE = 2 * ABOX;            // A_f bf16 [128][128], two 64-column boxes
+constexpr int UBOX = 128 * 128;            // 128 rows x 32 fp32
+constexpr int UTILE = 4 * UBOX;            // U_f fp32 [128][128], four 32-column boxes
+constexpr int STAGE = ATILE + UTILE;
+constexpr int OFF_IMG = AS * STAGE;        // bf16 image of the state, two 64-column boxes
+constexpr int OFF_BAR = OFF_IMG + ATILE;
+constexpr int BAR_BYTES = 256;
+constexpr size_t SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t T_C = 0;                // C = S_img A_f
+constexpr uint32_t T_S = 128;              // fp32 master state
+
+struct Params {
+    const float* alpha;     // [B, F, H]
+    const float* state_in;  // [B, H, dv, dk] or nullptr
+    float* state_out;       // [B, H, dv, dk] or nullptr
+    int B, H, F, dk, dv;
+    int reverse;            // scan the frames from F-1 down to 0
+    int alpha_gate;         // fused prologue: alpha <- exp(-softplus(alpha) * alpha_scale)
+    float alpha_scale;
+    int ring;               // W: ring slots per (b, h); step s of the scan uses slot s % W
+    const int* au_ready;    // [B][W][H] frames of A/U written into the slot
+    int* au_free;           // [B][W][H] frames of A/U read out of the slot
+    int* s_ready;           // [B][W][H] frames of state images stored into the slot
+    const int* s_free;      // [B][W][H] loads of the slot's image by output CTAs
+    int s_units;            // output CTA loads per image
+    unsigned long long wait_limit_ns;
+};
+
+__device__ __forceinline__ float decay_gate(const Params& p, float x) {
+    if (!p.alpha_gate) return x;
+    const float sp = x > 20.0f ? x : log1pf(expf(x));  // softplus
+    return expf(-sp * p.alpha_scale);
+}
+
+// byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled box
+__device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + (((c ^ (r & 7))) << 4); }
+
+// The scan of head `cta` = b * H + h.  Needs THREADS threads.
+__device__ __forceinline__ void scan_head_role(const CUtensorMap* tm_A, const CUtensorMap* tm_U,
+                                               const CUtensorMap* tm_S, const Params& p, int cta, uint8_t* smem) {
+    uint8_t* ring = smem;
+    uint8_t* img = smem + OFF_IMG;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* afull = bars;                 // [AS] loader -> compute, MMA
+    uint64_t* slot_free = afull + AS;       // [AS] compute -> loader
+    uint64_t* mma_done = slot_free + AS;    // MMA -> compute
+    uint64_t* img_init = mma_done + 1;      // compute -> MMA: the image of the state before frame 0
+    uint64_t* img_ready = img_init + 1;     // compute -> MMA, publisher: the image after frame f
+    uint64_t* img_free = img_ready + 1;     // publisher -> compute
+    uint64_t* final_bar = img_free + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int b = cta / p.H, h = cta % p.H;
+    const int aboxes = p.dk > 64 ? 2 : 1;
+    const int uboxes = (p.dk + 31) / 32;
+    const int nk = (p.dk + 15) / 16;
+    auto fr = [&](int s) { return p.reverse ? p.F - 1 - s : s; };
+    auto rslot = [&](int s) { return (b * p.ring + s % p.ring) * p.H + h; };
+
+    // boxes of A_f and U_f that are never loaded (dk < 128) must read as zero
+    if (p.dk < 128)
+        for (int i = tid; i < AS * STAGE / 16; i += blockDim.x) reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
+    if (tid == 0) {
+        for (int s = 0; s < AS; ++s) {
+            mbar_init(&afull[s], 1);
+            mbar_init(&slot_free[s], COMPUTE_THREADS);
+        }
+        mbar_init(mma_done, 1);
+        mbar_init(img_init, COMPUTE_THREADS);
+        mbar_init(img_ready, COMPUTE_THREADS);
+        mbar_init(img_free, 1);
+        mbar_init(final_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(tm_A);
+        prefetch_tmap(tm_U);
+        prefetch_tmap(tm_S);
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 8) {
+        // ---------------------------------------------------------- compute
+        const int i = (warp & 3) * 32 + lane;           // state row = TMEM lane
+        const int ch = warp >> 2;                       // column half
+        const uint32_t tw = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const size_t srow = ((static_cast<size_t>(b) * p.H + h) * p.dv + i) * p.dk;
+        const bool iv = i < p.dv;
+        // the state before frame 0: fp32 into TMEM, bf16 into the image
+#pragma unroll
+        for (int sc = 0; sc < 2; ++sc) {
+            const int c0 = 64 * ch + 32 * sc;
+            uint32_t v[32];
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (p.state_in != nullptr && iv && c0 + 4 * q4 < p.dk)
+                    x = *reinterpret_cast<const float4*>(p.state_in + srow + c0 + 4 * q4);
+                v[4 * q4] = __float_as_uint(x.x);
+                v[4 * q4 + 1] = __float_as_uint(x.y);
+                v[4 * q4 + 2] = __float_as_uint(x.z);
+                v[4 * q4 + 3] = __float_as_uint(x.w);
+            }
+            tmem_st32(tw + T_S + c0, v);
+            uint8_t* row = img + (c0 >> 6) * ABOX;
+            const int cb = (c0 & 63) >> 3;
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                *reinterpret_cast<uint4*>(row + sw128(i, cb + t)) = make_uint4(
+                    pack_bf16x2(__uint_as_float(v[8 * t + 0]), __uint_as_float(v[8 * t + 1])),
+                    pack_bf16x2(__uint_as_float(v[8 * t + 2]), __uint_as_float(v[8 * t + 3])),
+                    pack_bf16x2(__uint_as_float(v[8 * t + 4]), __uint_as_float(v[8 * t + 5])),
+                    pack_bf16x2(__uint_as_float(v[8 * t + 6]), __uint_as_float(v[8 * t + 7])));
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(img_init);   // the initial image (never published)
+        float a_next = decay_gate(p, __ldg(p.alpha + static_cast<size_t>(b * p.F + fr(0)) * p.H + h));
+        int f = 0;
+        for (; f < p.F; ++f) {
+            const int slot = f % AS;
+            const float a_f = a_next;
+            if (f + 1 < p.F) a_next = decay_gate(p, __ldg(p.alpha + static_cast<size_t>(b * p.F + fr(f + 1)) * p.H + h));
+            bool ok = mbar_wait(&afull[slot], static_cast<uint32_t>((f / AS) & 1), p.wait_limit_ns, abort_flag,
+                                1010000 + f);
+            ok = ok && mbar_wait(mma_done, static_cast<uint32_t>(f & 1), p.wait_limit_ns, abort_flag, 1020000 + f);
+            // the image may be rewritten once the store of the previous one has read it
+            ok = ok && (f == 0 || mbar_wait(img_free, static_cast<uint32_t>((f - 1) & 1), p.wait_limit_ns, abort_flag,
+                                            1030000 + f));
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const uint8_t* ut = ring + slot * STAGE + ATILE;
+#pragma unroll
+            for (int sc = 0; sc < 2; ++sc) {
+                const int c0 = 64 * ch + 32 * sc;
+                uint32_t cc[32], ss[32];
+                tmem_ld32(tw + T_C + c0, cc);
+                tmem_ld32(tw + T_S + c0, ss);
+                float4 u[8];
+                const uint8_t* ub = ut + (c0 >> 5) * UBOX;
+#pragma unroll
+                for (int t = 0; t < 8; ++t) u[t] = *reinterpret_cast<const float4*>(ub + sw128(i, t));
+                tmem_wait_ld();
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const float uu[4] = {u[t].x, u[t].y, u[t].z, u[t].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int x = 4 * t + e;
+                        ss[x] = __float_as_uint(a_f * (__uint_as_float(ss[x]) - __uint_as_float(cc[x])) + uu[e]);
+                    }
+                }
+                tmem_st32(tw + T_S + c0, ss);
+                uint8_t* row = img + (c0 >> 6) * ABOX;
+                const int cb = (c0 & 63) >> 3;
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    *reinterpret_cast<uint4*>(row + sw128(i, cb + t)) = make_uint4(
+                        pack_bf16x2(__uint_as_float(ss[8 * t + 0]), __uint_as_float(ss[8 * t + 1])),
+                        pack_bf16x2(__uint_as_float(ss[8 * t + 2]), __uint_as_float(ss[8 * t + 3])),
+                        pack_bf16x2(__uint_as_float(ss[8 * t + 4]), __uint_as_float(ss[8 * t + 5])),
+                        pack_bf16x2(__uint_as_float(ss[8 * t + 6]), __uint_as_float(ss[8 * t + 7])));
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(img_ready);
+            mbar_arrive(&slot_free[slot]);   // U_f read, the MMA that read A_f retired
+        }
+        // tcgen05.ld is warp-collective: every lane loads, only rows < dv are stored
+        if (__all_sync(0xffffffffu, f == p.F) && p.state_out != nullptr) {
+            tc_fence_after();
+#pragma unroll
+            for (int sc = 0; sc < 2; ++sc) {
+                const int c0 = 64 * ch + 32 * sc;
+                uint32_t ss[32];
+                tmem_ld32(tw + T_S + c0, ss);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4)
+                    if (iv && c0 + 4 * q4 < p.dk)
+                        *reinterpret_cast<float4*>(p.state_out + srow + c0 + 4 * q4) =
+                            make_float4(__uint_as_float(ss[4 * q4]), __uint_as_float(ss[4 * q4 + 1]),
+                                        __uint_as_float(ss[4 * q4 + 2]), __uint_as_float(ss[4 * q4 + 3]));
+            }
+        }
+    } else if (warp == MMA_WARP) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_bf16(128, 128, 0, 0);
+            for (int f = 0; f < p.F; ++f) {
+                const int slot = f % AS;
+                if (!mbar_wait(&afull[slot], static_cast<uint32_t>((f / AS) & 1), p.wait_limit_ns, abort_flag,
+                               1110000 + f))
+                    break;
+                // the slot's contents are in shared memory: the contraction may refill it
+                red_release_add(p.au_free + rslot(f), 1);
+                // the image of the state before frame f
+                if (!(f == 0 ? mbar_wait(img_init, 0, p.wait_limit_ns, abort_flag, 1120000)
+                             : mbar_wait(img_ready, static_cast<uint32_t>((f - 1) & 1), p.wait_limit_ns, abort_flag,
+                                         1120000 + f)))
+                    break;
+                tc_fence_after();
+                const uint32_t a_base = smem_u32(img);
+                const uint32_t b_base = smem_u32(ring + slot * STAGE);
+                for (int kk = 0; kk < nk; ++kk) {
+                    const uint32_t ko = (kk >> 2) * ABOX + (kk & 3) * 32;
+                    mma_bf16(tmem + T_C, smem_desc(a_base + ko, 16, 1024), smem_desc(b_base + ko, 16, 1024), IDESC,
+                             kk > 0 ? 1u : 0u);
+                }
+                mma_commit(mma_done);
+            }
+            mma_commit(final_bar);
+            mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
+        }
+    } else if (warp == PUB_WARP) {
+        // -------------------------------------------------------- publisher
+        if (lane == 0) {
+            int published = 0;
+            auto publish_upto = [&](int f_end) {
+                if (published >= f_end) return;
+                fence_proxy_async_global();  // the stores' writes ordered before the releases
+                for (; published < f_end; ++published) red_release_add(p.s_ready + rslot(published), 1);
+            };
+            const int sboxes = p.dk > 64 ? 2 : 1;
+            int f = 0;
+            for (; f < p.F; ++f) {
+                if (!mbar_wait(img_ready, static_cast<uint32_t>(f & 1), p.wait_limit_ns, abort_flag, 1210000 + f))
+                    break;
+                // the slot's previous image has been loaded by every output CTA that reads it
+                if (f >= p.ring) {
+                    if (!wait_count_geq(p.s_free + rslot(f), (f / p.ring) * p.s_units, p.wait_limit_ns, abort_flag,
+                                        1220000 + f))
+                        break;
+                    fence_proxy_async_global();
+                }
+                for (int bx = 0; bx < sboxes; ++bx) tma_store_3d(tm_S, img + bx * ABOX, 64 * bx, 0, rslot(f));
+                bulk_commit();
+                bulk_wait_read<0>();
+                mbar_arrive(img_free);
+                bulk_wait<1>();  // the stores of frames <= f - 1 are complete
+                publish_upto(f);
+            }
+            bulk_wait<0>();
+            publish_upto(f);
+        }
+    } else if (warp == LOADER_WARP) {
+        // ----------------------------------------------------------- loader
+        if (lane == 0) {
+            int issued = 0;
+            for (int f = 0; f < p.F; ++f) {
+                const int slot = f % AS;
+                if (f >= AS && !mbar_wait(&slot_free[slot], static_cast<uint32_t>(((f / AS) - 1) & 1),
+                                          p.wait_limit_ns, abort_flag, 1310000 + f))
+                    break;
+                if (!wait_count_geq(p.au_ready + rslot(f), f / p.ring + 1, p.wait_limit_ns, abort_flag, 1320000 + f))
+                    break;
+                fence_proxy_async_global();  // the contraction's stores are read through the async proxy
+                uint8_t* st = ring + slot * STAGE;
+                mbar_arrive_expect_tx(&afull[slot], aboxes * ABOX + uboxes * UBOX);
+                for (int bx = 0; bx < aboxes; ++bx) tma_load_3d(st + bx * ABOX, tm_A, &afull[slot], 64 * bx, 0, rslot(f));
+                for (int c = 0; c < uboxes; ++c)
+                    tma_load_3d(st + ATILE + c * UBOX, tm_U, &afull[slot], 32 * c, 0, rslot(f));
+                ++issued;
+            }
+            for (int k = (issued > AS ? issued - AS : 0); k < issued; ++k)
+                mbar_wait_drain(&afull[k % AS], static_cast<uint32_t>((k / AS) & 1), p.wait_limit_ns);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace k2h
+}  // namespace gdn

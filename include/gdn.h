@@ -75,10 +75,11 @@ typedef enum gdn_status {
  *   state_out  may be NULL (final state not wanted) or equal to state_in
  *              (in-place resident state); it must not partially overlap it.
  *   out        must not overlap q, k, v, alpha, beta or the states.
- * Phases (one launch each, in stream order): frame-parallel contractions
- * A_f = K_f^T B_f K_f and U_f = V_f^T B_f K_f on tcgen05 tensor cores; the
- * sequential scan S_f = alpha_f (S_{f-1} - S_{f-1} A_f) + U_f; the
- * frame-parallel output O_f = Q_f S_f^T on tcgen05 tensor cores.
+ * Phases: frame-parallel contractions A_f = K_f^T B_f K_f and
+ * U_f = V_f^T B_f K_f on tcgen05 tensor cores; the sequential scan
+ * S_f = alpha_f (S_{f-1} - S_{f-1} A_f) + U_f; the frame-parallel output
+ * O_f = Q_f S_f^T on tcgen05 tensor cores.  By default the three run side by
+ * side in one launch (gdn_set_single_pass); otherwise in stream order.
  */
 gdn_status gdn_frame_forward(const void* q, const void* k, const void* v,
                              const float* alpha, const float* beta,
@@ -178,6 +179,44 @@ gdn_status gdn_frame_backward(const void* q, const void* k, const void* v,
                               float* d_state_in,
                               int B, int H, int F, int N, int dk, int dv,
                               gdn_stream_t stream);
+
+/*
+ * Forward with NVFP4 inputs, the format of the distilled SANA-WM variant (the
+ * SANA-WM article, "NVIDIA's New 2.6B World Model...", intro: four sampling
+ * steps with NVFP4 quantization; the pages say no more).  Each of q, k, v is
+ *   codes   uint8 [B, F, N, H, d/2]   two FP4 E2M1 codes per byte, element 2i
+ *                                     in the low nibble (1 sign, 2 exponent
+ *                                     bits with bias 1, 1 mantissa bit)
+ *   scales  uint8 [B, F, N, H, d/16]  one OCP FP8 E4M3 block scale per 16
+ *                                     consecutive elements of a token's head
+ *   gs      one fp32 scale per tensor
+ * and element i of a row is gs * e4m3(scale[i / 16]) * e2m1(code i).  The
+ * recurrence is exactly that of gdn_frame_forward on the decoded values; out
+ * stays bf16 and the state fp32.  The kernels decode in shared memory (the
+ * product of a code and its block scale is exact in f16) and fold the
+ * per-tensor scales into A, U and out, so HBM carries half a byte per input
+ * element plus one byte per 16.  Head sizes dk, dv must be 64 or 128
+ * (GDN_ERR_UNSUPPORTED otherwise); codes and scales 16-byte aligned; every
+ * beta in [0, 512] (the contraction forms sqrt(beta) times values up to
+ * 6 * 448 in f16), anything else is reported as GDN_ERR_RANGE by
+ * gdn_sync_status.  Other validation and errors as gdn_frame_forward.
+ */
+gdn_status gdn_frame_forward_nvfp4(const void* q4, const void* k4, const void* v4,
+                                   const void* q_sf, const void* k_sf, const void* v_sf,
+                                   float q_gs, float k_gs, float v_gs,
+                                   const float* alpha, const float* beta,
+                                   const float* state_in, void* out, float* state_out,
+                                   int B, int H, int F, int N, int dk, int dv,
+                                   gdn_stream_t stream);
+
+/* gdn_frame_step with the NVFP4 inputs of gdn_frame_forward_nvfp4. */
+gdn_status gdn_frame_step_nvfp4(const void* q4, const void* k4, const void* v4,
+                                const void* q_sf, const void* k_sf, const void* v_sf,
+                                float q_gs, float k_gs, float v_gs,
+                                const float* alpha, const float* beta,
+                                const float* state_in, void* out, float* state_out,
+                                int B, int H, int N, int dk, int dv,
+                                gdn_stream_t stream);
 
 /* gdn_frame_step with the 8-bit inputs of gdn_frame_forward_fp8. */
 gdn_status gdn_frame_step_fp8(const void* q, const void* k, const void* v,
@@ -304,6 +343,33 @@ void gdn_set_contract_split(int max_split);
 void gdn_set_fused_step(int on);
 
 /*
+ * The single-pass forward.  on != 0 (default): gdn_frame_forward and its
+ * reverse, folded-prologue and 8-bit variants run a sequence of F >= 2
+ * frames as ONE cooperative launch when the device allows it and B*H is at
+ * most a quarter of the SMs: one CTA per head runs the scan, about 60 % of
+ * the other SMs run the frame-parallel contractions and the rest the output
+ * pass, each frame handed on through small ring buffers of the workspace
+ * that stay in L2 (per-slot counts raised with release semantics, bounded
+ * acquire waits), so HBM carries only the layer's own inputs and outputs.
+ * on = 0: phase 1 as its own launch followed by phases 2 and 3
+ * (gdn_set_fused_scan).  contract_ctas > 0 fixes the number of contraction
+ * CTAs and ring_frames > 0 the ring depth in frames (0: automatic).  The
+ * schedules differ only in the order of rounding of the scan's S * A_f
+ * product (the single pass multiplies by A_f's rows, the other schedules by
+ * its columns; A_f is symmetric): results agree to bf16 rounding.  Applies
+ * to calls made after it returns.  A scheduling control of this library; the
+ * pages have no counterpart.
+ */
+void gdn_set_single_pass(int on, int contract_ctas, int ring_frames);
+
+/*
+ * Schedule gdn_frame_forward takes for this shape on the current device:
+ * 2 single pass, 1 phase 1 then phases 2 and 3 in one cooperative launch,
+ * 0 three launches, -1 invalid shape or no usable device.
+ */
+int gdn_forward_schedule(int B, int H, int F, int N, int dk, int dv);
+
+/*
  * Schedule phases 2 and 3 take for this shape on the current device: +R when
  * they run as one cooperative launch with R rows of S per scan CTA, -R when
  * they run as two launches, 0 for invalid shapes or no usable device.
@@ -318,6 +384,16 @@ int gdn_scan_schedule(int B, int H, int dv);
  * gdn_sync_status().
  */
 gdn_status gdn_selftest_wait_timeout(unsigned long long limit_ns, gdn_stream_t stream);
+
+/*
+ * Diagnostics of the bounded waits: copies to info[0..4] where the first wait
+ * that ran out since the last call gave up -- {site, block index, thread
+ * index, value seen, value awaited} (site 0: no wait ran out; site codes are
+ * role * 10000 + step or unit, for example 1320000 + f: a scan CTA waiting
+ * for frame f's contraction) -- and clears the record.  Synchronous; call it
+ * after gdn_sync_status reported GDN_ERR_TIMEOUT.
+ */
+gdn_status gdn_debug_last_timeout(int* info);
 
 /* Library version string. */
 const char* gdn_version(void);

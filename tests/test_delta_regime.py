@@ -10,8 +10,8 @@ of a frame either strongly correlated (one shared direction plus noise, with
 sum_n beta_n |k_n|^2 in [0.5, 0.95] per frame) or orthonormal with beta in
 [0.5, 1] (A_f a near-projection, the exact-write case), over 64 frames at
 d = 128, and compare every entry point with the fp64 oracle element by
-element: the forward in both schedules of phases 2 and 3, the reverse
-direction, the step rollout on both step paths, the 8-bit inputs and the
+element: the forward in every schedule (single pass; phases 2 and 3 fused
+or apart), the reverse direction, the step rollout on both step paths, the 8-bit inputs and the
 backward.  Bars as everywhere: 2e-2 on outputs (and gradients), 1e-2 on the
 final state.
 """
@@ -75,9 +75,9 @@ def _dev(x):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("sched", ["single", "fused", "separate"])
 @pytest.mark.parametrize("reverse", [False, True])
-def test_forward_correlated_keys(fused, reverse):
+def test_forward_correlated_keys(sched, reverse):
     api = _gpu()
     d, x = shared_inputs()
     toks = sample_tokens(d["B"], d["F"], d["N"], n_random=2000, seed=3)
@@ -85,17 +85,19 @@ def test_forward_correlated_keys(fused, reverse):
                                want_out=False, sample_tokens=toks,
                                mode=oracle.MODE_REVERSE if reverse else oracle.MODE_GDN)
     xd = _dev(x)
-    api.set_fused_scan(fused)
+    api.set_single_pass(sched == "single")
+    api.set_fused_scan(sched != "separate")
     try:
         out, st = api.frame_forward(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], xd["state_in"],
                                     reverse=reverse)
         api.sync_status()
     finally:
         api.set_fused_scan(True)
+        api.set_single_pass(True)
     flat = out.view(-1, d["H"], d["dv"])[torch.as_tensor(toks, device="cuda")].float().cpu().numpy()
     eo = rel_err(flat, ref["sample_out"])
     es = rel_err(st.cpu().numpy(), ref["state"])
-    print(f"correlated keys fused={fused} reverse={reverse}: err_O={eo:.3e} err_S={es:.3e}")
+    print(f"correlated keys [{sched}] reverse={reverse}: err_O={eo:.3e} err_S={es:.3e}")
     assert eo <= TOL_OUT and es <= TOL_STATE
 
 

@@ -22,11 +22,14 @@ def _built():
     ensure_built()
 
 
-@pytest.fixture(params=["fused", "separate"])
+@pytest.fixture(params=["single", "fused", "separate"])
 def schedule(request):
-    """Phases 2 and 3 as one cooperative launch, or as two launches."""
-    api.set_fused_scan(request.param == "fused")
+    """The whole forward in one launch; or phase 1, then phases 2 and 3 as one
+    cooperative launch or as two launches."""
+    api.set_single_pass(request.param == "single")
+    api.set_fused_scan(request.param != "separate")
     yield request.param
+    api.set_single_pass(True)
     api.set_fused_scan(True)
 
 
@@ -52,7 +55,7 @@ def test_full_size_workloads(name, schedule):
     flat = out.view(-1, w.H, w.dv)[torch.as_tensor(toks, device=out.device)].float().cpu().numpy()
     eo = rel_err(flat, ref["sample_out"])
     es = rel_err(st.cpu().numpy(), ref["state"])
-    print(f"{name} [{schedule}, R={api.scan_schedule(w.B, w.H, w.dv)}]: "
+    print(f"{name} [{schedule}, sched={api.forward_schedule(w.B, w.H, w.F, w.N, w.dk, w.dv)}]: "
           f"err_O(sampled {toks.size})={eo:.3e} err_S={es:.3e}")
     assert np.isfinite(out.float().cpu().numpy()).all()
     assert eo <= TOL_OUT and es <= TOL_STATE
@@ -89,15 +92,43 @@ def test_streaming_rollout_121_steps(schedule):
 
 
 def test_schedules_agree_exactly():
-    """The fused and the two-launch schedules run the same arithmetic."""
+    """Phases 2 and 3 fused or as two launches run the same arithmetic."""
     w = inputs.WORKLOADS["seq60s"]
     x = to_dev(inputs.workload_inputs(w))
     res = {}
-    for fused in (True, False):
-        api.set_fused_scan(fused)
-        res[fused] = gpu_forward(x)
-    api.set_fused_scan(True)
+    api.set_single_pass(False)
+    try:
+        for fused in (True, False):
+            api.set_fused_scan(fused)
+            res[fused] = gpu_forward(x)
+    finally:
+        api.set_fused_scan(True)
+        api.set_single_pass(True)
     assert torch.equal(res[True][0], res[False][0]) and torch.equal(res[True][1], res[False][1])
+
+
+@pytest.mark.parametrize("contract_ctas,ring", [(0, 0), (20, 4), (100, 0), (0, 121), (1, 4)])
+def test_single_pass_role_splits_and_rings(contract_ctas, ring):
+    """The single pass with few or many contraction CTAs and shallow or full
+    rings (4 frames: every slot reused 30 times) gives the same bits as the
+    automatic plan (every item is summed the same way whoever computes it)
+    and matches the oracle."""
+    w = inputs.WORKLOADS["seq60s"]
+    x = inputs.workload_inputs(w)
+    xd = to_dev(x)
+    api.set_single_pass(True)
+    base = gpu_forward(xd)
+    api.set_single_pass(True, contract_ctas, ring)
+    try:
+        assert api.forward_schedule(w.B, w.H, w.F, w.N, w.dk, w.dv) == 2
+        out, st = gpu_forward(xd)
+    finally:
+        api.set_single_pass(True)
+    assert torch.equal(out, base[0]) and torch.equal(st, base[1])
+    toks = sample_tokens(w.B, w.F, w.N, n_random=300)
+    ref = oracle_run(x, w.B, w.H, w.F, w.N, w.dk, w.dv, want_out=False, sample_tokens=toks)
+    flat = out.view(-1, w.H, w.dv)[torch.as_tensor(toks, device=out.device)].float().cpu().numpy()
+    assert rel_err(flat, ref["sample_out"]) <= TOL_OUT and rel_err(st.cpu().numpy(), ref["state"]) <= TOL_STATE
 
 
 @pytest.mark.parametrize("name", ["tiny", "window9", "seq60s"])
