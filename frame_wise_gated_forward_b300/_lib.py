@@ -26,7 +26,7 @@ EXPORTS = (
     "gdn_version", "gdn_frame_step_noalloc", "gdn_set_fused_scan", "gdn_scan_schedule",
     "gdn_set_contract_split", "gdn_frame_forward_fp8", "gdn_frame_step_fp8", "gdn_frame_backward",
     "gdn_set_fused_step", "gdn_set_single_pass", "gdn_forward_schedule", "gdn_debug_last_timeout",
-    "gdn_frame_forward_nvfp4", "gdn_frame_step_nvfp4",
+    "gdn_frame_forward_nvfp4", "gdn_frame_step_nvfp4", "gdn_set_host_chunk_frames", "gdn_set_contract_pairs",
 )
 
 
@@ -106,6 +106,10 @@ def load(path: str | None = None):
     lib.gdn_scan_schedule.restype = ctypes.c_int
     lib.gdn_debug_last_timeout.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.gdn_debug_last_timeout.restype = ctypes.c_int
+    lib.gdn_set_contract_pairs.argtypes = [ctypes.c_int]
+    lib.gdn_set_contract_pairs.restype = None
+    lib.gdn_set_host_chunk_frames.argtypes = [ctypes.c_int]
+    lib.gdn_set_host_chunk_frames.restype = None
     lib.gdn_version.argtypes = []
     lib.gdn_version.restype = ctypes.c_char_p
     if path is None:

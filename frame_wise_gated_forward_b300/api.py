@@ -352,6 +352,17 @@ def frame_forward_host(q, k, v, alpha, beta, state_in=None, *, out=None, state_o
     return out, state_out
 
 
+def set_contract_pairs(on: bool) -> None:
+    """Phase 1 on head pairs where the shape allows it (True, the default) or
+    one head at a time (False); identical results."""
+    load().gdn_set_contract_pairs(1 if on else 0)
+
+
+def set_host_chunk_frames(frames: int) -> None:
+    """Frames per chunk of frame_forward_host's copy/compute pipeline (0: automatic)."""
+    load().gdn_set_host_chunk_frames(int(frames))
+
+
 def workspace_bytes(B, H, F, N, dk, dv) -> int:
     return int(load().gdn_workspace_bytes(B, H, F, N, dk, dv))
 

@@ -29,6 +29,8 @@ std::atomic<int> g_fused_step{1};  // one-launch step (gdn_step_fused.cuh) where
 std::atomic<int> g_single_pass{1};     // whole forward in one launch (gdn_fwd_single.cuh) where it applies
 std::atomic<int> g_single_contract{0}; // contraction CTAs of the single pass (0: automatic)
 std::atomic<int> g_single_ring{0};     // ring frames of the single pass (0: automatic)
+std::atomic<int> g_host_chunk{0};      // frames per chunk of the pipelined host call (0: automatic)
+std::atomic<int> g_pairs{0};           // phase 1 on head pairs where the shape allows it (off by default)
 
 // Kernels of each element format (gdn::FMT_BF16, FMT_FP8, FMT_FP4).
 using gdn::FMT_BF16;
@@ -78,6 +80,8 @@ struct DeviceState {
     bool coop_k1 = false;  // the same for the contraction kernel (needed to split items)
     bool coop_single = false;  // the same for the single-pass forward kernel
     cudaMemPool_t pool = nullptr;
+    cudaStream_t copy_in = nullptr;   // host -> device copies of the pipelined host call
+    cudaStream_t copy_out = nullptr;  // device -> host copies of the pipelined host call
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -122,6 +126,11 @@ gdn_status device_ready(int* dev_out, DeviceState** st_out) {
         if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) { cudaGetLastError(); return GDN_ERR_ALLOC; }
         unsigned long long keep = ~0ULL;  // keep freed workspace cached in the pool
         cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (cudaStreamCreateWithFlags(&d.copy_in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&d.copy_out, cudaStreamNonBlocking) != cudaSuccess) {
+            cudaGetLastError();
+            return GDN_ERR_LAUNCH;
+        }
         auto smem_attr = [](const void* fn, size_t bytes) {
             return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) ==
                    cudaSuccess;
@@ -138,6 +147,7 @@ gdn_status device_ready(int* dev_out, DeviceState** st_out) {
             !smem_attr(reinterpret_cast<const void*>(k2::scan_kernel<32>), k2::Cfg<32>::SMEM_BYTES) ||
             !smem_attr(reinterpret_cast<const void*>(k2::scan_kernel<64>), k2::Cfg<64>::SMEM_BYTES) ||
 
+            !smem_attr(reinterpret_cast<const void*>(k1p::contract_pair_kernel), k1p::SMEM_BYTES) ||
             !smem_attr(reinterpret_cast<const void*>(step::step_kernel), step::SMEM_BYTES) ||
             !smem_attr(reinterpret_cast<const void*>(bwd::frame_grad_kernel), bwd::FRAME_SMEM) ||
             !smem_attr(reinterpret_cast<const void*>(bwd::token_grad_kernel), bwd::TOKEN_SMEM)) {
@@ -333,6 +343,20 @@ bool encode_tokens4(CUtensorMap* m, const void* base, int BF, int N, int H, int 
 bool encode_inputs(CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tq, const void* q, const void* k, const void* v,
                    int fmt, int BF, int N, int H, int dk, int dv, int rows_k, int rows_q);
 
+// bf16 token tensor of two-head rows: [T, H, 128] as {64 columns, 8 tokens,
+// 2 halves, H heads, T / 8 groups}, box {64, 8, 2, 2, rows / 8}: each box row
+// spans the 512 contiguous bytes of two heads, and shared memory receives
+// 8-token x 128-byte swizzle atoms (gdn_k1_pair.cuh).  T % 8 == 0.
+bool encode_pairs(CUtensorMap* m, const void* base, long long T, int H, int rows) {
+    const cuuint64_t dims[5] = {64, 8, 2, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T / 8)};
+    const cuuint64_t strides[4] = {static_cast<cuuint64_t>(H) * 256, 128, 256, static_cast<cuuint64_t>(H) * 256 * 8};
+    const cuuint32_t box[5] = {64, 8, 2, 2, static_cast<cuuint32_t>(rows / 8)};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // per-item matrix [items, rows_total, cols] bf16, box (64, rows, 1)
 bool encode_mats(CUtensorMap* m, const void* base, long long items, int rows_total, int cols, int rows) {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows_total),
@@ -395,6 +419,13 @@ struct PassArgs {
     const uint8_t *q_sf = nullptr, *k_sf = nullptr, *v_sf = nullptr;   // NVFP4 block scales
     float q_scale = 1.0f, k_scale = 1.0f, v_scale = 1.0f;
 };
+
+// Phase 1 on head pairs (gdn_k1_pair.cuh): bf16 inputs, d = 128, an even
+// number of heads and frames of a multiple of 8 tokens.
+bool pair_applies(const PassArgs& a) {
+    return g_pairs.load() != 0 && a.fmt == gdn::FMT_BF16 && a.dk == 128 && a.dv == 128 && a.H % 2 == 0 &&
+           a.N % 8 == 0;
+}
 
 // Rows of S per scan CTA.  Standalone scan: the smallest slice that keeps
 // all scan CTAs in one wave.  Fused with the output pass: the smallest slice
@@ -468,14 +499,25 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
     p1.v_sf = a.v_sf;
     p1.wait_limit_ns = lim;
     if (ev) cudaEventRecord(ev[0], stream);
+    const bool pairs = pair_applies(a);
+    if (pairs) {
+        // head pairs, whole: one unit per (b, f, head pair)
+        if (!encode_pairs(&tm_k, a.k, static_cast<long long>(BF) * a.N, a.H, gdn::k1p::CHUNK) ||
+            !encode_pairs(&tm_v, a.v, static_cast<long long>(BF) * a.N, a.H, gdn::k1p::CHUNK))
+            return GDN_ERR_LAUNCH;
+        p1.whole = p1.items;
+        p1.split_per = 1;
+        p1.work = p1.items / 2;
+    }
     const int grid1 = std::min(p1.work, ds->sms);
-    const void* fn1 = k1_fn(a.fmt);
-    const size_t smem1 = k1_smem(a.fmt);
+    const void* fn1 = pairs ? reinterpret_cast<const void*>(gdn::k1p::contract_pair_kernel) : k1_fn(a.fmt);
+    const size_t smem1 = pairs ? gdn::k1p::SMEM_BYTES : k1_smem(a.fmt);
     void* args1[] = {&tm_k, &tm_v, &p1};
     // split items wait for each other's partial sums: then all CTAs must be resident
     const cudaError_t e1 =
-        sp.rem > 0 ? cudaLaunchCooperativeKernel(fn1, dim3(grid1), dim3(gdn::k1::THREADS), args1, smem1, stream)
-                   : cudaLaunchKernel(fn1, dim3(grid1), dim3(gdn::k1::THREADS), args1, smem1, stream);
+        (!pairs && sp.rem > 0)
+            ? cudaLaunchCooperativeKernel(fn1, dim3(grid1), dim3(gdn::k1::THREADS), args1, smem1, stream)
+            : cudaLaunchKernel(fn1, dim3(grid1), dim3(gdn::k1::THREADS), args1, smem1, stream);
     if (e1 != cudaSuccess) {
         cudaGetLastError();
         return GDN_ERR_LAUNCH;
@@ -621,10 +663,16 @@ gdn_status launch_single(const PassArgs& a, uint8_t* ws, const SingleLayout& L, 
     c.n_scan = a.B * a.H;
     const int rest = ds->sms - c.n_scan;
     const int forced = g_single_contract.load();
-    // automatic: 60 % of the free SMs contract (a contraction CTA streams k and v
-    // at about two thirds of an output CTA's rate of q in plus out; measured on
-    // B300 at the 60 s shape: 50 % 0.417 ms, 55 % 0.385 ms, 60 % 0.378 ms, 68 % 0.407 ms)
-    c.n_contract = forced > 0 ? std::min(forced, rest - 1) : (rest * 3 + 2) / 5;
+    c.pair = pair_applies(a) ? 1 : 0;
+    if (c.pair && (!encode_pairs(&tm_k, a.k, static_cast<long long>(BF) * a.N, a.H, k1p::CHUNK) ||
+                   !encode_pairs(&tm_v, a.v, static_cast<long long>(BF) * a.N, a.H, k1p::CHUNK)))
+        return GDN_ERR_LAUNCH;
+    // automatic: per head, 60 % of the free SMs contract (a contraction CTA
+    // streams k and v at about two thirds of an output CTA's rate of q in plus
+    // out; measured on B300 at the 60 s shape: 50 % 0.417 ms, 55 % 0.385 ms,
+    // 60 % 0.378 ms, 68 % 0.407 ms); on head pairs a contraction CTA streams
+    // about twice as fast, so 40 %
+    c.n_contract = forced > 0 ? std::min(forced, rest - 1) : c.pair ? (rest * 2 + 2) / 5 : (rest * 3 + 2) / 5;
     const int n_out = rest - c.n_contract;
     if (c.n_contract < 1 || n_out < 1) return GDN_ERR_LAUNCH;
 
@@ -641,7 +689,7 @@ gdn_status launch_single(const PassArgs& a, uint8_t* ws, const SingleLayout& L, 
     p1.whole = static_cast<int>(items);
     p1.split_per = 1;
     p1.chunks = chunks_of(a.N);
-    p1.work = static_cast<int>(items);
+    p1.work = static_cast<int>(c.pair ? items / 2 : items);
     p1.norm_k = a.prologue;
     p1.beta_sigmoid = a.prologue;
     p1.a_scale = a.fmt != FMT_BF16 ? a.k_scale * a.k_scale : 1.0f;
@@ -1260,38 +1308,104 @@ gdn_status gdn_frame_forward_host(const void* q, const void* k, const void* v, c
     s = device_ready(&dev, &ds);
     if (s != GDN_OK) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const size_t tok = static_cast<size_t>(B) * F * N;
-    const size_t bq = tok * H * dk * 2, bv = tok * H * dv * 2, ba = static_cast<size_t>(B) * F * H * 4,
-                 bb = tok * H * 4, bs = static_cast<size_t>(B) * H * dv * dk * 4;
-    size_t off[8], total = 0;
-    const size_t sizes[8] = {bq, bq, bv, ba, bb, state_in ? bs : 0, bv, state_out ? bs : 0};
-    for (int i = 0; i < 8; ++i) { off[i] = total; total = align256(total + sizes[i]); }
+    // Frame chunks of Fc frames, double-buffered on the device: chunk i's
+    // host->device copy (copy_in stream), forward (the caller's stream, the
+    // state carried in place from chunk to chunk, which is exact) and
+    // device->host copy of its outputs (copy_out stream) overlap with the
+    // neighbouring chunks'.  Events order the reuse of each buffer.
+    const int forced = g_host_chunk.load();
+    const int Fc = forced > 0 ? std::min(forced, F) : std::max(1, (F + 7) / 8);
+    const int nch = (F + Fc - 1) / Fc;
+    const size_t tokc = static_cast<size_t>(B) * Fc * N;
+    const size_t per_f_q = static_cast<size_t>(N) * H * dk * 2, per_f_v = static_cast<size_t>(N) * H * dv * 2,
+                 per_f_a = static_cast<size_t>(H) * 4, per_f_b = static_cast<size_t>(N) * H * 4;
+    const size_t bs = static_cast<size_t>(B) * H * dv * dk * 4;
+    // one slot: q, k, v, alpha, beta, out of Fc frames
+    const size_t sz[6] = {tokc * H * dk * 2, tokc * H * dk * 2, tokc * H * dv * 2,
+                          static_cast<size_t>(B) * Fc * H * 4, tokc * H * 4, tokc * H * dv * 2};
+    size_t off[6], slot_bytes = 0;
+    for (int i = 0; i < 6; ++i) { off[i] = slot_bytes; slot_bytes = align256(slot_bytes + sz[i]); }
     uint8_t* d = nullptr;
-    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&d), total, ds->pool, st) != cudaSuccess) {
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&d), 2 * slot_bytes + bs, ds->pool, st) != cudaSuccess) {
         cudaGetLastError();
         return GDN_ERR_ALLOC;
     }
-    const void* src[6] = {q, k, v, alpha, beta, state_in};
-    bool ok = true;
-    for (int i = 0; i < 6 && ok; ++i)
-        if (sizes[i]) ok = cudaMemcpyAsync(d + off[i], src[i], sizes[i], cudaMemcpyHostToDevice, st) == cudaSuccess;
-    gdn_status r = ok ? GDN_OK : GDN_ERR_LAUNCH;
-    if (r == GDN_OK)
-        r = run_pass(PassArgs{d + off[0], d + off[1], d + off[2], reinterpret_cast<const float*>(d + off[3]),
-                              reinterpret_cast<const float*>(d + off[4]),
-                              state_in ? reinterpret_cast<const float*>(d + off[5]) : nullptr, d + off[6],
-                              state_out ? reinterpret_cast<float*>(d + off[7]) : nullptr, B, H, F, N, dk, dv},
-                     false, st);
-    if (r == GDN_OK) {
-        ok = cudaMemcpyAsync(out, d + off[6], bv, cudaMemcpyDeviceToHost, st) == cudaSuccess;
-        if (ok && state_out) ok = cudaMemcpyAsync(state_out, d + off[7], bs, cudaMemcpyDeviceToHost, st) == cudaSuccess;
-        if (!ok) r = GDN_ERR_LAUNCH;
+    float* dstate = reinterpret_cast<float*>(d + 2 * slot_bytes);
+    cudaEvent_t ev[7];
+    int made = 0;
+    for (; made < 7; ++made)
+        if (cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming) != cudaSuccess) break;
+    cudaEvent_t* ev_in = ev;          // [2] a slot's inputs have landed
+    cudaEvent_t* ev_comp = ev + 2;    // [2] the forward of a slot has finished
+    cudaEvent_t* ev_out = ev + 4;     // [2] a slot's outputs have been copied out
+    cudaEvent_t ev_start = ev[6];
+    bool ok = made == 7;
+    // B rows of `width` bytes (one per batch row); a plain copy when B = 1
+    auto cp2 = [&](void* dst, size_t dpitch, const void* src, size_t spitch, size_t width, cudaMemcpyKind kind,
+                   cudaStream_t s2) {
+        ok = ok && (B == 1 ? cudaMemcpyAsync(dst, src, width, kind, s2)
+                           : cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, B, kind, s2)) == cudaSuccess;
+    };
+    if (ok) {
+        if (state_in)
+            ok = cudaMemcpyAsync(dstate, state_in, bs, cudaMemcpyHostToDevice, st) == cudaSuccess;
+        else
+            ok = cudaMemsetAsync(dstate, 0, bs, st) == cudaSuccess;
+        ok = ok && cudaEventRecord(ev_start, st) == cudaSuccess &&
+             cudaStreamWaitEvent(ds->copy_in, ev_start, 0) == cudaSuccess &&
+             cudaStreamWaitEvent(ds->copy_out, ev_start, 0) == cudaSuccess;
     }
+    gdn_status r = GDN_OK;
+    for (int i = 0; i < nch && ok && r == GDN_OK; ++i) {
+        const int slot = i & 1;
+        const int f0 = i * Fc, fc = std::min(Fc, F - f0);
+        uint8_t* b = d + slot * slot_bytes;
+        // inputs of chunk i (frames f0 .. f0 + fc - 1 of every batch row), dense [B, fc, ...]
+        if (i >= 2) ok = ok && cudaStreamWaitEvent(ds->copy_in, ev_comp[slot], 0) == cudaSuccess;
+        const uint8_t* hq = static_cast<const uint8_t*>(q);
+        const uint8_t* hk = static_cast<const uint8_t*>(k);
+        const uint8_t* hv = static_cast<const uint8_t*>(v);
+        const uint8_t* ha = reinterpret_cast<const uint8_t*>(alpha);
+        const uint8_t* hb = reinterpret_cast<const uint8_t*>(beta);
+        cp2(b + off[0], fc * per_f_q, hq + f0 * per_f_q, F * per_f_q, fc * per_f_q, cudaMemcpyHostToDevice, ds->copy_in);
+        cp2(b + off[1], fc * per_f_q, hk + f0 * per_f_q, F * per_f_q, fc * per_f_q, cudaMemcpyHostToDevice, ds->copy_in);
+        cp2(b + off[2], fc * per_f_v, hv + f0 * per_f_v, F * per_f_v, fc * per_f_v, cudaMemcpyHostToDevice, ds->copy_in);
+        cp2(b + off[3], fc * per_f_a, ha + f0 * per_f_a, F * per_f_a, fc * per_f_a, cudaMemcpyHostToDevice, ds->copy_in);
+        cp2(b + off[4], fc * per_f_b, hb + f0 * per_f_b, F * per_f_b, fc * per_f_b, cudaMemcpyHostToDevice, ds->copy_in);
+        ok = ok && cudaEventRecord(ev_in[slot], ds->copy_in) == cudaSuccess;
+        // the forward of chunk i, once its inputs are in and the slot's previous outputs are out
+        ok = ok && cudaStreamWaitEvent(st, ev_in[slot], 0) == cudaSuccess;
+        if (i >= 2) ok = ok && cudaStreamWaitEvent(st, ev_out[slot], 0) == cudaSuccess;
+        if (!ok) break;
+        r = run_pass(PassArgs{b + off[0], b + off[1], b + off[2], reinterpret_cast<const float*>(b + off[3]),
+                              reinterpret_cast<const float*>(b + off[4]), dstate, b + off[5], dstate, B, H, fc, N,
+                              dk, dv},
+                     false, st);
+        ok = ok && cudaEventRecord(ev_comp[slot], st) == cudaSuccess;
+        // its outputs back to the host
+        ok = ok && cudaStreamWaitEvent(ds->copy_out, ev_comp[slot], 0) == cudaSuccess;
+        cp2(static_cast<uint8_t*>(out) + f0 * per_f_v, F * per_f_v, b + off[5], fc * per_f_v, fc * per_f_v,
+            cudaMemcpyDeviceToHost, ds->copy_out);
+        ok = ok && cudaEventRecord(ev_out[slot], ds->copy_out) == cudaSuccess;
+    }
+    // the caller's stream waits for every copy, then returns the final state and frees
+    for (int x = 0; x < 2 && made == 7; ++x) {
+        cudaStreamWaitEvent(st, ev_in[x], 0);
+        cudaStreamWaitEvent(st, ev_out[x], 0);
+    }
+    if (ok && r == GDN_OK && state_out)
+        ok = cudaMemcpyAsync(state_out, dstate, bs, cudaMemcpyDeviceToHost, st) == cudaSuccess;
     cudaFreeAsync(d, st);
-    if (cudaStreamSynchronize(st) != cudaSuccess && r == GDN_OK) r = GDN_ERR_LAUNCH;
+    if (cudaStreamSynchronize(st) != cudaSuccess) ok = false;
+    for (int x = 0; x < made; ++x) cudaEventDestroy(ev[x]);
+    if (r == GDN_OK && !ok) r = GDN_ERR_LAUNCH;
     cudaGetLastError();
     return r;
 }
+
+void gdn_set_host_chunk_frames(int frames) { g_host_chunk.store(frames > 0 ? frames : 0); }
+
+void gdn_set_contract_pairs(int on) { g_pairs.store(on != 0 ? 1 : 0); }
 
 }  // extern "C"
 

@@ -9,8 +9,9 @@
 //   [0, n_scan)                       the scan of one (b, h) head each
 //                                     (gdn_scan_head.cuh)
 //   [n_scan, n_scan + n_contract)     A_f = K_f^T B_f K_f, U_f = V_f^T B_f K_f
-//                                     for whole (b, f, h) items in scan order
-//                                     (gdn_k1_contract.cuh, ring mode)
+//                                     for whole (b, f, h) items, or head pairs,
+//                                     in scan order (gdn_k1_contract.cuh,
+//                                     gdn_k1_pair.cuh, ring mode)
 //   the rest                          O_f = Q_f S_f^T for whole items in scan
 //                                     order (gdn_k3_output.cuh, ring mode)
 // Step s of the scan of head (b, h) uses ring slot (b * W + s % W) * H + h of
@@ -32,6 +33,7 @@
 #pragma once
 
 #include "gdn_k1_contract.cuh"
+#include "gdn_k1_pair.cuh"
 #include "gdn_k3_output.cuh"
 #include "gdn_scan_head.cuh"
 
@@ -43,9 +45,9 @@ static_assert(THREADS >= k1::THREADS && THREADS >= k3::threads<FMT_FP8>(), "the 
 
 template <int FMT>
 constexpr size_t smem_bytes() {
-    return k2h::SMEM_BYTES > k1::Lay<FMT>::SMEM
-               ? (k2h::SMEM_BYTES > k3::SMEM_BYTES ? k2h::SMEM_BYTES : k3::SMEM_BYTES)
-               : (k1::Lay<FMT>::SMEM > k3::SMEM_BYTES ? k1::Lay<FMT>::SMEM : k3::SMEM_BYTES);
+    constexpr size_t a = k2h::SMEM_BYTES > k1::Lay<FMT>::SMEM ? k2h::SMEM_BYTES : k1::Lay<FMT>::SMEM;
+    constexpr size_t b = k3::SMEM_BYTES > k1p::SMEM_BYTES ? k3::SMEM_BYTES : k1p::SMEM_BYTES;
+    return a > b ? a : b;
 }
 
 struct Counts {
@@ -53,6 +55,7 @@ struct Counts {
     int* s_free;    // [B][W][H]
     int n_scan;     // = B * H
     int n_contract;
+    int pair;       // bf16 only: the contraction CTAs take head pairs (gdn_k1_pair.cuh; tm_k, tm_v are pair maps)
 };
 
 template <int FMT>
@@ -68,6 +71,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (cta < c.n_scan) {
         k2h::scan_head_role(&tm_A, &tm_U, &tm_S, p2, cta, smem);
     } else if (cta < c.n_scan + c.n_contract) {
+        if constexpr (FMT == FMT_BF16) {
+            if (c.pair) {
+                k1p::contract_pair_role(tm_k, tm_v, p1, cta - c.n_scan, c.n_contract, smem);
+                return;
+            }
+        }
         k1::contract_role<FMT>(tm_k, tm_v, p1, cta - c.n_scan, c.n_contract, smem);
     } else {
         k3::Sched sc;

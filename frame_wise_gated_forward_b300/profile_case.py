@@ -2,7 +2,7 @@
 backward) a few times on a 60 s-sequence-shaped case with a chosen number of
 latent frames, for profilers (ncu) to capture.
 
-    python -m frame_wise_gated_forward_b300.profile_case --frames 31 --iters 2
+    python -m frame_wise_gated_forward_b300.profile_case --frames 31 --iters 2 [--schedule multi] [--pairs 1]
 
 Shapes are those of the 60 s 720p workload (H=16, N=880, d=128) with F
 frames; inputs come from the seeded generator.  Prints the event-timed
@@ -33,9 +33,14 @@ def main():
                     help="gdn_frame_forward, gdn_frame_step (F ignored), gdn_frame_forward_fp8 or "
                          "gdn_frame_backward")
     ap.add_argument("--step", action="store_true", help="same as --mode step")
+    ap.add_argument("--schedule", choices=["single", "multi"], default="single",
+                    help="the whole forward in one launch, or phase 1 then phases 2+3")
+    ap.add_argument("--pairs", type=int, default=0, help="phase 1 on head pairs (1) or single heads (0)")
     a = ap.parse_args()
     mode = "step" if a.step else a.mode
     build.build()
+    api.set_single_pass(a.schedule == "single")
+    api.set_contract_pairs(bool(a.pairs))
     F = 1 if mode == "step" else a.frames
     B, H, N, d = a.batch, a.heads, a.tokens, a.d
     if mode == "fp8":

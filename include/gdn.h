@@ -259,17 +259,37 @@ gdn_status gdn_frame_forward_timed(const void* q, const void* k, const void* v,
                                    gdn_stream_t stream, void* const* phase_events);
 
 /*
- * gdn_frame_forward on HOST buffers (same layouts): copies the inputs to
- * library-owned device memory on `stream`, runs the forward, copies `out` and
- * (if not NULL) `state_out` back, and returns after synchronising `stream`.
- * Page-locked host buffers make the copies run at full link speed.  The
- * end-to-end cost of one call therefore includes both transfers.
+ * gdn_frame_forward on HOST buffers (same layouts): the sequence is processed
+ * in chunks of frames (about F/8 each; gdn_set_host_chunk_frames), double-
+ * buffered in library-owned device memory.  Chunk i's inputs are copied in on
+ * a library copy stream while chunk i-1 runs on `stream` and chunk i-2's
+ * outputs are copied out on a second library copy stream, so both directions
+ * of the host link and the kernels overlap; the state is carried on the
+ * device from chunk to chunk (exactly: the result is bit-identical to one
+ * gdn_frame_forward over the whole sequence).  Returns after synchronising
+ * `stream`, with `out` and (if not NULL) `state_out` written.  Page-locked
+ * host buffers make the copies run at full link speed and asynchronously.
  */
 gdn_status gdn_frame_forward_host(const void* q, const void* k, const void* v,
                                   const float* alpha, const float* beta,
                                   const float* state_in, void* out, float* state_out,
                                   int B, int H, int F, int N, int dk, int dv,
                                   gdn_stream_t stream);
+
+/*
+ * Phase 1 on head pairs.  on != 0 (default): with bf16 inputs, dk = dv = 128,
+ * an even number of heads and N a multiple of 8, the contraction takes two
+ * heads of a frame at a time, its copies covering the 512 contiguous bytes
+ * both heads occupy per token (about twice the copy rate of one head's 256
+ * bytes).  on = 0: one head at a time.  Results are identical.  Applies to
+ * calls made after it returns.  A scheduling control of this library; the
+ * pages have no counterpart.
+ */
+void gdn_set_contract_pairs(int on);
+
+/* Frames per chunk of gdn_frame_forward_host (0: automatic, about F / 8).
+ * Applies to calls made after it returns. */
+void gdn_set_host_chunk_frames(int frames);
 
 /* Bytes of library workspace one gdn_frame_forward call of this shape takes
  * on the current device (0 for invalid shapes; with no usable device, an

@@ -194,3 +194,30 @@ def test_long_frames_split_across_ctas(max_split):
     es = rel_err(st.cpu().numpy(), ref["state"])
     print(f"N=4100 max_split={max_split}: err_O={eo:.3e} err_S={es:.3e}")
     assert eo <= TOL_OUT and es <= TOL_STATE
+
+
+@pytest.mark.parametrize("sched", ["single", "multi"])
+@pytest.mark.parametrize("shape", [
+    (1, 16, 10, 880, 128, 128),   # the 60 s shape's frames: last chunk reaches 16 tokens into the next frame
+    (2, 4, 5, 24, 128, 128),      # frames shorter than one chunk, two batch rows
+    (1, 2, 3, 8, 128, 128),       # one 8-token group per frame
+])
+def test_contract_pairs_match_single_heads(shape, sched):
+    """Phase 1 on head pairs (two heads' 512 contiguous bytes per token in one
+    copy) gives the same bits as one head at a time, and matches the oracle."""
+    B, H, F, N, dk, dv = shape
+    x = inputs.draw(B, H, F, N, dk, dv, seed=9, s0_std=0.1)
+    xd = to_dev(x)
+    api.set_single_pass(sched == "single")
+    try:
+        api.set_contract_pairs(True)
+        o1, s1 = gpu_forward(xd)
+        api.set_contract_pairs(False)
+        o2, s2 = gpu_forward(xd)
+    finally:
+        api.set_contract_pairs(True)
+        api.set_single_pass(True)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    ref = oracle_run(x, B, H, F, N, dk, dv)
+    assert rel_err(o1.float().cpu().numpy(), ref["out"]) <= TOL_OUT
+    assert rel_err(s1.cpu().numpy(), ref["state"]) <= TOL_STATE
