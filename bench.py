@@ -111,11 +111,12 @@ def path_floor_bytes(w, in_bytes=2):
             + w.B * w.H * w.dv * w.dk * 4)
 
 
-# the sources the forward pass's kernels (phase 1, phases 2+3) are built from;
+# the sources the forward pass's kernels (the single pass and the multi-launch
+# schedule) are built from;
 # the step and backward kernels live in files of their own, and the one-launch
 # step's host launcher is cut out of gdn_api.cu before hashing
-FORWARD_SOURCES = ("gdn_api.cu", "gdn_k1_contract.cuh", "gdn_k23_fused.cuh", "gdn_k2_scan.cuh", "gdn_k3_output.cuh",
-                   "gdn_ptx.cuh")
+FORWARD_SOURCES = ("gdn_api.cu", "gdn_fwd_single.cuh", "gdn_scan_head.cuh", "gdn_k1_contract.cuh", "gdn_k1_pair.cuh",
+                   "gdn_k23_fused.cuh", "gdn_k2_scan.cuh", "gdn_k3_output.cuh", "gdn_ptx.cuh")
 
 
 def forward_part(name, text):
@@ -537,11 +538,35 @@ def main():
     bwd_ms = r0.elapsed_time(r1) / nb
     # compulsory bytes: q, k, v, d_out, beta read; dq, dk, dv, d_beta written (bf16 / fp32)
     bwd_bytes = tokens * w.H * ((2 * w.dk + 2 * w.dv) * 2 + (2 * w.dk + w.dv) * 2 + 8)
+    # the same gradients from the activations a training forward keeps (no recompute)
+    _, _, sa, ss = api.frame_forward_save(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], s_in)
+    torch.cuda.synchronize(device)
+    r0.record(stream)
+    for _ in range(nb):
+        api.frame_forward_save(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], s_in, out=out, state_out=st,
+                               saved_A=sa, saved_S=ss)
+    r1.record(stream)
+    torch.cuda.synchronize(device)
+    fwd_save_ms = r0.elapsed_time(r1) / nb
+    api.frame_backward_saved(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], s_in, sa, ss, d_out)
+    torch.cuda.synchronize(device)
+    r0.record(stream)
+    for _ in range(nb):
+        api.frame_backward_saved(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], s_in, sa, ss, d_out)
+    r1.record(stream)
+    torch.cuda.synchronize(device)
+    api.sync_status()
+    bwd_saved_ms = r0.elapsed_time(r1) / nb
     backward_info = {"ms_per_step": bwd_ms, "tokens_per_s": tokens / (bwd_ms / 1e3), "steps": nb,
                      "path_floor_ms": bwd_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3,
                      "what": "gdn_frame_backward: dq, dk, dv, dalpha, dbeta, dS0 for upstream dO (forward states "
-                             "recomputed)"}
-    del d_out
+                             "recomputed)",
+                     "from_saved_activations": {
+                         "backward_ms": bwd_saved_ms, "forward_save_ms": fwd_save_ms,
+                         "saved_bytes": sa.numel() * 2 + ss.numel() * 2,
+                         "what": "gdn_frame_forward_save keeps A_f and the per-frame bf16 states; "
+                                 "gdn_frame_backward_saved skips their recompute (bit-identical gradients)"}}
+    del d_out, sa, ss
 
     # ------------------------------------------- interactive step (one frame)
     # the streaming rollout: F sequential gdn_frame_step calls on a resident state

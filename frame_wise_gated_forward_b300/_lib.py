@@ -27,6 +27,7 @@ EXPORTS = (
     "gdn_set_contract_split", "gdn_frame_forward_fp8", "gdn_frame_step_fp8", "gdn_frame_backward",
     "gdn_set_fused_step", "gdn_set_single_pass", "gdn_forward_schedule", "gdn_debug_last_timeout",
     "gdn_frame_forward_nvfp4", "gdn_frame_step_nvfp4", "gdn_set_host_chunk_frames", "gdn_set_contract_pairs",
+    "gdn_frame_forward_save", "gdn_frame_backward_saved",
 )
 
 
@@ -71,6 +72,11 @@ def load(path: str | None = None):
     lib.gdn_frame_backward.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, vp, vp, vp, fp, fp, fp,
                                        i, i, i, i, i, i, st]
     lib.gdn_frame_backward.restype = ctypes.c_int
+    lib.gdn_frame_backward_saved.argtypes = [vp, vp, vp, fp, fp, fp, vp, vp, vp, fp, vp, vp, vp, fp, fp, fp,
+                                             i, i, i, i, i, i, st]
+    lib.gdn_frame_backward_saved.restype = ctypes.c_int
+    lib.gdn_frame_forward_save.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, vp, vp, i, i, i, i, i, i, st]
+    lib.gdn_frame_forward_save.restype = ctypes.c_int
     lib.gdn_frame_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, st]
     lib.gdn_frame_step.restype = ctypes.c_int
     lib.gdn_frame_forward_timed.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, st,

@@ -116,8 +116,50 @@ def frame_step_gated(q, k, v, a_logit, b_logit, alpha_scale, state_in=None, *, o
     return out, state_out
 
 
+def frame_forward_save(q, k, v, alpha, beta, state_in=None, *, out=None, state_out=None, saved_A=None,
+                       saved_S=None, stream=None):
+    """frame_forward that also writes the activations its backward needs:
+    returns (out, state_out, saved_A, saved_S) with saved_A bf16 [B,F,H,dk,dk]
+    (A_f of every frame) and saved_S bf16 [B,F,H,dv,dk] (the state after every
+    frame); pass them to frame_backward_saved."""
+    lib = load()
+    B, F, N, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, F, N, H, dv), dtype=torch.bfloat16, device=dev)
+    if state_out is None:
+        state_out = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+    if saved_A is None:
+        saved_A = torch.empty((B, F, H, dk, dk), dtype=torch.bfloat16, device=dev)
+    if saved_S is None:
+        saved_S = torch.empty((B, F, H, dv, dk), dtype=torch.bfloat16, device=dev)
+    args = [
+        _dev(q, "q", torch.bfloat16, (B, F, N, H, dk)),
+        _dev(k, "k", torch.bfloat16, (B, F, N, H, dk)),
+        _dev(v, "v", torch.bfloat16, (B, F, N, H, dv)),
+        _dev(alpha, "alpha", torch.float32, (B, F, H)),
+        _dev(beta, "beta", torch.float32, (B, F, N, H)),
+        None if state_in is None else _dev(state_in, "state_in", torch.float32, (B, H, dv, dk)),
+        _dev(out, "out", torch.bfloat16, (B, F, N, H, dv)),
+        _dev(state_out, "state_out", torch.float32, (B, H, dv, dk)),
+        _dev(saved_A, "saved_A", torch.bfloat16, (B, F, H, dk, dk)),
+        _dev(saved_S, "saved_S", torch.bfloat16, (B, F, H, dv, dk)),
+    ]
+    check(lib.gdn_frame_forward_save(*args, B, H, F, N, dk, dv, _stream_handle(stream)), "gdn_frame_forward_save")
+    return out, state_out, saved_A, saved_S
+
+
+def frame_backward_saved(q, k, v, alpha, beta, state_in, saved_A, saved_S, d_out, d_state_out=None, *,
+                         want_d_state_in=True, stream=None):
+    """frame_backward from the activations of frame_forward_save (no
+    recompute of phase 1 and the forward scan); the same gradients."""
+    return frame_backward(q, k, v, alpha, beta, state_in, d_out, d_state_out, want_d_state_in=want_d_state_in,
+                          stream=stream, _saved=(saved_A, saved_S))
+
+
 def frame_backward(q, k, v, alpha, beta, state_in, d_out, d_state_out=None, *, want_d_state_in=True,
-                   stream=None):
+                   stream=None, _saved=None):
     """Gradients of frame_forward: returns (dq, dk, dv, d_alpha, d_beta,
     d_state_in) for upstream d_out [B,F,N,H,dv] (bf16) and d_state_out
     [B,H,dv,dk] (fp32, None = 0).  Shapes and dtypes as the inputs."""
@@ -143,7 +185,13 @@ def frame_backward(q, k, v, alpha, beta, state_in, d_out, d_state_out=None, *, w
         dq.data_ptr(), dkk.data_ptr(), dvv.data_ptr(), d_alpha.data_ptr(), d_beta.data_ptr(),
         None if d_s0 is None else d_s0.data_ptr(),
     ]
-    check(lib.gdn_frame_backward(*args, B, H, F, N, dk, dv, _stream_handle(stream)), "gdn_frame_backward")
+    if _saved is None:
+        check(lib.gdn_frame_backward(*args, B, H, F, N, dk, dv, _stream_handle(stream)), "gdn_frame_backward")
+    else:
+        sa = _dev(_saved[0], "saved_A", torch.bfloat16, (B, F, H, dk, dk))
+        ss = _dev(_saved[1], "saved_S", torch.bfloat16, (B, F, H, dv, dk))
+        check(lib.gdn_frame_backward_saved(*args[:6], sa, ss, *args[6:], B, H, F, N, dk, dv, _stream_handle(stream)),
+              "gdn_frame_backward_saved")
     return dq, dkk, dvv, d_alpha, d_beta, d_s0
 
 
@@ -437,7 +485,7 @@ def selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     return int(lib.gdn_sync_status(_stream_handle(stream)))
 
 
-__all__ = ["frame_forward", "frame_forward_nvfp4", "frame_step_nvfp4", "frame_forward_gated", "frame_step_gated", "frame_step", "frame_forward_timed", "frame_forward_host", "workspace_bytes",
+__all__ = ["frame_forward", "frame_forward_save", "frame_backward_saved", "frame_forward_nvfp4", "frame_step_nvfp4", "frame_forward_gated", "frame_step_gated", "frame_step", "frame_forward_timed", "frame_forward_host", "workspace_bytes",
            "step_workspace_bytes", "sync_status", "set_fused_scan", "scan_schedule", "set_single_pass",
            "forward_schedule", "set_wait_limit_ns", "selftest_wait_timeout",
            "GDNError"]

@@ -418,6 +418,11 @@ struct PassArgs {
     int fmt = gdn::FMT_BF16;   // q, k, v element format (FMT_FP8: value = scale * e4m3; FMT_FP4: NVFP4)
     const uint8_t *q_sf = nullptr, *k_sf = nullptr, *v_sf = nullptr;   // NVFP4 block scales
     float q_scale = 1.0f, k_scale = 1.0f, v_scale = 1.0f;
+    // forward with saved activations: A_f (bf16 [B, F, H, dk, dk]) and the
+    // per-frame state images (bf16 [B, F, H, dv, dk]) go to these caller
+    // buffers instead of the workspace (multi-launch schedule)
+    void* ext_A = nullptr;
+    void* ext_S = nullptr;
 };
 
 // Phase 1 on head pairs (gdn_k1_pair.cuh): bf16 inputs, d = 128, an even
@@ -452,9 +457,9 @@ gdn_status launch_phases(const PassArgs& a, uint8_t* ws, const Layout& L, const 
                          const DeviceState* ds, cudaStream_t stream, cudaEvent_t const* ev) {
     const long long items = static_cast<long long>(a.B) * a.F * a.H;
     const int BF = a.B * a.F;
-    __nv_bfloat16* A_ws = reinterpret_cast<__nv_bfloat16*>(ws + L.a_off);
+    __nv_bfloat16* A_ws = reinterpret_cast<__nv_bfloat16*>(a.ext_A ? static_cast<uint8_t*>(a.ext_A) : ws + L.a_off);
     float* U_ws = reinterpret_cast<float*>(ws + L.u_off);
-    __nv_bfloat16* S_all = reinterpret_cast<__nv_bfloat16*>(ws + L.s_off);
+    __nv_bfloat16* S_all = reinterpret_cast<__nv_bfloat16*>(a.ext_S ? static_cast<uint8_t*>(a.ext_S) : ws + L.s_off);
     float* partial = reinterpret_cast<float*>(ws + L.p_off);
     const int Rf = (g_fused_scan.load() != 0 && ds->coop) ? scan_rows_fused(a.B, a.H, a.dv, ds->sms) : 0;
     const int R = Rf != 0 ? Rf : scan_rows_standalone(a.B, a.H, a.dv, ds->sms);
@@ -814,7 +819,7 @@ gdn_status run_pass(const PassArgs& a, bool step, cudaStream_t stream, cudaEvent
     if (st != GDN_OK) return st;
     if (!all_device(a)) return GDN_ERR_NULL_PTR;
     if (step && fused_step_applies(a) && ev == nullptr) return launch_step_fused(a, stream);
-    if (!step && single_pass_heads(a, ds) > 0) {
+    if (!step && a.ext_A == nullptr && single_pass_heads(a, ds) > 0) {
         const SingleLayout L = single_layout(a);
         uint8_t* ws = nullptr;
         if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), L.total, ds->pool, stream) != cudaSuccess) {
@@ -858,6 +863,8 @@ struct BwdArgs {
     void *dq, *dk, *dv;
     float *d_alpha, *d_beta, *d_state_in;
     int B, H, F, N, dk_, dv_;
+    const void* saved_A = nullptr;   // forward activations (gdn_frame_forward_save), or null: recompute
+    const void* saved_S = nullptr;
 };
 
 // Workspace of one batch row (reused row after row); F1 = F + 1 frame slots.
@@ -987,8 +994,18 @@ gdn_status bwd_row(const BwdArgs& a, int b, uint8_t* ws, const BwdLayout& L, con
     else if (cudaMemsetAsync(Sx, 0, H * sd * 2, st) != cudaSuccess)
         return GDN_ERR_LAUNCH;
     // forward recompute: A_f, U_f, and the states S_0..S_{F-1} into slots 1..F
-    if ((r = bwd_contract(k, v, beta, A1, U, counters, H, F, N, dk, dv, ds, st)) != GDN_OK) return r;
-    if ((r = bwd_scan(A1, U, Sx + H * sd, alpha, s0, nullptr, H, F, dk, dv, 0, ds, st)) != GDN_OK) return r;
+    if (a.saved_A != nullptr) {
+        // the forward's own A_f and state images, saved by gdn_frame_forward_save
+        const size_t fa = static_cast<size_t>(F) * H * ad * 2, fs = static_cast<size_t>(F) * H * sd * 2;
+        if (cudaMemcpyAsync(A1, static_cast<const uint8_t*>(a.saved_A) + b * fa, fa, cudaMemcpyDeviceToDevice, st) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(Sx + H * sd, static_cast<const uint8_t*>(a.saved_S) + b * fs, fs,
+                            cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+            return GDN_ERR_LAUNCH;
+    } else {
+        if ((r = bwd_contract(k, v, beta, A1, U, counters, H, F, N, dk, dv, ds, st)) != GDN_OK) return r;
+        if ((r = bwd_scan(A1, U, Sx + H * sd, alpha, s0, nullptr, H, F, dk, dv, 0, ds, st)) != GDN_OK) return r;
+    }
     // M_f = dO_f^T Q_f into slots 1..F (the contraction with beta = 1; its A output is scratch)
     if ((r = bwd_contract(q, dO, ones, Wb, U2 + H * sd, counters, H, F, N, dk, dv, ds, st)) != GDN_OK) return r;
     // reverse scan over F + 1 slots: slot j >= 1 receives G_{j-1}, slot 0 dL/dS_0
@@ -1228,10 +1245,14 @@ gdn_status gdn_frame_step_nvfp4(const void* q4, const void* k4, const void* v4, 
     return run_pass(a, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
-gdn_status gdn_frame_backward(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
-                              const float* state_in, const void* d_out, const float* d_state_out, void* dq_out,
-                              void* dk_out, void* dv_out, float* d_alpha, float* d_beta, float* d_state_in, int B,
-                              int H, int F, int N, int dk, int dv, gdn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+gdn_status backward_impl(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
+                         const float* state_in, const void* saved_A, const void* saved_S, const void* d_out,
+                         const float* d_state_out, void* dq_out, void* dk_out, void* dv_out, float* d_alpha,
+                         float* d_beta, float* d_state_in, int B, int H, int F, int N, int dk, int dv,
+                         gdn_stream_t stream) {
     if (!q || !k || !v || !alpha || !beta || !d_out || !dq_out || !dk_out || !dv_out || !d_alpha || !d_beta)
         return GDN_ERR_NULL_PTR;
     gdn_status s = validate(q, k, v, alpha, beta, state_in, d_out, nullptr, B, H, F, N, dk, dv);
@@ -1246,10 +1267,13 @@ gdn_status gdn_frame_backward(const void* q, const void* k, const void* v, const
         const long long tok = static_cast<long long>(B) * F * N;
         const uintptr_t sb = static_cast<uintptr_t>(static_cast<long long>(B) * H * dv * dk * 4);
         auto R = [](const void* p, uintptr_t n) { return Range{reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p) + n}; };
-        const Range ins[8] = {R(q, tok * H * dk * 2), R(k, tok * H * dk * 2), R(v, tok * H * dv * 2),
-                              R(alpha, static_cast<uintptr_t>(B) * F * H * 4), R(beta, tok * H * 4),
-                              R(d_out, tok * H * dv * 2), state_in ? R(state_in, sb) : Range{0, 0},
-                              d_state_out ? R(d_state_out, sb) : Range{0, 0}};
+        const uintptr_t sab = static_cast<uintptr_t>(static_cast<long long>(B) * F * H * dk * dk * 2);
+        const uintptr_t ssb = static_cast<uintptr_t>(static_cast<long long>(B) * F * H * dv * dk * 2);
+        const Range ins[10] = {R(q, tok * H * dk * 2), R(k, tok * H * dk * 2), R(v, tok * H * dv * 2),
+                               R(alpha, static_cast<uintptr_t>(B) * F * H * 4), R(beta, tok * H * 4),
+                               R(d_out, tok * H * dv * 2), state_in ? R(state_in, sb) : Range{0, 0},
+                               d_state_out ? R(d_state_out, sb) : Range{0, 0},
+                               saved_A ? R(saved_A, sab) : Range{0, 0}, saved_S ? R(saved_S, ssb) : Range{0, 0}};
         const Range outs[6] = {R(dq_out, tok * H * dk * 2), R(dk_out, tok * H * dk * 2), R(dv_out, tok * H * dv * 2),
                                R(d_alpha, static_cast<uintptr_t>(B) * F * H * 4), R(d_beta, tok * H * 4),
                                d_state_in ? R(d_state_in, sb) : Range{0, 0}};
@@ -1264,7 +1288,8 @@ gdn_status gdn_frame_backward(const void* q, const void* k, const void* v, const
     DeviceState* ds;
     s = device_ready(&dev, &ds);
     if (s != GDN_OK) return s;
-    const void* ptrs[14] = {q, k, v, alpha, beta, state_in, d_out, d_state_out, dq_out, dk_out, dv_out, d_alpha, d_beta, d_state_in};
+    const void* ptrs[16] = {q, k, v, alpha, beta, state_in, d_out, d_state_out, dq_out, dk_out, dv_out, d_alpha, d_beta,
+                            d_state_in, saved_A, saved_S};
     for (const void* p : ptrs)
         if (!is_device_ptr(p)) return GDN_ERR_NULL_PTR;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -1276,12 +1301,69 @@ gdn_status gdn_frame_backward(const void* q, const void* k, const void* v, const
     }
     BwdArgs a{q, k, v, alpha, beta, state_in, d_out, d_state_out, dq_out, dk_out, dv_out, d_alpha, d_beta,
               d_state_in, B, H, F, N, dk, dv};
+    a.saved_A = saved_A;
+    a.saved_S = saved_S;
     fill_f32_kernel<<<2 * ds->sms, 256, 0, st>>>(reinterpret_cast<float*>(ws + L.one_off),
                                                  static_cast<long long>(F) * N * H, 1.0f);
     gdn_status r = GDN_OK;
     for (int b = 0; b < B && r == GDN_OK; ++b) r = bwd_row(a, b, ws, L, ds, st);
     cudaFreeAsync(ws, st);
     return r;
+}
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_frame_backward(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
+                              const float* state_in, const void* d_out, const float* d_state_out, void* dq_out,
+                              void* dk_out, void* dv_out, float* d_alpha, float* d_beta, float* d_state_in, int B,
+                              int H, int F, int N, int dk, int dv, gdn_stream_t stream) {
+    return backward_impl(q, k, v, alpha, beta, state_in, nullptr, nullptr, d_out, d_state_out, dq_out, dk_out, dv_out,
+                         d_alpha, d_beta, d_state_in, B, H, F, N, dk, dv, stream);
+}
+
+gdn_status gdn_frame_backward_saved(const void* q, const void* k, const void* v, const float* alpha,
+                                    const float* beta, const float* state_in, const void* saved_A,
+                                    const void* saved_S, const void* d_out, const float* d_state_out, void* dq_out,
+                                    void* dk_out, void* dv_out, float* d_alpha, float* d_beta, float* d_state_in,
+                                    int B, int H, int F, int N, int dk, int dv, gdn_stream_t stream) {
+    if (!saved_A || !saved_S) return GDN_ERR_NULL_PTR;
+    return backward_impl(q, k, v, alpha, beta, state_in, saved_A, saved_S, d_out, d_state_out, dq_out, dk_out, dv_out,
+                         d_alpha, d_beta, d_state_in, B, H, F, N, dk, dv, stream);
+}
+
+gdn_status gdn_frame_forward_save(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
+                                  const float* state_in, void* out, float* state_out, void* saved_A, void* saved_S,
+                                  int B, int H, int F, int N, int dk, int dv, gdn_stream_t stream) {
+    gdn_status s = validate(q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv);
+    if (s != GDN_OK) return s;
+    if (!saved_A || !saved_S) return GDN_ERR_NULL_PTR;
+    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!a16(saved_A) || !a16(saved_S)) return GDN_ERR_MISALIGNED;
+    {
+        const long long tok = static_cast<long long>(B) * F * N;
+        auto R = [](const void* p, long long n) {
+            return Range{reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(n)};
+        };
+        const Range ra = R(saved_A, static_cast<long long>(B) * F * H * dk * dk * 2);
+        const Range rs = R(saved_S, static_cast<long long>(B) * F * H * dv * dk * 2);
+        const Range others[7] = {R(q, tok * H * dk * 2), R(k, tok * H * dk * 2), R(v, tok * H * dv * 2),
+                                 R(alpha, static_cast<long long>(B) * F * H * 4), R(beta, tok * H * 4),
+                                 R(out, tok * H * dv * 2),
+                                 state_out ? R(state_out, static_cast<long long>(B) * H * dv * dk * 4) : Range{0, 0}};
+        if (overlap(ra, rs)) return GDN_ERR_ALIAS;
+        for (const Range& o : others)
+            if (o.hi > o.lo && (overlap(o, ra) || overlap(o, rs))) return GDN_ERR_ALIAS;
+        if (state_in) {
+            const Range ri = R(state_in, static_cast<long long>(B) * H * dv * dk * 4);
+            if (overlap(ri, ra) || overlap(ri, rs)) return GDN_ERR_ALIAS;
+        }
+    }
+    if (!is_device_ptr(saved_A) || !is_device_ptr(saved_S)) return GDN_ERR_NULL_PTR;
+    PassArgs a{q, k, v, alpha, beta, state_in, out, state_out, B, H, F, N, dk, dv};
+    a.ext_A = saved_A;
+    a.ext_S = saved_S;
+    return run_pass(a, false, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gdn_status gdn_frame_forward_timed(const void* q, const void* k, const void* v, const float* alpha,

@@ -218,6 +218,38 @@ gdn_status gdn_frame_step_nvfp4(const void* q4, const void* k4, const void* v4,
                                 int B, int H, int N, int dk, int dv,
                                 gdn_stream_t stream);
 
+/*
+ * Forward that keeps the activations its backward needs, for training: the
+ * same results as gdn_frame_forward, and in addition
+ *   saved_A  bf16 [B, F, H, dk, dk]   A_f = K_f^T B_f K_f of every frame
+ *   saved_S  bf16 [B, F, H, dv, dk]   the state after every frame, rounded to bf16
+ * (B*F*H*(dk*dk + dv*dk)*2 bytes, 127 MB at the 60 s shape), written by the
+ * kernels as they go (phase 1, then the scan and output pass).  Caller-owned
+ * device memory, 16-byte aligned, clear of every other argument.  Pass both to
+ * gdn_frame_backward_saved, which then skips recomputing them.
+ */
+gdn_status gdn_frame_forward_save(const void* q, const void* k, const void* v,
+                                  const float* alpha, const float* beta,
+                                  const float* state_in, void* out, float* state_out,
+                                  void* saved_A, void* saved_S,
+                                  int B, int H, int F, int N, int dk, int dv,
+                                  gdn_stream_t stream);
+
+/*
+ * gdn_frame_backward from the activations of gdn_frame_forward_save (same
+ * inputs, same shapes): the per-frame A_f and state images are copied from
+ * saved_A, saved_S instead of being recomputed (phase 1 and the forward scan
+ * are skipped).  The gradients are bit-identical to gdn_frame_backward's.
+ */
+gdn_status gdn_frame_backward_saved(const void* q, const void* k, const void* v,
+                                    const float* alpha, const float* beta, const float* state_in,
+                                    const void* saved_A, const void* saved_S,
+                                    const void* d_out, const float* d_state_out,
+                                    void* dq_out, void* dk_out, void* dv_out, float* d_alpha, float* d_beta,
+                                    float* d_state_in,
+                                    int B, int H, int F, int N, int dk, int dv,
+                                    gdn_stream_t stream);
+
 /* gdn_frame_step with the 8-bit inputs of gdn_frame_forward_fp8. */
 gdn_status gdn_frame_step_fp8(const void* q, const void* k, const void* v,
                               float q_scale, float k_scale, float v_scale,

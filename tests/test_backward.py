@@ -99,3 +99,41 @@ def test_backward_rejects_bad_arguments():
     assert call(dq=p[0] + 2) == 4                # misaligned
     assert call() == 0
     assert lib.gdn_sync_status(s) == 0
+
+
+@pytest.mark.parametrize("dims", [
+    (2, 2, 3, 130, 128, 128),    # two batch rows, ragged second tile
+    (1, 3, 3, 64, 64, 128),      # dk != dv
+    (1, 16, 16, 880, 128, 128),  # 16 frames of the 60 s shape
+])
+def test_forward_save_and_backward_from_saved_activations(dims):
+    """gdn_frame_forward_save gives the forward's results plus A_f and the
+    per-frame state images; gdn_frame_backward_saved from them gives the same
+    bits as the backward that recomputes them, and matches the oracle."""
+    B, H, F, N, dk, dv = dims
+    x, d_out, d_sf = case(*dims, seed=23)
+    xd = {k: v.cuda() for k, v in x.items()}
+    api.set_single_pass(False)
+    try:
+        o_ref, s_ref = api.frame_forward(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], xd["state_in"])
+    finally:
+        api.set_single_pass(True)
+    o, s, sa, ss = api.frame_forward_save(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], xd["state_in"])
+    api.sync_status()
+    assert torch.equal(o, o_ref) and torch.equal(s, s_ref)
+    st = oracle.frame_forward(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["state_in"], B=B, H=H, F=F, N=N,
+                              dk=dk, dv=dv, want_out=False, want_states=True)["states"]     # [B, H, F, dv, dk]
+    assert rel_err(ss.float().permute(0, 2, 1, 3, 4).cpu().numpy(), st) <= 1e-2
+    dd = d_out.cuda()
+    dsf = d_sf.cuda()
+    g_re = api.frame_backward(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], xd["state_in"], dd, dsf)
+    g_sv = api.frame_backward_saved(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], xd["state_in"], sa, ss, dd,
+                                    dsf)
+    api.sync_status()
+    names = ("dq", "dk", "dv", "d_alpha", "d_beta", "d_state_in")
+    for n, a, b in zip(names, g_re, g_sv):
+        assert torch.equal(a, b), n
+    ref = oracle.frame_backward(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["state_in"], d_out, d_sf,
+                                B=B, H=H, F=F, N=N, dk=dk, dv=dv)
+    for n, t in zip(names, g_sv):
+        assert rel_err(t.float().cpu().numpy(), ref[n]) <= TOL_GRAD, n

@@ -49,7 +49,8 @@ def test_hash_ignores_the_step_launcher_but_not_the_forward_sources():
     assert same == base
     # a change to a forward kernel, the shared PTX header or the forward's
     # launch code changes it
-    for f in ("gdn_k1_contract.cuh", "gdn_k3_output.cuh", "gdn_ptx.cuh"):
+    for f in ("gdn_fwd_single.cuh", "gdn_scan_head.cuh", "gdn_k1_contract.cuh", "gdn_k1_pair.cuh", "gdn_k3_output.cuh",
+              "gdn_ptx.cuh"):
         assert bench.kernel_source_sha(edited(f, b"#pragma once", b"#pragma  once")) != base
     assert bench.kernel_source_sha(edited("gdn_api.cu", b"launch_phases(", b"launch_phases (")) != base
     # the step and backward kernels' files are not part of it
