@@ -175,16 +175,26 @@ class _Nvml:
             raise RuntimeError("no NVML handle")
         return h
 
-    def sample(self, h):
+    def max_sm_mhz(self, h):
+        """The SM clock's maximum; it does not change while the process runs,
+        and the query takes about a millisecond (measured on B300), so it is
+        read once, outside the timed region."""
+        mx = self.ct.c_uint()
+        if self.lib.nvmlDeviceGetMaxClockInfo(h, self.SM, self.ct.byref(mx)) != 0:
+            raise RuntimeError("no NVML max clock")
+        return float(mx.value)
+
+    def sample(self, h, max_mhz):
+        """Current SM clock, power and throttle reasons: each query about a
+        microsecond."""
         ct = self.ct
-        sm, mx, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        sm, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
         if (self.lib.nvmlDeviceGetClockInfo(h, self.SM, ct.byref(sm)) != 0
-                or self.lib.nvmlDeviceGetMaxClockInfo(h, self.SM, ct.byref(mx)) != 0
                 or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons(h, ct.byref(rs)) != 0):
             return None
         if self.lib.nvmlDeviceGetPowerUsage(h, ct.byref(pw)) != 0:
             pw.value = 0
-        return (float(sm.value), float(mx.value), pw.value / 1000.0,
+        return (float(sm.value), max_mhz, pw.value / 1000.0,
                 {n for n, b in self.REASONS.items() if rs.value & b})
 
 
@@ -210,10 +220,11 @@ class ClockSampler:
         try:
             nv = _Nvml()
             h = nv.handle(self.pci_bus_id, self.gpu_index)
+            max_mhz = nv.max_sm_mhz(h)
 
             def poll():
                 while not self._stop.is_set():
-                    s = nv.sample(h)
+                    s = nv.sample(h, max_mhz)
                     if s is None:
                         break
                     self.samples.append((time.perf_counter(),) + s)

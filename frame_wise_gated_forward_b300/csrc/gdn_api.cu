@@ -392,19 +392,6 @@ bool encode_inputs(CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tq, const void
            encode_tokens(tq, q, BF, N, H, dk, rows_q);
 }
 
-// per-item fp32 matrix [items, rows_total, cols], 128-byte swizzle, box (32, rows, 1)
-bool encode_mats_f32_sw(CUtensorMap* m, const void* base, long long items, int rows_total, int cols, int rows) {
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows_total),
-                                static_cast<cuuint64_t>(items)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 4,
-                                   static_cast<cuuint64_t>(rows_total) * cols * 4};
-    const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(rows), 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // ------------------------------------------------------------- the pass
 struct PassArgs {
     const void *q, *k, *v;
@@ -607,12 +594,13 @@ int single_pass_heads(const PassArgs& a, const DeviceState* ds) {
 }
 
 // Ring frames: as many as keep the three rings within ~24 MiB (so they stay
-// in L2 next to the streaming inputs), at least 4, at most F.
+// in L2 next to the streaming inputs), at least 4, at most F.  A forced depth
+// is at least 2: the scan publishes frame f's image only once frame f + 1's
+// store is under way, so with one slot it would wait on itself.
 int single_pass_ring(const PassArgs& a) {
     const int forced = g_single_ring.load();
-    if (forced > 0) return std::min(forced, a.F);
-    const size_t per_frame = static_cast<size_t>(a.B) * a.H *
-                             (static_cast<size_t>(a.dk) * a.dk * 2 + static_cast<size_t>(a.dv) * a.dk * 6);
+    if (forced > 0) return std::min(std::max(forced, 2), a.F);
+    const size_t per_frame = static_cast<size_t>(a.B) * a.H * (2 * gdn::RING_TILE_BF16 + gdn::RING_TILE_F32);
     const int w = static_cast<int>(std::max<size_t>(4, (size_t(24) << 20) / per_frame));
     return std::min(w, a.F);
 }
@@ -627,9 +615,10 @@ SingleLayout single_layout(const PassArgs& a) {
     L.ring = single_pass_ring(a);
     L.slots = static_cast<long long>(a.B) * L.ring * a.H;
     L.a_off = 0;
-    L.u_off = align256(L.a_off + static_cast<size_t>(L.slots) * a.dk * a.dk * 2);
-    L.s_off = align256(L.u_off + static_cast<size_t>(L.slots) * a.dv * a.dk * 4);
-    L.c_off = align256(L.s_off + static_cast<size_t>(L.slots) * a.dv * a.dk * 2);
+    // whole 128 x 128 ring tiles (zero-padded for d = 64) in the consumers' shared-memory image
+    L.u_off = align256(L.a_off + static_cast<size_t>(L.slots) * gdn::RING_TILE_BF16);
+    L.s_off = align256(L.u_off + static_cast<size_t>(L.slots) * gdn::RING_TILE_F32);
+    L.c_off = align256(L.s_off + static_cast<size_t>(L.slots) * gdn::RING_TILE_BF16);
     L.total = align256(L.c_off + static_cast<size_t>(L.slots) * 4 * 4);
     return L;
 }
@@ -647,13 +636,10 @@ gdn_status launch_single(const PassArgs& a, uint8_t* ws, const SingleLayout& L, 
     int* au_free = cnt + L.slots;
     int* s_ready = cnt + 2 * L.slots;
     int* s_free = cnt + 3 * L.slots;
-    CUtensorMap tm_k, tm_v, tm_q, tm_out, tm_A, tm_U, tm_S;
+    CUtensorMap tm_k, tm_v, tm_q, tm_out;
     const bool enc_in =
         encode_inputs(&tm_k, &tm_v, &tm_q, a.q, a.k, a.v, a.fmt, BF, a.N, a.H, a.dk, a.dv, k1::CHUNK, k3::TILE_M);
-    if (!enc_in || !encode_tokens(&tm_out, a.out, BF, a.N, a.H, a.dv, 32) ||
-        !encode_mats(&tm_A, A_r, L.slots, a.dk, a.dk, 128) || !encode_mats_f32_sw(&tm_U, U_r, L.slots, a.dv, a.dk, 128) ||
-        !encode_mats(&tm_S, S_r, L.slots, a.dv, a.dk, 128))
-        return GDN_ERR_LAUNCH;
+    if (!enc_in || !encode_tokens(&tm_out, a.out, BF, a.N, a.H, a.dv, 32)) return GDN_ERR_LAUNCH;
     const unsigned long long lim = g_wait_limit_ns.load();
     if (ev) cudaEventRecord(ev[0], stream);
     if (cudaMemsetAsync(cnt, 0, static_cast<size_t>(L.slots) * 16, stream) != cudaSuccess) return GDN_ERR_LAUNCH;
@@ -665,6 +651,7 @@ gdn_status launch_single(const PassArgs& a, uint8_t* ws, const SingleLayout& L, 
     fwd::Counts c;
     c.s_ready = s_ready;
     c.s_free = s_free;
+    c.s_ring = S_r;
     c.n_scan = a.B * a.H;
     const int rest = ds->sms - c.n_scan;
     const int forced = g_single_contract.load();
@@ -726,6 +713,9 @@ gdn_status launch_single(const PassArgs& a, uint8_t* ws, const SingleLayout& L, 
     p3.wait_limit_ns = lim;
 
     k2h::Params p2;
+    p2.A_ring = A_r;
+    p2.U_ring = U_r;
+    p2.S_ring = S_r;
     p2.alpha = a.alpha;
     p2.state_in = a.state_in;
     p2.state_out = a.state_out;
@@ -748,7 +738,7 @@ gdn_status launch_single(const PassArgs& a, uint8_t* ws, const SingleLayout& L, 
     p2.wait_limit_ns = lim;
 
     const int grid = c.n_scan + c.n_contract + n_out;
-    void* args[] = {&tm_k, &tm_v, &tm_A, &tm_U, &tm_S, &tm_q, &tm_out, &p1, &p2, &p3, &c};
+    void* args[] = {&tm_k, &tm_v, &tm_q, &tm_out, &p1, &p2, &p3, &c};
     const void* fn = fwd_fn(a.fmt);
     const size_t smem = fwd_smem(a.fmt);
     if (cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(fwd::THREADS), args, smem, stream) != cudaSuccess) {

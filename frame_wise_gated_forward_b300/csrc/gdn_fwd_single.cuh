@@ -15,7 +15,9 @@
 //   the rest                          O_f = Q_f S_f^T for whole items in scan
 //                                     order (gdn_k3_output.cuh, ring mode)
 // Step s of the scan of head (b, h) uses ring slot (b * W + s % W) * H + h of
-// three rings: A (bf16), U (fp32) and the bf16 state image S.  Per slot four
+// three rings: A (bf16), U (fp32) and the bf16 state image S, each slot one
+// zero-padded 128 x 128 tile in its consumer's shared-memory image (ring_off
+// in gdn_ptx.cuh), copied in and out as one contiguous bulk copy.  Per slot four
 // counts order the hand-offs (all raised with release semantics and read
 // with bounded acquire waits):
 //   au_ready  frames of A/U written by the contraction   -> the scan loads
@@ -53,6 +55,7 @@ constexpr size_t smem_bytes() {
 struct Counts {
     int* s_ready;   // [B][W][H]
     int* s_free;    // [B][W][H]
+    const __nv_bfloat16* s_ring;   // [B][W][H] state image tiles
     int n_scan;     // = B * H
     int n_contract;
     int pair;       // bf16 only: the contraction CTAs take head pairs (gdn_k1_pair.cuh; tm_k, tm_v are pair maps)
@@ -61,15 +64,13 @@ struct Counts {
 template <int FMT>
 __global__ void __launch_bounds__(THREADS, 1)
     forward_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                   const __grid_constant__ CUtensorMap tm_A, const __grid_constant__ CUtensorMap tm_U,
-                   const __grid_constant__ CUtensorMap tm_S, const __grid_constant__ CUtensorMap tm_q,
-                   const __grid_constant__ CUtensorMap tm_out, const k1::Params p1, const k2h::Params p2,
-                   const k3::Params p3, const Counts c) {
+                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
+                   const k1::Params p1, const k2h::Params p2, const k3::Params p3, const Counts c) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int cta = static_cast<int>(blockIdx.x);
     if (cta < c.n_scan) {
-        k2h::scan_head_role(&tm_A, &tm_U, &tm_S, p2, cta, smem);
+        k2h::scan_head_role(p2, cta, smem);
     } else if (cta < c.n_scan + c.n_contract) {
         if constexpr (FMT == FMT_BF16) {
             if (c.pair) {
@@ -89,7 +90,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         sc.flag_target = 1;   // one scan CTA per head
         sc.ring = p2.ring;
         sc.s_free = c.s_free;
-        k3::output_role<FMT>(&tm_q, &tm_S, &tm_out, p3, sc, smem);
+        sc.s_ring = c.s_ring;
+        k3::output_role<FMT>(&tm_q, nullptr, &tm_out, p3, sc, smem);
     }
 }
 

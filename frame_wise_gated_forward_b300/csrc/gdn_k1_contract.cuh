@@ -134,7 +134,9 @@ struct Params {
     // Ring mode (single-pass forward; 0 = off): units are whole items in scan
     // order -- step s of the scan (frame s, or F-1-s when reversed) for every
     // (b, h) -- and A_f, U_f go to ring slot (b * ring + s % ring) * H + h of
-    // A_ws / U_ws instead of the item's own place.  Before a slot is
+    // A_ws / U_ws instead of the item's own place, as whole zero-padded ring
+    // tiles (RING_TILE_BF16 / RING_TILE_F32 bytes, the swizzled layout of
+    // ring_off in gdn_ptx.cuh).  Before a slot is
     // rewritten the scan must have read its previous frame (au_free counts
     // frames read per slot); after the stores au_ready counts one more frame.
     int ring;
@@ -586,8 +588,36 @@ __device__ __forceinline__ void contract_role(const CUtensorMap& tm_k, const CUt
             // partial sums in the same element order
             float* part = u.split < 0 ? nullptr
                                       : p.partial + (static_cast<size_t>(u.item - p.whole) * p.split_per + u.split) * per;
-            const size_t dst = static_cast<size_t>(u.slot >= 0 ? u.slot : u.item);   // A/U destination
-            {
+            const size_t dst = static_cast<size_t>(u.item);   // A/U destination outside ring mode
+            if (u.slot >= 0) {
+                // ring slot: the whole zero-padded 128 x 128 tiles (D is exactly 0
+                // past dk and dv), laid out as the scan's shared-memory image
+                uint8_t* At = reinterpret_cast<uint8_t*>(p.A_ws) + static_cast<size_t>(u.slot) * RING_TILE_BF16;
+                uint8_t* Ut = reinterpret_cast<uint8_t*>(p.U_ws) + static_cast<size_t>(u.slot) * RING_TILE_F32;
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    uint32_t r32[32];
+                    tmem_ld32(tbase + c0, r32);
+                    tmem_wait_ld();
+                    const float sa = LP ? p.a_scale : 1.0f;
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8)
+                        *reinterpret_cast<uint4*>(At + ring_off(j, 2 * (c0 + 8 * q8))) = make_uint4(
+                            pack_bf16x2(sa * __uint_as_float(r32[8 * q8 + 0]), sa * __uint_as_float(r32[8 * q8 + 1])),
+                            pack_bf16x2(sa * __uint_as_float(r32[8 * q8 + 2]), sa * __uint_as_float(r32[8 * q8 + 3])),
+                            pack_bf16x2(sa * __uint_as_float(r32[8 * q8 + 4]), sa * __uint_as_float(r32[8 * q8 + 5])),
+                            pack_bf16x2(sa * __uint_as_float(r32[8 * q8 + 6]), sa * __uint_as_float(r32[8 * q8 + 7])));
+                }
+                // U[i][j] (row i = D column 128 + i): a warp writes one 128-byte line per i
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    uint32_t r32[32];
+                    tmem_ld32(tbase + 128 + c0, r32);
+                    tmem_wait_ld();
+                    const float su = LP ? p.u_scale : 1.0f;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        *reinterpret_cast<float*>(Ut + ring_off(c0 + t, 4 * j)) = su * __uint_as_float(r32[t]);
+                }
+            } else {
                 // A: row j of D holds A[j][0..dk); stored as row j (A is symmetric)
                 for (int c0 = 0; c0 < p.dk; c0 += 32) {
                     uint32_t r32[32];

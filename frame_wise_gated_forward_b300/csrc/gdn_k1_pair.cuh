@@ -266,14 +266,12 @@ __device__ __forceinline__ void contract_pair_role(const CUtensorMap& tm_k, cons
                         }
                         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
                         const float inv = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
-                        sb *= inv;
-                        const k1::BSplit n2 = k1::bsplit(inv);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) x[i] = k1::bscale(x[i], n2);   // normalized k, the B operand
+                        sb *= inv;   // beta K = k * (beta / |k|), from the raw k (one rounding)
                         if (live) {
+                            const k1::BSplit n2 = k1::bsplit(inv);
 #pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                *reinterpret_cast<uint4*>(krow + (((i + r + 4 * bx) & 7) << 4)) = x[i];
+                            for (int i = 0; i < 8; ++i)   // normalized k, the B operand
+                                *reinterpret_cast<uint4*>(krow + (((i + r + 4 * bx) & 7) << 4)) = k1::bscale(x[i], n2);
                         }
                     }
                     if (!live) {
@@ -322,17 +320,31 @@ __device__ __forceinline__ void contract_pair_role(const CUtensorMap& tm_k, cons
                     tmem_ld32(tb + c0, a32);
                     tmem_ld32(tb + 128 + c0, u32);
                     tmem_wait_ld();
+                    // ring mode: the tiles in the scan's shared-memory image (ring_off)
+                    const bool rm = u.slot0 >= 0;
+                    uint8_t* At = reinterpret_cast<uint8_t*>(p.A_ws) + dst * RING_TILE_BF16;
+                    uint8_t* Ut = reinterpret_cast<uint8_t*>(p.U_ws) + dst * RING_TILE_F32;
                     __nv_bfloat16* Arow = p.A_ws + (dst * 128 + j) * 128 + c0;
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8)
-                        *reinterpret_cast<uint4*>(Arow + 8 * q8) = make_uint4(
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        const uint4 v4 = make_uint4(
                             pack_bf16x2(__uint_as_float(a32[8 * q8 + 0]), __uint_as_float(a32[8 * q8 + 1])),
                             pack_bf16x2(__uint_as_float(a32[8 * q8 + 2]), __uint_as_float(a32[8 * q8 + 3])),
                             pack_bf16x2(__uint_as_float(a32[8 * q8 + 4]), __uint_as_float(a32[8 * q8 + 5])),
                             pack_bf16x2(__uint_as_float(a32[8 * q8 + 6]), __uint_as_float(a32[8 * q8 + 7])));
+                        if (rm)
+                            *reinterpret_cast<uint4*>(At + ring_off(j, 2 * (c0 + 8 * q8))) = v4;
+                        else
+                            *reinterpret_cast<uint4*>(Arow + 8 * q8) = v4;
+                    }
                     float* Ucol = p.U_ws + dst * 128 * 128 + j;
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) Ucol[static_cast<size_t>(c0 + t) * 128] = __uint_as_float(u32[t]);
+                    for (int t = 0; t < 32; ++t) {
+                        if (rm)
+                            *reinterpret_cast<float*>(Ut + ring_off(c0 + t, 4 * j)) = __uint_as_float(u32[t]);
+                        else
+                            Ucol[static_cast<size_t>(c0 + t) * 128] = __uint_as_float(u32[t]);
+                    }
                 }
             }
             tc_fence_before();

@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(k3::threads<FMT>(), 1)
         sc.flag_target = p2.rsplit;
         sc.ring = 0;
         sc.s_free = nullptr;
+        sc.s_ring = nullptr;
         k3::output_role<FMT>(&tm_q, &tm_S_load, &tm_out, p3, sc, smem);
     }
 }

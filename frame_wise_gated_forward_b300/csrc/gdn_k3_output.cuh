@@ -63,6 +63,7 @@ static_assert((3 * QSTAGES + 2 * SSTAGES + 2 * ACCS + 1 + 2 * NSLOTS) * 8 + 8 <=
 constexpr size_t SMEM_BYTES =
     1024 + QSTAGES * QTILE_BYTES + SSTAGES * STILE_BYTES + 4 * 2 * OSTAGE_BYTES + BAR_BYTES + NSLOTS * TILE_M * 4;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
+static_assert(STILE_BYTES == RING_TILE_BF16, "a state stage holds one ring tile");
 
 struct Params {
     int B, H, F, N, dk, dv;
@@ -90,9 +91,12 @@ struct Sched {
     // ring mode (single-pass forward, 0 = off): the state of scan step s of
     // head (b, h) sits in slot (b * ring + s % ring) * H + h, which holds frames
     // s, s + ring, ... in turn; flags count published slices per slot, and
-    // s_free counts this role's loads of each slot's image
+    // s_free counts this role's loads of each slot's image; the images are
+    // whole ring tiles (RING_TILE_BF16 bytes, ring_off layout of gdn_ptx.cuh)
+    // at s_ring, each loaded with one bulk copy
     int ring;
     int* s_free;
+    const __nv_bfloat16* s_ring;
 
     __device__ __forceinline__ bool segment(const Params& p, int k, long long& item, int& nb, int& ne) const {
         long long slot;
@@ -196,7 +200,7 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(tm_q);
-        prefetch_tmap(tm_s);
+        if (sc.ring == 0) prefetch_tmap(tm_s);
         prefetch_tmap(tm_out);
     }
     if (warp == 1) {
@@ -228,10 +232,17 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
                         break;
                     fence_proxy_async_global();  // the published state is read through the async proxy
                 }
-                mbar_arrive_expect_tx(&sfull[ss], sboxes * BOX_BYTES);
-                for (int bx = 0; bx < sboxes; ++bx)
-                    tma_load_3d(sring + ss * STILE_BYTES + bx * BOX_BYTES, tm_s, &sfull[ss], 64 * bx, 0,
-                                static_cast<int>(slot));
+                if (sc.ring > 0) {
+                    mbar_arrive_expect_tx(&sfull[ss], STILE_BYTES);
+                    bulk_load(sring + ss * STILE_BYTES,
+                              reinterpret_cast<const uint8_t*>(sc.s_ring) + static_cast<size_t>(slot) * RING_TILE_BF16,
+                              STILE_BYTES, &sfull[ss]);
+                } else {
+                    mbar_arrive_expect_tx(&sfull[ss], sboxes * BOX_BYTES);
+                    for (int bx = 0; bx < sboxes; ++bx)
+                        tma_load_3d(sring + ss * STILE_BYTES + bx * BOX_BYTES, tm_s, &sfull[ss], 64 * bx, 0,
+                                    static_cast<int>(slot));
+                }
                 ++s_issued;
                 for (int nt = nb; nt < ne; ++nt) {
                     if constexpr (LP) {
@@ -273,8 +284,6 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
             for (int k = 0; !stop && !*abort_flag && sc.segment(p, k, item, nb, ne, slot, use); ++k) {
                 if (k > 0) { if (++ss == SSTAGES) { ss = 0; sph ^= 1; } }
                 if (!mbar_wait(&sfull[ss], sph, p.wait_limit_ns, abort_flag, 3110000 + (k & 0xffff))) break;
-                // ring mode: the image is in shared memory, the scan may reuse its slot
-                if (sc.ring > 0) red_release_add(sc.s_free + slot, 1);
                 for (int nt = nb; nt < ne; ++nt) {
                     if (!mbar_wait(&tempty[acc], aph ^ 1, p.wait_limit_ns, abort_flag) ||
                         !mbar_wait(LP ? &qdec[qs] : &qfull[qs], qph, p.wait_limit_ns, abort_flag)) {
@@ -297,6 +306,9 @@ __device__ __forceinline__ void output_role(const CUtensorMap* tm_q, const CUten
                     if (++qs == QS) { qs = 0; qph ^= 1; }
                     if (++acc == ACCS) { acc = 0; aph ^= 1; }
                 }
+                // ring mode: the image is in shared memory, the scan may reuse its slot
+                // (a release, which takes a while, so it follows the item's MMAs)
+                if (sc.ring > 0 && !stop) red_release_add(sc.s_free + slot, 1);
             }
             mma_commit(final_bar);
             mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
@@ -559,6 +571,7 @@ __global__ void __launch_bounds__(threads<FMT>(), 1)
     sc.flag_target = 0;
     sc.ring = 0;
     sc.s_free = nullptr;
+    sc.s_ring = nullptr;
     output_role<FMT>(&tm_q, &tm_s, &tm_out, p, sc, smem);
 }
 

@@ -172,6 +172,35 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, const void* s
         "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
 }
+// Untiled bulk copies (one contiguous run; both addresses 16-byte aligned,
+// the size a multiple of 16).  A contiguous run streams several times faster
+// than a tiled box of the same bytes whose rows lie apart.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+
+// Ring tiles of the single-pass forward (A_f bf16, U_f fp32, the bf16 state
+// images) are kept in global memory in exactly the shared-memory image their
+// consumer works on: 128 x 128 elements, zero-padded, as boxes of 128 rows x
+// 128 bytes with the 128-byte swizzle (16-byte chunk c of row r at chunk
+// c ^ (r % 8)), the boxes one after another.  A tile then moves between L2
+// and shared memory as one contiguous bulk copy.
+constexpr uint32_t RING_BOX_BYTES = 128 * 128;
+constexpr uint32_t RING_TILE_BF16 = 2 * RING_BOX_BYTES;   // 128 x 128 bf16
+constexpr uint32_t RING_TILE_F32 = 4 * RING_BOX_BYTES;    // 128 x 128 fp32
+// byte offset of byte `x` of row `r` of a ring tile (x = column * element size)
+__host__ __device__ __forceinline__ uint32_t ring_off(int r, int x) {
+    return static_cast<uint32_t>((x >> 7) * RING_BOX_BYTES + r * 128 + ((((x >> 4) & 7) ^ (r & 7)) << 4) + (x & 15));
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {

@@ -17,17 +17,21 @@
 // tensor memory, its row of U_f from the TMA-loaded tile, writes the new fp32
 // row back to tensor memory and its bf16 row into the image with 16-byte
 // stores.  One image buffer suffices: the image is rewritten only after the
-// MMA that reads it has retired and the TMA store that publishes it has read
-// it.
+// MMA that reads it has retired and the bulk store that publishes it has read
+// it; the update itself runs before that wait, the new row held in registers.
 //
 // A_f and U_f come from ring slots of the workspace that contraction CTAs of
 // the same launch fill (a per-slot count of frames written, raised with
 // release semantics after the slot's stores); the loader warp waits (bounded,
-// acquire) for the count, then copies the slot by TMA.  Once the copy has
-// landed the MMA warp hands the slot back (a count of frames read).  The
-// publisher warp stores each frame's image into the ring slot of the output
-// CTAs, after they have loaded the slot's previous occupant, and raises the
-// slot's ready count once the store has completed.
+// acquire) for the count, then copies the slot's two tiles with one bulk
+// copy each: the contraction writes them in this role's shared-memory image
+// (ring_off in gdn_ptx.cuh), so 96 KB move as two contiguous runs instead of
+// 768 separate 128-byte rows, which bounded the scan at about 2 us a frame.
+// Once the copy has landed the MMA warp hands the slot back (a count of
+// frames read).  The publisher warp stores each frame's image into the ring
+// slot of the output CTAs the same way (one 32 KB bulk store), after they
+// have loaded the slot's previous occupant, and raises the slot's ready count
+// once the store has completed.
 //
 // Warp roles (352 threads): warps 0-7 compute, warp 8 loads A_f / U_f, warp 9
 // issues the MMAs, warp 10 publishes the images.  The image of the initial
@@ -56,11 +60,15 @@ constexpr int OFF_BAR = OFF_IMG + ATILE;
 constexpr int BAR_BYTES = 256;
 constexpr size_t SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
+static_assert(ATILE == RING_TILE_BF16 && UTILE == RING_TILE_F32, "a stage holds one ring tile of each");
 constexpr uint32_t TMEM_COLS = 256;
 constexpr uint32_t T_C = 0;                // C = S_img A_f
 constexpr uint32_t T_S = 128;              // fp32 master state
 
 struct Params {
+    const __nv_bfloat16* A_ring;   // [B][W][H] ring tiles of A_f (RING_TILE_BF16 bytes each)
+    const float* U_ring;           // [B][W][H] ring tiles of U_f (RING_TILE_F32 bytes each)
+    __nv_bfloat16* S_ring;         // [B][W][H] ring tiles of the state images (RING_TILE_BF16 bytes each)
     const float* alpha;     // [B, F, H]
     const float* state_in;  // [B, H, dv, dk] or nullptr
     float* state_out;       // [B, H, dv, dk] or nullptr
@@ -87,13 +95,13 @@ __device__ __forceinline__ float decay_gate(const Params& p, float x) {
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + (((c ^ (r & 7))) << 4); }
 
 // The scan of head `cta` = b * H + h.  Needs THREADS threads.
-__device__ __forceinline__ void scan_head_role(const CUtensorMap* tm_A, const CUtensorMap* tm_U,
-                                               const CUtensorMap* tm_S, const Params& p, int cta, uint8_t* smem) {
+__device__ __forceinline__ void scan_head_role(const Params& p, int cta, uint8_t* smem) {
     uint8_t* ring = smem;
     uint8_t* img = smem + OFF_IMG;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    uint64_t* afull = bars;                 // [AS] loader -> compute, MMA
-    uint64_t* slot_free = afull + AS;       // [AS] compute -> loader
+    uint64_t* afull = bars;                 // [AS] loader -> MMA: A_f landed
+    uint64_t* ufull = afull + AS;           // [AS] loader -> compute, MMA: U_f landed
+    uint64_t* slot_free = ufull + AS;       // [AS] compute -> loader
     uint64_t* mma_done = slot_free + AS;    // MMA -> compute
     uint64_t* img_init = mma_done + 1;      // compute -> MMA: the image of the state before frame 0
     uint64_t* img_ready = img_init + 1;     // compute -> MMA, publisher: the image after frame f
@@ -105,18 +113,14 @@ __device__ __forceinline__ void scan_head_role(const CUtensorMap* tm_A, const CU
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int b = cta / p.H, h = cta % p.H;
-    const int aboxes = p.dk > 64 ? 2 : 1;
-    const int uboxes = (p.dk + 31) / 32;
     const int nk = (p.dk + 15) / 16;
     auto fr = [&](int s) { return p.reverse ? p.F - 1 - s : s; };
     auto rslot = [&](int s) { return (b * p.ring + s % p.ring) * p.H + h; };
 
-    // boxes of A_f and U_f that are never loaded (dk < 128) must read as zero
-    if (p.dk < 128)
-        for (int i = tid; i < AS * STAGE / 16; i += blockDim.x) reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         for (int s = 0; s < AS; ++s) {
             mbar_init(&afull[s], 1);
+            mbar_init(&ufull[s], 1);
             mbar_init(&slot_free[s], COMPUTE_THREADS);
         }
         mbar_init(mma_done, 1);
@@ -126,9 +130,6 @@ __device__ __forceinline__ void scan_head_role(const CUtensorMap* tm_A, const CU
         mbar_init(final_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tmap(tm_A);
-        prefetch_tmap(tm_U);
-        prefetch_tmap(tm_S);
     }
     if (warp == 0) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -183,15 +184,13 @@ __device__ __forceinline__ void scan_head_role(const CUtensorMap* tm_A, const CU
             const int slot = f % AS;
             const float a_f = a_next;
             if (f + 1 < p.F) a_next = decay_gate(p, __ldg(p.alpha + static_cast<size_t>(b * p.F + fr(f + 1)) * p.H + h));
-            bool ok = mbar_wait(&afull[slot], static_cast<uint32_t>((f / AS) & 1), p.wait_limit_ns, abort_flag,
+            bool ok = mbar_wait(&ufull[slot], static_cast<uint32_t>((f / AS) & 1), p.wait_limit_ns, abort_flag,
                                 1010000 + f);
             ok = ok && mbar_wait(mma_done, static_cast<uint32_t>(f & 1), p.wait_limit_ns, abort_flag, 1020000 + f);
-            // the image may be rewritten once the store of the previous one has read it
-            ok = ok && (f == 0 || mbar_wait(img_free, static_cast<uint32_t>((f - 1) & 1), p.wait_limit_ns, abort_flag,
-                                            1030000 + f));
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             const uint8_t* ut = ring + slot * STAGE + ATILE;
+            uint4 im[2][4];   // the new row's bf16 image, written once the previous image is stored
 #pragma unroll
             for (int sc = 0; sc < 2; ++sc) {
                 const int c0 = 64 * ch + 32 * sc;
@@ -213,21 +212,31 @@ __device__ __forceinline__ void scan_head_role(const CUtensorMap* tm_A, const CU
                     }
                 }
                 tmem_st32(tw + T_S + c0, ss);
-                uint8_t* row = img + (c0 >> 6) * ABOX;
-                const int cb = (c0 & 63) >> 3;
 #pragma unroll
                 for (int t = 0; t < 4; ++t)
-                    *reinterpret_cast<uint4*>(row + sw128(i, cb + t)) = make_uint4(
+                    im[sc][t] = make_uint4(
                         pack_bf16x2(__uint_as_float(ss[8 * t + 0]), __uint_as_float(ss[8 * t + 1])),
                         pack_bf16x2(__uint_as_float(ss[8 * t + 2]), __uint_as_float(ss[8 * t + 3])),
                         pack_bf16x2(__uint_as_float(ss[8 * t + 4]), __uint_as_float(ss[8 * t + 5])),
                         pack_bf16x2(__uint_as_float(ss[8 * t + 6]), __uint_as_float(ss[8 * t + 7])));
             }
+            mbar_arrive(&slot_free[slot]);   // U_f read, the MMA that read A_f retired
+            // the image may be rewritten once the store of the previous one has read it
+            ok = f == 0 || mbar_wait(img_free, static_cast<uint32_t>((f - 1) & 1), p.wait_limit_ns, abort_flag,
+                                     1030000 + f);
+            if (!__all_sync(0xffffffffu, ok)) break;
+#pragma unroll
+            for (int sc = 0; sc < 2; ++sc) {
+                const int c0 = 64 * ch + 32 * sc;
+                uint8_t* row = img + (c0 >> 6) * ABOX;
+                const int cb = (c0 & 63) >> 3;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) *reinterpret_cast<uint4*>(row + sw128(i, cb + t)) = im[sc][t];
+            }
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(img_ready);
-            mbar_arrive(&slot_free[slot]);   // U_f read, the MMA that read A_f retired
         }
         // tcgen05.ld is warp-collective: every lane loads, only rows < dv are stored
         if (__all_sync(0xffffffffu, f == p.F) && p.state_out != nullptr) {
@@ -255,8 +264,6 @@ __device__ __forceinline__ void scan_head_role(const CUtensorMap* tm_A, const CU
                 if (!mbar_wait(&afull[slot], static_cast<uint32_t>((f / AS) & 1), p.wait_limit_ns, abort_flag,
                                1110000 + f))
                     break;
-                // the slot's contents are in shared memory: the contraction may refill it
-                red_release_add(p.au_free + rslot(f), 1);
                 // the image of the state before frame f
                 if (!(f == 0 ? mbar_wait(img_init, 0, p.wait_limit_ns, abort_flag, 1120000)
                              : mbar_wait(img_ready, static_cast<uint32_t>((f - 1) & 1), p.wait_limit_ns, abort_flag,
@@ -271,6 +278,12 @@ __device__ __forceinline__ void scan_head_role(const CUtensorMap* tm_A, const CU
                              kk > 0 ? 1u : 0u);
                 }
                 mma_commit(mma_done);
+                // both tiles of the slot are in shared memory: the contraction may
+                // refill it (a release, which takes a while, so it follows the MMAs)
+                if (!mbar_wait(&ufull[slot], static_cast<uint32_t>((f / AS) & 1), p.wait_limit_ns, abort_flag,
+                               1130000 + f))
+                    break;
+                red_release_add(p.au_free + rslot(f), 1);
             }
             mma_commit(final_bar);
             mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
@@ -284,19 +297,19 @@ __device__ __forceinline__ void scan_head_role(const CUtensorMap* tm_A, const CU
                 fence_proxy_async_global();  // the stores' writes ordered before the releases
                 for (; published < f_end; ++published) red_release_add(p.s_ready + rslot(published), 1);
             };
-            const int sboxes = p.dk > 64 ? 2 : 1;
             int f = 0;
             for (; f < p.F; ++f) {
+                // the slot's previous image has been loaded by every output CTA that
+                // reads it (asked before the image is ready, so that the round trip
+                // to L2 overlaps the frame's update instead of delaying the store)
+                if (f >= p.ring && !wait_count_geq(p.s_free + rslot(f), (f / p.ring) * p.s_units, p.wait_limit_ns,
+                                                   abort_flag, 1220000 + f))
+                    break;
                 if (!mbar_wait(img_ready, static_cast<uint32_t>(f & 1), p.wait_limit_ns, abort_flag, 1210000 + f))
                     break;
-                // the slot's previous image has been loaded by every output CTA that reads it
-                if (f >= p.ring) {
-                    if (!wait_count_geq(p.s_free + rslot(f), (f / p.ring) * p.s_units, p.wait_limit_ns, abort_flag,
-                                        1220000 + f))
-                        break;
-                    fence_proxy_async_global();
-                }
-                for (int bx = 0; bx < sboxes; ++bx) tma_store_3d(tm_S, img + bx * ABOX, 64 * bx, 0, rslot(f));
+                if (f >= p.ring) fence_proxy_async_global();
+                bulk_store(reinterpret_cast<uint8_t*>(p.S_ring) + static_cast<size_t>(rslot(f)) * RING_TILE_BF16, img,
+                           RING_TILE_BF16);
                 bulk_commit();
                 bulk_wait_read<0>();
                 mbar_arrive(img_free);
@@ -312,21 +325,28 @@ __device__ __forceinline__ void scan_head_role(const CUtensorMap* tm_A, const CU
             int issued = 0;
             for (int f = 0; f < p.F; ++f) {
                 const int slot = f % AS;
+                // the contraction's count first (an L2 round trip that overlaps the
+                // wait for the stage), then the stage
+                if (!wait_count_geq(p.au_ready + rslot(f), f / p.ring + 1, p.wait_limit_ns, abort_flag, 1320000 + f))
+                    break;
                 if (f >= AS && !mbar_wait(&slot_free[slot], static_cast<uint32_t>(((f / AS) - 1) & 1),
                                           p.wait_limit_ns, abort_flag, 1310000 + f))
                     break;
-                if (!wait_count_geq(p.au_ready + rslot(f), f / p.ring + 1, p.wait_limit_ns, abort_flag, 1320000 + f))
-                    break;
                 fence_proxy_async_global();  // the contraction's stores are read through the async proxy
                 uint8_t* st = ring + slot * STAGE;
-                mbar_arrive_expect_tx(&afull[slot], aboxes * ABOX + uboxes * UBOX);
-                for (int bx = 0; bx < aboxes; ++bx) tma_load_3d(st + bx * ABOX, tm_A, &afull[slot], 64 * bx, 0, rslot(f));
-                for (int c = 0; c < uboxes; ++c)
-                    tma_load_3d(st + ATILE + c * UBOX, tm_U, &afull[slot], 32 * c, 0, rslot(f));
+                const size_t rs = static_cast<size_t>(rslot(f));
+                mbar_arrive_expect_tx(&afull[slot], RING_TILE_BF16);
+                bulk_load(st, reinterpret_cast<const uint8_t*>(p.A_ring) + rs * RING_TILE_BF16, RING_TILE_BF16,
+                          &afull[slot]);
+                mbar_arrive_expect_tx(&ufull[slot], RING_TILE_F32);
+                bulk_load(st + ATILE, reinterpret_cast<const uint8_t*>(p.U_ring) + rs * RING_TILE_F32, RING_TILE_F32,
+                          &ufull[slot]);
                 ++issued;
             }
-            for (int k = (issued > AS ? issued - AS : 0); k < issued; ++k)
+            for (int k = (issued > AS ? issued - AS : 0); k < issued; ++k) {
                 mbar_wait_drain(&afull[k % AS], static_cast<uint32_t>((k / AS) & 1), p.wait_limit_ns);
+                mbar_wait_drain(&ufull[k % AS], static_cast<uint32_t>((k / AS) & 1), p.wait_limit_ns);
+            }
         }
     }
 

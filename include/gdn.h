@@ -405,7 +405,8 @@ void gdn_set_fused_step(int on);
  * acquire waits), so HBM carries only the layer's own inputs and outputs.
  * on = 0: phase 1 as its own launch followed by phases 2 and 3
  * (gdn_set_fused_scan).  contract_ctas > 0 fixes the number of contraction
- * CTAs and ring_frames > 0 the ring depth in frames (0: automatic).  The
+ * CTAs and ring_frames > 0 the ring depth in frames (0: automatic; a
+ * forced depth is raised to at least 2 and capped at F).  The
  * schedules differ only in the order of rounding of the scan's S * A_f
  * product (the single pass multiplies by A_f's rows, the other schedules by
  * its columns; A_f is symmetric): results agree to bf16 rounding.  Applies

@@ -81,3 +81,35 @@ def test_gated_equals_plain_on_prenormalized_inputs():
     api.sync_status()
     assert rel_err(o1.float().cpu().numpy(), o2.float().cpu().numpy()) <= 1e-2
     assert rel_err(s1.cpu().numpy(), s2.cpu().numpy()) <= 5e-3
+
+
+@pytest.mark.parametrize("single", [True, False])
+def test_gated_contract_pairs_match_single_heads(single):
+    """Phase 1 on head pairs with the folded prologue (k normalized, beta =
+    sigmoid(b) inside the scalers) gives the same bits as one head at a time,
+    over more frames than the single pass's ring holds, and matches the
+    oracle."""
+    B, H, F, N, d = 1, 16, 14, 880, 128
+    x = inputs.draw_raw(B, H, F, N, d, d, seed=77, qk_std=1.0, s0_std=0.1)
+    xd = {k: v.cuda() for k, v in x.items()}
+
+    def run():
+        o, s = api.frame_forward_gated(xd["q"], xd["k"], xd["v"], xd["a_logit"], xd["b_logit"], ALPHA_SCALE,
+                                       xd["state_in"])
+        api.sync_status()
+        return o, s
+    api.set_single_pass(single)
+    try:
+        api.set_contract_pairs(True)
+        o1, s1 = run()
+        api.set_contract_pairs(False)
+        o2, s2 = run()
+    finally:
+        api.set_contract_pairs(False)
+        api.set_single_pass(True)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    toks = sample_tokens(B, F, N)
+    ref = oracle_gated(x, B, H, F, N, d, d, want_out=False, sample_tokens=toks)
+    flat = o1.view(-1, H, d)[torch.as_tensor(toks, device="cuda")].float().cpu().numpy()
+    assert rel_err(flat, ref["sample_out"]) <= TOL_OUT
+    assert rel_err(s1.cpu().numpy(), ref["state"]) <= TOL_STATE

@@ -215,7 +215,7 @@ def test_contract_pairs_match_single_heads(shape, sched):
         api.set_contract_pairs(False)
         o2, s2 = gpu_forward(xd)
     finally:
-        api.set_contract_pairs(True)
+        api.set_contract_pairs(False)
         api.set_single_pass(True)
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
     ref = oracle_run(x, B, H, F, N, dk, dv)
