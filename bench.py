@@ -364,11 +364,9 @@ def main():
     def step():
         api.frame_forward(xd["q"], xd["k"], xd["v"], xd["alpha"], xd["beta"], s_in, out=out, state_out=st)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    api.sync_status()
-
-    # ---------------------------------------------------------------- timed region
+    # the clock sampler starts before the warm-up, so that the GPU goes from the
+    # warm-up steps straight into the timed ones (an idle pause in between lets
+    # the clocks drop, and the first timed steps would pay for the ramp)
     cvd = [c for c in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if c.strip()]
     props = torch.cuda.get_device_properties(device)
     pci = None
@@ -377,6 +375,11 @@ def main():
     sampler = ClockSampler(cvd[local_rank].strip() if local_rank < len(cvd) else local_rank, pci)
     sampler.start()
     time.sleep(0.3)
+    for _ in range(max(3, args.warmup)):
+        step()
+    api.sync_status()
+
+    # ---------------------------------------------------------------- timed region
     torch.cuda.synchronize(device)
     replicas.barrier(device)
     torch.cuda.synchronize(device)
