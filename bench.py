@@ -151,59 +151,48 @@ def ncu_traffic(kernel):
     return None if k is None else k.get("dram_bytes_per_launch")
 
 
-class _Nvml:
-    """The few read-only NVML queries the clock sampler needs, through ctypes
-    on the driver's libnvidia-ml (no Python NVML package required)."""
-    SM = 1              # NVML_CLOCK_SM
-    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
-               "sw_power_cap": 0x4}
-
-    def __init__(self):
-        import ctypes
-        self.ct = ctypes
-        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
-        if self.lib.nvmlInit_v2() != 0:
-            raise RuntimeError("nvmlInit failed")
-
-    def handle(self, pci_bus_id=None, index=0):
-        ct = self.ct
-        h = ct.c_void_p()
-        if pci_bus_id is not None and self.lib.nvmlDeviceGetHandleByPciBusId_v2(
-                ct.c_char_p(pci_bus_id.encode()), ct.byref(h)) == 0:
-            return h
-        if self.lib.nvmlDeviceGetHandleByIndex_v2(ct.c_uint(index), ct.byref(h)) != 0:
-            raise RuntimeError("no NVML handle")
-        return h
-
-    def max_sm_mhz(self, h):
-        """The SM clock's maximum; it does not change while the process runs,
-        and the query takes about a millisecond (measured on B300), so it is
-        read once, outside the timed region."""
-        mx = self.ct.c_uint()
-        if self.lib.nvmlDeviceGetMaxClockInfo(h, self.SM, self.ct.byref(mx)) != 0:
-            raise RuntimeError("no NVML max clock")
-        return float(mx.value)
-
-    def sample(self, h, max_mhz):
-        """Current SM clock, power and throttle reasons: each query about a
-        microsecond."""
-        ct = self.ct
-        sm, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
-        if (self.lib.nvmlDeviceGetClockInfo(h, self.SM, ct.byref(sm)) != 0
-                or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons(h, ct.byref(rs)) != 0):
-            return None
-        if self.lib.nvmlDeviceGetPowerUsage(h, ct.byref(pw)) != 0:
-            pw.value = 0
-        return (float(sm.value), max_mhz, pw.value / 1000.0,
-                {n for n, b in self.REASONS.items() if rs.value & b})
+# The NVML sampler runs in a separate process (the plain ctypes NVML calls of
+# the driver's libnvidia-ml, read-only queries) and hands its samples over only
+# after the timed region: a sampling thread in this process takes the
+# interpreter lock every half millisecond, which delayed the host's launch of
+# the first timed step by ~0.1 ms.  The SM clock's maximum does not change
+# while the process runs and its query takes about a millisecond (measured on
+# B300), so it is read once before sampling starts.
+_NVML_CHILD = r"""
+import ctypes, select, sys, time
+lib = ctypes.CDLL("libnvidia-ml.so.1")
+if lib.nvmlInit_v2() != 0:
+    print("ERR nvmlInit", flush=True); sys.exit(0)
+h = ctypes.c_void_p()
+pci, idx = sys.argv[1], int(sys.argv[2])
+if not (pci != "-" and lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(pci.encode()), ctypes.byref(h)) == 0):
+    if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) != 0:
+        print("ERR no NVML handle", flush=True); sys.exit(0)
+mx = ctypes.c_uint()
+if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) != 0:
+    print("ERR no max clock", flush=True); sys.exit(0)
+print("READY", flush=True)
+sm, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+out = []
+while not select.select([sys.stdin], [], [], 0.0005)[0]:
+    if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons(h, ctypes.byref(rs)):
+        break
+    if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)):
+        pw.value = 0
+    out.append("%.7f %d %d %d %d" % (time.perf_counter(), sm.value, mx.value, pw.value, rs.value))
+print("\n".join(out), flush=True)
+"""
 
 
 class ClockSampler:
     """SM clock, max clock, power and throttle reasons of one GPU, polled
-    through NVML (read-only queries) about every millisecond in a background
-    thread, so that even a timed region of a few milliseconds holds samples.
-    Falls back to nvidia-smi at 100 ms when NVML cannot be loaded."""
+    through NVML about every half millisecond by a separate process, so that
+    even a timed region of a few milliseconds holds samples.  Falls back to
+    nvidia-smi at 100 ms when NVML cannot be loaded."""
     NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    REASON_BITS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+                   "sw_power_cap": 0x4}
 
     def __init__(self, gpu_index, pci_bus_id=None):
         self.pci_bus_id = pci_bus_id
@@ -211,30 +200,25 @@ class ClockSampler:
         g = str(gpu_index).strip()
         self.gpu_index = int(g) if g.isdigit() else 0
         self.samples = []          # (time, sm_mhz, max_mhz, power_w, set of reasons)
-        self._stop = threading.Event()
         self.thread = None
         self.proc = None
+        self.nvml = None
         self.source = None
 
     def start(self):
         try:
-            nv = _Nvml()
-            h = nv.handle(self.pci_bus_id, self.gpu_index)
-            max_mhz = nv.max_sm_mhz(h)
-
-            def poll():
-                while not self._stop.is_set():
-                    s = nv.sample(h, max_mhz)
-                    if s is None:
-                        break
-                    self.samples.append((time.perf_counter(),) + s)
-                    time.sleep(0.0005)
-            self.source = "nvml, ~1 ms"
-            self.thread = threading.Thread(target=poll, daemon=True)
-            self.thread.start()
-            return
-        except Exception as e:  # NVML unavailable: nvidia-smi every 100 ms
+            self.nvml = subprocess.Popen(
+                [sys.executable, "-c", _NVML_CHILD, self.pci_bus_id or "-", str(self.gpu_index)],
+                stdin=subprocess.PIPE, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            first = self.nvml.stdout.readline().strip()
+            if first == "READY":
+                self.source = "nvml (separate process), ~0.5 ms"
+                return
+            self.error = first or "NVML sampler exited"
+            self.nvml.wait(timeout=5)
+        except (OSError, ValueError, subprocess.TimeoutExpired) as e:
             self.error = f"{type(e).__name__}: {e}"
+        self.nvml = None
         fields = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
                   "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
                   "clocks_event_reasons.sw_power_cap")
@@ -259,7 +243,19 @@ class ClockSampler:
         self.thread.start()
 
     def stop(self):
-        self._stop.set()
+        if self.nvml is not None:
+            try:
+                out, _ = self.nvml.communicate(input="stop\n", timeout=10)
+            except subprocess.TimeoutExpired:
+                self.nvml.kill()
+                out = ""
+            for line in out.splitlines():
+                p = line.split()
+                if len(p) == 5:
+                    rs = int(p[4])
+                    self.samples.append((float(p[0]), float(p[1]), float(p[2]), int(p[3]) / 1000.0,
+                                         {n for n, b in self.REASON_BITS.items() if rs & b}))
+            self.nvml = None
         if self.proc is not None:
             self.proc.terminate()
             try:

@@ -659,12 +659,14 @@ gdn_status launch_single(const PassArgs& a, uint8_t* ws, const SingleLayout& L, 
     if (c.pair && (!encode_pairs(&tm_k, a.k, static_cast<long long>(BF) * a.N, a.H, k1p::CHUNK) ||
                    !encode_pairs(&tm_v, a.v, static_cast<long long>(BF) * a.N, a.H, k1p::CHUNK)))
         return GDN_ERR_LAUNCH;
-    // automatic: per head, 60 % of the free SMs contract (a contraction CTA
-    // streams k and v at about two thirds of an output CTA's rate of q in plus
-    // out; measured on B300 at the 60 s shape: 50 % 0.417 ms, 55 % 0.385 ms,
-    // 60 % 0.378 ms, 68 % 0.407 ms); on head pairs a contraction CTA streams
-    // about twice as fast, so 40 %
-    c.n_contract = forced > 0 ? std::min(forced, rest - 1) : c.pair ? (rest * 2 + 2) / 5 : (rest * 3 + 2) / 5;
+    // automatic: the share of the free SMs that contract, per mille, where the
+    // contraction and the output roles finish together (swept on B300 at the 60 s
+    // shape, 132 free SMs): bf16 48.5 % (0.352 ms; 60 % gives 0.375 ms), the
+    // folded prologue 62.5 % (normalizing k costs the scalers more than
+    // normalizing q costs the output), fp8 57.5 % and NVFP4 60.5 % (the decoders
+    // expand k and v in shared memory); on head pairs 40 %
+    const int share = c.pair ? 400 : a.prologue ? 625 : a.fmt == FMT_FP8 ? 575 : a.fmt == FMT_FP4 ? 605 : 485;
+    c.n_contract = forced > 0 ? std::min(forced, rest - 1) : std::max(1, (rest * share + 500) / 1000);
     const int n_out = rest - c.n_contract;
     if (c.n_contract < 1 || n_out < 1) return GDN_ERR_LAUNCH;
 

@@ -379,17 +379,26 @@ __device__ __forceinline__ void contract_role(const CUtensorMap& tm_k, const CUt
         // beta is copied to shared memory BETA_AHEAD chunks ahead of its use (a
         // cursor walks the same unit/chunk sequence), so its global-load
         // latency never sits between a landed K tile and its MMA.  Each thread
-        // reads back only the values it copied itself.
+        // reads back only the values it copied itself.  The cursor's unit and
+        // the row of its first token are computed once per unit: the integer
+        // divisions of unit_of, done per chunk by these four warps, had cost
+        // the contraction a third of its speed.
         int pw = w_begin, pc = 0;
-        if (pw < w_end) pc = unit_of(p, pw).c_begin;
+        Unit pu{};
+        size_t prow0 = 0;   // beta row of token 0 of the cursor's item
+        auto enter_unit = [&]() {
+            pu = unit_of(p, pw);
+            prow0 = static_cast<size_t>(pu.item / p.H) * p.N * p.H + (pu.item % p.H);
+            pc = pu.c_begin;
+        };
+        if (pw < w_end) enter_unit();
         int pslot = 0;
         auto beta_prefetch = [&]() {
             float* dst = beta_ring + pslot * SCALER_THREADS + t;
             uint32_t* sdst = sf_ring + (pslot * SCALER_THREADS + t) * 2;
             if (pw < w_end) {
-                const Unit u = unit_of(p, pw);
                 const int tok = pc * CHUNK + r;
-                const size_t row = (static_cast<size_t>(u.item / p.H) * p.N + tok) * p.H + (u.item % p.H);
+                const size_t row = prow0 + static_cast<size_t>(tok) * p.H;
                 if (tok < p.N)
                     cp_async_4(dst, p.beta + row);
                 else
@@ -401,9 +410,9 @@ __device__ __forceinline__ void contract_role(const CUtensorMap& tm_k, const CUt
                     if (tok < p.N && 64 * bx < p.dv) cp_async_4(sdst + 1, p.v_sf + row * (p.dv / 16) + 4 * bx);
                     else sdst[1] = 0u;
                 }
-                if (++pc >= u.c_end) {
+                if (++pc >= pu.c_end) {
                     pw += w_step;
-                    if (pw < w_end) pc = unit_of(p, pw).c_begin;
+                    if (pw < w_end) enter_unit();
                 }
             }
             cp_async_commit();

@@ -206,18 +206,24 @@ __device__ __forceinline__ void contract_pair_role(const CUtensorMap& tm_k, cons
         const int r = t >> 1, bx = t & 1;
         const int g = r >> 3, t8 = r & 7;
         int pw = w_begin, pc = 0, pslot = 0;
+        size_t prow0 = 0;   // beta row of token 0 of the cursor's pair (unit index math once per unit)
+        auto enter_unit = [&]() {
+            const Unit u = pair_unit_of(p, pw);
+            prow0 = static_cast<size_t>(u.item0 / p.H) * p.N * p.H + (u.item0 % p.H);
+        };
+        if (pw < w_end) enter_unit();
         auto beta_prefetch = [&]() {
             float2* dst = beta_ring + pslot * SCALER_THREADS + t;
             if (pw < w_end) {
-                const Unit u = pair_unit_of(p, pw);
                 const int tok = pc * CHUNK + r;
                 if (tok < p.N)
-                    cp_async_8(dst, p.beta + (static_cast<size_t>(u.item0 / p.H) * p.N + tok) * p.H + (u.item0 % p.H));
+                    cp_async_8(dst, p.beta + prow0 + static_cast<size_t>(tok) * p.H);
                 else
                     *dst = make_float2(0.0f, 0.0f);
                 if (++pc >= chunks) {
                     pc = 0;
                     pw += w_step;
+                    if (pw < w_end) enter_unit();
                 }
             }
             cp_async_commit();
