@@ -70,3 +70,37 @@ def test_traffic_lookup_checks_the_hash(tmp_path, monkeypatch):
     assert bench.ncu_traffic("k23_scan_output") is None
     monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(tmp_path / "absent.json"))
     assert bench.ncu_traffic("k23_scan_output") is None
+
+
+def test_clock_sampler_reads_the_sampling_process(monkeypatch):
+    """The NVML samples come from a separate process that hands them over at
+    stop(); their reason bits map to the names the timing rules use and only
+    samples inside the timed region are summarised."""
+    lines = ["10.0000000 1900 2032 400000 0", "10.5000000 2032 2032 500000 4", "11.5000000 2032 2032 510000 32"]
+
+    class FakeChild:
+        def __init__(self, *a, **k):
+            import io
+            self.stdout = io.StringIO("READY\n")
+
+        def communicate(self, input=None, timeout=None):
+            assert input is not None
+            return "\n".join(lines) + "\n", ""
+
+        def wait(self, timeout=None):
+            return 0
+
+        def kill(self):
+            pass
+
+    monkeypatch.setattr(bench.subprocess, "Popen", FakeChild)
+    s = bench.ClockSampler(0, None)
+    s.start()
+    assert s.source.startswith("nvml")
+    s.stop()
+    assert len(s.samples) == 3
+    r = s.summary(10.2, 11.0)   # only the sample at 10.5 s
+    assert r["samples_in_region"] == 1 and r["sm_mhz"] == 2032.0 and r["reasons"] == ["sw_power_cap"]
+    r = s.summary(9.0, 12.0)
+    assert r["samples_in_region"] == 3 and r["reasons"] == ["sw_power_cap", "sw_thermal_slowdown"]
+    assert bench.ClockSampler(0).summary(0.0, 1.0)["samples_in_region"] == 0
