@@ -118,21 +118,27 @@ struct Sched {
             slot = item;
             return true;
         }
-        const long long rank = wi + static_cast<long long>(k) * nw;
-        const long long BH = static_cast<long long>(p.B) * p.H;
-        const bool per_tile = BH * p.F < 2LL * nw;  // few items: spread single tiles instead
-        const long long units = per_tile ? BH * p.F * p.ntile : BH * p.F;
-        if (rank >= units) return false;
-        const long long ir = per_tile ? rank / p.ntile : rank;
-        const long long fs = ir / BH, bh = ir % BH;
-        const long long f = p.reverse ? p.F - 1 - fs : fs;
-        const long long b = bh / p.H, h = bh % p.H;
-        item = (b * p.F + f) * p.H + h;
-        nb = per_tile ? static_cast<int>(rank % p.ntile) : 0;
+        // 32-bit unsigned arithmetic: every count here is below 2^31 (tiles of
+        // one call), and several warps redo this per item, where 64-bit
+        // divisions cost as much as some of the item's own work
+        const unsigned BH = static_cast<unsigned>(p.B) * static_cast<unsigned>(p.H);
+        const bool per_tile = static_cast<long long>(BH) * p.F < 2LL * nw;  // few items: spread single tiles instead
+        const unsigned units = per_tile ? BH * p.F * p.ntile : BH * p.F;
+        const long long rank64 = wi + static_cast<long long>(k) * nw;
+        if (rank64 >= units) return false;
+        const unsigned rank = static_cast<unsigned>(rank64);
+        const unsigned nt = static_cast<unsigned>(p.ntile), H = static_cast<unsigned>(p.H);
+        const unsigned ir = per_tile ? rank / nt : rank;
+        const unsigned fs = ir / BH, bh = ir - fs * BH;
+        const unsigned f = p.reverse ? static_cast<unsigned>(p.F) - 1u - fs : fs;
+        const unsigned b = bh / H, h = bh - b * H;
+        item = (static_cast<long long>(b) * p.F + f) * p.H + h;
+        nb = per_tile ? static_cast<int>(rank - ir * nt) : 0;
         ne = per_tile ? nb + 1 : p.ntile;
         if (ring > 0) {
-            slot = (b * ring + fs % ring) * p.H + h;
-            use = static_cast<int>(fs / ring);
+            const unsigned R = static_cast<unsigned>(ring), use_u = fs / R;
+            slot = (static_cast<long long>(b) * ring + (fs - use_u * R)) * p.H + h;
+            use = static_cast<int>(use_u);
         } else {
             slot = item;
         }
