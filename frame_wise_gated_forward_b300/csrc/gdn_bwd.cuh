@@ -280,18 +280,37 @@ __global__ void __launch_bounds__(TOKEN_THREADS, 1)
     // contiguous unit ranges: a CTA's consecutive tiles mostly share an item
     const long long u_begin = (static_cast<long long>(blockIdx.x) * p.units) / gridDim.x;
     const long long u_end = (static_cast<long long>(blockIdx.x + 1) * p.units) / gridDim.x;
-    auto item_of = [&](long long u) { return static_cast<int>(u / p.ntile); };
+    // (item, tile, frame row, head) of unit u, stepped once per unit: the 64-bit
+    // divisions that give them directly cost every thread of the epilogue
+    // more than a little of each tile's work
+    struct TileCursor {
+        int item, tile, f, h;
+        __device__ TileCursor(long long u, int ntile, int H) {
+            item = static_cast<int>(u / ntile);
+            tile = static_cast<int>(u - static_cast<long long>(item) * ntile);
+            f = item / H;
+            h = item - f * H;
+        }
+        __device__ void next(int ntile, int H) {
+            if (++tile == ntile) {
+                tile = 0;
+                ++item;
+                if (++h == H) { h = 0; ++f; }
+            }
+        }
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             int gw_item = -1, gw_loads = 0;
             long long issued = 0;
-            for (long long u = u_begin; u < u_end; ++u) {
+            TileCursor cur(u_begin, p.ntile, p.H);
+            for (long long u = u_begin; u < u_end; ++u, cur.next(p.ntile, p.H)) {
                 const long long i = u - u_begin;
                 const int s = static_cast<int>(i % KV_STAGES);
-                const int item = item_of(u), tile = static_cast<int>(u % p.ntile);
-                const int f = item / p.H, h = item % p.H;
+                const int item = cur.item, tile = cur.tile;
+                const int f = cur.f, h = cur.h;
                 if (!mbar_wait(&kempty[s], static_cast<uint32_t>(((i / KV_STAGES) & 1) ^ 1), p.wait_limit_ns,
                                abort_flag))
                     break;
@@ -326,10 +345,11 @@ __global__ void __launch_bounds__(TOKEN_THREADS, 1)
             const int nkk = (p.dk + 15) / 16, nkv = (p.dv + 15) / 16;
             const uint32_t bG = smem_u32(sG), bW = smem_u32(sW);
             int gw_item = -1, gw_used = 0;
-            for (long long u = u_begin; u < u_end; ++u) {
+            TileCursor cur(u_begin, p.ntile, p.H);
+            for (long long u = u_begin; u < u_end; ++u, cur.next(p.ntile, p.H)) {
                 const long long i = u - u_begin;
                 const int s = static_cast<int>(i % KV_STAGES), a = static_cast<int>(i & 1);
-                const int item = item_of(u);
+                const int item = cur.item;
                 if (!mbar_wait(&tempty[a], static_cast<uint32_t>(((i >> 1) & 1) ^ 1), p.wait_limit_ns, abort_flag) ||
                     !mbar_wait(&kfull[s], static_cast<uint32_t>((i / KV_STAGES) & 1), p.wait_limit_ns, abort_flag))
                     break;
@@ -352,7 +372,7 @@ __global__ void __launch_bounds__(TOKEN_THREADS, 1)
                     mma_bf16(t12, smem_desc(aV + ko, 16, SBO), smem_desc(bG + kk * 2048, MN_LBO, SBO), ID_KM, 1u);
                 }
                 mma_commit(&tfull[a]);
-                if (u + 1 == u_end || item_of(u + 1) != item) mma_commit(gw_empty);
+                if (u + 1 == u_end || cur.tile + 1 == p.ntile) mma_commit(gw_empty);   // the item's last tile
             }
             mma_commit(final_bar);
             mbar_wait_drain(final_bar, 0, p.wait_limit_ns);
@@ -377,11 +397,12 @@ __global__ void __launch_bounds__(TOKEN_THREADS, 1)
                 x[2 * e + 1] = f2.y;
             }
         };
-        for (long long u = u_begin; u < u_end; ++u) {
+        TileCursor cur(u_begin, p.ntile, p.H);
+        for (long long u = u_begin; u < u_end; ++u, cur.next(p.ntile, p.H)) {
             const long long i = u - u_begin;
             const int s = static_cast<int>(i % KV_STAGES), a = static_cast<int>(i & 1);
-            const int item = item_of(u), tile = static_cast<int>(u % p.ntile);
-            const int f = item / p.H, h = item % p.H;
+            const int tile = cur.tile;
+            const int f = cur.f, h = cur.h;
             // both halves decide together: the named barrier below is never left waiting
             const bool ok = bar_and(1, TOKEN_EPI,
                                     mbar_wait(&tfull[a], static_cast<uint32_t>((i >> 1) & 1), p.wait_limit_ns,
