@@ -8,8 +8,7 @@
 // MMA chain D = Q_tile S_f^T with
 //     M = 128 tokens, N = 128 (dv, zero-padded), K = dk (<= 128)
 // both operands K-major in 128-byte-swizzled shared memory, loaded by TMA
-// straight from q's token-major layout and from the bf16 per-frame states (in
-// the single pass, one bulk copy of the state's ring tile).
+// straight from q's token-major layout and from the bf16 per-frame states.
 // S_f is loaded once per item (2-deep ring), q through a 3-deep ring, four
 // 128-column accumulators in TMEM let the MMA run up to three tiles ahead of
 // the epilogue.  Epilogue: each of four warps drains its 32-lane quarter,
