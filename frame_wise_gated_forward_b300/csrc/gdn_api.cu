@@ -662,10 +662,11 @@ gdn_status launch_single(const PassArgs& a, uint8_t* ws, const SingleLayout& L, 
     // automatic: the share of the free SMs that contract, per mille, where the
     // contraction and the output roles finish together (swept on B300 at the 60 s
     // shape, 132 free SMs): bf16 48.5 % (0.352 ms; 60 % gives 0.375 ms), the
-    // folded prologue 62.5 % (normalizing k costs the scalers more than
-    // normalizing q costs the output), fp8 57.5 % and NVFP4 60.5 % (the decoders
-    // expand k and v in shared memory); on head pairs 40 %
-    const int share = c.pair ? 400 : a.prologue ? 625 : a.fmt == FMT_FP8 ? 575 : a.fmt == FMT_FP4 ? 605 : 485;
+    // folded prologue 60.6 % (normalizing k costs the scalers more than
+    // normalizing q costs the output; 0.440 ms, against 0.480 ms at 63 %),
+    // fp8 57.5 % and NVFP4 60.5 % (the decoders expand k and v in shared
+    // memory); on head pairs 40 %
+    const int share = c.pair ? 400 : a.prologue ? 606 : a.fmt == FMT_FP8 ? 575 : a.fmt == FMT_FP4 ? 605 : 485;
     c.n_contract = forced > 0 ? std::min(forced, rest - 1) : std::max(1, (rest * share + 500) / 1000);
     const int n_out = rest - c.n_contract;
     if (c.n_contract < 1 || n_out < 1) return GDN_ERR_LAUNCH;

@@ -399,7 +399,7 @@ void gdn_set_fused_step(int on);
  * reverse, folded-prologue and 8-bit variants run a sequence of F >= 2
  * frames as ONE cooperative launch when the device allows it and B*H is at
  * most a quarter of the SMs: one CTA per head runs the scan, about half of
- * the other SMs (48.5 % for bf16, 57.5 % fp8, 60.5 % NVFP4, 62.5 % with the
+ * the other SMs (48.5 % for bf16, 57.5 % fp8, 60.5 % NVFP4, 60.6 % with the
  * folded prologue) run the frame-parallel contractions and the rest the output
  * pass, each frame handed on through small ring buffers of the workspace
  * that stay in L2 (per-slot counts raised with release semantics, bounded
